@@ -1,0 +1,181 @@
+"""Oracle for ``y = x @ W`` over GGUF/ggml-packed weights (plain C, f64 sums).
+
+TEST INFRASTRUCTURE ONLY. The tests, ``__graft_entry__.smoke()`` and the
+bench's ``cpu_baseline`` / reference leg may import this package; the CUDA
+product path never does, and nothing here imports the product package.
+
+The arithmetic lives in ``qmm_oracle.c`` (see its header for the passages it
+follows). This wrapper only compiles it with gcc, marshals numpy arrays to
+it, and holds the acceptance check:
+
+* per output ``|y - y_ref| <= 1e-4 * S`` where ``S = sum_i |x_i * w_ij|``
+  (plus ``|y_in|`` when accumulating into a prefilled y), the bar that the
+  matmul is held to;
+* cosine similarity over f64 sums, floor 0.9999, as moeflux
+  tests/graph_diff_oracle.rs ``cosine_sim`` / ``COSINE_FLOOR`` define it;
+  two all-zero vectors count as equal (that function returns 0 for them,
+  which is read here as "no disagreement").
+
+Every function here has parity pins in tests/test_oracle_pins.py.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "qmm_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+CODES = {"bf16": 0, "f16": 1, "q4_0": 2, "q4_k": 3, "q6_k": 4}
+TOL_REL = 1e-4
+COSINE_FLOOR = 0.9999
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (IEEE arithmetic, no FMA contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+                               "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, p = ctypes.c_int64, ctypes.c_void_p
+            lib.oracle_f16_value.restype = ctypes.c_double
+            lib.oracle_f16_value.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_value.restype = ctypes.c_float
+            lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
+            lib.oracle_row_bytes.restype = i64
+            lib.oracle_row_bytes.argtypes = [ctypes.c_int, i64]
+            lib.oracle_dequant.restype = ctypes.c_int
+            lib.oracle_dequant.argtypes = [ctypes.c_int, p, i64, i64, p]
+            lib.oracle_matmul.restype = ctypes.c_int
+            lib.oracle_matmul.argtypes = [ctypes.c_int, p, p, i64, i64, i64, p, p, p]
+            lib.oracle_matmul_sampled.restype = ctypes.c_int
+            lib.oracle_matmul_sampled.argtypes = [ctypes.c_int, p, p, i64, i64, i64, i64, p, p, p, p, p]
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def f16_value(h: int) -> float:
+    return _load().oracle_f16_value(int(h) & 0xFFFF)
+
+
+def bf16_value(h: int) -> float:
+    return _load().oracle_bf16_value(int(h) & 0xFFFF)
+
+
+def row_bytes(fmt: str, k: int) -> int:
+    return int(_load().oracle_row_bytes(CODES[fmt], int(k)))
+
+
+def dequant(fmt: str, w: np.ndarray, k: int, n: int) -> np.ndarray:
+    """fp32 weights [n, k] from packed bytes."""
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    rb = row_bytes(fmt, k)
+    if (rb == 0 and k != 0) or w.size != rb * n:
+        raise ValueError("bad shape for oracle dequant")
+    out = np.empty((n, k), np.float32)
+    if _load().oracle_dequant(CODES[fmt], _ptr(w), k, n, _ptr(out)) != 0:
+        raise ValueError("oracle dequant rejected its arguments")
+    return out
+
+
+def matmul(fmt: str, w: np.ndarray, x: np.ndarray, k: int, n: int):
+    """(y, S): y[t, j] = sum_i x[t, i] w[j, i] and S = sum_i |x w|, both f64 [N, n]."""
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
+    nt = x.shape[0]
+    if x.shape[1] != k:
+        raise ValueError("x must be [N, k]")
+    y = np.empty((nt, n), np.float64)
+    s = np.empty((nt, n), np.float64)
+    scratch = np.empty(max(k, 1), np.float32)
+    if _load().oracle_matmul(CODES[fmt], _ptr(w), _ptr(x), k, n, nt, _ptr(y), _ptr(s), _ptr(scratch)) != 0:
+        raise ValueError("oracle matmul rejected its arguments")
+    return y, s
+
+
+def matmul_sampled(fmt: str, w: np.ndarray, x: np.ndarray, k: int, n: int, t_idx, j_idx):
+    """(y, S) for the outputs (t_idx[c], j_idx[c]) only."""
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
+    t_idx = np.ascontiguousarray(t_idx, dtype=np.int64)
+    j_idx = np.ascontiguousarray(j_idx, dtype=np.int64)
+    cnt = t_idx.size
+    y = np.empty(cnt, np.float64)
+    s = np.empty(cnt, np.float64)
+    scratch = np.empty(max(k, 1), np.float32)
+    rc = _load().oracle_matmul_sampled(CODES[fmt], _ptr(w), _ptr(x), k, n, x.shape[0], cnt,
+                                       _ptr(t_idx), _ptr(j_idx), _ptr(y), _ptr(s), _ptr(scratch))
+    if rc != 0:
+        raise ValueError("oracle sampled matmul rejected its arguments")
+    return y, s
+
+
+def tiled(y_ref: np.ndarray, s_ref: np.ndarray, j_start: int, j_end: int, accumulate: bool,
+          y_in: np.ndarray):
+    """Expected output of an output-axis tile: columns [j_start, j_end) of y
+    become y_ref (or y_in + y_ref when accumulating); other columns keep y_in.
+    Returns (y_expected, S) with |y_in| added to S where it is summed in."""
+    y = np.array(y_in, dtype=np.float64, copy=True)
+    s = np.zeros_like(y)
+    sl = slice(j_start, j_end)
+    if accumulate:
+        y[:, sl] = y[:, sl] + y_ref[:, sl]
+        s[:, sl] = s_ref[:, sl] + np.abs(np.asarray(y_in, np.float64)[:, sl])
+    else:
+        y[:, sl] = y_ref[:, sl]
+        s[:, sl] = s_ref[:, sl]
+    return y, s
+
+
+def cosine(a: np.ndarray, b: np.ndarray) -> float:
+    """Cosine similarity with f64 sums; 1.0 when both vectors are all zero."""
+    a = np.asarray(a, np.float64).reshape(-1)
+    b = np.asarray(b, np.float64).reshape(-1)
+    na = float(np.dot(a, a))
+    nb = float(np.dot(b, b))
+    if na == 0.0 and nb == 0.0:
+        return 1.0
+    if na == 0.0 or nb == 0.0:
+        return 0.0
+    return float(np.dot(a, b) / (np.sqrt(na) * np.sqrt(nb)))
+
+
+def check(y: np.ndarray, y_ref: np.ndarray, s_ref: np.ndarray, tol: float = TOL_REL):
+    """Acceptance check. Returns (ok, worst_ratio, cosine, message)."""
+    y = np.asarray(y, np.float64)
+    err = np.abs(y - y_ref)
+    bound = tol * s_ref
+    nan_mismatch = np.isnan(y) != np.isnan(y_ref)
+    finite = ~np.isnan(y_ref)
+    bad = (err > bound) & finite
+    bad |= nan_mismatch
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(s_ref > 0, err / np.where(s_ref > 0, s_ref, 1.0), np.where(err > 0, np.inf, 0.0))
+    worst = float(np.nanmax(ratio[finite])) if finite.any() else 0.0
+    cos = cosine(np.where(finite, y, 0.0), np.where(finite, y_ref, 0.0))
+    ok = (not bad.any()) and cos >= COSINE_FLOOR
+    msg = f"bad={int(bad.sum())}/{y.size} worst err/S={worst:.3e} cosine={cos:.9f}"
+    if bad.any():
+        idx = np.argwhere(bad)[0]
+        msg += f" first bad at {tuple(int(i) for i in idx)}: y={y[tuple(idx)]!r} ref={y_ref[tuple(idx)]!r} S={s_ref[tuple(idx)]!r}"
+    return ok, worst, cos, msg

@@ -1,0 +1,129 @@
+"""Seeded synthetic inputs for the fused dequantize-and-multiply ``y = x @ W``.
+
+This module only draws random numbers and lays them out as GGUF/ggml block
+bytes; it holds none of the dequantization or matmul arithmetic. Both the
+oracle (under ``oracle/``) and the CUDA path are fed from here, so the two
+sides always see identical bytes.
+
+Workload recipes (sizes, value distributions, seeds) follow the synthetic
+stand-ins for the real-model shapes that the rullama ``matmul.rs`` tests use
+(Gemma-4 projections, the vocab-sized output head):
+
+* ``q4_0_gemv``     Q4_0, k=256, n=512; per-block f16 scale d ~ U[0.005, 0.05],
+                    16 uniform quant bytes (so every nibble is uniform 0..15);
+                    x ~ U[-1, 1]; seed 1.
+* ``bf16_gemv`` / ``f16_gemv``
+                    k=n=4096, w ~ N(0, 0.02) rounded to bf16 / f16
+                    (round-to-nearest-even); x ~ N(0, 1); seed 2.
+* ``q4_k_gemv``     Q4_K, k=4096, n=14336; d, dmin f16 ~ U[0.001, 0.02];
+                    12 uniform packed-scale bytes (every 6-bit scale/min
+                    uniform 0..63); 128 uniform quant bytes; x ~ N(0, 1); seed 3.
+* ``q6_k_head``     Q6_K, k=2560, n=262144; ql/qh uniform bytes; int8 scales
+                    uniform in [-32, 31]; f16 d ~ U[0.0005, 0.01]; x ~ N(0, 1);
+                    seed 4; run as 8 output tiles of 32768 columns.
+* ``q4_k_prefill``  Q4_K with the q4_k_gemv value distribution, N=512 tokens,
+                    k=4096, n=14336; X ~ N(0, 1) [N x k]; seed 5 (also N=1, 8, 64).
+
+Byte layouts written here (little-endian): Q4_0 block = f16 d then 16 quant
+bytes (18 B); Q4_K super-block = f16 d, f16 dmin, 12 scale bytes, 128 quant
+bytes (144 B); Q6_K super-block = 128 ql bytes, 64 qh bytes, 16 int8 scales,
+f16 d (210 B). BF16/F16 rows are plain 16-bit little-endian values.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+FORMATS = ("bf16", "f16", "q4_0", "q4_k", "q6_k")
+
+# elements per block and bytes per block of each format
+BLOCK_ELEMS = {"bf16": 1, "f16": 1, "q4_0": 32, "q4_k": 256, "q6_k": 256}
+BLOCK_BYTES = {"bf16": 2, "f16": 2, "q4_0": 18, "q4_k": 144, "q6_k": 210}
+
+
+def row_bytes(fmt: str, k: int) -> int:
+    """Bytes of one packed row of k weights (k must be a multiple of the block)."""
+    return (k // BLOCK_ELEMS[fmt]) * BLOCK_BYTES[fmt]
+
+
+def _f16_bytes(values: np.ndarray) -> np.ndarray:
+    """f16 (round-to-nearest-even via numpy) as little-endian byte pairs."""
+    h = values.astype(np.float16).astype("<f2")
+    return h.view(np.uint8).reshape(values.shape + (2,))
+
+
+def _bf16_bits_rne(values: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns of f32 values, round-to-nearest-even (finite inputs)."""
+    bits = values.astype(np.float32).view(np.uint32).astype(np.uint64)
+    rounded = (bits + 0x7FFF + ((bits >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
+
+
+def gen_weights(fmt: str, k: int, n: int, rng: np.random.Generator, **dist) -> np.ndarray:
+    """Packed weight bytes, shape [n * row_bytes(fmt, k)] uint8, row-major (row j = column j of W)."""
+    if fmt in ("bf16", "f16"):
+        std = dist.get("std", 0.02)
+        w = rng.normal(0.0, std, size=(n, k)).astype(np.float32)
+        if fmt == "bf16":
+            bits = _bf16_bits_rne(w).astype("<u2")
+        else:
+            bits = w.astype(np.float16).astype("<f2").view("<u2")
+        return np.ascontiguousarray(bits).view(np.uint8).reshape(-1)
+    if fmt == "q4_0":
+        lo, hi = dist.get("d_range", (0.005, 0.05))
+        nb = k // 32
+        blk = np.empty((n, nb, 18), np.uint8)
+        blk[..., 0:2] = _f16_bytes(rng.uniform(lo, hi, size=(n, nb)))
+        blk[..., 2:18] = rng.integers(0, 256, size=(n, nb, 16), dtype=np.uint8)
+        return blk.reshape(-1)
+    if fmt == "q4_k":
+        lo, hi = dist.get("d_range", (0.001, 0.02))
+        nb = k // 256
+        blk = np.empty((n, nb, 144), np.uint8)
+        blk[..., 0:2] = _f16_bytes(rng.uniform(lo, hi, size=(n, nb)))
+        blk[..., 2:4] = _f16_bytes(rng.uniform(lo, hi, size=(n, nb)))
+        blk[..., 4:144] = rng.integers(0, 256, size=(n, nb, 140), dtype=np.uint8)
+        return blk.reshape(-1)
+    if fmt == "q6_k":
+        lo, hi = dist.get("d_range", (0.0005, 0.01))
+        nb = k // 256
+        blk = np.empty((n, nb, 210), np.uint8)
+        blk[..., 0:192] = rng.integers(0, 256, size=(n, nb, 192), dtype=np.uint8)
+        sc = rng.integers(-32, 32, size=(n, nb, 16), dtype=np.int64).astype(np.int8)
+        blk[..., 192:208] = sc.view(np.uint8)
+        blk[..., 208:210] = _f16_bytes(rng.uniform(lo, hi, size=(n, nb)))
+        return blk.reshape(-1)
+    raise ValueError(f"unknown format {fmt!r}")
+
+
+def gen_x(n_tokens: int, k: int, rng: np.random.Generator, dist: str = "normal") -> np.ndarray:
+    """Activations [n_tokens, k] fp32."""
+    if dist == "uniform":
+        return rng.uniform(-1.0, 1.0, size=(n_tokens, k)).astype(np.float32)
+    return rng.normal(0.0, 1.0, size=(n_tokens, k)).astype(np.float32)
+
+
+# name -> (fmt, k, n, n_tokens, seed, x distribution, output tiles)
+WORKLOADS = {
+    "q4_0_gemv": ("q4_0", 256, 512, 1, 1, "uniform", 1),
+    "bf16_gemv": ("bf16", 4096, 4096, 1, 2, "normal", 1),
+    "f16_gemv": ("f16", 4096, 4096, 1, 2, "normal", 1),
+    "q4_k_gemv": ("q4_k", 4096, 14336, 1, 3, "normal", 1),
+    "q6_k_head": ("q6_k", 2560, 262144, 1, 4, "normal", 8),
+    "q4_k_prefill": ("q4_k", 4096, 14336, 512, 5, "normal", 1),
+}
+
+
+def workload(name: str, n_tokens: int | None = None, n: int | None = None):
+    """Seeded (fmt, k, n, W bytes, X) for a named workload.
+
+    ``n`` may shrink the output axis (rows of W) for oracle-sized cases; the
+    draws for the first rows do not change with n only for the byte formats'
+    layout, so shrunken cases are separate seeded draws, not prefixes.
+    """
+    fmt, k, n_full, nt_default, seed, xdist, _tiles = WORKLOADS[name]
+    n = n_full if n is None else n
+    nt = nt_default if n_tokens is None else n_tokens
+    rng = np.random.default_rng(seed)
+    w = gen_weights(fmt, k, n, rng)
+    x = gen_x(nt, k, rng, xdist)
+    return fmt, k, n, w, x

@@ -1,0 +1,388 @@
+"""Pins for the oracle: facts fixed by the pages and by the mathematics, each
+chosen so that a plausible slip in the oracle (a wrong field offset, swapped
+nibbles, a dropped min term, a wrong scale index, a transposed operand)
+fails at least one of them. CPU only."""
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import qmm_synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "pages_constants.txt")
+
+
+def _golden():
+    rows = []
+    with open(GOLDEN) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append(line.split())
+    return rows
+
+
+# ---------------------------------------------------------------- sizes ----
+
+def test_row_bytes_closed_forms():
+    # (k/32)*18, (k/256)*144, (k/256)*210, 2k bytes per row (rullama matmul.rs checks)
+    for k in (0, 32, 64, 96, 256, 512, 2560, 4096):
+        assert oracle.row_bytes("q4_0", k) == (k // 32) * 18
+        assert oracle.row_bytes("bf16", k) == 2 * k
+        assert oracle.row_bytes("f16", k) == 2 * k
+    for k in (0, 256, 512, 1536, 2560, 4096, 6144):
+        assert oracle.row_bytes("q4_k", k) == (k // 256) * 144
+        assert oracle.row_bytes("q6_k", k) == (k // 256) * 210
+    # shapes the formats reject
+    assert oracle.row_bytes("q4_0", 48) == 0
+    assert oracle.row_bytes("q4_k", 128) == 0
+    assert oracle.row_bytes("q6_k", 300) == 0
+    assert oracle.row_bytes("bf16", 3) == 0
+
+
+def test_golden_page_constants():
+    for row in _golden():
+        kind = row[0]
+        if kind == "f16":
+            assert oracle.f16_value(int(row[1], 16)) == float(row[2])
+        elif kind == "block":
+            fmt, elems, nbytes = row[1], int(row[2]), int(row[3])
+            assert oracle.row_bytes(fmt, elems) == nbytes
+            assert oracle.row_bytes(fmt, 4 * elems) == 4 * nbytes
+        elif kind == "rowbytes":
+            assert oracle.row_bytes(row[1], int(row[2])) == int(row[3])
+        elif kind == "offset":
+            fmt, field, off = row[1], row[2], int(row[3])
+            _check_offset(fmt, field, off)
+        else:
+            raise AssertionError(f"unknown golden kind {kind}")
+
+
+def _check_offset(fmt, field, off):
+    """Write f16(0.0625) at the page-given offset of a block built so that the
+    element values are exactly +-that field; the decoded weights must show it."""
+    if fmt == "q4_0":
+        blk = np.zeros(18, np.uint8)
+        blk[off:off + 2] = [0x00, 0x2C]
+        blk[2:] = 0x99  # q = 9 -> (9-8)*d = d
+        w = oracle.dequant("q4_0", blk, 32, 1)
+        assert np.all(w == 0.0625)
+    elif fmt == "q4_k":
+        blk = np.zeros(144, np.uint8)
+        blk[off:off + 2] = [0x00, 0x2C]
+        if field == "d":  # scale 1, min 0, q = 1 -> d
+            sc, m = [1] * 8, [0] * 8
+            q = np.ones(256, np.int64)
+        else:             # scale 0, min 1 -> -dmin
+            sc, m = [0] * 8, [1] * 8
+            q = np.zeros(256, np.int64)
+        blk[4:16] = _pack_q4_k_scales(sc, m)
+        blk[16:144] = _pack_q4_k_qs(q)
+        w = oracle.dequant("q4_k", blk, 256, 1)
+        assert np.all(w == (0.0625 if field == "d" else -0.0625))
+    elif fmt == "q6_k":
+        blk = np.zeros(210, np.uint8)
+        blk[off:off + 2] = [0x00, 0x2C]
+        blk[192:208] = 1                       # every scale = 1
+        q = np.full(256, 33, np.int64)         # q - 32 = 1
+        blk[0:192] = _pack_q6_k_q(q)
+        w = oracle.dequant("q6_k", blk, 256, 1)
+        assert np.all(w == 0.0625)
+    else:
+        raise AssertionError(fmt)
+
+
+# ----------------------------------------------------------- f16 / bf16 ----
+
+def test_f16_decoder_exhaustive_against_numpy():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16_value(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # signed zeros keep their sign
+    assert np.copysign(1.0, oracle.f16_value(0x8000)) == -1.0
+
+
+def test_f16_special_values():
+    assert oracle.f16_value(0x3C00) == 1.0
+    assert oracle.f16_value(0x0001) == 2.0 ** -24          # smallest subnormal
+    assert oracle.f16_value(0x03FF) == 1023 * 2.0 ** -24   # largest subnormal
+    assert oracle.f16_value(0x0400) == 2.0 ** -14          # smallest normal
+    assert oracle.f16_value(0x7BFF) == 65504.0
+    assert oracle.f16_value(0x7C00) == float("inf")
+    assert oracle.f16_value(0xFC00) == float("-inf")
+    assert np.isnan(oracle.f16_value(0x7E00))
+
+
+def test_bf16_is_upper_half_of_f32():
+    rng = np.random.default_rng(0)
+    f = rng.normal(0, 3, 4096).astype(np.float32)
+    hi = (f.view(np.uint32) >> 16).astype(np.uint16)
+    got = np.array([oracle.bf16_value(int(h)) for h in hi], np.float32)
+    # the page's CPU round trip: bits & 0xFFFF0000
+    assert np.array_equal(got.view(np.uint32), f.view(np.uint32) & 0xFFFF0000)
+
+
+# ------------------------------------------------------- block packing ----
+# Test-side inverses of the ggml layouts, used only to build blocks whose
+# element values are known in closed form.
+
+def _pack_q4_k_scales(sc, m):
+    b = [0] * 12
+    for s in range(4):
+        b[s] = (sc[s] & 63) | ((sc[s + 4] >> 4) << 6)
+        b[s + 4] = (m[s] & 63) | ((m[s + 4] >> 4) << 6)
+    for s in range(4, 8):
+        b[s + 4] = (sc[s] & 15) | ((m[s] & 15) << 4)
+    return np.array(b, np.uint8)
+
+
+def _pack_q4_k_qs(q):
+    qs = np.zeros(128, np.uint8)
+    for c in range(4):
+        for l in range(32):
+            qs[32 * c + l] = q[64 * c + l] | (q[64 * c + 32 + l] << 4)
+    return qs
+
+
+def _pack_q6_k_q(q):
+    out = np.zeros(192, np.uint8)
+    ql, qh = out[:128], out[128:]
+    for h in range(2):
+        for l in range(32):
+            e = 128 * h + l
+            ql[64 * h + l] = (q[e] & 15) | ((q[e + 64] & 15) << 4)
+            ql[64 * h + 32 + l] = (q[e + 32] & 15) | ((q[e + 96] & 15) << 4)
+            qh[32 * h + l] = ((q[e] >> 4) | ((q[e + 32] >> 4) << 2)
+                              | ((q[e + 64] >> 4) << 4) | ((q[e + 96] >> 4) << 6))
+    return out
+
+
+def test_q4_0_hand_packed():
+    blk = np.zeros(18, np.uint8)
+    blk[0:2] = [0x00, 0x3C]  # d = 1.0
+    for i in range(16):
+        blk[2 + i] = i | ((15 - i) << 4)
+    w = oracle.dequant("q4_0", blk, 32, 1)[0]
+    assert list(w[:16]) == [i - 8 for i in range(16)]
+    assert list(w[16:]) == [7 - i for i in range(16)]
+    # negative d flips the sign exactly
+    blk[0:2] = [0x00, 0xB8]  # d = -0.5
+    w = oracle.dequant("q4_0", blk, 32, 1)[0]
+    assert list(w[:16]) == [-(i - 8) * 0.5 for i in range(16)]
+
+
+@pytest.mark.parametrize("variant", ["small", "top_bits"])
+def test_q4_k_hand_packed(variant):
+    if variant == "small":
+        sc = [s + 1 for s in range(8)]
+        m = [s for s in range(8)]
+        d, dmin, dbits, dminbits = 1.0, 1.0, 0x3C00, 0x3C00
+    else:  # exercise the two top bits of every 6-bit field
+        sc = [63 - s for s in range(8)]
+        m = [32 + s for s in range(8)]
+        d, dmin, dbits, dminbits = 0.5, 0.25, 0x3800, 0x3400
+    q = np.array([(7 * e + e // 32) % 16 for e in range(256)], np.int64)  # low/high nibbles differ
+    blk = np.zeros(144, np.uint8)
+    blk[0:2] = [dbits & 0xFF, dbits >> 8]
+    blk[2:4] = [dminbits & 0xFF, dminbits >> 8]
+    blk[4:16] = _pack_q4_k_scales(sc, m)
+    blk[16:] = _pack_q4_k_qs(q)
+    w = oracle.dequant("q4_k", blk, 256, 1)[0]
+    expect = [d * sc[e // 32] * q[e] - dmin * m[e // 32] for e in range(256)]
+    assert list(w) == [np.float32(v) for v in expect]
+
+
+def test_q6_k_hand_packed():
+    q = np.array([(5 * e + e // 64) % 64 for e in range(256)], np.int64)
+    blk = np.zeros(210, np.uint8)
+    blk[0:192] = _pack_q6_k_q(q)
+    blk[192:208] = np.array([s - 8 for s in range(16)], np.int8).view(np.uint8)
+    blk[208:210] = [0x00, 0x3C]  # d = 1.0 at the page-given offset
+    w = oracle.dequant("q6_k", blk, 256, 1)[0]
+    expect = [(e // 16 - 8) * (q[e] - 32) for e in range(256)]
+    assert list(w) == expect
+
+
+def test_block_order_within_row():
+    """Row of 3 Q4_0 blocks with d = 1, 2, 4: block b scales elements 32b..32b+31."""
+    k = 96  # row_bytes = 54, not a multiple of 4: accepted (no u32-row constraint)
+    row = np.zeros(54, np.uint8)
+    for b, dbits in enumerate((0x3C00, 0x4000, 0x4400)):
+        row[18 * b:18 * b + 2] = [dbits & 0xFF, dbits >> 8]
+        row[18 * b + 2:18 * b + 18] = 0x9A  # low nibble 10 (q-8=2), high 9 (q-8=1)
+    w = oracle.dequant("q4_0", row, k, 1)[0]
+    for b, d in enumerate((1.0, 2.0, 4.0)):
+        assert np.all(w[32 * b:32 * b + 16] == 2 * d)
+        assert np.all(w[32 * b + 16:32 * b + 32] == 1 * d)
+
+
+# ------------------------------------------------ invariants on random ----
+
+def test_random_block_invariants():
+    rng = np.random.default_rng(11)
+    # Q4_0: w / d is an integer in [-8, 7]
+    w = qmm_synth.gen_weights("q4_0", 256, 8, rng)
+    deq = oracle.dequant("q4_0", w, 256, 8).reshape(8, 8, 32)
+    d = w.reshape(8, 8, 18)[..., 0:2].copy().view("<f2").astype(np.float64)
+    r = deq / d  # d has shape [8, 8, 1]: broadcasts over the 32 elements
+    assert np.all(r == np.round(r)) and r.min() >= -8 and r.max() <= 7
+    # Q6_K: w / (d * scale) is an integer in [-32, 31]
+    w = qmm_synth.gen_weights("q6_k", 512, 4, rng)
+    deq = oracle.dequant("q6_k", w, 512, 4).reshape(4, 2, 16, 16).astype(np.float64)
+    blk = w.reshape(4, 2, 210)
+    d = blk[..., 208:210].copy().view("<f2").astype(np.float64)[..., 0]
+    sc = blk[..., 192:208].view(np.int8).astype(np.float64)
+    denom = d[..., None] * sc
+    ok = denom != 0
+    r = deq[ok] / np.broadcast_to(denom[..., None], deq.shape)[ok]
+    assert np.all(r == np.round(r)) and r.min() >= -32 and r.max() <= 31
+    assert np.all(deq[~np.broadcast_to(ok[..., None], deq.shape)] == 0)
+
+
+def test_q4_k_single_rounding():
+    """A Q4_K block whose exact values need more than 24 bits: each decoded
+    weight is the f32 nearest the exact d*sc*q - dmin*m (rounded once)."""
+    d = Fraction(1) + Fraction(1, 1024)              # f16 0x3C01
+    dmin = Fraction(1, 2 ** 14) * (1 + Fraction(1, 1024))  # f16 0x0401
+    sc = [63, 62, 61, 60, 59, 58, 57, 55]
+    m = [1, 3, 5, 7, 63, 33, 17, 9]
+    q = np.array([(3 * e + 1) % 16 for e in range(256)], np.int64)
+    blk = np.zeros(144, np.uint8)
+    blk[0:2] = [0x01, 0x3C]
+    blk[2:4] = [0x01, 0x04]
+    blk[4:16] = _pack_q4_k_scales(sc, m)
+    blk[16:] = _pack_q4_k_qs(q)
+    w = oracle.dequant("q4_k", blk, 256, 1)[0]
+    rounded_somewhere = False
+    for e in range(256):
+        exact = d * sc[e // 32] * int(q[e]) - dmin * m[e // 32]
+        want = np.float32(float(exact))  # exact value fits a double; one RNE to f32
+        assert w[e] == want, e
+        rounded_somewhere |= Fraction(float(want)) != exact
+    assert rounded_somewhere
+
+
+# -------------------------------------------------------------- matmul ----
+
+def test_identity_f16_and_bf16():
+    # rullama matmul.rs f16_matmul_3x4_eye, widened: identity W gives y = x exactly
+    k = n = 8
+    x = (np.arange(k, dtype=np.float32) + 1) * 0.25
+    for fmt, one in (("f16", 0x3C00), ("bf16", 0x3F80)):
+        wbits = np.zeros((n, k), np.uint16)
+        for j in range(n):
+            wbits[j, j] = one
+        y, s = oracle.matmul(fmt, wbits.astype("<u2").view(np.uint8).reshape(-1), x, k, n)
+        assert np.array_equal(y[0], x.astype(np.float64))
+        assert np.array_equal(s[0], np.abs(x).astype(np.float64))
+
+
+def test_one_hot_x_picks_weight_column():
+    rng = np.random.default_rng(3)
+    for fmt, k in (("q4_0", 64), ("q4_k", 256), ("q6_k", 256), ("bf16", 32), ("f16", 32)):
+        n = 5
+        w = qmm_synth.gen_weights(fmt, k, n, rng)
+        deq = oracle.dequant(fmt, w, k, n)
+        for i in (0, 1, k // 2 + 3, k - 1):
+            x = np.zeros((1, k), np.float32)
+            x[0, i] = 1.0
+            y, _ = oracle.matmul(fmt, w, x, k, n)
+            assert np.array_equal(y[0], deq[:, i].astype(np.float64))
+
+
+def test_brute_force_tiny_q4_0():
+    """Hand-listed sums for a 2-row, k=32 Q4_0 product (row 1 uses d = -0.25)."""
+    w = np.zeros(36, np.uint8)
+    w[0:2] = [0x00, 0x3C]                    # d = 1
+    w[2:18] = [(i % 16) | (((i + 3) % 16) << 4) for i in range(16)]
+    w[18:20] = [0x00, 0xB4]                  # d = -0.25
+    w[20:36] = [15 - i for i in range(16)]   # high nibbles 0
+    x = np.array([[(i % 5) - 2 for i in range(32)]], np.float32)
+    y, s = oracle.matmul("q4_0", w, x, 32, 2)
+    r0 = Fraction(0)
+    r1 = Fraction(0)
+    for i in range(16):
+        r0 += (i - 8) * ((i % 5) - 2) + (((i + 3) % 16) - 8) * (((i + 16) % 5) - 2)
+        r1 += Fraction(-1, 4) * ((15 - i - 8) * ((i % 5) - 2) + (0 - 8) * (((i + 16) % 5) - 2))
+    assert y[0, 0] == float(r0) and y[0, 1] == float(r1)
+
+
+def test_matmul_matches_numpy_product_of_dequantized():
+    """Dequantize-then-dot equals numpy's f64 matmul of the oracle's own weights,
+    checked on multi-token inputs (catches a transposed operand or token stride)."""
+    rng = np.random.default_rng(5)
+    for fmt, k, n, nt in (("q4_0", 96, 7, 3), ("q4_k", 512, 5, 4), ("q6_k", 256, 9, 2),
+                          ("bf16", 40, 6, 3), ("f16", 24, 4, 5)):
+        w = qmm_synth.gen_weights(fmt, k, n, rng)
+        x = qmm_synth.gen_x(nt, k, rng)
+        deq = oracle.dequant(fmt, w, k, n).astype(np.float64)
+        y, s = oracle.matmul(fmt, w, x, k, n)
+        ref = x.astype(np.float64) @ deq.T
+        np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(s, np.abs(x.astype(np.float64)) @ np.abs(deq.T), rtol=1e-12)
+
+
+def test_sampled_equals_full():
+    rng = np.random.default_rng(6)
+    w = qmm_synth.gen_weights("q6_k", 512, 11, rng)
+    x = qmm_synth.gen_x(3, 512, rng)
+    y, s = oracle.matmul("q6_k", w, x, 512, 11)
+    t = np.array([0, 2, 1, 2])
+    j = np.array([10, 0, 5, 7])
+    ys, ss = oracle.matmul_sampled("q6_k", w, x, 512, 11, t, j)
+    assert np.array_equal(ys, y[t, j]) and np.array_equal(ss, s[t, j])
+
+
+def test_k_zero_gives_zero():
+    y, s = oracle.matmul("bf16", np.zeros(0, np.uint8), np.zeros((2, 0), np.float32), 0, 3)
+    assert np.all(y == 0) and np.all(s == 0)
+
+
+# ------------------------------------------------- acceptance checker ----
+
+def test_checker_catches_a_dropped_term():
+    """A mistake planted in the oracle's output (one product term dropped from
+    one output) must fail the 1e-4 * sum|x w| bar at the configs' k."""
+    rng = np.random.default_rng(7)
+    k, n = 4096, 64
+    w = qmm_synth.gen_weights("q4_k", k, n, rng)
+    x = qmm_synth.gen_x(1, k, rng)
+    y, s = oracle.matmul("q4_k", w, x, k, n)
+    deq = oracle.dequant("q4_k", w, k, n)
+    ok, _, _, _ = oracle.check(y, y, s)
+    assert ok
+    i = int(np.argmax(np.abs(x[0] * deq[3])))
+    bad = y.copy()
+    bad[0, 3] -= float(x[0, i]) * float(deq[3, i])
+    ok, worst, _, _ = oracle.check(bad, y, s)
+    assert not ok and worst > 1e-4
+
+
+def test_checker_catches_sign_flip_by_cosine():
+    y = np.linspace(-1, 1, 101)[None, :]
+    s = np.full_like(y, 1e9)  # elementwise bar loose: cosine must catch it
+    ok, _, cos, _ = oracle.check(-y, y, s)
+    assert not ok and cos < 0
+
+
+def test_cosine_zero_vectors():
+    z = np.zeros(5)
+    assert oracle.cosine(z, z) == 1.0
+    assert oracle.cosine(z, np.ones(5)) == 0.0
+
+
+def test_tiled_semantics():
+    y_ref = np.arange(12, dtype=np.float64).reshape(2, 6)
+    s_ref = np.ones_like(y_ref)
+    y_in = np.full((2, 6), 100.0)
+    y, s = oracle.tiled(y_ref, s_ref, 2, 4, True, y_in)
+    assert np.array_equal(y[:, 2:4], 100 + y_ref[:, 2:4])
+    assert np.array_equal(y[:, :2], y_in[:, :2]) and np.array_equal(y[:, 4:], y_in[:, 4:])
+    assert np.array_equal(s[:, 2:4], 101 * np.ones((2, 2)))
+    y, s = oracle.tiled(y_ref, s_ref, 0, 6, False, y_in)
+    assert np.array_equal(y, y_ref)
