@@ -1,0 +1,524 @@
+"""Benchmark of the fused dequantize-and-multiply hot path on GB300.
+
+Default workload (one step): the one-token BF16 GEMV and the one-token F16
+GEMV at k = n = 4096 (weights ~N(0, 0.02) rounded to 16 bits, x ~ N(0, 1),
+seed 2), i.e. 2 x 33,554,432 weight bytes per step. Metric: effective weight
+GB/s = weight bytes / time (x and y bytes excluded). Inputs are resident in
+HBM; every step reads a different one of several distinct weight copies whose
+total is > 3x the L2 size, so each step streams W from HBM.
+
+The JSON line also carries the other workloads of the path measured the same
+way (Q4_0 / Q4_K / Q6_K GEMV, and the Q4_K N-token product in TFLOP/s at
+N = 1, 8, 64, 512 on both paths), the roofline of the dominant kernel against
+the measured HBM copy bandwidth, an end-to-end figure through the host-buffer
+C entry point (qmm_matmul_host: W and x copied in, y copied out, every step),
+SM clocks sampled during the timed region, and the oracle timed on the host
+as a CPU baseline.
+
+--impl reference times the oracle (plain C, one host core) on the same
+workload: each step is the full oracle product of both weight matrices.
+Under torchrun (N > 1) every rank runs its own replica (weak scaling); the
+time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import qmm_synth  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES_DEFAULT = 129 * 1024 * 1024
+
+
+# ------------------------------------------------------------ utilities ----
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, ws: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity at world size 1)."""
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_weight_gguf_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the kernel sources as they are now."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[kernel]
+        if e.get("source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------ reference ----
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    fmts = [qmm_synth.workload("bf16_gemv"), qmm_synth.workload("f16_gemv")]
+    wbytes = sum(w.size for _, _, _, w, _ in fmts)
+
+    def step():
+        for fmt, k, n, w, x in fmts:
+            oracle.matmul(fmt, w, x, k, n)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = wbytes / dt / 1e9
+    line = {"impl": "reference", "metric": "effective weight GB/s", "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "bf16+f16 GEMV k=n=4096, 1 token (one step = both)",
+                       "weight_bytes_per_step": wbytes},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "full oracle product of both 4096x4096 weight matrices per step"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------- native ----
+
+def cpu_baseline(seconds: float = 10.0):
+    import oracle
+    oracle.build()
+    fmts = [qmm_synth.workload("bf16_gemv"), qmm_synth.workload("f16_gemv")]
+    done = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        for fmt, k, n, w, x in fmts:
+            oracle.matmul(fmt, w, x, k, n)
+            done += w.size
+    dt = time.perf_counter() - t0
+    return {"value": done / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"oracle (plain C, f64 sums) on the bf16+f16 4096x4096 GEMVs, repeated "
+                      f"for {dt:.1f} s ({done / 1e6:.0f} MB of weights)"}
+
+
+class Runner:
+    """Device-resident inputs with rotation over distinct weight copies."""
+
+    def __init__(self, torch, q, device):
+        self.torch, self.q, self.dev = torch, q, device
+        self.stream = torch.cuda.current_stream(device)
+        try:
+            self.l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        except Exception:
+            self.l2 = L2_BYTES_DEFAULT
+
+    def copies_for(self, nbytes: int) -> int:
+        return max(1, min(64, -(-3 * self.l2 // max(nbytes, 1))))
+
+    def weights(self, w_np, copies):
+        base = self.torch.from_numpy(w_np).to(self.dev)
+        return [base] + [base.clone() for _ in range(copies - 1)]
+
+
+def time_loop(torch, launch, steps, warmup, ncopies, stream, inner_events=None):
+    """Time `steps` calls of launch(i) (i rotates the weight copy) with CUDA
+    events on `stream`; returns seconds per call."""
+    for i in range(warmup):
+        launch(i % ncopies)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        launch(i % ncopies)
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3 / steps
+
+
+def run_native(args):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    import quantized_weight_gguf_gb300 as q
+    from quantized_weight_gguf_gb300 import build_lib
+    if not os.path.exists(q.LIB_PATH):
+        build_lib.build()
+    lib = q.load()
+    r = Runner(torch, q, device)
+    stream = r.stream
+    sptr = stream.cuda_stream
+    hbm_peak, tc_peak, tc_sust, peak_src = peaks()
+
+    # ---------------- headline: bf16 + f16 GEMV, k = n = 4096 ----------------
+    work = [qmm_synth.workload("bf16_gemv"), qmm_synth.workload("f16_gemv")]
+    wbytes_each = work[0][3].size
+    ncop = r.copies_for(wbytes_each)
+    wcopies = [r.weights(w, ncop) for (_, _, _, w, _) in work]
+    xs = [torch.from_numpy(x).to(device) for (*_, x) in work]
+    ys = [torch.empty((1, n), device=device) for (_, _, n, _, _) in work]
+    argsets = [[q.make_args(fmt, wc[c], xs[i], ys[i], k, n, 1, stream=stream)
+                for c in range(ncop)] for i, ((fmt, k, n, _, _), wc) in enumerate(zip(work, wcopies))]
+    import ctypes
+    refs = [[ctypes.byref(a) for a in al] for al in argsets]
+    mm = lib.qmm_matmul_ex
+
+    def step(c):
+        if mm(refs[0][c]) or mm(refs[1][c]):
+            raise RuntimeError(q.qmm_last_error())
+
+    for i in range(max(args.warmup, 3)):
+        step(i % ncop)
+    torch.cuda.synchronize()
+    q.qmm_device_status(stream)
+    # per-kernel events inside the timed region: bf16 launch between e[i] and m[i]
+    K = args.steps
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_c = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(K):
+            c = i % ncop
+            ev_a[i].record(stream)
+            if mm(refs[0][c]):
+                raise RuntimeError(q.qmm_last_error())
+            ev_b[i].record(stream)
+            if mm(refs[1][c]):
+                raise RuntimeError(q.qmm_last_error())
+            ev_c[i].record(stream)
+        end.record(stream)
+        end.synchronize()
+        time.sleep(0.3)
+    torch.cuda.synchronize()
+    barrier(ws)
+    elapsed = start.elapsed_time(end) / 1e3
+    elapsed = max_over_ranks(elapsed, ws, device)
+    q.qmm_device_status(stream)
+    t_bf16 = sum(ev_a[i].elapsed_time(ev_b[i]) for i in range(K)) / K / 1e3
+    t_f16 = sum(ev_b[i].elapsed_time(ev_c[i]) for i in range(K)) / K / 1e3
+    ms_per_step = elapsed / K * 1e3
+    value = ws * 2 * wbytes_each / (elapsed / K) / 1e9
+    clocks = clk.summary()
+
+    # ---------------- e2e: host buffers through qmm_matmul_host ----------------
+    e2e = None
+    try:
+        hw = [torch.from_numpy(w).pin_memory() for (_, _, _, w, _) in work]
+        hx = [torch.from_numpy(x).pin_memory() for (*_, x) in work]
+        hy = [torch.empty((1, n)).pin_memory() for (_, _, n, _, _) in work]
+        dw = [wc[0] for wc in wcopies]
+        hargs = [q.make_args(fmt, hw[i], hx[i], hy[i], k, n, 1, stream=stream)
+                 for i, (fmt, k, n, _, _) in enumerate(work)]
+
+        def e2e_step():
+            for i in range(2):
+                q.qmm_matmul_host(hargs[i], dw[i], xs[i], ys[i])
+            stream.synchronize()   # y must be on the host at the end of the step
+
+        for _ in range(3):
+            e2e_step()
+        ek = max(5, K // 4)
+        t0 = time.perf_counter()
+        for _ in range(ek):
+            e2e_step()
+        et = max_over_ranks((time.perf_counter() - t0) / ek, ws, device)
+        h2d = sum(w.size + x.nbytes for (_, _, _, w, x) in work)
+        d2h = sum(4 * n for (_, _, n, _, _) in work)
+        e2e = {"value": ws * 2 * wbytes_each / et / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": et * 1e3,
+               "note": "qmm_matmul_host: pinned host W and x copied in, y copied out, stream synchronized, every step"}
+    except Exception as ex:  # pragma: no cover - reported, not hidden
+        e2e = {"value": None, "unit": "GB/s", "error": str(ex)[:200]}
+
+    # ---------------- other workloads of the path ----------------
+    others = {}
+    if rank == 0 and not args.quick:
+        others = measure_other_workloads(torch, q, lib, r, stream, hbm_peak, tc_peak)
+
+    # roofline of the dominant kernel (bf16 GEMV)
+    achieved = wbytes_each / t_bf16 / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+            "frac": achieved / hbm_peak, "traffic": recorded_traffic("gemv_bf16_4096x4096"),
+            "kernel": "gemv_kernel<BF16> (k=n=4096)", "peak_source": f"{peak_src} hbm_gbs",
+            "f16_kernel_gbs": wbytes_each / t_f16 / 1e9}
+
+    line = {"metric": "effective weight GB/s", "value": value, "unit": "GB/s", "n_gpus": ws,
+            "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
+            "data": "synthetic",
+            "config": {"workload": "bf16+f16 GEMV k=n=4096, 1 token (one step = both GEMVs)",
+                       "weight_bytes_per_step": 2 * wbytes_each,
+                       "l2": f"rotating {ncop} distinct weight copies per format (> 3x L2 of {r.l2 >> 20} MiB)",
+                       "parallelism": f"replicas x{ws}"},
+            "roofline": roof, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": 2 * K,
+            "other_workloads": others}
+    if rank == 0 and not args.quick:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_other_workloads(torch, q, lib, r, stream, hbm_peak, tc_peak):
+    import ctypes
+    out = {}
+    mm = lib.qmm_matmul_ex
+    dev = r.dev
+
+    def gemv_case(name, tiles=1, reps=50):
+        fmt, k, n, w, x = qmm_synth.workload(name)
+        ncop = r.copies_for(w.size)
+        wc = r.weights(w, ncop)
+        xd = torch.from_numpy(x).to(dev)
+        yd = torch.empty((1, n), device=dev)
+        tile = n // tiles
+        al = [[ctypes.byref(q.make_args(fmt, wc[c], xd, yd, k, n, 1, j_start=t * tile,
+                                        j_end=(t + 1) * tile, accumulate=False, stream=stream))
+               for t in range(tiles)] for c in range(ncop)]
+        keep = al  # noqa: F841
+
+        def launch(c):
+            for a in al[c]:
+                if mm(a):
+                    raise RuntimeError(q.qmm_last_error())
+        dt = time_loop(torch, launch, reps, 5, ncop, stream)
+        q.qmm_device_status(stream)
+        gbs = w.size / dt / 1e9
+        return {"us": dt * 1e6, "weight_gbs": gbs, "frac_hbm": gbs / hbm_peak,
+                "weight_bytes": int(w.size), "launches_per_call": tiles}
+
+    out["q4_0_gemv"] = gemv_case("q4_0_gemv", reps=200)
+    out["q4_0_gemv"]["note"] = "73,728 weight bytes: launch-latency bound; fraction not meaningful"
+    out["q4_k_gemv"] = gemv_case("q4_k_gemv")
+    out["q6_k_head_8_tiles"] = gemv_case("q6_k_head", tiles=8, reps=20)
+    out["q6_k_head_untiled"] = gemv_case("q6_k_head", tiles=1, reps=20)
+
+    # Q4_K N-token product: both paths at N = 1, 8, 64, 512
+    fmt, k, n, w, _ = qmm_synth.workload("q4_k_prefill", n_tokens=1)
+    ncop = r.copies_for(w.size)
+    wc = r.weights(w, ncop)
+    pre = {}
+    for nt in (1, 8, 64, 512):
+        _, _, _, _, x = qmm_synth.workload("q4_k_prefill", n_tokens=nt)
+        xd = torch.from_numpy(x).to(dev)
+        yd = torch.empty((nt, n), device=dev)
+        ws_bytes = 0
+        row = {}
+        for pname, path in (("gemv", q.PATH_GEMV), ("mma", q.PATH_MMA)):
+            if pname == "gemv" and nt > 64:
+                continue
+            a0 = q.make_args(fmt, wc[0], xd, yd, k, n, nt, path=path, stream=stream)
+            need = q.qmm_workspace_bytes(a0)
+            wsb = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+            al = [q.make_args(fmt, wc[c], xd, yd, k, n, nt, path=path, workspace=wsb if need else None,
+                              workspace_bytes=need, stream=stream) for c in range(ncop)]
+            refs = [ctypes.byref(a) for a in al]
+
+            def launch(c, refs=refs):
+                if mm(refs[c]):
+                    raise RuntimeError(q.qmm_last_error())
+            reps = 20 if nt >= 64 else 50
+            dt = time_loop(torch, launch, reps, 5, ncop, stream)
+            q.qmm_device_status(stream)
+            flops = 2.0 * nt * k * n
+            row[pname] = {"us": dt * 1e6, "tflops": flops / dt / 1e12,
+                          "frac_bf16_peak": flops / dt / 1e12 / tc_peak,
+                          "weight_gbs": w.size / dt / 1e9}
+        pre[f"N={nt}"] = row
+    out["q4_k_prefill"] = pre
+    return out
+
+
+def run_case(args):
+    """One workload alone, for profiling: warmup + steps calls, per-call time printed."""
+    import ctypes
+    import torch
+    import quantized_weight_gguf_gb300 as q
+    device = torch.device("cuda:0")
+    torch.cuda.set_device(device)
+    lib = q.load()
+    r = Runner(torch, q, device)
+    stream = r.stream
+    name = args.case
+    nt = 1
+    path = q.PATH_AUTO
+    if name.startswith("q4_k_prefill"):
+        nt = int(name.split("N")[-1]) if "N" in name else 512
+        base = "q4_k_prefill"
+        if name.endswith("_gemv"):
+            path = q.PATH_GEMV
+    else:
+        base = name
+    fmt, k, n, w, x = qmm_synth.workload(base, n_tokens=nt)
+    ncop = 1 if args.no_rotate else r.copies_for(w.size)
+    wc = r.weights(w, ncop)
+    xd = torch.from_numpy(x).to(device)
+    yd = torch.empty((x.shape[0], n), device=device)
+    a0 = q.make_args(fmt, wc[0], xd, yd, k, n, x.shape[0], path=path, stream=stream)
+    need = q.qmm_workspace_bytes(a0)
+    wsb = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+    al = [q.make_args(fmt, wc[c], xd, yd, k, n, x.shape[0], path=path,
+                      workspace=wsb if need else None, workspace_bytes=need, stream=stream)
+          for c in range(ncop)]
+    refs = [ctypes.byref(a) for a in al]
+
+    def launch(c):
+        if lib.qmm_matmul_ex(refs[c]):
+            raise RuntimeError(q.qmm_last_error())
+    dt = time_loop(torch, launch, args.steps, args.warmup, ncop, stream)
+    q.qmm_device_status(stream)
+    print(json.dumps({"case": name, "us_per_call": dt * 1e6, "weight_gbs": w.size / dt / 1e9,
+                      "tflops": 2.0 * x.shape[0] * k * n / dt / 1e12, "copies": ncop}), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--case", default=None,
+                    help="profile one workload alone (bf16_gemv, f16_gemv, q4_0_gemv, q4_k_gemv, "
+                         "q6_k_head, q4_k_prefill_N<tokens>[_gemv])")
+    ap.add_argument("--no-rotate", action="store_true")
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--quick", action="store_true", help="headline only (no other workloads, no CPU baseline)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.case:
+        return run_case(args)
+    return run_native(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,162 @@
+/*
+ * qmm.h -- C ABI of libqmm: fused dequantize-and-multiply y = x @ W on one
+ * NVIDIA GB300 GPU (sm_103a), with W kept in its GGUF/ggml packed bytes.
+ *
+ * The operation (rullama 0.5.0, src/backend/matmul.rs, module doc and the
+ * `matmul_bf16` / `matmul_f16` / `matmul_q4_0` / `matmul_q4_k` /
+ * `matmul_q6_k` dispatchers): W is n rows of k weights, row-major; row j
+ * holds the k weights of output column j, packed in one of five formats.
+ * x holds n_tokens rows of k fp32 activations (the batched tests of the same
+ * page stack tokens as X[N x k] -> Y[N x n]); y[t][j] = sum_i x[t][i] *
+ * w[j][i], fp32. Output-axis tiling follows `MatmulBackInputParams` in
+ * rullama src/backend/dispatch/mod.rs: only columns j in [j_start, j_end)
+ * are computed; the first tile writes (accumulate = 0), later tiles add
+ * (accumulate = 1).
+ *
+ * Conventions shared by every entry point:
+ *  - Data pointers are DEVICE pointers owned by the caller (except in
+ *    qmm_matmul_host). The library keeps no reference after a call returns.
+ *  - Calls are stream-ordered and asynchronous: they validate on the host,
+ *    enqueue kernels on the given stream and return. Nothing is copied to
+ *    or from the host and nothing synchronizes, except the documented
+ *    first-use set-up.
+ *  - Invalid arguments are rejected on the host before anything is
+ *    enqueued; the call returns a qmm_status and qmm_last_error() holds a
+ *    message (per host thread).
+ *  - Layouts: w is n * qmm_weight_bytes(fmt, k, 1) bytes; x is [n_tokens][k]
+ *    fp32 row-major; y is [n_tokens][n] fp32 row-major (row stride n even
+ *    when only a column tile is computed).
+ *  - Alignment: w must be 16-byte aligned (its rows are streamed with bulk
+ *    copies); x and y must be 4-byte aligned. Otherwise QMM_ERR_ALIGN.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Weight formats. Block geometry from the rullama matmul.rs dispatchers:
+ * BF16 / F16: 2 bytes per weight, k even.
+ * Q4_0: blocks of 32 weights in 18 bytes (f16 d + 16 nibble bytes), k % 32 == 0.
+ * Q4_K: super-blocks of 256 weights in 144 bytes (f16 d, f16 dmin,
+ *       12 bytes of 6-bit scales/mins, 128 nibble bytes), k % 256 == 0.
+ * Q6_K: super-blocks of 256 weights in 210 bytes (128 low-nibble bytes,
+ *       64 high-bit bytes, 16 int8 scales, f16 d), k % 256 == 0.
+ * Inside the blocks the fields follow the standard ggml layouts. */
+typedef enum qmm_format {
+    QMM_BF16 = 0,
+    QMM_F16 = 1,
+    QMM_Q4_0 = 2,
+    QMM_Q4_K = 3,
+    QMM_Q6_K = 4
+} qmm_format;
+
+typedef enum qmm_status {
+    QMM_OK = 0,
+    QMM_ERR_FORMAT = 1,          /* unknown format code */
+    QMM_ERR_SHAPE = 2,           /* k not a multiple of the block, negative sizes, n_tokens < 1 */
+    QMM_ERR_SIZE = 3,            /* w_len given and != n * row bytes */
+    QMM_ERR_RANGE = 4,           /* not 0 <= j_start <= j_end <= n */
+    QMM_ERR_NULL = 5,            /* a pointer needed for the call is NULL */
+    QMM_ERR_ALIGN = 6,           /* w not 16-byte aligned, or x / y not 4-byte aligned */
+    QMM_ERR_CUDA = 7,            /* a CUDA runtime call failed (message has the CUDA error) */
+    QMM_ERR_DEVICE_TIMEOUT = 8,  /* a kernel gave up waiting on a pipeline barrier (reported by qmm_device_status) */
+    QMM_ERR_WORKSPACE = 9,       /* workspace given but smaller than qmm_workspace_bytes() */
+    QMM_ERR_UNSUPPORTED = 10     /* current device is not compute capability 10.3, or the path cannot take the shape */
+} qmm_status;
+
+/* Kernel path selection for qmm_args.path. */
+typedef enum qmm_path {
+    QMM_PATH_AUTO = 0,   /* by n_tokens: GEMV for small N, tensor-core (tcgen05) MMA above the crossover */
+    QMM_PATH_GEMV = 1,   /* force the streaming GEMV kernel (one launch per token) */
+    QMM_PATH_MMA = 2     /* force the tcgen05 N-token kernel */
+} qmm_path;
+
+typedef struct qmm_args {
+    int fmt;                 /* qmm_format */
+    const void *w;           /* device, n * row_bytes packed weight bytes, 16-byte aligned */
+    size_t w_len;            /* bytes the caller holds at w; 0 = not checked */
+    const float *x;          /* device, [n_tokens][k] */
+    float *y;                /* device, [n_tokens][n]; read too when accumulate != 0 */
+    int64_t k;               /* weights per row (reduction length) */
+    int64_t n;               /* rows of W = output columns */
+    int64_t n_tokens;        /* rows of x and y, >= 1 */
+    int64_t j_start, j_end;  /* output columns computed; both 0 means [0, n) */
+    int accumulate;          /* 0: y[t][j] = sum; else y[t][j] += sum (columns outside the tile untouched) */
+    int path;                /* qmm_path */
+    void *workspace;         /* device scratch for the MMA path, or NULL (library-owned grow-only buffer) */
+    size_t workspace_bytes;  /* bytes at workspace */
+    void *stream;            /* cudaStream_t; NULL = legacy default stream */
+} qmm_args;
+
+/* Bytes of n packed rows of k weights: (k/32)*18*n, (k/256)*144*n,
+ * (k/256)*210*n or 2*k*n (rullama matmul.rs shape checks). 0 when fmt is
+ * unknown, k does not fit the format, or k/n is negative. Host only. */
+size_t qmm_weight_bytes(int fmt, int64_t k, int64_t n);
+
+/* y = x @ W over the whole output axis, on the stream last given to
+ * qmm_set_stream (default: the legacy default stream), auto path, workspace
+ * from the library's own grow-only buffer. The spec signature:
+ * qmm_matmul(fmt, w_bytes, x, k, n, n_tokens, y). Returns a qmm_status. */
+int qmm_matmul(int fmt, const void *w, const float *x, int64_t k, int64_t n,
+               int64_t n_tokens, float *y);
+
+/* Stream used by qmm_matmul on the calling host thread (a cudaStream_t). */
+void qmm_set_stream(void *stream);
+
+/* Full form: column tile, accumulate, path, workspace and stream.
+ * k == 0 writes zeros to the tile's columns (or leaves them when
+ * accumulating); n == 0 or an empty tile enqueues nothing. */
+int qmm_matmul_ex(const qmm_args *a);
+
+/* Device scratch bytes qmm_matmul_ex needs for *a (0 for the GEMV path).
+ * The MMA path keeps an fp16 copy of x (k padded to a multiple of 64) plus
+ * one power-of-two scale per token; where it splits x into two fp16 terms
+ * (16-bit weight formats, and K-quant / Q4_0 weights with k < 4096) it keeps
+ * two copies: c * round256(n_tokens * kp * 2) + round256(n_tokens * 4) with
+ * c = 1 or 2. Host only. */
+size_t qmm_workspace_bytes(const qmm_args *a);
+
+/* Which kernel path qmm_matmul_ex would run for *a (a qmm_path value other
+ * than AUTO), or -1 if *a is invalid. Host only. */
+int qmm_select_path(const qmm_args *a);
+
+/* Host-buffer form of qmm_matmul_ex, matching the pages' one-shot
+ * dispatchers that take weight bytes and x from the host and return y
+ * (rullama matmul.rs `dispatch_matmul`). a->w, a->x and a->y are HOST
+ * pointers (page-locked memory makes the copies asynchronous); dev_w,
+ * dev_x and dev_y are caller-owned device buffers at least as large as W,
+ * x and y. Enqueues W -> dev_w, x -> dev_x (and y -> dev_y when
+ * accumulating), the product, then dev_y -> y, all on a->stream; the caller
+ * synchronizes the stream before reading y. */
+int qmm_matmul_host(const qmm_args *a, void *dev_w, float *dev_x, float *dev_y);
+
+/* Standalone dequantization: out[j][i] = the fp32 value of weight i of row
+ * j, bit-identical to the exact value rounded once to fp32 (only Q4_K's
+ * d*sc*q - dmin*m rounds; every other product is exact). out is device
+ * [n][k] fp32. Stream-ordered. */
+int qmm_dequant(int fmt, const void *w, int64_t k, int64_t n, float *out, void *stream);
+
+/* Synchronizes `stream`, then reports whether any kernel enqueued so far
+ * timed out on a pipeline barrier (QMM_ERR_DEVICE_TIMEOUT) and clears the
+ * flag; QMM_OK otherwise, QMM_ERR_CUDA if the synchronize failed. Every
+ * barrier wait in the kernels is bounded (about 2 s); on expiry the kernel
+ * records the fault, stops its pipeline, releases its tensor memory and
+ * returns, so the context stays usable. */
+int qmm_device_status(void *stream);
+
+/* Message for the last non-OK status on this host thread ("" if none). */
+const char *qmm_last_error(void);
+
+/* ABI version (major * 100 + minor). */
+int qmm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H */

@@ -113,6 +113,14 @@ def matmul(fmt: str, w: np.ndarray, x: np.ndarray, k: int, n: int):
     return y, s
 
 
+def matmul_blas(fmt: str, w: np.ndarray, x: np.ndarray, k: int, n: int):
+    """Same (y, S) as matmul, with the dot products done by numpy's f64 matrix
+    product over the oracle's own fp32 weights (for full-size checks)."""
+    deq = dequant(fmt, w, k, n).astype(np.float64)
+    x64 = np.atleast_2d(np.asarray(x, np.float64))
+    return x64 @ deq.T, np.abs(x64) @ np.abs(deq).T
+
+
 def matmul_sampled(fmt: str, w: np.ndarray, x: np.ndarray, k: int, n: int, t_idx, j_idx):
     """(y, S) for the outputs (t_idx[c], j_idx[c]) only."""
     w = np.ascontiguousarray(w, dtype=np.uint8)

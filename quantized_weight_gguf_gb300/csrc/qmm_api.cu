@@ -1,0 +1,332 @@
+// qmm_api.cu -- the C ABI declared in include/qmm.h: host-side validation,
+// path policy, workspace, stream handling and error reporting. Launches only;
+// no host synchronisation on the compute path.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/qmm.h"
+#include "qmm_device.cuh"
+#include "qmm_internal.h"
+
+namespace {
+
+// Device error word: kernels record the first barrier timeout here.
+__device__ unsigned int g_err_word;
+
+thread_local char t_err[512] = "";
+thread_local cudaStream_t t_stream = nullptr;
+
+int fail(int status, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_err, sizeof t_err, fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+qmm::DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ok[kMaxDevices];
+
+// Library-owned grow-only workspace per device (used when the caller passes none).
+void *g_ws[kMaxDevices];
+size_t g_ws_bytes[kMaxDevices];
+
+// Largest token count for which the GEMV path (one launch per token) is used
+// by default; above it the tensor-core path wins.
+constexpr int64_t kGemvMaxTokens = 1;
+
+int device_info(qmm::DeviceInfo **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(QMM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(QMM_ERR_UNSUPPORTED, "device index %d", dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_dev_ok[dev]) {
+        qmm::DeviceInfo d;
+        cudaDeviceProp prop;
+        e = cudaGetDeviceProperties(&prop, dev);
+        if (e != cudaSuccess)
+            return fail(QMM_ERR_CUDA, "cudaGetDeviceProperties: %s", cudaGetErrorString(e));
+        d.sm_count = prop.multiProcessorCount;
+        d.major = prop.major;
+        d.minor = prop.minor;
+        d.smem_optin = prop.sharedMemPerBlockOptin;
+        if (d.major != 10 || d.minor != 3)
+            return fail(QMM_ERR_UNSUPPORTED,
+                        "libqmm is built for sm_103a only; device %d is compute capability %d.%d",
+                        dev, d.major, d.minor);
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_err_word);
+        if (e != cudaSuccess)
+            return fail(QMM_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        d.err = static_cast<unsigned int *>(p);
+        g_dev[dev] = d;
+        g_dev_ok[dev] = true;
+    }
+    *out = &g_dev[dev];
+    return QMM_OK;
+}
+
+int64_t row_bytes_of(int fmt, int64_t k) {
+    switch (fmt) {
+    case QMM_BF16:
+    case QMM_F16: return (k % 2 == 0) ? 2 * k : -1;
+    case QMM_Q4_0: return (k % 32 == 0) ? (k / 32) * 18 : -1;
+    case QMM_Q4_K: return (k % 256 == 0) ? (k / 256) * 144 : -1;
+    case QMM_Q6_K: return (k % 256 == 0) ? (k / 256) * 210 : -1;
+    default: return -1;
+    }
+}
+
+const char *fmt_name(int fmt) {
+    static const char *names[] = {"BF16", "F16", "Q4_0", "Q4_K", "Q6_K"};
+    return (fmt >= 0 && fmt <= 4) ? names[fmt] : "?";
+}
+
+// Shape/pointer validation shared by the entry points. On success fills the
+// effective tile and row bytes.
+int validate(const qmm_args *a, int64_t *j0, int64_t *j1, int64_t *rb, bool check_ptrs) {
+    if (!a) return fail(QMM_ERR_NULL, "args is NULL");
+    if (a->fmt < QMM_BF16 || a->fmt > QMM_Q6_K)
+        return fail(QMM_ERR_FORMAT, "unknown format code %d", a->fmt);
+    if (a->k < 0 || a->n < 0) return fail(QMM_ERR_SHAPE, "negative k or n (k=%lld n=%lld)",
+                                          (long long)a->k, (long long)a->n);
+    if (a->n_tokens < 1) return fail(QMM_ERR_SHAPE, "n_tokens %lld < 1", (long long)a->n_tokens);
+    const int64_t r = row_bytes_of(a->fmt, a->k);
+    if (r < 0) {
+        const char *need = (a->fmt == QMM_Q4_0) ? "a multiple of 32"
+                           : (a->fmt == QMM_Q4_K || a->fmt == QMM_Q6_K) ? "a multiple of 256"
+                                                                        : "even";
+        return fail(QMM_ERR_SHAPE, "k %lld must be %s for %s matmul", (long long)a->k, need,
+                    fmt_name(a->fmt));
+    }
+    if (a->w_len != 0 && a->w_len != (size_t)(r * a->n))
+        return fail(QMM_ERR_SIZE, "%s W bytes %zu != row_bytes*n = %lld", fmt_name(a->fmt),
+                    a->w_len, (long long)(r * a->n));
+    int64_t s = a->j_start, e = a->j_end;
+    if (s == 0 && e == 0) e = a->n;
+    if (s < 0 || s > e || e > a->n)
+        return fail(QMM_ERR_RANGE, "tile [%lld, %lld) not within [0, %lld]", (long long)s,
+                    (long long)e, (long long)a->n);
+    *j0 = s;
+    *j1 = e;
+    *rb = r;
+    if (check_ptrs && e > s) {
+        if (!a->y) return fail(QMM_ERR_NULL, "y is NULL");
+        if (a->k > 0 && (!a->w || !a->x)) return fail(QMM_ERR_NULL, "w or x is NULL");
+        if (a->k > 0 && (reinterpret_cast<uintptr_t>(a->w) & 15u))
+            return fail(QMM_ERR_ALIGN, "w must be 16-byte aligned");
+        if ((a->k > 0 && (reinterpret_cast<uintptr_t>(a->x) & 3u)) ||
+            (reinterpret_cast<uintptr_t>(a->y) & 3u))
+            return fail(QMM_ERR_ALIGN, "x and y must be 4-byte aligned");
+    }
+    if (a->path < QMM_PATH_AUTO || a->path > QMM_PATH_MMA)
+        return fail(QMM_ERR_SHAPE, "unknown path %d", a->path);
+    return QMM_OK;
+}
+
+int choose_path(const qmm_args *a) {
+    if (a->path == QMM_PATH_GEMV) return QMM_PATH_GEMV;
+    if (a->path == QMM_PATH_MMA) return QMM_PATH_MMA;
+    if (a->n_tokens <= kGemvMaxTokens && qmm::gemv_supports(a->fmt, a->k)) return QMM_PATH_GEMV;
+    return QMM_PATH_MMA;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(QMM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int run(const qmm_args *a) {
+    int64_t j0, j1, rb;
+    int st = validate(a, &j0, &j1, &rb, true);
+    if (st != QMM_OK) return st;
+    if (j1 <= j0) return QMM_OK;
+    qmm::DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != QMM_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(a->stream);
+    if (a->k == 0) {
+        if (a->accumulate) return QMM_OK;
+        cudaError_t e = qmm::launch_zero_cols(a->y, a->n_tokens, a->n, j0, j1, s);
+        return e == cudaSuccess ? QMM_OK : cuda_fail(e, "zero-fill launch");
+    }
+    const int path = choose_path(a);
+    if (path == QMM_PATH_GEMV) {
+        if (!qmm::gemv_supports(a->fmt, a->k))
+            return fail(QMM_ERR_UNSUPPORTED, "GEMV path cannot take %s with k=%lld",
+                        fmt_name(a->fmt), (long long)a->k);
+        for (int64_t t = 0; t < a->n_tokens; ++t) {
+            qmm::GemvLaunch g;
+            g.fmt = a->fmt;
+            g.w = static_cast<const uint8_t *>(a->w);
+            g.x = a->x + t * a->k;
+            g.y = a->y + t * a->n;
+            g.k = a->k; g.n = a->n; g.row_bytes = rb;
+            g.j0 = j0; g.j1 = j1;
+            g.accumulate = a->accumulate;
+            cudaError_t e = qmm::launch_gemv(g, *dev, s);
+            if (e != cudaSuccess) return cuda_fail(e, "GEMV launch");
+        }
+        return QMM_OK;
+    }
+    const size_t need = qmm::mma_workspace_bytes(a->fmt, a->n_tokens, a->k);
+    void *ws = a->workspace;
+    if (ws) {
+        if (a->workspace_bytes < need)
+            return fail(QMM_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", a->workspace_bytes,
+                        need);
+        if (reinterpret_cast<uintptr_t>(ws) & 255u)
+            return fail(QMM_ERR_ALIGN, "workspace must be 256-byte aligned");
+    } else {
+        int d = 0;
+        cudaGetDevice(&d);
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_ws_bytes[d] < need) {
+            // grow-only; the old buffer may still be in use by queued work
+            cudaError_t e = cudaDeviceSynchronize();
+            if (e != cudaSuccess) return cuda_fail(e, "workspace grow sync");
+            if (g_ws[d]) cudaFree(g_ws[d]);
+            g_ws[d] = nullptr;
+            g_ws_bytes[d] = 0;
+            e = cudaMalloc(&g_ws[d], need);
+            if (e != cudaSuccess) return cuda_fail(e, "workspace cudaMalloc");
+            g_ws_bytes[d] = need;
+        }
+        ws = g_ws[d];
+    }
+    qmm::MmaLaunch m;
+    m.fmt = a->fmt;
+    m.w = static_cast<const uint8_t *>(a->w);
+    m.x = a->x;
+    m.y = a->y;
+    m.k = a->k; m.n = a->n; m.n_tokens = a->n_tokens; m.row_bytes = rb;
+    m.j0 = j0; m.j1 = j1;
+    m.accumulate = a->accumulate;
+    m.workspace = ws;
+    cudaError_t e = qmm::launch_mma(m, *dev, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tensor-core launch");
+    return QMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t qmm_weight_bytes(int fmt, int64_t k, int64_t n) {
+    if (k < 0 || n < 0) return 0;
+    const int64_t r = row_bytes_of(fmt, k);
+    return r < 0 ? 0 : (size_t)(r * n);
+}
+
+void qmm_set_stream(void *stream) { t_stream = static_cast<cudaStream_t>(stream); }
+
+int qmm_matmul(int fmt, const void *w, const float *x, int64_t k, int64_t n, int64_t n_tokens,
+               float *y) {
+    qmm_args a;
+    std::memset(&a, 0, sizeof a);
+    a.fmt = fmt;
+    a.w = w;
+    a.x = x;
+    a.y = y;
+    a.k = k;
+    a.n = n;
+    a.n_tokens = n_tokens;
+    a.stream = t_stream;
+    t_err[0] = 0;
+    return run(&a);
+}
+
+int qmm_matmul_ex(const qmm_args *a) {
+    t_err[0] = 0;
+    return run(a);
+}
+
+size_t qmm_workspace_bytes(const qmm_args *a) {
+    int64_t j0, j1, rb;
+    if (validate(a, &j0, &j1, &rb, false) != QMM_OK) return 0;
+    if (a->k == 0 || j1 <= j0 || choose_path(a) != QMM_PATH_MMA) return 0;
+    return qmm::mma_workspace_bytes(a->fmt, a->n_tokens, a->k);
+}
+
+int qmm_select_path(const qmm_args *a) {
+    int64_t j0, j1, rb;
+    if (validate(a, &j0, &j1, &rb, false) != QMM_OK) return -1;
+    return choose_path(a);
+}
+
+int qmm_matmul_host(const qmm_args *a, void *dev_w, float *dev_x, float *dev_y) {
+    t_err[0] = 0;
+    int64_t j0, j1, rb;
+    int st = validate(a, &j0, &j1, &rb, true);
+    if (st != QMM_OK) return st;
+    if (j1 <= j0) return QMM_OK;
+    if (!dev_w || !dev_x || !dev_y) return fail(QMM_ERR_NULL, "device staging buffer is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(a->stream);
+    const size_t wb = (size_t)(rb * a->n), xb = (size_t)(a->k * a->n_tokens) * 4,
+                 yb = (size_t)(a->n * a->n_tokens) * 4;
+    cudaError_t e;
+    if (wb && (e = cudaMemcpyAsync(dev_w, a->w, wb, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(e, "copy W to device");
+    if (xb && (e = cudaMemcpyAsync(dev_x, a->x, xb, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(e, "copy x to device");
+    if (a->accumulate &&
+        (e = cudaMemcpyAsync(dev_y, a->y, yb, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(e, "copy y to device");
+    qmm_args d = *a;
+    d.w = dev_w;
+    d.x = dev_x;
+    d.y = dev_y;
+    st = run(&d);
+    if (st != QMM_OK) return st;
+    if ((e = cudaMemcpyAsync(a->y, dev_y, yb, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return cuda_fail(e, "copy y to host");
+    return QMM_OK;
+}
+
+int qmm_dequant(int fmt, const void *w, int64_t k, int64_t n, float *out, void *stream) {
+    t_err[0] = 0;
+    if (fmt < QMM_BF16 || fmt > QMM_Q6_K) return fail(QMM_ERR_FORMAT, "unknown format code %d", fmt);
+    if (k < 0 || n < 0) return fail(QMM_ERR_SHAPE, "negative k or n");
+    const int64_t r = row_bytes_of(fmt, k);
+    if (r < 0) return fail(QMM_ERR_SHAPE, "k %lld does not fit %s blocks", (long long)k, fmt_name(fmt));
+    if (k == 0 || n == 0) return QMM_OK;
+    if (!w || !out) return fail(QMM_ERR_NULL, "w or out is NULL");
+    if ((reinterpret_cast<uintptr_t>(w) & 15u)) return fail(QMM_ERR_ALIGN, "w must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(out) & 3u)) return fail(QMM_ERR_ALIGN, "out must be 4-byte aligned");
+    qmm::DeviceInfo *dev = nullptr;
+    int st = device_info(&dev);
+    if (st != QMM_OK) return st;
+    cudaError_t e = qmm::launch_dequant(fmt, static_cast<const uint8_t *>(w), k, n, r, out,
+                                        static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QMM_OK : cuda_fail(e, "dequant launch");
+}
+
+int qmm_device_status(void *stream) {
+    t_err[0] = 0;
+    qmm::DeviceInfo *dev = nullptr;
+    int st = device_info(&dev);
+    if (st != QMM_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    unsigned int v = 0;
+    e = cudaMemcpy(&v, dev->err, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+    if (v != 0) {
+        const unsigned int zero = 0;
+        cudaMemcpy(dev->err, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        return fail(QMM_ERR_DEVICE_TIMEOUT, "a kernel gave up waiting on a pipeline barrier (code %u)", v);
+    }
+    return QMM_OK;
+}
+
+const char *qmm_last_error(void) { return t_err; }
+
+int qmm_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,514 @@
+// qmm_gemv.cu -- one-token fused dequantize + dot (GEMV), y[j] = sum_i w[j][i] x[i].
+//
+// Design (GB300, HBM-bound): each CTA owns a contiguous range of rows of W,
+// i.e. a contiguous byte range of the packed weight stream. One producer lane
+// streams it into a ring of shared-memory stages with 1-D bulk copies (TMA,
+// 16-byte aligned windows, so unaligned block formats need no special care on
+// the global side); 256 consumer threads decode from shared memory. Each
+// consumer owns a fixed "unit" of k (32 or 64 weights) for the whole kernel,
+// so its slice of x lives in registers and is read from global memory once.
+// Per stage, every consumer writes one partial sum per (row, unit) to shared
+// memory and one warp per row reduces them in a fixed order (deterministic).
+//
+// Decoding keeps the integer codes exact and out of the fp pipe as far as
+// possible: a byte permute builds the float 0.5 + q/256 from a code q < 128
+// (q lands in mantissa bits 16..22), so the dot over a sub-block is
+// sum q x = 256 * sum (0.5 + q/256) x - 128 * sum x, with sum x over each
+// unit's sub-blocks computed once per thread. Q4_0 subtracts its zero point
+// exactly instead (2^23 + q - (2^23 + 8)), so an all-zero-point block gives 0.
+#include "qmm_device.cuh"
+#include "qmm_internal.h"
+
+#include <algorithm>
+#include <mutex>
+
+namespace qmm {
+
+constexpr int kConsWarps = 8;
+constexpr int kCons = kConsWarps * 32;
+constexpr int kGemvThreads = kCons + 32;
+
+struct GemvParams {
+    const uint8_t *w;
+    const float *x;
+    float *y;
+    int64_t k, row_bytes, w_total;
+    int64_t j0;
+    int64_t rows_base;
+    int rows_rem;
+    int accumulate;
+    int U;    // units per row
+    int G;    // row groups per stage (one unit per thread), else 1
+    int PU;   // partial slots per row
+    int SR;   // rows per stage
+    int SB;   // bytes per stage buffer (multiple of 128)
+    int NS;   // stage buffers
+    unsigned int *err;
+};
+
+// Weights per unit: a 16-byte chunk for 16-bit formats (lane-contiguous in
+// shared memory), a 32-weight block for Q4_0 / a Q6_K quarter-half, and a
+// 64-weight chunk for Q4_K.
+template <int FMT>
+struct UnitK {
+    static constexpr int value = (FMT == F_Q4_K) ? 64 : (FMT == F_BF16 || FMT == F_F16) ? 8 : 32;
+};
+
+__device__ __forceinline__ uint32_t bfe(uint32_t a, uint32_t pos, uint32_t len) {
+    uint32_t d;
+    asm("bfe.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(pos), "r"(len));
+    return d;
+}
+__device__ __forceinline__ int32_t bfe_s(uint32_t a, uint32_t pos) {
+    int32_t d;
+    asm("bfe.s32 %0, %1, %2, 8;" : "=r"(d) : "r"(a), "r"(pos));
+    return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    uint64_t ra, rb, rd;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+    float2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+    return d;
+}
+
+// Per-thread constants of one unit (x slice and what is derived from it).
+template <int FMT>
+struct UnitState {
+    float xr[UnitK<FMT>::value];
+    float c0, c1, c2, c3;      // format-specific sums of x
+    uint32_t p0, p1, p2, p3;   // format-specific bit positions
+    uint32_t la, lb, lowgrp;
+};
+
+template <int FMT>
+__device__ __forceinline__ void unit_init(UnitState<FMT> &st, const float *xs, int u, bool valid) {
+    constexpr int UK = UnitK<FMT>::value;
+    if (FMT == F_Q6_K) {
+        const int b = u >> 3, h = (u >> 2) & 1, gq = u & 3;
+        const float *xb = xs + 256 * b + 128 * h + 8 * gq;
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) st.xr[8 * r + i] = valid ? xb[32 * r + i] : 0.0f;
+        float s[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            s[r] = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s[r] += st.xr[8 * r + i];
+        }
+        // sum (q - 32) x = 256 * sum (0.5 + q/256) x - 160 * sum x
+        st.c0 = -160.0f * s[0]; st.c1 = -160.0f * s[1];
+        st.c2 = -160.0f * s[2]; st.c3 = -160.0f * s[3];
+        // scale byte of quarter r sits at byte 2r + (gq >> 1) of scales[8h .. 8h+7]
+        st.p0 = 8 * (0 + (gq >> 1)); st.p1 = 8 * (2 + (gq >> 1));
+        st.p2 = st.p0; st.p3 = st.p1;
+    } else {
+        const float *xb = xs + (int64_t)UK * u;
+#pragma unroll
+        for (int i = 0; i < UK; ++i) st.xr[i] = valid ? xb[i] : 0.0f;
+        if (FMT == F_Q4_K) {
+            float slo = 0.0f, shi = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) { slo += st.xr[i]; shi += st.xr[32 + i]; }
+            st.c0 = slo; st.c1 = shi;
+            const int c = u & 3;
+            st.lowgrp = c < 2;
+            const int s0 = 2 * c, s1 = 2 * c + 1;
+            const int t0 = s0 >= 4 ? s0 - 4 : 0, t1 = s1 >= 4 ? s1 - 4 : 0;
+            // scale of sub-block s: low group -> bits 8s..8s+5 of word 0;
+            // high group -> bits 8t..8t+3 of word 2 | (bits 8t+6..8t+7 of word 0) << 4.
+            st.la = st.lowgrp ? 6u : 4u;
+            st.lb = st.lowgrp ? 0u : 2u;
+            st.p0 = st.lowgrp ? 8 * s0 : 8 * t0;  // scale, field A, sub-block 2c
+            st.p1 = st.lowgrp ? 8 * s1 : 8 * t1;  // scale, field A, sub-block 2c+1
+            st.p2 = 8 * t0 + 6;                   // field B (top bits), sub-block 2c
+            st.p3 = 8 * t1 + 6;                   // field B, sub-block 2c+1
+        }
+    }
+}
+
+// Partial dot of one unit of one row; `rowa` is the row's shared address.
+template <int FMT>
+__device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<FMT> &st) {
+    if (FMT == F_BF16 || FMT == F_F16) {
+        const uint4 v = lds128(rowa + 16u * u);
+        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+        float2 a0 = make_float2(0.f, 0.f), a1 = a0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 wf;
+            if (FMT == F_BF16) {
+                wf.x = __uint_as_float(wd[i] << 16);
+                wf.y = __uint_as_float(wd[i] & 0xFFFF0000u);
+            } else {
+                wf = __half22float2(*reinterpret_cast<const __half2 *>(&wd[i]));
+            }
+            const float2 xv = make_float2(st.xr[2 * i], st.xr[2 * i + 1]);
+            if (i & 1) a1 = ffma2(wf, xv, a1); else a0 = ffma2(wf, xv, a0);
+        }
+        return (a0.x + a0.y) + (a1.x + a1.y);
+    } else if (FMT == F_Q4_0) {
+        const uint32_t base = rowa + 18u * u;
+        const float d = f16_bits_to_f32(lds16(base));
+        uint32_t qw[4];
+        lds_words_a2<4>(base + 2, qw);
+        const float2 zp = make_float2(-8388616.0f, -8388616.0f);  // -(2^23 + 8)
+        float2 a0 = make_float2(0.f, 0.f), a1 = a0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = qw[i] & 0x0F0F0F0Fu, hi = (qw[i] >> 4) & 0x0F0F0F0Fu;
+            float2 f;
+            f = fadd2(make_float2(byte_magic23<0>(lo), byte_magic23<1>(lo)), zp);
+            a0 = ffma2(f, make_float2(st.xr[4 * i], st.xr[4 * i + 1]), a0);
+            f = fadd2(make_float2(byte_magic23<2>(lo), byte_magic23<3>(lo)), zp);
+            a1 = ffma2(f, make_float2(st.xr[4 * i + 2], st.xr[4 * i + 3]), a1);
+            f = fadd2(make_float2(byte_magic23<0>(hi), byte_magic23<1>(hi)), zp);
+            a0 = ffma2(f, make_float2(st.xr[16 + 4 * i], st.xr[16 + 4 * i + 1]), a0);
+            f = fadd2(make_float2(byte_magic23<2>(hi), byte_magic23<3>(hi)), zp);
+            a1 = ffma2(f, make_float2(st.xr[16 + 4 * i + 2], st.xr[16 + 4 * i + 3]), a1);
+        }
+        return d * ((a0.x + a0.y) + (a1.x + a1.y));
+    } else if (FMT == F_Q4_K) {
+        const int b = u >> 2, c = u & 3;
+        const uint32_t sb = rowa + 144u * b;
+        const uint4 hdr = lds128(sb);
+        const uint4 q0 = lds128(sb + 16u + 32u * c);
+        const uint4 q1 = lds128(sb + 32u + 32u * c);
+        const float d = f16_bits_to_f32(hdr.x & 0xFFFFu);
+        const float dmin = f16_bits_to_f32(hdr.x >> 16);
+        const uint32_t srcA_sc = st.lowgrp ? hdr.y : hdr.w;
+        const uint32_t srcA_m = st.lowgrp ? hdr.z : hdr.w;
+        const uint32_t off_m = st.lowgrp ? 0u : 4u;
+        const uint32_t sc0 = bfe(srcA_sc, st.p0, st.la) | (bfe(hdr.y, st.p2, st.lb) << 4);
+        const uint32_t sc1 = bfe(srcA_sc, st.p1, st.la) | (bfe(hdr.y, st.p3, st.lb) << 4);
+        const uint32_t m0 = bfe(srcA_m, st.p0 + off_m, st.la) | (bfe(hdr.z, st.p2, st.lb) << 4);
+        const uint32_t m1 = bfe(srcA_m, st.p1 + off_m, st.la) | (bfe(hdr.z, st.p3, st.lb) << 4);
+        const uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        float2 l0 = make_float2(0.f, 0.f), l1 = l0, h0 = l0, h1 = l0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t lo = wd[i] & 0x0F0F0F0Fu, hi = (wd[i] >> 4) & 0x0F0F0F0Fu;
+            l0 = ffma2(make_float2(byte_half_plus<0>(lo), byte_half_plus<1>(lo)),
+                       make_float2(st.xr[4 * i], st.xr[4 * i + 1]), l0);
+            l1 = ffma2(make_float2(byte_half_plus<2>(lo), byte_half_plus<3>(lo)),
+                       make_float2(st.xr[4 * i + 2], st.xr[4 * i + 3]), l1);
+            h0 = ffma2(make_float2(byte_half_plus<0>(hi), byte_half_plus<1>(hi)),
+                       make_float2(st.xr[32 + 4 * i], st.xr[32 + 4 * i + 1]), h0);
+            h1 = ffma2(make_float2(byte_half_plus<2>(hi), byte_half_plus<3>(hi)),
+                       make_float2(st.xr[32 + 4 * i + 2], st.xr[32 + 4 * i + 3]), h1);
+        }
+        const float alo = (l0.x + l0.y) + (l1.x + l1.y);
+        const float ahi = (h0.x + h0.y) + (h1.x + h1.y);
+        const float ds0 = d * (float)sc0, ds1 = d * (float)sc1;
+        const float dm0 = dmin * (float)m0, dm1 = dmin * (float)m1;
+        // ds * sum q x - dm * sum x, with sum q x = 256 * a - 128 * sum x
+        const float r0 = fmaf(256.0f * ds0, alo, -fmaf(128.0f, ds0, dm0) * st.c0);
+        const float r1 = fmaf(256.0f * ds1, ahi, -fmaf(128.0f, ds1, dm1) * st.c1);
+        return r0 + r1;
+    } else {  // F_Q6_K
+        const int b = u >> 3, h = (u >> 2) & 1, gq = u & 3;
+        const uint32_t sb = rowa + 210u * b;
+        uint32_t A[2], B[2], H[2], S[2];
+        lds_words_a2<2>(sb + 64u * h + 8u * gq, A);
+        lds_words_a2<2>(sb + 64u * h + 32u + 8u * gq, B);
+        lds_words_a2<2>(sb + 128u + 32u * h + 8u * gq, H);
+        lds_words_a2<2>(sb + 192u + 8u * h, S);
+        const float d = f16_bits_to_f32(lds16(sb + 208u));
+        float2 acc[4][2];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[r][0] = acc[r][1] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int wi = 0; wi < 2; ++wi) {
+            const uint32_t q[4] = {
+                (A[wi] & 0x0F0F0F0Fu) | ((H[wi] << 4) & 0x30303030u),
+                (B[wi] & 0x0F0F0F0Fu) | ((H[wi] << 2) & 0x30303030u),
+                ((A[wi] >> 4) & 0x0F0F0F0Fu) | (H[wi] & 0x30303030u),
+                ((B[wi] >> 4) & 0x0F0F0F0Fu) | ((H[wi] >> 2) & 0x30303030u)};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                acc[r][0] = ffma2(make_float2(byte_half_plus<0>(q[r]), byte_half_plus<1>(q[r])),
+                                  make_float2(st.xr[8 * r + 4 * wi], st.xr[8 * r + 4 * wi + 1]),
+                                  acc[r][0]);
+                acc[r][1] = ffma2(make_float2(byte_half_plus<2>(q[r]), byte_half_plus<3>(q[r])),
+                                  make_float2(st.xr[8 * r + 4 * wi + 2], st.xr[8 * r + 4 * wi + 3]),
+                                  acc[r][1]);
+            }
+        }
+        const float cr[4] = {st.c0, st.c1, st.c2, st.c3};
+        const uint32_t pr[4] = {st.p0, st.p1, st.p2, st.p3};
+        float sum = 0.0f;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const float a = (acc[r][0].x + acc[r][0].y) + (acc[r][1].x + acc[r][1].y);
+            const float sc = (float)bfe_s(S[r >> 1], pr[r]);
+            sum = fmaf(sc, fmaf(256.0f, a, cr[r]), sum);
+        }
+        return d * sum;
+    }
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
+                                              volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+template <int FMT, int UPT>
+__global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {
+    constexpr bool kChunked = (FMT == F_BF16 || FMT == F_F16);  // warp-reduced 16-byte chunks
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int NS = p.NS, SR = p.SR, SB = p.SB, PU = p.PU;
+    const uint32_t bar0 = smem_addr(smem);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 16 * NS);
+    float *part = reinterpret_cast<float *>(smem + 16 * NS + 16);
+    const int part_bytes = 8 * SR * PU;  // two buffers
+    const int xs_off = (16 * NS + 16 + part_bytes + 127) & ~127;
+    float *xs = reinterpret_cast<float *>(smem + xs_off);
+    const uint32_t stage_off = (uint32_t)((xs_off + 4 * (int)p.k + 127) & ~127);
+    uint8_t *stages = smem + stage_off;
+    const uint32_t stage0 = bar0 + stage_off;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (NS + s); };
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int cta = blockIdx.x;
+    const int64_t r0 = p.j0 + (int64_t)cta * p.rows_base + (cta < p.rows_rem ? cta : p.rows_rem);
+    const int64_t nrows = p.rows_base + (cta < p.rows_rem ? 1 : 0);
+    const int nst = (int)((nrows + SR - 1) / SR);
+    const int64_t R = p.row_bytes;
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), kConsWarps);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsWarps) {
+        // ---------------- producer: one lane streams the weight bytes ----------------
+        if (lane != 0) return;
+        const int64_t lim = p.w_total & ~(int64_t)15;
+        int issued = 0;
+        for (int s = 0; s < nst; ++s) {
+            const int slot = s % NS;
+            if (s >= NS && !wait_or_abort(empty(slot), ((s / NS) + 1) & 1, abort_flag)) {
+                record_error(p.err, DERR_GEMV_EMPTY);
+                *abort_flag = 1;
+                break;
+            }
+            const int64_t ra = r0 + (int64_t)s * SR;
+            const int64_t rb = min(ra + SR, r0 + nrows);
+            const int64_t A = ra * R, B = rb * R;
+            const int64_t a16 = A & ~(int64_t)15, b16 = (B + 15) & ~(int64_t)15;
+            const int64_t tend = min(b16, lim);
+            if (B > lim) {  // bytes after the last whole 16-byte chunk of W
+                for (int64_t q = max(a16, lim); q < B; ++q)
+                    stages[(int64_t)slot * SB + (q - a16)] = p.w[q];
+            }
+            const uint32_t tx = tend > a16 ? (uint32_t)(tend - a16) : 0u;
+            mbar_arrive_expect_tx(full(slot), tx);
+            if (tx) bulk_g2s(stage0 + (uint32_t)slot * SB, p.w + a16, tx, full(slot));
+            ++issued;
+        }
+        // no copy may land after this CTA exits
+        for (int s = max(0, issued - NS); s < issued; ++s)
+            if (!mbar_wait(full(s % NS), (s / NS) & 1)) record_error(p.err, DERR_TEARDOWN);
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    // x -> shared memory with coalesced loads (overlaps the first weight copies)
+    {
+        const int64_t k = p.k;
+        if ((reinterpret_cast<uintptr_t>(p.x) & 15u) == 0 && (k & 3) == 0) {
+            const float4 *x4 = reinterpret_cast<const float4 *>(p.x);
+            float4 *s4 = reinterpret_cast<float4 *>(xs);
+            for (int64_t i = tid; i < k / 4; i += kCons) s4[i] = __ldg(x4 + i);
+        } else {
+            for (int64_t i = tid; i < k; i += kCons) xs[i] = __ldg(p.x + i);
+        }
+        named_barrier(1, kCons);
+    }
+    const int t = tid;
+    int g, u0;
+    bool active;
+    if (UPT == 1 && !kChunked) {
+        g = t / p.U;
+        u0 = t - g * p.U;
+        active = g < p.G;
+    } else {
+        g = 0;
+        u0 = t;
+        active = true;
+    }
+    UnitState<FMT> st[UPT];
+#pragma unroll
+    for (int q = 0; q < UPT; ++q) {
+        const int u = u0 + q * kCons;
+        unit_init<FMT>(st[q], xs, active && u < p.U ? u : 0, active && u < p.U);
+    }
+    const int G = p.G;
+    const int pslot = kChunked ? warp : (UPT == 1 ? u0 : t);
+    bool failed = false;
+    for (int s = 0; s < nst; ++s) {
+        const int slot = s % NS;
+        if (!failed && !wait_or_abort(full(slot), (s / NS) & 1, abort_flag)) {
+            failed = true;
+            *abort_flag = 1;
+            record_error(p.err, DERR_GEMV_FULL);
+        }
+        const int64_t ra = r0 + (int64_t)s * SR;
+        const int64_t rb = min(ra + SR, r0 + nrows);
+        const int rows_in = (int)(rb - ra);
+        const int64_t a16 = (ra * R) & ~(int64_t)15;
+        const uint32_t sbase = stage0 + (uint32_t)slot * SB;
+        float *pb = part + (s & 1) * SR * PU;
+        if (!failed) {
+            if (kChunked) {
+                for (int rr = 0; rr < rows_in; ++rr) {
+                    const uint32_t rowa = sbase + (uint32_t)((ra + rr) * R - a16);
+                    float acc = 0.0f;
+#pragma unroll
+                    for (int q = 0; q < UPT; ++q) {
+                        const int u = u0 + q * kCons;
+                        if (u < p.U) acc += unit_dot<FMT>(rowa, u, st[q]);
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+                    if (lane == 0) pb[rr * PU + pslot] = acc;
+                }
+            } else if (active) {
+                for (int rr = g; rr < rows_in; rr += G) {
+                    const uint32_t rowa = sbase + (uint32_t)((ra + rr) * R - a16);
+                    float acc = 0.0f;
+#pragma unroll
+                    for (int q = 0; q < UPT; ++q) {
+                        const int u = u0 + q * kCons;
+                        if (UPT == 1 || u < p.U) acc += unit_dot<FMT>(rowa, u, st[q]);
+                    }
+                    pb[rr * PU + pslot] = acc;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(slot));
+        __syncwarp();
+        named_barrier(1, kCons);
+        if (!failed) {
+            for (int rr = warp; rr < rows_in; rr += kConsWarps) {
+                float v = 0.0f;
+                for (int i = lane; i < PU; i += 32) v += pb[rr * PU + i];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                if (lane == 0) {
+                    float *yp = p.y + ra + rr;
+                    *yp = p.accumulate ? *yp + v : v;
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ host ----
+
+static int unit_k(int fmt) { return fmt == F_Q4_K ? 64 : (fmt == F_BF16 || fmt == F_F16) ? 8 : 32; }
+static int max_upt(int fmt) { return fmt == F_Q4_K ? 1 : (fmt == F_BF16 || fmt == F_F16) ? 8 : 2; }
+
+bool gemv_supports(int fmt, int64_t k) {
+    if (fmt < F_BF16 || fmt > F_Q6_K || k <= 0) return false;
+    const int uk = unit_k(fmt);
+    if (k % uk) return false;
+    const int64_t U = k / uk;
+    return U <= (int64_t)kCons * max_upt(fmt);
+}
+
+template <int FMT, int UPT>
+static cudaError_t launch_t(const GemvParams &p, int grid, size_t smem, cudaStream_t s) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(gemv_kernel<FMT, UPT>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    gemv_kernel<FMT, UPT><<<grid, kGemvThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int FMT>
+static cudaError_t launch_chunked(const GemvParams &p, int upt, int grid, size_t smem, cudaStream_t s) {
+    switch (upt) {
+    case 1: return launch_t<FMT, 1>(p, grid, smem, s);
+    case 2: return launch_t<FMT, 2>(p, grid, smem, s);
+    case 4: return launch_t<FMT, 4>(p, grid, smem, s);
+    default: return launch_t<FMT, 8>(p, grid, smem, s);
+    }
+}
+
+cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t s) {
+    if (!gemv_supports(g.fmt, g.k)) return cudaErrorNotSupported;
+    const int64_t M = g.j1 - g.j0;
+    if (M <= 0) return cudaSuccess;
+    const bool chunked = g.fmt == F_BF16 || g.fmt == F_F16;
+    const int uk = unit_k(g.fmt);
+    const int U = (int)(g.k / uk);
+    int upt = (U + kCons - 1) / kCons;
+    if (chunked) {
+        int p2 = 1;
+        while (p2 < upt) p2 <<= 1;
+        upt = p2;
+    }
+    const int G = (!chunked && upt == 1) ? kCons / U : 1;
+    const int PU = chunked ? kConsWarps : (upt == 1 ? U : kCons);
+    const int64_t R = g.row_bytes;
+    // rows per stage: ~16 KB of weights, a multiple of the row groups, and
+    // small enough that every SM gets work on small problems
+    const int ctas_target = 2 * dev.sm_count;
+    int64_t rb = std::max<int64_t>(1, 16384 / (G * R));
+    int64_t SR = G * rb;
+    const int64_t per_cta = (M + ctas_target - 1) / ctas_target;
+    if (per_cta < SR) SR = std::max<int64_t>(G, ((per_cta + G - 1) / G) * G);
+    const int SB = (int)(((SR * R + 32) + 127) & ~127);
+    const size_t fixed = (size_t)((((16 * 8 + 16 + 8 * SR * PU + 127) & ~127) + 4 * g.k + 127) & ~127);
+    // two CTAs per SM when the ring still gets >= 2 stages in ~110 KB
+    const size_t budget = 110 * 1024;
+    int NS = (int)std::min<int64_t>(8, (int64_t)((budget > fixed ? budget - fixed : 0) / SB));
+    if (NS < 2) NS = (int)std::min<int64_t>(8, std::max<int64_t>(2, (int64_t)((200 * 1024 - fixed) / SB)));
+    const int64_t nstage_total = (M + SR - 1) / SR;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(nstage_total, ctas_target));
+    const size_t smem =
+        (size_t)((((16 * NS + 16 + 8 * SR * PU + 127) & ~127) + 4 * g.k + 127) & ~127) + (size_t)NS * SB;
+    if (smem > 200 * 1024) return cudaErrorNotSupported;
+
+    GemvParams p;
+    p.w = g.w; p.x = g.x; p.y = g.y;
+    p.k = g.k; p.row_bytes = R; p.w_total = R * g.n;
+    p.j0 = g.j0;
+    p.rows_base = M / grid;
+    p.rows_rem = (int)(M % grid);
+    p.accumulate = g.accumulate;
+    p.U = U; p.G = G; p.PU = PU; p.SR = (int)SR; p.SB = SB; p.NS = NS;
+    p.err = dev.err;
+    switch (g.fmt) {
+    case F_BF16: return launch_chunked<F_BF16>(p, upt, grid, smem, s);
+    case F_F16: return launch_chunked<F_F16>(p, upt, grid, smem, s);
+    case F_Q4_0: return upt == 1 ? launch_t<F_Q4_0, 1>(p, grid, smem, s) : launch_t<F_Q4_0, 2>(p, grid, smem, s);
+    case F_Q4_K: return launch_t<F_Q4_K, 1>(p, grid, smem, s);
+    case F_Q6_K: return upt == 1 ? launch_t<F_Q6_K, 1>(p, grid, smem, s) : launch_t<F_Q6_K, 2>(p, grid, smem, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace qmm

@@ -1,0 +1,56 @@
+// qmm_internal.h -- host-side interfaces between the C ABI (qmm_api.cu) and
+// the kernel translation units. Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace qmm {
+
+struct DeviceInfo {
+    int sm_count = 0;
+    int major = 0, minor = 0;
+    size_t smem_optin = 0;   // max dynamic shared memory per block
+    unsigned int *err = nullptr;  // device error word
+};
+
+// One GEMV launch: y[j] (+)= sum_i w[j][i] x[i] for j in [j0, j1), one token.
+struct GemvLaunch {
+    int fmt;
+    const uint8_t *w;
+    const float *x;
+    float *y;
+    int64_t k, n, row_bytes;
+    int64_t j0, j1;
+    int accumulate;
+};
+// Returns cudaSuccess or the launch error; cudaErrorNotSupported when no
+// GEMV variant takes the shape (the caller then uses the tensor-core path).
+cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t s);
+bool gemv_supports(int fmt, int64_t k);
+
+// N-token tensor-core product over [j0, j1) for all tokens.
+struct MmaLaunch {
+    int fmt;
+    const uint8_t *w;
+    const float *x;
+    float *y;
+    int64_t k, n, n_tokens, row_bytes;
+    int64_t j0, j1;
+    int accumulate;
+    void *workspace;        // >= mma_workspace_bytes(fmt, n_tokens, k)
+};
+size_t mma_workspace_bytes(int fmt, int64_t n_tokens, int64_t k);
+int mma_mode(int fmt, int64_t k);  // 1: W16.X16, 2: x split, 3: w and x split
+cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s);
+
+// Standalone dequantization of n rows into out[n][k].
+cudaError_t launch_dequant(int fmt, const uint8_t *w, int64_t k, int64_t n, int64_t row_bytes,
+                           float *out, cudaStream_t s);
+
+// y[t][j] = 0 for j in [j0, j1) (k == 0 with accumulate == 0).
+cudaError_t launch_zero_cols(float *y, int64_t n_tokens, int64_t n, int64_t j0, int64_t j1,
+                             cudaStream_t s);
+
+}  // namespace qmm

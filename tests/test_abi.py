@@ -1,0 +1,142 @@
+"""C ABI checks that need no GPU: the library builds and loads, exports every
+function include/qmm.h declares, sizes follow the closed forms, and invalid
+calls are rejected on the host with the documented status before any CUDA
+call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantized_weight_gguf_gb300 as q
+from quantized_weight_gguf_gb300 import build_lib
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "qmm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return q.load()
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(qmm_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 10
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(q.EXPORTS)
+
+
+def test_version(lib):
+    assert q.qmm_version() == 100
+
+
+@pytest.mark.parametrize("fmt,k,n,expect", [
+    ("bf16", 4096, 4096, 2 * 4096 * 4096),
+    ("f16", 4096, 4096, 2 * 4096 * 4096),
+    ("q4_0", 256, 512, 73728),
+    ("q4_k", 4096, 14336, 33030144),
+    ("q6_k", 2560, 262144, 550502400),
+    ("q4_0", 96, 7, 54 * 7),
+    ("q6_k", 1536, 1, 1260),
+    ("q6_k", 6144, 1, 5040),
+    ("q4_k", 128, 4, 0),     # k not a multiple of 256
+    ("q4_0", 48, 4, 0),      # k not a multiple of 32
+    ("bf16", 3, 4, 0),       # odd k
+    ("bf16", -2, 4, 0),
+    (9, 256, 4, 0),          # unknown format
+])
+def test_weight_bytes(lib, fmt, k, n, expect):
+    assert q.qmm_weight_bytes(fmt, k, n) == expect
+
+
+def _args(**kw):
+    base = dict(fmt="q4_k", w=16 * 1000, x=16 * 2000, y=16 * 3000, k=512, n=8, n_tokens=1,
+                stream=0)
+    base.update(kw)
+    fmt, w, x, y, k, n, nt = (base.pop(f) for f in ("fmt", "w", "x", "y", "k", "n", "n_tokens"))
+    return q.make_args(fmt, w, x, y, k, n, nt, **base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(fmt=7), 1),
+    (dict(k=300), 2),
+    (dict(fmt="q4_0", k=48), 2),
+    (dict(fmt="bf16", k=7), 2),
+    (dict(n_tokens=0), 2),
+    (dict(n=-1), 2),
+    (dict(w_len=10), 3),
+    (dict(j_start=3, j_end=2), 4),
+    (dict(j_start=0, j_end=9), 4),
+    (dict(j_start=-1, j_end=4), 4),
+    (dict(y=None), 5),
+    (dict(w=None), 5),
+    (dict(w=16 * 1000 + 8), 6),
+    (dict(x=16 * 2000 + 2), 6),
+    (dict(path=5), 2),
+])
+def test_invalid_calls_rejected_on_host(lib, kw, status):
+    a = _args(**kw)
+    rc = lib.qmm_matmul_ex(ctypes.byref(a))
+    assert rc == status, (rc, q.qmm_last_error())
+    assert q.qmm_last_error() != ""
+    assert q.qmm_select_path(a) == (-1 if status in (1, 2, 3, 4) else q.qmm_select_path(a))
+
+
+def test_error_message_names_the_problem(lib):
+    a = _args(k=300)
+    assert lib.qmm_matmul_ex(ctypes.byref(a)) == 2
+    assert "multiple of 256" in q.qmm_last_error()
+    a = _args(w_len=10)
+    assert lib.qmm_matmul_ex(ctypes.byref(a)) == 3
+    assert "W bytes" in q.qmm_last_error()
+
+
+def test_row_alignment_constraint_dropped(lib):
+    """Q4_0 with k=96 has 54-byte rows (not a multiple of 4); it is accepted."""
+    a = _args(fmt="q4_0", k=96, w_len=54 * 8)
+    assert q.qmm_select_path(a) in (q.PATH_GEMV, q.PATH_MMA)
+
+
+def test_path_policy_and_workspace(lib):
+    a = _args(k=4096, n=14336, n_tokens=1)
+    assert q.qmm_select_path(a) == q.PATH_GEMV
+    assert q.qmm_workspace_bytes(a) == 0
+    a = _args(k=4096, n=14336, n_tokens=512)
+    assert q.qmm_select_path(a) == q.PATH_MMA
+    assert q.qmm_workspace_bytes(a) == 512 * 4096 * 2 + 2048
+    # 16-bit weights split x into two fp16 terms; k is padded to 64 in the copies
+    a = _args(fmt="bf16", k=40, n=8, n_tokens=3)
+    assert q.qmm_workspace_bytes(a) == 2 * ((3 * 64 * 2 + 255) // 256) * 256 + 256
+    a = _args(k=512, n=8, n_tokens=3)              # small-k K-quant: split as well
+    assert q.qmm_workspace_bytes(a) == 2 * 3 * 512 * 2 + 256
+    a = _args(k=4096, n=14336, n_tokens=1, path=q.PATH_MMA)
+    assert q.qmm_select_path(a) == q.PATH_MMA
+    a = _args(k=4096, n=14336, n_tokens=64, path=q.PATH_GEMV)
+    assert q.qmm_select_path(a) == q.PATH_GEMV
+    assert q.qmm_workspace_bytes(a) == 0
+
+
+def test_dequant_rejects_bad_args(lib):
+    assert lib.qmm_dequant(9, 16, 256, 1, 16, None) == 1
+    assert lib.qmm_dequant(3, 16, 100, 1, 16, None) == 2
+    assert lib.qmm_dequant(3, None, 256, 1, 16, None) == 5
+    assert lib.qmm_dequant(3, 24, 256, 1, 16, None) == 6
+
+
+def test_host_variant_rejects_null_staging(lib):
+    a = _args()
+    assert lib.qmm_matmul_host(ctypes.byref(a), None, 16, 16) == 5
+
+
+def test_empty_work_needs_no_device(lib):
+    """n == 0 or an empty tile returns OK without touching CUDA."""
+    assert lib.qmm_matmul_ex(ctypes.byref(_args(n=0))) == 0
+    assert lib.qmm_matmul_ex(ctypes.byref(_args(j_start=3, j_end=3))) == 0

@@ -327,6 +327,17 @@ def test_matmul_matches_numpy_product_of_dequantized():
         np.testing.assert_allclose(s, np.abs(x.astype(np.float64)) @ np.abs(deq.T), rtol=1e-12)
 
 
+def test_blas_variant_equals_loop_oracle():
+    rng = np.random.default_rng(8)
+    for fmt, k, n, nt in (("q4_k", 512, 9, 3), ("bf16", 64, 5, 2), ("q6_k", 256, 4, 5)):
+        w = qmm_synth.gen_weights(fmt, k, n, rng)
+        x = qmm_synth.gen_x(nt, k, rng)
+        y, s = oracle.matmul(fmt, w, x, k, n)
+        yb, sb = oracle.matmul_blas(fmt, w, x, k, n)
+        np.testing.assert_allclose(yb, y, rtol=1e-12, atol=1e-12 * float(np.max(s)))
+        np.testing.assert_allclose(sb, s, rtol=1e-12)
+
+
 def test_sampled_equals_full():
     rng = np.random.default_rng(6)
     w = qmm_synth.gen_weights("q6_k", 512, 11, rng)
