@@ -274,7 +274,8 @@ def run_native(args):
     wcopies = [r.weights(w, ncop) for (_, _, _, w, _) in work]
     xs = [torch.from_numpy(x).to(device) for (*_, x) in work]
     ys = [torch.empty((1, n), device=device) for (_, _, n, _, _) in work]
-    argsets = [[q.make_args(fmt, wc[c], xs[i], ys[i], k, n, 1, stream=stream)
+    flags = 0 if args.no_overlap else q.FLAG_OVERLAP_PREV
+    argsets = [[q.make_args(fmt, wc[c], xs[i], ys[i], k, n, 1, stream=stream, flags=flags)
                 for c in range(ncop)] for i, ((fmt, k, n, _, _), wc) in enumerate(zip(work, wcopies))]
     import ctypes
     refs = [[ctypes.byref(a) for a in al] for al in argsets]
@@ -371,6 +372,9 @@ def run_native(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
             "data": "synthetic",
             "config": {"workload": "bf16+f16 GEMV k=n=4096, 1 token (one step = both GEMVs)",
+                       "launch": ("stream-ordered" if args.no_overlap else
+                                  "programmatic dependent launch (QMM_FLAG_OVERLAP_PREV): each GEMV "
+                                  "streams its weights while the previous kernel finishes"),
                        "weight_bytes_per_step": 2 * wbytes_each,
                        "l2": f"rotating {ncop} distinct weight copies per format (> 3x L2 of {r.l2 >> 20} MiB)",
                        "parallelism": f"replicas x{ws}"},
@@ -401,7 +405,8 @@ def measure_other_workloads(torch, q, lib, r, stream, hbm_peak, tc_peak):
         yd = torch.empty((1, n), device=dev)
         tile = n // tiles
         al = [[ctypes.byref(q.make_args(fmt, wc[c], xd, yd, k, n, 1, j_start=t * tile,
-                                        j_end=(t + 1) * tile, accumulate=False, stream=stream))
+                                        j_end=(t + 1) * tile, accumulate=False, stream=stream,
+                                        flags=q.FLAG_OVERLAP_PREV))
                for t in range(tiles)] for c in range(ncop)]
         keep = al  # noqa: F841
 
@@ -485,8 +490,10 @@ def run_case(args):
     a0 = q.make_args(fmt, wc[0], xd, yd, k, n, x.shape[0], path=path, stream=stream)
     need = q.qmm_workspace_bytes(a0)
     wsb = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+    flags = 0 if args.no_overlap else q.FLAG_OVERLAP_PREV
     al = [q.make_args(fmt, wc[c], xd, yd, k, n, x.shape[0], path=path,
-                      workspace=wsb if need else None, workspace_bytes=need, stream=stream)
+                      workspace=wsb if need else None, workspace_bytes=need, stream=stream,
+                      flags=flags)
           for c in range(ncop)]
     refs = [ctypes.byref(a) for a in al]
 
@@ -495,7 +502,7 @@ def run_case(args):
             raise RuntimeError(q.qmm_last_error())
     dt = time_loop(torch, launch, args.steps, args.warmup, ncop, stream)
     q.qmm_device_status(stream)
-    print(json.dumps({"case": name, "us_per_call": dt * 1e6, "weight_gbs": w.size / dt / 1e9,
+    print(json.dumps({"case": name, "overlap": not args.no_overlap, "us_per_call": dt * 1e6, "weight_gbs": w.size / dt / 1e9,
                       "tflops": 2.0 * x.shape[0] * k * n / dt / 1e12, "copies": ncop}), flush=True)
     return 0
 
@@ -506,6 +513,8 @@ def main():
                     help="profile one workload alone (bf16_gemv, f16_gemv, q4_0_gemv, q4_k_gemv, "
                          "q6_k_head, q4_k_prefill_N<tokens>[_gemv])")
     ap.add_argument("--no-rotate", action="store_true")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="plain stream-ordered launches (no programmatic dependent launch)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)

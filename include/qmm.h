@@ -91,7 +91,19 @@ typedef struct qmm_args {
     void *workspace;         /* device scratch for the MMA path, or NULL (library-owned grow-only buffer) */
     size_t workspace_bytes;  /* bytes at workspace */
     void *stream;            /* cudaStream_t; NULL = legacy default stream */
+    int flags;               /* bitwise OR of qmm_flags; 0 = none */
 } qmm_args;
+
+/* qmm_args.flags */
+typedef enum qmm_flags {
+    /* W is not written by the kernel that precedes this call in the stream.
+     * The GEMV kernel is then launched as a programmatic dependent of that
+     * kernel: it may start streaming W into shared memory while the
+     * preceding kernel is still running, and waits for that kernel to finish
+     * (and its writes to become visible) before it reads x or touches y.
+     * Without the flag the launch is ordinary stream-ordered. */
+    QMM_FLAG_OVERLAP_PREV = 1
+} qmm_flags;
 
 /* Bytes of n packed rows of k weights: (k/32)*18*n, (k/256)*144*n,
  * (k/256)*210*n or 2*k*n (rullama matmul.rs shape checks). 0 when fmt is

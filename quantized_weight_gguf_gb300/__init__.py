@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libqmm.so")
 
 FORMATS = {"bf16": 0, "f16": 1, "q4_0": 2, "q4_k": 3, "q6_k": 4}
 PATH_AUTO, PATH_GEMV, PATH_MMA = 0, 1, 2
+FLAG_OVERLAP_PREV = 1
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_FORMAT", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_SIZE",
           4: "QMM_ERR_RANGE", 5: "QMM_ERR_NULL", 6: "QMM_ERR_ALIGN", 7: "QMM_ERR_CUDA",
           8: "QMM_ERR_DEVICE_TIMEOUT", 9: "QMM_ERR_WORKSPACE", 10: "QMM_ERR_UNSUPPORTED"}
@@ -38,7 +39,7 @@ class qmm_args(ctypes.Structure):
                 ("n", ctypes.c_int64), ("n_tokens", ctypes.c_int64), ("j_start", ctypes.c_int64),
                 ("j_end", ctypes.c_int64), ("accumulate", ctypes.c_int), ("path", ctypes.c_int),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-                ("stream", ctypes.c_void_p)]
+                ("stream", ctypes.c_void_p), ("flags", ctypes.c_int)]
 
 
 _lib = None
@@ -120,10 +121,10 @@ def qmm_matmul(fmt, w, x, k: int, n: int, n_tokens: int, y) -> int:
 
 
 def make_args(fmt, w, x, y, k, n, n_tokens, *, w_len=0, j_start=0, j_end=0, accumulate=False,
-              path=PATH_AUTO, workspace=None, workspace_bytes=0, stream=None) -> qmm_args:
+              path=PATH_AUTO, workspace=None, workspace_bytes=0, stream=None, flags=0) -> qmm_args:
     return qmm_args(_fmt(fmt), _ptr(w), w_len, _ptr(x), _ptr(y), k, n, n_tokens, j_start, j_end,
                     int(bool(accumulate)), int(path), _ptr(workspace), workspace_bytes,
-                    _stream(stream) if stream != 0 else 0)
+                    _stream(stream) if stream != 0 else 0, int(flags))
 
 
 def qmm_matmul_ex(args: qmm_args) -> int:

@@ -128,6 +128,7 @@ int validate(const qmm_args *a, int64_t *j0, int64_t *j1, int64_t *rb, bool chec
     }
     if (a->path < QMM_PATH_AUTO || a->path > QMM_PATH_MMA)
         return fail(QMM_ERR_SHAPE, "unknown path %d", a->path);
+    if (a->flags & ~QMM_FLAG_OVERLAP_PREV) return fail(QMM_ERR_SHAPE, "unknown flags 0x%x", a->flags);
     return QMM_OK;
 }
 
@@ -170,6 +171,7 @@ int run(const qmm_args *a) {
             g.k = a->k; g.n = a->n; g.row_bytes = rb;
             g.j0 = j0; g.j1 = j1;
             g.accumulate = a->accumulate;
+            g.overlap_prev = (a->flags & QMM_FLAG_OVERLAP_PREV) != 0;
             cudaError_t e = qmm::launch_gemv(g, *dev, s);
             if (e != cudaSuccess) return cuda_fail(e, "GEMV launch");
         }
@@ -215,6 +217,16 @@ int run(const qmm_args *a) {
 }
 
 }  // namespace
+
+namespace qmm {
+int set_error(int status, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_err, sizeof t_err, fmt, ap);
+    va_end(ap);
+    return status;
+}
+}  // namespace qmm
 
 extern "C" {
 

@@ -47,11 +47,11 @@ struct GemvParams {
 };
 
 // Weights per unit: a 16-byte chunk for 16-bit formats (lane-contiguous in
-// shared memory), a 32-weight block for Q4_0 / a Q6_K quarter-half, and a
-// 64-weight chunk for Q4_K.
+// shared memory), a 32-weight block for Q4_0, a 32-weight sub-block for Q4_K
+// and a 32-weight quarter-half for Q6_K.
 template <int FMT>
 struct UnitK {
-    static constexpr int value = (FMT == F_Q4_K) ? 64 : (FMT == F_BF16 || FMT == F_F16) ? 8 : 32;
+    static constexpr int value = (FMT == F_BF16 || FMT == F_F16) ? 8 : 32;
 };
 
 __device__ __forceinline__ uint32_t bfe(uint32_t a, uint32_t pos, uint32_t len) {
@@ -74,6 +74,24 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
     return d;
 }
 
+// x is staged in shared memory "unit-transposed": element e of unit u lives at
+// e * (U + 1) + u, so the 32 lanes of a warp (consecutive units) read 32
+// consecutive words. x_slot maps a k index to that slot.
+template <int FMT>
+__device__ __forceinline__ int x_slot(int k, int U) {
+    int u, e;
+    if (FMT == F_Q6_K) {
+        // k = 256 b + 128 h + 32 r + 8 gq + i  ->  unit 8 b + 4 h + gq, element 8 r + i
+        u = ((k >> 8) << 3) + (((k >> 7) & 1) << 2) + ((k >> 3) & 3);
+        e = (((k >> 5) & 3) << 3) + (k & 7);
+    } else {
+        constexpr int UK = UnitK<FMT>::value;
+        u = k / UK;
+        e = k % UK;
+    }
+    return e * (U + 1) + u;
+}
+
 // Per-thread constants of one unit (x slice and what is derived from it).
 template <int FMT>
 struct UnitState {
@@ -84,15 +102,14 @@ struct UnitState {
 };
 
 template <int FMT>
-__device__ __forceinline__ void unit_init(UnitState<FMT> &st, const float *xs, int u, bool valid) {
+__device__ __forceinline__ void unit_init(UnitState<FMT> &st, const float *xs, int U, int u,
+                                          bool valid) {
     constexpr int UK = UnitK<FMT>::value;
+    // element e of unit u sits at xs[e * (U + 1) + u]
+#pragma unroll
+    for (int e = 0; e < UK; ++e) st.xr[e] = valid ? xs[e * (U + 1) + u] : 0.0f;
     if (FMT == F_Q6_K) {
-        const int b = u >> 3, h = (u >> 2) & 1, gq = u & 3;
-        const float *xb = xs + 256 * b + 128 * h + 8 * gq;
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) st.xr[8 * r + i] = valid ? xb[32 * r + i] : 0.0f;
+        const int gq = u & 3;
         float s[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
@@ -106,28 +123,23 @@ __device__ __forceinline__ void unit_init(UnitState<FMT> &st, const float *xs, i
         // scale byte of quarter r sits at byte 2r + (gq >> 1) of scales[8h .. 8h+7]
         st.p0 = 8 * (0 + (gq >> 1)); st.p1 = 8 * (2 + (gq >> 1));
         st.p2 = st.p0; st.p3 = st.p1;
-    } else {
-        const float *xb = xs + (int64_t)UK * u;
+    } else if (FMT == F_Q4_K) {
+        float sx = 0.0f;
 #pragma unroll
-        for (int i = 0; i < UK; ++i) st.xr[i] = valid ? xb[i] : 0.0f;
-        if (FMT == F_Q4_K) {
-            float slo = 0.0f, shi = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) { slo += st.xr[i]; shi += st.xr[32 + i]; }
-            st.c0 = slo; st.c1 = shi;
-            const int c = u & 3;
-            st.lowgrp = c < 2;
-            const int s0 = 2 * c, s1 = 2 * c + 1;
-            const int t0 = s0 >= 4 ? s0 - 4 : 0, t1 = s1 >= 4 ? s1 - 4 : 0;
-            // scale of sub-block s: low group -> bits 8s..8s+5 of word 0;
-            // high group -> bits 8t..8t+3 of word 2 | (bits 8t+6..8t+7 of word 0) << 4.
-            st.la = st.lowgrp ? 6u : 4u;
-            st.lb = st.lowgrp ? 0u : 2u;
-            st.p0 = st.lowgrp ? 8 * s0 : 8 * t0;  // scale, field A, sub-block 2c
-            st.p1 = st.lowgrp ? 8 * s1 : 8 * t1;  // scale, field A, sub-block 2c+1
-            st.p2 = 8 * t0 + 6;                   // field B (top bits), sub-block 2c
-            st.p3 = 8 * t1 + 6;                   // field B, sub-block 2c+1
-        }
+        for (int i = 0; i < 32; ++i) sx += st.xr[i];
+        st.c0 = sx;
+        const int sb = u & 7;  // sub-block within the super-block
+        st.lowgrp = sb < 4;
+        const int t = sb >= 4 ? sb - 4 : 0;
+        // sub-block s < 4: scale = bits 8s..8s+5 of word 0, min = same bits of word 1;
+        // s >= 4 (t = s - 4): scale = bits 8t..8t+3 of word 2 | (bits 8t+6..8t+7 of word 0) << 4,
+        //                     min = bits 8t+4..8t+7 of word 2 | (bits 8t+6..8t+7 of word 1) << 4.
+        st.la = st.lowgrp ? 6u : 4u;
+        st.lb = st.lowgrp ? 0u : 2u;
+        st.p0 = st.lowgrp ? 8 * sb : 8 * t;       // scale, field A
+        st.p1 = st.lowgrp ? 8 * sb : 8 * t + 4;   // min, field A
+        st.p2 = 8 * t + 6;                        // top bits, field B
+        st.p3 = (sb & 1) ? 4u : 0u;               // nibble of the quant bytes
     }
 }
 
@@ -173,7 +185,7 @@ __device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<
         }
         return d * ((a0.x + a0.y) + (a1.x + a1.y));
     } else if (FMT == F_Q4_K) {
-        const int b = u >> 2, c = u & 3;
+        const int b = u >> 3, c = (u >> 1) & 3;
         const uint32_t sb = rowa + 144u * b;
         const uint4 hdr = lds128(sb);
         const uint4 q0 = lds128(sb + 16u + 32u * c);
@@ -182,33 +194,22 @@ __device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<
         const float dmin = f16_bits_to_f32(hdr.x >> 16);
         const uint32_t srcA_sc = st.lowgrp ? hdr.y : hdr.w;
         const uint32_t srcA_m = st.lowgrp ? hdr.z : hdr.w;
-        const uint32_t off_m = st.lowgrp ? 0u : 4u;
-        const uint32_t sc0 = bfe(srcA_sc, st.p0, st.la) | (bfe(hdr.y, st.p2, st.lb) << 4);
-        const uint32_t sc1 = bfe(srcA_sc, st.p1, st.la) | (bfe(hdr.y, st.p3, st.lb) << 4);
-        const uint32_t m0 = bfe(srcA_m, st.p0 + off_m, st.la) | (bfe(hdr.z, st.p2, st.lb) << 4);
-        const uint32_t m1 = bfe(srcA_m, st.p1 + off_m, st.la) | (bfe(hdr.z, st.p3, st.lb) << 4);
+        const uint32_t sc = bfe(srcA_sc, st.p0, st.la) | (bfe(hdr.y, st.p2, st.lb) << 4);
+        const uint32_t m = bfe(srcA_m, st.p1, st.la) | (bfe(hdr.z, st.p2, st.lb) << 4);
         const uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-        float2 l0 = make_float2(0.f, 0.f), l1 = l0, h0 = l0, h1 = l0;
+        float2 a0 = make_float2(0.f, 0.f), a1 = a0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const uint32_t lo = wd[i] & 0x0F0F0F0Fu, hi = (wd[i] >> 4) & 0x0F0F0F0Fu;
-            l0 = ffma2(make_float2(byte_half_plus<0>(lo), byte_half_plus<1>(lo)),
-                       make_float2(st.xr[4 * i], st.xr[4 * i + 1]), l0);
-            l1 = ffma2(make_float2(byte_half_plus<2>(lo), byte_half_plus<3>(lo)),
-                       make_float2(st.xr[4 * i + 2], st.xr[4 * i + 3]), l1);
-            h0 = ffma2(make_float2(byte_half_plus<0>(hi), byte_half_plus<1>(hi)),
-                       make_float2(st.xr[32 + 4 * i], st.xr[32 + 4 * i + 1]), h0);
-            h1 = ffma2(make_float2(byte_half_plus<2>(hi), byte_half_plus<3>(hi)),
-                       make_float2(st.xr[32 + 4 * i + 2], st.xr[32 + 4 * i + 3]), h1);
+            const uint32_t nib = (wd[i] >> st.p3) & 0x0F0F0F0Fu;
+            a0 = ffma2(make_float2(byte_half_plus<0>(nib), byte_half_plus<1>(nib)),
+                       make_float2(st.xr[4 * i], st.xr[4 * i + 1]), a0);
+            a1 = ffma2(make_float2(byte_half_plus<2>(nib), byte_half_plus<3>(nib)),
+                       make_float2(st.xr[4 * i + 2], st.xr[4 * i + 3]), a1);
         }
-        const float alo = (l0.x + l0.y) + (l1.x + l1.y);
-        const float ahi = (h0.x + h0.y) + (h1.x + h1.y);
-        const float ds0 = d * (float)sc0, ds1 = d * (float)sc1;
-        const float dm0 = dmin * (float)m0, dm1 = dmin * (float)m1;
+        const float a = (a0.x + a0.y) + (a1.x + a1.y);
+        const float ds = d * (float)sc, dm = dmin * (float)m;
         // ds * sum q x - dm * sum x, with sum q x = 256 * a - 128 * sum x
-        const float r0 = fmaf(256.0f * ds0, alo, -fmaf(128.0f, ds0, dm0) * st.c0);
-        const float r1 = fmaf(256.0f * ds1, ahi, -fmaf(128.0f, ds1, dm1) * st.c1);
-        return r0 + r1;
+        return fmaf(256.0f * ds, a, -fmaf(128.0f, ds, dm) * st.c0);
     } else {  // F_Q6_K
         const int b = u >> 3, h = (u >> 2) & 1, gq = u & 3;
         const uint32_t sb = rowa + 210u * b;
@@ -263,7 +264,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 }
 
 template <int FMT, int UPT>
-__global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {
+__global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
     constexpr bool kChunked = (FMT == F_BF16 || FMT == F_F16);  // warp-reduced 16-byte chunks
     extern __shared__ __align__(128) uint8_t smem[];
     const int NS = p.NS, SR = p.SR, SB = p.SB, PU = p.PU;
@@ -273,7 +274,8 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {
     const int part_bytes = 8 * SR * PU;  // two buffers
     const int xs_off = (16 * NS + 16 + part_bytes + 127) & ~127;
     float *xs = reinterpret_cast<float *>(smem + xs_off);
-    const uint32_t stage_off = (uint32_t)((xs_off + 4 * (int)p.k + 127) & ~127);
+    const uint32_t stage_off =
+        (uint32_t)((xs_off + 4 * (int)(p.k + UnitK<FMT>::value) + 127) & ~127);
     uint8_t *stages = smem + stage_off;
     const uint32_t stage0 = bar0 + stage_off;
     auto full = [&](int s) { return bar0 + 8u * s; };
@@ -295,6 +297,9 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {
         fence_barrier_init();
     }
     __syncthreads();
+    // The next kernel in the stream may begin launching once every CTA of this
+    // one is running; it waits for this grid's completion before using its y.
+    pdl_launch_dependents();
 
     if (warp == kConsWarps) {
         // ---------------- producer: one lane streams the weight bytes ----------------
@@ -329,15 +334,24 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {
     }
 
     // ---------------- consumers ----------------
-    // x -> shared memory with coalesced loads (overlaps the first weight copies)
+    // x -> shared memory (unit-transposed) with coalesced global loads; waits
+    // for the preceding kernel first, since that kernel may be producing x
+    // (and may still read or write y)
+    pdl_wait_prev();
     {
-        const int64_t k = p.k;
+        const int k = (int)p.k;
+        const int U = p.U;
         if ((reinterpret_cast<uintptr_t>(p.x) & 15u) == 0 && (k & 3) == 0) {
             const float4 *x4 = reinterpret_cast<const float4 *>(p.x);
-            float4 *s4 = reinterpret_cast<float4 *>(xs);
-            for (int64_t i = tid; i < k / 4; i += kCons) s4[i] = __ldg(x4 + i);
+            for (int i = tid; i < k / 4; i += kCons) {
+                const float4 v = __ldg(x4 + i);
+                xs[x_slot<FMT>(4 * i, U)] = v.x;
+                xs[x_slot<FMT>(4 * i + 1, U)] = v.y;
+                xs[x_slot<FMT>(4 * i + 2, U)] = v.z;
+                xs[x_slot<FMT>(4 * i + 3, U)] = v.w;
+            }
         } else {
-            for (int64_t i = tid; i < k; i += kCons) xs[i] = __ldg(p.x + i);
+            for (int i = tid; i < k; i += kCons) xs[x_slot<FMT>(i, U)] = __ldg(p.x + i);
         }
         named_barrier(1, kCons);
     }
@@ -357,7 +371,7 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {
 #pragma unroll
     for (int q = 0; q < UPT; ++q) {
         const int u = u0 + q * kCons;
-        unit_init<FMT>(st[q], xs, active && u < p.U ? u : 0, active && u < p.U);
+        unit_init<FMT>(st[q], xs, p.U, active && u < p.U ? u : 0, active && u < p.U);
     }
     const int G = p.G;
     const int pslot = kChunked ? warp : (UPT == 1 ? u0 : t);
@@ -423,8 +437,8 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {
 
 // ------------------------------------------------------------------ host ----
 
-static int unit_k(int fmt) { return fmt == F_Q4_K ? 64 : (fmt == F_BF16 || fmt == F_F16) ? 8 : 32; }
-static int max_upt(int fmt) { return fmt == F_Q4_K ? 1 : (fmt == F_BF16 || fmt == F_F16) ? 8 : 2; }
+static int unit_k(int fmt) { return (fmt == F_BF16 || fmt == F_F16) ? 8 : 32; }
+static int max_upt(int fmt) { return (fmt == F_BF16 || fmt == F_F16) ? 8 : 2; }
 
 bool gemv_supports(int fmt, int64_t k) {
     if (fmt < F_BF16 || fmt > F_Q6_K || k <= 0) return false;
@@ -435,7 +449,8 @@ bool gemv_supports(int fmt, int64_t k) {
 }
 
 template <int FMT, int UPT>
-static cudaError_t launch_t(const GemvParams &p, int grid, size_t smem, cudaStream_t s) {
+static cudaError_t launch_t(const GemvParams &p, int grid, size_t smem, cudaStream_t s,
+                            bool overlap) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
@@ -443,17 +458,31 @@ static cudaError_t launch_t(const GemvParams &p, int grid, size_t smem, cudaStre
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    gemv_kernel<FMT, UPT><<<grid, kGemvThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    if (!overlap) {
+        gemv_kernel<FMT, UPT><<<grid, kGemvThreads, smem, s>>>(p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kGemvThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<FMT, UPT>, p);
 }
 
 template <int FMT>
-static cudaError_t launch_chunked(const GemvParams &p, int upt, int grid, size_t smem, cudaStream_t s) {
+static cudaError_t launch_chunked(const GemvParams &p, int upt, int grid, size_t smem,
+                                  cudaStream_t s, bool ov) {
     switch (upt) {
-    case 1: return launch_t<FMT, 1>(p, grid, smem, s);
-    case 2: return launch_t<FMT, 2>(p, grid, smem, s);
-    case 4: return launch_t<FMT, 4>(p, grid, smem, s);
-    default: return launch_t<FMT, 8>(p, grid, smem, s);
+    case 1: return launch_t<FMT, 1>(p, grid, smem, s, ov);
+    case 2: return launch_t<FMT, 2>(p, grid, smem, s, ov);
+    case 4: return launch_t<FMT, 4>(p, grid, smem, s, ov);
+    default: return launch_t<FMT, 8>(p, grid, smem, s, ov);
     }
 }
 
@@ -481,7 +510,8 @@ cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t
     const int64_t per_cta = (M + ctas_target - 1) / ctas_target;
     if (per_cta < SR) SR = std::max<int64_t>(G, ((per_cta + G - 1) / G) * G);
     const int SB = (int)(((SR * R + 32) + 127) & ~127);
-    const size_t fixed = (size_t)((((16 * 8 + 16 + 8 * SR * PU + 127) & ~127) + 4 * g.k + 127) & ~127);
+    const size_t fixed =
+        (size_t)((((16 * 8 + 16 + 8 * SR * PU + 127) & ~127) + 4 * (g.k + uk) + 127) & ~127);
     // two CTAs per SM when the ring still gets >= 2 stages in ~110 KB
     const size_t budget = 110 * 1024;
     int NS = (int)std::min<int64_t>(8, (int64_t)((budget > fixed ? budget - fixed : 0) / SB));
@@ -489,7 +519,8 @@ cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t
     const int64_t nstage_total = (M + SR - 1) / SR;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(nstage_total, ctas_target));
     const size_t smem =
-        (size_t)((((16 * NS + 16 + 8 * SR * PU + 127) & ~127) + 4 * g.k + 127) & ~127) + (size_t)NS * SB;
+        (size_t)((((16 * NS + 16 + 8 * SR * PU + 127) & ~127) + 4 * (g.k + uk) + 127) & ~127) +
+        (size_t)NS * SB;
     if (smem > 200 * 1024) return cudaErrorNotSupported;
 
     GemvParams p;
@@ -501,12 +532,13 @@ cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t
     p.accumulate = g.accumulate;
     p.U = U; p.G = G; p.PU = PU; p.SR = (int)SR; p.SB = SB; p.NS = NS;
     p.err = dev.err;
+    const bool ov = g.overlap_prev;
     switch (g.fmt) {
-    case F_BF16: return launch_chunked<F_BF16>(p, upt, grid, smem, s);
-    case F_F16: return launch_chunked<F_F16>(p, upt, grid, smem, s);
-    case F_Q4_0: return upt == 1 ? launch_t<F_Q4_0, 1>(p, grid, smem, s) : launch_t<F_Q4_0, 2>(p, grid, smem, s);
-    case F_Q4_K: return launch_t<F_Q4_K, 1>(p, grid, smem, s);
-    case F_Q6_K: return upt == 1 ? launch_t<F_Q6_K, 1>(p, grid, smem, s) : launch_t<F_Q6_K, 2>(p, grid, smem, s);
+    case F_BF16: return launch_chunked<F_BF16>(p, upt, grid, smem, s, ov);
+    case F_F16: return launch_chunked<F_F16>(p, upt, grid, smem, s, ov);
+    case F_Q4_0: return upt == 1 ? launch_t<F_Q4_0, 1>(p, grid, smem, s, ov) : launch_t<F_Q4_0, 2>(p, grid, smem, s, ov);
+    case F_Q4_K: return upt == 1 ? launch_t<F_Q4_K, 1>(p, grid, smem, s, ov) : launch_t<F_Q4_K, 2>(p, grid, smem, s, ov);
+    case F_Q6_K: return upt == 1 ? launch_t<F_Q6_K, 1>(p, grid, smem, s, ov) : launch_t<F_Q6_K, 2>(p, grid, smem, s, ov);
     default: return cudaErrorInvalidValue;
     }
 }

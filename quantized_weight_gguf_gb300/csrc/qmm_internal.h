@@ -24,6 +24,7 @@ struct GemvLaunch {
     int64_t k, n, row_bytes;
     int64_t j0, j1;
     int accumulate;
+    bool overlap_prev;   // programmatic dependent launch (W is not written by the previous kernel)
 };
 // Returns cudaSuccess or the launch error; cudaErrorNotSupported when no
 // GEMV variant takes the shape (the caller then uses the tensor-core path).
@@ -52,5 +53,8 @@ cudaError_t launch_dequant(int fmt, const uint8_t *w, int64_t k, int64_t n, int6
 // y[t][j] = 0 for j in [j0, j1) (k == 0 with accumulate == 0).
 cudaError_t launch_zero_cols(float *y, int64_t n_tokens, int64_t n, int64_t j0, int64_t j1,
                              cudaStream_t s);
+
+// Record a status and message for qmm_last_error() on this host thread; returns status.
+int set_error(int status, const char *fmt, ...);
 
 }  // namespace qmm
