@@ -161,6 +161,26 @@ int qmm_dequant(int fmt, const void *w, int64_t k, int64_t n, float *out, void *
  * returns, so the context stays usable. */
 int qmm_device_status(void *stream);
 
+/* qmm_matmul_ex on the tensor-core path for callers that cannot allocate
+ * device memory (no CUDA allocator of their own, or no allocation calls
+ * allowed on their hot path because those synchronize the device). The
+ * pages have no counterpart of this call. Its scratch (the fp16 copies of x
+ * and the per-token scales, qmm_workspace_bytes() of the same arguments on
+ * that path) lives in a fixed 16 MiB array in device memory that the library
+ * defines; every GPU that loads libqmm holds that array until the process
+ * exits. a->path, a->workspace and a->workspace_bytes are ignored; all other
+ * fields mean what they mean for qmm_matmul_ex, and the caller still passes
+ * w, x and y. A call that would need more than 16 MiB of scratch returns
+ * QMM_ERR_WORKSPACE without enqueuing anything. The call allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine). The first call on
+ * a device looks up the array's device address (cudaGetSymbolAddress, with
+ * that device current); make that first call before any stream capture.
+ * Every call uses the same array and leaves its contents behind (each call
+ * overwrites all the scratch it reads, so nothing needs clearing): calls
+ * whose kernels can overlap on the GPU (different streams without ordering
+ * between them) race on it. */
+int qmm_matmul_noalloc(const qmm_args *a);
+
 /* Message for the last non-OK status on this host thread ("" if none). */
 const char *qmm_last_error(void);
 

@@ -24,7 +24,7 @@ STATUS = {0: "QMM_OK", 1: "QMM_ERR_FORMAT", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_SIZE
           8: "QMM_ERR_DEVICE_TIMEOUT", 9: "QMM_ERR_WORKSPACE", 10: "QMM_ERR_UNSUPPORTED"}
 EXPORTS = ("qmm_weight_bytes", "qmm_matmul", "qmm_set_stream", "qmm_matmul_ex",
            "qmm_workspace_bytes", "qmm_select_path", "qmm_matmul_host", "qmm_dequant",
-           "qmm_device_status", "qmm_last_error", "qmm_version")
+           "qmm_device_status", "qmm_last_error", "qmm_version", "qmm_matmul_noalloc")
 
 
 class QmmError(RuntimeError):
@@ -68,6 +68,7 @@ def load(path: str = LIB_PATH):
         "qmm_device_status": (i, [vp]),
         "qmm_last_error": (ctypes.c_char_p, []),
         "qmm_version": (i, []),
+        "qmm_matmul_noalloc": (i, [pa]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -129,6 +130,10 @@ def make_args(fmt, w, x, y, k, n, n_tokens, *, w_len=0, j_start=0, j_end=0, accu
 
 def qmm_matmul_ex(args: qmm_args) -> int:
     return _check(load().qmm_matmul_ex(ctypes.byref(args)))
+
+
+def qmm_matmul_noalloc(args: qmm_args) -> int:
+    return _check(load().qmm_matmul_noalloc(ctypes.byref(args)))
 
 
 def qmm_workspace_bytes(args: qmm_args) -> int:
