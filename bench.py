@@ -274,7 +274,7 @@ def run_native(args):
     wcopies = [r.weights(w, ncop) for (_, _, _, w, _) in work]
     xs = [torch.from_numpy(x).to(device) for (*_, x) in work]
     ys = [torch.empty((1, n), device=device) for (_, _, n, _, _) in work]
-    flags = 0 if args.no_overlap else q.FLAG_OVERLAP_PREV
+    flags = 0 if args.no_overlap else (q.FLAG_OVERLAP_PREV | q.FLAG_X_READY)
     argsets = [[q.make_args(fmt, wc[c], xs[i], ys[i], k, n, 1, stream=stream, flags=flags)
                 for c in range(ncop)] for i, ((fmt, k, n, _, _), wc) in enumerate(zip(work, wcopies))]
     import ctypes
@@ -373,8 +373,10 @@ def run_native(args):
             "data": "synthetic",
             "config": {"workload": "bf16+f16 GEMV k=n=4096, 1 token (one step = both GEMVs)",
                        "launch": ("stream-ordered" if args.no_overlap else
-                                  "programmatic dependent launch (QMM_FLAG_OVERLAP_PREV): each GEMV "
-                                  "streams its weights while the previous kernel finishes"),
+                                  "programmatic dependent launch (QMM_FLAG_OVERLAP_PREV | "
+                                  "QMM_FLAG_X_READY): consecutive GEMVs on the same x; each streams "
+                                  "its weights and computes while the previous one finishes, and "
+                                  "stores y after it"),
                        "weight_bytes_per_step": 2 * wbytes_each,
                        "l2": f"rotating {ncop} distinct weight copies per format (> 3x L2 of {r.l2 >> 20} MiB)",
                        "parallelism": f"replicas x{ws}"},
@@ -406,7 +408,7 @@ def measure_other_workloads(torch, q, lib, r, stream, hbm_peak, tc_peak):
         tile = n // tiles
         al = [[ctypes.byref(q.make_args(fmt, wc[c], xd, yd, k, n, 1, j_start=t * tile,
                                         j_end=(t + 1) * tile, accumulate=False, stream=stream,
-                                        flags=q.FLAG_OVERLAP_PREV))
+                                        flags=q.FLAG_OVERLAP_PREV | q.FLAG_X_READY))
                for t in range(tiles)] for c in range(ncop)]
         keep = al  # noqa: F841
 
@@ -490,7 +492,7 @@ def run_case(args):
     a0 = q.make_args(fmt, wc[0], xd, yd, k, n, x.shape[0], path=path, stream=stream)
     need = q.qmm_workspace_bytes(a0)
     wsb = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
-    flags = 0 if args.no_overlap else q.FLAG_OVERLAP_PREV
+    flags = 0 if args.no_overlap else (q.FLAG_OVERLAP_PREV | (0 if args.x_wait else q.FLAG_X_READY))
     al = [q.make_args(fmt, wc[c], xd, yd, k, n, x.shape[0], path=path,
                       workspace=wsb if need else None, workspace_bytes=need, stream=stream,
                       flags=flags)
@@ -513,6 +515,8 @@ def main():
                     help="profile one workload alone (bf16_gemv, f16_gemv, q4_0_gemv, q4_k_gemv, "
                          "q6_k_head, q4_k_prefill_N<tokens>[_gemv])")
     ap.add_argument("--no-rotate", action="store_true")
+    ap.add_argument("--x-wait", action="store_true",
+                    help="overlap only the weight stream with the previous kernel (x read after it)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="plain stream-ordered launches (no programmatic dependent launch)")
     ap.add_argument("--gpus", type=int, default=1)

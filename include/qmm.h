@@ -102,7 +102,13 @@ typedef enum qmm_flags {
      * preceding kernel is still running, and waits for that kernel to finish
      * (and its writes to become visible) before it reads x or touches y.
      * Without the flag the launch is ordinary stream-ordered. */
-    QMM_FLAG_OVERLAP_PREV = 1
+    QMM_FLAG_OVERLAP_PREV = 1,
+    /* With QMM_FLAG_OVERLAP_PREV: x is not written by the preceding kernel
+     * either (for instance several projections of the same activations, or
+     * x produced two kernels back). The GEMV then also stages x and computes
+     * its partial sums before that kernel has finished; only its stores to y
+     * wait for it. */
+    QMM_FLAG_X_READY = 2
 } qmm_flags;
 
 /* Bytes of n packed rows of k weights: (k/32)*18*n, (k/256)*144*n,

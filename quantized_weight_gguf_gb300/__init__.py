@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libqmm.so")
 FORMATS = {"bf16": 0, "f16": 1, "q4_0": 2, "q4_k": 3, "q6_k": 4}
 PATH_AUTO, PATH_GEMV, PATH_MMA = 0, 1, 2
 FLAG_OVERLAP_PREV = 1
+FLAG_X_READY = 2
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_FORMAT", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_SIZE",
           4: "QMM_ERR_RANGE", 5: "QMM_ERR_NULL", 6: "QMM_ERR_ALIGN", 7: "QMM_ERR_CUDA",
           8: "QMM_ERR_DEVICE_TIMEOUT", 9: "QMM_ERR_WORKSPACE", 10: "QMM_ERR_UNSUPPORTED"}
@@ -167,7 +168,7 @@ def qmm_version() -> int:
 # ------------------------------------------------------ tensor helpers ----
 
 def matmul(fmt, w, x, k: int, n: int, *, y=None, j_start=0, j_end=0, accumulate=False,
-           path=PATH_AUTO, stream=None):
+           path=PATH_AUTO, stream=None, flags=0):
     """y = x @ W for torch CUDA tensors: w uint8 packed bytes, x float32 [N, k].
     Returns y float32 [N, n] (the given y when passed). Scratch for the
     tensor-core path is a torch allocation on x's device."""
@@ -178,7 +179,7 @@ def matmul(fmt, w, x, k: int, n: int, *, y=None, j_start=0, j_end=0, accumulate=
     if y is None:
         y = torch.empty((nt, n), dtype=torch.float32, device=x.device)
     a = make_args(fmt, w, x, y, k, n, nt, w_len=w.numel() * w.element_size(), j_start=j_start,
-                  j_end=j_end, accumulate=accumulate, path=path, stream=stream)
+                  j_end=j_end, accumulate=accumulate, path=path, stream=stream, flags=flags)
     need = qmm_workspace_bytes(a)
     ws = None
     if need:

@@ -128,7 +128,8 @@ int validate(const qmm_args *a, int64_t *j0, int64_t *j1, int64_t *rb, bool chec
     }
     if (a->path < QMM_PATH_AUTO || a->path > QMM_PATH_MMA)
         return fail(QMM_ERR_SHAPE, "unknown path %d", a->path);
-    if (a->flags & ~QMM_FLAG_OVERLAP_PREV) return fail(QMM_ERR_SHAPE, "unknown flags 0x%x", a->flags);
+    if (a->flags & ~(QMM_FLAG_OVERLAP_PREV | QMM_FLAG_X_READY))
+        return fail(QMM_ERR_SHAPE, "unknown flags 0x%x", a->flags);
     return QMM_OK;
 }
 
@@ -172,6 +173,7 @@ int run(const qmm_args *a) {
             g.j0 = j0; g.j1 = j1;
             g.accumulate = a->accumulate;
             g.overlap_prev = (a->flags & QMM_FLAG_OVERLAP_PREV) != 0;
+            g.x_ready = g.overlap_prev && (a->flags & QMM_FLAG_X_READY) != 0;
             cudaError_t e = qmm::launch_gemv(g, *dev, s);
             if (e != cudaSuccess) return cuda_fail(e, "GEMV launch");
         }

@@ -37,9 +37,12 @@ struct GemvParams {
     int64_t rows_base;
     int rows_rem;
     int accumulate;
+    int x_ready;  // x may be read before the preceding kernel completes
     int U;    // units per row
     int G;    // row groups per stage (one unit per thread), else 1
     int PU;   // partial slots per row
+    int SEG;  // lanes that share a row and pre-reduce by shuffles (0: one partial per thread)
+    int RPF;  // rows whose partials are buffered before a block-wide reduction (multiple of SR)
     int SR;   // rows per stage
     int SB;   // bytes per stage buffer (multiple of 128)
     int NS;   // stage buffers
@@ -271,7 +274,7 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
     const uint32_t bar0 = smem_addr(smem);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 16 * NS);
     float *part = reinterpret_cast<float *>(smem + 16 * NS + 16);
-    const int part_bytes = 8 * SR * PU;  // two buffers
+    const int part_bytes = 4 * p.RPF * PU;
     const int xs_off = (16 * NS + 16 + part_bytes + 127) & ~127;
     float *xs = reinterpret_cast<float *>(smem + xs_off);
     const uint32_t stage_off =
@@ -334,10 +337,11 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
     }
 
     // ---------------- consumers ----------------
-    // x -> shared memory (unit-transposed) with coalesced global loads; waits
-    // for the preceding kernel first, since that kernel may be producing x
-    // (and may still read or write y)
-    pdl_wait_prev();
+    // x -> shared memory (unit-transposed) with coalesced global loads. Unless
+    // the caller vouched that the preceding kernel does not write x, wait for
+    // that kernel first (it may be producing x); y is never touched before
+    // the wait.
+    if (!p.x_ready) pdl_wait_prev();
     {
         const int k = (int)p.k;
         const int U = p.U;
@@ -374,8 +378,13 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
         unit_init<FMT>(st[q], xs, p.U, active && u < p.U ? u : 0, active && u < p.U);
     }
     const int G = p.G;
-    const int pslot = kChunked ? warp : (UPT == 1 ? u0 : t);
+    const int SEG = p.SEG;
+    // slot of this thread's partial within a row: one per thread, or one per
+    // SEG-lane segment (written by the segment's first lane)
+    const int pslot = SEG == 0 ? u0 : (SEG == 32 ? (kChunked || UPT > 1 ? warp : (u0 >> 5)) : 0);
+    const bool writer = SEG == 0 || (lane & (SEG - 1)) == 0;
     bool failed = false;
+    int64_t fbase = r0;  // first row of the buffered window
     for (int s = 0; s < nst; ++s) {
         const int slot = s % NS;
         if (!failed && !wait_or_abort(full(slot), (s / NS) & 1, abort_flag)) {
@@ -388,49 +397,50 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
         const int rows_in = (int)(rb - ra);
         const int64_t a16 = (ra * R) & ~(int64_t)15;
         const uint32_t sbase = stage0 + (uint32_t)slot * SB;
-        float *pb = part + (s & 1) * SR * PU;
-        if (!failed) {
-            if (kChunked) {
-                for (int rr = 0; rr < rows_in; ++rr) {
+        float *pb = part + (ra - fbase) * PU;
+        if (!failed && active) {
+            // same trip count for every lane of a warp (segments of one warp may
+            // belong to different row groups), so the shuffles stay convergent
+            for (int base = 0; base < rows_in; base += G) {
+                const int rr = base + g;
+                const bool has = rr < rows_in;
+                float acc = 0.0f;
+                if (has) {
                     const uint32_t rowa = sbase + (uint32_t)((ra + rr) * R - a16);
-                    float acc = 0.0f;
 #pragma unroll
                     for (int q = 0; q < UPT; ++q) {
                         const int u = u0 + q * kCons;
-                        if (u < p.U) acc += unit_dot<FMT>(rowa, u, st[q]);
+                        if ((UPT == 1 && !kChunked) || u < p.U) acc += unit_dot<FMT>(rowa, u, st[q]);
                     }
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-                    if (lane == 0) pb[rr * PU + pslot] = acc;
                 }
-            } else if (active) {
-                for (int rr = g; rr < rows_in; rr += G) {
-                    const uint32_t rowa = sbase + (uint32_t)((ra + rr) * R - a16);
-                    float acc = 0.0f;
-#pragma unroll
-                    for (int q = 0; q < UPT; ++q) {
-                        const int u = u0 + q * kCons;
-                        if (UPT == 1 || u < p.U) acc += unit_dot<FMT>(rowa, u, st[q]);
-                    }
-                    pb[rr * PU + pslot] = acc;
+                if (SEG) {
+                    for (int o = SEG >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
                 }
+                if (writer && has) pb[rr * PU + pslot] = acc;
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty(slot));
         __syncwarp();
-        named_barrier(1, kCons);
-        if (!failed) {
-            for (int rr = warp; rr < rows_in; rr += kConsWarps) {
-                float v = 0.0f;
-                for (int i = lane; i < PU; i += 32) v += pb[rr * PU + i];
+        // block-wide reduction once the window is full, and at the end
+        if (rb - fbase >= p.RPF || s == nst - 1) {
+            if (p.x_ready) pdl_wait_prev();  // y may still be in use by the preceding kernel
+            named_barrier(1, kCons);
+            if (!failed) {
+                const int wrows = (int)(rb - fbase);
+                for (int rr = warp; rr < wrows; rr += kConsWarps) {
+                    float v = 0.0f;
+                    for (int i = lane; i < PU; i += 32) v += part[rr * PU + i];
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-                if (lane == 0) {
-                    float *yp = p.y + ra + rr;
-                    *yp = p.accumulate ? *yp + v : v;
+                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                    if (lane == 0) {
+                        float *yp = p.y + fbase + rr;
+                        *yp = p.accumulate ? *yp + v : v;
+                    }
                 }
             }
+            named_barrier(1, kCons);
+            fbase = rb;
         }
     }
 }
@@ -500,18 +510,32 @@ cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t
         upt = p2;
     }
     const int G = (!chunked && upt == 1) ? kCons / U : 1;
-    const int PU = chunked ? kConsWarps : (upt == 1 ? U : kCons);
+    // per-row pre-reduction: whole warps of one row (16-bit chunks, several units
+    // per thread, or U a multiple of 32), power-of-two segments (U < 32), else none
+    int SEG, PU;
+    // (quantized formats are ALU-bound: one shared-memory partial per thread is
+    // cheaper than shuffles; 16-bit formats have 8-weight units and headroom)
+    if (chunked || upt > 1) {
+        SEG = 32; PU = kConsWarps;
+    } else if (U < 32 && (32 % U) == 0) {
+        SEG = U; PU = 1;
+    } else {
+        SEG = 0; PU = U;
+    }
     const int64_t R = g.row_bytes;
-    // rows per stage: ~16 KB of weights, a multiple of the row groups, and
+    // rows per stage: ~32 KB of weights, a multiple of the row groups, and
     // small enough that every SM gets work on small problems
     const int ctas_target = 2 * dev.sm_count;
-    int64_t rb = std::max<int64_t>(1, 16384 / (G * R));
+    int64_t rb = std::max<int64_t>(1, 32768 / (G * R));
     int64_t SR = G * rb;
     const int64_t per_cta = (M + ctas_target - 1) / ctas_target;
     if (per_cta < SR) SR = std::max<int64_t>(G, ((per_cta + G - 1) / G) * G);
     const int SB = (int)(((SR * R + 32) + 127) & ~127);
+    // partial-sum window: ~24 KB, whole stages
+    int64_t RPF = std::max<int64_t>(SR, (6144 / PU) / SR * SR);
+    const size_t part_bytes = (size_t)4 * RPF * PU;
     const size_t fixed =
-        (size_t)((((16 * 8 + 16 + 8 * SR * PU + 127) & ~127) + 4 * (g.k + uk) + 127) & ~127);
+        (size_t)((((16 * 8 + 16 + part_bytes + 127) & ~(size_t)127) + 4 * (g.k + uk) + 127) & ~(size_t)127);
     // two CTAs per SM when the ring still gets >= 2 stages in ~110 KB
     const size_t budget = 110 * 1024;
     int NS = (int)std::min<int64_t>(8, (int64_t)((budget > fixed ? budget - fixed : 0) / SB));
@@ -519,7 +543,7 @@ cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t
     const int64_t nstage_total = (M + SR - 1) / SR;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(nstage_total, ctas_target));
     const size_t smem =
-        (size_t)((((16 * NS + 16 + 8 * SR * PU + 127) & ~127) + 4 * (g.k + uk) + 127) & ~127) +
+        (size_t)((((16 * NS + 16 + part_bytes + 127) & ~(size_t)127) + 4 * (g.k + uk) + 127) & ~(size_t)127) +
         (size_t)NS * SB;
     if (smem > 200 * 1024) return cudaErrorNotSupported;
 
@@ -530,7 +554,8 @@ cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t
     p.rows_base = M / grid;
     p.rows_rem = (int)(M % grid);
     p.accumulate = g.accumulate;
-    p.U = U; p.G = G; p.PU = PU; p.SR = (int)SR; p.SB = SB; p.NS = NS;
+    p.x_ready = g.x_ready ? 1 : 0;
+    p.U = U; p.G = G; p.PU = PU; p.SEG = SEG; p.RPF = (int)RPF; p.SR = (int)SR; p.SB = SB; p.NS = NS;
     p.err = dev.err;
     const bool ov = g.overlap_prev;
     switch (g.fmt) {

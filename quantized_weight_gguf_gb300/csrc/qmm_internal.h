@@ -25,6 +25,7 @@ struct GemvLaunch {
     int64_t j0, j1;
     int accumulate;
     bool overlap_prev;   // programmatic dependent launch (W is not written by the previous kernel)
+    bool x_ready;        // x is not written by the previous kernel either: only y waits
 };
 // Returns cudaSuccess or the launch error; cudaErrorNotSupported when no
 // GEMV variant takes the shape (the caller then uses the tensor-core path).

@@ -247,6 +247,52 @@ def test_q4_k_prefill_full_size_every_output(nt):
     assert_parity(y, y_ref, s_ref, f"prefill all outputs N={nt}")
 
 
+# ------------------------------------------- overlapped (PDL) launches ----
+
+def test_overlap_chain_reads_previous_output():
+    """y1 = W1 x, then y2 = W2 y1 with QMM_FLAG_OVERLAP_PREV: the second GEMV
+    streams W2 early but must read x = y1 only after the first one finished."""
+    rng = np.random.default_rng(41)
+    k1, n1, n2 = 4096, 2048, 3000
+    w1 = qmm_synth.gen_weights("bf16", k1, n1, rng)
+    w2 = qmm_synth.gen_weights("q4_k", n1, n2, rng)
+    x = qmm_synth.gen_x(1, k1, rng)
+    w1d, w2d, xd = _dev(w1), _dev(w2), _dev(x)
+    for rep in range(3):
+        y1 = torch.full((1, n1), float("nan"), device=DEV)
+        y2 = torch.full((1, n2), float("nan"), device=DEV)
+        q.matmul("bf16", w1d, xd, k1, n1, y=y1, flags=q.FLAG_OVERLAP_PREV)
+        q.matmul("q4_k", w2d, y1, n1, n2, y=y2, flags=q.FLAG_OVERLAP_PREV)
+        torch.cuda.synchronize()
+        q.qmm_device_status()
+        y1h = y1.cpu().numpy()
+        r1, s1 = oracle.matmul("bf16", w1, x, k1, n1)
+        assert_parity(y1h, r1, s1, "chain stage 1")
+        r2, s2 = oracle.matmul("q4_k", w2, y1h, n1, n2)
+        assert_parity(y2.cpu().numpy(), r2, s2, "chain stage 2")
+
+
+def test_overlap_x_ready_accumulates_after_previous_store():
+    """y = W1 x, then y += W2 x with OVERLAP_PREV | X_READY on the same y: the
+    second kernel computes early but must add to y only after the first stored it."""
+    rng = np.random.default_rng(42)
+    k, n = 4096, 5000
+    w1 = qmm_synth.gen_weights("q6_k", k, n, rng)
+    w2 = qmm_synth.gen_weights("f16", k, n, rng)
+    x = qmm_synth.gen_x(1, k, rng)
+    w1d, w2d, xd = _dev(w1), _dev(w2), _dev(x)
+    r1, s1 = oracle.matmul("q6_k", w1, x, k, n)
+    r2, s2 = oracle.matmul("f16", w2, x, k, n)
+    fl = q.FLAG_OVERLAP_PREV | q.FLAG_X_READY
+    for rep in range(3):
+        y = torch.full((1, n), float("nan"), device=DEV)
+        q.matmul("q6_k", w1d, xd, k, n, y=y, flags=fl)
+        q.matmul("f16", w2d, xd, k, n, y=y, accumulate=True, flags=fl)
+        torch.cuda.synchronize()
+        q.qmm_device_status()
+        assert_parity(y.cpu().numpy(), r1 + r2, s1 + s2, "x-ready accumulate")
+
+
 # ------------------------------------------------------------ edge cases ----
 
 def test_k_zero_and_empty():
