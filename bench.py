@@ -289,37 +289,38 @@ def run_native(args):
         step(i % ncop)
     torch.cuda.synchronize()
     q.qmm_device_status(stream)
-    # per-kernel events inside the timed region: bf16 launch between e[i] and m[i]
     K = args.steps
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_c = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        time.sleep(0.3)
+        time.sleep(0.25)
+        # timed region: K steps back to back, events only at its ends (an event
+        # between launches would stop each GEMV from overlapping the previous one)
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for i in range(K):
-            c = i % ncop
-            ev_a[i].record(stream)
-            if mm(refs[0][c]):
-                raise RuntimeError(q.qmm_last_error())
-            ev_b[i].record(stream)
-            if mm(refs[1][c]):
-                raise RuntimeError(q.qmm_last_error())
-            ev_c[i].record(stream)
+            step(i % ncop)
         end.record(stream)
         end.synchronize()
-        time.sleep(0.3)
+        # dominant kernel alone: average launch duration of the BF16 GEMV over a
+        # back-to-back loop of it (same flags, same rotation)
+        r0 = torch.cuda.Event(enable_timing=True)
+        r1 = torch.cuda.Event(enable_timing=True)
+        KR = max(K, 100)
+        r0.record(stream)
+        for i in range(KR):
+            if mm(refs[0][i % ncop]):
+                raise RuntimeError(q.qmm_last_error())
+        r1.record(stream)
+        r1.synchronize()
+        time.sleep(0.25)
     torch.cuda.synchronize()
     barrier(ws)
     elapsed = start.elapsed_time(end) / 1e3
     elapsed = max_over_ranks(elapsed, ws, device)
     q.qmm_device_status(stream)
-    t_bf16 = sum(ev_a[i].elapsed_time(ev_b[i]) for i in range(K)) / K / 1e3
-    t_f16 = sum(ev_b[i].elapsed_time(ev_c[i]) for i in range(K)) / K / 1e3
+    t_bf16 = r0.elapsed_time(r1) / 1e3 / KR
     ms_per_step = elapsed / K * 1e3
     value = ws * 2 * wbytes_each / (elapsed / K) / 1e9
     clocks = clk.summary()
@@ -365,7 +366,8 @@ def run_native(args):
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
             "frac": achieved / hbm_peak, "traffic": recorded_traffic("gemv_bf16_4096x4096"),
             "kernel": "gemv_kernel<BF16> (k=n=4096)", "peak_source": f"{peak_src} hbm_gbs",
-            "f16_kernel_gbs": wbytes_each / t_f16 / 1e9}
+            "duration_us": t_bf16 * 1e6,
+            "duration_from": f"CUDA events around {KR} back-to-back launches of this kernel alone"}
 
     line = {"metric": "effective weight GB/s", "value": value, "unit": "GB/s", "n_gpus": ws,
             "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
@@ -520,7 +522,7 @@ def main():
     ap.add_argument("--no-overlap", action="store_true",
                     help="plain stream-ordered launches (no programmatic dependent launch)")
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline only (no other workloads, no CPU baseline)")
