@@ -8,7 +8,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/qmm.h"
+#include "qmm.h"
 #include "qmm_device.cuh"
 #include "qmm_internal.h"
 

@@ -88,17 +88,19 @@ template <> struct Raw32<F_F16> : Raw16bit<F_F16> {};
 
 template <>
 struct Raw32<F_Q4_0> {
-    uint32_t h[9];  // 18 bytes as 2-byte halves: d, then 16 quant bytes
+    uint32_t dbits;   // f16 d
+    uint32_t qw[4];   // the 16 quant bytes, packed little-endian
     __device__ __forceinline__ void load(const uint8_t *row, int64_t k0, int) {
         const uint8_t *p = row + 18 * (k0 >> 5);
+        dbits = ldg_u16(p);
 #pragma unroll
-        for (int i = 0; i < 9; ++i) h[i] = ldg_u16(p + 2 * i);
+        for (int i = 0; i < 4; ++i) qw[i] = ldg_u16(p + 2 + 4 * i) | (ldg_u16(p + 4 + 4 * i) << 16);
     }
     __device__ __forceinline__ void decode(float (&w)[32]) const {
-        const float d = f16_bits_to_f32(h[0]);
+        const float d = f16_bits_to_f32(dbits);
 #pragma unroll
         for (int b = 0; b < 16; ++b) {
-            const uint32_t q = (h[1 + (b >> 1)] >> (8 * (b & 1))) & 0xFFu;
+            const uint32_t q = (qw[b >> 2] >> (8 * (b & 3))) & 0xFFu;
             w[b] = __fmul_rn((float)((int)(q & 15u) - 8), d);
             w[b + 16] = __fmul_rn((float)((int)(q >> 4) - 8), d);
         }
@@ -137,9 +139,9 @@ struct Raw32<F_Q4_K> {
 
 template <>
 struct Raw32<F_Q6_K> {
-    uint32_t ql[16], qh[16];  // 2-byte halves of the 32 ql and 32 qh bytes used
-    uint32_t sc2, dbits;      // the two int8 scales of these 32 weights; f16 d
-    int r;                    // which quarter of the half (selects nibble and qh bits)
+    uint32_t ql[8], qh[8];  // the 32 ql and 32 qh bytes used, packed little-endian
+    uint32_t sc2, dbits;    // the two int8 scales of these 32 weights; f16 d
+    int r;                  // which quarter of the half (selects nibble and qh bits)
     __device__ __forceinline__ void load(const uint8_t *row, int64_t k0, int) {
         const uint8_t *p = row + 210 * (k0 >> 8);
         const int e0 = (int)(k0 & 255);
@@ -148,9 +150,9 @@ struct Raw32<F_Q6_K> {
         const uint8_t *pl = p + 64 * h + 32 * (r & 1);
         const uint8_t *ph = p + 128 + 32 * h;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            ql[i] = ldg_u16(pl + 2 * i);
-            qh[i] = ldg_u16(ph + 2 * i);
+        for (int i = 0; i < 8; ++i) {
+            ql[i] = ldg_u16(pl + 4 * i) | (ldg_u16(pl + 4 * i + 2) << 16);
+            qh[i] = ldg_u16(ph + 4 * i) | (ldg_u16(ph + 4 * i + 2) << 16);
         }
         sc2 = ldg_u16(p + 192 + 8 * h + 2 * r);
         dbits = ldg_u16(p + 208);
@@ -163,8 +165,8 @@ struct Raw32<F_Q6_K> {
         const uint32_t hsh = 2u * (uint32_t)r;
 #pragma unroll
         for (int l = 0; l < 32; ++l) {
-            const uint32_t lo = (ql[l >> 1] >> (8 * (l & 1))) & 0xFFu;
-            const uint32_t hi = (qh[l >> 1] >> (8 * (l & 1))) & 0xFFu;
+            const uint32_t lo = (ql[l >> 2] >> (8 * (l & 3))) & 0xFFu;
+            const uint32_t hi = (qh[l >> 2] >> (8 * (l & 3))) & 0xFFu;
             const int q = (int)(((lo >> nsh) & 15u) | (((hi >> hsh) & 3u) << 4));
             w[l] = __fmul_rn(l < 16 ? ds0 : ds1, (float)(q - 32));
         }

@@ -7,9 +7,10 @@
 //               (128-byte swizzle) through a tensor map;
 //   warp 1      allocates the fp32 accumulator in tensor memory (TMEM) and one
 //               lane issues tcgen05.mma (M=128, N=BN, K=16, fp16 in, fp32 acc);
-//   warps 2..9  dequantize W: thread (r, h) turns 32 weights of row r per
-//               k-step into fp16 and stores them in the same swizzled K-major
-//               layout the MMA descriptor describes; after the k-loop they
+//   warps 2..17 dequantize W in two groups of 8 warps that take alternate
+//               k-steps: thread (r, h) turns 32 weights of row r per k-step
+//               into fp16 and stores them in the same swizzled K-major layout
+//               the MMA descriptor describes; after the k-loop all 16 warps
 //               drain the accumulator TMEM -> registers -> y.
 // X is converted to fp16 once per call by a small kernel that also scales each
 // token row by a power of two (exact) so it fits fp16's range; the epilogue
@@ -34,7 +35,8 @@
 
 namespace qmm {
 
-constexpr int kMmaThreads = 320;
+constexpr int kDeqWarps = 16;                     // two groups of 8, alternate k-steps
+constexpr int kMmaThreads = 64 + 32 * kDeqWarps;
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kABytes = kBM * kBK * 2;  // 16 KB per stage
@@ -47,16 +49,30 @@ struct MmaParams {
     int64_t j0, j1;
     int KS;
     int accumulate;
+    int tma_store;   // y tile written by one TMA store / reduce-add (alignment permits)
     unsigned int *err;
 };
 
-template <int BN>
+// Q4_K super-blocks of 128 rows staged raw by TMA (one 128 x 144-byte box per
+// 256-wide slice of k), then decoded from shared memory.
+constexpr int kRawBytes = kBM * 144;
+
+// Shared memory: a ring of NA dequantized W stages (made on chip), a deeper
+// ring of NB x stages (streamed from L2, latency-bound: it gets the room),
+// and for raw staging kNR raw W super-block tiles.
+template <int BN, bool RAW>
 struct MmaCfg {
     static constexpr int kBBytes = BN * kBK * 2;
-    static constexpr int kStage = kABytes + kBBytes;
-    static constexpr int NS = (192 * 1024 / kStage) > 8 ? 8 : (192 * 1024 / kStage);
+    static constexpr int kNR = RAW ? 2 : 1;  // (1 unused slot keeps the layout uniform)
+    static constexpr int NA = 3;
+    static constexpr int kAvail = 212 * 1024 - (RAW ? kNR * kRawBytes : 0) - NA * kABytes;
+    static constexpr int NB = (kAvail / kBBytes) > 8 ? 8 : (kAvail / kBBytes);
     static constexpr int kCols = BN < 32 ? 32 : BN;  // TMEM columns (power of two >= 32)
-    static constexpr size_t kSmem = (size_t)NS * kStage + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr size_t kSmem = (size_t)NA * kABytes + (size_t)NB * kBBytes +
+                                    (RAW ? (size_t)kNR * kRawBytes : 0) + 1024 /*align*/ +
+                                    512 /*barriers*/;
+    // the output tile (rows x tokens fp32) is staged in the x ring for the TMA store
+    static_assert(NB * kBBytes >= kBM * BN * 4, "x ring too small for the output tile");
 };
 
 __device__ __forceinline__ bool wait_abortable(uint32_t bar, uint32_t parity,
@@ -110,9 +126,40 @@ __device__ __forceinline__ void to_half_words<F_Q4_K>(const Raw32<F_Q4_K> &raw,
     }
 }
 
+// Half h of a Q4_K 64-weight chunk c: quant bytes 16h .. 16h+15 of the chunk (q),
+// i.e. weights 16h + 0..15 (low nibbles, sub-block 2c) and 32 + 16h + 0..15
+// (high nibbles, sub-block 2c+1) -> 16 fp16x2 words: 0..7 low, 8..15 high.
+__device__ __forceinline__ void q4k_half_chunk_to_half(const uint4 &hdr, const uint4 &q, int c,
+                                                       uint32_t (&hw)[16]) {
+    uint32_t sc0, m0, sc1, m1;
+    q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * c, sc0, m0);
+    q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * c + 1, sc1, m1);
+    const float d = f16_bits_to_f32(hdr.x & 0xFFFFu);
+    const float dmin = f16_bits_to_f32(hdr.x >> 16);
+    const float ds0 = d * (float)sc0, ds1 = d * (float)sc1;
+    const float2 a0 = make_float2(256.0f * ds0, 256.0f * ds0);
+    const float2 a1 = make_float2(256.0f * ds1, 256.0f * ds1);
+    const float cc0 = -fmaf(128.0f, ds0, dmin * (float)m0);
+    const float cc1 = -fmaf(128.0f, ds1, dmin * (float)m1);
+    const float2 c0 = make_float2(cc0, cc0), c1 = make_float2(cc1, cc1);
+    const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = wd[i] & 0x0F0F0F0Fu, hi = (wd[i] >> 4) & 0x0F0F0F0Fu;
+        const float2 l01 = ffma2(a0, make_float2(byte_half_plus<0>(lo), byte_half_plus<1>(lo)), c0);
+        const float2 l23 = ffma2(a0, make_float2(byte_half_plus<2>(lo), byte_half_plus<3>(lo)), c0);
+        const float2 h01 = ffma2(a1, make_float2(byte_half_plus<0>(hi), byte_half_plus<1>(hi)), c1);
+        const float2 h23 = ffma2(a1, make_float2(byte_half_plus<2>(hi), byte_half_plus<3>(hi)), c1);
+        hw[2 * i] = pack_half2(l01.x, l01.y);
+        hw[2 * i + 1] = pack_half2(l23.x, l23.y);
+        hw[8 + 2 * i] = pack_half2(h01.x, h01.y);
+        hw[8 + 2 * i + 1] = pack_half2(h23.x, h23.y);
+    }
+}
+
 template <int FMT>
 struct Prefetch {
-    static constexpr int value = (FMT == F_Q4_K || FMT == F_Q4_0) ? 4 : 3;
+    static constexpr int value = (FMT == F_Q4_K || FMT == F_Q4_0) ? 4 : (FMT == F_Q6_K ? 2 : 3);
 };
 
 __device__ __forceinline__ void split_half_words(const float (&v)[32], bool lo, uint32_t (&hw)[16]) {
@@ -131,25 +178,38 @@ __device__ __forceinline__ void split_half_words(const float (&v)[32], bool lo, 
 template <int FMT, int BN, int MODE>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     mma_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmx_lo,
+               const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmy,
                const MmaParams p) {
     constexpr int kRowsOut = MODE == 3 ? 64 : kBM;   // output rows per CTA
     constexpr int kTokOut = MODE == 1 ? BN : BN / 2;  // tokens per CTA
-    using C = MmaCfg<BN>;
-    constexpr int NS = C::NS;
+    constexpr bool kRaw = FMT == F_Q4_K && MODE != 3;  // raw W tiles by TMA
+    using C = MmaCfg<BN, kRaw>;
+    constexpr int NA = C::NA, NB = C::NB, kNR = C::kNR;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
     const uint32_t A0 = sbase;
-    const uint32_t B0 = sbase + NS * kABytes;
-    const uint32_t bar0 = B0 + NS * C::kBBytes;
+    const uint32_t B0 = sbase + NA * kABytes;
+    const uint32_t W0 = B0 + NB * C::kBBytes;                      // raw W stages (kRaw)
+    const uint32_t bar0 = W0 + (kRaw ? kNR * kRawBytes : 0);
     auto fullA = [&](int s) { return bar0 + 8u * s; };
-    auto fullB = [&](int s) { return bar0 + 8u * (NS + s); };
-    auto empty = [&](int s) { return bar0 + 8u * (2 * NS + s); };
-    const uint32_t accb = bar0 + 8u * (3 * NS);
-    const uint32_t slot_addr = accb + 8u;
+    auto emptyA = [&](int s) { return bar0 + 8u * (NA + s); };
+    auto fullB = [&](int s) { return bar0 + 8u * (2 * NA + s); };
+    auto emptyB = [&](int s) { return bar0 + 8u * (2 * NA + NB + s); };
+    const uint32_t accb = bar0 + 8u * (2 * NA + 2 * NB);
+    auto rawFull = [&](int s) { return accb + 8u * (1 + s); };
+    auto rawEmpty = [&](int s) { return accb + 8u * (1 + kNR + s); };
+    const uint32_t slot_off = 8u * (2 * NA + 2 * NB + 1 + 2 * kNR);
+    const uint32_t slot_addr = bar0 + slot_off;
     uint8_t *gen = smem_raw + (bar0 - raw_addr);
-    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gen + 8 * (3 * NS) + 8);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(gen + 8 * (3 * NS) + 16);
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gen + slot_off);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gen + slot_off + 8);
+    // arrivals that complete a dequantized A stage: the 8 warps of the group
+    // that owns the k-step (two groups take alternate k-steps). The A ring must
+    // hold at least as many stages as there are groups, so that no group can
+    // wait on a phase two ahead of the barrier.
+    constexpr int kFullACount = kDeqWarps / 2;
+    static_assert(C::NA >= 2, "A ring shallower than the number of producer groups");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t m0 = p.j0 + (int64_t)blockIdx.x * kRowsOut;
@@ -157,12 +217,21 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const int KS = p.KS;
 
     if (tid == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(fullA(s), 8);
+        for (int s = 0; s < NA; ++s) {
+            mbar_init(fullA(s), kFullACount);
+            mbar_init(emptyA(s), 1);
+        }
+        for (int s = 0; s < NB; ++s) {
             mbar_init(fullB(s), 1);
-            mbar_init(empty(s), 1);
+            mbar_init(emptyB(s), 1);
         }
         mbar_init(accb, 1);
+        if (kRaw) {
+            for (int s = 0; s < kNR; ++s) {
+                mbar_init(rawFull(s), 1);
+                mbar_init(rawEmpty(s), kDeqWarps);
+            }
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -180,10 +249,22 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         if (lane == 0) {
             prefetch_tmap(&tmx);
             if (MODE != 1) prefetch_tmap(&tmx_lo);
-            int issued = 0;
+            if (kRaw) prefetch_tmap(&tmw);
+            int issued = 0, raw_issued = 0;
             for (int ks = 0; ks < KS; ++ks) {
-                const int slot = ks % NS;
-                if (ks >= NS && !wait_abortable(empty(slot), ((ks / NS) + 1) & 1, abort_flag)) {
+                if (kRaw && (ks & 3) == 0) {
+                    const int b = ks >> 2, rs = b % kNR;
+                    if (b >= kNR && !wait_abortable(rawEmpty(rs), ((b / kNR) + 1) & 1, abort_flag)) {
+                        record_error(p.err, DERR_MMA_EMPTY);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(rawFull(rs), kRawBytes);
+                    tma_load_2d(W0 + rs * kRawBytes, &tmw, 144 * b, (int)m0, rawFull(rs));
+                    ++raw_issued;
+                }
+                const int slot = ks % NB;
+                if (ks >= NB && !wait_abortable(emptyB(slot), ((ks / NB) + 1) & 1, abort_flag)) {
                     record_error(p.err, DERR_MMA_EMPTY);
                     *abort_flag = 1;
                     break;
@@ -198,41 +279,99 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 }
                 ++issued;
             }
-            for (int s = std::max(0, issued - NS); s < issued; ++s)
-                if (!mbar_wait(fullB(s % NS), (s / NS) & 1)) record_error(p.err, DERR_TEARDOWN);
+            for (int s = std::max(0, issued - NB); s < issued; ++s)
+                if (!mbar_wait(fullB(s % NB), (s / NB) & 1)) record_error(p.err, DERR_TEARDOWN);
+            for (int s = std::max(0, raw_issued - kNR); s < raw_issued; ++s)
+                if (!mbar_wait(rawFull(s % kNR), (s / kNR) & 1)) record_error(p.err, DERR_TEARDOWN);
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issue ------------------------------
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
             for (int ks = 0; ks < KS; ++ks) {
-                const int slot = ks % NS;
-                const uint32_t par = (ks / NS) & 1;
-                if (!wait_abortable(fullA(slot), par, abort_flag)) {
+                const int sa = ks % NA, sb = ks % NB;
+                if (!wait_abortable(fullA(sa), (ks / NA) & 1, abort_flag)) {
                     record_error(p.err, DERR_MMA_A);
                     *abort_flag = 1;
                     break;
                 }
-                if (!wait_abortable(fullB(slot), par, abort_flag)) {
+                if (!wait_abortable(fullB(sb), (ks / NB) & 1, abort_flag)) {
                     record_error(p.err, DERR_MMA_B);
                     *abort_flag = 1;
                     break;
                 }
                 tc_fence_after();
-                const uint64_t ad = sdesc_sw128(A0 + slot * kABytes);
-                const uint64_t bd = sdesc_sw128(B0 + slot * C::kBBytes);
+                const uint64_t ad = sdesc_sw128(A0 + sa * kABytes);
+                const uint64_t bd = sdesc_sw128(B0 + sb * C::kBBytes);
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16 per instruction: +32 bytes
                     tc_mma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (ks | kk) != 0);
-                tc_commit(empty(slot));
+                tc_commit(emptyA(sa));
+                tc_commit(emptyB(sb));
             }
             tc_commit(accb);  // fires when every MMA issued above has completed
         }
     } else {
         // ------------------------------ W dequant producers ------------------------------
+        if constexpr (kRaw) {
+            // two groups of 256 threads take alternate k-steps; thread (r, h) of a
+            // group decodes half h of row r's 64-weight chunk from the raw tile
+            const int dt = tid - 64;
+            const int r = dt & (kBM - 1);
+            const int h = (dt >> 7) & 1;
+            const int g = dt >> 8;
+            const bool row_ok = m0 + r < p.j1;
+            const uint32_t swz = (uint32_t)(r & 7);
+            const int NI = (KS - g + 1) / 2;
+            bool failed = false;
+            for (int i = 0; i < NI; ++i) {
+                const int ks = g + 2 * i;
+                const int b = ks >> 2, c = ks & 3;
+                const int rs = b % kNR;
+                uint32_t hw[16];
+                if (!failed && !wait_abortable(rawFull(rs), (b / kNR) & 1, abort_flag)) {
+                    failed = true;
+                    *abort_flag = 1;
+                    record_error(p.err, DERR_MMA_A);
+                }
+                if (!failed && row_ok) {
+                    const uint32_t rb = W0 + rs * kRawBytes + (uint32_t)r * 144u;
+                    const uint4 hdr = lds128(rb);
+                    const uint4 qv = lds128(rb + 16u + 32u * c + 16u * h);
+                    q4k_half_chunk_to_half(hdr, qv, c, hw);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) hw[e] = 0u;
+                }
+                __syncwarp();
+                // the last k-step of the super-block this group takes releases it
+                if (lane == 0 && !failed && c >= 2) mbar_arrive(rawEmpty(rs));
+                const int slot = ks % NA;
+                if (!failed && ks >= NA &&
+                    !wait_abortable(emptyA(slot), ((ks / NA) + 1) & 1, abort_flag)) {
+                    failed = true;
+                    *abort_flag = 1;
+                    record_error(p.err, DERR_MMA_EMPTY);
+                }
+                if (!failed) {
+                    const uint32_t arow = A0 + slot * kABytes + (uint32_t)r * 128u;
+                    // weights 16h..16h+15 -> chunks 2h, 2h+1; 32+16h.. -> chunks 4+2h, 5+2h
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const uint32_t chunk = (uint32_t)((cc >> 1) * 4 + 2 * h + (cc & 1)) ^ swz;
+                        sts128(arow + (chunk << 4), hw[4 * cc], hw[4 * cc + 1], hw[4 * cc + 2],
+                               hw[4 * cc + 3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && !failed) mbar_arrive(fullA(slot));
+            }
+        } else {
         const int dt = tid - 64;
         const int r = dt & (kBM - 1);
-        const int h = dt >> 7;
+        const int h = (dt >> 7) & 1;
+        const int par = dt >> 8;  // this group's k-steps: par, par + 2, ...
         const bool lo_part = MODE == 3 && r >= 64;   // MODE 3: rows 64..127 hold W_lo
         const int64_t j = m0 + (MODE == 3 ? (r & 63) : r);
         const bool row_ok = j < p.j1;
@@ -240,24 +379,27 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         const uint32_t swz = (uint32_t)(r & 7);
         constexpr int PD = Prefetch<FMT>::value;
         Raw32<FMT> ring[PD];
-        auto k0_of = [&](int ks) { return (int64_t)ks * kBK + 32 * h; };
+        // this thread's i-th k-step is par + 2 i
+        auto k0_of = [&](int i) { return (int64_t)(par + 2 * i) * kBK + 32 * h; };
         auto nvalid_of = [&](int64_t k0) {
             const int64_t v = p.k - k0;
             return (int)(v < 0 ? 0 : (v > 32 ? 32 : v));
         };
+        const int NI = (KS - par + 1) / 2;  // k-steps of this group
 #pragma unroll
         for (int q = 0; q < PD; ++q) {
             const int64_t k0 = k0_of(q);
             const int nv = nvalid_of(k0);
-            if (q < KS && row_ok && nv > 0) ring[q].load(rowp, k0, nv);
+            if (q < NI && row_ok && nv > 0) ring[q].load(rowp, k0, nv);
         }
         bool failed = false;
-        for (int ks0 = 0; ks0 < KS; ks0 += PD) {
+        for (int i0 = 0; i0 < NI; i0 += PD) {
 #pragma unroll
             for (int q = 0; q < PD; ++q) {
-                const int ks = ks0 + q;
-                if (ks < KS) {
-                    const int64_t k0 = k0_of(ks);
+                const int i = i0 + q;
+                if (i < NI) {
+                    const int ks = par + 2 * i;
+                    const int64_t k0 = k0_of(i);
                     const int nv = nvalid_of(k0);
                     uint32_t hw[16];
                     if (row_ok && nv > 0) {
@@ -270,19 +412,19 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                         }
                         if (nv < 32) {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                if (2 * i >= nv) hw[i] = 0u;  // nv is even
+                            for (int e = 0; e < 16; ++e)
+                                if (2 * e >= nv) hw[e] = 0u;  // nv is even
                         }
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) hw[i] = 0u;
+                        for (int e = 0; e < 16; ++e) hw[e] = 0u;
                     }
-                    const int64_t kn = k0_of(ks + PD);
+                    const int64_t kn = k0_of(i + PD);
                     const int nvn = nvalid_of(kn);
-                    if (ks + PD < KS && row_ok && nvn > 0) ring[q].load(rowp, kn, nvn);
-                    const int slot = ks % NS;
-                    if (!failed && ks >= NS &&
-                        !wait_abortable(empty(slot), ((ks / NS) + 1) & 1, abort_flag)) {
+                    if (i + PD < NI && row_ok && nvn > 0) ring[q].load(rowp, kn, nvn);
+                    const int slot = ks % NA;
+                    if (!failed && ks >= NA &&
+                        !wait_abortable(emptyA(slot), ((ks / NA) + 1) & 1, abort_flag)) {
                         failed = true;
                         *abort_flag = 1;
                         record_error(p.err, DERR_MMA_EMPTY);
@@ -302,70 +444,101 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 }
             }
         }
+        }  // generic dequant
         // ------------------------------ epilogue ------------------------------
         __syncwarp();
         const bool acc_ok = mbar_wait(accb, 0);
         if (!acc_ok) record_error(p.err, DERR_MMA_ACC);
         tc_fence_after();
         const int quarter = warp & 3;
-        const int half = (warp - 2) >> 2;
-        // token columns of this warp within [0, kTokOut)
-        int c_lo, c_hi;
-        if (kTokOut >= 32) {
-            c_lo = half * (kTokOut / 2);
-            c_hi = c_lo + kTokOut / 2;
-        } else {
-            c_lo = 0;
-            c_hi = half == 0 ? kTokOut : 0;
-        }
+        const int slice = (warp - 2) >> 2;  // 0..3: which part of the token columns
+        constexpr int kSlices = kTokOut >= 64 ? 4 : (kTokOut >= 32 ? 2 : 1);
+        constexpr int kSliceCols = kTokOut / kSlices;
+        const int c_lo = slice < kSlices ? slice * kSliceCols : 0;
+        const int c_hi = slice < kSlices ? c_lo + kSliceCols : 0;
         const int rl = 32 * quarter + lane;                 // accumulator row (TMEM lane)
         const int64_t je = m0 + (MODE == 3 ? (rl & 63) : rl);
         const bool store_ok = acc_ok && !*abort_flag && je < p.j1;
         const uint32_t tbase = tmem + ((uint32_t)(32 * quarter) << 16);
         float *scratch = reinterpret_cast<float *>(smem_raw + (A0 - raw_addr));  // [col][64]
+        // columns in chunks of 16 (kSliceCols is a multiple of 16)
+        auto load_acc = [&](int col, float (&acc)[16]) {
+            uint32_t v[16];
+            tmem_ld16(tbase + (uint32_t)col, v);
+            if (MODE == 1) {
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[i] = __uint_as_float(v[i]);
+            } else {
+                uint32_t w2[16];
+                tmem_ld16(tbase + (uint32_t)(col + BN / 2), w2);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[i] = __uint_as_float(v[i]) + __uint_as_float(w2[i]);
+            }
+        };
         if (MODE == 3 && quarter >= 2) {
             // lo rows: park (D[r][c] + D[r][c + BN/2]) for the hi warps
             __syncwarp();
             for (int col = c_lo; col < c_hi; col += 16) {
-                uint32_t v[16], w2[16];
-                tmem_ld16(tbase + (uint32_t)col, v);
-                tmem_ld16(tbase + (uint32_t)(col + BN / 2), w2);
-                tmem_ld_wait();
+                float acc[16];
+                load_acc(col, acc);
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    scratch[(col + i) * 64 + (rl & 63)] = __uint_as_float(v[i]) + __uint_as_float(w2[i]);
+                for (int i = 0; i < 16; ++i) scratch[(col + i) * 64 + (rl & 63)] = acc[i];
             }
         }
-        if (MODE == 3) named_barrier(2, 256);
-        if (MODE != 3 || quarter < 2) {
-            __syncwarp();
-            for (int col = c_lo; col < c_hi; col += 16) {
-                uint32_t v[16];
-                tmem_ld16(tbase + (uint32_t)col, v);
-                float acc[16];
-                if (MODE == 1) {
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[i] = __uint_as_float(v[i]);
-                } else {
-                    uint32_t w2[16];
-                    tmem_ld16(tbase + (uint32_t)(col + BN / 2), w2);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[i] = __uint_as_float(v[i]) + __uint_as_float(w2[i]);
+        if (MODE == 3) named_barrier(2, 32 * kDeqWarps);
+        if (p.tma_store) {
+            // stage the [tokens][rows] fp32 tile in the (now idle) x ring, then one
+            // TMA store (or reduce-add) writes it; the map clips rows >= n_tokens
+            // and columns >= j_end
+            float *stile = reinterpret_cast<float *>(smem_raw + (B0 - raw_addr));
+            if (MODE != 3 || quarter < 2) {
+                __syncwarp();
+                const int row = MODE == 3 ? (rl & 63) : rl;
+                for (int col = c_lo; col < c_hi; col += 16) {
+                    float acc[16];
+                    load_acc(col, acc);
                     if (MODE == 3) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) acc[i] += scratch[(col + i) * 64 + (rl & 63)];
                     }
-                }
-                if (store_ok) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int64_t t = n0 + col + i;
-                        if (t < p.n_tokens) {
-                            const float val = acc[i] * __ldg(p.xscale + t);
-                            float *yp = p.y + t * p.n + je;
-                            *yp = p.accumulate ? *yp + val : val;
+                        const float sc = t < p.n_tokens ? __ldg(p.xscale + t) : 0.0f;
+                        stile[(col + i) * kRowsOut + row] = acc[i] * sc;
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            named_barrier(3, 32 * kDeqWarps);
+            if (tid == 64 && acc_ok && !*abort_flag) {
+                if (p.accumulate)
+                    tma_reduce_add_2d(&tmy, (int)m0, n0, B0);
+                else
+                    tma_store_2d(&tmy, (int)m0, n0, B0);
+                bulk_commit_group();
+                bulk_wait_group_read0();
+            }
+        } else if (MODE != 3 || quarter < 2) {
+            __syncwarp();
+            for (int col = c_lo; col < c_hi; col += 16) {
+                float acc[16];
+                load_acc(col, acc);
+                if (MODE == 3) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[i] += scratch[(col + i) * 64 + (rl & 63)];
+                }
+                if (store_ok) {
+                    const int64_t t0 = n0 + col;
+                    float *yp = p.y + t0 * p.n + je;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        if (t0 + i < p.n_tokens) {
+                            const float val = acc[i] * __ldg(p.xscale + t0 + i);
+                            float *yq = yp + (int64_t)i * p.n;
+                            *yq = p.accumulate ? *yq + val : val;
                         }
                     }
                 }
@@ -459,10 +632,13 @@ static EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
+struct Maps {
+    CUtensorMap x, xlo, w, y;
+};
+
 template <int FMT, int BN, int MODE>
-static cudaError_t launch_t(const CUtensorMap &tm, const CUtensorMap &tl, const MmaParams &p,
-                            dim3 grid, cudaStream_t s) {
-    using C = MmaCfg<BN>;
+static cudaError_t launch_t(const Maps &mp, const MmaParams &p, dim3 grid, cudaStream_t s) {
+    using C = MmaCfg<BN, FMT == F_Q4_K && MODE != 3>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
@@ -470,31 +646,30 @@ static cudaError_t launch_t(const CUtensorMap &tm, const CUtensorMap &tl, const 
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    mma_kernel<FMT, BN, MODE><<<grid, kMmaThreads, C::kSmem, s>>>(tm, tl, p);
+    mma_kernel<FMT, BN, MODE><<<grid, kMmaThreads, C::kSmem, s>>>(mp.x, mp.xlo, mp.w, mp.y, p);
     return cudaGetLastError();
 }
 
 template <int FMT, int MODE>
-static cudaError_t launch_bn(int bn, const CUtensorMap &tm, const CUtensorMap &tl,
-                             const MmaParams &p, dim3 grid, cudaStream_t s) {
+static cudaError_t launch_bn(int bn, const Maps &mp, const MmaParams &p, dim3 grid, cudaStream_t s) {
     switch (bn) {
-    case 16: if (MODE == 1) return launch_t<FMT, 16, MODE>(tm, tl, p, grid, s); break;
-    case 32: return launch_t<FMT, 32, MODE>(tm, tl, p, grid, s);
-    case 64: return launch_t<FMT, 64, MODE>(tm, tl, p, grid, s);
-    case 128: return launch_t<FMT, 128, MODE>(tm, tl, p, grid, s);
-    case 256: return launch_t<FMT, 256, MODE>(tm, tl, p, grid, s);
+    case 16: if (MODE == 1) return launch_t<FMT, 16, MODE>(mp, p, grid, s); break;
+    case 32: return launch_t<FMT, 32, MODE>(mp, p, grid, s);
+    case 64: return launch_t<FMT, 64, MODE>(mp, p, grid, s);
+    case 128: return launch_t<FMT, 128, MODE>(mp, p, grid, s);
+    case 256: return launch_t<FMT, 256, MODE>(mp, p, grid, s);
     default: break;
     }
     return cudaErrorInvalidValue;
 }
 
 template <int FMT>
-static cudaError_t launch_fmt(int mode, int bn, const CUtensorMap &tm, const CUtensorMap &tl,
-                              const MmaParams &p, dim3 grid, cudaStream_t s) {
+static cudaError_t launch_fmt(int mode, int bn, const Maps &mp, const MmaParams &p, dim3 grid,
+                              cudaStream_t s) {
     constexpr bool quant = FMT != F_BF16 && FMT != F_F16;
-    if (mode == 2) return launch_bn<FMT, 2>(bn, tm, tl, p, grid, s);
-    if (quant && mode == 1) return launch_bn<FMT, quant ? 1 : 2>(bn, tm, tl, p, grid, s);
-    if (quant && mode == 3) return launch_bn<FMT, quant ? 3 : 2>(bn, tm, tl, p, grid, s);
+    if (mode == 2) return launch_bn<FMT, 2>(bn, mp, p, grid, s);
+    if (quant && mode == 1) return launch_bn<FMT, quant ? 1 : 2>(bn, mp, p, grid, s);
+    if (quant && mode == 3) return launch_bn<FMT, quant ? 3 : 2>(bn, mp, p, grid, s);
     return cudaErrorInvalidValue;
 }
 
@@ -534,29 +709,64 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
         while (tok < m.n_tokens) tok <<= 1;
     }
     const int bn = mode == 1 ? tok : 2 * tok;
-    CUtensorMap tm, tl;
-    if (!encode_x_map(encode, &tm, x16, kp, m.n_tokens, tok)) return cudaErrorInvalidValue;
+    Maps mp;
+    if (!encode_x_map(encode, &mp.x, x16, kp, m.n_tokens, tok)) return cudaErrorInvalidValue;
     if (mode >= 2) {
-        if (!encode_x_map(encode, &tl, x16lo, kp, m.n_tokens, tok)) return cudaErrorInvalidValue;
+        if (!encode_x_map(encode, &mp.xlo, x16lo, kp, m.n_tokens, tok)) return cudaErrorInvalidValue;
     } else {
-        tl = tm;
+        mp.xlo = mp.x;
+    }
+    CUtensorMap &tm = mp.x;
+    CUtensorMap &tw = mp.w;
+    // raw Q4_K weight tiles: the packed rows as a 2-D byte tensor [n][row_bytes],
+    // boxes of 128 rows x one 144-byte super-block
+    tw = tm;
+    if (m.fmt == F_Q4_K && mode != 3) {
+        const cuuint64_t dims[2] = {(cuuint64_t)m.row_bytes, (cuuint64_t)m.n};
+        const cuuint64_t strides[1] = {(cuuint64_t)m.row_bytes};
+        const cuuint32_t box[2] = {144u, (cuuint32_t)kBM};
+        const cuuint32_t estr[2] = {1, 1};
+        if (encode(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(m.w), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    // y as a [n_tokens][j_end] fp32 tensor with row stride n; one box = one
+    // output tile. TMA needs a 16-byte aligned base and row stride and a
+    // 16-byte aligned first column (j_start % 4 == 0); its bound on the inner
+    // dimension acts in 16-byte steps, so j_end must be a multiple of 4 too
+    // (otherwise up to 3 columns past j_end would be written).
+    const int rows_out = mode == 3 ? 64 : kBM;
+    const bool tma_store = (reinterpret_cast<uintptr_t>(m.y) & 15u) == 0 && (m.n % 4) == 0 &&
+                           (m.j0 % 4) == 0 && (m.j1 % 4) == 0;
+    mp.y = tm;
+    if (tma_store) {
+        const cuuint64_t dims[2] = {(cuuint64_t)m.j1, (cuuint64_t)m.n_tokens};
+        const cuuint64_t strides[1] = {(cuuint64_t)m.n * 4};
+        const cuuint32_t box[2] = {(cuuint32_t)rows_out, (cuuint32_t)tok};
+        const cuuint32_t estr[2] = {1, 1};
+        if (encode(&mp.y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, m.y, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
     }
     MmaParams p;
     p.w = m.w; p.y = m.y; p.xscale = xscale;
+    p.tma_store = tma_store ? 1 : 0;
     p.k = m.k; p.n = m.n; p.n_tokens = m.n_tokens; p.row_bytes = m.row_bytes;
     p.j0 = m.j0; p.j1 = m.j1;
     p.KS = (int)(kp / kBK);
     p.accumulate = m.accumulate;
     p.err = dev.err;
-    const int rows_out = mode == 3 ? 64 : kBM;
     const dim3 grid((unsigned)((M + rows_out - 1) / rows_out),
                     (unsigned)((m.n_tokens + tok - 1) / tok));
     switch (m.fmt) {
-    case F_BF16: return launch_fmt<F_BF16>(mode, bn, tm, tl, p, grid, s);
-    case F_F16: return launch_fmt<F_F16>(mode, bn, tm, tl, p, grid, s);
-    case F_Q4_0: return launch_fmt<F_Q4_0>(mode, bn, tm, tl, p, grid, s);
-    case F_Q4_K: return launch_fmt<F_Q4_K>(mode, bn, tm, tl, p, grid, s);
-    case F_Q6_K: return launch_fmt<F_Q6_K>(mode, bn, tm, tl, p, grid, s);
+    case F_BF16: return launch_fmt<F_BF16>(mode, bn, mp, p, grid, s);
+    case F_F16: return launch_fmt<F_F16>(mode, bn, mp, p, grid, s);
+    case F_Q4_0: return launch_fmt<F_Q4_0>(mode, bn, mp, p, grid, s);
+    case F_Q4_K: return launch_fmt<F_Q4_K>(mode, bn, mp, p, grid, s);
+    case F_Q6_K: return launch_fmt<F_Q6_K>(mode, bn, mp, p, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -11,7 +11,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/qmm.h"
+#include "qmm.h"
 #include "qmm_internal.h"
 
 namespace {

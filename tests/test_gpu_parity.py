@@ -153,7 +153,8 @@ def test_q6_k_head_tiled_and_accumulated():
 
 @pytest.mark.parametrize("path", [q.PATH_GEMV, q.PATH_MMA])
 @pytest.mark.parametrize("j0,j1,acc", [(5, 301, False), (130, 131, True), (0, 1, False),
-                                      (257, 700, True)])
+                                      (257, 700, True), (256, 601, True), (0, 700, True),
+                                      (128, 700, False)])
 def test_partial_tile_leaves_other_columns(path, j0, j1, acc):
     rng = np.random.default_rng(j0 * 13 + j1)
     k, n, nt = 512, 700, (1 if path == q.PATH_GEMV else 5)
