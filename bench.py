@@ -504,10 +504,12 @@ def run_case(args):
     def launch(c):
         if lib.qmm_matmul_ex(refs[c]):
             raise RuntimeError(q.qmm_last_error())
-    dt = time_loop(torch, launch, args.steps, args.warmup, ncop, stream)
+    with ClockSampler(0) as clk:
+        dt = time_loop(torch, launch, args.steps, args.warmup, ncop, stream)
     q.qmm_device_status(stream)
     print(json.dumps({"case": name, "overlap": not args.no_overlap, "us_per_call": dt * 1e6, "weight_gbs": w.size / dt / 1e9,
-                      "tflops": 2.0 * x.shape[0] * k * n / dt / 1e12, "copies": ncop}), flush=True)
+                      "tflops": 2.0 * x.shape[0] * k * n / dt / 1e12, "copies": ncop,
+                      "clocks": clk.summary()}), flush=True)
     return 0
 
 

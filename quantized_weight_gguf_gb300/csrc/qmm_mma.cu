@@ -2,9 +2,12 @@
 // Y[t][j] = sum_i X[t][i] W[j][i] for a tile of 128 output columns j and BN
 // tokens t per CTA.
 //
+// CTAs run in clusters of two: the pair works on adjacent 128-row tiles of W
+// and the same tokens, and each CTA fetches half of every X tile with a TMA
+// multicast into both CTAs' shared memory, halving the L2 traffic for X.
 // Pipeline per CTA (one CTA per SM, warp-specialised):
-//   warp 0      TMA producer: fp16 X tiles [BN tokens x 64 k] -> shared memory
-//               (128-byte swizzle) through a tensor map;
+//   warp 0      TMA producer: its half of each fp16 X tile [BN tokens x 64 k]
+//               -> shared memory of both CTAs (128-byte swizzle);
 //   warp 1      allocates the fp32 accumulator in tensor memory (TMEM) and one
 //               lane issues tcgen05.mma (M=128, N=BN, K=16, fp16 in, fp32 acc);
 //   warps 2..17 dequantize W in two groups of 8 warps that take alternate
@@ -62,17 +65,27 @@ constexpr int kRawBytes = kBM * 144;
 // and for raw staging kNR raw W super-block tiles.
 template <int BN, bool RAW>
 struct MmaCfg {
-    static constexpr int kBBytes = BN * kBK * 2;
+    // a pipeline stage holds KSUB consecutive 64-wide k-steps: small token
+    // tiles carry little MMA work per k-step, so their stages cover more k to
+    // amortise the fixed cost of each barrier round trip
+    static constexpr int KSUB = BN >= 128 ? 1 : (BN >= 64 ? 2 : 4);
+    static constexpr int kBBytes = BN * kBK * 2;            // one k-step of x
+    static constexpr int kAStage = KSUB * kABytes;
+    static constexpr int kBStage = KSUB * kBBytes;
     static constexpr int kNR = RAW ? 2 : 1;  // (1 unused slot keeps the layout uniform)
-    static constexpr int NA = 3;
-    static constexpr int kAvail = 212 * 1024 - (RAW ? kNR * kRawBytes : 0) - NA * kABytes;
-    static constexpr int NB = (kAvail / kBBytes) > 8 ? 8 : (kAvail / kBBytes);
-    static constexpr int kCols = BN < 32 ? 32 : BN;  // TMEM columns (power of two >= 32)
-    static constexpr size_t kSmem = (size_t)NA * kABytes + (size_t)NB * kBBytes +
+    static constexpr int NA = KSUB == 4 ? 2 : 3;
+    static constexpr int kAvail = 212 * 1024 - (RAW ? kNR * kRawBytes : 0) - NA * kAStage;
+    static constexpr int NB = (kAvail / kBStage) > 8 ? 8 : (kAvail / kBStage);
+    static constexpr int kAccCols = BN < 32 ? 32 : BN;  // one accumulator (power of two >= 32)
+    // two accumulators: even k-steps into one, odd into the other, so that
+    // back-to-back MMAs do not wait on each other's result; summed at the end
+    static constexpr int kCols = 2 * kAccCols;
+    static constexpr size_t kSmem = (size_t)NA * kAStage + (size_t)NB * kBStage +
                                     (RAW ? (size_t)kNR * kRawBytes : 0) + 1024 /*align*/ +
                                     512 /*barriers*/;
-    // the output tile (rows x tokens fp32) is staged in the x ring for the TMA store
-    static_assert(NB * kBBytes >= kBM * BN * 4, "x ring too small for the output tile");
+    // the output tile (rows x tokens fp32) is staged over the A and x rings
+    static_assert(NA * kAStage + NB * kBStage >= kBM * BN * 4, "rings too small for the output tile");
+    static_assert(NB >= 2, "x ring too shallow");
 };
 
 __device__ __forceinline__ bool wait_abortable(uint32_t bar, uint32_t parity,
@@ -184,13 +197,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     constexpr int kTokOut = MODE == 1 ? BN : BN / 2;  // tokens per CTA
     constexpr bool kRaw = FMT == F_Q4_K && MODE != 3;  // raw W tiles by TMA
     using C = MmaCfg<BN, kRaw>;
-    constexpr int NA = C::NA, NB = C::NB, kNR = C::kNR;
+    constexpr int NA = C::NA, NB = C::NB, kNR = C::kNR, KSUB = C::KSUB;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
     const uint32_t A0 = sbase;
-    const uint32_t B0 = sbase + NA * kABytes;
-    const uint32_t W0 = B0 + NB * C::kBBytes;                      // raw W stages (kRaw)
+    const uint32_t B0 = sbase + NA * C::kAStage;
+    const uint32_t W0 = B0 + NB * C::kBStage;                      // raw W stages (kRaw)
     const uint32_t bar0 = W0 + (kRaw ? kNR * kRawBytes : 0);
     auto fullA = [&](int s) { return bar0 + 8u * s; };
     auto emptyA = [&](int s) { return bar0 + 8u * (NA + s); };
@@ -204,17 +217,21 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     uint8_t *gen = smem_raw + (bar0 - raw_addr);
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gen + slot_off);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gen + slot_off + 8);
-    // arrivals that complete a dequantized A stage: the 8 warps of the group
-    // that owns the k-step (two groups take alternate k-steps). The A ring must
-    // hold at least as many stages as there are groups, so that no group can
-    // wait on a phase two ahead of the barrier.
-    constexpr int kFullACount = kDeqWarps / 2;
-    static_assert(C::NA >= 2, "A ring shallower than the number of producer groups");
+    // Two groups of 8 dequant warps take alternate k-steps. An A stage is done
+    // when every group with a k-step in it has arrived: one group when a stage
+    // is one k-step, both otherwise. The A ring must cover the groups' reach
+    // (NA * KSUB >= 2 k-steps) so that no group waits on a phase two ahead of
+    // the barrier.
+    constexpr int kGroups = 2;
+    constexpr int kFullACount = KSUB == 1 ? kDeqWarps / kGroups : kDeqWarps;
+    static_assert(C::NA * C::KSUB >= kGroups, "A ring shallower than the producer groups' reach");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t crank = cluster_ctarank();  // 0 or 1 within the CTA pair
     const int64_t m0 = p.j0 + (int64_t)blockIdx.x * kRowsOut;
     const int n0 = blockIdx.y * kTokOut;
-    const int KS = p.KS;
+    const int KS = p.KS;                    // 64-wide k-steps
+    const int NSTG = (KS + KSUB - 1) / KSUB;  // pipeline stages
 
     if (tid == 0) {
         for (int s = 0; s < NA; ++s) {
@@ -223,7 +240,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
         for (int s = 0; s < NB; ++s) {
             mbar_init(fullB(s), 1);
-            mbar_init(emptyB(s), 1);
+            mbar_init(emptyB(s), 2);  // both CTAs of the pair have consumed the stage
         }
         mbar_init(accb, 1);
         if (kRaw) {
@@ -241,6 +258,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // the peer's barriers exist before any multicast reaches them
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -251,31 +269,46 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             if (MODE != 1) prefetch_tmap(&tmx_lo);
             if (kRaw) prefetch_tmap(&tmw);
             int issued = 0, raw_issued = 0;
-            for (int ks = 0; ks < KS; ++ks) {
-                if (kRaw && (ks & 3) == 0) {
-                    const int b = ks >> 2, rs = b % kNR;
-                    if (b >= kNR && !wait_abortable(rawEmpty(rs), ((b / kNR) + 1) & 1, abort_flag)) {
-                        record_error(p.err, DERR_MMA_EMPTY);
-                        *abort_flag = 1;
-                        break;
+            for (int st = 0; st < NSTG; ++st) {
+                bool ok = true;
+                for (int sub = 0; sub < KSUB; ++sub) {
+                    const int ks = st * KSUB + sub;
+                    if (kRaw && ks < KS && (ks & 3) == 0) {
+                        const int b = ks >> 2, rs = b % kNR;
+                        if (b >= kNR &&
+                            !wait_abortable(rawEmpty(rs), ((b / kNR) + 1) & 1, abort_flag)) {
+                            record_error(p.err, DERR_MMA_EMPTY);
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(rawFull(rs), kRawBytes);
+                        tma_load_2d(W0 + rs * kRawBytes, &tmw, 144 * b, (int)m0, rawFull(rs));
+                        ++raw_issued;
                     }
-                    mbar_arrive_expect_tx(rawFull(rs), kRawBytes);
-                    tma_load_2d(W0 + rs * kRawBytes, &tmw, 144 * b, (int)m0, rawFull(rs));
-                    ++raw_issued;
                 }
-                const int slot = ks % NB;
-                if (ks >= NB && !wait_abortable(emptyB(slot), ((ks / NB) + 1) & 1, abort_flag)) {
+                if (!ok) break;
+                const int slot = st % NB;
+                if (st >= NB && !wait_abortable(emptyB(slot), ((st / NB) + 1) & 1, abort_flag)) {
                     record_error(p.err, DERR_MMA_EMPTY);
                     *abort_flag = 1;
                     break;
                 }
-                mbar_arrive_expect_tx(fullB(slot), C::kBBytes);
-                if (MODE == 1) {
-                    tma_load_2d(B0 + slot * C::kBBytes, &tmx, ks * kBK, n0, fullB(slot));
-                } else {  // hi rows then lo rows of the same tokens
-                    tma_load_2d(B0 + slot * C::kBBytes, &tmx, ks * kBK, n0, fullB(slot));
-                    tma_load_2d(B0 + slot * C::kBBytes + (BN / 2) * 128, &tmx_lo, ks * kBK, n0,
-                                fullB(slot));
+                // the whole stage lands here: this CTA's halves and the peer's halves
+                mbar_arrive_expect_tx(fullB(slot), C::kBStage);
+                for (int sub = 0; sub < KSUB; ++sub) {
+                    const int ks = st * KSUB + sub;  // past KS: zero-filled by the map
+                    // MODE 1: this CTA fetches token rows [n0 + crank BN/2, +BN/2);
+                    // MODE 2/3: CTA 0 the hi rows, CTA 1 the lo rows of the tile's tokens
+                    const uint32_t dst =
+                        B0 + slot * C::kBStage + sub * C::kBBytes + crank * (BN / 2) * 128;
+                    if (MODE == 1)
+                        tma_load_2d_multicast(dst, &tmx, ks * kBK, n0 + (int)crank * (BN / 2),
+                                              fullB(slot), (uint16_t)3);
+                    else
+                        tma_load_2d_multicast(dst,
+                                              crank ? (const void *)&tmx_lo : (const void *)&tmx,
+                                              ks * kBK, n0, fullB(slot), (uint16_t)3);
                 }
                 ++issued;
             }
@@ -288,26 +321,33 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         // ------------------------------ MMA issue ------------------------------
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
-            for (int ks = 0; ks < KS; ++ks) {
-                const int sa = ks % NA, sb = ks % NB;
-                if (!wait_abortable(fullA(sa), (ks / NA) & 1, abort_flag)) {
+            for (int st = 0; st < NSTG; ++st) {
+                const int sa = st % NA, sb = st % NB;
+                if (!wait_abortable(fullA(sa), (st / NA) & 1, abort_flag)) {
                     record_error(p.err, DERR_MMA_A);
                     *abort_flag = 1;
                     break;
                 }
-                if (!wait_abortable(fullB(sb), (ks / NB) & 1, abort_flag)) {
+                if (!wait_abortable(fullB(sb), (st / NB) & 1, abort_flag)) {
                     record_error(p.err, DERR_MMA_B);
                     *abort_flag = 1;
                     break;
                 }
                 tc_fence_after();
-                const uint64_t ad = sdesc_sw128(A0 + sa * kABytes);
-                const uint64_t bd = sdesc_sw128(B0 + sb * C::kBBytes);
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16 per instruction: +32 bytes
-                    tc_mma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (ks | kk) != 0);
+                for (int sub = 0; sub < KSUB; ++sub) {
+                    const int ks = st * KSUB + sub;
+                    if (ks < KS) {
+                        const uint64_t ad = sdesc_sw128(A0 + sa * C::kAStage + sub * kABytes);
+                        const uint64_t bd = sdesc_sw128(B0 + sb * C::kBStage + sub * C::kBBytes);
+                        const uint32_t dacc = tmem + (uint32_t)((ks & 1) * C::kAccCols);
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16 per instruction: +32 bytes
+                            tc_mma_f16(dacc, ad + 2 * kk, bd + 2 * kk, idesc, (ks > 1) || kk != 0);
+                    }
+                }
                 tc_commit(emptyA(sa));
-                tc_commit(emptyB(sb));
+                tc_commit_multicast(emptyB(sb), (uint16_t)3);  // both CTAs may refill
             }
             tc_commit(accb);  // fires when every MMA issued above has completed
         }
@@ -346,15 +386,21 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 __syncwarp();
                 // the last k-step of the super-block this group takes releases it
                 if (lane == 0 && !failed && c >= 2) mbar_arrive(rawEmpty(rs));
-                const int slot = ks % NA;
-                if (!failed && ks >= NA &&
-                    !wait_abortable(emptyA(slot), ((ks / NA) + 1) & 1, abort_flag)) {
+                // stage st holds k-steps st*KSUB .. +KSUB-1; this group's first
+                // k-step in a stage waits for the slot, its last one signals it
+                const int st = ks / KSUB, sub = ks % KSUB;
+                const int slot = st % NA;
+                const bool first_in_stage = sub < kGroups;
+                const bool last_in_stage = sub + kGroups >= KSUB;  // KS % 4 == 0 here
+                if (!failed && first_in_stage && st >= NA &&
+                    !wait_abortable(emptyA(slot), ((st / NA) + 1) & 1, abort_flag)) {
                     failed = true;
                     *abort_flag = 1;
                     record_error(p.err, DERR_MMA_EMPTY);
                 }
                 if (!failed) {
-                    const uint32_t arow = A0 + slot * kABytes + (uint32_t)r * 128u;
+                    const uint32_t arow =
+                        A0 + slot * C::kAStage + sub * kABytes + (uint32_t)r * 128u;
                     // weights 16h..16h+15 -> chunks 2h, 2h+1; 32+16h.. -> chunks 4+2h, 5+2h
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
@@ -363,9 +409,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                                hw[4 * cc + 3]);
                     }
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0 && !failed) mbar_arrive(fullA(slot));
+                if (last_in_stage) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && !failed) mbar_arrive(fullA(slot));
+                }
             }
         } else {
         const int dt = tid - 64;
@@ -385,7 +433,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             const int64_t v = p.k - k0;
             return (int)(v < 0 ? 0 : (v > 32 ? 32 : v));
         };
-        const int NI = (KS - par + 1) / 2;  // k-steps of this group
+        // k-steps of this group, over the stage-padded range: a k-step past k
+        // stores zeros (the MMA skips it) but still takes part in its stage's
+        // arrival count
+        const int NI = (NSTG * KSUB - par + 1) / 2;
 #pragma unroll
         for (int q = 0; q < PD; ++q) {
             const int64_t k0 = k0_of(q);
@@ -422,15 +473,19 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                     const int64_t kn = k0_of(i + PD);
                     const int nvn = nvalid_of(kn);
                     if (i + PD < NI && row_ok && nvn > 0) ring[q].load(rowp, kn, nvn);
-                    const int slot = ks % NA;
-                    if (!failed && ks >= NA &&
-                        !wait_abortable(emptyA(slot), ((ks / NA) + 1) & 1, abort_flag)) {
+                    const int st = ks / KSUB, sub = ks % KSUB;
+                    const int slot = st % NA;
+                    const bool first_in_stage = sub < kGroups;
+                    const bool last_in_stage = sub + kGroups >= KSUB;
+                    if (!failed && first_in_stage && st >= NA &&
+                        !wait_abortable(emptyA(slot), ((st / NA) + 1) & 1, abort_flag)) {
                         failed = true;
                         *abort_flag = 1;
                         record_error(p.err, DERR_MMA_EMPTY);
                     }
                     if (!failed) {
-                        const uint32_t arow = A0 + slot * kABytes + (uint32_t)r * 128u;
+                        const uint32_t arow =
+                            A0 + slot * C::kAStage + sub * kABytes + (uint32_t)r * 128u;
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
                             const uint32_t chunk = (uint32_t)(4 * h + c) ^ swz;
@@ -438,9 +493,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                                    hw[4 * c + 3]);
                         }
                     }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0 && !failed) mbar_arrive(fullA(slot));
+                    if (last_in_stage) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0 && !failed) mbar_arrive(fullA(slot));
+                    }
                 }
             }
         }
@@ -462,19 +519,28 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         const uint32_t tbase = tmem + ((uint32_t)(32 * quarter) << 16);
         float *scratch = reinterpret_cast<float *>(smem_raw + (A0 - raw_addr));  // [col][64]
         // columns in chunks of 16 (kSliceCols is a multiple of 16)
+        // the two accumulators (even / odd k-steps) are summed here; KS == 1
+        // leaves the odd one unwritten
+        const bool two_acc = KS > 1;
         auto load_acc = [&](int col, float (&acc)[16]) {
-            uint32_t v[16];
+            uint32_t v[16], v2[16];
             tmem_ld16(tbase + (uint32_t)col, v);
+            if (two_acc) tmem_ld16(tbase + (uint32_t)(C::kAccCols + col), v2);
             if (MODE == 1) {
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) acc[i] = __uint_as_float(v[i]);
+                for (int i = 0; i < 16; ++i)
+                    acc[i] = __uint_as_float(v[i]) + (two_acc ? __uint_as_float(v2[i]) : 0.0f);
             } else {
-                uint32_t w2[16];
+                uint32_t w2[16], w3[16];
                 tmem_ld16(tbase + (uint32_t)(col + BN / 2), w2);
+                if (two_acc) tmem_ld16(tbase + (uint32_t)(C::kAccCols + col + BN / 2), w3);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) acc[i] = __uint_as_float(v[i]) + __uint_as_float(w2[i]);
+                for (int i = 0; i < 16; ++i) {
+                    acc[i] = __uint_as_float(v[i]) + __uint_as_float(w2[i]);
+                    if (two_acc) acc[i] += __uint_as_float(v2[i]) + __uint_as_float(w3[i]);
+                }
             }
         };
         if (MODE == 3 && quarter >= 2) {
@@ -492,7 +558,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             // stage the [tokens][rows] fp32 tile in the (now idle) x ring, then one
             // TMA store (or reduce-add) writes it; the map clips rows >= n_tokens
             // and columns >= j_end
-            float *stile = reinterpret_cast<float *>(smem_raw + (B0 - raw_addr));
+            // over the A and x rings (MODE 3 keeps its row-pair scratch in the A
+            // ring, and its smaller tile fits the x ring)
+            const uint32_t st0 = MODE == 3 ? B0 : A0;
+            float *stile = reinterpret_cast<float *>(smem_raw + (st0 - raw_addr));
             if (MODE != 3 || quarter < 2) {
                 __syncwarp();
                 const int row = MODE == 3 ? (rl & 63) : rl;
@@ -515,9 +584,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             named_barrier(3, 32 * kDeqWarps);
             if (tid == 64 && acc_ok && !*abort_flag) {
                 if (p.accumulate)
-                    tma_reduce_add_2d(&tmy, (int)m0, n0, B0);
+                    tma_reduce_add_2d(&tmy, (int)m0, n0, st0);
                 else
-                    tma_store_2d(&tmy, (int)m0, n0, B0);
+                    tma_store_2d(&tmy, (int)m0, n0, st0);
                 bulk_commit_group();
                 bulk_wait_group_read0();
             }
@@ -547,6 +616,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // no multicast or remote arrival is still headed for this CTA
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -646,8 +716,19 @@ static cudaError_t launch_t(const Maps &mp, const MmaParams &p, dim3 grid, cudaS
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    mma_kernel<FMT, BN, MODE><<<grid, kMmaThreads, C::kSmem, s>>>(mp.x, mp.xlo, mp.w, mp.y, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kMmaThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mma_kernel<FMT, BN, MODE>, mp.x, mp.xlo, mp.w, mp.y, p);
 }
 
 template <int FMT, int MODE>
@@ -709,10 +790,13 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
         while (tok < m.n_tokens) tok <<= 1;
     }
     const int bn = mode == 1 ? tok : 2 * tok;
+    // each CTA of a pair fetches half of an x tile: BN/2 token rows
+    const int box_rows = bn / 2;
     Maps mp;
-    if (!encode_x_map(encode, &mp.x, x16, kp, m.n_tokens, tok)) return cudaErrorInvalidValue;
+    if (!encode_x_map(encode, &mp.x, x16, kp, m.n_tokens, box_rows)) return cudaErrorInvalidValue;
     if (mode >= 2) {
-        if (!encode_x_map(encode, &mp.xlo, x16lo, kp, m.n_tokens, tok)) return cudaErrorInvalidValue;
+        if (!encode_x_map(encode, &mp.xlo, x16lo, kp, m.n_tokens, box_rows))
+            return cudaErrorInvalidValue;
     } else {
         mp.xlo = mp.x;
     }
@@ -759,8 +843,10 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
     p.KS = (int)(kp / kBK);
     p.accumulate = m.accumulate;
     p.err = dev.err;
-    const dim3 grid((unsigned)((M + rows_out - 1) / rows_out),
-                    (unsigned)((m.n_tokens + tok - 1) / tok));
+    // pairs of CTAs (clusters of two) along the row tiles: round up to even
+    unsigned gx = (unsigned)((M + rows_out - 1) / rows_out);
+    gx += gx & 1u;
+    const dim3 grid(gx, (unsigned)((m.n_tokens + tok - 1) / tok));
     switch (m.fmt) {
     case F_BF16: return launch_fmt<F_BF16>(mode, bn, mp, p, grid, s);
     case F_F16: return launch_fmt<F_F16>(mode, bn, mp, p, grid, s);
