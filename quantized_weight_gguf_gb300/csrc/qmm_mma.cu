@@ -42,7 +42,6 @@ constexpr int kDeqWarps = 16;                     // two groups of 8, alternate 
 constexpr int kMmaThreads = 64 + 32 * kDeqWarps;
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kABytes = kBM * kBK * 2;  // 16 KB per stage
 
 struct MmaParams {
     const uint8_t *w;
@@ -60,32 +59,50 @@ struct MmaParams {
 // 256-wide slice of k), then decoded from shared memory.
 constexpr int kRawBytes = kBM * 144;
 
-// Shared memory: a ring of NA dequantized W stages (made on chip), a deeper
-// ring of NB x stages (streamed from L2, latency-bound: it gets the room),
-// and for raw staging kNR raw W super-block tiles.
+#ifndef QMM_KSUB_WIDE
+#define QMM_KSUB_WIDE 2
+#endif
+
+// Tensor memory (512 columns x 128 lanes of 32 bits, all taken by the one CTA
+// on the SM): the fp32 accumulator(s) first, then a ring of NA dequantized W
+// stages (A operand: row r on lane r, k pairs packed per column, 32 columns
+// per 64-wide k-step). Shared memory: a ring of NB x stages (streamed from
+// L2 by TMA) and, for Q4_K, kNR raw super-block tiles of 128 rows.
 template <int BN, bool RAW>
 struct MmaCfg {
-    // a pipeline stage holds KSUB consecutive 64-wide k-steps: small token
-    // tiles carry little MMA work per k-step, so their stages cover more k to
-    // amortise the fixed cost of each barrier round trip
-    static constexpr int KSUB = BN >= 128 ? 1 : (BN >= 64 ? 2 : 4);
+    // a pipeline stage holds KSUB consecutive 64-wide k-steps: every barrier
+    // round trip, commit and TMA issue is paid once per stage
+    static constexpr int KSUB = BN >= 256 ? QMM_KSUB_WIDE : 2;
     static constexpr int kBBytes = BN * kBK * 2;            // one k-step of x
-    static constexpr int kAStage = KSUB * kABytes;
     static constexpr int kBStage = KSUB * kBBytes;
-    static constexpr int kNR = RAW ? 2 : 1;  // (1 unused slot keeps the layout uniform)
-    static constexpr int NA = KSUB == 4 ? 2 : 3;
-    static constexpr int kAvail = 212 * 1024 - (RAW ? kNR * kRawBytes : 0) - NA * kAStage;
+    static constexpr int kAccCols = BN < 32 ? 32 : BN;      // one accumulator
+    // two accumulators (even k-steps into one, odd into the other, summed at
+    // the end) where TMEM has room: back-to-back MMAs then do not wait on
+    // each other's result
+    static constexpr int kNAcc = BN >= 256 ? 1 : 2;
+    static constexpr int kACol0 = kNAcc * kAccCols;         // first A column
+    static constexpr int kAStageCols = KSUB * 32;
+    static constexpr int kNAFit = (512 - kACol0) / kAStageCols;
+    static constexpr int NA = kNAFit > 6 ? 6 : kNAFit;
+    static constexpr int kCols = 512;
+    // raw W stages: as many as fit, up to 4, next to a minimum x ring; HBM
+    // latency is hidden by the raw ring, L2 latency by the x ring
+    static constexpr int kNBMin = (4 + KSUB - 1) / KSUB;
+    static constexpr int kRawFit = (212 * 1024 - kNBMin * kBStage) / kRawBytes;
+    static constexpr int kNR = RAW ? (kRawFit > 4 ? 4 : kRawFit) : 1;
+    static_assert(!RAW || kNR >= 2, "raw W ring too shallow");
+    static constexpr int kAvail = 212 * 1024 - (RAW ? kNR * kRawBytes : 0);
     static constexpr int NB = (kAvail / kBStage) > 8 ? 8 : (kAvail / kBStage);
-    static constexpr int kAccCols = BN < 32 ? 32 : BN;  // one accumulator (power of two >= 32)
-    // two accumulators: even k-steps into one, odd into the other, so that
-    // back-to-back MMAs do not wait on each other's result; summed at the end
-    static constexpr int kCols = 2 * kAccCols;
-    static constexpr size_t kSmem = (size_t)NA * kAStage + (size_t)NB * kBStage +
-                                    (RAW ? (size_t)kNR * kRawBytes : 0) + 1024 /*align*/ +
-                                    512 /*barriers*/;
-    // the output tile (rows x tokens fp32) is staged over the A and x rings
-    static_assert(NA * kAStage + NB * kBStage >= kBM * BN * 4, "rings too small for the output tile");
-    static_assert(NB >= 2, "x ring too shallow");
+    static constexpr size_t kSmemUsed = (size_t)NB * kBStage +
+                                        (RAW ? (size_t)kNR * kRawBytes : 0) + 1024 /*align*/ +
+                                        512 /*barriers*/;
+    // at least half of the SM's shared memory, so that no second CTA can be
+    // resident and block in its TMEM allocation (every CTA takes all 512
+    // columns) while holding resources its cluster peer waits for
+    static constexpr size_t kSmem = kSmemUsed < 120 * 1024 ? 120 * 1024 : kSmemUsed;
+    // the output tile (rows x tokens fp32) is staged over the x ring
+    static_assert(NB * kBStage >= kBM * BN * 4, "x ring too small for the output tile");
+    static_assert(NB >= 2 && NA >= 2, "rings too shallow");
 };
 
 __device__ __forceinline__ bool wait_abortable(uint32_t bar, uint32_t parity,
@@ -201,8 +218,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
-    const uint32_t A0 = sbase;
-    const uint32_t B0 = sbase + NA * C::kAStage;
+    const uint32_t B0 = sbase;                                     // x ring
     const uint32_t W0 = B0 + NB * C::kBStage;                      // raw W stages (kRaw)
     const uint32_t bar0 = W0 + (kRaw ? kNR * kRawBytes : 0);
     auto fullA = [&](int s) { return bar0 + 8u * s; };
@@ -232,6 +248,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const int n0 = blockIdx.y * kTokOut;
     const int KS = p.KS;                    // 64-wide k-steps
     const int NSTG = (KS + KSUB - 1) / KSUB;  // pipeline stages
+    // Every tile walks k in its own rotated order (whole super-blocks), so
+    // that the CTAs do not all fetch the same x tile from the same L2 lines
+    // at the same moment. The sum is the same up to rounding order.
+    const int rot = (KS % 4 == 0) ? 4 * (int)((blockIdx.x >> 1) % (unsigned)(KS / 4)) : 0;
+    auto kx = [&](int ks) { return rot ? (ks + rot) % KS : ks; };
 
     if (tid == 0) {
         for (int s = 0; s < NA; ++s) {
@@ -283,7 +304,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                             break;
                         }
                         mbar_arrive_expect_tx(rawFull(rs), kRawBytes);
-                        tma_load_2d(W0 + rs * kRawBytes, &tmw, 144 * b, (int)m0, rawFull(rs));
+                        tma_load_2d(W0 + rs * kRawBytes, &tmw, 144 * (kx(ks) >> 2), (int)m0,
+                                    rawFull(rs));
                         ++raw_issued;
                     }
                 }
@@ -303,12 +325,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                     const uint32_t dst =
                         B0 + slot * C::kBStage + sub * C::kBBytes + crank * (BN / 2) * 128;
                     if (MODE == 1)
-                        tma_load_2d_multicast(dst, &tmx, ks * kBK, n0 + (int)crank * (BN / 2),
+                        tma_load_2d_multicast(dst, &tmx, kx(ks) * kBK, n0 + (int)crank * (BN / 2),
                                               fullB(slot), (uint16_t)3);
                     else
                         tma_load_2d_multicast(dst,
                                               crank ? (const void *)&tmx_lo : (const void *)&tmx,
-                                              ks * kBK, n0, fullB(slot), (uint16_t)3);
+                                              kx(ks) * kBK, n0, fullB(slot), (uint16_t)3);
                 }
                 ++issued;
             }
@@ -319,60 +341,100 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issue ------------------------------
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
-            for (int st = 0; st < NSTG; ++st) {
-                const int sa = st % NA, sb = st % NB;
-                if (!wait_abortable(fullA(sa), (st / NA) & 1, abort_flag)) {
-                    record_error(p.err, DERR_MMA_A);
-                    *abort_flag = 1;
-                    break;
-                }
-                if (!wait_abortable(fullB(sb), (st / NB) & 1, abort_flag)) {
-                    record_error(p.err, DERR_MMA_B);
-                    *abort_flag = 1;
-                    break;
-                }
-                tc_fence_after();
+        // The whole warp runs the loop (so that descriptors and addresses stay
+        // warp-uniform); one elected lane issues the MMAs and their commits.
+        constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
+        const bool leader = elect_one();
+        for (int st = 0; st < NSTG; ++st) {
+            const int sa = st % NA, sb = st % NB;
+            bool ok = wait_abortable(fullA(sa), (st / NA) & 1, abort_flag);
+            if (__all_sync(0xFFFFFFFFu, ok) == 0) {
+                if (leader) { record_error(p.err, DERR_MMA_A); *abort_flag = 1; }
+                break;
+            }
+            ok = wait_abortable(fullB(sb), (st / NB) & 1, abort_flag);
+            if (__all_sync(0xFFFFFFFFu, ok) == 0) {
+                if (leader) { record_error(p.err, DERR_MMA_B); *abort_flag = 1; }
+                break;
+            }
+            tc_fence_after();
+            if (leader) {
 #pragma unroll
                 for (int sub = 0; sub < KSUB; ++sub) {
                     const int ks = st * KSUB + sub;
                     if (ks < KS) {
-                        const uint64_t ad = sdesc_sw128(A0 + sa * C::kAStage + sub * kABytes);
+                        const uint32_t at = tmem + (uint32_t)(C::kACol0 + sa * C::kAStageCols +
+                                                              sub * 32);
                         const uint64_t bd = sdesc_sw128(B0 + sb * C::kBStage + sub * C::kBBytes);
-                        const uint32_t dacc = tmem + (uint32_t)((ks & 1) * C::kAccCols);
+                        const uint32_t dacc =
+                            tmem + (uint32_t)((C::kNAcc == 2 ? (ks & 1) : 0) * C::kAccCols);
+                        const bool acc0 = C::kNAcc == 2 ? ks > 1 : ks > 0;
 #pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16 per instruction: +32 bytes
-                            tc_mma_f16(dacc, ad + 2 * kk, bd + 2 * kk, idesc, (ks > 1) || kk != 0);
+                        for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16: 8 A columns, 32 B bytes
+                            tc_mma_f16_ts(dacc, at + 8 * kk, bd + 2 * kk, idesc, acc0 || kk != 0);
                     }
                 }
                 tc_commit(emptyA(sa));
                 tc_commit_multicast(emptyB(sb), (uint16_t)3);  // both CTAs may refill
             }
-            tc_commit(accb);  // fires when every MMA issued above has completed
+            __syncwarp();
         }
+        if (leader) tc_commit(accb);  // fires when every MMA issued above has completed
+        __syncwarp();
     } else {
         // ------------------------------ W dequant producers ------------------------------
+        // Warp w (2..17) owns TMEM lanes 32 (w % 4) .. +31, i.e. rows r of the
+        // tile; (w - 2) / 4 picks the half h of each 64-wide k-step and the
+        // group g (k-step parity) it takes. Each group's first k-step in a
+        // stage waits for the stage to be free, its last one signals it.
+        const int quarter = warp & 3;
+        const int r = 32 * quarter + lane;
+        const int dq = (warp - 2) >> 2;
+        const int h = dq & 1;
+        const int g = dq >> 1;
+        const uint32_t tlane = tmem + ((uint32_t)(32 * quarter) << 16);
+        // k-step ks of the group: wait for its A slot (when first in the stage)
+        // and return the TMEM address of its 32 columns
+        auto a_slot = [&](int ks, bool &failed) {
+            const int st = ks / KSUB, sub = ks % KSUB;
+            const int slot = st % NA;
+            if (sub < kGroups && st >= NA) {
+                const bool ok = wait_abortable(emptyA(slot), ((st / NA) + 1) & 1, abort_flag);
+                if (__all_sync(0xFFFFFFFFu, ok) == 0) {
+                    if (!failed) record_error(p.err, DERR_MMA_EMPTY);
+                    failed = true;
+                    *abort_flag = 1;
+                }
+                tc_fence_after();  // the MMAs that read the slot are done
+            }
+            return tlane + (uint32_t)(C::kACol0 + slot * C::kAStageCols + sub * 32);
+        };
+        auto a_done = [&](int ks, bool failed) {
+            const int st = ks / KSUB, sub = ks % KSUB;
+            if (sub + kGroups >= KSUB) {
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0 && !failed) mbar_arrive(fullA(st % NA));
+            }
+        };
         if constexpr (kRaw) {
-            // two groups of 256 threads take alternate k-steps; thread (r, h) of a
-            // group decodes half h of row r's 64-weight chunk from the raw tile
-            const int dt = tid - 64;
-            const int r = dt & (kBM - 1);
-            const int h = (dt >> 7) & 1;
-            const int g = dt >> 8;
+            // thread (r, h) decodes half h of row r's 64-weight chunk from the raw tile
             const bool row_ok = m0 + r < p.j1;
-            const uint32_t swz = (uint32_t)(r & 7);
-            const int NI = (KS - g + 1) / 2;
+            const int NI = (KS - g + 1) / 2;  // KS % 4 == 0: every stage is full
             bool failed = false;
             for (int i = 0; i < NI; ++i) {
                 const int ks = g + 2 * i;
                 const int b = ks >> 2, c = ks & 3;
                 const int rs = b % kNR;
                 uint32_t hw[16];
-                if (!failed && !wait_abortable(rawFull(rs), (b / kNR) & 1, abort_flag)) {
-                    failed = true;
-                    *abort_flag = 1;
-                    record_error(p.err, DERR_MMA_A);
+                if (!failed) {
+                    const bool ok = wait_abortable(rawFull(rs), (b / kNR) & 1, abort_flag);
+                    if (__all_sync(0xFFFFFFFFu, ok) == 0) {
+                        record_error(p.err, DERR_MMA_A);
+                        failed = true;
+                        *abort_flag = 1;
+                    }
                 }
                 if (!failed && row_ok) {
                     const uint32_t rb = W0 + rs * kRawBytes + (uint32_t)r * 144u;
@@ -386,49 +448,21 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 __syncwarp();
                 // the last k-step of the super-block this group takes releases it
                 if (lane == 0 && !failed && c >= 2) mbar_arrive(rawEmpty(rs));
-                // stage st holds k-steps st*KSUB .. +KSUB-1; this group's first
-                // k-step in a stage waits for the slot, its last one signals it
-                const int st = ks / KSUB, sub = ks % KSUB;
-                const int slot = st % NA;
-                const bool first_in_stage = sub < kGroups;
-                const bool last_in_stage = sub + kGroups >= KSUB;  // KS % 4 == 0 here
-                if (!failed && first_in_stage && st >= NA &&
-                    !wait_abortable(emptyA(slot), ((st / NA) + 1) & 1, abort_flag)) {
-                    failed = true;
-                    *abort_flag = 1;
-                    record_error(p.err, DERR_MMA_EMPTY);
-                }
-                if (!failed) {
-                    const uint32_t arow =
-                        A0 + slot * C::kAStage + sub * kABytes + (uint32_t)r * 128u;
-                    // weights 16h..16h+15 -> chunks 2h, 2h+1; 32+16h.. -> chunks 4+2h, 5+2h
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const uint32_t chunk = (uint32_t)((cc >> 1) * 4 + 2 * h + (cc & 1)) ^ swz;
-                        sts128(arow + (chunk << 4), hw[4 * cc], hw[4 * cc + 1], hw[4 * cc + 2],
-                               hw[4 * cc + 3]);
-                    }
-                }
-                if (last_in_stage) {
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0 && !failed) mbar_arrive(fullA(slot));
-                }
+                const uint32_t ta = a_slot(ks, failed);
+                // weights 16h + 0..15 -> columns 8h..8h+7; 32 + 16h + 0..15 -> 16 + 8h..
+                tmem_st8(ta + 8u * h, hw);
+                tmem_st8(ta + 16u + 8u * h, hw + 8);
+                a_done(ks, failed);
             }
         } else {
-        const int dt = tid - 64;
-        const int r = dt & (kBM - 1);
-        const int h = (dt >> 7) & 1;
-        const int par = dt >> 8;  // this group's k-steps: par, par + 2, ...
         const bool lo_part = MODE == 3 && r >= 64;   // MODE 3: rows 64..127 hold W_lo
         const int64_t j = m0 + (MODE == 3 ? (r & 63) : r);
         const bool row_ok = j < p.j1;
         const uint8_t *rowp = p.w + (row_ok ? j : 0) * p.row_bytes;
-        const uint32_t swz = (uint32_t)(r & 7);
         constexpr int PD = Prefetch<FMT>::value;
         Raw32<FMT> ring[PD];
-        // this thread's i-th k-step is par + 2 i
-        auto k0_of = [&](int i) { return (int64_t)(par + 2 * i) * kBK + 32 * h; };
+        // this thread's i-th k-step is g + 2 i
+        auto k0_of = [&](int i) { return (int64_t)kx(g + 2 * i) * kBK + 32 * h; };
         auto nvalid_of = [&](int64_t k0) {
             const int64_t v = p.k - k0;
             return (int)(v < 0 ? 0 : (v > 32 ? 32 : v));
@@ -436,7 +470,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         // k-steps of this group, over the stage-padded range: a k-step past k
         // stores zeros (the MMA skips it) but still takes part in its stage's
         // arrival count
-        const int NI = (NSTG * KSUB - par + 1) / 2;
+        const int NI = (NSTG * KSUB - g + 1) / 2;
 #pragma unroll
         for (int q = 0; q < PD; ++q) {
             const int64_t k0 = k0_of(q);
@@ -449,7 +483,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             for (int q = 0; q < PD; ++q) {
                 const int i = i0 + q;
                 if (i < NI) {
-                    const int ks = par + 2 * i;
+                    const int ks = g + 2 * i;
                     const int64_t k0 = k0_of(i);
                     const int nv = nvalid_of(k0);
                     uint32_t hw[16];
@@ -473,31 +507,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                     const int64_t kn = k0_of(i + PD);
                     const int nvn = nvalid_of(kn);
                     if (i + PD < NI && row_ok && nvn > 0) ring[q].load(rowp, kn, nvn);
-                    const int st = ks / KSUB, sub = ks % KSUB;
-                    const int slot = st % NA;
-                    const bool first_in_stage = sub < kGroups;
-                    const bool last_in_stage = sub + kGroups >= KSUB;
-                    if (!failed && first_in_stage && st >= NA &&
-                        !wait_abortable(emptyA(slot), ((st / NA) + 1) & 1, abort_flag)) {
-                        failed = true;
-                        *abort_flag = 1;
-                        record_error(p.err, DERR_MMA_EMPTY);
-                    }
-                    if (!failed) {
-                        const uint32_t arow =
-                            A0 + slot * C::kAStage + sub * kABytes + (uint32_t)r * 128u;
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint32_t chunk = (uint32_t)(4 * h + c) ^ swz;
-                            sts128(arow + chunk * 16u, hw[4 * c], hw[4 * c + 1], hw[4 * c + 2],
-                                   hw[4 * c + 3]);
-                        }
-                    }
-                    if (last_in_stage) {
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0 && !failed) mbar_arrive(fullA(slot));
-                    }
+                    const uint32_t ta = a_slot(ks, failed);
+                    tmem_st16(ta + 16u * h, hw);  // weights 32h + 0..31 -> columns 16h..16h+15
+                    a_done(ks, failed);
                 }
             }
         }
@@ -507,21 +519,21 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         const bool acc_ok = mbar_wait(accb, 0);
         if (!acc_ok) record_error(p.err, DERR_MMA_ACC);
         tc_fence_after();
-        const int quarter = warp & 3;
-        const int slice = (warp - 2) >> 2;  // 0..3: which part of the token columns
+        const int slice = dq;  // 0..3: which part of the token columns  // 0..3: which part of the token columns
         constexpr int kSlices = kTokOut >= 64 ? 4 : (kTokOut >= 32 ? 2 : 1);
         constexpr int kSliceCols = kTokOut / kSlices;
         const int c_lo = slice < kSlices ? slice * kSliceCols : 0;
         const int c_hi = slice < kSlices ? c_lo + kSliceCols : 0;
-        const int rl = 32 * quarter + lane;                 // accumulator row (TMEM lane)
+        const int rl = r;                                   // accumulator row (TMEM lane)
         const int64_t je = m0 + (MODE == 3 ? (rl & 63) : rl);
         const bool store_ok = acc_ok && !*abort_flag && je < p.j1;
         const uint32_t tbase = tmem + ((uint32_t)(32 * quarter) << 16);
-        float *scratch = reinterpret_cast<float *>(smem_raw + (A0 - raw_addr));  // [col][64]
+        // MODE 3 row-pair scratch [col][64] and the output tile: over the x ring
+        float *scratch = reinterpret_cast<float *>(smem_raw + (B0 - raw_addr));
         // columns in chunks of 16 (kSliceCols is a multiple of 16)
         // the two accumulators (even / odd k-steps) are summed here; KS == 1
         // leaves the odd one unwritten
-        const bool two_acc = KS > 1;
+        const bool two_acc = C::kNAcc == 2 && KS > 1;
         auto load_acc = [&](int col, float (&acc)[16]) {
             uint32_t v[16], v2[16];
             tmem_ld16(tbase + (uint32_t)col, v);
@@ -557,10 +569,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         if (p.tma_store) {
             // stage the [tokens][rows] fp32 tile in the (now idle) x ring, then one
             // TMA store (or reduce-add) writes it; the map clips rows >= n_tokens
-            // and columns >= j_end
-            // over the A and x rings (MODE 3 keeps its row-pair scratch in the A
-            // ring, and its smaller tile fits the x ring)
-            const uint32_t st0 = MODE == 3 ? B0 : A0;
+            // and columns >= j_end (MODE 3: after its row-pair scratch)
+            const uint32_t st0 = MODE == 3 ? B0 + (uint32_t)(kTokOut * 64 * 4) : B0;
             float *stile = reinterpret_cast<float *>(smem_raw + (st0 - raw_addr));
             if (MODE != 3 || quarter < 2) {
                 __syncwarp();
