@@ -39,7 +39,8 @@
 namespace qmm {
 
 constexpr int kDeqWarps = 16;                     // two groups of 8, alternate k-steps
-constexpr int kMmaThreads = 64 + 32 * kDeqWarps;
+constexpr int kRawWarp = 2 + kDeqWarps;             // streams raw Q4_K tiles
+constexpr int kMmaThreads = 32 * (kRawWarp + 1);
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 
@@ -59,35 +60,35 @@ struct MmaParams {
 // 256-wide slice of k), then decoded from shared memory.
 constexpr int kRawBytes = kBM * 144;
 
-#ifndef QMM_KSUB_WIDE
-#define QMM_KSUB_WIDE 2
-#endif
-
 // Tensor memory (512 columns x 128 lanes of 32 bits, all taken by the one CTA
 // on the SM): the fp32 accumulator(s) first, then a ring of NA dequantized W
 // stages (A operand: row r on lane r, k pairs packed per column, 32 columns
 // per 64-wide k-step). Shared memory: a ring of NB x stages (streamed from
 // L2 by TMA) and, for Q4_K, kNR raw super-block tiles of 128 rows.
+//
+// A stage is KA = 4 k-steps (one 256-wide super-block): each dequant thread
+// then pays one raw-tile wait, one slot wait and one arrival per two decoded
+// chunks. An x stage is KB k-steps, 32 KB at most (the x tile of 256 tokens
+// is 32 KB per k-step).
 template <int BN, bool RAW>
 struct MmaCfg {
-    // a pipeline stage holds KSUB consecutive 64-wide k-steps: every barrier
-    // round trip, commit and TMA issue is paid once per stage
-    static constexpr int KSUB = BN >= 256 ? QMM_KSUB_WIDE : 2;
+    static constexpr int KA = 4;
+    static constexpr int KB = BN >= 256 ? 1 : (BN >= 128 ? 2 : 4);
     static constexpr int kBBytes = BN * kBK * 2;            // one k-step of x
-    static constexpr int kBStage = KSUB * kBBytes;
+    static constexpr int kBStage = KB * kBBytes;
     static constexpr int kAccCols = BN < 32 ? 32 : BN;      // one accumulator
     // two accumulators (even k-steps into one, odd into the other, summed at
     // the end) where TMEM has room: back-to-back MMAs then do not wait on
     // each other's result
     static constexpr int kNAcc = BN >= 256 ? 1 : 2;
     static constexpr int kACol0 = kNAcc * kAccCols;         // first A column
-    static constexpr int kAStageCols = KSUB * 32;
+    static constexpr int kAStageCols = KA * 32;
     static constexpr int kNAFit = (512 - kACol0) / kAStageCols;
-    static constexpr int NA = kNAFit > 6 ? 6 : kNAFit;
+    static constexpr int NA = kNAFit > 3 ? 3 : kNAFit;
     static constexpr int kCols = 512;
-    // raw W stages: as many as fit, up to 4, next to a minimum x ring; HBM
-    // latency is hidden by the raw ring, L2 latency by the x ring
-    static constexpr int kNBMin = (4 + KSUB - 1) / KSUB;
+    // raw W stages: as many as fit, up to 4, next to a minimum x ring of four
+    // k-steps; HBM latency is hidden by the raw ring, L2 latency by the x ring
+    static constexpr int kNBMin = (4 + KB - 1) / KB;
     static constexpr int kRawFit = (212 * 1024 - kNBMin * kBStage) / kRawBytes;
     static constexpr int kNR = RAW ? (kRawFit > 4 ? 4 : kRawFit) : 1;
     static_assert(!RAW || kNR >= 2, "raw W ring too shallow");
@@ -156,34 +157,59 @@ __device__ __forceinline__ void to_half_words<F_Q4_K>(const Raw32<F_Q4_K> &raw,
     }
 }
 
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t v) {
+    return *reinterpret_cast<const __half2 *>(&v);
+}
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) {
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
 // Half h of a Q4_K 64-weight chunk c: quant bytes 16h .. 16h+15 of the chunk (q),
 // i.e. weights 16h + 0..15 (low nibbles, sub-block 2c) and 32 + 16h + 0..15
 // (high nibbles, sub-block 2c+1) -> 16 fp16x2 words: 0..7 low, 8..15 high.
+//
+// All in fp16x2 arithmetic, two weights per instruction:
+//   a nibble pair becomes (1024 + q) exactly by OR-ing it into the fp16
+//   pattern of 1024 (a high nibble, kept in place, gives 1024 + 16 q);
+//   sc * q = (1024 + q) * sc - 1024 sc is exact in one fma (the result is an
+//   integer below 2048; 1024 sc and sc / 16 are exact in fp16);
+//   w = d * (sc q) - fp16(dmin m) is then rounded once.
+// Only dmin * m picks up an extra fp16 rounding against RN(ds q - dm); the
+// error stays at the level of rounding w itself.
 __device__ __forceinline__ void q4k_half_chunk_to_half(const uint4 &hdr, const uint4 &q, int c,
                                                        uint32_t (&hw)[16]) {
     uint32_t sc0, m0, sc1, m1;
     q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * c, sc0, m0);
     q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * c + 1, sc1, m1);
-    const float d = f16_bits_to_f32(hdr.x & 0xFFFFu);
-    const float dmin = f16_bits_to_f32(hdr.x >> 16);
-    const float ds0 = d * (float)sc0, ds1 = d * (float)sc1;
-    const float2 a0 = make_float2(256.0f * ds0, 256.0f * ds0);
-    const float2 a1 = make_float2(256.0f * ds1, 256.0f * ds1);
-    const float cc0 = -fmaf(128.0f, ds0, dmin * (float)m0);
-    const float cc1 = -fmaf(128.0f, ds1, dmin * (float)m1);
-    const float2 c0 = make_float2(cc0, cc0), c1 = make_float2(cc1, cc1);
+    // small integers v < 1024 as exact fp16 pairs: (1024 + v) - 1024
+    auto int_h2 = [](uint32_t v) {
+        return __hsub2(u32_as_h2((0x6400u | v) * 0x10001u), u32_as_h2(0x64006400u));
+    };
+    const __half2 d2 = u32_as_h2((hdr.x & 0xFFFFu) * 0x10001u);
+    const __half2 dmin2 = u32_as_h2((hdr.x >> 16) * 0x10001u);
+    const __half2 s0 = int_h2(sc0);
+    const __half2 n0 = __hmul2(s0, u32_as_h2(0xE400E400u));                   // * -1024
+    const __half2 sc1h = int_h2(sc1);
+    const __half2 s1 = __hmul2(sc1h, u32_as_h2(0x2C002C00u));                 // / 16
+    const __half2 n1 = __hmul2(sc1h, u32_as_h2(0xD400D400u));                 // * -64
+    // -fp16(dmin m): the exact product rounded once
+    const __half2 e0 = __hneg2(__hmul2(dmin2, int_h2(m0)));
+    const __half2 e1 = __hneg2(__hmul2(dmin2, int_h2(m1)));
     const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t lo = wd[i] & 0x0F0F0F0Fu, hi = (wd[i] >> 4) & 0x0F0F0F0Fu;
-        const float2 l01 = ffma2(a0, make_float2(byte_half_plus<0>(lo), byte_half_plus<1>(lo)), c0);
-        const float2 l23 = ffma2(a0, make_float2(byte_half_plus<2>(lo), byte_half_plus<3>(lo)), c0);
-        const float2 h01 = ffma2(a1, make_float2(byte_half_plus<0>(hi), byte_half_plus<1>(hi)), c1);
-        const float2 h23 = ffma2(a1, make_float2(byte_half_plus<2>(hi), byte_half_plus<3>(hi)), c1);
-        hw[2 * i] = pack_half2(l01.x, l01.y);
-        hw[2 * i + 1] = pack_half2(l23.x, l23.y);
-        hw[8 + 2 * i] = pack_half2(h01.x, h01.y);
-        hw[8 + 2 * i + 1] = pack_half2(h23.x, h23.y);
+        // bytes (0, 2, 1, 3): weights 4i, 4i+1 in the two 16-bit halves of t,
+        // 4i+2, 4i+3 in those of t >> 8
+        const uint32_t t = prmt(wd[i], 0u, 0x3120u);
+        const uint32_t u = t >> 8;
+        const __half2 l01 = u32_as_h2((t & 0x000F000Fu) | 0x64006400u);
+        const __half2 l23 = u32_as_h2((u & 0x000F000Fu) | 0x64006400u);
+        const __half2 h01 = u32_as_h2((t & 0x00F000F0u) | 0x64006400u);
+        const __half2 h23 = u32_as_h2((u & 0x00F000F0u) | 0x64006400u);
+        hw[2 * i] = h2_as_u32(__hfma2(__hfma2(l01, s0, n0), d2, e0));
+        hw[2 * i + 1] = h2_as_u32(__hfma2(__hfma2(l23, s0, n0), d2, e0));
+        hw[8 + 2 * i] = h2_as_u32(__hfma2(__hfma2(h01, s1, n1), d2, e1));
+        hw[8 + 2 * i + 1] = h2_as_u32(__hfma2(__hfma2(h23, s1, n1), d2, e1));
     }
 }
 
@@ -214,7 +240,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     constexpr int kTokOut = MODE == 1 ? BN : BN / 2;  // tokens per CTA
     constexpr bool kRaw = FMT == F_Q4_K && MODE != 3;  // raw W tiles by TMA
     using C = MmaCfg<BN, kRaw>;
-    constexpr int NA = C::NA, NB = C::NB, kNR = C::kNR, KSUB = C::KSUB;
+    constexpr int NA = C::NA, NB = C::NB, kNR = C::kNR, KA = C::KA, KB = C::KB;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
@@ -233,21 +259,19 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     uint8_t *gen = smem_raw + (bar0 - raw_addr);
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gen + slot_off);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gen + slot_off + 8);
-    // Two groups of 8 dequant warps take alternate k-steps. An A stage is done
-    // when every group with a k-step in it has arrived: one group when a stage
-    // is one k-step, both otherwise. The A ring must cover the groups' reach
-    // (NA * KSUB >= 2 k-steps) so that no group waits on a phase two ahead of
-    // the barrier.
+    // Two groups of 8 dequant warps take alternate k-steps; an A stage (KA = 4
+    // k-steps) is done when both groups have arrived.
     constexpr int kGroups = 2;
-    constexpr int kFullACount = KSUB == 1 ? kDeqWarps / kGroups : kDeqWarps;
-    static_assert(C::NA * C::KSUB >= kGroups, "A ring shallower than the producer groups' reach");
+    constexpr int kFullACount = kDeqWarps;
+    static_assert(KA % kGroups == 0, "every group needs a k-step in every A stage");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t crank = cluster_ctarank();  // 0 or 1 within the CTA pair
     const int64_t m0 = p.j0 + (int64_t)blockIdx.x * kRowsOut;
     const int n0 = blockIdx.y * kTokOut;
     const int KS = p.KS;                    // 64-wide k-steps
-    const int NSTG = (KS + KSUB - 1) / KSUB;  // pipeline stages
+    const int NSA = (KS + KA - 1) / KA;      // A stages (the last one may be padded)
+    const int NSB = (KS + KB - 1) / KB;      // x stages
     // Every tile walks k in its own rotated order (whole super-blocks), so
     // that the CTAs do not all fetch the same x tile from the same L2 lines
     // at the same moment. The sum is the same up to rounding order.
@@ -288,28 +312,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         if (lane == 0) {
             prefetch_tmap(&tmx);
             if (MODE != 1) prefetch_tmap(&tmx_lo);
-            if (kRaw) prefetch_tmap(&tmw);
-            int issued = 0, raw_issued = 0;
-            for (int st = 0; st < NSTG; ++st) {
-                bool ok = true;
-                for (int sub = 0; sub < KSUB; ++sub) {
-                    const int ks = st * KSUB + sub;
-                    if (kRaw && ks < KS && (ks & 3) == 0) {
-                        const int b = ks >> 2, rs = b % kNR;
-                        if (b >= kNR &&
-                            !wait_abortable(rawEmpty(rs), ((b / kNR) + 1) & 1, abort_flag)) {
-                            record_error(p.err, DERR_MMA_EMPTY);
-                            *abort_flag = 1;
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(rawFull(rs), kRawBytes);
-                        tma_load_2d(W0 + rs * kRawBytes, &tmw, 144 * (kx(ks) >> 2), (int)m0,
-                                    rawFull(rs));
-                        ++raw_issued;
-                    }
-                }
-                if (!ok) break;
+            int issued = 0;
+            for (int st = 0; st < NSB; ++st) {
                 const int slot = st % NB;
                 if (st >= NB && !wait_abortable(emptyB(slot), ((st / NB) + 1) & 1, abort_flag)) {
                     record_error(p.err, DERR_MMA_EMPTY);
@@ -318,8 +322,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 }
                 // the whole stage lands here: this CTA's halves and the peer's halves
                 mbar_arrive_expect_tx(fullB(slot), C::kBStage);
-                for (int sub = 0; sub < KSUB; ++sub) {
-                    const int ks = st * KSUB + sub;  // past KS: zero-filled by the map
+                for (int sub = 0; sub < KB; ++sub) {
+                    const int ks = st * KB + sub;  // past KS: zero-filled by the map
                     // MODE 1: this CTA fetches token rows [n0 + crank BN/2, +BN/2);
                     // MODE 2/3: CTA 0 the hi rows, CTA 1 the lo rows of the tile's tokens
                     const uint32_t dst =
@@ -336,8 +340,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             }
             for (int s = std::max(0, issued - NB); s < issued; ++s)
                 if (!mbar_wait(fullB(s % NB), (s / NB) & 1)) record_error(p.err, DERR_TEARDOWN);
-            for (int s = std::max(0, raw_issued - kNR); s < raw_issued; ++s)
-                if (!mbar_wait(rawFull(s % kNR), (s / kNR) & 1)) record_error(p.err, DERR_TEARDOWN);
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issue ------------------------------
@@ -345,42 +347,67 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         // warp-uniform); one elected lane issues the MMAs and their commits.
         constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
         const bool leader = elect_one();
-        for (int st = 0; st < NSTG; ++st) {
-            const int sa = st % NA, sb = st % NB;
-            bool ok = wait_abortable(fullA(sa), (st / NA) & 1, abort_flag);
-            if (__all_sync(0xFFFFFFFFu, ok) == 0) {
-                if (leader) { record_error(p.err, DERR_MMA_A); *abort_flag = 1; }
-                break;
+        for (int ks = 0; ks < KS; ++ks) {
+            const int st = ks / KA, sa = st % NA;
+            const int bt = ks / KB, sb = bt % NB;
+            if (ks % KA == 0) {
+                const bool ok = wait_abortable(fullA(sa), (st / NA) & 1, abort_flag);
+                if (__all_sync(0xFFFFFFFFu, ok) == 0) {
+                    if (leader) { record_error(p.err, DERR_MMA_A); *abort_flag = 1; }
+                    break;
+                }
             }
-            ok = wait_abortable(fullB(sb), (st / NB) & 1, abort_flag);
-            if (__all_sync(0xFFFFFFFFu, ok) == 0) {
-                if (leader) { record_error(p.err, DERR_MMA_B); *abort_flag = 1; }
-                break;
+            if (ks % KB == 0) {
+                const bool ok = wait_abortable(fullB(sb), (bt / NB) & 1, abort_flag);
+                if (__all_sync(0xFFFFFFFFu, ok) == 0) {
+                    if (leader) { record_error(p.err, DERR_MMA_B); *abort_flag = 1; }
+                    break;
+                }
             }
             tc_fence_after();
             if (leader) {
+                const uint32_t at =
+                    tmem + (uint32_t)(C::kACol0 + sa * C::kAStageCols + (ks % KA) * 32);
+                const uint64_t bd = sdesc_sw128(B0 + sb * C::kBStage + (ks % KB) * C::kBBytes);
+                const uint32_t dacc =
+                    tmem + (uint32_t)((C::kNAcc == 2 ? (ks & 1) : 0) * C::kAccCols);
+                const bool acc0 = C::kNAcc == 2 ? ks > 1 : ks > 0;
 #pragma unroll
-                for (int sub = 0; sub < KSUB; ++sub) {
-                    const int ks = st * KSUB + sub;
-                    if (ks < KS) {
-                        const uint32_t at = tmem + (uint32_t)(C::kACol0 + sa * C::kAStageCols +
-                                                              sub * 32);
-                        const uint64_t bd = sdesc_sw128(B0 + sb * C::kBStage + sub * C::kBBytes);
-                        const uint32_t dacc =
-                            tmem + (uint32_t)((C::kNAcc == 2 ? (ks & 1) : 0) * C::kAccCols);
-                        const bool acc0 = C::kNAcc == 2 ? ks > 1 : ks > 0;
-#pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16: 8 A columns, 32 B bytes
-                            tc_mma_f16_ts(dacc, at + 8 * kk, bd + 2 * kk, idesc, acc0 || kk != 0);
-                    }
-                }
-                tc_commit(emptyA(sa));
-                tc_commit_multicast(emptyB(sb), (uint16_t)3);  // both CTAs may refill
+                for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16: 8 A columns, 32 B bytes
+                    tc_mma_f16_ts(dacc, at + 8 * kk, bd + 2 * kk, idesc, acc0 || kk != 0);
+                const bool last = ks == KS - 1;
+                if (ks % KB == KB - 1 || last)
+                    tc_commit_multicast(emptyB(sb), (uint16_t)3);  // both CTAs may refill
+                if (ks % KA == KA - 1 || last) tc_commit(emptyA(sa));
             }
             __syncwarp();
         }
         if (leader) tc_commit(accb);  // fires when every MMA issued above has completed
         __syncwarp();
+    } else if (warp == kRawWarp) {
+        // ------------------------------ raw Q4_K tiles via TMA ------------------------------
+        // its own warp, so that the raw ring runs as far ahead of the dequant
+        // warps as it is deep, whatever the x ring is doing
+        if (kRaw && lane == 0) {
+            prefetch_tmap(&tmw);
+            const int NSBLK = KS / 4;
+            int raw_issued = 0;
+            for (int b = 0; b < NSBLK; ++b) {
+                const int rs = b % kNR;
+                if (b >= kNR && !wait_abortable(rawEmpty(rs), ((b / kNR) + 1) & 1, abort_flag)) {
+                    record_error(p.err, DERR_MMA_EMPTY);
+                    *abort_flag = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(rawFull(rs), kRawBytes);
+                tma_load_2d(W0 + rs * kRawBytes, &tmw, 144 * (kx(4 * b) >> 2), (int)m0,
+                            rawFull(rs));
+                ++raw_issued;
+            }
+            // no copy may land after this CTA exits
+            for (int s = std::max(0, raw_issued - kNR); s < raw_issued; ++s)
+                if (!mbar_wait(rawFull(s % kNR), (s / kNR) & 1)) record_error(p.err, DERR_TEARDOWN);
+        }
     } else {
         // ------------------------------ W dequant producers ------------------------------
         // Warp w (2..17) owns TMEM lanes 32 (w % 4) .. +31, i.e. rows r of the
@@ -396,7 +423,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         // k-step ks of the group: wait for its A slot (when first in the stage)
         // and return the TMEM address of its 32 columns
         auto a_slot = [&](int ks, bool &failed) {
-            const int st = ks / KSUB, sub = ks % KSUB;
+            const int st = ks / KA, sub = ks % KA;
             const int slot = st % NA;
             if (sub < kGroups && st >= NA) {
                 const bool ok = wait_abortable(emptyA(slot), ((st / NA) + 1) & 1, abort_flag);
@@ -410,8 +437,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             return tlane + (uint32_t)(C::kACol0 + slot * C::kAStageCols + sub * 32);
         };
         auto a_done = [&](int ks, bool failed) {
-            const int st = ks / KSUB, sub = ks % KSUB;
-            if (sub + kGroups >= KSUB) {
+            const int st = ks / KA, sub = ks % KA;
+            if (sub + kGroups >= KA) {
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -419,15 +446,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             }
         };
         if constexpr (kRaw) {
-            // thread (r, h) decodes half h of row r's 64-weight chunk from the raw tile
+            // per super-block b (one A stage): thread (r, h) of group g decodes
+            // half h of row r's 64-weight chunks c = g and g + 2
             const bool row_ok = m0 + r < p.j1;
-            const int NI = (KS - g + 1) / 2;  // KS % 4 == 0: every stage is full
+            const int NSBLK = KS / 4;  // k % 256 == 0
             bool failed = false;
-            for (int i = 0; i < NI; ++i) {
-                const int ks = g + 2 * i;
-                const int b = ks >> 2, c = ks & 3;
+            for (int b = 0; b < NSBLK; ++b) {
                 const int rs = b % kNR;
-                uint32_t hw[16];
+                uint32_t hw0[16], hw1[16];
                 if (!failed) {
                     const bool ok = wait_abortable(rawFull(rs), (b / kNR) & 1, abort_flag);
                     if (__all_sync(0xFFFFFFFFu, ok) == 0) {
@@ -439,20 +465,24 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 if (!failed && row_ok) {
                     const uint32_t rb = W0 + rs * kRawBytes + (uint32_t)r * 144u;
                     const uint4 hdr = lds128(rb);
-                    const uint4 qv = lds128(rb + 16u + 32u * c + 16u * h);
-                    q4k_half_chunk_to_half(hdr, qv, c, hw);
+                    const uint4 q0 = lds128(rb + 16u + 32u * g + 16u * h);
+                    const uint4 q1 = lds128(rb + 16u + 32u * (g + 2) + 16u * h);
+                    q4k_half_chunk_to_half(hdr, q0, g, hw0);
+                    q4k_half_chunk_to_half(hdr, q1, g + 2, hw1);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) hw[e] = 0u;
+                    for (int e = 0; e < 16; ++e) hw0[e] = hw1[e] = 0u;
                 }
                 __syncwarp();
-                // the last k-step of the super-block this group takes releases it
-                if (lane == 0 && !failed && c >= 2) mbar_arrive(rawEmpty(rs));
-                const uint32_t ta = a_slot(ks, failed);
+                if (lane == 0 && !failed) mbar_arrive(rawEmpty(rs));  // raw tile read
                 // weights 16h + 0..15 -> columns 8h..8h+7; 32 + 16h + 0..15 -> 16 + 8h..
-                tmem_st8(ta + 8u * h, hw);
-                tmem_st8(ta + 16u + 8u * h, hw + 8);
-                a_done(ks, failed);
+                const uint32_t ta0 = a_slot(4 * b + g, failed);
+                tmem_st8(ta0 + 8u * h, hw0);
+                tmem_st8(ta0 + 16u + 8u * h, hw0 + 8);
+                const uint32_t ta1 = a_slot(4 * b + g + 2, failed);
+                tmem_st8(ta1 + 8u * h, hw1);
+                tmem_st8(ta1 + 16u + 8u * h, hw1 + 8);
+                a_done(4 * b + g + 2, failed);
             }
         } else {
         const bool lo_part = MODE == 3 && r >= 64;   // MODE 3: rows 64..127 hold W_lo
@@ -470,7 +500,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         // k-steps of this group, over the stage-padded range: a k-step past k
         // stores zeros (the MMA skips it) but still takes part in its stage's
         // arrival count
-        const int NI = (NSTG * KSUB - g + 1) / 2;
+        const int NI = (NSA * KA - g + 1) / 2;
 #pragma unroll
         for (int q = 0; q < PD; ++q) {
             const int64_t k0 = k0_of(q);
