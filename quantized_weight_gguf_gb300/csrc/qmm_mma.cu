@@ -52,7 +52,8 @@ struct MmaParams {
     int64_t j0, j1;
     int KS;
     int accumulate;
-    int tma_store;   // y tile written by one TMA store / reduce-add (alignment permits)
+    int pairs;       // pairs of 128-row tiles (a cluster of two CTAs takes one pair)
+    int tiles_n;     // token tiles
     unsigned int *err;
 };
 
@@ -96,7 +97,7 @@ struct MmaCfg {
     static constexpr int NB = (kAvail / kBStage) > 8 ? 8 : (kAvail / kBStage);
     static constexpr size_t kSmemUsed = (size_t)NB * kBStage +
                                         (RAW ? (size_t)kNR * kRawBytes : 0) + 1024 /*align*/ +
-                                        512 /*barriers*/;
+                                        512 /*barriers*/ + 2048 /*token scales*/;
     // at least half of the SM's shared memory, so that no second CTA can be
     // resident and block in its TMEM allocation (every CTA takes all 512
     // columns) while holding resources its cluster peer waits for
@@ -234,8 +235,7 @@ __device__ __forceinline__ void split_half_words(const float (&v)[32], bool lo, 
 template <int FMT, int BN, int MODE>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     mma_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmx_lo,
-               const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmy,
-               const MmaParams p) {
+               const __grid_constant__ CUtensorMap tmw, const MmaParams p) {
     constexpr int kRowsOut = MODE == 3 ? 64 : kBM;   // output rows per CTA
     constexpr int kTokOut = MODE == 1 ? BN : BN / 2;  // tokens per CTA
     constexpr bool kRaw = FMT == F_Q4_K && MODE != 3;  // raw W tiles by TMA
@@ -251,14 +251,20 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     auto emptyA = [&](int s) { return bar0 + 8u * (NA + s); };
     auto fullB = [&](int s) { return bar0 + 8u * (2 * NA + s); };
     auto emptyB = [&](int s) { return bar0 + 8u * (2 * NA + NB + s); };
-    const uint32_t accb = bar0 + 8u * (2 * NA + 2 * NB);
-    auto rawFull = [&](int s) { return accb + 8u * (1 + s); };
-    auto rawEmpty = [&](int s) { return accb + 8u * (1 + kNR + s); };
-    const uint32_t slot_off = 8u * (2 * NA + 2 * NB + 1 + 2 * kNR);
+    auto rawFull = [&](int s) { return bar0 + 8u * (2 * NA + 2 * NB + s); };
+    auto rawEmpty = [&](int s) { return bar0 + 8u * (2 * NA + 2 * NB + kNR + s); };
+    const uint32_t accFull = bar0 + 8u * (2 * NA + 2 * NB + 2 * kNR);
+    const uint32_t accEmpty = accFull + 8u;
+    auto xsFull = [&](int b) { return accFull + 8u * (2 + b); };
+    auto xsFree = [&](int b) { return accFull + 8u * (4 + b); };
+    const uint32_t scrReady = accFull + 8u * 6;  // MODE 3: lo rows parked in scratch
+    const uint32_t slot_off = 8u * (2 * NA + 2 * NB + 2 * kNR + 7);
     const uint32_t slot_addr = bar0 + slot_off;
     uint8_t *gen = smem_raw + (bar0 - raw_addr);
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gen + slot_off);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gen + slot_off + 8);
+    // token scales of the tile in flight, double-buffered: [2][kTokOut]
+    float *xs_s = reinterpret_cast<float *>(gen + 512);
     // Two groups of 8 dequant warps take alternate k-steps; an A stage (KA = 4
     // k-steps) is done when both groups have arrived.
     constexpr int kGroups = 2;
@@ -267,16 +273,28 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t crank = cluster_ctarank();  // 0 or 1 within the CTA pair
-    const int64_t m0 = p.j0 + (int64_t)blockIdx.x * kRowsOut;
-    const int n0 = blockIdx.y * kTokOut;
-    const int KS = p.KS;                    // 64-wide k-steps
-    const int NSA = (KS + KA - 1) / KA;      // A stages (the last one may be padded)
-    const int NSB = (KS + KB - 1) / KB;      // x stages
-    // Every tile walks k in its own rotated order (whole super-blocks), so
-    // that the CTAs do not all fetch the same x tile from the same L2 lines
-    // at the same moment. The sum is the same up to rounding order.
-    const int rot = (KS % 4 == 0) ? 4 * (int)((blockIdx.x >> 1) % (unsigned)(KS / 4)) : 0;
-    auto kx = [&](int ks) { return rot ? (ks + rot) % KS : ks; };
+    const int KS = p.KS;                     // 64-wide k-steps
+    const int NSA = (KS + KA - 1) / KA;      // A stages per tile (the last may be padded)
+    const int NSB = (KS + KB - 1) / KB;      // x stages per tile
+    // Tiles: the pair of CTAs takes 128-row tiles 2q and 2q + 1 of token tile
+    // nt together; pair-tile u = q * tiles_n + nt, and cluster c of C takes
+    // u = c, c + C, ... (the two token tiles of one W row pair run side by
+    // side on neighbouring clusters, so W is read from HBM about once).
+    const int n_units = p.pairs * p.tiles_n;
+    const int c0 = (int)(blockIdx.x >> 1), cstep = (int)(gridDim.x >> 1);
+    struct Tile { int64_t m0; int n0; int rot; };
+    auto tile_of = [&](int u) {
+        const int q = u / p.tiles_n, nt = u - q * p.tiles_n;
+        Tile t;
+        t.m0 = p.j0 + (int64_t)(2 * q + (int)crank) * kRowsOut;
+        t.n0 = nt * kTokOut;
+        // each pair walks k in its own rotated order (whole super-blocks) so
+        // that the CTAs do not all fetch the same x tile at the same moment;
+        // the sum is the same up to rounding order
+        t.rot = (KS % 4 == 0) ? 4 * (q % (KS / 4)) : 0;
+        return t;
+    };
+    auto kx = [&](const Tile &t, int ks) { return t.rot ? (ks + t.rot) % KS : ks; };
 
     if (tid == 0) {
         for (int s = 0; s < NA; ++s) {
@@ -287,13 +305,17 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             mbar_init(fullB(s), 1);
             mbar_init(emptyB(s), 2);  // both CTAs of the pair have consumed the stage
         }
-        mbar_init(accb, 1);
-        if (kRaw) {
-            for (int s = 0; s < kNR; ++s) {
-                mbar_init(rawFull(s), 1);
-                mbar_init(rawEmpty(s), kDeqWarps);
-            }
+        for (int s = 0; s < kNR; ++s) {
+            mbar_init(rawFull(s), 1);
+            mbar_init(rawEmpty(s), kDeqWarps);
         }
+        mbar_init(accFull, 1);
+        mbar_init(accEmpty, kDeqWarps);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(xsFull(b), 1);
+            mbar_init(xsFree(b), kDeqWarps);
+        }
+        mbar_init(scrReady, kDeqWarps / 2);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -308,104 +330,157 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------ X tiles via TMA ------------------------------
+        // ------------------ token scales + x tiles via TMA ------------------
+        // x16 and the scales come from the conversion kernel just before this
+        // one, which lets this grid start early: only this warp waits for it
+        pdl_wait_prev();
         if (lane == 0) {
             prefetch_tmap(&tmx);
             if (MODE != 1) prefetch_tmap(&tmx_lo);
-            int issued = 0;
-            for (int st = 0; st < NSB; ++st) {
-                const int slot = st % NB;
-                if (st >= NB && !wait_abortable(emptyB(slot), ((st / NB) + 1) & 1, abort_flag)) {
-                    record_error(p.err, DERR_MMA_EMPTY);
-                    *abort_flag = 1;
+        }
+        int bcount = 0;  // x stages issued so far (all tiles)
+        int it = 0;
+        for (int u = c0; u < n_units; u += cstep, ++it) {
+            if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
+            const Tile t = tile_of(u);
+            // the tile's token scales (2^e of each token's fp16 conversion) for
+            // its epilogue, into buffer it & 1 once the tile two back is done
+            const int xb = it & 1;
+            if (it >= 2) {
+                const bool ok = wait_abortable(xsFree(xb), ((it >> 1) + 1) & 1, abort_flag);
+                if (__all_sync(0xFFFFFFFFu, ok) == 0) {
+                    if (lane == 0) { record_error(p.err, DERR_MMA_EMPTY); *abort_flag = 1; }
                     break;
                 }
-                // the whole stage lands here: this CTA's halves and the peer's halves
-                mbar_arrive_expect_tx(fullB(slot), C::kBStage);
-                for (int sub = 0; sub < KB; ++sub) {
-                    const int ks = st * KB + sub;  // past KS: zero-filled by the map
-                    // MODE 1: this CTA fetches token rows [n0 + crank BN/2, +BN/2);
-                    // MODE 2/3: CTA 0 the hi rows, CTA 1 the lo rows of the tile's tokens
-                    const uint32_t dst =
-                        B0 + slot * C::kBStage + sub * C::kBBytes + crank * (BN / 2) * 128;
-                    if (MODE == 1)
-                        tma_load_2d_multicast(dst, &tmx, kx(ks) * kBK, n0 + (int)crank * (BN / 2),
-                                              fullB(slot), (uint16_t)3);
-                    else
-                        tma_load_2d_multicast(dst,
-                                              crank ? (const void *)&tmx_lo : (const void *)&tmx,
-                                              kx(ks) * kBK, n0, fullB(slot), (uint16_t)3);
-                }
-                ++issued;
             }
-            for (int s = std::max(0, issued - NB); s < issued; ++s)
-                if (!mbar_wait(fullB(s % NB), (s / NB) & 1)) record_error(p.err, DERR_TEARDOWN);
+            for (int i = lane; i < kTokOut; i += 32)
+                xs_s[xb * kTokOut + i] = t.n0 + i < p.n_tokens ? __ldg(p.xscale + t.n0 + i) : 0.0f;
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(xsFull(xb));
+                for (int st = 0; st < NSB; ++st, ++bcount) {
+                    const int slot = bcount % NB;
+                    if (bcount >= NB &&
+                        !wait_abortable(emptyB(slot), ((bcount / NB) + 1) & 1, abort_flag)) {
+                        record_error(p.err, DERR_MMA_EMPTY);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    // the whole stage lands here: this CTA's halves and the peer's halves
+                    mbar_arrive_expect_tx(fullB(slot), C::kBStage);
+                    for (int sub = 0; sub < KB; ++sub) {
+                        const int ks = st * KB + sub;  // past KS: zero-filled by the map
+                        const int kc = ks < KS ? kx(t, ks) : ks;
+                        // MODE 1: this CTA fetches token rows [n0 + crank BN/2, +BN/2);
+                        // MODE 2/3: CTA 0 the hi rows, CTA 1 the lo rows of the tile's tokens
+                        const uint32_t dst =
+                            B0 + slot * C::kBStage + sub * C::kBBytes + crank * (BN / 2) * 128;
+                        if (MODE == 1)
+                            tma_load_2d_multicast(dst, &tmx, kc * kBK,
+                                                  t.n0 + (int)crank * (BN / 2), fullB(slot),
+                                                  (uint16_t)3);
+                        else
+                            tma_load_2d_multicast(
+                                dst, crank ? (const void *)&tmx_lo : (const void *)&tmx, kc * kBK,
+                                t.n0, fullB(slot), (uint16_t)3);
+                    }
+                }
+            }
+            __syncwarp();
         }
+        // no copy may land after this CTA exits
+        if (lane == 0)
+            for (int s = std::max(0, bcount - NB); s < bcount; ++s)
+                if (!mbar_wait(fullB(s % NB), (s / NB) & 1)) record_error(p.err, DERR_TEARDOWN);
     } else if (warp == 1) {
         // ------------------------------ MMA issue ------------------------------
         // The whole warp runs the loop (so that descriptors and addresses stay
         // warp-uniform); one elected lane issues the MMAs and their commits.
         constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
         const bool leader = elect_one();
-        for (int ks = 0; ks < KS; ++ks) {
-            const int st = ks / KA, sa = st % NA;
-            const int bt = ks / KB, sb = bt % NB;
-            if (ks % KA == 0) {
-                const bool ok = wait_abortable(fullA(sa), (st / NA) & 1, abort_flag);
+        int abase = 0, bbase = 0;  // A / x stages consumed by earlier tiles
+        int it = 0;
+        bool failed = false;
+        for (int u = c0; u < n_units && !failed; u += cstep, ++it) {
+            if (it > 0) {  // the epilogue has drained the accumulator
+                const bool ok = wait_abortable(accEmpty, (it - 1) & 1, abort_flag);
                 if (__all_sync(0xFFFFFFFFu, ok) == 0) {
-                    if (leader) { record_error(p.err, DERR_MMA_A); *abort_flag = 1; }
+                    if (leader) { record_error(p.err, DERR_MMA_ACC); *abort_flag = 1; }
                     break;
                 }
+                tc_fence_after();
             }
-            if (ks % KB == 0) {
-                const bool ok = wait_abortable(fullB(sb), (bt / NB) & 1, abort_flag);
-                if (__all_sync(0xFFFFFFFFu, ok) == 0) {
-                    if (leader) { record_error(p.err, DERR_MMA_B); *abort_flag = 1; }
-                    break;
+            for (int ks = 0; ks < KS; ++ks) {
+                const int st = abase + ks / KA, sa = st % NA;
+                const int bt = bbase + ks / KB, sb = bt % NB;
+                if (ks % KA == 0) {
+                    const bool ok = wait_abortable(fullA(sa), (st / NA) & 1, abort_flag);
+                    if (__all_sync(0xFFFFFFFFu, ok) == 0) {
+                        if (leader) { record_error(p.err, DERR_MMA_A); *abort_flag = 1; }
+                        failed = true;
+                        break;
+                    }
                 }
-            }
-            tc_fence_after();
-            if (leader) {
-                const uint32_t at =
-                    tmem + (uint32_t)(C::kACol0 + sa * C::kAStageCols + (ks % KA) * 32);
-                const uint64_t bd = sdesc_sw128(B0 + sb * C::kBStage + (ks % KB) * C::kBBytes);
-                const uint32_t dacc =
-                    tmem + (uint32_t)((C::kNAcc == 2 ? (ks & 1) : 0) * C::kAccCols);
-                const bool acc0 = C::kNAcc == 2 ? ks > 1 : ks > 0;
+                if (ks % KB == 0) {
+                    const bool ok = wait_abortable(fullB(sb), (bt / NB) & 1, abort_flag);
+                    if (__all_sync(0xFFFFFFFFu, ok) == 0) {
+                        if (leader) { record_error(p.err, DERR_MMA_B); *abort_flag = 1; }
+                        failed = true;
+                        break;
+                    }
+                }
+                tc_fence_after();
+                if (leader) {
+                    const uint32_t at =
+                        tmem + (uint32_t)(C::kACol0 + sa * C::kAStageCols + (ks % KA) * 32);
+                    const uint64_t bd =
+                        sdesc_sw128(B0 + sb * C::kBStage + (ks % KB) * C::kBBytes);
+                    const uint32_t dacc =
+                        tmem + (uint32_t)((C::kNAcc == 2 ? (ks & 1) : 0) * C::kAccCols);
+                    const bool acc0 = C::kNAcc == 2 ? ks > 1 : ks > 0;
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16: 8 A columns, 32 B bytes
-                    tc_mma_f16_ts(dacc, at + 8 * kk, bd + 2 * kk, idesc, acc0 || kk != 0);
-                const bool last = ks == KS - 1;
-                if (ks % KB == KB - 1 || last)
-                    tc_commit_multicast(emptyB(sb), (uint16_t)3);  // both CTAs may refill
-                if (ks % KA == KA - 1 || last) tc_commit(emptyA(sa));
+                    for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16: 8 A columns, 32 B bytes
+                        tc_mma_f16_ts(dacc, at + 8 * kk, bd + 2 * kk, idesc, acc0 || kk != 0);
+                    const bool last = ks == KS - 1;
+                    if (ks % KB == KB - 1 || last)
+                        tc_commit_multicast(emptyB(sb), (uint16_t)3);  // both CTAs may refill
+                    if (ks % KA == KA - 1 || last) tc_commit(emptyA(sa));
+                    if (last) tc_commit(accFull);  // the tile's product is complete
+                }
+                __syncwarp();
             }
-            __syncwarp();
+            abase += NSA;
+            bbase += NSB;
         }
-        if (leader) tc_commit(accb);  // fires when every MMA issued above has completed
-        __syncwarp();
     } else if (warp == kRawWarp) {
         // ------------------------------ raw Q4_K tiles via TMA ------------------------------
         // its own warp, so that the raw ring runs as far ahead of the dequant
-        // warps as it is deep, whatever the x ring is doing
+        // warps as it is deep (into the next tile), whatever the x ring does
         if (kRaw && lane == 0) {
             prefetch_tmap(&tmw);
-            const int NSBLK = KS / 4;
-            int raw_issued = 0;
-            for (int b = 0; b < NSBLK; ++b) {
-                const int rs = b % kNR;
-                if (b >= kNR && !wait_abortable(rawEmpty(rs), ((b / kNR) + 1) & 1, abort_flag)) {
-                    record_error(p.err, DERR_MMA_EMPTY);
-                    *abort_flag = 1;
-                    break;
+            const int NSBLK = KS / 4;  // k % 256 == 0
+            int rcount = 0;
+            for (int u = c0; u < n_units; u += cstep) {
+                if (*abort_flag) break;
+                const Tile t = tile_of(u);
+                bool ok = true;
+                for (int b = 0; b < NSBLK; ++b, ++rcount) {
+                    const int rs = rcount % kNR;
+                    if (rcount >= kNR &&
+                        !wait_abortable(rawEmpty(rs), ((rcount / kNR) + 1) & 1, abort_flag)) {
+                        record_error(p.err, DERR_MMA_EMPTY);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(rawFull(rs), kRawBytes);
+                    tma_load_2d(W0 + rs * kRawBytes, &tmw, 144 * (kx(t, 4 * b) >> 2),
+                                (int)t.m0, rawFull(rs));
                 }
-                mbar_arrive_expect_tx(rawFull(rs), kRawBytes);
-                tma_load_2d(W0 + rs * kRawBytes, &tmw, 144 * (kx(4 * b) >> 2), (int)m0,
-                            rawFull(rs));
-                ++raw_issued;
+                if (!ok) break;
             }
             // no copy may land after this CTA exits
-            for (int s = std::max(0, raw_issued - kNR); s < raw_issued; ++s)
+            for (int s = std::max(0, rcount - kNR); s < rcount; ++s)
                 if (!mbar_wait(rawFull(s % kNR), (s / kNR) & 1)) record_error(p.err, DERR_TEARDOWN);
         }
     } else {
@@ -420,10 +495,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         const int h = dq & 1;
         const int g = dq >> 1;
         const uint32_t tlane = tmem + ((uint32_t)(32 * quarter) << 16);
-        // k-step ks of the group: wait for its A slot (when first in the stage)
+        bool failed = false;
+        int abase = 0;   // A stages of earlier tiles
+        int rcount = 0;  // raw super-blocks consumed (all tiles)
+        // k-step ks of the tile: wait for its A slot (when first in the stage)
         // and return the TMEM address of its 32 columns
-        auto a_slot = [&](int ks, bool &failed) {
-            const int st = ks / KA, sub = ks % KA;
+        auto a_slot = [&](int ks) {
+            const int st = abase + ks / KA, sub = ks % KA;
             const int slot = st % NA;
             if (sub < kGroups && st >= NA) {
                 const bool ok = wait_abortable(emptyA(slot), ((st / NA) + 1) & 1, abort_flag);
@@ -436,8 +514,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             }
             return tlane + (uint32_t)(C::kACol0 + slot * C::kAStageCols + sub * 32);
         };
-        auto a_done = [&](int ks, bool failed) {
-            const int st = ks / KA, sub = ks % KA;
+        auto a_done = [&](int ks) {
+            const int st = abase + ks / KA, sub = ks % KA;
             if (sub + kGroups >= KA) {
                 tmem_st_wait();
                 tc_fence_before();
@@ -445,212 +523,205 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 if (lane == 0 && !failed) mbar_arrive(fullA(st % NA));
             }
         };
-        if constexpr (kRaw) {
-            // per super-block b (one A stage): thread (r, h) of group g decodes
-            // half h of row r's 64-weight chunks c = g and g + 2
-            const bool row_ok = m0 + r < p.j1;
-            const int NSBLK = KS / 4;  // k % 256 == 0
-            bool failed = false;
-            for (int b = 0; b < NSBLK; ++b) {
-                const int rs = b % kNR;
-                uint32_t hw0[16], hw1[16];
-                if (!failed) {
-                    const bool ok = wait_abortable(rawFull(rs), (b / kNR) & 1, abort_flag);
+        int it = 0;
+        for (int u = c0; u < n_units && !failed; u += cstep, ++it) {
+            const Tile t = tile_of(u);
+            if constexpr (kRaw) {
+                // per super-block b (one A stage): thread (r, h) of group g decodes
+                // half h of row r's 64-weight chunks c = g and g + 2
+                const bool row_ok = t.m0 + r < p.j1;
+                const int NSBLK = KS / 4;  // k % 256 == 0
+                for (int b = 0; b < NSBLK && !failed; ++b, ++rcount) {
+                    const int rs = rcount % kNR;
+                    uint32_t hw0[16], hw1[16];
+                    const bool ok = wait_abortable(rawFull(rs), (rcount / kNR) & 1, abort_flag);
                     if (__all_sync(0xFFFFFFFFu, ok) == 0) {
                         record_error(p.err, DERR_MMA_A);
                         failed = true;
                         *abort_flag = 1;
+                        break;
                     }
-                }
-                if (!failed && row_ok) {
-                    const uint32_t rb = W0 + rs * kRawBytes + (uint32_t)r * 144u;
-                    const uint4 hdr = lds128(rb);
-                    const uint4 q0 = lds128(rb + 16u + 32u * g + 16u * h);
-                    const uint4 q1 = lds128(rb + 16u + 32u * (g + 2) + 16u * h);
-                    q4k_half_chunk_to_half(hdr, q0, g, hw0);
-                    q4k_half_chunk_to_half(hdr, q1, g + 2, hw1);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) hw0[e] = hw1[e] = 0u;
-                }
-                __syncwarp();
-                if (lane == 0 && !failed) mbar_arrive(rawEmpty(rs));  // raw tile read
-                // weights 16h + 0..15 -> columns 8h..8h+7; 32 + 16h + 0..15 -> 16 + 8h..
-                const uint32_t ta0 = a_slot(4 * b + g, failed);
-                tmem_st8(ta0 + 8u * h, hw0);
-                tmem_st8(ta0 + 16u + 8u * h, hw0 + 8);
-                const uint32_t ta1 = a_slot(4 * b + g + 2, failed);
-                tmem_st8(ta1 + 8u * h, hw1);
-                tmem_st8(ta1 + 16u + 8u * h, hw1 + 8);
-                a_done(4 * b + g + 2, failed);
-            }
-        } else {
-        const bool lo_part = MODE == 3 && r >= 64;   // MODE 3: rows 64..127 hold W_lo
-        const int64_t j = m0 + (MODE == 3 ? (r & 63) : r);
-        const bool row_ok = j < p.j1;
-        const uint8_t *rowp = p.w + (row_ok ? j : 0) * p.row_bytes;
-        constexpr int PD = Prefetch<FMT>::value;
-        Raw32<FMT> ring[PD];
-        // this thread's i-th k-step is g + 2 i
-        auto k0_of = [&](int i) { return (int64_t)kx(g + 2 * i) * kBK + 32 * h; };
-        auto nvalid_of = [&](int64_t k0) {
-            const int64_t v = p.k - k0;
-            return (int)(v < 0 ? 0 : (v > 32 ? 32 : v));
-        };
-        // k-steps of this group, over the stage-padded range: a k-step past k
-        // stores zeros (the MMA skips it) but still takes part in its stage's
-        // arrival count
-        const int NI = (NSA * KA - g + 1) / 2;
-#pragma unroll
-        for (int q = 0; q < PD; ++q) {
-            const int64_t k0 = k0_of(q);
-            const int nv = nvalid_of(k0);
-            if (q < NI && row_ok && nv > 0) ring[q].load(rowp, k0, nv);
-        }
-        bool failed = false;
-        for (int i0 = 0; i0 < NI; i0 += PD) {
-#pragma unroll
-            for (int q = 0; q < PD; ++q) {
-                const int i = i0 + q;
-                if (i < NI) {
-                    const int ks = g + 2 * i;
-                    const int64_t k0 = k0_of(i);
-                    const int nv = nvalid_of(k0);
-                    uint32_t hw[16];
-                    if (row_ok && nv > 0) {
-                        if (MODE == 3) {
-                            float v[32];
-                            ring[q].decode(v);
-                            split_half_words(v, lo_part, hw);
-                        } else {
-                            to_half_words<FMT>(ring[q], hw);
-                        }
-                        if (nv < 32) {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                if (2 * e >= nv) hw[e] = 0u;  // nv is even
-                        }
+                    if (row_ok) {
+                        const uint32_t rb = W0 + rs * kRawBytes + (uint32_t)r * 144u;
+                        const uint4 hdr = lds128(rb);
+                        const uint4 q0 = lds128(rb + 16u + 32u * g + 16u * h);
+                        const uint4 q1 = lds128(rb + 16u + 32u * (g + 2) + 16u * h);
+                        q4k_half_chunk_to_half(hdr, q0, g, hw0);
+                        q4k_half_chunk_to_half(hdr, q1, g + 2, hw1);
                     } else {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) hw[e] = 0u;
+                        for (int e = 0; e < 16; ++e) hw0[e] = hw1[e] = 0u;
                     }
-                    const int64_t kn = k0_of(i + PD);
-                    const int nvn = nvalid_of(kn);
-                    if (i + PD < NI && row_ok && nvn > 0) ring[q].load(rowp, kn, nvn);
-                    const uint32_t ta = a_slot(ks, failed);
-                    tmem_st16(ta + 16u * h, hw);  // weights 32h + 0..31 -> columns 16h..16h+15
-                    a_done(ks, failed);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(rawEmpty(rs));  // raw tile read
+                    // weights 16h + 0..15 -> columns 8h..8h+7; 32 + 16h + 0..15 -> 16 + 8h..
+                    const uint32_t ta0 = a_slot(4 * b + g);
+                    tmem_st8(ta0 + 8u * h, hw0);
+                    tmem_st8(ta0 + 16u + 8u * h, hw0 + 8);
+                    const uint32_t ta1 = a_slot(4 * b + g + 2);
+                    tmem_st8(ta1 + 8u * h, hw1);
+                    tmem_st8(ta1 + 16u + 8u * h, hw1 + 8);
+                    a_done(4 * b + g + 2);
                 }
-            }
-        }
-        }  // generic dequant
-        // ------------------------------ epilogue ------------------------------
-        __syncwarp();
-        const bool acc_ok = mbar_wait(accb, 0);
-        if (!acc_ok) record_error(p.err, DERR_MMA_ACC);
-        tc_fence_after();
-        const int slice = dq;  // 0..3: which part of the token columns  // 0..3: which part of the token columns
-        constexpr int kSlices = kTokOut >= 64 ? 4 : (kTokOut >= 32 ? 2 : 1);
-        constexpr int kSliceCols = kTokOut / kSlices;
-        const int c_lo = slice < kSlices ? slice * kSliceCols : 0;
-        const int c_hi = slice < kSlices ? c_lo + kSliceCols : 0;
-        const int rl = r;                                   // accumulator row (TMEM lane)
-        const int64_t je = m0 + (MODE == 3 ? (rl & 63) : rl);
-        const bool store_ok = acc_ok && !*abort_flag && je < p.j1;
-        const uint32_t tbase = tmem + ((uint32_t)(32 * quarter) << 16);
-        // MODE 3 row-pair scratch [col][64] and the output tile: over the x ring
-        float *scratch = reinterpret_cast<float *>(smem_raw + (B0 - raw_addr));
-        // columns in chunks of 16 (kSliceCols is a multiple of 16)
-        // the two accumulators (even / odd k-steps) are summed here; KS == 1
-        // leaves the odd one unwritten
-        const bool two_acc = C::kNAcc == 2 && KS > 1;
-        auto load_acc = [&](int col, float (&acc)[16]) {
-            uint32_t v[16], v2[16];
-            tmem_ld16(tbase + (uint32_t)col, v);
-            if (two_acc) tmem_ld16(tbase + (uint32_t)(C::kAccCols + col), v2);
-            if (MODE == 1) {
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    acc[i] = __uint_as_float(v[i]) + (two_acc ? __uint_as_float(v2[i]) : 0.0f);
             } else {
-                uint32_t w2[16], w3[16];
-                tmem_ld16(tbase + (uint32_t)(col + BN / 2), w2);
-                if (two_acc) tmem_ld16(tbase + (uint32_t)(C::kAccCols + col + BN / 2), w3);
-                tmem_ld_wait();
+                const bool lo_part = MODE == 3 && r >= 64;  // MODE 3: rows 64..127 hold W_lo
+                const int64_t j = t.m0 + (MODE == 3 ? (r & 63) : r);
+                const bool row_ok = j < p.j1;
+                const uint8_t *rowp = p.w + (row_ok ? j : 0) * p.row_bytes;
+                constexpr int PD = Prefetch<FMT>::value;
+                Raw32<FMT> ring[PD];
+                // this thread's i-th k-step is g + 2 i
+                auto ks_of = [&](int i) { return g + 2 * i; };
+                auto k0_of = [&](int i) {
+                    const int ks = ks_of(i);
+                    return (int64_t)(ks < KS ? kx(t, ks) : ks) * kBK + 32 * h;
+                };
+                auto nvalid_of = [&](int64_t k0) {
+                    const int64_t v = p.k - k0;
+                    return (int)(v < 0 ? 0 : (v > 32 ? 32 : v));
+                };
+                // k-steps of this group over the stage-padded range: a k-step
+                // past k stores zeros (the MMA skips it) but still takes part
+                // in its stage's arrival count
+                const int NI = (NSA * KA - g + 1) / 2;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    acc[i] = __uint_as_float(v[i]) + __uint_as_float(w2[i]);
-                    if (two_acc) acc[i] += __uint_as_float(v2[i]) + __uint_as_float(w3[i]);
+                for (int q = 0; q < PD; ++q) {
+                    const int64_t k0 = k0_of(q);
+                    const int nv = nvalid_of(k0);
+                    if (q < NI && row_ok && nv > 0) ring[q].load(rowp, k0, nv);
+                }
+                for (int i0 = 0; i0 < NI && !failed; i0 += PD) {
+#pragma unroll
+                    for (int q = 0; q < PD; ++q) {
+                        const int i = i0 + q;
+                        if (i < NI) {
+                            const int ks = ks_of(i);
+                            const int64_t k0 = k0_of(i);
+                            const int nv = nvalid_of(k0);
+                            uint32_t hw[16];
+                            if (row_ok && nv > 0) {
+                                if (MODE == 3) {
+                                    float v[32];
+                                    ring[q].decode(v);
+                                    split_half_words(v, lo_part, hw);
+                                } else {
+                                    to_half_words<FMT>(ring[q], hw);
+                                }
+                                if (nv < 32) {
+#pragma unroll
+                                    for (int e = 0; e < 16; ++e)
+                                        if (2 * e >= nv) hw[e] = 0u;  // nv is even
+                                }
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) hw[e] = 0u;
+                            }
+                            const int64_t kn = k0_of(i + PD);
+                            const int nvn = nvalid_of(kn);
+                            if (i + PD < NI && row_ok && nvn > 0) ring[q].load(rowp, kn, nvn);
+                            const uint32_t ta = a_slot(ks);
+                            tmem_st16(ta + 16u * h, hw);  // weights 32h + 0..31 -> columns 16h..
+                            a_done(ks);
+                        }
+                    }
                 }
             }
-        };
-        if (MODE == 3 && quarter >= 2) {
-            // lo rows: park (D[r][c] + D[r][c + BN/2]) for the hi warps
-            __syncwarp();
-            for (int col = c_lo; col < c_hi; col += 16) {
-                float acc[16];
-                load_acc(col, acc);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) scratch[(col + i) * 64 + (rl & 63)] = acc[i];
+            abase += NSA;
+            if (failed) break;
+            // ------------------------------ epilogue ------------------------------
+            // TMEM -> registers -> y: per warp store, 32 consecutive rows of one
+            // token (128 contiguous bytes)
+            const int xb = it & 1;
+            const bool acc_ok = mbar_wait(accFull, it & 1) && mbar_wait(xsFull(xb), (it >> 1) & 1);
+            if (!acc_ok) {
+                record_error(p.err, DERR_MMA_ACC);
+                *abort_flag = 1;
+                failed = true;
+                break;
             }
-        }
-        if (MODE == 3) named_barrier(2, 32 * kDeqWarps);
-        if (p.tma_store) {
-            // stage the [tokens][rows] fp32 tile in the (now idle) x ring, then one
-            // TMA store (or reduce-add) writes it; the map clips rows >= n_tokens
-            // and columns >= j_end (MODE 3: after its row-pair scratch)
-            const uint32_t st0 = MODE == 3 ? B0 + (uint32_t)(kTokOut * 64 * 4) : B0;
-            float *stile = reinterpret_cast<float *>(smem_raw + (st0 - raw_addr));
-            if (MODE != 3 || quarter < 2) {
+            tc_fence_after();
+            const float *xsc = xs_s + xb * kTokOut;
+            const int slice = dq;  // 0..3: which part of the token columns
+            constexpr int kSlices = kTokOut >= 64 ? 4 : (kTokOut >= 32 ? 2 : 1);
+            constexpr int kSliceCols = kTokOut / kSlices;
+            const int c_lo = slice < kSlices ? slice * kSliceCols : 0;
+            const int c_hi = slice < kSlices ? c_lo + kSliceCols : 0;
+            const int64_t je = t.m0 + (MODE == 3 ? (r & 63) : r);
+            const bool store_ok = !*abort_flag && je < p.j1;
+            // MODE 3 row-pair scratch [col][64] over the x ring (MODE 3 CTAs
+            // take one tile each: nothing is prefetched into the ring)
+            float *scratch = reinterpret_cast<float *>(smem_raw + (B0 - raw_addr));
+            // the two accumulators (even / odd k-steps) are summed here; KS == 1
+            // leaves the odd one unwritten
+            const bool two_acc = C::kNAcc == 2 && KS > 1;
+            auto load_acc = [&](int col, float (&acc)[16]) {
+                uint32_t v[16], v2[16];
+                tmem_ld16(tlane + (uint32_t)col, v);
+                if (two_acc) tmem_ld16(tlane + (uint32_t)(C::kAccCols + col), v2);
+                if (MODE == 1) {
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        acc[i] = __uint_as_float(v[i]) + (two_acc ? __uint_as_float(v2[i]) : 0.0f);
+                } else {
+                    uint32_t w2[16], w3[16];
+                    tmem_ld16(tlane + (uint32_t)(col + BN / 2), w2);
+                    if (two_acc) tmem_ld16(tlane + (uint32_t)(C::kAccCols + col + BN / 2), w3);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        acc[i] = __uint_as_float(v[i]) + __uint_as_float(w2[i]);
+                        if (two_acc) acc[i] += __uint_as_float(v2[i]) + __uint_as_float(w3[i]);
+                    }
+                }
+            };
+            if (MODE == 3 && quarter >= 2) {
+                // lo rows: park (D[r][c] + D[r][c + BN/2]) for the hi warps
+                for (int col = c_lo; col < c_hi; col += 16) {
+                    float acc[16];
+                    load_acc(col, acc);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) scratch[(col + i) * 64 + (r & 63)] = acc[i];
+                }
                 __syncwarp();
-                const int row = MODE == 3 ? (rl & 63) : rl;
+                if (lane == 0) mbar_arrive(scrReady);
+            }
+            bool scr_ok = true;
+            if (MODE == 3 && quarter < 2) {
+                scr_ok = mbar_wait(scrReady, 0);  // one tile per CTA in MODE 3
+                if (!scr_ok) {
+                    record_error(p.err, DERR_MMA_ACC);
+                    *abort_flag = 1;
+                }
+            }
+            if ((MODE != 3 || quarter < 2) && scr_ok) {
                 for (int col = c_lo; col < c_hi; col += 16) {
                     float acc[16];
                     load_acc(col, acc);
                     if (MODE == 3) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) acc[i] += scratch[(col + i) * 64 + (rl & 63)];
+                        for (int i = 0; i < 16; ++i) acc[i] += scratch[(col + i) * 64 + (r & 63)];
                     }
+                    if (store_ok) {
+                        const int64_t t0 = t.n0 + col;
+                        float *yp = p.y + t0 * p.n + je;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int64_t t = n0 + col + i;
-                        const float sc = t < p.n_tokens ? __ldg(p.xscale + t) : 0.0f;
-                        stile[(col + i) * kRowsOut + row] = acc[i] * sc;
-                    }
-                }
-            }
-            fence_proxy_async_smem();
-            named_barrier(3, 32 * kDeqWarps);
-            if (tid == 64 && acc_ok && !*abort_flag) {
-                if (p.accumulate)
-                    tma_reduce_add_2d(&tmy, (int)m0, n0, st0);
-                else
-                    tma_store_2d(&tmy, (int)m0, n0, st0);
-                bulk_commit_group();
-                bulk_wait_group_read0();
-            }
-        } else if (MODE != 3 || quarter < 2) {
-            __syncwarp();
-            for (int col = c_lo; col < c_hi; col += 16) {
-                float acc[16];
-                load_acc(col, acc);
-                if (MODE == 3) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[i] += scratch[(col + i) * 64 + (rl & 63)];
-                }
-                if (store_ok) {
-                    const int64_t t0 = n0 + col;
-                    float *yp = p.y + t0 * p.n + je;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        if (t0 + i < p.n_tokens) {
-                            const float val = acc[i] * __ldg(p.xscale + t0 + i);
-                            float *yq = yp + (int64_t)i * p.n;
-                            *yq = p.accumulate ? *yq + val : val;
+                        for (int i = 0; i < 16; ++i) {
+                            if (t0 + i < p.n_tokens) {
+                                const float val = acc[i] * xsc[col + i];
+                                float *yq = yp + (int64_t)i * p.n;
+                                *yq = p.accumulate ? *yq + val : val;
+                            }
                         }
                     }
                 }
+            }
+            // accumulator and token scales free for the next tile
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(accEmpty);
+                mbar_arrive(xsFree(xb));
             }
         }
     }
@@ -672,6 +743,7 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const float *__restrict__
                                                        __half *__restrict__ x16lo,
                                                        float *__restrict__ xscale) {
     __shared__ float red[8];
+    pdl_launch_dependents();  // the product kernel may start its W pipeline now
     const int64_t t = blockIdx.x;
     const float *xt = x + t * k;
     float m = 0.0f;
@@ -743,54 +815,76 @@ static EncodeTiledFn get_encode_fn() {
 }
 
 struct Maps {
-    CUtensorMap x, xlo, w, y;
+    CUtensorMap x, xlo, w;
 };
 
+// Persistent grid: clusters of two CTAs, as many as can be resident at once
+// (one CTA per SM), capped by the number of row-tile pairs x token tiles.
+// MODE 3 keeps one tile per CTA (its epilogue scratch lives in the x ring).
 template <int FMT, int BN, int MODE>
-static cudaError_t launch_t(const Maps &mp, const MmaParams &p, dim3 grid, cudaStream_t s) {
+static cudaError_t launch_t(const Maps &mp, const MmaParams &p, const DeviceInfo &dev,
+                            cudaStream_t s) {
     using C = MmaCfg<BN, FMT == F_Q4_K && MODE != 3>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(mma_kernel<FMT, BN, MODE>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    static int max_clusters = 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
     cfg.blockDim = dim3(kMmaThreads);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mma_kernel<FMT, BN, MODE>, mp.x, mp.xlo, mp.w, mp.y, p);
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(mma_kernel<FMT, BN, MODE>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+        if (attr_err != cudaSuccess) return;
+        cudaLaunchConfig_t q = cfg;
+        q.gridDim = dim3(2 * (unsigned)(dev.sm_count / 2));
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<FMT, BN, MODE>, &q) != cudaSuccess ||
+            n <= 0) {
+            (void)cudaGetLastError();
+            n = dev.sm_count / 2;
+        }
+        max_clusters = n;
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int units = p.pairs * p.tiles_n;
+    const int clusters = MODE == 3 ? units : std::min(units, max_clusters);
+    cfg.gridDim = dim3(2 * (unsigned)clusters);
+    // programmatic launch after the x conversion kernel (see pdl_wait_prev)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, mma_kernel<FMT, BN, MODE>, mp.x, mp.xlo, mp.w, p);
 }
 
 template <int FMT, int MODE>
-static cudaError_t launch_bn(int bn, const Maps &mp, const MmaParams &p, dim3 grid, cudaStream_t s) {
+static cudaError_t launch_bn(int bn, const Maps &mp, const MmaParams &p, const DeviceInfo &dev,
+                             cudaStream_t s) {
     switch (bn) {
-    case 16: if (MODE == 1) return launch_t<FMT, 16, MODE>(mp, p, grid, s); break;
-    case 32: return launch_t<FMT, 32, MODE>(mp, p, grid, s);
-    case 64: return launch_t<FMT, 64, MODE>(mp, p, grid, s);
-    case 128: return launch_t<FMT, 128, MODE>(mp, p, grid, s);
-    case 256: return launch_t<FMT, 256, MODE>(mp, p, grid, s);
+    case 16: if (MODE == 1) return launch_t<FMT, 16, MODE>(mp, p, dev, s); break;
+    case 32: return launch_t<FMT, 32, MODE>(mp, p, dev, s);
+    case 64: return launch_t<FMT, 64, MODE>(mp, p, dev, s);
+    case 128: return launch_t<FMT, 128, MODE>(mp, p, dev, s);
+    case 256: return launch_t<FMT, 256, MODE>(mp, p, dev, s);
     default: break;
     }
     return cudaErrorInvalidValue;
 }
 
 template <int FMT>
-static cudaError_t launch_fmt(int mode, int bn, const Maps &mp, const MmaParams &p, dim3 grid,
-                              cudaStream_t s) {
+static cudaError_t launch_fmt(int mode, int bn, const Maps &mp, const MmaParams &p,
+                              const DeviceInfo &dev, cudaStream_t s) {
     constexpr bool quant = FMT != F_BF16 && FMT != F_F16;
-    if (mode == 2) return launch_bn<FMT, 2>(bn, mp, p, grid, s);
-    if (quant && mode == 1) return launch_bn<FMT, quant ? 1 : 2>(bn, mp, p, grid, s);
-    if (quant && mode == 3) return launch_bn<FMT, quant ? 3 : 2>(bn, mp, p, grid, s);
+    if (mode == 2) return launch_bn<FMT, 2>(bn, mp, p, dev, s);
+    if (quant && mode == 1) return launch_bn<FMT, quant ? 1 : 2>(bn, mp, p, dev, s);
+    if (quant && mode == 3) return launch_bn<FMT, quant ? 3 : 2>(bn, mp, p, dev, s);
     return cudaErrorInvalidValue;
 }
 
@@ -856,43 +950,23 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    // y as a [n_tokens][j_end] fp32 tensor with row stride n; one box = one
-    // output tile. TMA needs a 16-byte aligned base and row stride and a
-    // 16-byte aligned first column (j_start % 4 == 0); its bound on the inner
-    // dimension acts in 16-byte steps, so j_end must be a multiple of 4 too
-    // (otherwise up to 3 columns past j_end would be written).
-    const int rows_out = mode == 3 ? 64 : kBM;
-    const bool tma_store = (reinterpret_cast<uintptr_t>(m.y) & 15u) == 0 && (m.n % 4) == 0 &&
-                           (m.j0 % 4) == 0 && (m.j1 % 4) == 0;
-    mp.y = tm;
-    if (tma_store) {
-        const cuuint64_t dims[2] = {(cuuint64_t)m.j1, (cuuint64_t)m.n_tokens};
-        const cuuint64_t strides[1] = {(cuuint64_t)m.n * 4};
-        const cuuint32_t box[2] = {(cuuint32_t)rows_out, (cuuint32_t)tok};
-        const cuuint32_t estr[2] = {1, 1};
-        if (encode(&mp.y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, m.y, dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
     MmaParams p;
     p.w = m.w; p.y = m.y; p.xscale = xscale;
-    p.tma_store = tma_store ? 1 : 0;
     p.k = m.k; p.n = m.n; p.n_tokens = m.n_tokens; p.row_bytes = m.row_bytes;
     p.j0 = m.j0; p.j1 = m.j1;
     p.KS = (int)(kp / kBK);
     p.accumulate = m.accumulate;
     p.err = dev.err;
-    // pairs of CTAs (clusters of two) along the row tiles: round up to even
-    unsigned gx = (unsigned)((M + rows_out - 1) / rows_out);
-    gx += gx & 1u;
-    const dim3 grid(gx, (unsigned)((m.n_tokens + tok - 1) / tok));
+    const int rows_out = mode == 3 ? 64 : kBM;
+    const int64_t tiles_m = (M + rows_out - 1) / rows_out;
+    p.pairs = (int)((tiles_m + 1) / 2);
+    p.tiles_n = (int)((m.n_tokens + tok - 1) / tok);
     switch (m.fmt) {
-    case F_BF16: return launch_fmt<F_BF16>(mode, bn, mp, p, grid, s);
-    case F_F16: return launch_fmt<F_F16>(mode, bn, mp, p, grid, s);
-    case F_Q4_0: return launch_fmt<F_Q4_0>(mode, bn, mp, p, grid, s);
-    case F_Q4_K: return launch_fmt<F_Q4_K>(mode, bn, mp, p, grid, s);
-    case F_Q6_K: return launch_fmt<F_Q6_K>(mode, bn, mp, p, grid, s);
+    case F_BF16: return launch_fmt<F_BF16>(mode, bn, mp, p, dev, s);
+    case F_F16: return launch_fmt<F_F16>(mode, bn, mp, p, dev, s);
+    case F_Q4_0: return launch_fmt<F_Q4_0>(mode, bn, mp, p, dev, s);
+    case F_Q4_K: return launch_fmt<F_Q4_K>(mode, bn, mp, p, dev, s);
+    case F_Q6_K: return launch_fmt<F_Q6_K>(mode, bn, mp, p, dev, s);
     default: return cudaErrorInvalidValue;
     }
 }
