@@ -278,6 +278,13 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t tmem_d, uint64_t adesc, uint
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Load with acquire semantics at GPU scope (pairs with a release or a fence
+// + atomic by another CTA).
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 // True in exactly one lane of the (converged) warp.
 __device__ __forceinline__ bool elect_one() {
     uint32_t pred;

@@ -54,6 +54,9 @@ struct MmaParams {
     int accumulate;
     int pairs;       // pairs of 128-row tiles (a cluster of two CTAs takes one pair)
     int tiles_n;     // token tiles
+    int full_units;  // pair-tiles computed whole (the first units)
+    int split;       // the remaining pair-tiles are computed as `split` k-ranges each
+    int n_units;     // full_units + (pairs * tiles_n - full_units) * split
     unsigned int *err;
 };
 
@@ -274,27 +277,54 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t crank = cluster_ctarank();  // 0 or 1 within the CTA pair
     const int KS = p.KS;                     // 64-wide k-steps
-    const int NSA = (KS + KA - 1) / KA;      // A stages per tile (the last may be padded)
-    const int NSB = (KS + KB - 1) / KB;      // x stages per tile
     // Tiles: the pair of CTAs takes 128-row tiles 2q and 2q + 1 of token tile
-    // nt together; pair-tile u = q * tiles_n + nt, and cluster c of C takes
-    // u = c, c + C, ... (the two token tiles of one W row pair run side by
-    // side on neighbouring clusters, so W is read from HBM about once).
-    const int n_units = p.pairs * p.tiles_n;
+    // nt together; pair-tile v = q * tiles_n + nt (the token tiles of one W
+    // row pair run side by side on neighbouring clusters, so W is read from
+    // HBM about once). Units: the first full_units pair-tiles whole, then the
+    // rest in split = 2 super-block-aligned k-halves each, so that the last
+    // round keeps every cluster busy; the halves add into a y region the
+    // conversion kernel zeroed (0 + a + b is the same in either order, so the
+    // result does not depend on which half lands first). Cluster c of C takes
+    // units c, c + C, ...
     const int c0 = (int)(blockIdx.x >> 1), cstep = (int)(gridDim.x >> 1);
-    struct Tile { int64_t m0; int n0; int rot; };
+    struct Tile {
+        int64_t m0;
+        int n0, rot;
+        int k_lo, k_hi;  // k-steps of this unit
+        int part;        // k-range index, or -1 for a whole tile
+    };
     auto tile_of = [&](int u) {
-        const int q = u / p.tiles_n, nt = u - q * p.tiles_n;
+        int v = u, part = -1;
+        if (u >= p.full_units) {
+            const int w = u - p.full_units;
+            v = p.full_units + w / p.split;
+            part = w % p.split;
+        }
+        const int q = v / p.tiles_n, nt = v - q * p.tiles_n;
         Tile t;
         t.m0 = p.j0 + (int64_t)(2 * q + (int)crank) * kRowsOut;
         t.n0 = nt * kTokOut;
-        // each pair walks k in its own rotated order (whole super-blocks) so
-        // that the CTAs do not all fetch the same x tile at the same moment;
-        // the sum is the same up to rounding order
-        t.rot = (KS % 4 == 0) ? 4 * (q % (KS / 4)) : 0;
+        t.part = part;
+        if (part < 0) {
+            t.k_lo = 0;
+            t.k_hi = KS;
+            // each whole tile walks k in its own rotated order (whole super-blocks)
+            // so that the CTAs do not all fetch the same x tile at the same
+            // moment; the sum is the same up to rounding order
+            t.rot = (KS % 4 == 0) ? 4 * (q % (KS / 4)) : 0;
+        } else {
+            const int nsb = (KS + 3) / 4;
+            t.k_lo = 4 * (part * nsb / p.split);
+            t.k_hi = std::min(KS, 4 * ((part + 1) * nsb / p.split));
+            t.rot = 0;
+        }
         return t;
     };
     auto kx = [&](const Tile &t, int ks) { return t.rot ? (ks + t.rot) % KS : ks; };
+    auto nks = [&](const Tile &t) { return t.k_hi - t.k_lo; };
+    // A stages (the last may be padded) and x stages of a unit
+    auto nsa = [&](const Tile &t) { return (nks(t) + KA - 1) / KA; };
+    auto nsb = [&](const Tile &t) { return (nks(t) + KB - 1) / KB; };
 
     if (tid == 0) {
         for (int s = 0; s < NA; ++s) {
@@ -340,7 +370,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
         int bcount = 0;  // x stages issued so far (all tiles)
         int it = 0;
-        for (int u = c0; u < n_units; u += cstep, ++it) {
+        for (int u = c0; u < p.n_units; u += cstep, ++it) {
             if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
             const Tile t = tile_of(u);
             // the tile's token scales (2^e of each token's fp16 conversion) for
@@ -358,6 +388,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(xsFull(xb));
+                const int NSB = nsb(t);
                 for (int st = 0; st < NSB; ++st, ++bcount) {
                     const int slot = bcount % NB;
                     if (bcount >= NB &&
@@ -369,7 +400,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                     // the whole stage lands here: this CTA's halves and the peer's halves
                     mbar_arrive_expect_tx(fullB(slot), C::kBStage);
                     for (int sub = 0; sub < KB; ++sub) {
-                        const int ks = st * KB + sub;  // past KS: zero-filled by the map
+                        // past k_hi: not used; past KS: zero-filled by the map
+                        const int ks = t.k_lo + st * KB + sub;
                         const int kc = ks < KS ? kx(t, ks) : ks;
                         // MODE 1: this CTA fetches token rows [n0 + crank BN/2, +BN/2);
                         // MODE 2/3: CTA 0 the hi rows, CTA 1 the lo rows of the tile's tokens
@@ -401,7 +433,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         int abase = 0, bbase = 0;  // A / x stages consumed by earlier tiles
         int it = 0;
         bool failed = false;
-        for (int u = c0; u < n_units && !failed; u += cstep, ++it) {
+        for (int u = c0; u < p.n_units && !failed; u += cstep, ++it) {
+            const Tile t = tile_of(u);
+            const int KSu = nks(t);
             if (it > 0) {  // the epilogue has drained the accumulator
                 const bool ok = wait_abortable(accEmpty, (it - 1) & 1, abort_flag);
                 if (__all_sync(0xFFFFFFFFu, ok) == 0) {
@@ -410,7 +444,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 }
                 tc_fence_after();
             }
-            for (int ks = 0; ks < KS; ++ks) {
+            for (int ks = 0; ks < KSu; ++ks) {
                 const int st = abase + ks / KA, sa = st % NA;
                 const int bt = bbase + ks / KB, sb = bt % NB;
                 if (ks % KA == 0) {
@@ -441,7 +475,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16: 8 A columns, 32 B bytes
                         tc_mma_f16_ts(dacc, at + 8 * kk, bd + 2 * kk, idesc, acc0 || kk != 0);
-                    const bool last = ks == KS - 1;
+                    const bool last = ks == KSu - 1;
                     if (ks % KB == KB - 1 || last)
                         tc_commit_multicast(emptyB(sb), (uint16_t)3);  // both CTAs may refill
                     if (ks % KA == KA - 1 || last) tc_commit(emptyA(sa));
@@ -449,8 +483,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 }
                 __syncwarp();
             }
-            abase += NSA;
-            bbase += NSB;
+            abase += nsa(t);
+            bbase += nsb(t);
         }
     } else if (warp == kRawWarp) {
         // ------------------------------ raw Q4_K tiles via TMA ------------------------------
@@ -458,13 +492,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         // warps as it is deep (into the next tile), whatever the x ring does
         if (kRaw && lane == 0) {
             prefetch_tmap(&tmw);
-            const int NSBLK = KS / 4;  // k % 256 == 0
             int rcount = 0;
-            for (int u = c0; u < n_units; u += cstep) {
+            for (int u = c0; u < p.n_units; u += cstep) {
                 if (*abort_flag) break;
                 const Tile t = tile_of(u);
                 bool ok = true;
-                for (int b = 0; b < NSBLK; ++b, ++rcount) {
+                for (int b = t.k_lo / 4; b < t.k_hi / 4; ++b, ++rcount) {  // k % 256 == 0
                     const int rs = rcount % kNR;
                     if (rcount >= kNR &&
                         !wait_abortable(rawEmpty(rs), ((rcount / kNR) + 1) & 1, abort_flag)) {
@@ -524,13 +557,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             }
         };
         int it = 0;
-        for (int u = c0; u < n_units && !failed; u += cstep, ++it) {
+        for (int u = c0; u < p.n_units && !failed; u += cstep, ++it) {
             const Tile t = tile_of(u);
+            const int KSu = nks(t);
             if constexpr (kRaw) {
                 // per super-block b (one A stage): thread (r, h) of group g decodes
                 // half h of row r's 64-weight chunks c = g and g + 2
                 const bool row_ok = t.m0 + r < p.j1;
-                const int NSBLK = KS / 4;  // k % 256 == 0
+                const int NSBLK = KSu / 4;  // k % 256 == 0: whole super-blocks
                 for (int b = 0; b < NSBLK && !failed; ++b, ++rcount) {
                     const int rs = rcount % kNR;
                     uint32_t hw0[16], hw1[16];
@@ -572,9 +606,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 Raw32<FMT> ring[PD];
                 // this thread's i-th k-step is g + 2 i
                 auto ks_of = [&](int i) { return g + 2 * i; };
+                // unit-relative k-step -> first weight index; past the unit's
+                // range: beyond k (nothing loaded, zeros stored)
                 auto k0_of = [&](int i) {
-                    const int ks = ks_of(i);
-                    return (int64_t)(ks < KS ? kx(t, ks) : ks) * kBK + 32 * h;
+                    const int ks = t.k_lo + ks_of(i);
+                    return ks < t.k_hi ? (int64_t)kx(t, ks) * kBK + 32 * h : p.k;
                 };
                 auto nvalid_of = [&](int64_t k0) {
                     const int64_t v = p.k - k0;
@@ -583,7 +619,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 // k-steps of this group over the stage-padded range: a k-step
                 // past k stores zeros (the MMA skips it) but still takes part
                 // in its stage's arrival count
-                const int NI = (NSA * KA - g + 1) / 2;
+                const int NI = (nsa(t) * KA - g + 1) / 2;
 #pragma unroll
                 for (int q = 0; q < PD; ++q) {
                     const int64_t k0 = k0_of(q);
@@ -626,7 +662,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                     }
                 }
             }
-            abase += NSA;
+            abase += nsa(t);
             if (failed) break;
             // ------------------------------ epilogue ------------------------------
             // TMEM -> registers -> y: per warp store, 32 consecutive rows of one
@@ -648,12 +684,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             const int c_hi = slice < kSlices ? c_lo + kSliceCols : 0;
             const int64_t je = t.m0 + (MODE == 3 ? (r & 63) : r);
             const bool store_ok = !*abort_flag && je < p.j1;
+            // the k-halves of a split tile add into zeros
+            const bool split = t.part >= 0;
+            if (split) pdl_wait_prev();  // the conversion kernel zeroed the region
             // MODE 3 row-pair scratch [col][64] over the x ring (MODE 3 CTAs
             // take one tile each: nothing is prefetched into the ring)
             float *scratch = reinterpret_cast<float *>(smem_raw + (B0 - raw_addr));
             // the two accumulators (even / odd k-steps) are summed here; KS == 1
             // leaves the odd one unwritten
-            const bool two_acc = C::kNAcc == 2 && KS > 1;
+            const bool two_acc = C::kNAcc == 2 && KSu > 1;
             auto load_acc = [&](int col, float (&acc)[16]) {
                 uint32_t v[16], v2[16];
                 tmem_ld16(tlane + (uint32_t)col, v);
@@ -710,7 +749,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                             if (t0 + i < p.n_tokens) {
                                 const float val = acc[i] * xsc[col + i];
                                 float *yq = yp + (int64_t)i * p.n;
-                                *yq = p.accumulate ? *yq + val : val;
+                                if (split)
+                                    atomicAdd(yq, val);
+                                else
+                                    *yq = p.accumulate ? *yq + val : val;
                             }
                         }
                     }
@@ -735,15 +777,35 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
 }
 
+// y columns that split tiles add into: zeroed per token by the conversion kernel
+struct SplitZero {
+    float *y;          // null: no split tiles
+    int64_t n, j0, j1;
+    int first;         // first split pair-tile
+    int pairs, tiles_n, tok, rows;
+};
+
 // X [N][k] fp32 -> X16 [N][kp] fp16 (zero padded) scaled by 2^-e per row so the
 // row's largest magnitude lands in [2^14, 2^15); xscale[t] = 2^e. With x16lo,
 // also the fp16 rounding of what X16 missed (x = hi + lo to ~22 bits).
 __global__ void __launch_bounds__(256) x_to_f16_kernel(const float *__restrict__ x, int64_t k,
                                                        int64_t kp, __half *__restrict__ x16,
                                                        __half *__restrict__ x16lo,
-                                                       float *__restrict__ xscale) {
+                                                       float *__restrict__ xscale,
+                                                       const SplitZero z) {
     __shared__ float red[8];
     pdl_launch_dependents();  // the product kernel may start its W pipeline now
+    if (z.y) {
+        // split pair-tiles v >= first (v = q * tiles_n + nt) of this token's
+        // token tile start at the first such v; they run to the last row tile
+        const int nt = (int)(blockIdx.x / z.tok);
+        const int v0 = z.first + ((nt - z.first % z.tiles_n) % z.tiles_n + z.tiles_n) % z.tiles_n;
+        if (v0 < z.pairs * z.tiles_n) {
+            const int64_t c0 = z.j0 + (int64_t)(v0 / z.tiles_n) * 2 * z.rows;
+            float *yt = z.y + (int64_t)blockIdx.x * z.n;
+            for (int64_t j = c0 + threadIdx.x; j < z.j1; j += blockDim.x) yt[j] = 0.0f;
+        }
+    }
     const int64_t t = blockIdx.x;
     const float *xt = x + t * k;
     float m = 0.0f;
@@ -818,6 +880,37 @@ struct Maps {
     CUtensorMap x, xlo, w;
 };
 
+// Clusters of two CTAs (one CTA per SM) that can be resident at once: every
+// instance of the kernel has the same footprint class, so one query serves all.
+static int mma_clusters(const DeviceInfo &dev) {
+    static std::once_flag once;
+    static int n = 0;
+    std::call_once(once, [&] {
+        cudaLaunchConfig_t q = {};
+        q.gridDim = dim3(2 * (unsigned)(dev.sm_count / 2));
+        q.blockDim = dim3(kMmaThreads);
+        q.dynamicSmemBytes = MmaCfg<256, true>::kSmem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        q.attrs = attr;
+        q.numAttrs = 1;
+        int v = 0;
+        if (cudaFuncSetAttribute(mma_kernel<F_Q4_K, 256, 1>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)MmaCfg<256, true>::kSmem) != cudaSuccess ||
+            cudaOccupancyMaxActiveClusters(&v, mma_kernel<F_Q4_K, 256, 1>, &q) != cudaSuccess ||
+            v <= 0) {
+            (void)cudaGetLastError();
+            v = dev.sm_count / 2;
+        }
+        n = v;
+    });
+    return n;
+}
+
 // Persistent grid: clusters of two CTAs, as many as can be resident at once
 // (one CTA per SM), capped by the number of row-tile pairs x token tiles.
 // MODE 3 keeps one tile per CTA (its epilogue scratch lives in the x ring).
@@ -851,11 +944,11 @@ static cudaError_t launch_t(const Maps &mp, const MmaParams &p, const DeviceInfo
             (void)cudaGetLastError();
             n = dev.sm_count / 2;
         }
-        max_clusters = n;
+        max_clusters = std::min(n, mma_clusters(dev));
     });
     if (attr_err != cudaSuccess) return attr_err;
-    const int units = p.pairs * p.tiles_n;
-    const int clusters = MODE == 3 ? units : std::min(units, max_clusters);
+    const int P = p.pairs * p.tiles_n;
+    const int clusters = MODE == 3 ? P : std::min(p.n_units, max_clusters);
     cfg.gridDim = dim3(2 * (unsigned)clusters);
     // programmatic launch after the x conversion kernel (see pdl_wait_prev)
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -912,10 +1005,6 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
     __half *x16 = reinterpret_cast<__half *>(ws);
     __half *x16lo = mode >= 2 ? reinterpret_cast<__half *>(ws + one) : nullptr;
     float *xscale = reinterpret_cast<float *>(ws + (mode >= 2 ? 2 : 1) * one);
-    x_to_f16_kernel<<<(unsigned)m.n_tokens, 256, 0, s>>>(m.x, m.k, kp, x16, x16lo, xscale);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-
     // tokens per CTA tile: up to 256 (MODE 1) or 128 (hi + lo rows share the tile)
     const int tok_max = mode == 1 ? 256 : 128;
     int tok = tok_max;
@@ -923,6 +1012,27 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
         tok = 16;
         while (tok < m.n_tokens) tok <<= 1;
     }
+    // schedule: P pair-tiles over NC resident clusters; when the last round is
+    // at most half full, its R pair-tiles run as two k-halves each
+    const int rows_out = mode == 3 ? 64 : kBM;
+    const int64_t tiles_m = (M + rows_out - 1) / rows_out;
+    const int pairs = (int)((tiles_m + 1) / 2);
+    const int tiles_n = (int)((m.n_tokens + tok - 1) / tok);
+    const int P = pairs * tiles_n, NC = mma_clusters(dev);
+    const int R = P % NC;
+    const int KS = (int)(kp / kBK);
+    const bool split = mode != 3 && !m.accumulate && R > 0 && 2 * R <= NC && (KS + 3) / 4 >= 2;
+    SplitZero z = {};
+    if (split) {
+        z.y = m.y;
+        z.n = m.n; z.j0 = m.j0; z.j1 = m.j1;
+        z.first = P - R;
+        z.pairs = pairs; z.tiles_n = tiles_n; z.tok = mode == 1 ? tok : tok;
+        z.rows = rows_out;
+    }
+    x_to_f16_kernel<<<(unsigned)m.n_tokens, 256, 0, s>>>(m.x, m.k, kp, x16, x16lo, xscale, z);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     const int bn = mode == 1 ? tok : 2 * tok;
     // each CTA of a pair fetches half of an x tile: BN/2 token rows
     const int box_rows = bn / 2;
@@ -957,10 +1067,11 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
     p.KS = (int)(kp / kBK);
     p.accumulate = m.accumulate;
     p.err = dev.err;
-    const int rows_out = mode == 3 ? 64 : kBM;
-    const int64_t tiles_m = (M + rows_out - 1) / rows_out;
-    p.pairs = (int)((tiles_m + 1) / 2);
-    p.tiles_n = (int)((m.n_tokens + tok - 1) / tok);
+    p.pairs = pairs;
+    p.tiles_n = tiles_n;
+    p.full_units = split ? P - R : P;
+    p.split = split ? 2 : 1;
+    p.n_units = p.full_units + (P - p.full_units) * p.split;
     switch (m.fmt) {
     case F_BF16: return launch_fmt<F_BF16>(mode, bn, mp, p, dev, s);
     case F_F16: return launch_fmt<F_F16>(mode, bn, mp, p, dev, s);
