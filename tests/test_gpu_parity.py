@@ -248,6 +248,28 @@ def test_q4_k_prefill_full_size_every_output(nt):
     assert_parity(y, y_ref, s_ref, f"prefill all outputs N={nt}")
 
 
+def test_mma_repeatable_bits():
+    """The tensor-core path gives the same bits on every call, including the
+    row tiles of the last round that run as two k-halves adding into zeros
+    (0 + a + b rounds the same in either order); accumulate mode adds the same
+    result onto y."""
+    fmt, k, n, w, x = qmm_synth.workload("q4_k_prefill", n_tokens=512)
+    wd, xd = _dev(w), _dev(x)
+    ys = []
+    for _ in range(3):
+        ys.append(q.matmul(fmt, wd, xd, k, n).cpu().numpy())
+    torch.cuda.synchronize()
+    q.qmm_device_status()
+    _bits_equal(ys[0], ys[1])
+    _bits_equal(ys[0], ys[2])
+    # accumulate computes every tile whole (no k-halves): same sum up to the
+    # rounding order of the halves
+    y0 = np.full((512, n), 0.5, np.float32)
+    yacc = run(fmt, w, x, k, n, y0=y0, accumulate=True)
+    scale = float(np.abs(ys[0]).max())
+    np.testing.assert_allclose(yacc, ys[0] + np.float32(0.5), rtol=1e-5, atol=1e-5 * scale)
+
+
 # ------------------------------------------- overlapped (PDL) launches ----
 
 def test_overlap_chain_reads_previous_output():
