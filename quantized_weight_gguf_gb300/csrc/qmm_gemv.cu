@@ -146,6 +146,27 @@ __device__ __forceinline__ void unit_init(UnitState<FMT> &st, const float *xs, i
     }
 }
 
+// 16-bit formats: the unit's 8 x values straight from global memory (two
+// 16-byte loads when aligned; the units of a warp are consecutive).
+template <int FMT>
+__device__ __forceinline__ void unit_init_direct(UnitState<FMT> &st, const float *x, int u,
+                                                 bool valid) {
+    static_assert(UnitK<FMT>::value == 8, "16-bit formats only");
+    const float *xu = x + 8 * u;
+    if (!valid) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) st.xr[e] = 0.0f;
+    } else if ((reinterpret_cast<uintptr_t>(xu) & 15u) == 0) {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(xu));
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(xu) + 1);
+        st.xr[0] = a.x; st.xr[1] = a.y; st.xr[2] = a.z; st.xr[3] = a.w;
+        st.xr[4] = b.x; st.xr[5] = b.y; st.xr[6] = b.z; st.xr[7] = b.w;
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) st.xr[e] = __ldg(xu + e);
+    }
+}
+
 // Partial dot of one unit of one row; `rowa` is the row's shared address.
 template <int FMT>
 __device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<FMT> &st) {
@@ -277,8 +298,10 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
     const int part_bytes = 4 * p.RPF * PU;
     const int xs_off = (16 * NS + 16 + part_bytes + 127) & ~127;
     float *xs = reinterpret_cast<float *>(smem + xs_off);
-    const uint32_t stage_off =
-        (uint32_t)((xs_off + 4 * (int)(p.k + UnitK<FMT>::value) + 127) & ~127);
+    // 16-bit formats read their x slices straight from global memory (each
+    // thread's units are contiguous 32-byte runs): no staging area
+    const int xs_bytes = kChunked ? 0 : 4 * (int)(p.k + UnitK<FMT>::value);
+    const uint32_t stage_off = (uint32_t)((xs_off + xs_bytes + 127) & ~127);
     uint8_t *stages = smem + stage_off;
     const uint32_t stage0 = bar0 + stage_off;
     auto full = [&](int s) { return bar0 + 8u * s; };
@@ -342,7 +365,7 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
     // that kernel first (it may be producing x); y is never touched before
     // the wait.
     if (!p.x_ready) pdl_wait_prev();
-    {
+    if (!kChunked) {
         const int k = (int)p.k;
         const int U = p.U;
         if ((reinterpret_cast<uintptr_t>(p.x) & 15u) == 0 && (k & 3) == 0) {
@@ -375,7 +398,10 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
 #pragma unroll
     for (int q = 0; q < UPT; ++q) {
         const int u = u0 + q * kCons;
-        unit_init<FMT>(st[q], xs, p.U, active && u < p.U ? u : 0, active && u < p.U);
+        if constexpr (kChunked)
+            unit_init_direct<FMT>(st[q], p.x, u, u < p.U);
+        else
+            unit_init<FMT>(st[q], xs, p.U, active && u < p.U ? u : 0, active && u < p.U);
     }
     const int G = p.G;
     const int SEG = p.SEG;
@@ -523,28 +549,52 @@ cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t
         SEG = 0; PU = U;
     }
     const int64_t R = g.row_bytes;
-    // rows per stage: ~32 KB of weights, a multiple of the row groups, and
-    // small enough that every SM gets work on small problems
     const int ctas_target = 2 * dev.sm_count;
-    int64_t rb = std::max<int64_t>(1, 32768 / (G * R));
-    int64_t SR = G * rb;
     const int64_t per_cta = (M + ctas_target - 1) / ctas_target;
-    if (per_cta < SR) SR = std::max<int64_t>(G, ((per_cta + G - 1) / G) * G);
-    const int SB = (int)(((SR * R + 32) + 127) & ~127);
-    // partial-sum window: ~24 KB, whole stages
-    int64_t RPF = std::max<int64_t>(SR, (6144 / PU) / SR * SR);
-    const size_t part_bytes = (size_t)4 * RPF * PU;
-    const size_t fixed =
-        (size_t)((((16 * 8 + 16 + part_bytes + 127) & ~(size_t)127) + 4 * (g.k + uk) + 127) & ~(size_t)127);
-    // two CTAs per SM when the ring still gets >= 2 stages in ~110 KB
-    const size_t budget = 110 * 1024;
-    int NS = (int)std::min<int64_t>(8, (int64_t)((budget > fixed ? budget - fixed : 0) / SB));
-    if (NS < 2) NS = (int)std::min<int64_t>(8, std::max<int64_t>(2, (int64_t)((200 * 1024 - fixed) / SB)));
+    const size_t xs_bytes = chunked ? 0 : (size_t)4 * (g.k + uk);
+    auto smem_for = [&](int ns, int64_t sr, int64_t rpf) {
+        const size_t part_bytes = (size_t)4 * rpf * PU;
+        const size_t sb = (size_t)(((sr * R + 32) + 127) & ~(int64_t)127);
+        return (size_t)((((16 * ns + 16 + part_bytes + 127) & ~(size_t)127) + xs_bytes + 127) &
+                        ~(size_t)127) +
+               (size_t)ns * sb;
+    };
+    // The grid is two CTAs per SM. For 16-bit formats each CTA is also kept
+    // small enough that a third fits (3 x (smem + 1 KB reserved per block)
+    // within 228 KB): under programmatic dependent launch the next GEMV's CTA
+    // then starts streaming on an SM while this kernel's two still run, which
+    // hides most of the kernel boundary. Quantized formats need their x slices
+    // staged and more ring, so they keep two CTAs' worth of room.
+    const size_t two_cta_limit = chunked ? 228 * 1024 / 3 - 1024 : 228 * 1024 / 2 - 1024;
+    int64_t SR, RPF;
+    int NS;
+    const int64_t half = G * (((per_cta + 1) / 2 + G - 1) / G);
+    if (smem_for(2, half, 2 * half) <= two_cta_limit) {
+        // the CTA's whole share fits in two stages: all of it is requested at
+        // once, one memory round trip per CTA
+        SR = half;
+        NS = 2;
+        RPF = 2 * half;
+    } else {
+        // rows per stage: ~32 KB of weights, a multiple of the row groups, and
+        // small enough that every SM gets work on small problems
+        const int64_t rb = std::max<int64_t>(1, 32768 / (G * R));
+        SR = G * rb;
+        if (per_cta < SR) SR = std::max<int64_t>(G, ((per_cta + G - 1) / G) * G);
+        // partial-sum window: ~24 KB, whole stages, no more than a CTA's rows
+        RPF = std::max<int64_t>(SR, (6144 / PU) / SR * SR);
+        RPF = std::min<int64_t>(RPF, std::max<int64_t>(SR, (per_cta + SR - 1) / SR * SR));
+        NS = 8;
+        while (NS > 2 && smem_for(NS, SR, RPF) > two_cta_limit) --NS;
+        if (smem_for(NS, SR, RPF) > two_cta_limit) {  // one CTA per SM, up to 8 stages
+            NS = 8;
+            while (NS > 2 && smem_for(NS, SR, RPF) > 200 * 1024) --NS;
+        }
+    }
+    const int SB = (int)(((SR * R + 32) + 127) & ~(int64_t)127);
     const int64_t nstage_total = (M + SR - 1) / SR;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(nstage_total, ctas_target));
-    const size_t smem =
-        (size_t)((((16 * NS + 16 + part_bytes + 127) & ~(size_t)127) + 4 * (g.k + uk) + 127) & ~(size_t)127) +
-        (size_t)NS * SB;
+    const size_t smem = smem_for(NS, SR, RPF);
     if (smem > 200 * 1024) return cudaErrorNotSupported;
 
     GemvParams p;
