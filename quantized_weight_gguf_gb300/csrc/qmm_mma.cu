@@ -271,7 +271,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // Two groups of 8 dequant warps take alternate k-steps; an A stage (KA = 4
     // k-steps) is done when both groups have arrived.
     constexpr int kGroups = 2;
-    constexpr int kFullACount = kDeqWarps;
+    // Q4_K raw tiles: one group fills a whole stage; otherwise both groups
+    constexpr int kFullACount = kRaw ? kDeqWarps / kGroups : kDeqWarps;
     static_assert(KA % kGroups == 0, "every group needs a k-step in every A stage");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -337,7 +338,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
         for (int s = 0; s < kNR; ++s) {
             mbar_init(rawFull(s), 1);
-            mbar_init(rawEmpty(s), kDeqWarps);
+            mbar_init(rawEmpty(s), kDeqWarps / kGroups);  // the group that decodes it
         }
         mbar_init(accFull, 1);
         mbar_init(accEmpty, kDeqWarps);
@@ -561,42 +562,65 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             const Tile t = tile_of(u);
             const int KSu = nks(t);
             if constexpr (kRaw) {
-                // per super-block b (one A stage): thread (r, h) of group g decodes
-                // half h of row r's 64-weight chunks c = g and g + 2
+                // Super-block b is one A stage. Group g takes the super-blocks
+                // whose global index has parity g, so the two groups run out of
+                // phase: thread (r, h) decodes half h of all four 64-weight
+                // chunks of row r.
                 const bool row_ok = t.m0 + r < p.j1;
                 const int NSBLK = KSu / 4;  // k % 256 == 0: whole super-blocks
-                for (int b = 0; b < NSBLK && !failed; ++b, ++rcount) {
-                    const int rs = rcount % kNR;
-                    uint32_t hw0[16], hw1[16];
-                    const bool ok = wait_abortable(rawFull(rs), (rcount / kNR) & 1, abort_flag);
+                const int rbase = rcount;   // global index of the unit's first super-block
+                for (int b = (g - rbase) & 1; b < NSBLK && !failed; b += 2) {
+                    const int rc = rbase + b;
+                    const int rs = rc % kNR;
+                    const bool ok = wait_abortable(rawFull(rs), (rc / kNR) & 1, abort_flag);
                     if (__all_sync(0xFFFFFFFFu, ok) == 0) {
                         record_error(p.err, DERR_MMA_A);
                         failed = true;
                         *abort_flag = 1;
                         break;
                     }
+                    uint4 hdr = make_uint4(0u, 0u, 0u, 0u), qv[4];
+                    const uint32_t rb = W0 + rs * kRawBytes + (uint32_t)r * 144u;
                     if (row_ok) {
-                        const uint32_t rb = W0 + rs * kRawBytes + (uint32_t)r * 144u;
-                        const uint4 hdr = lds128(rb);
-                        const uint4 q0 = lds128(rb + 16u + 32u * g + 16u * h);
-                        const uint4 q1 = lds128(rb + 16u + 32u * (g + 2) + 16u * h);
-                        q4k_half_chunk_to_half(hdr, q0, g, hw0);
-                        q4k_half_chunk_to_half(hdr, q1, g + 2, hw1);
-                    } else {
+                        hdr = lds128(rb);
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) hw0[e] = hw1[e] = 0u;
+                        for (int c = 0; c < 4; ++c) qv[c] = lds128(rb + 16u + 32u * c + 16u * h);
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(rawEmpty(rs));  // raw tile read
-                    // weights 16h + 0..15 -> columns 8h..8h+7; 32 + 16h + 0..15 -> 16 + 8h..
-                    const uint32_t ta0 = a_slot(4 * b + g);
-                    tmem_st8(ta0 + 8u * h, hw0);
-                    tmem_st8(ta0 + 16u + 8u * h, hw0 + 8);
-                    const uint32_t ta1 = a_slot(4 * b + g + 2);
-                    tmem_st8(ta1 + 8u * h, hw1);
-                    tmem_st8(ta1 + 16u + 8u * h, hw1 + 8);
-                    a_done(4 * b + g + 2);
+                    // the stage's slot, once the MMAs that read it last are done
+                    const int st = abase + b, slot = st % NA;
+                    if (st >= NA) {
+                        const bool ok2 =
+                            wait_abortable(emptyA(slot), ((st / NA) + 1) & 1, abort_flag);
+                        if (__all_sync(0xFFFFFFFFu, ok2) == 0) {
+                            record_error(p.err, DERR_MMA_EMPTY);
+                            failed = true;
+                            *abort_flag = 1;
+                        }
+                        tc_fence_after();
+                    }
+                    const uint32_t ta = tlane + (uint32_t)(C::kACol0 + slot * C::kAStageCols);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t hw[16];
+                        if (row_ok) {
+                            q4k_half_chunk_to_half(hdr, qv[c], c, hw);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) hw[e] = 0u;
+                        }
+                        // chunk c = k-step c of the stage: weights 16h + 0..15 ->
+                        // columns 8h..8h+7, 32 + 16h + 0..15 -> 16 + 8h..
+                        tmem_st8(ta + 32u * c + 8u * h, hw);
+                        tmem_st8(ta + 32u * c + 16u + 8u * h, hw + 8);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0 && !failed) mbar_arrive(fullA(slot));
                 }
+                rcount = rbase + NSBLK;
             } else {
                 const bool lo_part = MODE == 3 && r >= 64;  // MODE 3: rows 64..127 hold W_lo
                 const int64_t j = t.m0 + (MODE == 3 ? (r & 63) : r);
