@@ -64,6 +64,8 @@ def _load():
             lib.oracle_dequant.argtypes = [ctypes.c_int, p, i64, i64, p]
             lib.oracle_matmul.restype = ctypes.c_int
             lib.oracle_matmul.argtypes = [ctypes.c_int, p, p, i64, i64, i64, p, p, p]
+            lib.oracle_matmul_back_input.restype = ctypes.c_int
+            lib.oracle_matmul_back_input.argtypes = [ctypes.c_int, p, p, i64, i64, i64, i64, p, p, p]
             lib.oracle_matmul_sampled.restype = ctypes.c_int
             lib.oracle_matmul_sampled.argtypes = [ctypes.c_int, p, p, i64, i64, i64, i64, p, p, p, p, p]
             _lib = lib
@@ -136,6 +138,35 @@ def matmul_sampled(fmt: str, w: np.ndarray, x: np.ndarray, k: int, n: int, t_idx
     if rc != 0:
         raise ValueError("oracle sampled matmul rejected its arguments")
     return y, s
+
+
+def matmul_back_input(fmt: str, w: np.ndarray, dy: np.ndarray, k: int, n: int,
+                      j_start: int = 0, j_end: int | None = None):
+    """(dx, S) of the backward with respect to the input over rows
+    [j_start, j_end): dx[i] = sum_j dy[j] w[j, i], S = sum_j |dy[j] w[j, i]|,
+    both f64 [k]."""
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    dy = np.ascontiguousarray(np.asarray(dy).reshape(-1), dtype=np.float32)
+    if dy.size != n:
+        raise ValueError("dy must have n entries")
+    j_end = n if j_end is None else j_end
+    dx = np.empty(k, np.float64)
+    s = np.empty(k, np.float64)
+    scratch = np.empty(max(k, 1), np.float32)
+    if _load().oracle_matmul_back_input(CODES[fmt], _ptr(w), _ptr(dy), k, n, j_start, j_end,
+                                        _ptr(dx), _ptr(s), _ptr(scratch)) != 0:
+        raise ValueError("oracle backward-input rejected its arguments")
+    return dx, s
+
+
+def matmul_back_input_blas(fmt: str, w: np.ndarray, dy: np.ndarray, k: int, n: int,
+                           j_start: int = 0, j_end: int | None = None):
+    """Same (dx, S) as matmul_back_input, by numpy's f64 product over the
+    oracle's own fp32 weights (for full-size checks)."""
+    j_end = n if j_end is None else j_end
+    deq = dequant(fmt, w, k, n)[j_start:j_end].astype(np.float64)
+    d = np.asarray(dy, np.float64).reshape(-1)[j_start:j_end]
+    return d @ deq, np.abs(d) @ np.abs(deq)
 
 
 def tiled(y_ref: np.ndarray, s_ref: np.ndarray, j_start: int, j_end: int, accumulate: bool,

@@ -23,6 +23,12 @@
  *    scale packing, Q6_K ql/qh/scales) is the standard ggml block layout,
  *    which the pages name but do not print; it is written out below.
  *
+ *  - rullama src/backend/dispatch/mod.rs, `MatmulBackInputParams` and the
+ *    `matmul_q*_backward_input` dispatchers and parity tests: the gradient
+ *    with respect to the input, dx[i] = sum_j w[j][i] * dy[j] for the rows
+ *    j in [j_start, j_end) (the sum axis is tiled), written on the first
+ *    tile and added on the others; dy has n entries, dx has k.
+ *
  * Parity pins live in tests/test_oracle_pins.py (hand-packed blocks with
  * known values, closed-form sizes, exhaustive f16 decode against numpy,
  * identity / one-hot products, brute-force tiny products).
@@ -238,6 +244,32 @@ int oracle_matmul_sampled(int fmt, const uint8_t *w, const float *x, int64_t k, 
         }
         y[c] = acc;
         s[c] = mag;
+    }
+    return 0;
+}
+
+/* Backward with respect to the input (transposed product over a row range):
+ * dx[i] = sum_{j in [j0, j1)} dy[j] * w[j][i] and s[i] = sum |dy[j] * w[j][i]|,
+ * both accumulated in double; dy has n entries, dx and s have k.
+ * wrow_scratch holds k floats. */
+int oracle_matmul_back_input(int fmt, const uint8_t *w, const float *dy, int64_t k, int64_t n,
+                             int64_t j0, int64_t j1, double *dx, double *s,
+                             float *wrow_scratch)
+{
+    int64_t rb = oracle_row_bytes(fmt, k);
+    if (rb == 0 && k != 0) return -1;
+    if (j0 < 0 || j1 < j0 || j1 > n) return -1;
+    for (int64_t i = 0; i < k; ++i) {
+        dx[i] = 0.0;
+        s[i] = 0.0;
+    }
+    for (int64_t j = j0; j < j1; ++j) {
+        if (oracle_dequant_row(fmt, w + j * rb, k, wrow_scratch)) return -1;
+        for (int64_t i = 0; i < k; ++i) {
+            double p = (double)dy[j] * (double)wrow_scratch[i];
+            dx[i] += p;
+            s[i] += fabs(p);
+        }
     }
     return 0;
 }

@@ -397,3 +397,73 @@ def test_tiled_semantics():
     assert np.array_equal(s[:, 2:4], 101 * np.ones((2, 2)))
     y, s = oracle.tiled(y_ref, s_ref, 0, 6, False, y_in)
     assert np.array_equal(y, y_ref)
+
+
+# ------------------------------------------------- backward w.r.t. input ----
+
+def test_back_input_brute_force_tiny_q4_0():
+    """Hand-listed dx for the 2-row Q4_0 weights of the forward brute-force pin:
+    dx[i] = 3 * w0[i] - 2 * w1[i] (row 1 has d = -0.25 and zero high nibbles)."""
+    w = np.zeros(36, np.uint8)
+    w[0:2] = [0x00, 0x3C]                    # d = 1
+    w[2:18] = [(i % 16) | (((i + 3) % 16) << 4) for i in range(16)]
+    w[18:20] = [0x00, 0xB4]                  # d = -0.25
+    w[20:36] = [15 - i for i in range(16)]
+    dx, s = oracle.matmul_back_input("q4_0", w, np.array([3.0, -2.0], np.float32), 32, 2)
+    want = []
+    for i in range(32):
+        w0 = (i - 8) if i < 16 else (((i - 16 + 3) % 16) - 8)
+        w1 = Fraction(-1, 4) * ((15 - i - 8) if i < 16 else (0 - 8))
+        want.append(3 * w0 - 2 * w1)
+    assert [Fraction(v) for v in dx] == want
+    assert s[0] == abs(3 * (0 - 8)) + abs(2 * Fraction(-1, 4) * (15 - 8))
+
+
+@pytest.mark.parametrize("fmt,k,n", [("q4_0", 64, 7), ("q4_k", 512, 5), ("q6_k", 256, 6),
+                                     ("bf16", 40, 9), ("f16", 24, 3)])
+def test_back_input_one_hot_dy_picks_a_row(fmt, k, n):
+    """dy = e_j gives dx = row j of the dequantized weights, exactly."""
+    rng = np.random.default_rng(11)
+    w = qmm_synth.gen_weights(fmt, k, n, rng)
+    deq = oracle.dequant(fmt, w, k, n)
+    for j in (0, n - 1, n // 2):
+        dy = np.zeros(n, np.float32)
+        dy[j] = 1.0
+        dx, s = oracle.matmul_back_input(fmt, w, dy, k, n)
+        assert np.array_equal(dx, deq[j].astype(np.float64))
+        assert np.array_equal(s, np.abs(deq[j]).astype(np.float64))
+
+
+@pytest.mark.parametrize("fmt,k,n", [("q4_k", 512, 33), ("q6_k", 512, 17), ("q4_0", 96, 20)])
+def test_back_input_is_the_adjoint_of_the_forward(fmt, k, n):
+    """dy . (W x) == x . (W^T dy): ties the transposed product to the pinned
+    forward one (a swapped index or operand breaks it)."""
+    rng = np.random.default_rng(5)
+    w = qmm_synth.gen_weights(fmt, k, n, rng)
+    x = rng.standard_normal(k).astype(np.float32)
+    dy = rng.standard_normal(n).astype(np.float32)
+    y, _ = oracle.matmul(fmt, w, x, k, n)
+    dx, _ = oracle.matmul_back_input(fmt, w, dy, k, n)
+    lhs = float(np.dot(dy.astype(np.float64), y[0]))
+    rhs = float(np.dot(x.astype(np.float64), dx))
+    assert abs(lhs - rhs) <= 1e-12 * max(1.0, float(np.abs(dy) @ np.abs(y[0])))
+
+
+def test_back_input_sum_axis_tiles_add_up():
+    """Tiles [0, m) and [m, n) of the sum axis add to the whole; an empty tile
+    is zero; the blas variant agrees with the loop oracle."""
+    fmt, k, n = "q6_k", 256, 40
+    rng = np.random.default_rng(9)
+    w = qmm_synth.gen_weights(fmt, k, n, rng)
+    dy = rng.standard_normal(n).astype(np.float32)
+    full, sf = oracle.matmul_back_input(fmt, w, dy, k, n)
+    a, sa = oracle.matmul_back_input(fmt, w, dy, k, n, 0, 13)
+    b, sb = oracle.matmul_back_input(fmt, w, dy, k, n, 13, n)
+    np.testing.assert_allclose(a + b, full, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(sa + sb, sf, rtol=1e-12, atol=1e-12)
+    z, sz = oracle.matmul_back_input(fmt, w, dy, k, n, 7, 7)
+    assert not z.any() and not sz.any()
+    c, sc = oracle.matmul_back_input_blas(fmt, w, dy, k, n, 13, n)
+    np.testing.assert_allclose(c, b, rtol=1e-12, atol=1e-12)
+    with pytest.raises(ValueError):
+        oracle.matmul_back_input(fmt, w, dy, k, n, 10, 5)
