@@ -153,6 +153,30 @@ int qmm_select_path(const qmm_args *a);
  * synchronizes the stream before reading y. */
 int qmm_matmul_host(const qmm_args *a, void *dev_w, float *dev_x, float *dev_y);
 
+/* Backward of y = x @ W with respect to the input, for one vector (rullama
+ * src/backend/dispatch/mod.rs, `MatmulBackInputParams` and the
+ * `matmul_q*_backward_input` dispatchers):
+ *     dx[i] (+)= sum_{j in [j_start, j_end)} dy[j] * w[j][i],  i in [0, k)
+ * The row range tiles the SUM axis (the reference's tiling of the vocabulary
+ * head): the first tile writes dx (accumulate = 0), later tiles add to it
+ * (accumulate = 1); j_start == j_end == 0 means all n rows, and an empty
+ * range writes zeros (or leaves dx when accumulating). Fields: a->x is dy
+ * (device, n floats), a->y is dx (device, k floats), a->n_tokens must be 1,
+ * a->path and a->flags must be 0; fmt, w, w_len, k, n, workspace, stream as
+ * for qmm_matmul_ex. Units of k are 32 weights (8 for 16-bit formats) and at
+ * most 256 per row: k <= 8192 for the block formats, k <= 2048 for BF16/F16
+ * (QMM_ERR_UNSUPPORTED beyond). The result is the same on every call (the
+ * per-CTA partial sums are added in a fixed order). Stream-ordered, no
+ * host synchronization; acceptance bar as for the forward product, with
+ * S = sum_j |dy[j] w[j][i]|. */
+int qmm_matmul_backward_input(const qmm_args *a);
+
+/* Device scratch bytes qmm_matmul_backward_input needs for *a (one fp32
+ * partial dx per CTA: grid * k * 4; 0 for an empty call or invalid
+ * arguments). With a->workspace NULL the library's own grow-only buffer is
+ * used. Host only (reads the device's SM count). */
+size_t qmm_backward_input_workspace_bytes(const qmm_args *a);
+
 /* Standalone dequantization: out[j][i] = the fp32 value of weight i of row
  * j, bit-identical to the exact value rounded once to fp32 (only Q4_K's
  * d*sc*q - dmin*m rounds; every other product is exact). out is device

@@ -25,7 +25,8 @@ STATUS = {0: "QMM_OK", 1: "QMM_ERR_FORMAT", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_SIZE
           8: "QMM_ERR_DEVICE_TIMEOUT", 9: "QMM_ERR_WORKSPACE", 10: "QMM_ERR_UNSUPPORTED"}
 EXPORTS = ("qmm_weight_bytes", "qmm_matmul", "qmm_set_stream", "qmm_matmul_ex",
            "qmm_workspace_bytes", "qmm_select_path", "qmm_matmul_host", "qmm_dequant",
-           "qmm_device_status", "qmm_last_error", "qmm_version", "qmm_matmul_noalloc")
+           "qmm_device_status", "qmm_last_error", "qmm_version", "qmm_matmul_noalloc",
+           "qmm_matmul_backward_input", "qmm_backward_input_workspace_bytes")
 
 
 class QmmError(RuntimeError):
@@ -70,6 +71,8 @@ def load(path: str = LIB_PATH):
         "qmm_last_error": (ctypes.c_char_p, []),
         "qmm_version": (i, []),
         "qmm_matmul_noalloc": (i, [pa]),
+        "qmm_matmul_backward_input": (i, [pa]),
+        "qmm_backward_input_workspace_bytes": (sz, [pa]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -137,6 +140,14 @@ def qmm_matmul_noalloc(args: qmm_args) -> int:
     return _check(load().qmm_matmul_noalloc(ctypes.byref(args)))
 
 
+def qmm_matmul_backward_input(args: qmm_args) -> int:
+    return _check(load().qmm_matmul_backward_input(ctypes.byref(args)))
+
+
+def qmm_backward_input_workspace_bytes(args: qmm_args) -> int:
+    return load().qmm_backward_input_workspace_bytes(ctypes.byref(args))
+
+
 def qmm_workspace_bytes(args: qmm_args) -> int:
     return load().qmm_workspace_bytes(ctypes.byref(args))
 
@@ -188,6 +199,20 @@ def matmul(fmt, w, x, k: int, n: int, *, y=None, j_start=0, j_end=0, accumulate=
         a.workspace_bytes = need
     qmm_matmul_ex(a)
     return y
+
+
+def matmul_backward_input(fmt, w, dy, k: int, n: int, *, dx=None, j_start=0, j_end=0,
+                          accumulate=False, stream=None):
+    """dx = W^T dy over the rows [j_start, j_end) for torch CUDA tensors: w
+    uint8 packed bytes, dy float32 [n]. Returns dx float32 [k] (the given dx
+    when passed). Scratch is the library's own buffer."""
+    import torch
+    if dx is None:
+        dx = torch.empty(k, dtype=torch.float32, device=dy.device)
+    a = make_args(fmt, w, dy, dx, k, n, 1, w_len=w.numel() * w.element_size(), j_start=j_start,
+                  j_end=j_end, accumulate=accumulate, stream=stream)
+    qmm_matmul_backward_input(a)
+    return dx
 
 
 def dequant(fmt, w, k: int, n: int, stream=None):

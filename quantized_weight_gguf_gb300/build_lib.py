@@ -14,7 +14,8 @@ CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqmm.so")
-SOURCES = ["qmm_api.cu", "qmm_gemv.cu", "qmm_mma.cu", "qmm_dequant.cu", "qmm_noalloc.cu"]
+SOURCES = ["qmm_api.cu", "qmm_gemv.cu", "qmm_mma.cu", "qmm_dequant.cu", "qmm_noalloc.cu",
+           "qmm_back_input.cu"]
 GENCODE = "arch=compute_103a,code=sm_103a"
 
 

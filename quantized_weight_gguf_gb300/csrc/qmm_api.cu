@@ -144,6 +144,26 @@ int cuda_fail(cudaError_t e, const char *what) {
     return fail(QMM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// The library-owned grow-only scratch of the current device, at least `need` bytes.
+int library_workspace(size_t need, void **out) {
+    int d = 0;
+    cudaGetDevice(&d);
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_ws_bytes[d] < need) {
+        // grow-only; the old buffer may still be in use by queued work
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e, "workspace grow sync");
+        if (g_ws[d]) cudaFree(g_ws[d]);
+        g_ws[d] = nullptr;
+        g_ws_bytes[d] = 0;
+        e = cudaMalloc(&g_ws[d], need);
+        if (e != cudaSuccess) return cuda_fail(e, "workspace cudaMalloc");
+        g_ws_bytes[d] = need;
+    }
+    *out = g_ws[d];
+    return QMM_OK;
+}
+
 int run(const qmm_args *a) {
     int64_t j0, j1, rb;
     int st = validate(a, &j0, &j1, &rb, true);
@@ -188,21 +208,8 @@ int run(const qmm_args *a) {
         if (reinterpret_cast<uintptr_t>(ws) & 255u)
             return fail(QMM_ERR_ALIGN, "workspace must be 256-byte aligned");
     } else {
-        int d = 0;
-        cudaGetDevice(&d);
-        std::lock_guard<std::mutex> lk(g_mu);
-        if (g_ws_bytes[d] < need) {
-            // grow-only; the old buffer may still be in use by queued work
-            cudaError_t e = cudaDeviceSynchronize();
-            if (e != cudaSuccess) return cuda_fail(e, "workspace grow sync");
-            if (g_ws[d]) cudaFree(g_ws[d]);
-            g_ws[d] = nullptr;
-            g_ws_bytes[d] = 0;
-            e = cudaMalloc(&g_ws[d], need);
-            if (e != cudaSuccess) return cuda_fail(e, "workspace cudaMalloc");
-            g_ws_bytes[d] = need;
-        }
-        ws = g_ws[d];
+        st = library_workspace(need, &ws);
+        if (st != QMM_OK) return st;
     }
     qmm::MmaLaunch m;
     m.fmt = a->fmt;
@@ -301,6 +308,67 @@ int qmm_matmul_host(const qmm_args *a, void *dev_w, float *dev_x, float *dev_y) 
     if ((e = cudaMemcpyAsync(a->y, dev_y, yb, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
         return cuda_fail(e, "copy y to host");
     return QMM_OK;
+}
+
+int qmm_matmul_backward_input(const qmm_args *a) {
+    t_err[0] = 0;
+    if (!a) return fail(QMM_ERR_NULL, "args is NULL");
+    if (a->n_tokens != 1)
+        return fail(QMM_ERR_SHAPE, "backward-input takes one dy vector (n_tokens %lld != 1)",
+                    (long long)a->n_tokens);
+    if (a->flags != 0) return fail(QMM_ERR_SHAPE, "backward-input takes no flags");
+    int64_t j0, j1, rb;
+    // x = dy (n entries), y = dx (k entries): the pointer checks of validate()
+    // hold for the swapped lengths too
+    int st = validate(a, &j0, &j1, &rb, true);
+    if (st != QMM_OK) return st;
+    if (a->k == 0) return QMM_OK;
+    if (!a->y) return fail(QMM_ERR_NULL, "dx (y) is NULL");
+    if (a->n > 0 && (!a->w || !a->x)) return fail(QMM_ERR_NULL, "w or dy (x) is NULL");
+    if (!qmm::back_input_supports(a->fmt, a->k))
+        return fail(QMM_ERR_UNSUPPORTED, "backward-input cannot take %s with k=%lld",
+                    fmt_name(a->fmt), (long long)a->k);
+    qmm::DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != QMM_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(a->stream);
+    if (j1 <= j0) {  // empty sum: dx = 0, or unchanged when accumulating
+        if (a->accumulate) return QMM_OK;
+        cudaError_t e = qmm::launch_zero_cols(a->y, 1, a->k, 0, a->k, s);
+        return e == cudaSuccess ? QMM_OK : cuda_fail(e, "zero-fill launch");
+    }
+    const size_t need = qmm::back_input_workspace_bytes(a->fmt, a->k, a->n, j0, j1, *dev);
+    void *ws = a->workspace;
+    if (ws) {
+        if (a->workspace_bytes < need)
+            return fail(QMM_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", a->workspace_bytes,
+                        need);
+        if (reinterpret_cast<uintptr_t>(ws) & 255u)
+            return fail(QMM_ERR_ALIGN, "workspace must be 256-byte aligned");
+    } else {
+        st = library_workspace(need, &ws);
+        if (st != QMM_OK) return st;
+    }
+    qmm::BackLaunch b;
+    b.fmt = a->fmt;
+    b.w = static_cast<const uint8_t *>(a->w);
+    b.dy = a->x;
+    b.dx = a->y;
+    b.k = a->k; b.n = a->n; b.row_bytes = rb;
+    b.j0 = j0; b.j1 = j1;
+    b.accumulate = a->accumulate;
+    b.workspace = ws;
+    cudaError_t e = qmm::launch_back_input(b, *dev, s);
+    return e == cudaSuccess ? QMM_OK : cuda_fail(e, "backward-input launch");
+}
+
+size_t qmm_backward_input_workspace_bytes(const qmm_args *a) {
+    int64_t j0, j1, rb;
+    if (!a || a->n_tokens != 1 || validate(a, &j0, &j1, &rb, false) != QMM_OK) return 0;
+    if (a->k == 0 || j1 <= j0 || !qmm::back_input_supports(a->fmt, a->k)) return 0;
+    qmm::DeviceInfo *dev = nullptr;
+    if (device_info(&dev) != QMM_OK) return 0;
+    return qmm::back_input_workspace_bytes(a->fmt, a->k, a->n, j0, j1, *dev);
 }
 
 int qmm_dequant(int fmt, const void *w, int64_t k, int64_t n, float *out, void *stream) {

@@ -1,0 +1,458 @@
+// qmm_back_input.cu -- backward of y = x @ W with respect to the input, one
+// vector: dx[i] (+)= sum_{j in [j0, j1)} dy[j] * w[j][i] (the transposed
+// product; the row range tiles the sum axis).
+//
+// Same weight stream as the GEMV: each CTA owns a contiguous range of rows,
+// i.e. a contiguous byte range of W, which one producer lane streams through a
+// ring of shared-memory stages with 1-D bulk copies. Each of the 256 consumer
+// threads owns a fixed unit of k (8 weights for 16-bit formats, one 32-weight
+// block / sub-block / quarter-half otherwise) and keeps that unit's dx partial
+// sums in registers; for every row it decodes the unit and adds dy[j] times
+// the weights. Codes stay exact: a byte permute builds 0.5 + q/256, so a unit
+// accumulates sum_j a_j (0.5 + q/256) with a_j = dy[j] * scale, plus the
+// per-unit sums of a_j that remove the carrier and the zero point / min
+// (e.g. Q4_K: dx = 256 acc - 128 sum a - sum dy dmin m).
+// At the end the row groups of a CTA are summed in shared memory and the CTA
+// writes its partial dx; a second small kernel adds the partials of all CTAs in
+// a fixed order (deterministic) into dx.
+#include "qmm_device.cuh"
+#include "qmm_internal.h"
+
+#include <algorithm>
+#include <mutex>
+
+namespace qmm {
+
+namespace {
+
+constexpr int kBwWarps = 8;
+constexpr int kBwCons = kBwWarps * 32;
+constexpr int kBwThreads = kBwCons + 32;
+
+struct BackParams {
+    const uint8_t *w;
+    const float *dy;
+    float *part;     // [grid][k] partial dx of each CTA
+    int64_t k, row_bytes, w_total;
+    int64_t j0;
+    int64_t rows_base;
+    int rows_rem;
+    int U;    // units per row
+    int G;    // row groups (each thread takes rows g, g + G, ...)
+    int SR;   // rows per stage
+    int SB;   // bytes per stage buffer (multiple of 128)
+    int NS;   // stage buffers
+    int dy_cap;  // rows of dy staged (>= rows per CTA)
+    unsigned int *err;
+};
+
+template <int FMT>
+struct BUnitK {
+    static constexpr int value = (FMT == F_BF16 || FMT == F_F16) ? 8 : 32;
+};
+
+template <int FMT>
+struct BAcc {
+    float a[BUnitK<FMT>::value];
+    float s0, s1, s2, s3;  // carrier sums (per scale group) and Q4_K's min term
+};
+
+__device__ __forceinline__ uint32_t bw_bfe(uint32_t a, uint32_t pos, uint32_t len) {
+    uint32_t d;
+    asm("bfe.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(pos), "r"(len));
+    return d;
+}
+
+// acc += dyj * (unit u of the row at shared address rowa)
+template <int FMT>
+__device__ __forceinline__ void unit_axpy(uint32_t rowa, int u, float dyj, BAcc<FMT> &st) {
+    if (FMT == F_BF16 || FMT == F_F16) {
+        const uint4 v = lds128(rowa + 16u * u);
+        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+        const float2 dd = make_float2(dyj, dyj);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 wf;
+            if (FMT == F_BF16) {
+                wf.x = __uint_as_float(wd[i] << 16);
+                wf.y = __uint_as_float(wd[i] & 0xFFFF0000u);
+            } else {
+                wf = __half22float2(*reinterpret_cast<const __half2 *>(&wd[i]));
+            }
+            const float2 r = ffma2(wf, dd, make_float2(st.a[2 * i], st.a[2 * i + 1]));
+            st.a[2 * i] = r.x;
+            st.a[2 * i + 1] = r.y;
+        }
+    } else if (FMT == F_Q4_0) {
+        const uint32_t base = rowa + 18u * u;
+        const float a = dyj * f16_bits_to_f32(lds16(base));
+        uint32_t qw[4];
+        lds_words_a2<4>(base + 2, qw);
+        const float2 aa = make_float2(a, a);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = qw[i] & 0x0F0F0F0Fu, hi = (qw[i] >> 4) & 0x0F0F0F0Fu;
+            // element 4i + b: low nibble of byte 4i + b; element 16 + 4i + b: its high nibble
+            float2 r;
+            r = ffma2(make_float2(byte_half_plus<0>(lo), byte_half_plus<1>(lo)), aa,
+                      make_float2(st.a[4 * i], st.a[4 * i + 1]));
+            st.a[4 * i] = r.x; st.a[4 * i + 1] = r.y;
+            r = ffma2(make_float2(byte_half_plus<2>(lo), byte_half_plus<3>(lo)), aa,
+                      make_float2(st.a[4 * i + 2], st.a[4 * i + 3]));
+            st.a[4 * i + 2] = r.x; st.a[4 * i + 3] = r.y;
+            r = ffma2(make_float2(byte_half_plus<0>(hi), byte_half_plus<1>(hi)), aa,
+                      make_float2(st.a[16 + 4 * i], st.a[16 + 4 * i + 1]));
+            st.a[16 + 4 * i] = r.x; st.a[16 + 4 * i + 1] = r.y;
+            r = ffma2(make_float2(byte_half_plus<2>(hi), byte_half_plus<3>(hi)), aa,
+                      make_float2(st.a[16 + 4 * i + 2], st.a[16 + 4 * i + 3]));
+            st.a[16 + 4 * i + 2] = r.x; st.a[16 + 4 * i + 3] = r.y;
+        }
+        st.s0 += a;
+    } else if (FMT == F_Q4_K) {
+        // unit u = sub-block s of super-block b; its 32 codes are the low
+        // (s even) or high (s odd) nibbles of quant bytes 32 (s / 2) ..
+        const int b = u >> 3, s = u & 7, c = s >> 1;
+        const uint32_t sb = rowa + 144u * b;
+        const uint4 hdr = lds128(sb);
+        const uint4 q0 = lds128(sb + 16u + 32u * c);
+        const uint4 q1 = lds128(sb + 32u + 32u * c);
+        uint32_t sc, m;
+        if (s < 4) {
+            sc = bw_bfe(hdr.y, 8 * s, 6);
+            m = bw_bfe(hdr.z, 8 * s, 6);
+        } else {
+            const uint32_t t = 8 * (s - 4);
+            sc = bw_bfe(hdr.w, t, 4) | (bw_bfe(hdr.y, t + 6, 2) << 4);
+            m = bw_bfe(hdr.w, t + 4, 4) | (bw_bfe(hdr.z, t + 6, 2) << 4);
+        }
+        const float a = dyj * (f16_bits_to_f32(hdr.x & 0xFFFFu) * (float)sc);
+        const float bm = dyj * (f16_bits_to_f32(hdr.x >> 16) * (float)m);
+        const uint32_t sh = (s & 1) ? 4u : 0u;
+        const uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        const float2 aa = make_float2(a, a);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t nib = (wd[i] >> sh) & 0x0F0F0F0Fu;
+            float2 r;
+            r = ffma2(make_float2(byte_half_plus<0>(nib), byte_half_plus<1>(nib)), aa,
+                      make_float2(st.a[4 * i], st.a[4 * i + 1]));
+            st.a[4 * i] = r.x; st.a[4 * i + 1] = r.y;
+            r = ffma2(make_float2(byte_half_plus<2>(nib), byte_half_plus<3>(nib)), aa,
+                      make_float2(st.a[4 * i + 2], st.a[4 * i + 3]));
+            st.a[4 * i + 2] = r.x; st.a[4 * i + 3] = r.y;
+        }
+        st.s0 += a;
+        st.s1 += bm;
+    } else {  // F_Q6_K
+        // unit u: super-block b, half h, byte group gq; element 8 r + i is
+        // weight 128 h + 32 r + 8 gq + i, with scale scales[8 h + 2 r + gq / 2]
+        const int b = u >> 3, h = (u >> 2) & 1, gq = u & 3;
+        const uint32_t sb = rowa + 210u * b;
+        uint32_t A[2], B[2], H[2], S[2];
+        lds_words_a2<2>(sb + 64u * h + 8u * gq, A);
+        lds_words_a2<2>(sb + 64u * h + 32u + 8u * gq, B);
+        lds_words_a2<2>(sb + 128u + 32u * h + 8u * gq, H);
+        lds_words_a2<2>(sb + 192u + 8u * h, S);
+        const float dd = dyj * f16_bits_to_f32(lds16(sb + 208u));
+        float ar[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const uint32_t pos = 8u * (2u * (uint32_t)(r & 1) + (uint32_t)(gq >> 1));
+            int32_t scv;
+            asm("bfe.s32 %0, %1, %2, 8;" : "=r"(scv) : "r"(S[r >> 1]), "r"(pos));
+            ar[r] = dd * (float)scv;
+        }
+#pragma unroll
+        for (int wi = 0; wi < 2; ++wi) {
+            const uint32_t q[4] = {
+                (A[wi] & 0x0F0F0F0Fu) | ((H[wi] << 4) & 0x30303030u),
+                (B[wi] & 0x0F0F0F0Fu) | ((H[wi] << 2) & 0x30303030u),
+                ((A[wi] >> 4) & 0x0F0F0F0Fu) | (H[wi] & 0x30303030u),
+                ((B[wi] >> 4) & 0x0F0F0F0Fu) | ((H[wi] >> 2) & 0x30303030u)};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float2 aa = make_float2(ar[r], ar[r]);
+                const int e = 8 * r + 4 * wi;
+                float2 v;
+                v = ffma2(make_float2(byte_half_plus<0>(q[r]), byte_half_plus<1>(q[r])), aa,
+                          make_float2(st.a[e], st.a[e + 1]));
+                st.a[e] = v.x; st.a[e + 1] = v.y;
+                v = ffma2(make_float2(byte_half_plus<2>(q[r]), byte_half_plus<3>(q[r])), aa,
+                          make_float2(st.a[e + 2], st.a[e + 3]));
+                st.a[e + 2] = v.x; st.a[e + 3] = v.y;
+            }
+        }
+        st.s0 += ar[0];
+        st.s1 += ar[1];
+        st.s2 += ar[2];
+        st.s3 += ar[3];
+    }
+}
+
+// Final dx value of element e of unit u, and its k index.
+template <int FMT>
+__device__ __forceinline__ void unit_result(const BAcc<FMT> &st, int u, int e, float &v,
+                                            int64_t &kidx) {
+    if (FMT == F_BF16 || FMT == F_F16) {
+        v = st.a[e];
+        kidx = 8 * (int64_t)u + e;
+    } else if (FMT == F_Q4_0) {
+        // sum a (q - 8) = 256 sum a (0.5 + q/256) - 136 sum a
+        v = fmaf(256.0f, st.a[e], -136.0f * st.s0);
+        kidx = 32 * (int64_t)u + e;
+    } else if (FMT == F_Q4_K) {
+        // sum (a q - dy dm) = 256 sum a (0.5 + q/256) - 128 sum a - sum dy dm
+        v = fmaf(256.0f, st.a[e], -fmaf(128.0f, st.s0, st.s1));
+        kidx = 32 * (int64_t)u + e;
+    } else {
+        const int r = e >> 3, i = e & 7;
+        const float sr = r == 0 ? st.s0 : (r == 1 ? st.s1 : (r == 2 ? st.s2 : st.s3));
+        // sum a (q - 32) = 256 sum a (0.5 + q/256) - 160 sum a
+        v = fmaf(256.0f, st.a[e], -160.0f * sr);
+        const int b = u >> 3, h = (u >> 2) & 1, gq = u & 3;
+        kidx = 256 * (int64_t)b + 128 * h + 32 * r + 8 * gq + i;
+    }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kBwThreads, 2) back_input_kernel(const BackParams p) {
+    constexpr int UK = BUnitK<FMT>::value;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int NS = p.NS, SR = p.SR, SB = p.SB;
+    const uint32_t bar0 = smem_addr(smem);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 16 * NS);
+    float *dys = reinterpret_cast<float *>(smem + ((16 * NS + 16 + 127) & ~127));
+    const uint32_t stage_off =
+        (uint32_t)((((16 * NS + 16 + 127) & ~127) + 4 * p.dy_cap + 127) & ~127);
+    uint8_t *stages = smem + stage_off;
+    const uint32_t stage0 = bar0 + stage_off;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (NS + s); };
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int cta = blockIdx.x;
+    const int64_t r0 = p.j0 + (int64_t)cta * p.rows_base + (cta < p.rows_rem ? cta : p.rows_rem);
+    const int64_t nrows = p.rows_base + (cta < p.rows_rem ? 1 : 0);
+    const int nst = (int)((nrows + SR - 1) / SR);
+    const int64_t R = p.row_bytes;
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), kBwWarps);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kBwWarps) {
+        // ---------------- producer: one lane streams the weight bytes ----------------
+        if (lane != 0) return;
+        const int64_t lim = p.w_total & ~(int64_t)15;
+        int issued = 0;
+        for (int s = 0; s < nst; ++s) {
+            const int slot = s % NS;
+            if (s >= NS && !mbar_wait(empty(slot), ((s / NS) + 1) & 1)) {
+                record_error(p.err, DERR_GEMV_EMPTY);
+                *abort_flag = 1;
+                break;
+            }
+            if (*abort_flag) break;
+            const int64_t ra = r0 + (int64_t)s * SR;
+            const int64_t rb = min(ra + SR, r0 + nrows);
+            const int64_t A = ra * R, B = rb * R;
+            const int64_t a16 = A & ~(int64_t)15, b16 = (B + 15) & ~(int64_t)15;
+            const int64_t tend = min(b16, lim);
+            if (B > lim) {  // bytes after the last whole 16-byte chunk of W
+                for (int64_t q = max(a16, lim); q < B; ++q)
+                    stages[(int64_t)slot * SB + (q - a16)] = p.w[q];
+            }
+            const uint32_t tx = tend > a16 ? (uint32_t)(tend - a16) : 0u;
+            mbar_arrive_expect_tx(full(slot), tx);
+            if (tx) bulk_g2s(stage0 + (uint32_t)slot * SB, p.w + a16, tx, full(slot));
+            ++issued;
+        }
+        // no copy may land after this CTA exits
+        for (int s = max(0, issued - NS); s < issued; ++s)
+            if (!mbar_wait(full(s % NS), (s / NS) & 1)) record_error(p.err, DERR_TEARDOWN);
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    for (int64_t i = tid; i < nrows; i += kBwCons) dys[i] = __ldg(p.dy + r0 + i);
+    named_barrier(1, kBwCons);
+    const int U = p.U, G = p.G;
+    // thread -> (row group g, unit u); units beyond U (G * U < 256) idle
+    const int g = tid / U;
+    const int u = tid - g * U;
+    const bool active = g < G;
+    BAcc<FMT> st;
+#pragma unroll
+    for (int e = 0; e < UK; ++e) st.a[e] = 0.0f;
+    st.s0 = st.s1 = st.s2 = st.s3 = 0.0f;
+    bool failed = false;
+    for (int s = 0; s < nst; ++s) {
+        const int slot = s % NS;
+        if (!failed && !mbar_wait(full(slot), (s / NS) & 1)) {
+            failed = true;
+            *abort_flag = 1;
+            record_error(p.err, DERR_GEMV_FULL);
+        }
+        const int64_t ra = r0 + (int64_t)s * SR;
+        const int64_t rb = min(ra + SR, r0 + nrows);
+        const int rows_in = (int)(rb - ra);
+        const int64_t a16 = (ra * R) & ~(int64_t)15;
+        const uint32_t sbase = stage0 + (uint32_t)slot * SB;
+        if (!failed && active) {
+            for (int rr = g; rr < rows_in; rr += G) {
+                const uint32_t rowa = sbase + (uint32_t)((ra + rr) * R - a16);
+                unit_axpy<FMT>(rowa, u, dys[ra - r0 + rr], st);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(slot));
+    }
+    // row groups -> one partial per k index, through shared memory (the ring
+    // is idle: every stage has been consumed)
+    named_barrier(1, kBwCons);
+    float *red = reinterpret_cast<float *>(stages);  // [G][k]
+    const int64_t k = p.k;
+    if (active) {
+#pragma unroll
+        for (int e = 0; e < UK; ++e) {
+            float v;
+            int64_t ki;
+            unit_result<FMT>(st, u, e, v, ki);
+            red[(int64_t)g * k + ki] = v;
+        }
+    }
+    named_barrier(1, kBwCons);
+    float *out = p.part + (int64_t)cta * k;
+    for (int64_t i = tid; i < k; i += kBwCons) {
+        float v = 0.0f;
+        for (int gg = 0; gg < G; ++gg) v += red[(int64_t)gg * k + i];
+        out[i] = (failed || *abort_flag) ? 0.0f : v;
+    }
+}
+
+// dx[i] (+)= sum over CTAs c in order of part[c][i]
+__global__ void __launch_bounds__(256) back_input_sum_kernel(const float *__restrict__ part,
+                                                             int parts, int64_t k, float *dx,
+                                                             int accumulate) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < k;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        float v = accumulate ? dx[i] : 0.0f;
+        for (int c = 0; c < parts; ++c) v += __ldg(part + (int64_t)c * k + i);
+        dx[i] = v;
+    }
+}
+
+template <int FMT>
+cudaError_t launch_bw_t(const BackParams &p, int grid, size_t smem, cudaStream_t s) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(back_input_kernel<FMT>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    back_input_kernel<FMT><<<grid, kBwThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+int unit_k_of(int fmt) { return (fmt == F_BF16 || fmt == F_F16) ? 8 : 32; }
+
+}  // namespace
+
+bool back_input_supports(int fmt, int64_t k) {
+    if (fmt < F_BF16 || fmt > F_Q6_K || k <= 0) return false;
+    const int uk = unit_k_of(fmt);
+    return k % uk == 0 && k / uk <= kBwCons;
+}
+
+static int64_t bw_plan(int fmt, int64_t k, int64_t R, int64_t M, int sm_count, int *grid_out,
+                       int64_t *SR_out, int *NS_out, int *SB_out, size_t *smem_out,
+                       int *dy_cap_out) {
+    const int uk = unit_k_of(fmt);
+    const int U = (int)(k / uk);
+    const int G = kBwCons / U;
+    const int ctas_target = 2 * sm_count;
+    const int64_t per_cta = (M + ctas_target - 1) / ctas_target;
+    int64_t SR = std::max<int64_t>(G, 32768 / R / G * G);
+    if (per_cta < SR) SR = std::max<int64_t>(G, (per_cta + G - 1) / G * G);
+    const int SB = (int)(((SR * R + 32) + 127) & ~(int64_t)127);
+    const int64_t nstage_total = (M + SR - 1) / SR;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(nstage_total, ctas_target));
+    const int64_t rows_max = (M + grid - 1) / grid;
+    const int dy_cap = (int)rows_max;
+    const size_t fixed = (size_t)(((16 * 8 + 16 + 127) & ~127) + 4 * dy_cap + 127) & ~(size_t)127;
+    // the reduction reuses the ring: it must hold G x k floats
+    const size_t red = (size_t)4 * G * k;
+    int NS = 2;
+    while (NS < 8 && fixed + (size_t)(NS + 1) * SB <= 110 * 1024) ++NS;
+    while ((size_t)NS * SB < red && NS < 16) ++NS;
+    *grid_out = grid;
+    *SR_out = SR;
+    *NS_out = NS;
+    *SB_out = SB;
+    *dy_cap_out = dy_cap;
+    *smem_out = fixed + (size_t)NS * SB;
+    return (int64_t)grid * k * 4;
+}
+
+size_t back_input_workspace_bytes(int fmt, int64_t k, int64_t n, int64_t j0, int64_t j1,
+                                  const DeviceInfo &dev) {
+    if (!back_input_supports(fmt, k) || j1 <= j0) return 0;
+    int grid, NS, SB, dy_cap;
+    int64_t SR;
+    size_t smem;
+    const int64_t R = (fmt == F_BF16 || fmt == F_F16) ? 2 * k
+                      : fmt == F_Q4_0 ? (k / 32) * 18
+                      : fmt == F_Q4_K ? (k / 256) * 144 : (k / 256) * 210;
+    (void)n;
+    return (size_t)bw_plan(fmt, k, R, j1 - j0, dev.sm_count, &grid, &SR, &NS, &SB, &smem, &dy_cap);
+}
+
+cudaError_t launch_back_input(const BackLaunch &b, const DeviceInfo &dev, cudaStream_t s) {
+    if (!back_input_supports(b.fmt, b.k)) return cudaErrorNotSupported;
+    const int64_t M = b.j1 - b.j0;
+    if (M <= 0) return cudaSuccess;
+    int grid, NS, SB, dy_cap;
+    int64_t SR;
+    size_t smem;
+    bw_plan(b.fmt, b.k, b.row_bytes, M, dev.sm_count, &grid, &SR, &NS, &SB, &smem, &dy_cap);
+    if (smem > 200 * 1024) return cudaErrorNotSupported;
+    BackParams p;
+    p.w = b.w;
+    p.dy = b.dy;
+    p.part = static_cast<float *>(b.workspace);
+    p.k = b.k;
+    p.row_bytes = b.row_bytes;
+    p.w_total = b.row_bytes * b.n;
+    p.j0 = b.j0;
+    p.rows_base = M / grid;
+    p.rows_rem = (int)(M % grid);
+    p.U = (int)(b.k / unit_k_of(b.fmt));
+    p.G = kBwCons / p.U;
+    p.SR = (int)SR;
+    p.SB = SB;
+    p.NS = NS;
+    p.dy_cap = dy_cap;
+    p.err = dev.err;
+    cudaError_t e;
+    switch (b.fmt) {
+    case F_BF16: e = launch_bw_t<F_BF16>(p, grid, smem, s); break;
+    case F_F16: e = launch_bw_t<F_F16>(p, grid, smem, s); break;
+    case F_Q4_0: e = launch_bw_t<F_Q4_0>(p, grid, smem, s); break;
+    case F_Q4_K: e = launch_bw_t<F_Q4_K>(p, grid, smem, s); break;
+    case F_Q6_K: e = launch_bw_t<F_Q6_K>(p, grid, smem, s); break;
+    default: return cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return e;
+    const int sum_grid = (int)std::min<int64_t>((b.k + 255) / 256, 4 * dev.sm_count);
+    back_input_sum_kernel<<<sum_grid, 256, 0, s>>>(p.part, grid, b.k, b.dx, b.accumulate);
+    return cudaGetLastError();
+}
+
+}  // namespace qmm

@@ -47,6 +47,23 @@ size_t mma_workspace_bytes(int fmt, int64_t n_tokens, int64_t k);
 int mma_mode(int fmt, int64_t k);  // 1: W16.X16, 2: x split, 3: w and x split
 cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s);
 
+// Backward with respect to the input, one vector:
+// dx[i] (+)= sum_{j in [j0, j1)} dy[j] w[j][i].
+struct BackLaunch {
+    int fmt;
+    const uint8_t *w;
+    const float *dy;        // n entries
+    float *dx;              // k entries
+    int64_t k, n, row_bytes;
+    int64_t j0, j1;         // rows of the sum axis
+    int accumulate;
+    void *workspace;        // >= back_input_workspace_bytes(...): per-CTA partials
+};
+bool back_input_supports(int fmt, int64_t k);
+size_t back_input_workspace_bytes(int fmt, int64_t k, int64_t n, int64_t j0, int64_t j1,
+                                  const DeviceInfo &dev);
+cudaError_t launch_back_input(const BackLaunch &b, const DeviceInfo &dev, cudaStream_t s);
+
 // Standalone dequantization of n rows into out[n][k].
 cudaError_t launch_dequant(int fmt, const uint8_t *w, int64_t k, int64_t n, int64_t row_bytes,
                            float *out, cudaStream_t s);

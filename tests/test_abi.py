@@ -140,3 +140,27 @@ def test_empty_work_needs_no_device(lib):
     """n == 0 or an empty tile returns OK without touching CUDA."""
     assert lib.qmm_matmul_ex(ctypes.byref(_args(n=0))) == 0
     assert lib.qmm_matmul_ex(ctypes.byref(_args(j_start=3, j_end=3))) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(n_tokens=2), 2),                 # one dy vector only
+    (dict(flags=q.FLAG_OVERLAP_PREV), 2),  # no launch flags
+    (dict(k=300), 2),
+    (dict(fmt=9), 1),
+    (dict(w_len=10), 3),
+    (dict(j_start=5, j_end=3), 4),
+    (dict(y=None), 5),
+    (dict(k=16384), 10),                   # 512 units per row: beyond the kernel
+    (dict(fmt="bf16", k=4096), 10),
+])
+def test_backward_input_rejected_on_host(lib, kw, status):
+    a = _args(**kw)
+    with pytest.raises(q.QmmError) as ei:
+        q.qmm_matmul_backward_input(a)
+    assert ei.value.status == status, q.qmm_last_error()
+    assert q.qmm_backward_input_workspace_bytes(a) == 0
+
+
+def test_backward_input_empty_work_needs_no_device(lib):
+    # k == 0: nothing to write, no device touched
+    assert q.qmm_matmul_backward_input(_args(k=0)) == 0
