@@ -430,6 +430,39 @@ def measure_other_workloads(torch, q, lib, r, stream, hbm_peak, tc_peak):
     out["q6_k_head_8_tiles"] = gemv_case("q6_k_head", tiles=8, reps=20)
     out["q6_k_head_untiled"] = gemv_case("q6_k_head", tiles=1, reps=20)
 
+    # backward with respect to the input, dx = W^T dy: the output head in 8
+    # sum-axis tiles (first writes, the rest accumulate), and the Q4_K FFN shape
+    bw = lib.qmm_matmul_backward_input
+
+    def back_case(name, tiles=1, reps=20):
+        fmt, k, n, w, _ = qmm_synth.workload(name)
+        ncop = r.copies_for(w.size)
+        wc = r.weights(w, ncop)
+        dyd = torch.from_numpy(np.random.default_rng(4).standard_normal(n).astype(np.float32)).to(dev)
+        dxd = torch.empty(k, device=dev)
+        tile = n // tiles
+        al = [[q.make_args(fmt, wc[c], dyd, dxd, k, n, 1, j_start=t * tile, j_end=(t + 1) * tile,
+                           accumulate=t > 0, stream=stream) for t in range(tiles)] for c in range(ncop)]
+        need = max(q.qmm_backward_input_workspace_bytes(a) for a in al[0])
+        wsb = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        for row in al:
+            for a in row:
+                a.workspace, a.workspace_bytes = wsb.data_ptr(), need
+        refs = [[ctypes.byref(a) for a in row] for row in al]
+
+        def launch(c):
+            for a in refs[c]:
+                if bw(a):
+                    raise RuntimeError(q.qmm_last_error())
+        dt = time_loop(torch, launch, reps, 3, ncop, stream)
+        q.qmm_device_status(stream)
+        gbs = w.size / dt / 1e9
+        return {"us": dt * 1e6, "weight_gbs": gbs, "frac_hbm": gbs / hbm_peak,
+                "weight_bytes": int(w.size), "launches_per_call": 2 * tiles}
+
+    out["q6_k_head_backward_input_8_tiles"] = back_case("q6_k_head", tiles=8)
+    out["q4_k_backward_input"] = back_case("q4_k_gemv", reps=50)
+
     # Q4_K N-token product: both paths at N = 1, 8, 64, 512
     fmt, k, n, w, _ = qmm_synth.workload("q4_k_prefill", n_tokens=1)
     ncop = r.copies_for(w.size)
@@ -486,6 +519,8 @@ def run_case(args):
             path = q.PATH_GEMV
     else:
         base = name
+    if name.endswith("_backward_input"):
+        return run_case_backward(args, torch, q, lib, r, name[:-len("_backward_input")])
     fmt, k, n, w, x = qmm_synth.workload(base, n_tokens=nt)
     ncop = 1 if args.no_rotate else r.copies_for(w.size)
     wc = r.weights(w, ncop)
@@ -513,11 +548,38 @@ def run_case(args):
     return 0
 
 
+def run_case_backward(args, torch, q, lib, r, base):
+    """dx = W^T dy over all rows of a workload's weights, timed alone."""
+    import ctypes
+    fmt, k, n, w, _ = qmm_synth.workload(base)
+    dev = r.dev
+    stream = r.stream
+    ncop = 1 if args.no_rotate else r.copies_for(w.size)
+    wc = r.weights(w, ncop)
+    dyd = torch.from_numpy(np.random.default_rng(4).standard_normal(n).astype(np.float32)).to(dev)
+    dxd = torch.empty(k, device=dev)
+    al = [q.make_args(fmt, wc[c], dyd, dxd, k, n, 1, stream=stream) for c in range(ncop)]
+    need = q.qmm_backward_input_workspace_bytes(al[0])
+    wsb = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    for a in al:
+        a.workspace, a.workspace_bytes = wsb.data_ptr(), need
+    refs = [ctypes.byref(a) for a in al]
+
+    def launch(c):
+        if lib.qmm_matmul_backward_input(refs[c]):
+            raise RuntimeError(q.qmm_last_error())
+    dt = time_loop(torch, launch, args.steps, args.warmup, ncop, stream)
+    q.qmm_device_status(stream)
+    print(json.dumps({"case": args.case, "us_per_call": dt * 1e6, "weight_gbs": w.size / dt / 1e9,
+                      "copies": ncop}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
                     help="profile one workload alone (bf16_gemv, f16_gemv, q4_0_gemv, q4_k_gemv, "
-                         "q6_k_head, q4_k_prefill_N<tokens>[_gemv])")
+                         "q6_k_head, q4_k_prefill_N<tokens>[_gemv], <gemv workload>_backward_input)")
     ap.add_argument("--no-rotate", action="store_true")
     ap.add_argument("--x-wait", action="store_true",
                     help="overlap only the weight stream with the previous kernel (x read after it)")

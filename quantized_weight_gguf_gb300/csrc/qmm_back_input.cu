@@ -316,35 +316,59 @@ __global__ void __launch_bounds__(kBwThreads, 2) back_input_kernel(const BackPar
     // row groups -> one partial per k index, through shared memory (the ring
     // is idle: every stage has been consumed)
     named_barrier(1, kBwCons);
-    float *red = reinterpret_cast<float *>(stages);  // [G][k]
+    // [G][k + k/32] floats: one padding word per 32 keeps a warp's writes
+    // (32 units at the same element) on distinct banks
+    float *red = reinterpret_cast<float *>(stages);
     const int64_t k = p.k;
+    const int64_t kpad = k + k / 32;
     if (active) {
 #pragma unroll
         for (int e = 0; e < UK; ++e) {
             float v;
             int64_t ki;
             unit_result<FMT>(st, u, e, v, ki);
-            red[(int64_t)g * k + ki] = v;
+            red[(int64_t)g * kpad + ki + (ki >> 5)] = v;
         }
     }
     named_barrier(1, kBwCons);
     float *out = p.part + (int64_t)cta * k;
     for (int64_t i = tid; i < k; i += kBwCons) {
         float v = 0.0f;
-        for (int gg = 0; gg < G; ++gg) v += red[(int64_t)gg * k + i];
+        for (int gg = 0; gg < G; ++gg) v += red[(int64_t)gg * kpad + i + (i >> 5)];
         out[i] = (failed || *abort_flag) ? 0.0f : v;
     }
 }
 
-// dx[i] (+)= sum over CTAs c in order of part[c][i]
+// dx[i] (+)= sum over CTAs c of part[c][i], in a fixed order: a CTA takes 32
+// consecutive i; warp w sums the partials c = w, w + 8, ... (four loads in
+// flight), then one warp adds the eight warp sums in order.
 __global__ void __launch_bounds__(256) back_input_sum_kernel(const float *__restrict__ part,
                                                              int parts, int64_t k, float *dx,
                                                              int accumulate) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < k;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        float v = accumulate ? dx[i] : 0.0f;
-        for (int c = 0; c < parts; ++c) v += __ldg(part + (int64_t)c * k + i);
-        dx[i] = v;
+    __shared__ float ws[8][33];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t i = (int64_t)blockIdx.x * 32 + lane;
+    float v = 0.0f;
+    if (i < k) {
+        float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+        int c = w;
+        for (; c + 24 < parts; c += 32) {
+            a0 += __ldg(part + (int64_t)c * k + i);
+            a1 += __ldg(part + (int64_t)(c + 8) * k + i);
+            a2 += __ldg(part + (int64_t)(c + 16) * k + i);
+            a3 += __ldg(part + (int64_t)(c + 24) * k + i);
+        }
+        for (; c < parts; c += 8) a0 += __ldg(part + (int64_t)c * k + i);
+        v = (a0 + a1) + (a2 + a3);
+    }
+    ws[w][lane] = v;
+    __syncthreads();
+    if (w == 0 && i < k) {
+        float t = accumulate ? dx[i] : 0.0f;
+        float sum = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sum += ws[j][lane];
+        dx[i] = t + sum;
     }
 }
 
@@ -388,7 +412,7 @@ static int64_t bw_plan(int fmt, int64_t k, int64_t R, int64_t M, int sm_count, i
     const int dy_cap = (int)rows_max;
     const size_t fixed = (size_t)(((16 * 8 + 16 + 127) & ~127) + 4 * dy_cap + 127) & ~(size_t)127;
     // the reduction reuses the ring: it must hold G x k floats
-    const size_t red = (size_t)4 * G * k;
+    const size_t red = (size_t)4 * G * (k + k / 32);
     int NS = 2;
     while (NS < 8 && fixed + (size_t)(NS + 1) * SB <= 110 * 1024) ++NS;
     while ((size_t)NS * SB < red && NS < 16) ++NS;
@@ -450,8 +474,8 @@ cudaError_t launch_back_input(const BackLaunch &b, const DeviceInfo &dev, cudaSt
     default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
-    const int sum_grid = (int)std::min<int64_t>((b.k + 255) / 256, 4 * dev.sm_count);
-    back_input_sum_kernel<<<sum_grid, 256, 0, s>>>(p.part, grid, b.k, b.dx, b.accumulate);
+    back_input_sum_kernel<<<(unsigned)((b.k + 31) / 32), 256, 0, s>>>(p.part, grid, b.k, b.dx,
+                                                                      b.accumulate);
     return cudaGetLastError();
 }
 
