@@ -33,7 +33,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-CODES = {"bf16": 0, "f16": 1, "q4_0": 2, "q4_k": 3, "q6_k": 4}
+CODES = {"bf16": 0, "f16": 1, "q4_0": 2, "q4_k": 3, "q6_k": 4, "q8_0": 5, "q5_0": 6}
 TOL_REL = 1e-4
 COSINE_FLOOR = 0.9999
 
@@ -66,6 +66,9 @@ def _load():
             lib.oracle_matmul.argtypes = [ctypes.c_int, p, p, i64, i64, i64, p, p, p]
             lib.oracle_matmul_back_input.restype = ctypes.c_int
             lib.oracle_matmul_back_input.argtypes = [ctypes.c_int, p, p, i64, i64, i64, i64, p, p, p]
+            lib.oracle_matmul_experts.restype = ctypes.c_int
+            lib.oracle_matmul_experts.argtypes = [ctypes.c_int, p, p, i64, i64, i64, i64, i64, p, p,
+                                                  p, p]
             lib.oracle_matmul_sampled.restype = ctypes.c_int
             lib.oracle_matmul_sampled.argtypes = [ctypes.c_int, p, p, i64, i64, i64, i64, p, p, p, p, p]
             _lib = lib
@@ -137,6 +140,26 @@ def matmul_sampled(fmt: str, w: np.ndarray, x: np.ndarray, k: int, n: int, t_idx
                                        _ptr(t_idx), _ptr(j_idx), _ptr(y), _ptr(s), _ptr(scratch))
     if rc != 0:
         raise ValueError("oracle sampled matmul rejected its arguments")
+    return y, s
+
+
+def matmul_experts(fmt: str, w: np.ndarray, x: np.ndarray, k: int, n: int, n_experts: int,
+                   ids: np.ndarray):
+    """(y, S) of the expert-indexed product: x [n_pos, k], ids [n_pos, top_k]
+    (int32) into n_experts stacked slices of n rows; y and S are f64
+    [n_pos * top_k, n] (row p * top_k + s)."""
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
+    ids = np.ascontiguousarray(np.atleast_2d(ids), dtype=np.int32)
+    n_pos, top_k = ids.shape
+    if x.shape != (n_pos, k) or w.size != row_bytes(fmt, k) * n * n_experts:
+        raise ValueError("bad shapes for the expert product")
+    y = np.empty((n_pos * top_k, n), np.float64)
+    s = np.empty((n_pos * top_k, n), np.float64)
+    scratch = np.empty(max(k, 1), np.float32)
+    if _load().oracle_matmul_experts(CODES[fmt], _ptr(w), _ptr(x), k, n, n_experts, n_pos, top_k,
+                                     _ptr(ids), _ptr(y), _ptr(s), _ptr(scratch)) != 0:
+        raise ValueError("oracle expert product rejected its arguments")
     return y, s
 
 

@@ -19,9 +19,16 @@
  *  - rullama src/backend/dispatch/mod.rs, backward-input parity tests: the
  *    f16 d sits at bytes 0..2 of a Q4_0 block, Q4_K keeps d at 0..2 and
  *    dmin at 2..4, Q6_K keeps d at bytes 208..210.
+ *  - rullama src/backend/matmul.rs, the expert-matmul tests (Q8_0 and Q5_0
+ *    stacked experts): a Q8_0 block is an f16 d then 32 bytes of codes; a
+ *    Q5_0 block is an f16 d, a 4-byte little-endian word of high bits, then
+ *    16 bytes of nibbles (22 bytes per 32 elements); experts are stacked as
+ *    whole [n rows x row bytes] slices, and position p, slot s uses the
+ *    expert ids[p * top_k + s].
  *  - the remaining field layout inside the blocks (nibble order, 6-bit
- *    scale packing, Q6_K ql/qh/scales) is the standard ggml block layout,
- *    which the pages name but do not print; it is written out below.
+ *    scale packing, Q6_K ql/qh/scales, which high bit of Q5_0 belongs to
+ *    which element, Q8_0 codes as signed bytes) is the standard ggml block
+ *    layout, which the pages name but do not print; it is written out below.
  *
  *  - rullama src/backend/dispatch/mod.rs, `MatmulBackInputParams` and the
  *    `matmul_q*_backward_input` dispatchers and parity tests: the gradient
@@ -38,7 +45,7 @@
 #include <string.h>
 
 /* Format codes of this oracle (the Python wrapper maps names to them). */
-enum { OR_BF16 = 0, OR_F16 = 1, OR_Q4_0 = 2, OR_Q4_K = 3, OR_Q6_K = 4 };
+enum { OR_BF16 = 0, OR_F16 = 1, OR_Q4_0 = 2, OR_Q4_K = 3, OR_Q6_K = 4, OR_Q8_0 = 5, OR_Q5_0 = 6 };
 
 static uint16_t rd_u16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }
 
@@ -77,6 +84,8 @@ int64_t oracle_row_bytes(int fmt, int64_t k)
     case OR_Q4_0: return (k % 32 == 0) ? (k / 32) * 18 : 0;
     case OR_Q4_K: return (k % 256 == 0) ? (k / 256) * 144 : 0;
     case OR_Q6_K: return (k % 256 == 0) ? (k / 256) * 210 : 0;
+    case OR_Q8_0: return (k % 32 == 0) ? (k / 32) * 34 : 0;
+    case OR_Q5_0: return (k % 32 == 0) ? (k / 32) * 22 : 0;
     default: return 0;
     }
 }
@@ -164,6 +173,34 @@ static void dequant_q6_k_block(const uint8_t *blk, float *out)
     }
 }
 
+/* Q8_0 block: f16 d, then 32 signed bytes; value = q * d. */
+static void dequant_q8_0_block(const uint8_t *blk, float *out)
+{
+    double d = oracle_f16_value(rd_u16(blk));
+    for (int i = 0; i < 32; ++i) {
+        int q = (int)(int8_t)blk[2 + i];
+        out[i] = (float)(q * d);
+    }
+}
+
+/* Q5_0 block: f16 d, a little-endian 32-bit word qh, 16 bytes qs; element
+ * i (< 16) is the low nibble of qs[i] with bit i of qh as its fifth bit,
+ * element i + 16 the high nibble of qs[i] with bit i + 16 of qh;
+ * value = (q - 16) * d. */
+static void dequant_q5_0_block(const uint8_t *blk, float *out)
+{
+    double d = oracle_f16_value(rd_u16(blk));
+    uint32_t qh = (uint32_t)blk[2] | ((uint32_t)blk[3] << 8) | ((uint32_t)blk[4] << 16) |
+                  ((uint32_t)blk[5] << 24);
+    const uint8_t *qs = blk + 6;
+    for (int i = 0; i < 16; ++i) {
+        int q_lo = (qs[i] & 0x0F) | ((int)((qh >> i) & 1u) << 4);
+        int q_hi = (qs[i] >> 4) | ((int)((qh >> (i + 16)) & 1u) << 4);
+        out[i] = (float)((q_lo - 16) * d);
+        out[i + 16] = (float)((q_hi - 16) * d);
+    }
+}
+
 /* Dequantize one row of k weights into out[k]. Returns 0, or -1 on bad args. */
 int oracle_dequant_row(int fmt, const uint8_t *row, int64_t k, float *out)
 {
@@ -183,6 +220,12 @@ int oracle_dequant_row(int fmt, const uint8_t *row, int64_t k, float *out)
         return 0;
     case OR_Q6_K:
         for (int64_t b = 0; b < k / 256; ++b) dequant_q6_k_block(row + 210 * b, out + 256 * b);
+        return 0;
+    case OR_Q8_0:
+        for (int64_t b = 0; b < k / 32; ++b) dequant_q8_0_block(row + 34 * b, out + 32 * b);
+        return 0;
+    case OR_Q5_0:
+        for (int64_t b = 0; b < k / 32; ++b) dequant_q5_0_block(row + 22 * b, out + 32 * b);
         return 0;
     default:
         return -1;
@@ -269,6 +312,37 @@ int oracle_matmul_back_input(int fmt, const uint8_t *w, const float *dy, int64_t
             double p = (double)dy[j] * (double)wrow_scratch[i];
             dx[i] += p;
             s[i] += fabs(p);
+        }
+    }
+    return 0;
+}
+
+/* Expert-indexed product: W holds n_experts slices of n rows; position p of
+ * x [n_pos x k] and slot s (< top_k) use slice e = ids[p * top_k + s]:
+ * y[(p * top_k + s) * n + j] = sum_i x[p][i] * w_e[j][i], and s likewise with
+ * |x w|; double sums. Returns -1 on an id outside [0, n_experts). */
+int oracle_matmul_experts(int fmt, const uint8_t *w, const float *x, int64_t k, int64_t n,
+                          int64_t n_experts, int64_t n_pos, int64_t top_k, const int32_t *ids,
+                          double *y, double *s, float *wrow_scratch)
+{
+    int64_t rb = oracle_row_bytes(fmt, k);
+    if (rb == 0 && k != 0) return -1;
+    for (int64_t p = 0; p < n_pos; ++p) {
+        for (int64_t sl = 0; sl < top_k; ++sl) {
+            int64_t e = ids[p * top_k + sl];
+            if (e < 0 || e >= n_experts) return -1;
+            const uint8_t *we = w + e * rb * n;
+            for (int64_t j = 0; j < n; ++j) {
+                if (oracle_dequant_row(fmt, we + j * rb, k, wrow_scratch)) return -1;
+                double acc = 0.0, mag = 0.0;
+                for (int64_t i = 0; i < k; ++i) {
+                    double v = (double)x[p * k + i] * (double)wrow_scratch[i];
+                    acc += v;
+                    mag += fabs(v);
+                }
+                y[(p * top_k + sl) * n + j] = acc;
+                s[(p * top_k + sl) * n + j] = mag;
+            }
         }
     }
     return 0;

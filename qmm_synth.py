@@ -23,9 +23,16 @@ stand-ins for the real-model shapes that the rullama ``matmul.rs`` tests use
                     seed 4; run as 8 output tiles of 32768 columns.
 * ``q4_k_prefill``  Q4_K with the q4_k_gemv value distribution, N=512 tokens,
                     k=4096, n=14336; X ~ N(0, 1) [N x k]; seed 5 (also N=1, 8, 64).
+* ``q8_0_experts`` / ``q5_0_experts``
+                    expert-indexed decode: 64 stacked experts of n=768 rows,
+                    k=2048, top_k = 8 experts per position, 1 position (also 4);
+                    Q8_0 d ~ U[0.002, 0.02] with uniform int8 codes, Q5_0
+                    d ~ U[0.005, 0.05] with uniform high-bit words and nibbles;
+                    ids drawn without repetition per position; x ~ N(0, 1); seeds 6, 7.
 
 Byte layouts written here (little-endian): Q4_0 block = f16 d then 16 quant
-bytes (18 B); Q4_K super-block = f16 d, f16 dmin, 12 scale bytes, 128 quant
+bytes (18 B); Q8_0 block = f16 d then 32 code bytes (34 B); Q5_0 block = f16 d,
+a 4-byte high-bit word, 16 nibble bytes (22 B); Q4_K super-block = f16 d, f16 dmin, 12 scale bytes, 128 quant
 bytes (144 B); Q6_K super-block = 128 ql bytes, 64 qh bytes, 16 int8 scales,
 f16 d (210 B). BF16/F16 rows are plain 16-bit little-endian values.
 """
@@ -33,11 +40,11 @@ from __future__ import annotations
 
 import numpy as np
 
-FORMATS = ("bf16", "f16", "q4_0", "q4_k", "q6_k")
+FORMATS = ("bf16", "f16", "q4_0", "q4_k", "q6_k", "q8_0", "q5_0")
 
 # elements per block and bytes per block of each format
-BLOCK_ELEMS = {"bf16": 1, "f16": 1, "q4_0": 32, "q4_k": 256, "q6_k": 256}
-BLOCK_BYTES = {"bf16": 2, "f16": 2, "q4_0": 18, "q4_k": 144, "q6_k": 210}
+BLOCK_ELEMS = {"bf16": 1, "f16": 1, "q4_0": 32, "q4_k": 256, "q6_k": 256, "q8_0": 32, "q5_0": 32}
+BLOCK_BYTES = {"bf16": 2, "f16": 2, "q4_0": 18, "q4_k": 144, "q6_k": 210, "q8_0": 34, "q5_0": 22}
 
 
 def row_bytes(fmt: str, k: int) -> int:
@@ -92,7 +99,45 @@ def gen_weights(fmt: str, k: int, n: int, rng: np.random.Generator, **dist) -> n
         blk[..., 192:208] = sc.view(np.uint8)
         blk[..., 208:210] = _f16_bytes(rng.uniform(lo, hi, size=(n, nb)))
         return blk.reshape(-1)
+    if fmt == "q8_0":
+        lo, hi = dist.get("d_range", (0.002, 0.02))
+        nb = k // 32
+        blk = np.empty((n, nb, 34), np.uint8)
+        blk[..., 0:2] = _f16_bytes(rng.uniform(lo, hi, size=(n, nb)))
+        blk[..., 2:34] = rng.integers(0, 256, size=(n, nb, 32), dtype=np.uint8)
+        return blk.reshape(-1)
+    if fmt == "q5_0":
+        lo, hi = dist.get("d_range", (0.005, 0.05))
+        nb = k // 32
+        blk = np.empty((n, nb, 22), np.uint8)
+        blk[..., 0:2] = _f16_bytes(rng.uniform(lo, hi, size=(n, nb)))
+        blk[..., 2:22] = rng.integers(0, 256, size=(n, nb, 20), dtype=np.uint8)
+        return blk.reshape(-1)
     raise ValueError(f"unknown format {fmt!r}")
+
+
+def gen_ids(n_pos: int, top_k: int, n_experts: int, rng: np.random.Generator) -> np.ndarray:
+    """Expert ids [n_pos, top_k] int32, distinct within a position."""
+    return np.stack([rng.choice(n_experts, size=top_k, replace=False) for _ in range(n_pos)]
+                    ).astype(np.int32)
+
+
+# name -> (fmt, k, n, n_experts, top_k, n_pos, seed)
+EXPERT_WORKLOADS = {
+    "q8_0_experts": ("q8_0", 2048, 768, 64, 8, 1, 6),
+    "q5_0_experts": ("q5_0", 2048, 768, 64, 8, 1, 7),
+}
+
+
+def expert_workload(name: str, n_pos: int | None = None):
+    """Seeded (fmt, k, n, n_experts, W bytes of all experts, X [n_pos, k], ids [n_pos, top_k])."""
+    fmt, k, n, n_exp, top_k, pos_default, seed = EXPERT_WORKLOADS[name]
+    npos = pos_default if n_pos is None else n_pos
+    rng = np.random.default_rng(seed)
+    w = gen_weights(fmt, k, n * n_exp, rng)
+    x = gen_x(npos, k, rng)
+    ids = gen_ids(npos, top_k, n_exp, rng)
+    return fmt, k, n, n_exp, w, x, ids
 
 
 def gen_x(n_tokens: int, k: int, rng: np.random.Generator, dist: str = "normal") -> np.ndarray:

@@ -467,3 +467,79 @@ def test_back_input_sum_axis_tiles_add_up():
     np.testing.assert_allclose(c, b, rtol=1e-12, atol=1e-12)
     with pytest.raises(ValueError):
         oracle.matmul_back_input(fmt, w, dy, k, n, 10, 5)
+
+
+# ------------------------------------------------- Q8_0, Q5_0 and experts ----
+
+def test_q8_0_and_q5_0_row_bytes():
+    for k in (0, 32, 64, 2048):
+        assert oracle.row_bytes("q8_0", k) == (k // 32) * 34
+        assert oracle.row_bytes("q5_0", k) == (k // 32) * 22
+    assert oracle.row_bytes("q8_0", 48) == 0 and oracle.row_bytes("q5_0", 16) == 0
+
+
+def test_q8_0_hand_packed():
+    """d = 0.5 (f16 0x3800) and codes -16 .. 15 as signed bytes."""
+    blk = np.zeros(34, np.uint8)
+    blk[0:2] = [0x00, 0x38]
+    codes = np.arange(-16, 16, dtype=np.int64)
+    blk[2:34] = codes.astype(np.int8).view(np.uint8)
+    w = oracle.dequant("q8_0", blk, 32, 1)[0]
+    assert list(w) == [0.5 * c for c in range(-16, 16)]
+    blk[2] = 0x80  # -128
+    assert oracle.dequant("q8_0", blk, 32, 1)[0][0] == -64.0
+
+
+def _pack_q5_0(d_bytes, q):
+    """Pack 32 five-bit codes: element i < 16 -> low nibble of byte i and bit i
+    of the high-bit word; element i + 16 -> high nibble and bit i + 16."""
+    blk = np.zeros(22, np.uint8)
+    blk[0:2] = d_bytes
+    qh = 0
+    for i in range(32):
+        qh |= ((int(q[i]) >> 4) & 1) << i
+    blk[2:6] = [(qh >> (8 * b)) & 0xFF for b in range(4)]
+    for i in range(16):
+        blk[6 + i] = (int(q[i]) & 15) | ((int(q[i + 16]) & 15) << 4)
+    return blk
+
+
+def test_q5_0_hand_packed():
+    """Every code 0..31 once (a permutation, so a wrong bit index or nibble
+    order moves values), d = 1 then d = -0.25."""
+    q = np.random.default_rng(0).permutation(32)
+    w = oracle.dequant("q5_0", _pack_q5_0([0x00, 0x3C], q), 32, 1)[0]
+    assert list(w) == [float(v - 16) for v in q]
+    w = oracle.dequant("q5_0", _pack_q5_0([0x00, 0xB4], q), 32, 1)[0]
+    assert list(w) == [-0.25 * (v - 16) for v in q]
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q5_0"])
+def test_new_formats_product_matches_numpy(fmt):
+    rng = np.random.default_rng(2)
+    k, n = 96, 7
+    w = qmm_synth.gen_weights(fmt, k, n, rng)
+    x = rng.standard_normal((3, k)).astype(np.float32)
+    y, s = oracle.matmul(fmt, w, x, k, n)
+    deq = oracle.dequant(fmt, w, k, n).astype(np.float64)
+    np.testing.assert_allclose(y, x.astype(np.float64) @ deq.T, rtol=1e-12, atol=1e-12)
+
+
+def test_experts_product_selects_slices():
+    """Row (p, s) of the expert product equals the plain product of x[p] with
+    the slice ids[p, s] cut out of the stacked bytes by hand; a bad id is
+    rejected."""
+    fmt, k, n, n_exp = "q5_0", 64, 5, 6
+    rng = np.random.default_rng(4)
+    w = qmm_synth.gen_weights(fmt, k, n * n_exp, rng)
+    x = rng.standard_normal((3, k)).astype(np.float32)
+    ids = np.array([[4, 0], [5, 2], [1, 3]], np.int32)
+    y, s = oracle.matmul_experts(fmt, w, x, k, n, n_exp, ids)
+    sl = oracle.row_bytes(fmt, k) * n
+    for p in range(3):
+        for t in range(2):
+            e = ids[p, t]
+            ye, se = oracle.matmul(fmt, w[e * sl:(e + 1) * sl], x[p], k, n)
+            assert np.array_equal(y[p * 2 + t], ye[0]) and np.array_equal(s[p * 2 + t], se[0])
+    with pytest.raises(ValueError):
+        oracle.matmul_experts(fmt, w, x, k, n, n_exp, np.array([[6, 0], [0, 0], [0, 0]], np.int32))
