@@ -429,6 +429,40 @@ def measure_other_workloads(torch, q, lib, r, stream, hbm_peak, tc_peak):
     out["q4_k_gemv"] = gemv_case("q4_k_gemv")
     out["q6_k_head_8_tiles"] = gemv_case("q6_k_head", tiles=8, reps=20)
     out["q6_k_head_untiled"] = gemv_case("q6_k_head", tiles=1, reps=20)
+    out["q8_0_gemv"] = gemv_case("q8_0_gemv")
+    out["q5_0_gemv"] = gemv_case("q5_0_gemv")
+
+    # expert-indexed product: each (position, slot) multiplies by the slice its
+    # id selects; the bytes are the selected slices (one read per pair)
+    ex = lib.qmm_matmul_experts
+
+    def expert_case(name, n_pos, reps=50):
+        fmt, k, n, n_exp, w, x, ids = qmm_synth.expert_workload(name, n_pos=n_pos)
+        slice_bytes = w.size // n_exp
+        pairs = ids.size
+        touched = len(np.unique(ids)) * slice_bytes
+        ncop = r.copies_for(touched)
+        wc = r.weights(w, ncop)
+        xd = torch.from_numpy(x).to(dev)
+        idd = torch.from_numpy(ids).to(dev)
+        yd = torch.empty((pairs, n), device=dev)
+        al = [ctypes.byref(q.make_args(fmt, wc[c], xd, yd, k, n, n_pos, stream=stream))
+              for c in range(ncop)]
+        ip = ctypes.c_void_p(idd.data_ptr())
+
+        def launch(c):
+            if ex(al[c], ip, n_exp, ids.shape[1]):
+                raise RuntimeError(q.qmm_last_error())
+        dt = time_loop(torch, launch, reps, 5, ncop, stream)
+        q.qmm_device_status(stream)
+        gbs = pairs * slice_bytes / dt / 1e9
+        return {"us": dt * 1e6, "weight_gbs": gbs, "frac_hbm": gbs / hbm_peak,
+                "weight_bytes": int(pairs * slice_bytes), "distinct_bytes": int(touched),
+                "pairs": int(pairs), "launches_per_call": 1}
+
+    for name in sorted(qmm_synth.EXPERT_WORKLOADS):
+        out[f"{name}_pos1"] = expert_case(name, 1)
+        out[f"{name}_pos4"] = expert_case(name, 4)
 
     # backward with respect to the input, dx = W^T dy: the output head in 8
     # sum-axis tiles (first writes, the rest accumulate), and the Q4_K FFN shape

@@ -46,13 +46,18 @@ extern "C" {
  *       12 bytes of 6-bit scales/mins, 128 nibble bytes), k % 256 == 0.
  * Q6_K: super-blocks of 256 weights in 210 bytes (128 low-nibble bytes,
  *       64 high-bit bytes, 16 int8 scales, f16 d), k % 256 == 0.
+ * Q8_0: blocks of 32 weights in 34 bytes (f16 d + 32 signed bytes), k % 32 == 0.
+ * Q5_0: blocks of 32 weights in 22 bytes (f16 d, a 32-bit word of fifth
+ *       bits, 16 nibble bytes), k % 32 == 0 (rullama matmul.rs expert tests).
  * Inside the blocks the fields follow the standard ggml layouts. */
 typedef enum qmm_format {
     QMM_BF16 = 0,
     QMM_F16 = 1,
     QMM_Q4_0 = 2,
     QMM_Q4_K = 3,
-    QMM_Q6_K = 4
+    QMM_Q6_K = 4,
+    QMM_Q8_0 = 5,
+    QMM_Q5_0 = 6
 } qmm_format;
 
 typedef enum qmm_status {
@@ -66,7 +71,8 @@ typedef enum qmm_status {
     QMM_ERR_CUDA = 7,            /* a CUDA runtime call failed (message has the CUDA error) */
     QMM_ERR_DEVICE_TIMEOUT = 8,  /* a kernel gave up waiting on a pipeline barrier (reported by qmm_device_status) */
     QMM_ERR_WORKSPACE = 9,       /* workspace given but smaller than qmm_workspace_bytes() */
-    QMM_ERR_UNSUPPORTED = 10     /* current device is not compute capability 10.3, or the path cannot take the shape */
+    QMM_ERR_UNSUPPORTED = 10,    /* current device is not compute capability 10.3, or the path cannot take the shape */
+    QMM_ERR_BAD_ID = 11          /* an expert id outside [0, n_experts) (reported by qmm_device_status) */
 } qmm_status;
 
 /* Kernel path selection for qmm_args.path. */
@@ -177,6 +183,20 @@ int qmm_matmul_backward_input(const qmm_args *a);
  * used. Host only (reads the device's SM count). */
 size_t qmm_backward_input_workspace_bytes(const qmm_args *a);
 
+/* Expert-indexed product (mixture of experts; rullama src/backend/matmul.rs,
+ * the expert-matmul tests and `moe_expert_matmul_chained`): W holds n_experts
+ * slices of n rows stacked one after another (each qmm_weight_bytes(fmt, k, n)
+ * bytes); a->x is [n_pos x k] with n_pos = a->n_tokens; ids is a DEVICE int32
+ * array [n_pos x top_k]; a->y is [n_pos * top_k x n]:
+ *     y[p * top_k + s][j] (+)= sum_i x[p][i] * w_{ids[p * top_k + s]}[j][i]
+ * for j in [j_start, j_end). a->w_len, when nonzero, must be n_experts times
+ * the slice bytes; n_pos * top_k <= 65535; a->flags == 0; a->path AUTO or GEMV
+ * (each (position, slot) runs as one GEMV of the one-token path, side by side
+ * in one launch; the ids are read on the device, nothing synchronizes). An id
+ * outside [0, n_experts) leaves that y row untouched and records an error that
+ * qmm_device_status reports as QMM_ERR_BAD_ID. Same formats and k limits as the one-token path. */
+int qmm_matmul_experts(const qmm_args *a, const int32_t *ids, int64_t n_experts, int64_t top_k);
+
 /* Standalone dequantization: out[j][i] = the fp32 value of weight i of row
  * j, bit-identical to the exact value rounded once to fp32 (only Q4_K's
  * d*sc*q - dmin*m rounds; every other product is exact). out is device
@@ -184,8 +204,9 @@ size_t qmm_backward_input_workspace_bytes(const qmm_args *a);
 int qmm_dequant(int fmt, const void *w, int64_t k, int64_t n, float *out, void *stream);
 
 /* Synchronizes `stream`, then reports whether any kernel enqueued so far
- * timed out on a pipeline barrier (QMM_ERR_DEVICE_TIMEOUT) and clears the
- * flag; QMM_OK otherwise, QMM_ERR_CUDA if the synchronize failed. Every
+ * timed out on a pipeline barrier (QMM_ERR_DEVICE_TIMEOUT) or met an expert
+ * id out of range (QMM_ERR_BAD_ID), and clears the flag; QMM_OK otherwise,
+ * QMM_ERR_CUDA if the synchronize failed. Every
  * barrier wait in the kernels is bounded (about 2 s); on expiry the kernel
  * records the fault, stops its pipeline, releases its tensor memory and
  * returns, so the context stays usable. */

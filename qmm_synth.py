@@ -155,6 +155,8 @@ WORKLOADS = {
     "q4_k_gemv": ("q4_k", 4096, 14336, 1, 3, "normal", 1),
     "q6_k_head": ("q6_k", 2560, 262144, 1, 4, "normal", 8),
     "q4_k_prefill": ("q4_k", 4096, 14336, 512, 5, "normal", 1),
+    "q8_0_gemv": ("q8_0", 4096, 14336, 1, 8, "normal", 1),
+    "q5_0_gemv": ("q5_0", 4096, 14336, 1, 9, "normal", 1),
 }
 
 

@@ -16,17 +16,19 @@ import os
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libqmm.so")
 
-FORMATS = {"bf16": 0, "f16": 1, "q4_0": 2, "q4_k": 3, "q6_k": 4}
+FORMATS = {"bf16": 0, "f16": 1, "q4_0": 2, "q4_k": 3, "q6_k": 4, "q8_0": 5, "q5_0": 6}
 PATH_AUTO, PATH_GEMV, PATH_MMA = 0, 1, 2
 FLAG_OVERLAP_PREV = 1
 FLAG_X_READY = 2
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_FORMAT", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_SIZE",
           4: "QMM_ERR_RANGE", 5: "QMM_ERR_NULL", 6: "QMM_ERR_ALIGN", 7: "QMM_ERR_CUDA",
-          8: "QMM_ERR_DEVICE_TIMEOUT", 9: "QMM_ERR_WORKSPACE", 10: "QMM_ERR_UNSUPPORTED"}
+          8: "QMM_ERR_DEVICE_TIMEOUT", 9: "QMM_ERR_WORKSPACE", 10: "QMM_ERR_UNSUPPORTED",
+          11: "QMM_ERR_BAD_ID"}
 EXPORTS = ("qmm_weight_bytes", "qmm_matmul", "qmm_set_stream", "qmm_matmul_ex",
            "qmm_workspace_bytes", "qmm_select_path", "qmm_matmul_host", "qmm_dequant",
            "qmm_device_status", "qmm_last_error", "qmm_version", "qmm_matmul_noalloc",
-           "qmm_matmul_backward_input", "qmm_backward_input_workspace_bytes")
+           "qmm_matmul_backward_input", "qmm_backward_input_workspace_bytes",
+           "qmm_matmul_experts")
 
 
 class QmmError(RuntimeError):
@@ -73,6 +75,7 @@ def load(path: str = LIB_PATH):
         "qmm_matmul_noalloc": (i, [pa]),
         "qmm_matmul_backward_input": (i, [pa]),
         "qmm_backward_input_workspace_bytes": (sz, [pa]),
+        "qmm_matmul_experts": (i, [pa, vp, i64, i64]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -144,6 +147,10 @@ def qmm_matmul_backward_input(args: qmm_args) -> int:
     return _check(load().qmm_matmul_backward_input(ctypes.byref(args)))
 
 
+def qmm_matmul_experts(args: qmm_args, ids, n_experts: int, top_k: int) -> int:
+    return _check(load().qmm_matmul_experts(ctypes.byref(args), _ptr(ids), n_experts, top_k))
+
+
 def qmm_backward_input_workspace_bytes(args: qmm_args) -> int:
     return load().qmm_backward_input_workspace_bytes(ctypes.byref(args))
 
@@ -213,6 +220,25 @@ def matmul_backward_input(fmt, w, dy, k: int, n: int, *, dx=None, j_start=0, j_e
                   j_end=j_end, accumulate=accumulate, stream=stream)
     qmm_matmul_backward_input(a)
     return dx
+
+
+def matmul_experts(fmt, w, x, ids, k: int, n: int, n_experts: int, *, y=None, j_start=0,
+                   j_end=0, accumulate=False, stream=None):
+    """Expert-indexed product for torch CUDA tensors: w uint8 (n_experts
+    stacked slices of n rows), x float32 [n_pos, k], ids int32 [n_pos, top_k]
+    on the device. Returns y float32 [n_pos * top_k, n] (the given y when passed)."""
+    import torch
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    if ids.dim() == 1:
+        ids = ids.unsqueeze(0)
+    n_pos, top_k = ids.shape
+    if y is None:
+        y = torch.empty((n_pos * top_k, n), dtype=torch.float32, device=x.device)
+    a = make_args(fmt, w, x, y, k, n, n_pos, w_len=w.numel() * w.element_size(), j_start=j_start,
+                  j_end=j_end, accumulate=accumulate, stream=stream)
+    qmm_matmul_experts(a, ids, n_experts, top_k)
+    return y
 
 
 def dequant(fmt, w, k: int, n: int, stream=None):

@@ -80,27 +80,30 @@ int64_t row_bytes_of(int fmt, int64_t k) {
     case QMM_Q4_0: return (k % 32 == 0) ? (k / 32) * 18 : -1;
     case QMM_Q4_K: return (k % 256 == 0) ? (k / 256) * 144 : -1;
     case QMM_Q6_K: return (k % 256 == 0) ? (k / 256) * 210 : -1;
+    case QMM_Q8_0: return (k % 32 == 0) ? (k / 32) * 34 : -1;
+    case QMM_Q5_0: return (k % 32 == 0) ? (k / 32) * 22 : -1;
     default: return -1;
     }
 }
 
 const char *fmt_name(int fmt) {
-    static const char *names[] = {"BF16", "F16", "Q4_0", "Q4_K", "Q6_K"};
-    return (fmt >= 0 && fmt <= 4) ? names[fmt] : "?";
+    static const char *names[] = {"BF16", "F16", "Q4_0", "Q4_K", "Q6_K", "Q8_0", "Q5_0"};
+    return (fmt >= 0 && fmt <= 6) ? names[fmt] : "?";
 }
 
 // Shape/pointer validation shared by the entry points. On success fills the
 // effective tile and row bytes.
 int validate(const qmm_args *a, int64_t *j0, int64_t *j1, int64_t *rb, bool check_ptrs) {
     if (!a) return fail(QMM_ERR_NULL, "args is NULL");
-    if (a->fmt < QMM_BF16 || a->fmt > QMM_Q6_K)
+    if (a->fmt < QMM_BF16 || a->fmt > QMM_Q5_0)
         return fail(QMM_ERR_FORMAT, "unknown format code %d", a->fmt);
     if (a->k < 0 || a->n < 0) return fail(QMM_ERR_SHAPE, "negative k or n (k=%lld n=%lld)",
                                           (long long)a->k, (long long)a->n);
     if (a->n_tokens < 1) return fail(QMM_ERR_SHAPE, "n_tokens %lld < 1", (long long)a->n_tokens);
     const int64_t r = row_bytes_of(a->fmt, a->k);
     if (r < 0) {
-        const char *need = (a->fmt == QMM_Q4_0) ? "a multiple of 32"
+        const char *need = (a->fmt == QMM_Q4_0 || a->fmt == QMM_Q8_0 || a->fmt == QMM_Q5_0)
+                               ? "a multiple of 32"
                            : (a->fmt == QMM_Q4_K || a->fmt == QMM_Q6_K) ? "a multiple of 256"
                                                                         : "even";
         return fail(QMM_ERR_SHAPE, "k %lld must be %s for %s matmul", (long long)a->k, need,
@@ -362,6 +365,60 @@ int qmm_matmul_backward_input(const qmm_args *a) {
     return e == cudaSuccess ? QMM_OK : cuda_fail(e, "backward-input launch");
 }
 
+int qmm_matmul_experts(const qmm_args *a, const int32_t *ids, int64_t n_experts, int64_t top_k) {
+    t_err[0] = 0;
+    if (!a) return fail(QMM_ERR_NULL, "args is NULL");
+    if (n_experts < 1 || top_k < 1)
+        return fail(QMM_ERR_SHAPE, "n_experts %lld and top_k %lld must be >= 1",
+                    (long long)n_experts, (long long)top_k);
+    if (a->flags != 0) return fail(QMM_ERR_SHAPE, "expert products take no flags");
+    if (a->path == QMM_PATH_MMA) return fail(QMM_ERR_UNSUPPORTED, "expert products run as GEMVs");
+    // shape checks of one expert slice (w_len is checked against all slices below)
+    qmm_args one = *a;
+    one.w_len = 0;
+    int64_t j0, j1, rb;
+    int st = validate(&one, &j0, &j1, &rb, true);
+    if (st != QMM_OK) return st;
+    const int64_t slice = rb * a->n;
+    if (a->w_len != 0 && a->w_len != (size_t)(slice * n_experts))
+        return fail(QMM_ERR_SIZE, "%s W bytes %zu != n_experts*row_bytes*n = %lld",
+                    fmt_name(a->fmt), a->w_len, (long long)(slice * n_experts));
+    const int64_t pairs = a->n_tokens * top_k;
+    if (pairs > 65535)
+        return fail(QMM_ERR_SHAPE, "n_tokens * top_k = %lld exceeds 65535", (long long)pairs);
+    if (j1 <= j0) return QMM_OK;
+    if (!ids) return fail(QMM_ERR_NULL, "ids is NULL");
+    if (reinterpret_cast<uintptr_t>(ids) & 3u) return fail(QMM_ERR_ALIGN, "ids must be 4-byte aligned");
+    if (a->k > 0 && !qmm::gemv_supports(a->fmt, a->k))
+        return fail(QMM_ERR_UNSUPPORTED, "expert GEMV cannot take %s with k=%lld", fmt_name(a->fmt),
+                    (long long)a->k);
+    qmm::DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != QMM_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(a->stream);
+    if (a->k == 0) {
+        if (a->accumulate) return QMM_OK;
+        cudaError_t e = qmm::launch_zero_cols(a->y, pairs, a->n, j0, j1, s);
+        return e == cudaSuccess ? QMM_OK : cuda_fail(e, "zero-fill launch");
+    }
+    qmm::GemvLaunch g;
+    g.fmt = a->fmt;
+    g.w = static_cast<const uint8_t *>(a->w);
+    g.x = a->x;
+    g.y = a->y;
+    g.k = a->k; g.n = a->n; g.row_bytes = rb;
+    g.j0 = j0; g.j1 = j1;
+    g.accumulate = a->accumulate;
+    g.overlap_prev = false;
+    g.x_ready = false;
+    g.ids = ids;
+    g.n_experts = (int)n_experts;
+    g.top_k = (int)top_k;
+    g.pairs = (int)pairs;
+    cudaError_t e = qmm::launch_gemv(g, *dev, s);
+    return e == cudaSuccess ? QMM_OK : cuda_fail(e, "expert GEMV launch");
+}
+
 size_t qmm_backward_input_workspace_bytes(const qmm_args *a) {
     int64_t j0, j1, rb;
     if (!a || a->n_tokens != 1 || validate(a, &j0, &j1, &rb, false) != QMM_OK) return 0;
@@ -373,7 +430,7 @@ size_t qmm_backward_input_workspace_bytes(const qmm_args *a) {
 
 int qmm_dequant(int fmt, const void *w, int64_t k, int64_t n, float *out, void *stream) {
     t_err[0] = 0;
-    if (fmt < QMM_BF16 || fmt > QMM_Q6_K) return fail(QMM_ERR_FORMAT, "unknown format code %d", fmt);
+    if (fmt < QMM_BF16 || fmt > QMM_Q5_0) return fail(QMM_ERR_FORMAT, "unknown format code %d", fmt);
     if (k < 0 || n < 0) return fail(QMM_ERR_SHAPE, "negative k or n");
     const int64_t r = row_bytes_of(fmt, k);
     if (r < 0) return fail(QMM_ERR_SHAPE, "k %lld does not fit %s blocks", (long long)k, fmt_name(fmt));
@@ -402,6 +459,8 @@ int qmm_device_status(void *stream) {
     if (v != 0) {
         const unsigned int zero = 0;
         cudaMemcpy(dev->err, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        if (v == qmm::DERR_BAD_ID)
+            return fail(QMM_ERR_BAD_ID, "an expert id was outside [0, n_experts)");
         return fail(QMM_ERR_DEVICE_TIMEOUT, "a kernel gave up waiting on a pipeline barrier (code %u)", v);
     }
     return QMM_OK;

@@ -143,6 +143,52 @@ __device__ __forceinline__ void unit_axpy(uint32_t rowa, int u, float dyj, BAcc<
         }
         st.s0 += a;
         st.s1 += bm;
+    } else if (FMT == F_Q8_0) {
+        // signed codes exactly: 2^23 + (q + 128) - (2^23 + 128)
+        const uint32_t base = rowa + 34u * u;
+        const float a = dyj * f16_bits_to_f32(lds16(base));
+        uint32_t qw[8];
+        lds_words_a2<8>(base + 2, qw);
+        const float2 aa = make_float2(a, a);
+        const float2 zp = make_float2(-8388736.0f, -8388736.0f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t v = qw[i] ^ 0x80808080u;
+            float2 f = fadd2(make_float2(byte_magic23<0>(v), byte_magic23<1>(v)), zp);
+            float2 r = ffma2(f, aa, make_float2(st.a[4 * i], st.a[4 * i + 1]));
+            st.a[4 * i] = r.x; st.a[4 * i + 1] = r.y;
+            f = fadd2(make_float2(byte_magic23<2>(v), byte_magic23<3>(v)), zp);
+            r = ffma2(f, aa, make_float2(st.a[4 * i + 2], st.a[4 * i + 3]));
+            st.a[4 * i + 2] = r.x; st.a[4 * i + 3] = r.y;
+        }
+    } else if (FMT == F_Q5_0) {
+        const uint32_t base = rowa + 22u * u;
+        const float a = dyj * f16_bits_to_f32(lds16(base));
+        uint32_t qh[1], qw[4];
+        lds_words_a2<1>(base + 2, qh);
+        lds_words_a2<4>(base + 6, qw);
+        const float2 aa = make_float2(a, a);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            // bits j of a 4-bit field of qh -> bit 4 of byte j
+            const uint32_t hl = (((qh[0] >> (4 * i)) & 15u) * 0x02040810u) & 0x10101010u;
+            const uint32_t hh = (((qh[0] >> (16 + 4 * i)) & 15u) * 0x02040810u) & 0x10101010u;
+            const uint32_t lo = (qw[i] & 0x0F0F0F0Fu) | hl, hi = ((qw[i] >> 4) & 0x0F0F0F0Fu) | hh;
+            float2 r;
+            r = ffma2(make_float2(byte_half_plus<0>(lo), byte_half_plus<1>(lo)), aa,
+                      make_float2(st.a[4 * i], st.a[4 * i + 1]));
+            st.a[4 * i] = r.x; st.a[4 * i + 1] = r.y;
+            r = ffma2(make_float2(byte_half_plus<2>(lo), byte_half_plus<3>(lo)), aa,
+                      make_float2(st.a[4 * i + 2], st.a[4 * i + 3]));
+            st.a[4 * i + 2] = r.x; st.a[4 * i + 3] = r.y;
+            r = ffma2(make_float2(byte_half_plus<0>(hi), byte_half_plus<1>(hi)), aa,
+                      make_float2(st.a[16 + 4 * i], st.a[16 + 4 * i + 1]));
+            st.a[16 + 4 * i] = r.x; st.a[16 + 4 * i + 1] = r.y;
+            r = ffma2(make_float2(byte_half_plus<2>(hi), byte_half_plus<3>(hi)), aa,
+                      make_float2(st.a[16 + 4 * i + 2], st.a[16 + 4 * i + 3]));
+            st.a[16 + 4 * i + 2] = r.x; st.a[16 + 4 * i + 3] = r.y;
+        }
+        st.s0 += a;
     } else {  // F_Q6_K
         // unit u: super-block b, half h, byte group gq; element 8 r + i is
         // weight 128 h + 32 r + 8 gq + i, with scale scales[8 h + 2 r + gq / 2]
@@ -199,6 +245,13 @@ __device__ __forceinline__ void unit_result(const BAcc<FMT> &st, int u, int e, f
     } else if (FMT == F_Q4_0) {
         // sum a (q - 8) = 256 sum a (0.5 + q/256) - 136 sum a
         v = fmaf(256.0f, st.a[e], -136.0f * st.s0);
+        kidx = 32 * (int64_t)u + e;
+    } else if (FMT == F_Q8_0) {
+        v = st.a[e];  // exact codes: no carrier
+        kidx = 32 * (int64_t)u + e;
+    } else if (FMT == F_Q5_0) {
+        // sum a (q - 16) = 256 sum a (0.5 + q/256) - 144 sum a
+        v = fmaf(256.0f, st.a[e], -144.0f * st.s0);
         kidx = 32 * (int64_t)u + e;
     } else if (FMT == F_Q4_K) {
         // sum (a q - dy dm) = 256 sum a (0.5 + q/256) - 128 sum a - sum dy dm
@@ -390,7 +443,7 @@ int unit_k_of(int fmt) { return (fmt == F_BF16 || fmt == F_F16) ? 8 : 32; }
 }  // namespace
 
 bool back_input_supports(int fmt, int64_t k) {
-    if (fmt < F_BF16 || fmt > F_Q6_K || k <= 0) return false;
+    if (fmt < F_BF16 || fmt > kLastFmt || k <= 0) return false;
     const int uk = unit_k_of(fmt);
     return k % uk == 0 && k / uk <= kBwCons;
 }
@@ -431,9 +484,7 @@ size_t back_input_workspace_bytes(int fmt, int64_t k, int64_t n, int64_t j0, int
     int grid, NS, SB, dy_cap;
     int64_t SR;
     size_t smem;
-    const int64_t R = (fmt == F_BF16 || fmt == F_F16) ? 2 * k
-                      : fmt == F_Q4_0 ? (k / 32) * 18
-                      : fmt == F_Q4_K ? (k / 256) * 144 : (k / 256) * 210;
+    const int64_t R = (k / block_elems(fmt)) * block_bytes(fmt);
     (void)n;
     return (size_t)bw_plan(fmt, k, R, j1 - j0, dev.sm_count, &grid, &SR, &NS, &SB, &smem, &dy_cap);
 }
@@ -471,6 +522,8 @@ cudaError_t launch_back_input(const BackLaunch &b, const DeviceInfo &dev, cudaSt
     case F_Q4_0: e = launch_bw_t<F_Q4_0>(p, grid, smem, s); break;
     case F_Q4_K: e = launch_bw_t<F_Q4_K>(p, grid, smem, s); break;
     case F_Q6_K: e = launch_bw_t<F_Q6_K>(p, grid, smem, s); break;
+    case F_Q8_0: e = launch_bw_t<F_Q8_0>(p, grid, smem, s); break;
+    case F_Q5_0: e = launch_bw_t<F_Q5_0>(p, grid, smem, s); break;
     default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;

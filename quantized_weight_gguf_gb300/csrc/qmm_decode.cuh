@@ -16,6 +16,10 @@
 //                       | 128 nibble bytes; weights 64c..64c+31 are the low
 //                       nibbles of bytes 32c..32c+31, 64c+32..64c+63 their high
 //                       nibbles; sub-block s = weight / 32; w = d*sc_s*q - dmin*m_s.
+//   Q8_0  (32 w, 34 B): f16 d | 32 signed bytes q; w = q * d.
+//   Q5_0  (32 w, 22 B): f16 d | u32 qh | 16 bytes; weight i < 16 = low nibble of
+//                       byte i with bit i of qh as bit 4, weight i + 16 = its
+//                       high nibble with bit i + 16 of qh; w = (q - 16) * d.
 //   Q6_K (256 w, 210 B): ql[128] | qh[64] | int8 scales[16] | f16 d; for half h and
 //                       l < 32, weight 128h + 32r + l takes nibble (r < 2: low,
 //                       else high) of ql[64h + 32(r & 1) + l] and bits 2r..2r+1 of
@@ -169,6 +173,50 @@ struct Raw32<F_Q6_K> {
             const uint32_t hi = (qh[l >> 2] >> (8 * (l & 3))) & 0xFFu;
             const int q = (int)(((lo >> nsh) & 15u) | (((hi >> hsh) & 3u) << 4));
             w[l] = __fmul_rn(l < 16 ? ds0 : ds1, (float)(q - 32));
+        }
+    }
+};
+
+template <>
+struct Raw32<F_Q8_0> {
+    uint32_t dbits;
+    uint32_t qw[8];   // the 32 code bytes, packed little-endian
+    __device__ __forceinline__ void load(const uint8_t *row, int64_t k0, int) {
+        const uint8_t *p = row + 34 * (k0 >> 5);
+        dbits = ldg_u16(p);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) qw[i] = ldg_u16(p + 2 + 4 * i) | (ldg_u16(p + 4 + 4 * i) << 16);
+    }
+    __device__ __forceinline__ void decode(float (&w)[32]) const {
+        const float d = f16_bits_to_f32(dbits);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int q = (int)(int8_t)((qw[i >> 2] >> (8 * (i & 3))) & 0xFFu);
+            w[i] = __fmul_rn((float)q, d);
+        }
+    }
+};
+
+template <>
+struct Raw32<F_Q5_0> {
+    uint32_t dbits, qh;
+    uint32_t qw[4];   // the 16 nibble bytes, packed little-endian
+    __device__ __forceinline__ void load(const uint8_t *row, int64_t k0, int) {
+        const uint8_t *p = row + 22 * (k0 >> 5);
+        dbits = ldg_u16(p);
+        qh = ldg_u16(p + 2) | (ldg_u16(p + 4) << 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qw[i] = ldg_u16(p + 6 + 4 * i) | (ldg_u16(p + 8 + 4 * i) << 16);
+    }
+    __device__ __forceinline__ void decode(float (&w)[32]) const {
+        const float d = f16_bits_to_f32(dbits);
+#pragma unroll
+        for (int b = 0; b < 16; ++b) {
+            const uint32_t byte = (qw[b >> 2] >> (8 * (b & 3))) & 0xFFu;
+            const int lo = (int)((byte & 15u) | (((qh >> b) & 1u) << 4));
+            const int hi = (int)((byte >> 4) | (((qh >> (b + 16)) & 1u) << 4));
+            w[b] = __fmul_rn((float)(lo - 16), d);
+            w[b + 16] = __fmul_rn((float)(hi - 16), d);
         }
     }
 };

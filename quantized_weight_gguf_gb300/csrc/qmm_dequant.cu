@@ -49,6 +49,8 @@ cudaError_t launch_dequant(int fmt, const uint8_t *w, int64_t k, int64_t n, int6
     case F_Q4_0: dequant_kernel<F_Q4_0><<<grid, block, 0, s>>>(w, k, n, row_bytes, out); break;
     case F_Q4_K: dequant_kernel<F_Q4_K><<<grid, block, 0, s>>>(w, k, n, row_bytes, out); break;
     case F_Q6_K: dequant_kernel<F_Q6_K><<<grid, block, 0, s>>>(w, k, n, row_bytes, out); break;
+    case F_Q8_0: dequant_kernel<F_Q8_0><<<grid, block, 0, s>>>(w, k, n, row_bytes, out); break;
+    case F_Q5_0: dequant_kernel<F_Q5_0><<<grid, block, 0, s>>>(w, k, n, row_bytes, out); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

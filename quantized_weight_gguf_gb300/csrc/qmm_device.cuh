@@ -11,7 +11,8 @@
 
 namespace qmm {
 
-enum Fmt : int { F_BF16 = 0, F_F16 = 1, F_Q4_0 = 2, F_Q4_K = 3, F_Q6_K = 4 };
+enum Fmt : int { F_BF16 = 0, F_F16 = 1, F_Q4_0 = 2, F_Q4_K = 3, F_Q6_K = 4, F_Q8_0 = 5, F_Q5_0 = 6 };
+constexpr int kLastFmt = F_Q5_0;
 
 // Error codes written to the device error word (first fault wins).
 enum DevErr : unsigned int {
@@ -22,15 +23,17 @@ enum DevErr : unsigned int {
     DERR_MMA_B = 4,        // MMA issuer gave up waiting for an x tile
     DERR_MMA_EMPTY = 5,    // a producer gave up waiting for a free stage
     DERR_MMA_ACC = 6,      // epilogue gave up waiting for the accumulator
-    DERR_TEARDOWN = 7      // copies still in flight at exit after a fault
+    DERR_TEARDOWN = 7,     // copies still in flight at exit after a fault
+    DERR_BAD_ID = 8        // an expert id outside [0, n_experts)
 };
 
 // Block geometry (elements per block, bytes per block) of each format.
 __host__ __device__ constexpr int block_elems(int f) {
-    return f == F_Q4_0 ? 32 : (f == F_Q4_K || f == F_Q6_K) ? 256 : 1;
+    return (f == F_Q4_0 || f == F_Q8_0 || f == F_Q5_0) ? 32 : (f == F_Q4_K || f == F_Q6_K) ? 256 : 1;
 }
 __host__ __device__ constexpr int block_bytes(int f) {
-    return f == F_Q4_0 ? 18 : f == F_Q4_K ? 144 : f == F_Q6_K ? 210 : 2;
+    return f == F_Q4_0 ? 18 : f == F_Q4_K ? 144 : f == F_Q6_K ? 210 : f == F_Q8_0 ? 34
+           : f == F_Q5_0 ? 22 : 2;
 }
 
 // ------------------------------------------------------------ numbers ----
@@ -49,6 +52,17 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
     asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+    float2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+    return d;
+}
+
+// Two fp32 additions in one packed instruction.
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    uint64_t ra, rb, rd;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
     float2 d;
     asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
     return d;

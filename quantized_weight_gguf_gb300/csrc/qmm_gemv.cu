@@ -47,6 +47,12 @@ struct GemvParams {
     int SB;   // bytes per stage buffer (multiple of 128)
     int NS;   // stage buffers
     unsigned int *err;
+    // expert-indexed calls (ids != null): blockIdx.y = position * top_k + slot
+    // selects the expert slice ids[blockIdx.y] of W, x row position, y row blockIdx.y
+    const int32_t *ids;
+    int64_t slice_bytes;
+    int n_experts, top_k;
+    int64_t n;  // row stride of y
 };
 
 // Weights per unit: a 16-byte chunk for 16-bit formats (lane-contiguous in
@@ -65,15 +71,6 @@ __device__ __forceinline__ uint32_t bfe(uint32_t a, uint32_t pos, uint32_t len) 
 __device__ __forceinline__ int32_t bfe_s(uint32_t a, uint32_t pos) {
     int32_t d;
     asm("bfe.s32 %0, %1, %2, 8;" : "=r"(d) : "r"(a), "r"(pos));
-    return d;
-}
-__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
-    uint64_t ra, rb, rd;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
-    float2 d;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
     return d;
 }
 
@@ -126,6 +123,11 @@ __device__ __forceinline__ void unit_init(UnitState<FMT> &st, const float *xs, i
         // scale byte of quarter r sits at byte 2r + (gq >> 1) of scales[8h .. 8h+7]
         st.p0 = 8 * (0 + (gq >> 1)); st.p1 = 8 * (2 + (gq >> 1));
         st.p2 = st.p0; st.p3 = st.p1;
+    } else if (FMT == F_Q5_0) {
+        float sx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sx += st.xr[i];
+        st.c0 = sx;
     } else if (FMT == F_Q4_K) {
         float sx = 0.0f;
 #pragma unroll
@@ -234,6 +236,50 @@ __device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<
         const float ds = d * (float)sc, dm = dmin * (float)m;
         // ds * sum q x - dm * sum x, with sum q x = 256 * a - 128 * sum x
         return fmaf(256.0f * ds, a, -fmaf(128.0f, ds, dm) * st.c0);
+    } else if (FMT == F_Q8_0) {
+        // codes are signed bytes: flipping the top bit gives q + 128 unsigned,
+        // 2^23 + (q + 128) - (2^23 + 128) = q exactly
+        const uint32_t base = rowa + 34u * u;
+        const float d = f16_bits_to_f32(lds16(base));
+        uint32_t qw[8];
+        lds_words_a2<8>(base + 2, qw);
+        const float2 zp = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+        float2 a0 = make_float2(0.f, 0.f), a1 = a0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t v = qw[i] ^ 0x80808080u;
+            float2 f = fadd2(make_float2(byte_magic23<0>(v), byte_magic23<1>(v)), zp);
+            a0 = ffma2(f, make_float2(st.xr[4 * i], st.xr[4 * i + 1]), a0);
+            f = fadd2(make_float2(byte_magic23<2>(v), byte_magic23<3>(v)), zp);
+            a1 = ffma2(f, make_float2(st.xr[4 * i + 2], st.xr[4 * i + 3]), a1);
+        }
+        return d * ((a0.x + a0.y) + (a1.x + a1.y));
+    } else if (FMT == F_Q5_0) {
+        // 5-bit codes (< 128): nibble | fifth bit spread to bit 4 of each byte,
+        // then the 0.5 + q/256 permute; sum (q - 16) x = 256 a - 144 sum x
+        const uint32_t base = rowa + 22u * u;
+        const float d = f16_bits_to_f32(lds16(base));
+        uint32_t qh[1], qw[4];
+        lds_words_a2<1>(base + 2, qh);
+        lds_words_a2<4>(base + 6, qw);
+        float2 a0 = make_float2(0.f, 0.f), a1 = a0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            // bits j of a 4-bit field -> bit 4 of byte j
+            const uint32_t hl = (((qh[0] >> (4 * i)) & 15u) * 0x02040810u) & 0x10101010u;
+            const uint32_t hh = (((qh[0] >> (16 + 4 * i)) & 15u) * 0x02040810u) & 0x10101010u;
+            const uint32_t lo = (qw[i] & 0x0F0F0F0Fu) | hl, hi = ((qw[i] >> 4) & 0x0F0F0F0Fu) | hh;
+            a0 = ffma2(make_float2(byte_half_plus<0>(lo), byte_half_plus<1>(lo)),
+                       make_float2(st.xr[4 * i], st.xr[4 * i + 1]), a0);
+            a1 = ffma2(make_float2(byte_half_plus<2>(lo), byte_half_plus<3>(lo)),
+                       make_float2(st.xr[4 * i + 2], st.xr[4 * i + 3]), a1);
+            a0 = ffma2(make_float2(byte_half_plus<0>(hi), byte_half_plus<1>(hi)),
+                       make_float2(st.xr[16 + 4 * i], st.xr[16 + 4 * i + 1]), a0);
+            a1 = ffma2(make_float2(byte_half_plus<2>(hi), byte_half_plus<3>(hi)),
+                       make_float2(st.xr[16 + 4 * i + 2], st.xr[16 + 4 * i + 3]), a1);
+        }
+        const float a = (a0.x + a0.y) + (a1.x + a1.y);
+        return d * fmaf(256.0f, a, -144.0f * st.c0);
     } else {  // F_Q6_K
         const int b = u >> 3, h = (u >> 2) & 1, gq = u & 3;
         const uint32_t sb = rowa + 210u * b;
@@ -309,6 +355,21 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cta = blockIdx.x;
+    // byte offset of this call's weight slice, and its x and y rows
+    int64_t w_off = 0;
+    const float *xg = p.x;
+    float *yg = p.y;
+    if (p.ids) {
+        const int pair = blockIdx.y;
+        const int e = __ldg(p.ids + pair);
+        if (e < 0 || e >= p.n_experts) {  // nothing read or written for a bad id
+            if (threadIdx.x == 0) record_error(p.err, DERR_BAD_ID);
+            return;
+        }
+        w_off = (int64_t)e * p.slice_bytes;
+        xg = p.x + (int64_t)(pair / p.top_k) * p.k;
+        yg = p.y + (int64_t)pair * p.n;
+    }
     const int64_t r0 = p.j0 + (int64_t)cta * p.rows_base + (cta < p.rows_rem ? cta : p.rows_rem);
     const int64_t nrows = p.rows_base + (cta < p.rows_rem ? 1 : 0);
     const int nst = (int)((nrows + SR - 1) / SR);
@@ -341,7 +402,7 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
             }
             const int64_t ra = r0 + (int64_t)s * SR;
             const int64_t rb = min(ra + SR, r0 + nrows);
-            const int64_t A = ra * R, B = rb * R;
+            const int64_t A = w_off + ra * R, B = w_off + rb * R;
             const int64_t a16 = A & ~(int64_t)15, b16 = (B + 15) & ~(int64_t)15;
             const int64_t tend = min(b16, lim);
             if (B > lim) {  // bytes after the last whole 16-byte chunk of W
@@ -368,8 +429,8 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
     if (!kChunked) {
         const int k = (int)p.k;
         const int U = p.U;
-        if ((reinterpret_cast<uintptr_t>(p.x) & 15u) == 0 && (k & 3) == 0) {
-            const float4 *x4 = reinterpret_cast<const float4 *>(p.x);
+        if ((reinterpret_cast<uintptr_t>(xg) & 15u) == 0 && (k & 3) == 0) {
+            const float4 *x4 = reinterpret_cast<const float4 *>(xg);
             for (int i = tid; i < k / 4; i += kCons) {
                 const float4 v = __ldg(x4 + i);
                 xs[x_slot<FMT>(4 * i, U)] = v.x;
@@ -378,7 +439,7 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
                 xs[x_slot<FMT>(4 * i + 3, U)] = v.w;
             }
         } else {
-            for (int i = tid; i < k; i += kCons) xs[x_slot<FMT>(i, U)] = __ldg(p.x + i);
+            for (int i = tid; i < k; i += kCons) xs[x_slot<FMT>(i, U)] = __ldg(xg + i);
         }
         named_barrier(1, kCons);
     }
@@ -399,7 +460,7 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
     for (int q = 0; q < UPT; ++q) {
         const int u = u0 + q * kCons;
         if constexpr (kChunked)
-            unit_init_direct<FMT>(st[q], p.x, u, u < p.U);
+            unit_init_direct<FMT>(st[q], xg, u, u < p.U);
         else
             unit_init<FMT>(st[q], xs, p.U, active && u < p.U ? u : 0, active && u < p.U);
     }
@@ -421,7 +482,7 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
         const int64_t ra = r0 + (int64_t)s * SR;
         const int64_t rb = min(ra + SR, r0 + nrows);
         const int rows_in = (int)(rb - ra);
-        const int64_t a16 = (ra * R) & ~(int64_t)15;
+        const int64_t a16 = (w_off + ra * R) & ~(int64_t)15;
         const uint32_t sbase = stage0 + (uint32_t)slot * SB;
         float *pb = part + (ra - fbase) * PU;
         if (!failed && active) {
@@ -432,7 +493,7 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
                 const bool has = rr < rows_in;
                 float acc = 0.0f;
                 if (has) {
-                    const uint32_t rowa = sbase + (uint32_t)((ra + rr) * R - a16);
+                    const uint32_t rowa = sbase + (uint32_t)(w_off + (ra + rr) * R - a16);
 #pragma unroll
                     for (int q = 0; q < UPT; ++q) {
                         const int u = u0 + q * kCons;
@@ -460,7 +521,7 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
                     if (lane == 0) {
-                        float *yp = p.y + fbase + rr;
+                        float *yp = yg + fbase + rr;
                         *yp = p.accumulate ? *yp + v : v;
                     }
                 }
@@ -477,7 +538,7 @@ static int unit_k(int fmt) { return (fmt == F_BF16 || fmt == F_F16) ? 8 : 32; }
 static int max_upt(int fmt) { return (fmt == F_BF16 || fmt == F_F16) ? 8 : 2; }
 
 bool gemv_supports(int fmt, int64_t k) {
-    if (fmt < F_BF16 || fmt > F_Q6_K || k <= 0) return false;
+    if (fmt < F_BF16 || fmt > kLastFmt || k <= 0) return false;
     const int uk = unit_k(fmt);
     if (k % uk) return false;
     const int64_t U = k / uk;
@@ -485,7 +546,7 @@ bool gemv_supports(int fmt, int64_t k) {
 }
 
 template <int FMT, int UPT>
-static cudaError_t launch_t(const GemvParams &p, int grid, size_t smem, cudaStream_t s,
+static cudaError_t launch_t(const GemvParams &p, dim3 grid, size_t smem, cudaStream_t s,
                             bool overlap) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -499,7 +560,7 @@ static cudaError_t launch_t(const GemvParams &p, int grid, size_t smem, cudaStre
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
+    cfg.gridDim = grid;
     cfg.blockDim = dim3(kGemvThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -512,7 +573,7 @@ static cudaError_t launch_t(const GemvParams &p, int grid, size_t smem, cudaStre
 }
 
 template <int FMT>
-static cudaError_t launch_chunked(const GemvParams &p, int upt, int grid, size_t smem,
+static cudaError_t launch_chunked(const GemvParams &p, int upt, dim3 grid, size_t smem,
                                   cudaStream_t s, bool ov) {
     switch (upt) {
     case 1: return launch_t<FMT, 1>(p, grid, smem, s, ov);
@@ -549,7 +610,9 @@ cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t
         SEG = 0; PU = U;
     }
     const int64_t R = g.row_bytes;
-    const int ctas_target = 2 * dev.sm_count;
+    // expert-indexed calls run `pairs` independent GEMVs side by side (grid.y)
+    const int pairs = g.ids ? g.pairs : 1;
+    const int ctas_target = std::max(1, 2 * dev.sm_count / pairs);
     const int64_t per_cta = (M + ctas_target - 1) / ctas_target;
     const size_t xs_bytes = chunked ? 0 : (size_t)4 * (g.k + uk);
     auto smem_for = [&](int ns, int64_t sr, int64_t rpf) {
@@ -593,16 +656,23 @@ cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t
     }
     const int SB = (int)(((SR * R + 32) + 127) & ~(int64_t)127);
     const int64_t nstage_total = (M + SR - 1) / SR;
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(nstage_total, ctas_target));
+    const int gx = (int)std::max<int64_t>(1, std::min<int64_t>(nstage_total, ctas_target));
+    const dim3 grid((unsigned)gx, (unsigned)pairs);
     const size_t smem = smem_for(NS, SR, RPF);
     if (smem > 200 * 1024) return cudaErrorNotSupported;
 
     GemvParams p;
     p.w = g.w; p.x = g.x; p.y = g.y;
-    p.k = g.k; p.row_bytes = R; p.w_total = R * g.n;
+    p.k = g.k; p.row_bytes = R;
+    p.w_total = R * g.n * (g.ids ? g.n_experts : 1);
+    p.ids = g.ids;
+    p.slice_bytes = R * g.n;
+    p.n_experts = g.n_experts;
+    p.top_k = g.top_k;
+    p.n = g.n;
     p.j0 = g.j0;
-    p.rows_base = M / grid;
-    p.rows_rem = (int)(M % grid);
+    p.rows_base = M / gx;
+    p.rows_rem = (int)(M % gx);
     p.accumulate = g.accumulate;
     p.x_ready = g.x_ready ? 1 : 0;
     p.U = U; p.G = G; p.PU = PU; p.SEG = SEG; p.RPF = (int)RPF; p.SR = (int)SR; p.SB = SB; p.NS = NS;
@@ -614,6 +684,8 @@ cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t
     case F_Q4_0: return upt == 1 ? launch_t<F_Q4_0, 1>(p, grid, smem, s, ov) : launch_t<F_Q4_0, 2>(p, grid, smem, s, ov);
     case F_Q4_K: return upt == 1 ? launch_t<F_Q4_K, 1>(p, grid, smem, s, ov) : launch_t<F_Q4_K, 2>(p, grid, smem, s, ov);
     case F_Q6_K: return upt == 1 ? launch_t<F_Q6_K, 1>(p, grid, smem, s, ov) : launch_t<F_Q6_K, 2>(p, grid, smem, s, ov);
+    case F_Q8_0: return upt == 1 ? launch_t<F_Q8_0, 1>(p, grid, smem, s, ov) : launch_t<F_Q8_0, 2>(p, grid, smem, s, ov);
+    case F_Q5_0: return upt == 1 ? launch_t<F_Q5_0, 1>(p, grid, smem, s, ov) : launch_t<F_Q5_0, 2>(p, grid, smem, s, ov);
     default: return cudaErrorInvalidValue;
     }
 }

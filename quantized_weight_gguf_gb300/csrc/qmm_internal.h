@@ -26,6 +26,10 @@ struct GemvLaunch {
     int accumulate;
     bool overlap_prev;   // programmatic dependent launch (W is not written by the previous kernel)
     bool x_ready;        // x is not written by the previous kernel either: only y waits
+    // expert-indexed calls: w holds n_experts slices of n rows; GEMV number
+    // q < pairs uses slice ids[q], x row q / top_k and y row q (device ids)
+    const int32_t *ids = nullptr;
+    int n_experts = 0, top_k = 1, pairs = 1;
 };
 // Returns cudaSuccess or the launch error; cudaErrorNotSupported when no
 // GEMV variant takes the shape (the caller then uses the tensor-core path).

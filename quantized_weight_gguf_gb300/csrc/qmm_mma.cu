@@ -1102,6 +1102,8 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
     case F_Q4_0: return launch_fmt<F_Q4_0>(mode, bn, mp, p, dev, s);
     case F_Q4_K: return launch_fmt<F_Q4_K>(mode, bn, mp, p, dev, s);
     case F_Q6_K: return launch_fmt<F_Q6_K>(mode, bn, mp, p, dev, s);
+    case F_Q8_0: return launch_fmt<F_Q8_0>(mode, bn, mp, p, dev, s);
+    case F_Q5_0: return launch_fmt<F_Q5_0>(mode, bn, mp, p, dev, s);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -164,3 +164,33 @@ def test_backward_input_rejected_on_host(lib, kw, status):
 def test_backward_input_empty_work_needs_no_device(lib):
     # k == 0: nothing to write, no device touched
     assert q.qmm_matmul_backward_input(_args(k=0)) == 0
+
+
+@pytest.mark.parametrize("kw,extra,status", [
+    (dict(), dict(n_experts=0), 2),
+    (dict(), dict(top_k=0), 2),
+    (dict(flags=q.FLAG_X_READY), dict(), 2),
+    (dict(path=q.PATH_MMA), dict(), 10),
+    (dict(k=300), dict(), 2),
+    (dict(fmt=7), dict(), 1),
+    (dict(w_len=144 * 2 * 8), dict(n_experts=3), 3),   # two slices given, three claimed
+    (dict(j_start=5, j_end=3), dict(), 4),
+    (dict(n_tokens=300), dict(top_k=300), 2),           # more than 65535 GEMVs
+    (dict(), dict(ids=None), 5),
+    (dict(), dict(ids=16 * 500 + 2), 6),
+    (dict(k=16384 * 4), dict(), 10),                    # beyond the one-token kernel
+])
+def test_experts_rejected_on_host(lib, kw, extra, status):
+    a = _args(**kw)
+    e = dict(ids=16 * 500, n_experts=4, top_k=2)
+    e.update(extra)
+    with pytest.raises(q.QmmError) as ei:
+        q.qmm_matmul_experts(a, e["ids"], e["n_experts"], e["top_k"])
+    assert ei.value.status == status, q.qmm_last_error()
+
+
+def test_experts_empty_work_needs_no_device(lib):
+    # an empty tile: nothing to write, no ids read, no device touched
+    assert q.qmm_matmul_experts(_args(j_start=3, j_end=3), None, 4, 2) == 0
+    # all slices given: w_len = n_experts * slice bytes is accepted
+    assert q.qmm_matmul_experts(_args(w_len=144 * 2 * 8 * 3, j_start=2, j_end=2), 16, 3, 1) == 0
