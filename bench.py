@@ -446,7 +446,8 @@ def measure_other_workloads(torch, q, lib, r, stream, hbm_peak, tc_peak):
         xd = torch.from_numpy(x).to(dev)
         idd = torch.from_numpy(ids).to(dev)
         yd = torch.empty((pairs, n), device=dev)
-        al = [ctypes.byref(q.make_args(fmt, wc[c], xd, yd, k, n, n_pos, stream=stream))
+        al = [ctypes.byref(q.make_args(fmt, wc[c], xd, yd, k, n, n_pos, stream=stream,
+                                       flags=q.FLAG_OVERLAP_PREV | q.FLAG_X_READY))
               for c in range(ncop)]
         ip = ctypes.c_void_p(idd.data_ptr())
 

@@ -48,7 +48,7 @@ extern "C" {
  *       64 high-bit bytes, 16 int8 scales, f16 d), k % 256 == 0.
  * Q8_0: blocks of 32 weights in 34 bytes (f16 d + 32 signed bytes), k % 32 == 0.
  * Q5_0: blocks of 32 weights in 22 bytes (f16 d, a 32-bit word of fifth
- *       bits, 16 nibble bytes), k % 32 == 0 (rullama matmul.rs expert tests).
+ *       bits, 16 nibble bytes), k % 32 == 0 (rullama dispatch/mod.rs expert tests).
  * Inside the blocks the fields follow the standard ggml layouts. */
 typedef enum qmm_format {
     QMM_BF16 = 0,
@@ -183,16 +183,20 @@ int qmm_matmul_backward_input(const qmm_args *a);
  * used. Host only (reads the device's SM count). */
 size_t qmm_backward_input_workspace_bytes(const qmm_args *a);
 
-/* Expert-indexed product (mixture of experts; rullama src/backend/matmul.rs,
- * the expert-matmul tests and `moe_expert_matmul_chained`): W holds n_experts
+/* Expert-indexed product (mixture of experts; rullama src/backend/dispatch/mod.rs,
+ * tests `moe_expert_matmul_q5_0_gpu_vs_cpu` and `moe_expert_matmul_batched_gpu_vs_cpu`): W holds n_experts
  * slices of n rows stacked one after another (each qmm_weight_bytes(fmt, k, n)
  * bytes); a->x is [n_pos x k] with n_pos = a->n_tokens; ids is a DEVICE int32
  * array [n_pos x top_k]; a->y is [n_pos * top_k x n]:
  *     y[p * top_k + s][j] (+)= sum_i x[p][i] * w_{ids[p * top_k + s]}[j][i]
  * for j in [j_start, j_end). a->w_len, when nonzero, must be n_experts times
- * the slice bytes; n_pos * top_k <= 65535; a->flags == 0; a->path AUTO or GEMV
- * (each (position, slot) runs as one GEMV of the one-token path, side by side
- * in one launch; the ids are read on the device, nothing synchronizes). An id
+ * the slice bytes; n_pos * top_k <= 65535; a->path AUTO or GEMV (each
+ * (position, slot) runs as one GEMV of the one-token path, side by side in
+ * one launch; the ids are read on the device, nothing synchronizes).
+ * a->flags as for qmm_matmul_ex, with ids counted as input: under
+ * QMM_FLAG_OVERLAP_PREV alone the kernel waits for the preceding one before
+ * it reads ids (so no weight byte moves before then); QMM_FLAG_X_READY
+ * vouches that neither x nor ids is written by the preceding kernel. An id
  * outside [0, n_experts) leaves that y row untouched and records an error that
  * qmm_device_status reports as QMM_ERR_BAD_ID. Same formats and k limits as the one-token path. */
 int qmm_matmul_experts(const qmm_args *a, const int32_t *ids, int64_t n_experts, int64_t top_k);

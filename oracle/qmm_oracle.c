@@ -19,7 +19,7 @@
  *  - rullama src/backend/dispatch/mod.rs, backward-input parity tests: the
  *    f16 d sits at bytes 0..2 of a Q4_0 block, Q4_K keeps d at 0..2 and
  *    dmin at 2..4, Q6_K keeps d at bytes 208..210.
- *  - rullama src/backend/matmul.rs, the expert-matmul tests (Q8_0 and Q5_0
+ *  - rullama src/backend/dispatch/mod.rs, the expert-matmul tests (Q8_0 and Q5_0
  *    stacked experts): a Q8_0 block is an f16 d then 32 bytes of codes; a
  *    Q5_0 block is an f16 d, a 4-byte little-endian word of high bits, then
  *    16 bytes of nibbles (22 bytes per 32 elements); experts are stacked as

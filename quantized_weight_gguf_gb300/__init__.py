@@ -223,7 +223,7 @@ def matmul_backward_input(fmt, w, dy, k: int, n: int, *, dx=None, j_start=0, j_e
 
 
 def matmul_experts(fmt, w, x, ids, k: int, n: int, n_experts: int, *, y=None, j_start=0,
-                   j_end=0, accumulate=False, stream=None):
+                   j_end=0, accumulate=False, stream=None, flags=0):
     """Expert-indexed product for torch CUDA tensors: w uint8 (n_experts
     stacked slices of n rows), x float32 [n_pos, k], ids int32 [n_pos, top_k]
     on the device. Returns y float32 [n_pos * top_k, n] (the given y when passed)."""
@@ -236,7 +236,7 @@ def matmul_experts(fmt, w, x, ids, k: int, n: int, n_experts: int, *, y=None, j_
     if y is None:
         y = torch.empty((n_pos * top_k, n), dtype=torch.float32, device=x.device)
     a = make_args(fmt, w, x, y, k, n, n_pos, w_len=w.numel() * w.element_size(), j_start=j_start,
-                  j_end=j_end, accumulate=accumulate, stream=stream)
+                  j_end=j_end, accumulate=accumulate, stream=stream, flags=flags)
     qmm_matmul_experts(a, ids, n_experts, top_k)
     return y
 

@@ -371,7 +371,6 @@ int qmm_matmul_experts(const qmm_args *a, const int32_t *ids, int64_t n_experts,
     if (n_experts < 1 || top_k < 1)
         return fail(QMM_ERR_SHAPE, "n_experts %lld and top_k %lld must be >= 1",
                     (long long)n_experts, (long long)top_k);
-    if (a->flags != 0) return fail(QMM_ERR_SHAPE, "expert products take no flags");
     if (a->path == QMM_PATH_MMA) return fail(QMM_ERR_UNSUPPORTED, "expert products run as GEMVs");
     // shape checks of one expert slice (w_len is checked against all slices below)
     qmm_args one = *a;
@@ -409,8 +408,8 @@ int qmm_matmul_experts(const qmm_args *a, const int32_t *ids, int64_t n_experts,
     g.k = a->k; g.n = a->n; g.row_bytes = rb;
     g.j0 = j0; g.j1 = j1;
     g.accumulate = a->accumulate;
-    g.overlap_prev = false;
-    g.x_ready = false;
+    g.overlap_prev = (a->flags & QMM_FLAG_OVERLAP_PREV) != 0;
+    g.x_ready = g.overlap_prev && (a->flags & QMM_FLAG_X_READY) != 0;
     g.ids = ids;
     g.n_experts = (int)n_experts;
     g.top_k = (int)top_k;

@@ -21,6 +21,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 namespace qmm {
 
@@ -47,13 +48,20 @@ struct GemvParams {
     int SB;   // bytes per stage buffer (multiple of 128)
     int NS;   // stage buffers
     unsigned int *err;
-    // expert-indexed calls (ids != null): blockIdx.y = position * top_k + slot
-    // selects the expert slice ids[blockIdx.y] of W, x row position, y row blockIdx.y
+};
+
+// Expert-indexed calls: blockIdx.y = position * top_k + slot selects the
+// expert slice ids[blockIdx.y] of W, x row `position` and y row blockIdx.y.
+// A separate parameter type, so that the plain GEMV's kernel parameters (and
+// its code) stay as they are.
+struct GemvExpParams : GemvParams {
     const int32_t *ids;
     int64_t slice_bytes;
     int n_experts, top_k;
     int64_t n;  // row stride of y
 };
+template <bool EXP>
+using GemvParamsOf = typename std::conditional<EXP, GemvExpParams, GemvParams>::type;
 
 // Weights per unit: a 16-byte chunk for 16-bit formats (lane-contiguous in
 // shared memory), a 32-weight block for Q4_0, a 32-weight sub-block for Q4_K
@@ -333,8 +341,27 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
     return true;
 }
 
-template <int FMT, int UPT>
-__global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
+// Where a CTA's weight slice, x row and y row start: the call's own for a
+// plain GEMV (read from the parameters where used), the selected expert's
+// slice and the pair's rows for an expert-indexed one.
+template <bool EXP>
+struct SliceSel {
+    __device__ __forceinline__ const float *x(const GemvParams &p) const { return p.x; }
+    __device__ __forceinline__ float *y(const GemvParams &p) const { return p.y; }
+    __device__ __forceinline__ int64_t w_off() const { return 0; }
+};
+template <>
+struct SliceSel<true> {
+    const float *xg;
+    float *yg;
+    int64_t off;
+    __device__ __forceinline__ const float *x(const GemvParams &) const { return xg; }
+    __device__ __forceinline__ float *y(const GemvParams &) const { return yg; }
+    __device__ __forceinline__ int64_t w_off() const { return off; }
+};
+
+template <int FMT, int UPT, bool EXP>
+__global__ void __maxnreg__(96) gemv_kernel(const GemvParamsOf<EXP> p) {
     constexpr bool kChunked = (FMT == F_BF16 || FMT == F_F16);  // warp-reduced 16-byte chunks
     extern __shared__ __align__(128) uint8_t smem[];
     const int NS = p.NS, SR = p.SR, SB = p.SB, PU = p.PU;
@@ -356,19 +383,20 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cta = blockIdx.x;
     // byte offset of this call's weight slice, and its x and y rows
-    int64_t w_off = 0;
-    const float *xg = p.x;
-    float *yg = p.y;
-    if (p.ids) {
+    SliceSel<EXP> sel;
+    if constexpr (EXP) {
+        // the ids count as input: produced by the preceding kernel unless the
+        // caller vouched otherwise
+        if (!p.x_ready) pdl_wait_prev();
         const int pair = blockIdx.y;
-        const int e = __ldg(p.ids + pair);
+        const int e = p.x_ready ? __ldg(p.ids + pair) : p.ids[pair];
         if (e < 0 || e >= p.n_experts) {  // nothing read or written for a bad id
             if (threadIdx.x == 0) record_error(p.err, DERR_BAD_ID);
             return;
         }
-        w_off = (int64_t)e * p.slice_bytes;
-        xg = p.x + (int64_t)(pair / p.top_k) * p.k;
-        yg = p.y + (int64_t)pair * p.n;
+        sel.off = (int64_t)e * p.slice_bytes;
+        sel.xg = p.x + (int64_t)(pair / p.top_k) * p.k;
+        sel.yg = p.y + (int64_t)pair * p.n;
     }
     const int64_t r0 = p.j0 + (int64_t)cta * p.rows_base + (cta < p.rows_rem ? cta : p.rows_rem);
     const int64_t nrows = p.rows_base + (cta < p.rows_rem ? 1 : 0);
@@ -402,7 +430,7 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
             }
             const int64_t ra = r0 + (int64_t)s * SR;
             const int64_t rb = min(ra + SR, r0 + nrows);
-            const int64_t A = w_off + ra * R, B = w_off + rb * R;
+            const int64_t A = sel.w_off() + ra * R, B = sel.w_off() + rb * R;
             const int64_t a16 = A & ~(int64_t)15, b16 = (B + 15) & ~(int64_t)15;
             const int64_t tend = min(b16, lim);
             if (B > lim) {  // bytes after the last whole 16-byte chunk of W
@@ -429,8 +457,8 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
     if (!kChunked) {
         const int k = (int)p.k;
         const int U = p.U;
-        if ((reinterpret_cast<uintptr_t>(xg) & 15u) == 0 && (k & 3) == 0) {
-            const float4 *x4 = reinterpret_cast<const float4 *>(xg);
+        if ((reinterpret_cast<uintptr_t>(sel.x(p)) & 15u) == 0 && (k & 3) == 0) {
+            const float4 *x4 = reinterpret_cast<const float4 *>(sel.x(p));
             for (int i = tid; i < k / 4; i += kCons) {
                 const float4 v = __ldg(x4 + i);
                 xs[x_slot<FMT>(4 * i, U)] = v.x;
@@ -439,7 +467,7 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
                 xs[x_slot<FMT>(4 * i + 3, U)] = v.w;
             }
         } else {
-            for (int i = tid; i < k; i += kCons) xs[x_slot<FMT>(i, U)] = __ldg(xg + i);
+            for (int i = tid; i < k; i += kCons) xs[x_slot<FMT>(i, U)] = __ldg(sel.x(p) + i);
         }
         named_barrier(1, kCons);
     }
@@ -460,7 +488,7 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
     for (int q = 0; q < UPT; ++q) {
         const int u = u0 + q * kCons;
         if constexpr (kChunked)
-            unit_init_direct<FMT>(st[q], xg, u, u < p.U);
+            unit_init_direct<FMT>(st[q], sel.x(p), u, u < p.U);
         else
             unit_init<FMT>(st[q], xs, p.U, active && u < p.U ? u : 0, active && u < p.U);
     }
@@ -482,7 +510,7 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
         const int64_t ra = r0 + (int64_t)s * SR;
         const int64_t rb = min(ra + SR, r0 + nrows);
         const int rows_in = (int)(rb - ra);
-        const int64_t a16 = (w_off + ra * R) & ~(int64_t)15;
+        const int64_t a16 = (sel.w_off() + ra * R) & ~(int64_t)15;
         const uint32_t sbase = stage0 + (uint32_t)slot * SB;
         float *pb = part + (ra - fbase) * PU;
         if (!failed && active) {
@@ -493,7 +521,7 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
                 const bool has = rr < rows_in;
                 float acc = 0.0f;
                 if (has) {
-                    const uint32_t rowa = sbase + (uint32_t)(w_off + (ra + rr) * R - a16);
+                    const uint32_t rowa = sbase + (uint32_t)(sel.w_off() + (ra + rr) * R - a16);
 #pragma unroll
                     for (int q = 0; q < UPT; ++q) {
                         const int u = u0 + q * kCons;
@@ -521,7 +549,7 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParams p) {
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
                     if (lane == 0) {
-                        float *yp = yg + fbase + rr;
+                        float *yp = sel.y(p) + fbase + rr;
                         *yp = p.accumulate ? *yp + v : v;
                     }
                 }
@@ -545,18 +573,19 @@ bool gemv_supports(int fmt, int64_t k) {
     return U <= (int64_t)kCons * max_upt(fmt);
 }
 
-template <int FMT, int UPT>
-static cudaError_t launch_t(const GemvParams &p, dim3 grid, size_t smem, cudaStream_t s,
+template <int FMT, int UPT, bool EXP>
+static cudaError_t launch_e(const GemvExpParams &pe, dim3 grid, size_t smem, cudaStream_t s,
                             bool overlap) {
+    const GemvParamsOf<EXP> p = pe;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(gemv_kernel<FMT, UPT>,
+        attr_err = cudaFuncSetAttribute(gemv_kernel<FMT, UPT, EXP>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (!overlap) {
-        gemv_kernel<FMT, UPT><<<grid, kGemvThreads, smem, s>>>(p);
+        gemv_kernel<FMT, UPT, EXP><<<grid, kGemvThreads, smem, s>>>(p);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -569,11 +598,20 @@ static cudaError_t launch_t(const GemvParams &p, dim3 grid, size_t smem, cudaStr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<FMT, UPT>, p);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<FMT, UPT, EXP>, p);
+}
+
+// the expert-indexed kernels are separate instances: the plain GEMV carries
+// no id lookup or slice offset
+template <int FMT, int UPT>
+static cudaError_t launch_t(const GemvExpParams &p, dim3 grid, size_t smem, cudaStream_t s,
+                            bool overlap) {
+    return p.ids ? launch_e<FMT, UPT, true>(p, grid, smem, s, overlap)
+                 : launch_e<FMT, UPT, false>(p, grid, smem, s, overlap);
 }
 
 template <int FMT>
-static cudaError_t launch_chunked(const GemvParams &p, int upt, dim3 grid, size_t smem,
+static cudaError_t launch_chunked(const GemvExpParams &p, int upt, dim3 grid, size_t smem,
                                   cudaStream_t s, bool ov) {
     switch (upt) {
     case 1: return launch_t<FMT, 1>(p, grid, smem, s, ov);
@@ -661,7 +699,7 @@ cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t
     const size_t smem = smem_for(NS, SR, RPF);
     if (smem > 200 * 1024) return cudaErrorNotSupported;
 
-    GemvParams p;
+    GemvExpParams p;
     p.w = g.w; p.x = g.x; p.y = g.y;
     p.k = g.k; p.row_bytes = R;
     p.w_total = R * g.n * (g.ids ? g.n_experts : 1);

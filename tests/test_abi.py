@@ -169,7 +169,7 @@ def test_backward_input_empty_work_needs_no_device(lib):
 @pytest.mark.parametrize("kw,extra,status", [
     (dict(), dict(n_experts=0), 2),
     (dict(), dict(top_k=0), 2),
-    (dict(flags=q.FLAG_X_READY), dict(), 2),
+    (dict(flags=8), dict(), 2),
     (dict(path=q.PATH_MMA), dict(), 10),
     (dict(k=300), dict(), 2),
     (dict(fmt=7), dict(), 1),

@@ -202,3 +202,35 @@ def test_experts_k_zero_and_empty_tile():
     assert np.all(y == 0.0)
     y = _experts("q8_0", w, x, ids, 0, 8, 1, y0=y_in, j_start=4, j_end=4).cpu().numpy()
     assert np.all(y == 3.0)
+
+
+def test_experts_overlapped_launches():
+    """Under programmatic dependent launch: ids rewritten by the preceding
+    kernel are read after it (OVERLAP_PREV alone), and a chain of accumulating
+    calls with X_READY stores in order."""
+    fmt, k, n, n_exp = "q8_0", 2048, 768, 16
+    rng = np.random.default_rng(21)
+    w = qmm_synth.gen_weights(fmt, k, n * n_exp, rng)
+    x = qmm_synth.gen_x(2, k, rng)
+    ids_a = qmm_synth.gen_ids(2, 4, n_exp, rng)
+    ids_b = qmm_synth.gen_ids(2, 4, n_exp, rng)
+    wd, xd = _dev(w), _dev(x)
+    idd = _dev(ids_a)
+    src = _dev(ids_b)
+    y = torch.zeros((8, n), device=DEV)
+    for _ in range(3):
+        idd.copy_(_dev(ids_a))
+        q.matmul_experts(fmt, wd, xd, idd, k, n, n_exp, y=y)
+        idd.copy_(src)   # the preceding kernel writes the ids
+        q.matmul_experts(fmt, wd, xd, idd, k, n, n_exp, y=y, flags=q.FLAG_OVERLAP_PREV)
+    torch.cuda.synchronize()
+    q.qmm_device_status()
+    y_ref, s_ref = oracle.matmul_experts(fmt, w, x, k, n, n_exp, ids_b)
+    _assert(y.cpu().numpy(), y_ref, s_ref, "ids written by the preceding kernel")
+    y.zero_()
+    for _ in range(4):
+        q.matmul_experts(fmt, wd, xd, idd, k, n, n_exp, y=y, accumulate=True,
+                         flags=q.FLAG_OVERLAP_PREV | q.FLAG_X_READY)
+    torch.cuda.synchronize()
+    q.qmm_device_status()
+    _assert(y.cpu().numpy(), 4 * y_ref, 4 * s_ref, "accumulating chain")
