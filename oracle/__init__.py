@@ -71,6 +71,15 @@ def _load():
                                                   p, p]
             lib.oracle_matmul_sampled.restype = ctypes.c_int
             lib.oracle_matmul_sampled.argtypes = [ctypes.c_int, p, p, i64, i64, i64, i64, p, p, p, p, p]
+            lib.oracle_affine_row_bytes.restype = i64
+            lib.oracle_affine_row_bytes.argtypes = [ctypes.c_int, i64]
+            lib.oracle_dequant_affine.restype = ctypes.c_int
+            lib.oracle_dequant_affine.argtypes = [ctypes.c_int, p, p, p, i64, i64, p]
+            lib.oracle_matmul_affine.restype = ctypes.c_int
+            lib.oracle_matmul_affine.argtypes = [ctypes.c_int, p, p, p, p, i64, i64, i64, p, p, p]
+            lib.oracle_matmul_affine_sampled.restype = ctypes.c_int
+            lib.oracle_matmul_affine_sampled.argtypes = [ctypes.c_int, p, p, p, p, i64, i64, i64,
+                                                         i64, p, p, p, p, p]
             _lib = lib
     return _lib
 
@@ -241,3 +250,73 @@ def check(y: np.ndarray, y_ref: np.ndarray, s_ref: np.ndarray, tol: float = TOL_
         idx = np.argwhere(bad)[0]
         msg += f" first bad at {tuple(int(i) for i in idx)}: y={y[tuple(idx)]!r} ref={y_ref[tuple(idx)]!r} S={s_ref[tuple(idx)]!r}"
     return ok, worst, cos, msg
+
+
+# ------------------------------------------------- MLX-style affine rows ----
+# bits = 4 or 8; w: [n, k*bits/8] bytes of little-endian u32 code words;
+# scales, biases: bf16 bit patterns [n, k/64] (uint16).
+
+def affine_row_bytes(bits: int, k: int) -> int:
+    return int(_load().oracle_affine_row_bytes(int(bits), int(k)))
+
+
+def _affine_args(bits, w, scales, biases, k, n):
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    biases = np.ascontiguousarray(biases, dtype=np.uint16)
+    rb = affine_row_bytes(bits, k)
+    if rb < 0 or w.size != rb * n or scales.size != n * (k // 64) or biases.size != scales.size:
+        raise ValueError("bad shapes for an affine matrix")
+    return w, scales, biases
+
+
+def dequant_affine(bits: int, w, scales, biases, k: int, n: int) -> np.ndarray:
+    """fp32 weights [n, k]: code * scale + bias, rounded once."""
+    w, scales, biases = _affine_args(bits, w, scales, biases, k, n)
+    out = np.empty((n, k), np.float32)
+    if _load().oracle_dequant_affine(bits, _ptr(w), _ptr(scales), _ptr(biases), k, n,
+                                     _ptr(out)) != 0:
+        raise ValueError("oracle affine dequant rejected its arguments")
+    return out
+
+
+def matmul_affine(bits: int, w, scales, biases, x, k: int, n: int):
+    """(y, S) of x [N, k] times the affine matrix, f64 [N, n]."""
+    w, scales, biases = _affine_args(bits, w, scales, biases, k, n)
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
+    if x.shape[1] != k:
+        raise ValueError("x must be [N, k]")
+    nt = x.shape[0]
+    y = np.empty((nt, n), np.float64)
+    s = np.empty((nt, n), np.float64)
+    scratch = np.empty(max(k, 1), np.float32)
+    if _load().oracle_matmul_affine(bits, _ptr(w), _ptr(scales), _ptr(biases), _ptr(x), k, n, nt,
+                                    _ptr(y), _ptr(s), _ptr(scratch)) != 0:
+        raise ValueError("oracle affine matmul rejected its arguments")
+    return y, s
+
+
+def matmul_affine_sampled(bits: int, w, scales, biases, x, k: int, n: int, t_idx, j_idx):
+    """(y, S) for the outputs (t_idx[c], j_idx[c]) only."""
+    w, scales, biases = _affine_args(bits, w, scales, biases, k, n)
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
+    t_idx = np.ascontiguousarray(t_idx, dtype=np.int64)
+    j_idx = np.ascontiguousarray(j_idx, dtype=np.int64)
+    cnt = t_idx.size
+    y = np.empty(cnt, np.float64)
+    s = np.empty(cnt, np.float64)
+    scratch = np.empty(max(k, 1), np.float32)
+    rc = _load().oracle_matmul_affine_sampled(bits, _ptr(w), _ptr(scales), _ptr(biases), _ptr(x),
+                                              k, n, x.shape[0], cnt, _ptr(t_idx), _ptr(j_idx),
+                                              _ptr(y), _ptr(s), _ptr(scratch))
+    if rc != 0:
+        raise ValueError("oracle affine sampled matmul rejected its arguments")
+    return y, s
+
+
+def matmul_affine_blas(bits: int, w, scales, biases, x, k: int, n: int):
+    """Same (y, S) as matmul_affine via numpy's f64 product over the oracle's
+    own fp32 weights (for full-size checks)."""
+    deq = dequant_affine(bits, w, scales, biases, k, n).astype(np.float64)
+    x64 = np.atleast_2d(np.asarray(x, np.float64))
+    return x64 @ deq.T, np.abs(x64) @ np.abs(deq).T

@@ -36,6 +36,18 @@
  *    j in [j_start, j_end) (the sum axis is tiled), written on the first
  *    tile and added on the others; dy has n entries, dx has k.
  *
+ *  - moeflux tests/graph_diff_oracle.rs, the `EmbedGatherNTokens` test and
+ *    the `MatvecNTokens (4-bit + 8-bit)` op it names: MLX-style affine
+ *    weights, three arrays per matrix: codes packed into little-endian
+ *    32-bit words ([n][k/8] words at 4 bits, 8 codes per word), a bf16
+ *    scale and a bf16 bias per group of 64 consecutive weights of a row
+ *    ([n][k/64] each), value = code * scale + bias; k a multiple of 64.
+ *    Where the page leaves it open (the code order inside a word, the 8-bit
+ *    packing) the plain reading is taken: code i of a word sits at bits
+ *    bits*i .. bits*i + bits - 1 (lowest first), 32/bits codes per word;
+ *    the value is rounded once to f32 (the page's GPU kernel contracts
+ *    code * scale + bias into one fused multiply-add).
+ *
  * Parity pins live in tests/test_oracle_pins.py (hand-packed blocks with
  * known values, closed-form sizes, exhaustive f16 decode against numpy,
  * identity / one-hot products, brute-force tiny products).
@@ -344,6 +356,105 @@ int oracle_matmul_experts(int fmt, const uint8_t *w, const float *x, int64_t k, 
                 s[(p * top_k + sl) * n + j] = mag;
             }
         }
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * MLX-style affine rows (4 or 8 bits per code, group size 64).
+ * wrow: k*bits/8 bytes of little-endian 32-bit words; srow, brow: k/64 bf16
+ * values each (2 bytes, little-endian). */
+
+static uint32_t rd_u32(const uint8_t *p)
+{
+    return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+}
+
+int64_t oracle_affine_row_bytes(int bits, int64_t k)
+{
+    if ((bits != 4 && bits != 8) || k < 0 || k % 64) return -1;
+    return k * bits / 8;
+}
+
+int oracle_dequant_affine_row(int bits, const uint8_t *wrow, const uint8_t *srow,
+                              const uint8_t *brow, int64_t k, float *out)
+{
+    if (oracle_affine_row_bytes(bits, k) < 0) return -1;
+    const int per_word = 32 / bits;
+    const uint32_t mask = (1u << bits) - 1u;
+    for (int64_t i = 0; i < k; ++i) {
+        uint32_t word = rd_u32(wrow + 4 * (i / per_word));
+        uint32_t q = (word >> (bits * (i % per_word))) & mask;
+        double scale = (double)oracle_bf16_value(rd_u16(srow + 2 * (i / 64)));
+        double bias = (double)oracle_bf16_value(rd_u16(brow + 2 * (i / 64)));
+        /* q * scale is exact in double (at most 8 + 8 significant bits); the
+         * sum is exact too unless bias lies far below half an f32 ulp of it,
+         * so the cast is the one rounding of the exact value */
+        out[i] = (float)((double)q * scale + bias);
+    }
+    return 0;
+}
+
+/* All n rows into out[n][k]; scales and biases are [n][k/64]. */
+int oracle_dequant_affine(int bits, const uint8_t *w, const uint8_t *sc, const uint8_t *bi,
+                          int64_t k, int64_t n, float *out)
+{
+    int64_t rb = oracle_affine_row_bytes(bits, k);
+    if (rb < 0) return -1;
+    for (int64_t j = 0; j < n; ++j)
+        if (oracle_dequant_affine_row(bits, w + j * rb, sc + j * (k / 32), bi + j * (k / 32), k,
+                                      out + j * k))
+            return -1;
+    return 0;
+}
+
+/* y[t][j] = sum_i x[t][i] * w[j][i], s[t][j] = sum_i |x w|, double sums. */
+int oracle_matmul_affine(int bits, const uint8_t *w, const uint8_t *sc, const uint8_t *bi,
+                         const float *x, int64_t k, int64_t n, int64_t n_tokens, double *y,
+                         double *s, float *wrow_scratch)
+{
+    int64_t rb = oracle_affine_row_bytes(bits, k);
+    if (rb < 0) return -1;
+    for (int64_t j = 0; j < n; ++j) {
+        if (oracle_dequant_affine_row(bits, w + j * rb, sc + j * (k / 32), bi + j * (k / 32), k,
+                                      wrow_scratch))
+            return -1;
+        for (int64_t t = 0; t < n_tokens; ++t) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t i = 0; i < k; ++i) {
+                double v = (double)x[t * k + i] * (double)wrow_scratch[i];
+                acc += v;
+                mag += fabs(v);
+            }
+            y[t * n + j] = acc;
+            s[t * n + j] = mag;
+        }
+    }
+    return 0;
+}
+
+/* The same product for `count` chosen outputs (t_idx[c], j_idx[c]). */
+int oracle_matmul_affine_sampled(int bits, const uint8_t *w, const uint8_t *sc,
+                                 const uint8_t *bi, const float *x, int64_t k, int64_t n,
+                                 int64_t n_tokens, int64_t count, const int64_t *t_idx,
+                                 const int64_t *j_idx, double *y, double *s, float *wrow_scratch)
+{
+    int64_t rb = oracle_affine_row_bytes(bits, k);
+    if (rb < 0) return -1;
+    for (int64_t c = 0; c < count; ++c) {
+        int64_t t = t_idx[c], j = j_idx[c];
+        if (t < 0 || t >= n_tokens || j < 0 || j >= n) return -1;
+        if (oracle_dequant_affine_row(bits, w + j * rb, sc + j * (k / 32), bi + j * (k / 32), k,
+                                      wrow_scratch))
+            return -1;
+        double acc = 0.0, mag = 0.0;
+        for (int64_t i = 0; i < k; ++i) {
+            double v = (double)x[t * k + i] * (double)wrow_scratch[i];
+            acc += v;
+            mag += fabs(v);
+        }
+        y[c] = acc;
+        s[c] = mag;
     }
     return 0;
 }

@@ -140,6 +140,43 @@ def expert_workload(name: str, n_pos: int | None = None):
     return fmt, k, n, n_exp, w, x, ids
 
 
+def _bf16_trunc(v: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns of fp32 values by dropping the low 16 bits."""
+    return (np.asarray(v, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def gen_affine(bits: int, k: int, n: int, rng: np.random.Generator):
+    """MLX-style affine matrix (group 64): code words [n, k*bits/8] bytes of
+    uniform random u32 words (every code uniform), bf16 scales U[0.01, 0.06)
+    and biases U[-0.1, 0.1) [n, k/64], each an fp32 draw truncated to bf16."""
+    if bits not in (4, 8) or k % 64:
+        raise ValueError("affine matrices take 4 or 8 bits and k % 64 == 0")
+    w = rng.integers(0, 256, size=n * k * bits // 8, dtype=np.uint8)
+    g = k // 64
+    scales = _bf16_trunc(rng.random((n, g), dtype=np.float32) * 0.05 + 0.01)
+    biases = _bf16_trunc(rng.random((n, g), dtype=np.float32) * 0.2 - 0.1)
+    return w, scales, biases
+
+
+# name -> (bits, k, n, n_tokens, seed)
+AFFINE_WORKLOADS = {
+    "affine4_gemv": (4, 4096, 14336, 1, 10),
+    "affine8_gemv": (8, 4096, 14336, 1, 11),
+    "affine4_prefill": (4, 4096, 14336, 512, 12),
+}
+
+
+def affine_workload(name: str, n_tokens: int | None = None, n: int | None = None):
+    """Seeded (bits, k, n, W code bytes, scales, biases, X [n_tokens, k])."""
+    bits, k, n_full, nt_default, seed = AFFINE_WORKLOADS[name]
+    n = n_full if n is None else n
+    nt = nt_default if n_tokens is None else n_tokens
+    rng = np.random.default_rng(seed)
+    w, scales, biases = gen_affine(bits, k, n, rng)
+    x = gen_x(nt, k, rng)
+    return bits, k, n, w, scales, biases, x
+
+
 def gen_x(n_tokens: int, k: int, rng: np.random.Generator, dist: str = "normal") -> np.ndarray:
     """Activations [n_tokens, k] fp32."""
     if dist == "uniform":

@@ -56,6 +56,16 @@ def test_golden_page_constants():
         elif kind == "offset":
             fmt, field, off = row[1], row[2], int(row[3])
             _check_offset(fmt, field, off)
+        elif kind == "affine":
+            bits, k, rb, groups = (int(v) for v in row[1:5])
+            assert oracle.affine_row_bytes(bits, k) == rb
+            # one scale and one bias per group: the oracle accepts exactly
+            # [n, groups] of each
+            w = np.zeros(rb, np.uint8)
+            sb = np.zeros(groups, np.uint16)
+            oracle.dequant_affine(bits, w, sb, sb, k, 1)
+            with pytest.raises(ValueError):
+                oracle.dequant_affine(bits, w, sb[:-1], sb[:-1], k, 1)
         else:
             raise AssertionError(f"unknown golden kind {kind}")
 
@@ -543,3 +553,114 @@ def test_experts_product_selects_slices():
             assert np.array_equal(y[p * 2 + t], ye[0]) and np.array_equal(s[p * 2 + t], se[0])
     with pytest.raises(ValueError):
         oracle.matmul_experts(fmt, w, x, k, n, n_exp, np.array([[6, 0], [0, 0], [0, 0]], np.int32))
+
+
+
+# ------------------------------------------------- MLX-style affine rows ----
+
+BF16_ONE, BF16_MINUS_ONE, BF16_HALF, BF16_TWO = 0x3F80, 0xBF80, 0x3F00, 0x4000
+
+
+def _words_le(words):
+    return np.array(words, dtype="<u4").view(np.uint8)
+
+
+def test_affine_row_bytes():
+    for k in (64, 128, 4096):
+        assert oracle.affine_row_bytes(4, k) == k // 2
+        assert oracle.affine_row_bytes(8, k) == k
+    assert oracle.affine_row_bytes(4, 32) < 0 and oracle.affine_row_bytes(3, 64) < 0
+
+
+def test_affine4_hand_packed_code_order():
+    """Words 0x76543210, 0xFEDCBA98: codes 0..15 in order (lowest nibble
+    first); scale 1, bias -1 give q - 1 exactly."""
+    w = _words_le([0x76543210, 0xFEDCBA98] * 4)
+    got = oracle.dequant_affine(4, w, np.array([BF16_ONE], np.uint16),
+                                np.array([BF16_MINUS_ONE], np.uint16), 64, 1)[0]
+    assert list(got) == [float(q - 1) for q in list(range(16)) * 4]
+
+
+def test_affine8_hand_packed_code_order():
+    """Bytes 0..63 (four codes per word, lowest byte first); scale 2^-7 (bf16
+    0x3C00), bias 0: value i / 128."""
+    w = np.arange(64, dtype=np.uint8)
+    got = oracle.dequant_affine(8, w, np.array([0x3C00], np.uint16), np.array([0], np.uint16), 64, 1)[0]
+    assert list(got) == [i / 128 for i in range(64)]
+    w = np.full(64, 255, np.uint8)
+    got = oracle.dequant_affine(8, w, np.array([BF16_ONE], np.uint16), np.array([BF16_HALF], np.uint16), 64, 1)[0]
+    assert np.all(got == 255.5)
+
+
+def test_affine_group_index():
+    """Two rows of two groups: each group of 64 takes its own scale and bias,
+    row-major [n, k/64]."""
+    k, n = 128, 2
+    w = _words_le([0x11111111] * 32)            # every code 1
+    scales = np.array([[BF16_ONE, BF16_TWO], [BF16_HALF, BF16_ONE]], np.uint16)
+    biases = np.array([[0, BF16_HALF], [BF16_MINUS_ONE, BF16_TWO]], np.uint16)
+    got = oracle.dequant_affine(4, w, scales, biases, k, n)
+    assert np.all(got[0, :64] == 1.0) and np.all(got[0, 64:] == 2.5)
+    assert np.all(got[1, :64] == -0.5) and np.all(got[1, 64:] == 3.0)
+
+
+def test_affine_4bit_and_8bit_agree_on_small_codes():
+    """The same codes (< 16) packed at 4 and at 8 bits decode alike."""
+    rng = np.random.default_rng(8)
+    k, n = 192, 3
+    codes = rng.integers(0, 16, size=(n, k))
+    w8 = codes.astype(np.uint8).reshape(-1)
+    w4 = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8).reshape(-1)
+    _, scales, biases = qmm_synth.gen_affine(4, k, n, rng)
+    a = oracle.dequant_affine(4, w4, scales, biases, k, n)
+    b = oracle.dequant_affine(8, w8, scales, biases, k, n)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_affine_value_rounds_once():
+    """code 1, scale 1, bias 2^-24 + 2^-30: the exact value lies just above
+    half an f32 ulp past 1 and must round up to 1 + 2^-23 (one rounding of
+    the exact value); bias bf16 pattern 0x3382 = 2^-24 * (1 + 2^-6)."""
+    w = _words_le([0x00000001] + [0] * 7)
+    got = oracle.dequant_affine(4, w, np.array([BF16_ONE], np.uint16), np.array([0x3382], np.uint16), 64, 1)[0]
+    exact = Fraction(1) + Fraction(1, 2 ** 24) + Fraction(1, 2 ** 30)
+    assert oracle.bf16_value(0x3382) == float(Fraction(1, 2 ** 24) + Fraction(1, 2 ** 30))
+    assert float(exact) != 1.0 + 2.0 ** -23
+    assert got[0] == np.float32(1.0 + 2.0 ** -23)
+    assert got[1] == np.float32(2.0 ** -24 + 2.0 ** -30)   # code 0: the bias alone
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_affine_product_closed_form(bits):
+    """Every code c: y = sum_g (c s_g + b_g) sum_{i in g} x_i, in fractions."""
+    k, n, c = 256, 2, (5 if bits == 4 else 200)
+    per = 32 // bits
+    word = sum(c << (bits * i) for i in range(per))
+    w = _words_le([word] * (n * k * bits // 32))
+    rng = np.random.default_rng(6)
+    _, scales, biases = qmm_synth.gen_affine(bits, k, n, rng)
+    x = rng.standard_normal((2, k)).astype(np.float32)
+    y, s = oracle.matmul_affine(bits, w, scales, biases, x, k, n)
+    for t in range(2):
+        for j in range(n):
+            tot = Fraction(0)
+            for g in range(k // 64):
+                sc = Fraction(float(oracle.bf16_value(scales[j, g])))
+                bi = Fraction(float(oracle.bf16_value(biases[j, g])))
+                v = Fraction(float(np.float32(float(c * sc + bi))))   # the weight, rounded once
+                tot += v * sum(Fraction(float(xv)) for xv in x[t, 64 * g:64 * g + 64])
+            assert abs(Fraction(y[t, j]) - tot) <= Fraction(1, 10 ** 9) * (1 + abs(tot))
+
+
+def test_affine_product_matches_numpy_and_sampled():
+    rng = np.random.default_rng(9)
+    k, n = 192, 11
+    w, scales, biases = qmm_synth.gen_affine(4, k, n, rng)
+    x = rng.standard_normal((3, k)).astype(np.float32)
+    y, s = oracle.matmul_affine(4, w, scales, biases, x, k, n)
+    deq = oracle.dequant_affine(4, w, scales, biases, k, n).astype(np.float64)
+    np.testing.assert_allclose(y, x.astype(np.float64) @ deq.T, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(s, np.abs(x.astype(np.float64)) @ np.abs(deq).T, rtol=1e-12)
+    ti, ji = np.array([0, 2, 1]), np.array([10, 0, 5])
+    ys, ss = oracle.matmul_affine_sampled(4, w, scales, biases, x, k, n, ti, ji)
+    assert np.array_equal(ys, y[ti, ji]) and np.array_equal(ss, s[ti, ji])
