@@ -465,6 +465,46 @@ def measure_other_workloads(torch, q, lib, r, stream, hbm_peak, tc_peak):
         out[f"{name}_pos1"] = expert_case(name, 1)
         out[f"{name}_pos4"] = expert_case(name, 4)
 
+    # MLX-style affine matrices: bytes = codes + bf16 scales + bf16 biases
+    aff = lib.qmm_matmul_affine
+
+    def affine_case(name, n_tokens=None, reps=50):
+        bits, k, n, w, sc, bi, x = qmm_synth.affine_workload(name, n_tokens=n_tokens)
+        nt = x.shape[0]
+        total = w.size + sc.nbytes + bi.nbytes
+        ncop = r.copies_for(total)
+        wc = r.weights(w, ncop)
+        sc_c = r.weights(sc.view(np.int16), ncop)
+        bi_c = r.weights(bi.view(np.int16), ncop)
+        xd = torch.from_numpy(x).to(dev)
+        yd = torch.empty((nt, n), device=dev)
+        fl = q.FLAG_OVERLAP_PREV | q.FLAG_X_READY if nt == 1 else 0
+        a0 = q.make_args(f"affine{bits}", wc[0], xd, yd, k, n, nt, stream=stream, flags=fl)
+        need = q.qmm_workspace_bytes(a0)
+        wsb = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        al = [q.make_args(f"affine{bits}", wc[c], xd, yd, k, n, nt, stream=stream, flags=fl,
+                          workspace=wsb if need else None, workspace_bytes=need)
+              for c in range(ncop)]
+        refs = [(ctypes.byref(al[c]), ctypes.c_void_p(sc_c[c].data_ptr()),
+                 ctypes.c_void_p(bi_c[c].data_ptr())) for c in range(ncop)]
+
+        def launch(c):
+            if aff(*refs[c]):
+                raise RuntimeError(q.qmm_last_error())
+        dt = time_loop(torch, launch, reps, 5, ncop, stream)
+        q.qmm_device_status(stream)
+        gbs = total / dt / 1e9
+        res = {"us": dt * 1e6, "weight_gbs": gbs, "frac_hbm": gbs / hbm_peak,
+               "weight_bytes": int(total), "launches_per_call": 1 if nt == 1 else 2}
+        if nt > 1:
+            fl_ = 2.0 * nt * k * n
+            res.update({"tflops": fl_ / dt / 1e12, "frac_bf16_peak": fl_ / dt / 1e12 / tc_peak})
+        return res
+
+    out["affine4_gemv"] = affine_case("affine4_gemv")
+    out["affine8_gemv"] = affine_case("affine8_gemv")
+    out["affine4_prefill_512"] = affine_case("affine4_prefill", reps=20)
+
     # backward with respect to the input, dx = W^T dy: the output head in 8
     # sum-axis tiles (first writes, the rest accumulate), and the Q4_K FFN shape
     bw = lib.qmm_matmul_backward_input

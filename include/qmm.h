@@ -49,7 +49,15 @@ extern "C" {
  * Q8_0: blocks of 32 weights in 34 bytes (f16 d + 32 signed bytes), k % 32 == 0.
  * Q5_0: blocks of 32 weights in 22 bytes (f16 d, a 32-bit word of fifth
  *       bits, 16 nibble bytes), k % 32 == 0 (rullama dispatch/mod.rs expert tests).
- * Inside the blocks the fields follow the standard ggml layouts. */
+ * Inside the blocks the fields follow the standard ggml layouts.
+ * AFFINE4 / AFFINE8: MLX-style affine matrices (moeflux
+ *       tests/graph_diff_oracle.rs, the EmbedGatherNTokens test and the
+ *       MatvecNTokens op it names), three arrays: the codes (w, k/2 or k bytes
+ *       per row: little-endian 32-bit words of 8 four-bit or 4 eight-bit codes,
+ *       lowest bits first), and a bf16 scale and a bf16 bias per group of 64
+ *       consecutive weights of a row ([n][k/64] each); weight = code * scale +
+ *       bias, rounded once to fp32; k % 64 == 0. Only qmm_matmul_affine and
+ *       qmm_dequant_affine take them; qmm_weight_bytes counts the code bytes. */
 typedef enum qmm_format {
     QMM_BF16 = 0,
     QMM_F16 = 1,
@@ -57,7 +65,9 @@ typedef enum qmm_format {
     QMM_Q4_K = 3,
     QMM_Q6_K = 4,
     QMM_Q8_0 = 5,
-    QMM_Q5_0 = 6
+    QMM_Q5_0 = 6,
+    QMM_AFFINE4 = 7,
+    QMM_AFFINE8 = 8
 } qmm_format;
 
 typedef enum qmm_status {
@@ -206,6 +216,20 @@ int qmm_matmul_experts(const qmm_args *a, const int32_t *ids, int64_t n_experts,
  * d*sc*q - dmin*m rounds; every other product is exact). out is device
  * [n][k] fp32. Stream-ordered. */
 int qmm_dequant(int fmt, const void *w, int64_t k, int64_t n, float *out, void *stream);
+
+/* y = x @ W for an affine matrix (a->fmt = QMM_AFFINE4 or QMM_AFFINE8):
+ * a->w holds the code words, `scales` and `biases` the bf16 arrays [n][k/64]
+ * (device memory, 16-byte aligned; NULL only when there is no work). Every
+ * other field as for qmm_matmul_ex: tiles, accumulate, path (one token: the
+ * GEMV; several: the tensor-core path), workspace, stream, flags. Errors as
+ * for qmm_matmul_ex; QMM_ERR_FORMAT for any other format. */
+int qmm_matmul_affine(const qmm_args *a, const void *scales, const void *biases);
+
+/* out[j][i] = the fp32 weight i of row j of an affine matrix, bit-identical
+ * to code * scale + bias rounded once. Device pointers; scales and biases
+ * 2-byte aligned. Stream-ordered. */
+int qmm_dequant_affine(int fmt, const void *w, const void *scales, const void *biases, int64_t k,
+                       int64_t n, float *out, void *stream);
 
 /* Synchronizes `stream`, then reports whether any kernel enqueued so far
  * timed out on a pipeline barrier (QMM_ERR_DEVICE_TIMEOUT) or met an expert

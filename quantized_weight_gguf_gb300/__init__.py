@@ -16,7 +16,8 @@ import os
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libqmm.so")
 
-FORMATS = {"bf16": 0, "f16": 1, "q4_0": 2, "q4_k": 3, "q6_k": 4, "q8_0": 5, "q5_0": 6}
+FORMATS = {"bf16": 0, "f16": 1, "q4_0": 2, "q4_k": 3, "q6_k": 4, "q8_0": 5, "q5_0": 6,
+           "affine4": 7, "affine8": 8}
 PATH_AUTO, PATH_GEMV, PATH_MMA = 0, 1, 2
 FLAG_OVERLAP_PREV = 1
 FLAG_X_READY = 2
@@ -28,7 +29,7 @@ EXPORTS = ("qmm_weight_bytes", "qmm_matmul", "qmm_set_stream", "qmm_matmul_ex",
            "qmm_workspace_bytes", "qmm_select_path", "qmm_matmul_host", "qmm_dequant",
            "qmm_device_status", "qmm_last_error", "qmm_version", "qmm_matmul_noalloc",
            "qmm_matmul_backward_input", "qmm_backward_input_workspace_bytes",
-           "qmm_matmul_experts")
+           "qmm_matmul_experts", "qmm_matmul_affine", "qmm_dequant_affine")
 
 
 class QmmError(RuntimeError):
@@ -76,6 +77,8 @@ def load(path: str = LIB_PATH):
         "qmm_matmul_backward_input": (i, [pa]),
         "qmm_backward_input_workspace_bytes": (sz, [pa]),
         "qmm_matmul_experts": (i, [pa, vp, i64, i64]),
+        "qmm_matmul_affine": (i, [pa, vp, vp]),
+        "qmm_dequant_affine": (i, [i, vp, vp, vp, i64, i64, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -145,6 +148,15 @@ def qmm_matmul_noalloc(args: qmm_args) -> int:
 
 def qmm_matmul_backward_input(args: qmm_args) -> int:
     return _check(load().qmm_matmul_backward_input(ctypes.byref(args)))
+
+
+def qmm_matmul_affine(args: qmm_args, scales, biases) -> int:
+    return _check(load().qmm_matmul_affine(ctypes.byref(args), _ptr(scales), _ptr(biases)))
+
+
+def qmm_dequant_affine(fmt, w, scales, biases, k: int, n: int, out, stream=None) -> int:
+    return _check(load().qmm_dequant_affine(_fmt(fmt), _ptr(w), _ptr(scales), _ptr(biases), k, n,
+                                            _ptr(out), _stream(stream)))
 
 
 def qmm_matmul_experts(args: qmm_args, ids, n_experts: int, top_k: int) -> int:
@@ -246,4 +258,37 @@ def dequant(fmt, w, k: int, n: int, stream=None):
     import torch
     out = torch.empty((n, k), dtype=torch.float32, device=w.device)
     qmm_dequant(fmt, w, k, n, out, stream)
+    return out
+
+
+def matmul_affine(fmt, w, scales, biases, x, k: int, n: int, *, y=None, j_start=0, j_end=0,
+                  accumulate=False, path=PATH_AUTO, workspace=None, workspace_bytes=0,
+                  stream=None, flags=0):
+    """y = x @ W for an affine matrix ("affine4" / "affine8") on torch CUDA
+    tensors: w uint8 code words, scales / biases bf16 or int16 [n, k/64],
+    x float32 [N, k]. Returns y float32 [N, n] (the given y when passed)."""
+    import torch
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    nt = x.shape[0]
+    if y is None:
+        y = torch.empty((nt, n), dtype=torch.float32, device=x.device)
+    a = make_args(fmt, w, x, y, k, n, nt, w_len=w.numel() * w.element_size(), j_start=j_start,
+                  j_end=j_end, accumulate=accumulate, path=path, stream=stream, flags=flags)
+    if workspace is None:
+        need = qmm_workspace_bytes(a)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+            workspace_bytes = need
+    if workspace is not None:
+        a.workspace, a.workspace_bytes = _ptr(workspace), workspace_bytes
+    qmm_matmul_affine(a, scales, biases)
+    return y
+
+
+def dequant_affine(fmt, w, scales, biases, k: int, n: int, stream=None):
+    """fp32 [n, k] weights of an affine matrix (torch CUDA tensors)."""
+    import torch
+    out = torch.empty((n, k), dtype=torch.float32, device=w.device)
+    qmm_dequant_affine(fmt, w, scales, biases, k, n, out, stream)
     return out

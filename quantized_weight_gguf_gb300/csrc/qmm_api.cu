@@ -82,20 +82,23 @@ int64_t row_bytes_of(int fmt, int64_t k) {
     case QMM_Q6_K: return (k % 256 == 0) ? (k / 256) * 210 : -1;
     case QMM_Q8_0: return (k % 32 == 0) ? (k / 32) * 34 : -1;
     case QMM_Q5_0: return (k % 32 == 0) ? (k / 32) * 22 : -1;
+    case QMM_AFFINE4: return (k % 64 == 0) ? k / 2 : -1;
+    case QMM_AFFINE8: return (k % 64 == 0) ? k : -1;
     default: return -1;
     }
 }
 
 const char *fmt_name(int fmt) {
-    static const char *names[] = {"BF16", "F16", "Q4_0", "Q4_K", "Q6_K", "Q8_0", "Q5_0"};
-    return (fmt >= 0 && fmt <= 6) ? names[fmt] : "?";
+    static const char *names[] = {"BF16", "F16", "Q4_0", "Q4_K", "Q6_K", "Q8_0", "Q5_0",
+                                  "AFFINE4", "AFFINE8"};
+    return (fmt >= 0 && fmt <= 8) ? names[fmt] : "?";
 }
 
 // Shape/pointer validation shared by the entry points. On success fills the
 // effective tile and row bytes.
 int validate(const qmm_args *a, int64_t *j0, int64_t *j1, int64_t *rb, bool check_ptrs) {
     if (!a) return fail(QMM_ERR_NULL, "args is NULL");
-    if (a->fmt < QMM_BF16 || a->fmt > QMM_Q5_0)
+    if (a->fmt < QMM_BF16 || a->fmt > QMM_AFFINE8)
         return fail(QMM_ERR_FORMAT, "unknown format code %d", a->fmt);
     if (a->k < 0 || a->n < 0) return fail(QMM_ERR_SHAPE, "negative k or n (k=%lld n=%lld)",
                                           (long long)a->k, (long long)a->n);
@@ -105,7 +108,8 @@ int validate(const qmm_args *a, int64_t *j0, int64_t *j1, int64_t *rb, bool chec
         const char *need = (a->fmt == QMM_Q4_0 || a->fmt == QMM_Q8_0 || a->fmt == QMM_Q5_0)
                                ? "a multiple of 32"
                            : (a->fmt == QMM_Q4_K || a->fmt == QMM_Q6_K) ? "a multiple of 256"
-                                                                        : "even";
+                           : (a->fmt == QMM_AFFINE4 || a->fmt == QMM_AFFINE8) ? "a multiple of 64"
+                                                                              : "even";
         return fail(QMM_ERR_SHAPE, "k %lld must be %s for %s matmul", (long long)a->k, need,
                     fmt_name(a->fmt));
     }
@@ -167,11 +171,26 @@ int library_workspace(size_t need, void **out) {
     return QMM_OK;
 }
 
-int run(const qmm_args *a) {
+bool affine_fmt(int fmt) { return fmt == QMM_AFFINE4 || fmt == QMM_AFFINE8; }
+
+// The product of every entry point. Affine formats come with their scale and
+// bias arrays (sc, bi), which only qmm_matmul_affine passes (affine_entry).
+int run(const qmm_args *a, const void *sc = nullptr, const void *bi = nullptr,
+        bool affine_entry = false) {
     int64_t j0, j1, rb;
     int st = validate(a, &j0, &j1, &rb, true);
     if (st != QMM_OK) return st;
+    if (affine_fmt(a->fmt) != affine_entry)
+        return fail(QMM_ERR_FORMAT, affine_entry
+                                        ? "qmm_matmul_affine takes QMM_AFFINE4 or QMM_AFFINE8"
+                                        : "affine weights need their scales and biases: use "
+                                          "qmm_matmul_affine");
     if (j1 <= j0) return QMM_OK;
+    if (affine_fmt(a->fmt) && a->k > 0) {
+        if (!sc || !bi) return fail(QMM_ERR_NULL, "scales or biases is NULL");
+        if ((reinterpret_cast<uintptr_t>(sc) & 15u) || (reinterpret_cast<uintptr_t>(bi) & 15u))
+            return fail(QMM_ERR_ALIGN, "scales and biases must be 16-byte aligned");
+    }
     qmm::DeviceInfo *dev = nullptr;
     st = device_info(&dev);
     if (st != QMM_OK) return st;
@@ -197,6 +216,8 @@ int run(const qmm_args *a) {
             g.accumulate = a->accumulate;
             g.overlap_prev = (a->flags & QMM_FLAG_OVERLAP_PREV) != 0;
             g.x_ready = g.overlap_prev && (a->flags & QMM_FLAG_X_READY) != 0;
+            g.sc = static_cast<const uint8_t *>(sc);
+            g.bi = static_cast<const uint8_t *>(bi);
             cudaError_t e = qmm::launch_gemv(g, *dev, s);
             if (e != cudaSuccess) return cuda_fail(e, "GEMV launch");
         }
@@ -223,6 +244,8 @@ int run(const qmm_args *a) {
     m.j0 = j0; m.j1 = j1;
     m.accumulate = a->accumulate;
     m.workspace = ws;
+    m.sc = static_cast<const uint8_t *>(sc);
+    m.bi = static_cast<const uint8_t *>(bi);
     cudaError_t e = qmm::launch_mma(m, *dev, s);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core launch");
     return QMM_OK;
@@ -320,6 +343,8 @@ int qmm_matmul_backward_input(const qmm_args *a) {
         return fail(QMM_ERR_SHAPE, "backward-input takes one dy vector (n_tokens %lld != 1)",
                     (long long)a->n_tokens);
     if (a->flags != 0) return fail(QMM_ERR_SHAPE, "backward-input takes no flags");
+    if (affine_fmt(a->fmt))
+        return fail(QMM_ERR_FORMAT, "backward-input takes single-stream (GGUF) formats");
     int64_t j0, j1, rb;
     // x = dy (n entries), y = dx (k entries): the pointer checks of validate()
     // hold for the swapped lengths too
@@ -372,6 +397,8 @@ int qmm_matmul_experts(const qmm_args *a, const int32_t *ids, int64_t n_experts,
         return fail(QMM_ERR_SHAPE, "n_experts %lld and top_k %lld must be >= 1",
                     (long long)n_experts, (long long)top_k);
     if (a->path == QMM_PATH_MMA) return fail(QMM_ERR_UNSUPPORTED, "expert products run as GEMVs");
+    if (affine_fmt(a->fmt))
+        return fail(QMM_ERR_FORMAT, "expert products take single-stream (GGUF) formats");
     // shape checks of one expert slice (w_len is checked against all slices below)
     qmm_args one = *a;
     one.w_len = 0;
@@ -429,6 +456,9 @@ size_t qmm_backward_input_workspace_bytes(const qmm_args *a) {
 
 int qmm_dequant(int fmt, const void *w, int64_t k, int64_t n, float *out, void *stream) {
     t_err[0] = 0;
+    if (affine_fmt(fmt))
+        return fail(QMM_ERR_FORMAT, "%s weights need their scales and biases: use qmm_dequant_affine",
+                    fmt_name(fmt));
     if (fmt < QMM_BF16 || fmt > QMM_Q5_0) return fail(QMM_ERR_FORMAT, "unknown format code %d", fmt);
     if (k < 0 || n < 0) return fail(QMM_ERR_SHAPE, "negative k or n");
     const int64_t r = row_bytes_of(fmt, k);
@@ -442,6 +472,37 @@ int qmm_dequant(int fmt, const void *w, int64_t k, int64_t n, float *out, void *
     if (st != QMM_OK) return st;
     cudaError_t e = qmm::launch_dequant(fmt, static_cast<const uint8_t *>(w), k, n, r, out,
                                         static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QMM_OK : cuda_fail(e, "dequant launch");
+}
+
+int qmm_matmul_affine(const qmm_args *a, const void *scales, const void *biases) {
+    t_err[0] = 0;
+    if (!a) return fail(QMM_ERR_NULL, "args is NULL");
+    return run(a, scales, biases, true);
+}
+
+int qmm_dequant_affine(int fmt, const void *w, const void *scales, const void *biases, int64_t k,
+                       int64_t n, float *out, void *stream) {
+    t_err[0] = 0;
+    if (!affine_fmt(fmt))
+        return fail(QMM_ERR_FORMAT, "qmm_dequant_affine takes QMM_AFFINE4 or QMM_AFFINE8 (got %d)", fmt);
+    if (k < 0 || n < 0) return fail(QMM_ERR_SHAPE, "negative k or n");
+    const int64_t r = row_bytes_of(fmt, k);
+    if (r < 0) return fail(QMM_ERR_SHAPE, "k %lld must be a multiple of 64 for %s", (long long)k,
+                           fmt_name(fmt));
+    if (k == 0 || n == 0) return QMM_OK;
+    if (!w || !scales || !biases || !out) return fail(QMM_ERR_NULL, "w, scales, biases or out is NULL");
+    if ((reinterpret_cast<uintptr_t>(w) & 15u)) return fail(QMM_ERR_ALIGN, "w must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(scales) & 1u) || (reinterpret_cast<uintptr_t>(biases) & 1u))
+        return fail(QMM_ERR_ALIGN, "scales and biases must be 2-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(out) & 3u)) return fail(QMM_ERR_ALIGN, "out must be 4-byte aligned");
+    qmm::DeviceInfo *dev = nullptr;
+    int st = device_info(&dev);
+    if (st != QMM_OK) return st;
+    cudaError_t e = qmm::launch_dequant(fmt, static_cast<const uint8_t *>(w), k, n, r, out,
+                                        static_cast<cudaStream_t>(stream),
+                                        static_cast<const uint8_t *>(scales),
+                                        static_cast<const uint8_t *>(biases));
     return e == cudaSuccess ? QMM_OK : cuda_fail(e, "dequant launch");
 }
 

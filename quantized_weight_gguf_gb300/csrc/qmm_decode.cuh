@@ -20,6 +20,11 @@
 //   Q5_0  (32 w, 22 B): f16 d | u32 qh | 16 bytes; weight i < 16 = low nibble of
 //                       byte i with bit i of qh as bit 4, weight i + 16 = its
 //                       high nibble with bit i + 16 of qh; w = (q - 16) * d.
+//   AFF4 / AFF8 (MLX-style affine, groups of 64): three arrays per matrix --
+//                       codes in little-endian u32 words (8 four-bit or 4
+//                       eight-bit codes per word, lowest bits first), a bf16
+//                       scale and a bf16 bias per group ([n][k/64] each);
+//                       w = fma(q, scale, bias) (q * scale is exact in fp32).
 //   Q6_K (256 w, 210 B): ql[128] | qh[64] | int8 scales[16] | f16 d; for half h and
 //                       l < 32, weight 128h + 32r + l takes nibble (r < 2: low,
 //                       else high) of ql[64h + 32(r & 1) + l] and bits 2r..2r+1 of
@@ -220,5 +225,36 @@ struct Raw32<F_Q5_0> {
         }
     }
 };
+
+// Affine formats: 32 codes (half a group) of row `row`, with the group's
+// scale and bias from the rows `srow` / `brow` of the two bf16 arrays; k0 is
+// a multiple of 32 and every 32-weight unit is whole (k % 64 == 0).
+template <int BITS>
+struct RawAffine {
+    uint32_t qw[BITS];          // 32 codes: BITS words
+    uint32_t sbits, bbits;      // bf16 patterns
+    __device__ __forceinline__ void load(const uint8_t *row, const uint8_t *srow,
+                                         const uint8_t *brow, int64_t k0) {
+        const uint8_t *p = row + (k0 * BITS) / 8;
+#pragma unroll
+        for (int q = 0; q < BITS / 4; ++q) {
+            const uint4 v = ldg_u128(p + 16 * q);
+            qw[4 * q] = v.x; qw[4 * q + 1] = v.y; qw[4 * q + 2] = v.z; qw[4 * q + 3] = v.w;
+        }
+        sbits = ldg_u16(srow + 2 * (k0 >> 6));
+        bbits = ldg_u16(brow + 2 * (k0 >> 6));
+    }
+    __device__ __forceinline__ void decode(float (&w)[32]) const {
+        const float sc = __uint_as_float(sbits << 16), bi = __uint_as_float(bbits << 16);
+        constexpr int per = 32 / BITS;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const uint32_t q = (qw[i / per] >> (BITS * (i % per))) & ((1u << BITS) - 1u);
+            w[i] = __fmaf_rn((float)q, sc, bi);
+        }
+    }
+};
+template <> struct Raw32<F_AFF4> : RawAffine<4> {};
+template <> struct Raw32<F_AFF8> : RawAffine<8> {};
 
 }  // namespace qmm

@@ -6,10 +6,14 @@
 namespace qmm {
 
 // One thread per 32-weight unit (row j, weights 32u .. 32u+31).
+// Affine formats also read their scale and bias rows (aux_row_bytes apart).
 template <int FMT>
 __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict__ w, int64_t k,
                                                       int64_t n, int64_t row_bytes,
-                                                      float *__restrict__ out) {
+                                                      float *__restrict__ out,
+                                                      const uint8_t *__restrict__ sc,
+                                                      const uint8_t *__restrict__ bi,
+                                                      int64_t aux_row_bytes) {
     const int64_t units_per_row = (k + 31) / 32;
     const int64_t total = units_per_row * n;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -19,7 +23,10 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
         const int64_t k0 = 32 * u;
         const int nvalid = (int)((k - k0) < 32 ? (k - k0) : 32);
         Raw32<FMT> raw;
-        raw.load(w + j * row_bytes, k0, nvalid);
+        if constexpr (is_affine(FMT))
+            raw.load(w + j * row_bytes, sc + j * aux_row_bytes, bi + j * aux_row_bytes, k0);
+        else
+            raw.load(w + j * row_bytes, k0, nvalid);
         float v[32];
         raw.decode(v);
         float *o = out + j * k + k0;
@@ -37,20 +44,23 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
 }
 
 cudaError_t launch_dequant(int fmt, const uint8_t *w, int64_t k, int64_t n, int64_t row_bytes,
-                           float *out, cudaStream_t s) {
+                           float *out, cudaStream_t s, const uint8_t *sc, const uint8_t *bi) {
+    const int64_t ab = (k / 64) * 2;
     const int64_t total = ((k + 31) / 32) * n;
     if (total == 0) return cudaSuccess;
     int64_t blocks = (total + 255) / 256;
     if (blocks > (int64_t)1 << 20) blocks = (int64_t)1 << 20;
     const dim3 grid((unsigned)blocks), block(256);
     switch (fmt) {
-    case F_BF16: dequant_kernel<F_BF16><<<grid, block, 0, s>>>(w, k, n, row_bytes, out); break;
-    case F_F16: dequant_kernel<F_F16><<<grid, block, 0, s>>>(w, k, n, row_bytes, out); break;
-    case F_Q4_0: dequant_kernel<F_Q4_0><<<grid, block, 0, s>>>(w, k, n, row_bytes, out); break;
-    case F_Q4_K: dequant_kernel<F_Q4_K><<<grid, block, 0, s>>>(w, k, n, row_bytes, out); break;
-    case F_Q6_K: dequant_kernel<F_Q6_K><<<grid, block, 0, s>>>(w, k, n, row_bytes, out); break;
-    case F_Q8_0: dequant_kernel<F_Q8_0><<<grid, block, 0, s>>>(w, k, n, row_bytes, out); break;
-    case F_Q5_0: dequant_kernel<F_Q5_0><<<grid, block, 0, s>>>(w, k, n, row_bytes, out); break;
+    case F_BF16: dequant_kernel<F_BF16><<<grid, block, 0, s>>>(w, k, n, row_bytes, out, sc, bi, ab); break;
+    case F_F16: dequant_kernel<F_F16><<<grid, block, 0, s>>>(w, k, n, row_bytes, out, sc, bi, ab); break;
+    case F_Q4_0: dequant_kernel<F_Q4_0><<<grid, block, 0, s>>>(w, k, n, row_bytes, out, sc, bi, ab); break;
+    case F_Q4_K: dequant_kernel<F_Q4_K><<<grid, block, 0, s>>>(w, k, n, row_bytes, out, sc, bi, ab); break;
+    case F_Q6_K: dequant_kernel<F_Q6_K><<<grid, block, 0, s>>>(w, k, n, row_bytes, out, sc, bi, ab); break;
+    case F_Q8_0: dequant_kernel<F_Q8_0><<<grid, block, 0, s>>>(w, k, n, row_bytes, out, sc, bi, ab); break;
+    case F_Q5_0: dequant_kernel<F_Q5_0><<<grid, block, 0, s>>>(w, k, n, row_bytes, out, sc, bi, ab); break;
+    case F_AFF4: dequant_kernel<F_AFF4><<<grid, block, 0, s>>>(w, k, n, row_bytes, out, sc, bi, ab); break;
+    case F_AFF8: dequant_kernel<F_AFF8><<<grid, block, 0, s>>>(w, k, n, row_bytes, out, sc, bi, ab); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

@@ -11,8 +11,12 @@
 
 namespace qmm {
 
-enum Fmt : int { F_BF16 = 0, F_F16 = 1, F_Q4_0 = 2, F_Q4_K = 3, F_Q6_K = 4, F_Q8_0 = 5, F_Q5_0 = 6 };
-constexpr int kLastFmt = F_Q5_0;
+enum Fmt : int {
+    F_BF16 = 0, F_F16 = 1, F_Q4_0 = 2, F_Q4_K = 3, F_Q6_K = 4, F_Q8_0 = 5, F_Q5_0 = 6,
+    F_AFF4 = 7, F_AFF8 = 8  // MLX-style affine: code words + bf16 scale and bias per 64
+};
+constexpr int kLastFmt = F_Q5_0;  // the last single-stream (GGUF) format
+__host__ __device__ constexpr bool is_affine(int f) { return f == F_AFF4 || f == F_AFF8; }
 
 // Error codes written to the device error word (first fault wins).
 enum DevErr : unsigned int {
@@ -29,11 +33,13 @@ enum DevErr : unsigned int {
 
 // Block geometry (elements per block, bytes per block) of each format.
 __host__ __device__ constexpr int block_elems(int f) {
-    return (f == F_Q4_0 || f == F_Q8_0 || f == F_Q5_0) ? 32 : (f == F_Q4_K || f == F_Q6_K) ? 256 : 1;
+    return (f == F_Q4_0 || f == F_Q8_0 || f == F_Q5_0) ? 32
+           : (f == F_Q4_K || f == F_Q6_K) ? 256
+           : is_affine(f) ? 64 : 1;
 }
 __host__ __device__ constexpr int block_bytes(int f) {
     return f == F_Q4_0 ? 18 : f == F_Q4_K ? 144 : f == F_Q6_K ? 210 : f == F_Q8_0 ? 34
-           : f == F_Q5_0 ? 22 : 2;
+           : f == F_Q5_0 ? 22 : f == F_AFF4 ? 32 : f == F_AFF8 ? 64 : 2;
 }
 
 // ------------------------------------------------------------ numbers ----

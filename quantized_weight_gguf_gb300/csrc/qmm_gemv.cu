@@ -60,8 +60,36 @@ struct GemvExpParams : GemvParams {
     int n_experts, top_k;
     int64_t n;  // row stride of y
 };
-template <bool EXP>
-using GemvParamsOf = typename std::conditional<EXP, GemvExpParams, GemvParams>::type;
+// Affine formats: the bf16 scale and bias arrays ([n][k/64] each, aux_row_bytes
+// per row, aux_total bytes each) are staged beside the codes of every stage:
+// scales at byte aux_off of the stage buffer, biases aux_sb bytes further.
+struct GemvAffFields {
+    const uint8_t *sc, *bi;
+    int64_t aux_row_bytes, aux_total;
+    int aux_off, aux_sb;
+};
+struct GemvAffParams : GemvParams, GemvAffFields {};
+// everything the host fills in; each kernel instance takes only its own part
+struct GemvHostParams : GemvExpParams, GemvAffFields {};
+
+template <int FMT, bool EXP>
+using GemvParamsOf = typename std::conditional<
+    is_affine(FMT), GemvAffParams,
+    typename std::conditional<EXP, GemvExpParams, GemvParams>::type>::type;
+
+template <int FMT, bool EXP>
+__host__ GemvParamsOf<FMT, EXP> params_of(const GemvHostParams &h) {
+    if constexpr (is_affine(FMT)) {
+        GemvAffParams a;
+        static_cast<GemvParams &>(a) = static_cast<const GemvParams &>(h);
+        static_cast<GemvAffFields &>(a) = static_cast<const GemvAffFields &>(h);
+        return a;
+    } else if constexpr (EXP) {
+        return static_cast<const GemvExpParams &>(h);
+    } else {
+        return static_cast<const GemvParams &>(h);
+    }
+}
 
 // Weights per unit: a 16-byte chunk for 16-bit formats (lane-contiguous in
 // shared memory), a 32-weight block for Q4_0, a 32-weight sub-block for Q4_K
@@ -131,7 +159,7 @@ __device__ __forceinline__ void unit_init(UnitState<FMT> &st, const float *xs, i
         // scale byte of quarter r sits at byte 2r + (gq >> 1) of scales[8h .. 8h+7]
         st.p0 = 8 * (0 + (gq >> 1)); st.p1 = 8 * (2 + (gq >> 1));
         st.p2 = st.p0; st.p3 = st.p1;
-    } else if (FMT == F_Q5_0) {
+    } else if (FMT == F_Q5_0 || is_affine(FMT)) {
         float sx = 0.0f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) sx += st.xr[i];
@@ -330,6 +358,54 @@ __device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<
     }
 }
 
+// Partial dot of one 32-weight unit (half a group) of an affine row: codes at
+// `rowa`, the row's scales at `auxa`, its biases aux_sb bytes further.
+//   sum_i (q_i s + b) x_i = s * sum q x + b * sum x
+template <int FMT>
+__device__ __forceinline__ float unit_dot_aff(uint32_t rowa, uint32_t auxa, uint32_t aux_sb, int u,
+                                              const UnitState<FMT> &st) {
+    const uint32_t ga = auxa + 2u * (uint32_t)(u >> 1);
+    const float sc = __uint_as_float(lds16(ga) << 16);
+    const float bi = __uint_as_float(lds16(ga + aux_sb) << 16);
+    float2 a0 = make_float2(0.f, 0.f), a1 = a0;
+    if (FMT == F_AFF4) {
+        // word i holds elements 8i .. 8i+7, lowest nibble first: byte j of the
+        // low-nibble mask is element 8i + 2j, of the high-nibble mask 8i + 2j + 1;
+        // codes ride the exact carrier 0.5 + q/256 and
+        // sum q x = 256 * sum (0.5 + q/256) x - 128 * sum x
+        const uint4 v = lds128(rowa + 16u * u);
+        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = wd[i] & 0x0F0F0F0Fu, hi = (wd[i] >> 4) & 0x0F0F0F0Fu;
+            a0 = ffma2(make_float2(byte_half_plus<0>(lo), byte_half_plus<0>(hi)),
+                       make_float2(st.xr[8 * i], st.xr[8 * i + 1]), a0);
+            a1 = ffma2(make_float2(byte_half_plus<1>(lo), byte_half_plus<1>(hi)),
+                       make_float2(st.xr[8 * i + 2], st.xr[8 * i + 3]), a1);
+            a0 = ffma2(make_float2(byte_half_plus<2>(lo), byte_half_plus<2>(hi)),
+                       make_float2(st.xr[8 * i + 4], st.xr[8 * i + 5]), a0);
+            a1 = ffma2(make_float2(byte_half_plus<3>(lo), byte_half_plus<3>(hi)),
+                       make_float2(st.xr[8 * i + 6], st.xr[8 * i + 7]), a1);
+        }
+        const float a = (a0.x + a0.y) + (a1.x + a1.y);
+        return fmaf(256.0f * sc, a, fmaf(-128.0f, sc, bi) * st.c0);
+    } else {
+        // 8-bit codes: element 4i + j is byte j of word i; 2^23 + q - 2^23 = q exactly
+        const uint4 v0 = lds128(rowa + 32u * u), v1 = lds128(rowa + 32u * u + 16u);
+        const uint32_t wd[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        const float2 zp = make_float2(-8388608.0f, -8388608.0f);  // -2^23
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float2 f = fadd2(make_float2(byte_magic23<0>(wd[i]), byte_magic23<1>(wd[i])), zp);
+            a0 = ffma2(f, make_float2(st.xr[4 * i], st.xr[4 * i + 1]), a0);
+            f = fadd2(make_float2(byte_magic23<2>(wd[i]), byte_magic23<3>(wd[i])), zp);
+            a1 = ffma2(f, make_float2(st.xr[4 * i + 2], st.xr[4 * i + 3]), a1);
+        }
+        const float a = (a0.x + a0.y) + (a1.x + a1.y);
+        return fmaf(sc, a, bi * st.c0);
+    }
+}
+
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
                                               volatile int *abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -361,7 +437,7 @@ struct SliceSel<true> {
 };
 
 template <int FMT, int UPT, bool EXP>
-__global__ void __maxnreg__(96) gemv_kernel(const GemvParamsOf<EXP> p) {
+__global__ void __maxnreg__(96) gemv_kernel(const GemvParamsOf<FMT, EXP> p) {
     constexpr bool kChunked = (FMT == F_BF16 || FMT == F_F16);  // warp-reduced 16-byte chunks
     extern __shared__ __align__(128) uint8_t smem[];
     const int NS = p.NS, SR = p.SR, SB = p.SB, PU = p.PU;
@@ -438,8 +514,30 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParamsOf<EXP> p) {
                     stages[(int64_t)slot * SB + (q - a16)] = p.w[q];
             }
             const uint32_t tx = tend > a16 ? (uint32_t)(tend - a16) : 0u;
-            mbar_arrive_expect_tx(full(slot), tx);
-            if (tx) bulk_g2s(stage0 + (uint32_t)slot * SB, p.w + a16, tx, full(slot));
+            if constexpr (is_affine(FMT)) {
+                // the stage's rows of the scale and bias arrays, the same way
+                const int64_t AR = p.aux_row_bytes, alim = p.aux_total & ~(int64_t)15;
+                const int64_t SA = ra * AR, SE = rb * AR;
+                const int64_t s16 = SA & ~(int64_t)15;
+                const int64_t send = min((SE + 15) & ~(int64_t)15, alim);
+                const int64_t sdst = (int64_t)slot * SB + p.aux_off;
+                if (SE > alim) {
+                    for (int64_t q = max(s16, alim); q < SE; ++q) {
+                        stages[sdst + (q - s16)] = p.sc[q];
+                        stages[sdst + p.aux_sb + (q - s16)] = p.bi[q];
+                    }
+                }
+                const uint32_t atx = send > s16 ? (uint32_t)(send - s16) : 0u;
+                mbar_arrive_expect_tx(full(slot), tx + 2u * atx);
+                if (tx) bulk_g2s(stage0 + (uint32_t)slot * SB, p.w + a16, tx, full(slot));
+                if (atx) {
+                    bulk_g2s(stage0 + (uint32_t)sdst, p.sc + s16, atx, full(slot));
+                    bulk_g2s(stage0 + (uint32_t)(sdst + p.aux_sb), p.bi + s16, atx, full(slot));
+                }
+            } else {
+                mbar_arrive_expect_tx(full(slot), tx);
+                if (tx) bulk_g2s(stage0 + (uint32_t)slot * SB, p.w + a16, tx, full(slot));
+            }
             ++issued;
         }
         // no copy may land after this CTA exits
@@ -522,10 +620,22 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParamsOf<EXP> p) {
                 float acc = 0.0f;
                 if (has) {
                     const uint32_t rowa = sbase + (uint32_t)(sel.w_off() + (ra + rr) * R - a16);
+                    if constexpr (is_affine(FMT)) {
+                        const int64_t AR = p.aux_row_bytes;
+                        const uint32_t auxa = sbase + (uint32_t)p.aux_off +
+                                              (uint32_t)((ra + rr) * AR - ((ra * AR) & ~(int64_t)15));
 #pragma unroll
-                    for (int q = 0; q < UPT; ++q) {
-                        const int u = u0 + q * kCons;
-                        if ((UPT == 1 && !kChunked) || u < p.U) acc += unit_dot<FMT>(rowa, u, st[q]);
+                        for (int q = 0; q < UPT; ++q) {
+                            const int u = u0 + q * kCons;
+                            if (UPT == 1 || u < p.U)
+                                acc += unit_dot_aff<FMT>(rowa, auxa, (uint32_t)p.aux_sb, u, st[q]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < UPT; ++q) {
+                            const int u = u0 + q * kCons;
+                            if ((UPT == 1 && !kChunked) || u < p.U) acc += unit_dot<FMT>(rowa, u, st[q]);
+                        }
                     }
                 }
                 if (SEG) {
@@ -566,7 +676,8 @@ static int unit_k(int fmt) { return (fmt == F_BF16 || fmt == F_F16) ? 8 : 32; }
 static int max_upt(int fmt) { return (fmt == F_BF16 || fmt == F_F16) ? 8 : 2; }
 
 bool gemv_supports(int fmt, int64_t k) {
-    if (fmt < F_BF16 || fmt > kLastFmt || k <= 0) return false;
+    if (fmt < F_BF16 || (fmt > kLastFmt && !is_affine(fmt)) || k <= 0) return false;
+    if (is_affine(fmt) && k % 64) return false;
     const int uk = unit_k(fmt);
     if (k % uk) return false;
     const int64_t U = k / uk;
@@ -574,9 +685,9 @@ bool gemv_supports(int fmt, int64_t k) {
 }
 
 template <int FMT, int UPT, bool EXP>
-static cudaError_t launch_e(const GemvExpParams &pe, dim3 grid, size_t smem, cudaStream_t s,
+static cudaError_t launch_e(const GemvHostParams &h, dim3 grid, size_t smem, cudaStream_t s,
                             bool overlap) {
-    const GemvParamsOf<EXP> p = pe;
+    const GemvParamsOf<FMT, EXP> p = params_of<FMT, EXP>(h);
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
@@ -604,14 +715,19 @@ static cudaError_t launch_e(const GemvExpParams &pe, dim3 grid, size_t smem, cud
 // the expert-indexed kernels are separate instances: the plain GEMV carries
 // no id lookup or slice offset
 template <int FMT, int UPT>
-static cudaError_t launch_t(const GemvExpParams &p, dim3 grid, size_t smem, cudaStream_t s,
+static cudaError_t launch_t(const GemvHostParams &p, dim3 grid, size_t smem, cudaStream_t s,
                             bool overlap) {
-    return p.ids ? launch_e<FMT, UPT, true>(p, grid, smem, s, overlap)
-                 : launch_e<FMT, UPT, false>(p, grid, smem, s, overlap);
+    if constexpr (is_affine(FMT)) {
+        if (p.ids) return cudaErrorNotSupported;  // no expert-indexed affine matrices
+        return launch_e<FMT, UPT, false>(p, grid, smem, s, overlap);
+    } else {
+        return p.ids ? launch_e<FMT, UPT, true>(p, grid, smem, s, overlap)
+                     : launch_e<FMT, UPT, false>(p, grid, smem, s, overlap);
+    }
 }
 
 template <int FMT>
-static cudaError_t launch_chunked(const GemvExpParams &p, int upt, dim3 grid, size_t smem,
+static cudaError_t launch_chunked(const GemvHostParams &p, int upt, dim3 grid, size_t smem,
                                   cudaStream_t s, bool ov) {
     switch (upt) {
     case 1: return launch_t<FMT, 1>(p, grid, smem, s, ov);
@@ -653,9 +769,15 @@ cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t
     const int ctas_target = std::max(1, 2 * dev.sm_count / pairs);
     const int64_t per_cta = (M + ctas_target - 1) / ctas_target;
     const size_t xs_bytes = chunked ? 0 : (size_t)4 * (g.k + uk);
+    // affine formats: scale and bias rows of the stage beside its codes
+    const bool aff = is_affine(g.fmt);
+    const int64_t AR = aff ? (g.k / 64) * 2 : 0;
+    auto code_bytes = [&](int64_t sr) { return ((sr * R + 32) + 127) & ~(int64_t)127; };
+    auto aux_bytes = [&](int64_t sr) { return aff ? ((sr * AR + 32) + 127) & ~(int64_t)127 : 0; };
+    auto stage_bytes = [&](int64_t sr) { return code_bytes(sr) + 2 * aux_bytes(sr); };
     auto smem_for = [&](int ns, int64_t sr, int64_t rpf) {
         const size_t part_bytes = (size_t)4 * rpf * PU;
-        const size_t sb = (size_t)(((sr * R + 32) + 127) & ~(int64_t)127);
+        const size_t sb = (size_t)stage_bytes(sr);
         return (size_t)((((16 * ns + 16 + part_bytes + 127) & ~(size_t)127) + xs_bytes + 127) &
                         ~(size_t)127) +
                (size_t)ns * sb;
@@ -692,15 +814,21 @@ cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t
             while (NS > 2 && smem_for(NS, SR, RPF) > 200 * 1024) --NS;
         }
     }
-    const int SB = (int)(((SR * R + 32) + 127) & ~(int64_t)127);
+    const int SB = (int)stage_bytes(SR);
     const int64_t nstage_total = (M + SR - 1) / SR;
     const int gx = (int)std::max<int64_t>(1, std::min<int64_t>(nstage_total, ctas_target));
     const dim3 grid((unsigned)gx, (unsigned)pairs);
     const size_t smem = smem_for(NS, SR, RPF);
     if (smem > 200 * 1024) return cudaErrorNotSupported;
 
-    GemvExpParams p;
+    GemvHostParams p;
     p.w = g.w; p.x = g.x; p.y = g.y;
+    p.sc = g.sc;
+    p.bi = g.bi;
+    p.aux_row_bytes = AR;
+    p.aux_total = AR * g.n;
+    p.aux_off = (int)code_bytes(SR);
+    p.aux_sb = (int)aux_bytes(SR);
     p.k = g.k; p.row_bytes = R;
     p.w_total = R * g.n * (g.ids ? g.n_experts : 1);
     p.ids = g.ids;
@@ -724,6 +852,8 @@ cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t
     case F_Q6_K: return upt == 1 ? launch_t<F_Q6_K, 1>(p, grid, smem, s, ov) : launch_t<F_Q6_K, 2>(p, grid, smem, s, ov);
     case F_Q8_0: return upt == 1 ? launch_t<F_Q8_0, 1>(p, grid, smem, s, ov) : launch_t<F_Q8_0, 2>(p, grid, smem, s, ov);
     case F_Q5_0: return upt == 1 ? launch_t<F_Q5_0, 1>(p, grid, smem, s, ov) : launch_t<F_Q5_0, 2>(p, grid, smem, s, ov);
+    case F_AFF4: return upt == 1 ? launch_t<F_AFF4, 1>(p, grid, smem, s, ov) : launch_t<F_AFF4, 2>(p, grid, smem, s, ov);
+    case F_AFF8: return upt == 1 ? launch_t<F_AFF8, 1>(p, grid, smem, s, ov) : launch_t<F_AFF8, 2>(p, grid, smem, s, ov);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -30,6 +30,8 @@ struct GemvLaunch {
     // q < pairs uses slice ids[q], x row q / top_k and y row q (device ids)
     const int32_t *ids = nullptr;
     int n_experts = 0, top_k = 1, pairs = 1;
+    // affine formats: bf16 scale and bias arrays [n][k/64]
+    const uint8_t *sc = nullptr, *bi = nullptr;
 };
 // Returns cudaSuccess or the launch error; cudaErrorNotSupported when no
 // GEMV variant takes the shape (the caller then uses the tensor-core path).
@@ -46,6 +48,8 @@ struct MmaLaunch {
     int64_t j0, j1;
     int accumulate;
     void *workspace;        // >= mma_workspace_bytes(fmt, n_tokens, k)
+    // affine formats: bf16 scale and bias arrays [n][k/64]
+    const uint8_t *sc = nullptr, *bi = nullptr;
 };
 size_t mma_workspace_bytes(int fmt, int64_t n_tokens, int64_t k);
 int mma_mode(int fmt, int64_t k);  // 1: W16.X16, 2: x split, 3: w and x split
@@ -69,8 +73,10 @@ size_t back_input_workspace_bytes(int fmt, int64_t k, int64_t n, int64_t j0, int
 cudaError_t launch_back_input(const BackLaunch &b, const DeviceInfo &dev, cudaStream_t s);
 
 // Standalone dequantization of n rows into out[n][k].
+// Affine formats pass their bf16 scale and bias arrays ([n][k/64] each).
 cudaError_t launch_dequant(int fmt, const uint8_t *w, int64_t k, int64_t n, int64_t row_bytes,
-                           float *out, cudaStream_t s);
+                           float *out, cudaStream_t s, const uint8_t *sc = nullptr,
+                           const uint8_t *bi = nullptr);
 
 // y[t][j] = 0 for j in [j0, j1) (k == 0 with accumulate == 0).
 cudaError_t launch_zero_cols(float *y, int64_t n_tokens, int64_t n, int64_t j0, int64_t j1,

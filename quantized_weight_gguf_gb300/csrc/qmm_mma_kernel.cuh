@@ -1,0 +1,915 @@
+// qmm_mma_kernel.cuh -- N-token fused dequantize + tensor-core product on sm_103a:
+// Y[t][j] = sum_i X[t][i] W[j][i] for a tile of 128 output columns j and BN
+// tokens t per CTA.
+//
+// CTAs run in clusters of two: the pair works on adjacent 128-row tiles of W
+// and the same tokens, and each CTA fetches half of every X tile with a TMA
+// multicast into both CTAs' shared memory, halving the L2 traffic for X.
+// Pipeline per CTA (one CTA per SM, warp-specialised):
+//   warp 0      TMA producer: its half of each fp16 X tile [BN tokens x 64 k]
+//               -> shared memory of both CTAs (128-byte swizzle);
+//   warp 1      allocates the fp32 accumulator in tensor memory (TMEM) and one
+//               lane issues tcgen05.mma (M=128, N=BN, K=16, fp16 in, fp32 acc);
+//   warps 2..17 dequantize W in two groups of 8 warps that take alternate
+//               k-steps: thread (r, h) turns 32 weights of row r per k-step
+//               into fp16 and stores them in the same swizzled K-major layout
+//               the MMA descriptor describes; after the k-loop all 16 warps
+//               drain the accumulator TMEM -> registers -> y.
+// X is converted to fp16 once per call by a small kernel that also scales each
+// token row by a power of two (exact) so it fits fp16's range; the epilogue
+// multiplies by the inverse power.
+//
+// Precision modes (fp16 operands round each product's inputs to 11 bits; the
+// resulting error relative to sum |x w| shrinks like 1/sqrt(k)):
+//   MODE 1  W16 . X16                      one product per output
+//   MODE 2  W16 . (X_hi + X_lo)            x split into two fp16 terms: the B
+//           tile holds BN/2 tokens' hi rows then their lo rows, and the
+//           epilogue adds column c and c + BN/2 (exact for fp16-exact W)
+//   MODE 3  (W_hi + W_lo) . (X_hi + X_lo)  also w split: the A tile holds 64
+//           rows' hi parts then their lo parts; the epilogue adds the row
+//           pair through shared memory.
+//
+// The kernel and its launch templates live here; qmm_mma.cu holds the host
+// planning and the x conversion, and the qmm_mma_inst_*.cu units instantiate
+// the kernel for groups of formats (compiled in parallel).
+#pragma once
+#include <cuda.h>
+
+#include <algorithm>
+#include <mutex>
+#include <type_traits>
+
+#include "qmm_decode.cuh"
+#include "qmm_internal.h"
+
+namespace qmm {
+
+constexpr int kDeqWarps = 16;                     // two groups of 8, alternate k-steps
+constexpr int kRawWarp = 2 + kDeqWarps;             // streams raw Q4_K tiles
+constexpr int kMmaThreads = 32 * (kRawWarp + 1);
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+
+struct MmaParams {
+    const uint8_t *w;
+    float *y;
+    const float *xscale;
+    int64_t k, n, n_tokens, row_bytes;
+    int64_t j0, j1;
+    int KS;
+    int accumulate;
+    int pairs;       // pairs of 128-row tiles (a cluster of two CTAs takes one pair)
+    int tiles_n;     // token tiles
+    int full_units;  // pair-tiles computed whole (the first units)
+    int split;       // the remaining pair-tiles are computed as `split` k-ranges each
+    int n_units;     // full_units + (pairs * tiles_n - full_units) * split
+    unsigned int *err;
+};
+
+// Affine formats also read a bf16 scale and bias per group of 64 from two
+// arrays [n][k/64] (aux_row_bytes per row). A separate parameter type: the
+// other formats' kernels keep their parameters as they are.
+struct MmaAffFields {
+    const uint8_t *sc, *bi;
+    int64_t aux_row_bytes;
+};
+struct MmaAffParams : MmaParams, MmaAffFields {};
+template <int FMT>
+using MmaParamsOf = typename std::conditional<is_affine(FMT), MmaAffParams, MmaParams>::type;
+
+// Q4_K super-blocks of 128 rows staged raw by TMA (one 128 x 144-byte box per
+// 256-wide slice of k), then decoded from shared memory.
+constexpr int kRawBytes = kBM * 144;
+
+// Tensor memory (512 columns x 128 lanes of 32 bits, all taken by the one CTA
+// on the SM): the fp32 accumulator(s) first, then a ring of NA dequantized W
+// stages (A operand: row r on lane r, k pairs packed per column, 32 columns
+// per 64-wide k-step). Shared memory: a ring of NB x stages (streamed from
+// L2 by TMA) and, for Q4_K, kNR raw super-block tiles of 128 rows.
+//
+// A stage is KA = 4 k-steps (one 256-wide super-block): each dequant thread
+// then pays one raw-tile wait, one slot wait and one arrival per two decoded
+// chunks. An x stage is KB k-steps, 32 KB at most (the x tile of 256 tokens
+// is 32 KB per k-step).
+template <int BN, bool RAW>
+struct MmaCfg {
+    static constexpr int KA = 4;
+    static constexpr int KB = BN >= 256 ? 1 : (BN >= 128 ? 2 : 4);
+    static constexpr int kBBytes = BN * kBK * 2;            // one k-step of x
+    static constexpr int kBStage = KB * kBBytes;
+    static constexpr int kAccCols = BN < 32 ? 32 : BN;      // one accumulator
+    // two accumulators (even k-steps into one, odd into the other, summed at
+    // the end) where TMEM has room: back-to-back MMAs then do not wait on
+    // each other's result
+    static constexpr int kNAcc = BN >= 256 ? 1 : 2;
+    static constexpr int kACol0 = kNAcc * kAccCols;         // first A column
+    static constexpr int kAStageCols = KA * 32;
+    static constexpr int kNAFit = (512 - kACol0) / kAStageCols;
+    static constexpr int NA = kNAFit > 3 ? 3 : kNAFit;
+    static constexpr int kCols = 512;
+    // raw W stages: as many as fit, up to 4, next to a minimum x ring of four
+    // k-steps; HBM latency is hidden by the raw ring, L2 latency by the x ring
+    static constexpr int kNBMin = (4 + KB - 1) / KB;
+    static constexpr int kRawFit = (212 * 1024 - kNBMin * kBStage) / kRawBytes;
+    static constexpr int kNR = RAW ? (kRawFit > 4 ? 4 : kRawFit) : 1;
+    static_assert(!RAW || kNR >= 2, "raw W ring too shallow");
+    static constexpr int kAvail = 212 * 1024 - (RAW ? kNR * kRawBytes : 0);
+    static constexpr int NB = (kAvail / kBStage) > 8 ? 8 : (kAvail / kBStage);
+    static constexpr size_t kSmemUsed = (size_t)NB * kBStage +
+                                        (RAW ? (size_t)kNR * kRawBytes : 0) + 1024 /*align*/ +
+                                        512 /*barriers*/ + 2048 /*token scales*/;
+    // at least half of the SM's shared memory, so that no second CTA can be
+    // resident and block in its TMEM allocation (every CTA takes all 512
+    // columns) while holding resources its cluster peer waits for
+    static constexpr size_t kSmem = kSmemUsed < 120 * 1024 ? 120 * 1024 : kSmemUsed;
+    // the output tile (rows x tokens fp32) is staged over the x ring
+    static_assert(NB * kBStage >= kBM * BN * 4, "x ring too small for the output tile");
+    static_assert(NB >= 2 && NA >= 2, "rings too shallow");
+};
+
+__device__ __forceinline__ bool wait_abortable(uint32_t bar, uint32_t parity,
+                                               volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// 32 weights -> 16 fp16x2 words, generic formats: exact fp32, then RN to fp16.
+template <int FMT>
+__device__ __forceinline__ void to_half_words(const Raw32<FMT> &raw, uint32_t (&hw)[16]) {
+    float v[32];
+    raw.decode(v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) hw[i] = pack_half2(v[2 * i], v[2 * i + 1]);
+}
+
+// Q4_K: w = ds*q - dm computed as (256 ds) * (0.5 + q/256) - (128 ds + dm),
+// one fp32 fma per weight, then RN to fp16 (the fp16 rounding dominates).
+template <>
+__device__ __forceinline__ void to_half_words<F_Q4_K>(const Raw32<F_Q4_K> &raw,
+                                                      uint32_t (&hw)[16]) {
+    uint32_t sc, m;
+    q4k_scale_min(raw.hdr.y, raw.hdr.z, raw.hdr.w, raw.s, sc, m);
+    const float d = f16_bits_to_f32(raw.hdr.x & 0xFFFFu);
+    const float dmin = f16_bits_to_f32(raw.hdr.x >> 16);
+    const float ds = d * (float)sc;
+    const float a = 256.0f * ds;
+    const float c = -fmaf(128.0f, ds, dmin * (float)m);
+    const float2 av = make_float2(a, a), cv = make_float2(c, c);
+    const uint32_t sh = (raw.s & 1) ? 4u : 0u;
+    const uint32_t wd[8] = {raw.qs[0].x, raw.qs[0].y, raw.qs[0].z, raw.qs[0].w,
+                            raw.qs[1].x, raw.qs[1].y, raw.qs[1].z, raw.qs[1].w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t nib = (wd[i] >> sh) & 0x0F0F0F0Fu;
+        const float2 f01 = ffma2(av, make_float2(byte_half_plus<0>(nib), byte_half_plus<1>(nib)), cv);
+        const float2 f23 = ffma2(av, make_float2(byte_half_plus<2>(nib), byte_half_plus<3>(nib)), cv);
+        hw[2 * i] = pack_half2(f01.x, f01.y);
+        hw[2 * i + 1] = pack_half2(f23.x, f23.y);
+    }
+}
+
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t v) {
+    return *reinterpret_cast<const __half2 *>(&v);
+}
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) {
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// Half h of a Q4_K 64-weight chunk c: quant bytes 16h .. 16h+15 of the chunk (q),
+// i.e. weights 16h + 0..15 (low nibbles, sub-block 2c) and 32 + 16h + 0..15
+// (high nibbles, sub-block 2c+1) -> 16 fp16x2 words: 0..7 low, 8..15 high.
+//
+// All in fp16x2 arithmetic, two weights per instruction:
+//   a nibble pair becomes (1024 + q) exactly by OR-ing it into the fp16
+//   pattern of 1024 (a high nibble, kept in place, gives 1024 + 16 q);
+//   sc * q = (1024 + q) * sc - 1024 sc is exact in one fma (the result is an
+//   integer below 2048; 1024 sc and sc / 16 are exact in fp16);
+//   w = d * (sc q) - fp16(dmin m) is then rounded once.
+// Only dmin * m picks up an extra fp16 rounding against RN(ds q - dm); the
+// error stays at the level of rounding w itself.
+__device__ __forceinline__ void q4k_half_chunk_to_half(const uint4 &hdr, const uint4 &q, int c,
+                                                       uint32_t (&hw)[16]) {
+    uint32_t sc0, m0, sc1, m1;
+    q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * c, sc0, m0);
+    q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * c + 1, sc1, m1);
+    // small integers v < 1024 as exact fp16 pairs: (1024 + v) - 1024
+    auto int_h2 = [](uint32_t v) {
+        return __hsub2(u32_as_h2((0x6400u | v) * 0x10001u), u32_as_h2(0x64006400u));
+    };
+    const __half2 d2 = u32_as_h2((hdr.x & 0xFFFFu) * 0x10001u);
+    const __half2 dmin2 = u32_as_h2((hdr.x >> 16) * 0x10001u);
+    const __half2 s0 = int_h2(sc0);
+    const __half2 n0 = __hmul2(s0, u32_as_h2(0xE400E400u));                   // * -1024
+    const __half2 sc1h = int_h2(sc1);
+    const __half2 s1 = __hmul2(sc1h, u32_as_h2(0x2C002C00u));                 // / 16
+    const __half2 n1 = __hmul2(sc1h, u32_as_h2(0xD400D400u));                 // * -64
+    // -fp16(dmin m): the exact product rounded once
+    const __half2 e0 = __hneg2(__hmul2(dmin2, int_h2(m0)));
+    const __half2 e1 = __hneg2(__hmul2(dmin2, int_h2(m1)));
+    const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        // bytes (0, 2, 1, 3): weights 4i, 4i+1 in the two 16-bit halves of t,
+        // 4i+2, 4i+3 in those of t >> 8
+        const uint32_t t = prmt(wd[i], 0u, 0x3120u);
+        const uint32_t u = t >> 8;
+        const __half2 l01 = u32_as_h2((t & 0x000F000Fu) | 0x64006400u);
+        const __half2 l23 = u32_as_h2((u & 0x000F000Fu) | 0x64006400u);
+        const __half2 h01 = u32_as_h2((t & 0x00F000F0u) | 0x64006400u);
+        const __half2 h23 = u32_as_h2((u & 0x00F000F0u) | 0x64006400u);
+        hw[2 * i] = h2_as_u32(__hfma2(__hfma2(l01, s0, n0), d2, e0));
+        hw[2 * i + 1] = h2_as_u32(__hfma2(__hfma2(l23, s0, n0), d2, e0));
+        hw[8 + 2 * i] = h2_as_u32(__hfma2(__hfma2(h01, s1, n1), d2, e1));
+        hw[8 + 2 * i + 1] = h2_as_u32(__hfma2(__hfma2(h23, s1, n1), d2, e1));
+    }
+}
+
+template <int FMT>
+struct Prefetch {
+    static constexpr int value = (FMT == F_Q4_K || FMT == F_Q4_0) ? 4 : (FMT == F_Q6_K ? 2 : 3);
+};
+
+__device__ __forceinline__ void split_half_words(const float (&v)[32], bool lo, uint32_t (&hw)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+        if (!lo) {
+            hw[i] = *reinterpret_cast<const uint32_t *>(&h);
+        } else {
+            const float2 f = __half22float2(h);
+            hw[i] = pack_half2(v[2 * i] - f.x, v[2 * i + 1] - f.y);
+        }
+    }
+}
+
+template <int FMT, int BN, int MODE>
+__global__ void __launch_bounds__(kMmaThreads, 1)
+    mma_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmx_lo,
+               const __grid_constant__ CUtensorMap tmw, const MmaParamsOf<FMT> p) {
+    constexpr int kRowsOut = MODE == 3 ? 64 : kBM;   // output rows per CTA
+    constexpr int kTokOut = MODE == 1 ? BN : BN / 2;  // tokens per CTA
+    constexpr bool kRaw = FMT == F_Q4_K && MODE != 3;  // raw W tiles by TMA
+    using C = MmaCfg<BN, kRaw>;
+    constexpr int NA = C::NA, NB = C::NB, kNR = C::kNR, KA = C::KA, KB = C::KB;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
+    const uint32_t B0 = sbase;                                     // x ring
+    const uint32_t W0 = B0 + NB * C::kBStage;                      // raw W stages (kRaw)
+    const uint32_t bar0 = W0 + (kRaw ? kNR * kRawBytes : 0);
+    auto fullA = [&](int s) { return bar0 + 8u * s; };
+    auto emptyA = [&](int s) { return bar0 + 8u * (NA + s); };
+    auto fullB = [&](int s) { return bar0 + 8u * (2 * NA + s); };
+    auto emptyB = [&](int s) { return bar0 + 8u * (2 * NA + NB + s); };
+    auto rawFull = [&](int s) { return bar0 + 8u * (2 * NA + 2 * NB + s); };
+    auto rawEmpty = [&](int s) { return bar0 + 8u * (2 * NA + 2 * NB + kNR + s); };
+    const uint32_t accFull = bar0 + 8u * (2 * NA + 2 * NB + 2 * kNR);
+    const uint32_t accEmpty = accFull + 8u;
+    auto xsFull = [&](int b) { return accFull + 8u * (2 + b); };
+    auto xsFree = [&](int b) { return accFull + 8u * (4 + b); };
+    const uint32_t scrReady = accFull + 8u * 6;  // MODE 3: lo rows parked in scratch
+    const uint32_t slot_off = 8u * (2 * NA + 2 * NB + 2 * kNR + 7);
+    const uint32_t slot_addr = bar0 + slot_off;
+    uint8_t *gen = smem_raw + (bar0 - raw_addr);
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gen + slot_off);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gen + slot_off + 8);
+    // token scales of the tile in flight, double-buffered: [2][kTokOut]
+    float *xs_s = reinterpret_cast<float *>(gen + 512);
+    // Two groups of 8 dequant warps take alternate k-steps; an A stage (KA = 4
+    // k-steps) is done when both groups have arrived.
+    constexpr int kGroups = 2;
+    // Q4_K raw tiles: one group fills a whole stage; otherwise both groups
+    constexpr int kFullACount = kRaw ? kDeqWarps / kGroups : kDeqWarps;
+    static_assert(KA % kGroups == 0, "every group needs a k-step in every A stage");
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t crank = cluster_ctarank();  // 0 or 1 within the CTA pair
+    const int KS = p.KS;                     // 64-wide k-steps
+    // Tiles: the pair of CTAs takes 128-row tiles 2q and 2q + 1 of token tile
+    // nt together; pair-tile v = q * tiles_n + nt (the token tiles of one W
+    // row pair run side by side on neighbouring clusters, so W is read from
+    // HBM about once). Units: the first full_units pair-tiles whole, then the
+    // rest in split = 2 super-block-aligned k-halves each, so that the last
+    // round keeps every cluster busy; the halves add into a y region the
+    // conversion kernel zeroed (0 + a + b is the same in either order, so the
+    // result does not depend on which half lands first). Cluster c of C takes
+    // units c, c + C, ...
+    const int c0 = (int)(blockIdx.x >> 1), cstep = (int)(gridDim.x >> 1);
+    struct Tile {
+        int64_t m0;
+        int n0, rot;
+        int k_lo, k_hi;  // k-steps of this unit
+        int part;        // k-range index, or -1 for a whole tile
+    };
+    auto tile_of = [&](int u) {
+        int v = u, part = -1;
+        if (u >= p.full_units) {
+            const int w = u - p.full_units;
+            v = p.full_units + w / p.split;
+            part = w % p.split;
+        }
+        const int q = v / p.tiles_n, nt = v - q * p.tiles_n;
+        Tile t;
+        t.m0 = p.j0 + (int64_t)(2 * q + (int)crank) * kRowsOut;
+        t.n0 = nt * kTokOut;
+        t.part = part;
+        if (part < 0) {
+            t.k_lo = 0;
+            t.k_hi = KS;
+            // each whole tile walks k in its own rotated order (whole super-blocks)
+            // so that the CTAs do not all fetch the same x tile at the same
+            // moment; the sum is the same up to rounding order
+            t.rot = (KS % 4 == 0) ? 4 * (q % (KS / 4)) : 0;
+        } else {
+            const int nsb = (KS + 3) / 4;
+            t.k_lo = 4 * (part * nsb / p.split);
+            t.k_hi = std::min(KS, 4 * ((part + 1) * nsb / p.split));
+            t.rot = 0;
+        }
+        return t;
+    };
+    auto kx = [&](const Tile &t, int ks) { return t.rot ? (ks + t.rot) % KS : ks; };
+    auto nks = [&](const Tile &t) { return t.k_hi - t.k_lo; };
+    // A stages (the last may be padded) and x stages of a unit
+    auto nsa = [&](const Tile &t) { return (nks(t) + KA - 1) / KA; };
+    auto nsb = [&](const Tile &t) { return (nks(t) + KB - 1) / KB; };
+
+    if (tid == 0) {
+        for (int s = 0; s < NA; ++s) {
+            mbar_init(fullA(s), kFullACount);
+            mbar_init(emptyA(s), 1);
+        }
+        for (int s = 0; s < NB; ++s) {
+            mbar_init(fullB(s), 1);
+            mbar_init(emptyB(s), 2);  // both CTAs of the pair have consumed the stage
+        }
+        for (int s = 0; s < kNR; ++s) {
+            mbar_init(rawFull(s), 1);
+            mbar_init(rawEmpty(s), kDeqWarps / kGroups);  // the group that decodes it
+        }
+        mbar_init(accFull, 1);
+        mbar_init(accEmpty, kDeqWarps);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(xsFull(b), 1);
+            mbar_init(xsFree(b), kDeqWarps);
+        }
+        mbar_init(scrReady, kDeqWarps / 2);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(slot_addr, C::kCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the peer's barriers exist before any multicast reaches them
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------ token scales + x tiles via TMA ------------------
+        // x16 and the scales come from the conversion kernel just before this
+        // one, which lets this grid start early: only this warp waits for it
+        pdl_wait_prev();
+        if (lane == 0) {
+            prefetch_tmap(&tmx);
+            if (MODE != 1) prefetch_tmap(&tmx_lo);
+        }
+        int bcount = 0;  // x stages issued so far (all tiles)
+        int it = 0;
+        for (int u = c0; u < p.n_units; u += cstep, ++it) {
+            if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
+            const Tile t = tile_of(u);
+            // the tile's token scales (2^e of each token's fp16 conversion) for
+            // its epilogue, into buffer it & 1 once the tile two back is done
+            const int xb = it & 1;
+            if (it >= 2) {
+                const bool ok = wait_abortable(xsFree(xb), ((it >> 1) + 1) & 1, abort_flag);
+                if (__all_sync(0xFFFFFFFFu, ok) == 0) {
+                    if (lane == 0) { record_error(p.err, DERR_MMA_EMPTY); *abort_flag = 1; }
+                    break;
+                }
+            }
+            for (int i = lane; i < kTokOut; i += 32)
+                xs_s[xb * kTokOut + i] = t.n0 + i < p.n_tokens ? __ldg(p.xscale + t.n0 + i) : 0.0f;
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(xsFull(xb));
+                const int NSB = nsb(t);
+                for (int st = 0; st < NSB; ++st, ++bcount) {
+                    const int slot = bcount % NB;
+                    if (bcount >= NB &&
+                        !wait_abortable(emptyB(slot), ((bcount / NB) + 1) & 1, abort_flag)) {
+                        record_error(p.err, DERR_MMA_EMPTY);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    // the whole stage lands here: this CTA's halves and the peer's halves
+                    mbar_arrive_expect_tx(fullB(slot), C::kBStage);
+                    for (int sub = 0; sub < KB; ++sub) {
+                        // past k_hi: not used; past KS: zero-filled by the map
+                        const int ks = t.k_lo + st * KB + sub;
+                        const int kc = ks < KS ? kx(t, ks) : ks;
+                        // MODE 1: this CTA fetches token rows [n0 + crank BN/2, +BN/2);
+                        // MODE 2/3: CTA 0 the hi rows, CTA 1 the lo rows of the tile's tokens
+                        const uint32_t dst =
+                            B0 + slot * C::kBStage + sub * C::kBBytes + crank * (BN / 2) * 128;
+                        if (MODE == 1)
+                            tma_load_2d_multicast(dst, &tmx, kc * kBK,
+                                                  t.n0 + (int)crank * (BN / 2), fullB(slot),
+                                                  (uint16_t)3);
+                        else
+                            tma_load_2d_multicast(
+                                dst, crank ? (const void *)&tmx_lo : (const void *)&tmx, kc * kBK,
+                                t.n0, fullB(slot), (uint16_t)3);
+                    }
+                }
+            }
+            __syncwarp();
+        }
+        // no copy may land after this CTA exits
+        if (lane == 0)
+            for (int s = std::max(0, bcount - NB); s < bcount; ++s)
+                if (!mbar_wait(fullB(s % NB), (s / NB) & 1)) record_error(p.err, DERR_TEARDOWN);
+    } else if (warp == 1) {
+        // ------------------------------ MMA issue ------------------------------
+        // The whole warp runs the loop (so that descriptors and addresses stay
+        // warp-uniform); one elected lane issues the MMAs and their commits.
+        constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
+        const bool leader = elect_one();
+        int abase = 0, bbase = 0;  // A / x stages consumed by earlier tiles
+        int it = 0;
+        bool failed = false;
+        for (int u = c0; u < p.n_units && !failed; u += cstep, ++it) {
+            const Tile t = tile_of(u);
+            const int KSu = nks(t);
+            if (it > 0) {  // the epilogue has drained the accumulator
+                const bool ok = wait_abortable(accEmpty, (it - 1) & 1, abort_flag);
+                if (__all_sync(0xFFFFFFFFu, ok) == 0) {
+                    if (leader) { record_error(p.err, DERR_MMA_ACC); *abort_flag = 1; }
+                    break;
+                }
+                tc_fence_after();
+            }
+            for (int ks = 0; ks < KSu; ++ks) {
+                const int st = abase + ks / KA, sa = st % NA;
+                const int bt = bbase + ks / KB, sb = bt % NB;
+                if (ks % KA == 0) {
+                    const bool ok = wait_abortable(fullA(sa), (st / NA) & 1, abort_flag);
+                    if (__all_sync(0xFFFFFFFFu, ok) == 0) {
+                        if (leader) { record_error(p.err, DERR_MMA_A); *abort_flag = 1; }
+                        failed = true;
+                        break;
+                    }
+                }
+                if (ks % KB == 0) {
+                    const bool ok = wait_abortable(fullB(sb), (bt / NB) & 1, abort_flag);
+                    if (__all_sync(0xFFFFFFFFu, ok) == 0) {
+                        if (leader) { record_error(p.err, DERR_MMA_B); *abort_flag = 1; }
+                        failed = true;
+                        break;
+                    }
+                }
+                tc_fence_after();
+                if (leader) {
+                    const uint32_t at =
+                        tmem + (uint32_t)(C::kACol0 + sa * C::kAStageCols + (ks % KA) * 32);
+                    const uint64_t bd =
+                        sdesc_sw128(B0 + sb * C::kBStage + (ks % KB) * C::kBBytes);
+                    const uint32_t dacc =
+                        tmem + (uint32_t)((C::kNAcc == 2 ? (ks & 1) : 0) * C::kAccCols);
+                    const bool acc0 = C::kNAcc == 2 ? ks > 1 : ks > 0;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16: 8 A columns, 32 B bytes
+                        tc_mma_f16_ts(dacc, at + 8 * kk, bd + 2 * kk, idesc, acc0 || kk != 0);
+                    const bool last = ks == KSu - 1;
+                    if (ks % KB == KB - 1 || last)
+                        tc_commit_multicast(emptyB(sb), (uint16_t)3);  // both CTAs may refill
+                    if (ks % KA == KA - 1 || last) tc_commit(emptyA(sa));
+                    if (last) tc_commit(accFull);  // the tile's product is complete
+                }
+                __syncwarp();
+            }
+            abase += nsa(t);
+            bbase += nsb(t);
+        }
+    } else if (warp == kRawWarp) {
+        // ------------------------------ raw Q4_K tiles via TMA ------------------------------
+        // its own warp, so that the raw ring runs as far ahead of the dequant
+        // warps as it is deep (into the next tile), whatever the x ring does
+        if (kRaw && lane == 0) {
+            prefetch_tmap(&tmw);
+            int rcount = 0;
+            for (int u = c0; u < p.n_units; u += cstep) {
+                if (*abort_flag) break;
+                const Tile t = tile_of(u);
+                bool ok = true;
+                for (int b = t.k_lo / 4; b < t.k_hi / 4; ++b, ++rcount) {  // k % 256 == 0
+                    const int rs = rcount % kNR;
+                    if (rcount >= kNR &&
+                        !wait_abortable(rawEmpty(rs), ((rcount / kNR) + 1) & 1, abort_flag)) {
+                        record_error(p.err, DERR_MMA_EMPTY);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(rawFull(rs), kRawBytes);
+                    tma_load_2d(W0 + rs * kRawBytes, &tmw, 144 * (kx(t, 4 * b) >> 2),
+                                (int)t.m0, rawFull(rs));
+                }
+                if (!ok) break;
+            }
+            // no copy may land after this CTA exits
+            for (int s = std::max(0, rcount - kNR); s < rcount; ++s)
+                if (!mbar_wait(rawFull(s % kNR), (s / kNR) & 1)) record_error(p.err, DERR_TEARDOWN);
+        }
+    } else {
+        // ------------------------------ W dequant producers ------------------------------
+        // Warp w (2..17) owns TMEM lanes 32 (w % 4) .. +31, i.e. rows r of the
+        // tile; (w - 2) / 4 picks the half h of each 64-wide k-step and the
+        // group g (k-step parity) it takes. Each group's first k-step in a
+        // stage waits for the stage to be free, its last one signals it.
+        const int quarter = warp & 3;
+        const int r = 32 * quarter + lane;
+        const int dq = (warp - 2) >> 2;
+        const int h = dq & 1;
+        const int g = dq >> 1;
+        const uint32_t tlane = tmem + ((uint32_t)(32 * quarter) << 16);
+        bool failed = false;
+        int abase = 0;   // A stages of earlier tiles
+        int rcount = 0;  // raw super-blocks consumed (all tiles)
+        // k-step ks of the tile: wait for its A slot (when first in the stage)
+        // and return the TMEM address of its 32 columns
+        auto a_slot = [&](int ks) {
+            const int st = abase + ks / KA, sub = ks % KA;
+            const int slot = st % NA;
+            if (sub < kGroups && st >= NA) {
+                const bool ok = wait_abortable(emptyA(slot), ((st / NA) + 1) & 1, abort_flag);
+                if (__all_sync(0xFFFFFFFFu, ok) == 0) {
+                    if (!failed) record_error(p.err, DERR_MMA_EMPTY);
+                    failed = true;
+                    *abort_flag = 1;
+                }
+                tc_fence_after();  // the MMAs that read the slot are done
+            }
+            return tlane + (uint32_t)(C::kACol0 + slot * C::kAStageCols + sub * 32);
+        };
+        auto a_done = [&](int ks) {
+            const int st = abase + ks / KA, sub = ks % KA;
+            if (sub + kGroups >= KA) {
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0 && !failed) mbar_arrive(fullA(st % NA));
+            }
+        };
+        int it = 0;
+        for (int u = c0; u < p.n_units && !failed; u += cstep, ++it) {
+            const Tile t = tile_of(u);
+            const int KSu = nks(t);
+            if constexpr (kRaw) {
+                // Super-block b is one A stage. Group g takes the super-blocks
+                // whose global index has parity g, so the two groups run out of
+                // phase: thread (r, h) decodes half h of all four 64-weight
+                // chunks of row r.
+                const bool row_ok = t.m0 + r < p.j1;
+                const int NSBLK = KSu / 4;  // k % 256 == 0: whole super-blocks
+                const int rbase = rcount;   // global index of the unit's first super-block
+                for (int b = (g - rbase) & 1; b < NSBLK && !failed; b += 2) {
+                    const int rc = rbase + b;
+                    const int rs = rc % kNR;
+                    const bool ok = wait_abortable(rawFull(rs), (rc / kNR) & 1, abort_flag);
+                    if (__all_sync(0xFFFFFFFFu, ok) == 0) {
+                        record_error(p.err, DERR_MMA_A);
+                        failed = true;
+                        *abort_flag = 1;
+                        break;
+                    }
+                    uint4 hdr = make_uint4(0u, 0u, 0u, 0u), qv[4];
+                    const uint32_t rb = W0 + rs * kRawBytes + (uint32_t)r * 144u;
+                    if (row_ok) {
+                        hdr = lds128(rb);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) qv[c] = lds128(rb + 16u + 32u * c + 16u * h);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(rawEmpty(rs));  // raw tile read
+                    // the stage's slot, once the MMAs that read it last are done
+                    const int st = abase + b, slot = st % NA;
+                    if (st >= NA) {
+                        const bool ok2 =
+                            wait_abortable(emptyA(slot), ((st / NA) + 1) & 1, abort_flag);
+                        if (__all_sync(0xFFFFFFFFu, ok2) == 0) {
+                            record_error(p.err, DERR_MMA_EMPTY);
+                            failed = true;
+                            *abort_flag = 1;
+                        }
+                        tc_fence_after();
+                    }
+                    const uint32_t ta = tlane + (uint32_t)(C::kACol0 + slot * C::kAStageCols);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t hw[16];
+                        if (row_ok) {
+                            q4k_half_chunk_to_half(hdr, qv[c], c, hw);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) hw[e] = 0u;
+                        }
+                        // chunk c = k-step c of the stage: weights 16h + 0..15 ->
+                        // columns 8h..8h+7, 32 + 16h + 0..15 -> 16 + 8h..
+                        tmem_st8(ta + 32u * c + 8u * h, hw);
+                        tmem_st8(ta + 32u * c + 16u + 8u * h, hw + 8);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0 && !failed) mbar_arrive(fullA(slot));
+                }
+                rcount = rbase + NSBLK;
+            } else {
+                const bool lo_part = MODE == 3 && r >= 64;  // MODE 3: rows 64..127 hold W_lo
+                const int64_t j = t.m0 + (MODE == 3 ? (r & 63) : r);
+                const bool row_ok = j < p.j1;
+                const uint8_t *rowp = p.w + (row_ok ? j : 0) * p.row_bytes;
+                // 32 weights of this row at k0 (affine: with the group's scale and bias)
+                auto load_raw = [&](Raw32<FMT> &r, int64_t k0, int nv) {
+                    if constexpr (is_affine(FMT)) {
+                        const int64_t ao = (row_ok ? j : 0) * p.aux_row_bytes;
+                        r.load(rowp, p.sc + ao, p.bi + ao, k0);
+                    } else {
+                        r.load(rowp, k0, nv);
+                    }
+                };
+                constexpr int PD = Prefetch<FMT>::value;
+                Raw32<FMT> ring[PD];
+                // this thread's i-th k-step is g + 2 i
+                auto ks_of = [&](int i) { return g + 2 * i; };
+                // unit-relative k-step -> first weight index; past the unit's
+                // range: beyond k (nothing loaded, zeros stored)
+                auto k0_of = [&](int i) {
+                    const int ks = t.k_lo + ks_of(i);
+                    return ks < t.k_hi ? (int64_t)kx(t, ks) * kBK + 32 * h : p.k;
+                };
+                auto nvalid_of = [&](int64_t k0) {
+                    const int64_t v = p.k - k0;
+                    return (int)(v < 0 ? 0 : (v > 32 ? 32 : v));
+                };
+                // k-steps of this group over the stage-padded range: a k-step
+                // past k stores zeros (the MMA skips it) but still takes part
+                // in its stage's arrival count
+                const int NI = (nsa(t) * KA - g + 1) / 2;
+#pragma unroll
+                for (int q = 0; q < PD; ++q) {
+                    const int64_t k0 = k0_of(q);
+                    const int nv = nvalid_of(k0);
+                    if (q < NI && row_ok && nv > 0) load_raw(ring[q], k0, nv);
+                }
+                for (int i0 = 0; i0 < NI && !failed; i0 += PD) {
+#pragma unroll
+                    for (int q = 0; q < PD; ++q) {
+                        const int i = i0 + q;
+                        if (i < NI) {
+                            const int ks = ks_of(i);
+                            const int64_t k0 = k0_of(i);
+                            const int nv = nvalid_of(k0);
+                            uint32_t hw[16];
+                            if (row_ok && nv > 0) {
+                                if (MODE == 3) {
+                                    float v[32];
+                                    ring[q].decode(v);
+                                    split_half_words(v, lo_part, hw);
+                                } else {
+                                    to_half_words<FMT>(ring[q], hw);
+                                }
+                                if (nv < 32) {
+#pragma unroll
+                                    for (int e = 0; e < 16; ++e)
+                                        if (2 * e >= nv) hw[e] = 0u;  // nv is even
+                                }
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) hw[e] = 0u;
+                            }
+                            const int64_t kn = k0_of(i + PD);
+                            const int nvn = nvalid_of(kn);
+                            if (i + PD < NI && row_ok && nvn > 0) load_raw(ring[q], kn, nvn);
+                            const uint32_t ta = a_slot(ks);
+                            tmem_st16(ta + 16u * h, hw);  // weights 32h + 0..31 -> columns 16h..
+                            a_done(ks);
+                        }
+                    }
+                }
+            }
+            abase += nsa(t);
+            if (failed) break;
+            // ------------------------------ epilogue ------------------------------
+            // TMEM -> registers -> y: per warp store, 32 consecutive rows of one
+            // token (128 contiguous bytes)
+            const int xb = it & 1;
+            const bool acc_ok = mbar_wait(accFull, it & 1) && mbar_wait(xsFull(xb), (it >> 1) & 1);
+            if (!acc_ok) {
+                record_error(p.err, DERR_MMA_ACC);
+                *abort_flag = 1;
+                failed = true;
+                break;
+            }
+            tc_fence_after();
+            const float *xsc = xs_s + xb * kTokOut;
+            const int slice = dq;  // 0..3: which part of the token columns
+            constexpr int kSlices = kTokOut >= 64 ? 4 : (kTokOut >= 32 ? 2 : 1);
+            constexpr int kSliceCols = kTokOut / kSlices;
+            const int c_lo = slice < kSlices ? slice * kSliceCols : 0;
+            const int c_hi = slice < kSlices ? c_lo + kSliceCols : 0;
+            const int64_t je = t.m0 + (MODE == 3 ? (r & 63) : r);
+            const bool store_ok = !*abort_flag && je < p.j1;
+            // the k-halves of a split tile add into zeros
+            const bool split = t.part >= 0;
+            if (split) pdl_wait_prev();  // the conversion kernel zeroed the region
+            // MODE 3 row-pair scratch [col][64] over the x ring (MODE 3 CTAs
+            // take one tile each: nothing is prefetched into the ring)
+            float *scratch = reinterpret_cast<float *>(smem_raw + (B0 - raw_addr));
+            // the two accumulators (even / odd k-steps) are summed here; KS == 1
+            // leaves the odd one unwritten
+            const bool two_acc = C::kNAcc == 2 && KSu > 1;
+            auto load_acc = [&](int col, float (&acc)[16]) {
+                uint32_t v[16], v2[16];
+                tmem_ld16(tlane + (uint32_t)col, v);
+                if (two_acc) tmem_ld16(tlane + (uint32_t)(C::kAccCols + col), v2);
+                if (MODE == 1) {
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        acc[i] = __uint_as_float(v[i]) + (two_acc ? __uint_as_float(v2[i]) : 0.0f);
+                } else {
+                    uint32_t w2[16], w3[16];
+                    tmem_ld16(tlane + (uint32_t)(col + BN / 2), w2);
+                    if (two_acc) tmem_ld16(tlane + (uint32_t)(C::kAccCols + col + BN / 2), w3);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        acc[i] = __uint_as_float(v[i]) + __uint_as_float(w2[i]);
+                        if (two_acc) acc[i] += __uint_as_float(v2[i]) + __uint_as_float(w3[i]);
+                    }
+                }
+            };
+            if (MODE == 3 && quarter >= 2) {
+                // lo rows: park (D[r][c] + D[r][c + BN/2]) for the hi warps
+                for (int col = c_lo; col < c_hi; col += 16) {
+                    float acc[16];
+                    load_acc(col, acc);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) scratch[(col + i) * 64 + (r & 63)] = acc[i];
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(scrReady);
+            }
+            bool scr_ok = true;
+            if (MODE == 3 && quarter < 2) {
+                scr_ok = mbar_wait(scrReady, 0);  // one tile per CTA in MODE 3
+                if (!scr_ok) {
+                    record_error(p.err, DERR_MMA_ACC);
+                    *abort_flag = 1;
+                }
+            }
+            if ((MODE != 3 || quarter < 2) && scr_ok) {
+                for (int col = c_lo; col < c_hi; col += 16) {
+                    float acc[16];
+                    load_acc(col, acc);
+                    if (MODE == 3) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[i] += scratch[(col + i) * 64 + (r & 63)];
+                    }
+                    if (store_ok) {
+                        const int64_t t0 = t.n0 + col;
+                        float *yp = p.y + t0 * p.n + je;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            if (t0 + i < p.n_tokens) {
+                                const float val = acc[i] * xsc[col + i];
+                                float *yq = yp + (int64_t)i * p.n;
+                                if (split)
+                                    atomicAdd(yq, val);
+                                else
+                                    *yq = p.accumulate ? *yq + val : val;
+                            }
+                        }
+                    }
+                }
+            }
+            // accumulator and token scales free for the next tile
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(accEmpty);
+                mbar_arrive(xsFree(xb));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // no multicast or remote arrival is still headed for this CTA
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kCols);
+    }
+}
+
+struct Maps {
+    CUtensorMap x, xlo, w;
+};
+
+// Clusters of two CTAs that can be resident at once (defined beside the Q4_K
+// instances, whose footprint it queries).
+int mma_clusters(const DeviceInfo &dev);
+
+// Persistent grid: clusters of two CTAs, as many as can be resident at once
+// (one CTA per SM), capped by the number of row-tile pairs x token tiles.
+// MODE 3 keeps one tile per CTA (its epilogue scratch lives in the x ring).
+template <int FMT, int BN, int MODE>
+static cudaError_t launch_t(const Maps &mp, const MmaAffParams &h, const DeviceInfo &dev,
+                            cudaStream_t s) {
+    const MmaParamsOf<FMT> p = h;
+    using C = MmaCfg<BN, FMT == F_Q4_K && MODE != 3>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    static int max_clusters = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kMmaThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(mma_kernel<FMT, BN, MODE>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+        if (attr_err != cudaSuccess) return;
+        cudaLaunchConfig_t q = cfg;
+        q.gridDim = dim3(2 * (unsigned)(dev.sm_count / 2));
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<FMT, BN, MODE>, &q) != cudaSuccess ||
+            n <= 0) {
+            (void)cudaGetLastError();
+            n = dev.sm_count / 2;
+        }
+        max_clusters = std::min(n, mma_clusters(dev));
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int P = p.pairs * p.tiles_n;
+    const int clusters = MODE == 3 ? P : std::min(p.n_units, max_clusters);
+    cfg.gridDim = dim3(2 * (unsigned)clusters);
+    // programmatic launch after the x conversion kernel (see pdl_wait_prev)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, mma_kernel<FMT, BN, MODE>, mp.x, mp.xlo, mp.w, p);
+}
+
+template <int FMT, int MODE>
+static cudaError_t launch_bn(int bn, const Maps &mp, const MmaAffParams &p, const DeviceInfo &dev,
+                             cudaStream_t s) {
+    switch (bn) {
+    case 16: if (MODE == 1) return launch_t<FMT, 16, MODE>(mp, p, dev, s); break;
+    case 32: return launch_t<FMT, 32, MODE>(mp, p, dev, s);
+    case 64: return launch_t<FMT, 64, MODE>(mp, p, dev, s);
+    case 128: return launch_t<FMT, 128, MODE>(mp, p, dev, s);
+    case 256: return launch_t<FMT, 256, MODE>(mp, p, dev, s);
+    default: break;
+    }
+    return cudaErrorInvalidValue;
+}
+
+// Instantiated (explicitly) by the qmm_mma_inst_*.cu units, one group of
+// formats each.
+template <int FMT>
+cudaError_t launch_fmt(int mode, int bn, const Maps &mp, const MmaAffParams &p,
+                       const DeviceInfo &dev, cudaStream_t s) {
+    constexpr bool quant = FMT != F_BF16 && FMT != F_F16;
+    if (mode == 2) return launch_bn<FMT, 2>(bn, mp, p, dev, s);
+    if (quant && mode == 1) return launch_bn<FMT, quant ? 1 : 2>(bn, mp, p, dev, s);
+    if (quant && mode == 3) return launch_bn<FMT, quant ? 3 : 2>(bn, mp, p, dev, s);
+    return cudaErrorInvalidValue;
+}
+
+#define QMM_MMA_INSTANTIATE(F)                                                               \
+    template cudaError_t launch_fmt<F>(int, int, const Maps &, const MmaAffParams &,          \
+                                       const DeviceInfo &, cudaStream_t)
+
+}  // namespace qmm

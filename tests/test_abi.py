@@ -66,7 +66,7 @@ def _args(**kw):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(fmt=7), 1),
+    (dict(fmt=9), 1),
     (dict(k=300), 2),
     (dict(fmt="q4_0", k=48), 2),
     (dict(fmt="bf16", k=7), 2),
@@ -172,7 +172,7 @@ def test_backward_input_empty_work_needs_no_device(lib):
     (dict(flags=8), dict(), 2),
     (dict(path=q.PATH_MMA), dict(), 10),
     (dict(k=300), dict(), 2),
-    (dict(fmt=7), dict(), 1),
+    (dict(fmt=9), dict(), 1),
     (dict(w_len=144 * 2 * 8), dict(n_experts=3), 3),   # two slices given, three claimed
     (dict(j_start=5, j_end=3), dict(), 4),
     (dict(n_tokens=300), dict(top_k=300), 2),           # more than 65535 GEMVs
@@ -194,3 +194,54 @@ def test_experts_empty_work_needs_no_device(lib):
     assert q.qmm_matmul_experts(_args(j_start=3, j_end=3), None, 4, 2) == 0
     # all slices given: w_len = n_experts * slice bytes is accepted
     assert q.qmm_matmul_experts(_args(w_len=144 * 2 * 8 * 3, j_start=2, j_end=2), 16, 3, 1) == 0
+
+
+# ------------------------------------------------------- affine formats ----
+
+def test_affine_sizes_and_policy(lib):
+    assert q.qmm_weight_bytes("affine4", 128, 3) == 192
+    assert q.qmm_weight_bytes("affine8", 128, 3) == 384
+    assert q.qmm_weight_bytes("affine4", 100, 1) == 0
+    a = _args(fmt="affine4", k=4096, n=14336, n_tokens=1)
+    assert q.qmm_select_path(a) == q.PATH_GEMV and q.qmm_workspace_bytes(a) == 0
+    a = _args(fmt="affine8", k=4096, n=14336, n_tokens=64)
+    assert q.qmm_select_path(a) == q.PATH_MMA
+    assert q.qmm_workspace_bytes(a) == 64 * 4096 * 2 + 256
+
+
+@pytest.mark.parametrize("fn,kw,sb,status", [
+    ("ex", dict(fmt="affine4", k=128), None, 1),          # needs its scales and biases
+    ("aff", dict(fmt="q4_k"), (16 * 700, 16 * 800), 1),   # not an affine format
+    ("aff", dict(fmt="affine4", k=100), (16 * 700, 16 * 800), 2),
+    ("aff", dict(fmt="affine8", k=128), (None, 16 * 800), 5),
+    ("aff", dict(fmt="affine8", k=128), (16 * 700 + 2, 16 * 800), 6),
+    ("aff", dict(fmt="affine4", k=128, w_len=10), (16 * 700, 16 * 800), 3),
+    ("experts", dict(fmt="affine4", k=128), None, 1),
+    ("back", dict(fmt="affine4", k=128), None, 1),
+])
+def test_affine_rejected_on_host(lib, fn, kw, sb, status):
+    a = _args(**kw)
+    with pytest.raises(q.QmmError) as ei:
+        if fn == "ex":
+            q.qmm_matmul_ex(a)
+        elif fn == "aff":
+            q.qmm_matmul_affine(a, *sb)
+        elif fn == "experts":
+            q.qmm_matmul_experts(a, 16 * 500, 4, 2)
+        else:
+            q.qmm_matmul_backward_input(a)
+    assert ei.value.status == status, q.qmm_last_error()
+
+
+def test_affine_dequant_rejected_on_host(lib):
+    assert lib.qmm_dequant(7, 16, 128, 1, 16, None) == 1
+    assert lib.qmm_dequant_affine(2, 16, 16, 16, 128, 1, 16, None) == 1
+    assert lib.qmm_dequant_affine(7, 16, 16, 16, 100, 1, 16, None) == 2
+    assert lib.qmm_dequant_affine(7, 16, None, 16, 128, 1, 16, None) == 5
+    assert lib.qmm_dequant_affine(7, 24, 16, 16, 128, 1, 16, None) == 6
+    assert lib.qmm_dequant_affine(7, 16, 17, 16, 128, 1, 16, None) == 6
+    assert lib.qmm_dequant_affine(7, 16, 16, 16, 0, 1, 16, None) == 0   # nothing to do
+
+
+def test_affine_empty_work_needs_no_device(lib):
+    assert q.qmm_matmul_affine(_args(fmt="affine4", k=128, j_start=3, j_end=3), None, None) == 0
