@@ -80,6 +80,13 @@ def _load():
             lib.oracle_matmul_affine_sampled.restype = ctypes.c_int
             lib.oracle_matmul_affine_sampled.argtypes = [ctypes.c_int, p, p, p, p, i64, i64, i64,
                                                          i64, p, p, p, p, p]
+            lib.oracle_act.restype = ctypes.c_double
+            lib.oracle_act.argtypes = [ctypes.c_int, ctypes.c_double]
+            lib.oracle_act_deriv.restype = ctypes.c_double
+            lib.oracle_act_deriv.argtypes = [ctypes.c_int, ctypes.c_double]
+            lib.oracle_matmul_glu.restype = ctypes.c_int
+            lib.oracle_matmul_glu.argtypes = [ctypes.c_int, ctypes.c_int, p, p, p, i64, i64, i64, p,
+                                              p, p]
             _lib = lib
     return _lib
 
@@ -320,3 +327,33 @@ def matmul_affine_blas(bits: int, w, scales, biases, x, k: int, n: int):
     deq = dequant_affine(bits, w, scales, biases, k, n).astype(np.float64)
     x64 = np.atleast_2d(np.asarray(x, np.float64))
     return x64 @ deq.T, np.abs(x64) @ np.abs(deq).T
+
+
+# ------------------------------------------------------- gated products ----
+ACTS = {"swiglu": 0, "geglu": 1}
+
+
+def act(name: str, g: float) -> float:
+    """silu (swiglu) or tanh-form GELU (geglu) of one value, in double."""
+    return _load().oracle_act(ACTS[name], float(g))
+
+
+def act_deriv(name: str, g: float) -> float:
+    return _load().oracle_act_deriv(ACTS[name], float(g))
+
+
+def matmul_glu(name: str, fmt: str, wg, wu, x, k: int, n: int):
+    """(y, S): y = act(x Wg) * (x Wu), S its propagated error scale, f64 [N, n]."""
+    wg = np.ascontiguousarray(wg, dtype=np.uint8)
+    wu = np.ascontiguousarray(wu, dtype=np.uint8)
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
+    if x.shape[1] != k or wg.size != wu.size:
+        raise ValueError("bad shapes for the gated product")
+    nt = x.shape[0]
+    y = np.empty((nt, n), np.float64)
+    s = np.empty((nt, n), np.float64)
+    scratch = np.empty(max(k, 1), np.float32)
+    if _load().oracle_matmul_glu(ACTS[name], CODES[fmt], _ptr(wg), _ptr(wu), _ptr(x), k, n, nt,
+                                 _ptr(y), _ptr(s), _ptr(scratch)) != 0:
+        raise ValueError("oracle gated matmul rejected its arguments")
+    return y, s

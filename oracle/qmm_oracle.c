@@ -48,6 +48,15 @@
  *    the value is rounded once to f32 (the page's GPU kernel contracts
  *    code * scale + bias into one fused multiply-add).
  *
+ *  - gated FFN activations: rullama src/backend/dispatch/mod.rs, `silu_chained`
+ *    (silu(x) = x * sigmoid(x)) and `geglu_chained` / the GeGLU backward
+ *    tests (the GELU there is the tanh form, whose saturation the tests
+ *    exercise); moeflux tests/graph_diff_oracle.rs, `SwigluFusedBatched`:
+ *    out = act(gate) * up elementwise, gate = x Wg and up = x Wu two
+ *    products of the same x. The tanh-form constants (sqrt(2/pi), 0.044715)
+ *    are the published tanh approximation of GELU, which the pages name but
+ *    do not print.
+ *
  * Parity pins live in tests/test_oracle_pins.py (hand-packed blocks with
  * known values, closed-form sizes, exhaustive f16 decode against numpy,
  * identity / one-hot products, brute-force tiny products).
@@ -455,6 +464,62 @@ int oracle_matmul_affine_sampled(int bits, const uint8_t *w, const uint8_t *sc,
         }
         y[c] = acc;
         s[c] = mag;
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Gated products: y = act(x Wg) * (x Wu). act 0: silu(g) = g / (1 + e^-g);
+ * act 1: GELU, tanh form, 0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))). */
+
+double oracle_act(int act, double g)
+{
+    if (act == 0) return g / (1.0 + exp(-g));
+    const double c = sqrt(2.0 / 3.14159265358979323846);
+    return 0.5 * g * (1.0 + tanh(c * (g + 0.044715 * g * g * g)));
+}
+
+/* d act / d g, for the error bar of the gated product. */
+double oracle_act_deriv(int act, double g)
+{
+    if (act == 0) {
+        const double sg = 1.0 / (1.0 + exp(-g));
+        return sg * (1.0 + g * (1.0 - sg));
+    }
+    const double c = sqrt(2.0 / 3.14159265358979323846);
+    const double z = c * (g + 0.044715 * g * g * g);
+    const double t = tanh(z);
+    return 0.5 * (1.0 + t) + 0.5 * g * (1.0 - t * t) * c * (1.0 + 3.0 * 0.044715 * g * g);
+}
+
+/* y[t][j] = act(gate) * up with gate = sum_i x w_g, up = sum_i x w_u (double
+ * sums), and the error scale s[t][j] = |act'(gate)| |up| Sg + |act(gate)| Su
+ * (Sg, Su the sums of |x w|): a product bar e * S on gate and up propagates to
+ * at most e * s on y, to first order. */
+int oracle_matmul_glu(int act, int fmt, const uint8_t *wg, const uint8_t *wu, const float *x,
+                      int64_t k, int64_t n, int64_t n_tokens, double *y, double *s,
+                      float *wrow_scratch)
+{
+    int64_t rb = oracle_row_bytes(fmt, k);
+    if ((rb == 0 && k != 0) || (act != 0 && act != 1)) return -1;
+    for (int64_t j = 0; j < n; ++j) {
+        for (int64_t t = 0; t < n_tokens; ++t) {
+            double gu[2], su[2];
+            for (int m = 0; m < 2; ++m) {
+                if (oracle_dequant_row(fmt, (m ? wu : wg) + j * rb, k, wrow_scratch)) return -1;
+                double acc = 0.0, mag = 0.0;
+                for (int64_t i = 0; i < k; ++i) {
+                    double v = (double)x[t * k + i] * (double)wrow_scratch[i];
+                    acc += v;
+                    mag += fabs(v);
+                }
+                gu[m] = acc;
+                su[m] = mag;
+            }
+            const double a = oracle_act(act, gu[0]);
+            y[t * n + j] = a * gu[1];
+            s[t * n + j] = fabs(oracle_act_deriv(act, gu[0])) * fabs(gu[1]) * su[0] + fabs(a) * su[1];
+        }
     }
     return 0;
 }

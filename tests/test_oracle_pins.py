@@ -664,3 +664,63 @@ def test_affine_product_matches_numpy_and_sampled():
     ti, ji = np.array([0, 2, 1]), np.array([10, 0, 5])
     ys, ss = oracle.matmul_affine_sampled(4, w, scales, biases, x, k, n, ti, ji)
     assert np.array_equal(ys, y[ti, ji]) and np.array_equal(ss, s[ti, ji])
+
+
+
+# ------------------------------------------------------- gated products ----
+
+def test_activation_odd_part_identity():
+    """act(g) - act(-g) = g for both (sigmoid(g) + sigmoid(-g) = 1, and the
+    same for the tanh form): a sign or constant slip breaks it."""
+    for name in ("swiglu", "geglu"):
+        for g in (0.0, 0.3, 1.0, 2.5, 7.0, 30.0):
+            assert abs(oracle.act(name, g) - oracle.act(name, -g) - g) <= 1e-12 * max(1.0, g)
+
+
+def test_silu_against_library_sigmoid():
+    from scipy.special import expit
+    for g in np.linspace(-40, 40, 161):
+        assert abs(oracle.act("swiglu", g) - g * expit(g)) <= 1e-14 * max(1.0, abs(g))
+    assert oracle.act("swiglu", 0.0) == 0.0
+
+
+def test_gelu_tanh_form_against_erf_gelu_and_sigmoid_identity():
+    """The tanh form stays within 5e-4 of the erf GELU everywhere, equals
+    g * sigmoid(2 z) with z its tanh argument (0.5 (1 + tanh z) = sigmoid(2z)),
+    and gelu(1) = 0.8411919906 (the published tanh-form value)."""
+    from scipy.special import erf, expit
+    c = np.sqrt(2.0 / np.pi)
+    for g in np.linspace(-10, 10, 401):
+        v = oracle.act("geglu", g)
+        assert abs(v - 0.5 * g * (1 + erf(g / np.sqrt(2)))) <= 5e-4
+        assert abs(v - g * expit(2 * c * (g + 0.044715 * g ** 3))) <= 1e-13 * max(1.0, abs(g))
+    assert abs(oracle.act("geglu", 1.0) - 0.8411919906) < 1e-10
+
+
+def test_activation_derivatives_by_central_differences():
+    for name in ("swiglu", "geglu"):
+        for g in (-6.0, -1.3, -0.2, 0.0, 0.4, 1.7, 5.0):
+            h = 1e-5
+            fd = (oracle.act(name, g + h) - oracle.act(name, g - h)) / (2 * h)
+            assert abs(oracle.act_deriv(name, g) - fd) < 1e-7
+
+
+@pytest.mark.parametrize("name", ["swiglu", "geglu"])
+def test_glu_product_composes_the_plain_products(name):
+    rng = np.random.default_rng(31)
+    fmt, k, n = "q4_k", 512, 9
+    wg = qmm_synth.gen_weights(fmt, k, n, rng)
+    wu = qmm_synth.gen_weights(fmt, k, n, rng)
+    x = rng.standard_normal((2, k)).astype(np.float32)
+    y, s = oracle.matmul_glu(name, fmt, wg, wu, x, k, n)
+    g, sg = oracle.matmul(fmt, wg, x, k, n)
+    u, su = oracle.matmul(fmt, wu, x, k, n)
+    for t in range(2):
+        for j in range(n):
+            a = oracle.act(name, g[t, j])
+            assert y[t, j] == a * u[t, j]
+            exp_s = abs(oracle.act_deriv(name, g[t, j])) * abs(u[t, j]) * sg[t, j] + abs(a) * su[t, j]
+            assert s[t, j] == exp_s
+    # swapping gate and up changes the result (the gate is the activated one)
+    y2, _ = oracle.matmul_glu(name, fmt, wu, wg, x, k, n)
+    assert not np.allclose(y, y2)
