@@ -501,6 +501,34 @@ def measure_other_workloads(torch, q, lib, r, stream, hbm_peak, tc_peak):
             res.update({"tflops": fl_ / dt / 1e12, "frac_bf16_peak": fl_ / dt / 1e12 / tc_peak})
         return res
 
+    # gated pair (SwiGLU) on the Q4_K FFN shape: gate and up matrices, one
+    # fused launch; bytes = both matrices
+    glu = lib.qmm_matmul_glu
+
+    def glu_case(name, act, reps=50):
+        fmt, k, n, w, x = qmm_synth.workload(name)
+        w2 = qmm_synth.gen_weights(fmt, k, n, np.random.default_rng(77))
+        ncop = r.copies_for(2 * w.size)
+        wg, wu = r.weights(w, ncop), r.weights(w2, ncop)
+        xd = torch.from_numpy(x).to(dev)
+        yd = torch.empty((1, n), device=dev)
+        al = [ctypes.byref(q.make_args(fmt, wg[c], xd, yd, k, n, 1, stream=stream,
+                                       flags=q.FLAG_OVERLAP_PREV | q.FLAG_X_READY))
+              for c in range(ncop)]
+        ups = [ctypes.c_void_p(wu[c].data_ptr()) for c in range(ncop)]
+
+        def launch(c):
+            if glu(al[c], ups[c], act):
+                raise RuntimeError(q.qmm_last_error())
+        dt = time_loop(torch, launch, reps, 5, ncop, stream)
+        q.qmm_device_status(stream)
+        gbs = 2 * w.size / dt / 1e9
+        return {"us": dt * 1e6, "weight_gbs": gbs, "frac_hbm": gbs / hbm_peak,
+                "weight_bytes": int(2 * w.size), "launches_per_call": 1}
+
+    out["q4_k_swiglu_pair"] = glu_case("q4_k_gemv", q.ACT_SWIGLU)
+    out["q8_0_geglu_pair"] = glu_case("q8_0_gemv", q.ACT_GEGLU)
+
     out["affine4_gemv"] = affine_case("affine4_gemv")
     out["affine8_gemv"] = affine_case("affine8_gemv")
     out["affine4_prefill_512"] = affine_case("affine4_prefill", reps=20)

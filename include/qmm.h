@@ -217,6 +217,26 @@ int qmm_matmul_experts(const qmm_args *a, const int32_t *ids, int64_t n_experts,
  * [n][k] fp32. Stream-ordered. */
 int qmm_dequant(int fmt, const void *w, int64_t k, int64_t n, float *out, void *stream);
 
+/* Gate activations of gated FFN pairs. */
+typedef enum qmm_act {
+    QMM_ACT_SWIGLU = 1,  /* silu(g) = g / (1 + e^-g) */
+    QMM_ACT_GEGLU = 2    /* GELU, tanh form: g/2 (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))) */
+} qmm_act;
+
+/* Gated pair (rullama src/backend/dispatch/mod.rs `silu_chained`,
+ * `geglu_chained`; moeflux tests/graph_diff_oracle.rs `SwigluFusedBatched`):
+ *     y[t][j] (+)= act((x Wg)[t][j]) * (x Wu)[t][j],  j in [j_start, j_end)
+ * a->w is the gate matrix, w_up the up matrix (same format, k, n and w_len;
+ * device, 16-byte aligned). One token on the GEMV path: one fused launch
+ * that streams a CTA's rows of Wg, keeps the gate values on chip, streams
+ * the same rows of Wu and writes only y. Several tokens: the two products
+ * go through the tensor-core path into scratch (a->workspace of at least
+ * qmm_glu_workspace_bytes(a) bytes, else the library's) and one
+ * elementwise launch combines them. GGUF formats only (QMM_ERR_FORMAT for
+ * affine ones or an unknown act); flags as for qmm_matmul_ex. */
+int qmm_matmul_glu(const qmm_args *a, const void *w_up, int act);
+size_t qmm_glu_workspace_bytes(const qmm_args *a);
+
 /* y = x @ W for an affine matrix (a->fmt = QMM_AFFINE4 or QMM_AFFINE8):
  * a->w holds the code words, `scales` and `biases` the bf16 arrays [n][k/64]
  * (device memory, 16-byte aligned; NULL only when there is no work). Every

@@ -470,13 +470,17 @@ int oracle_matmul_affine_sampled(int bits, const uint8_t *w, const uint8_t *sc,
 
 /* ---------------------------------------------------------------------------
  * Gated products: y = act(x Wg) * (x Wu). act 0: silu(g) = g / (1 + e^-g);
- * act 1: GELU, tanh form, 0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))). */
+ * act 1: GELU, tanh form, 0.5 g (1 + tanh(z)) with z = sqrt(2/pi) (g +
+ * 0.044715 g^3). Since 0.5 (1 + tanh z) = 1 / (1 + e^(-2z)) exactly, the
+ * second form is evaluated: the first cancels to nothing in double once
+ * z < -19, the second keeps its relative precision. */
 
 double oracle_act(int act, double g)
 {
     if (act == 0) return g / (1.0 + exp(-g));
     const double c = sqrt(2.0 / 3.14159265358979323846);
-    return 0.5 * g * (1.0 + tanh(c * (g + 0.044715 * g * g * g)));
+    const double z = c * (g + 0.044715 * g * g * g);
+    return g / (1.0 + exp(-2.0 * z));
 }
 
 /* d act / d g, for the error bar of the gated product. */
@@ -486,10 +490,11 @@ double oracle_act_deriv(int act, double g)
         const double sg = 1.0 / (1.0 + exp(-g));
         return sg * (1.0 + g * (1.0 - sg));
     }
+    /* d/dg [g s(2z)] = s(2z) + g s(2z) (1 - s(2z)) 2 z', s the logistic function */
     const double c = sqrt(2.0 / 3.14159265358979323846);
     const double z = c * (g + 0.044715 * g * g * g);
-    const double t = tanh(z);
-    return 0.5 * (1.0 + t) + 0.5 * g * (1.0 - t * t) * c * (1.0 + 3.0 * 0.044715 * g * g);
+    const double sg = 1.0 / (1.0 + exp(-2.0 * z));
+    return sg + g * sg * (1.0 - sg) * 2.0 * c * (1.0 + 3.0 * 0.044715 * g * g);
 }
 
 /* y[t][j] = act(gate) * up with gate = sum_i x w_g, up = sum_i x w_u (double

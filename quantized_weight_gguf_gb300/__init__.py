@@ -29,7 +29,8 @@ EXPORTS = ("qmm_weight_bytes", "qmm_matmul", "qmm_set_stream", "qmm_matmul_ex",
            "qmm_workspace_bytes", "qmm_select_path", "qmm_matmul_host", "qmm_dequant",
            "qmm_device_status", "qmm_last_error", "qmm_version", "qmm_matmul_noalloc",
            "qmm_matmul_backward_input", "qmm_backward_input_workspace_bytes",
-           "qmm_matmul_experts", "qmm_matmul_affine", "qmm_dequant_affine")
+           "qmm_matmul_experts", "qmm_matmul_affine", "qmm_dequant_affine", "qmm_matmul_glu",
+           "qmm_glu_workspace_bytes")
 
 
 class QmmError(RuntimeError):
@@ -78,6 +79,8 @@ def load(path: str = LIB_PATH):
         "qmm_backward_input_workspace_bytes": (sz, [pa]),
         "qmm_matmul_experts": (i, [pa, vp, i64, i64]),
         "qmm_matmul_affine": (i, [pa, vp, vp]),
+        "qmm_matmul_glu": (i, [pa, vp, i]),
+        "qmm_glu_workspace_bytes": (sz, [pa]),
         "qmm_dequant_affine": (i, [i, vp, vp, vp, i64, i64, vp, vp]),
     }
     for name, (res, args) in sig.items():
@@ -148,6 +151,19 @@ def qmm_matmul_noalloc(args: qmm_args) -> int:
 
 def qmm_matmul_backward_input(args: qmm_args) -> int:
     return _check(load().qmm_matmul_backward_input(ctypes.byref(args)))
+
+
+ACT_SWIGLU, ACT_GEGLU = 1, 2
+ACTS = {"swiglu": ACT_SWIGLU, "geglu": ACT_GEGLU}
+
+
+def qmm_matmul_glu(args: qmm_args, w_up, act) -> int:
+    act = ACTS[act] if isinstance(act, str) else int(act)
+    return _check(load().qmm_matmul_glu(ctypes.byref(args), _ptr(w_up), act))
+
+
+def qmm_glu_workspace_bytes(args: qmm_args) -> int:
+    return load().qmm_glu_workspace_bytes(ctypes.byref(args))
 
 
 def qmm_matmul_affine(args: qmm_args, scales, biases) -> int:
@@ -292,3 +308,25 @@ def dequant_affine(fmt, w, scales, biases, k: int, n: int, stream=None):
     out = torch.empty((n, k), dtype=torch.float32, device=w.device)
     qmm_dequant_affine(fmt, w, scales, biases, k, n, out, stream)
     return out
+
+
+def matmul_glu(act, fmt, w_gate, w_up, x, k: int, n: int, *, y=None, j_start=0, j_end=0,
+               accumulate=False, path=PATH_AUTO, stream=None, flags=0):
+    """y = act(x Wg) * (x Wu) ("swiglu" / "geglu") for torch CUDA tensors; the
+    scratch of the several-token form is a torch allocation on x's device."""
+    import torch
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    nt = x.shape[0]
+    if y is None:
+        y = torch.empty((nt, n), dtype=torch.float32, device=x.device)
+    a = make_args(fmt, w_gate, x, y, k, n, nt, w_len=w_gate.numel() * w_gate.element_size(),
+                  j_start=j_start, j_end=j_end, accumulate=accumulate, path=path, stream=stream,
+                  flags=flags)
+    need = qmm_glu_workspace_bytes(a)
+    ws = None
+    if need:
+        ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+        a.workspace, a.workspace_bytes = ws.data_ptr(), need
+    qmm_matmul_glu(a, w_up, act)
+    return y

@@ -251,6 +251,18 @@ int run(const qmm_args *a, const void *sc = nullptr, const void *bi = nullptr,
     return QMM_OK;
 }
 
+size_t round256_bytes(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// One token on the GEMV path: the fused gated GEMV; otherwise two products
+// into scratch and an elementwise combine.
+bool glu_fused(const qmm_args *a) {
+    return a->n_tokens == 1 && a->path != QMM_PATH_MMA && qmm::gemv_supports(a->fmt, a->k);
+}
+
+size_t glu_scratch_bytes(const qmm_args *a) {
+    const size_t one = round256_bytes((size_t)a->n_tokens * (size_t)a->n * 4);
+    return 2 * one + qmm::mma_workspace_bytes(a->fmt, a->n_tokens, a->k);
+}
 }  // namespace
 
 namespace qmm {
@@ -473,6 +485,92 @@ int qmm_dequant(int fmt, const void *w, int64_t k, int64_t n, float *out, void *
     cudaError_t e = qmm::launch_dequant(fmt, static_cast<const uint8_t *>(w), k, n, r, out,
                                         static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QMM_OK : cuda_fail(e, "dequant launch");
+}
+
+
+size_t qmm_glu_workspace_bytes(const qmm_args *a) {
+    int64_t j0, j1, rb;
+    if (!a || affine_fmt(a->fmt) || validate(a, &j0, &j1, &rb, false) != QMM_OK) return 0;
+    if (a->k == 0 || j1 <= j0 || glu_fused(a)) return 0;
+    return glu_scratch_bytes(a);
+}
+
+int qmm_matmul_glu(const qmm_args *a, const void *w_up, int act) {
+    t_err[0] = 0;
+    if (!a) return fail(QMM_ERR_NULL, "args is NULL");
+    if (act != QMM_ACT_SWIGLU && act != QMM_ACT_GEGLU)
+        return fail(QMM_ERR_FORMAT, "unknown activation %d", act);
+    if (affine_fmt(a->fmt))
+        return fail(QMM_ERR_FORMAT, "gated products take single-stream (GGUF) formats");
+    int64_t j0, j1, rb;
+    int st = validate(a, &j0, &j1, &rb, true);
+    if (st != QMM_OK) return st;
+    if (j1 <= j0) return QMM_OK;
+    if (a->k > 0) {
+        if (!w_up) return fail(QMM_ERR_NULL, "w_up is NULL");
+        if (reinterpret_cast<uintptr_t>(w_up) & 15u)
+            return fail(QMM_ERR_ALIGN, "w_up must be 16-byte aligned");
+    }
+    if (a->n_tokens == 1 && a->path == QMM_PATH_GEMV && !qmm::gemv_supports(a->fmt, a->k))
+        return fail(QMM_ERR_UNSUPPORTED, "GEMV path cannot take %s with k=%lld", fmt_name(a->fmt),
+                    (long long)a->k);
+    qmm::DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != QMM_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(a->stream);
+    if (a->k == 0) {  // gate = up = 0: y = 0 (unchanged when accumulating)
+        if (a->accumulate) return QMM_OK;
+        cudaError_t e = qmm::launch_zero_cols(a->y, a->n_tokens, a->n, j0, j1, s);
+        return e == cudaSuccess ? QMM_OK : cuda_fail(e, "zero-fill launch");
+    }
+    if (glu_fused(a)) {
+        qmm::GemvLaunch g;
+        g.fmt = a->fmt;
+        g.w = static_cast<const uint8_t *>(a->w);
+        g.w2 = static_cast<const uint8_t *>(w_up);
+        g.glu = act;
+        g.x = a->x;
+        g.y = a->y;
+        g.k = a->k; g.n = a->n; g.row_bytes = rb;
+        g.j0 = j0; g.j1 = j1;
+        g.accumulate = a->accumulate;
+        g.overlap_prev = (a->flags & QMM_FLAG_OVERLAP_PREV) != 0;
+        g.x_ready = g.overlap_prev && (a->flags & QMM_FLAG_X_READY) != 0;
+        cudaError_t e = qmm::launch_gemv(g, *dev, s);
+        return e == cudaSuccess ? QMM_OK : cuda_fail(e, "gated GEMV launch");
+    }
+    const size_t need = glu_scratch_bytes(a);
+    void *ws = a->workspace;
+    if (ws) {
+        if (a->workspace_bytes < need)
+            return fail(QMM_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", a->workspace_bytes,
+                        need);
+        if (reinterpret_cast<uintptr_t>(ws) & 255u)
+            return fail(QMM_ERR_ALIGN, "workspace must be 256-byte aligned");
+    } else {
+        st = library_workspace(need, &ws);
+        if (st != QMM_OK) return st;
+    }
+    const size_t one = round256_bytes((size_t)a->n_tokens * (size_t)a->n * 4);
+    float *gbuf = static_cast<float *>(ws);
+    float *ubuf = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + one);
+    void *mws = static_cast<uint8_t *>(ws) + 2 * one;
+    for (int m = 0; m < 2; ++m) {
+        qmm::MmaLaunch ml;
+        ml.fmt = a->fmt;
+        ml.w = static_cast<const uint8_t *>(m ? w_up : a->w);
+        ml.x = a->x;
+        ml.y = m ? ubuf : gbuf;
+        ml.k = a->k; ml.n = a->n; ml.n_tokens = a->n_tokens; ml.row_bytes = rb;
+        ml.j0 = j0; ml.j1 = j1;
+        ml.accumulate = 0;
+        ml.workspace = mws;
+        cudaError_t e = qmm::launch_mma(ml, *dev, s);
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core launch");
+    }
+    cudaError_t e = qmm::launch_glu_combine(gbuf, ubuf, a->y, a->n_tokens, a->n, j0, j1, act,
+                                            a->accumulate, s);
+    return e == cudaSuccess ? QMM_OK : cuda_fail(e, "gated combine launch");
 }
 
 int qmm_matmul_affine(const qmm_args *a, const void *scales, const void *biases) {

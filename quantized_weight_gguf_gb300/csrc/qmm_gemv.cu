@@ -69,27 +69,49 @@ struct GemvAffFields {
     int aux_off, aux_sb;
 };
 struct GemvAffParams : GemvParams, GemvAffFields {};
+// Gated pairs: w is the gate matrix, w2 the up matrix (same format and
+// shape); y = act(x Wg) * (x Wu). A CTA's stages alternate between a block
+// of rows of Wg and the same rows of Wu; each window of rows keeps two sets
+// of partial sums, and its flush writes act(gate) * up.
+struct GemvGluParams : GemvParams {
+    const uint8_t *w2;
+};
 // everything the host fills in; each kernel instance takes only its own part
-struct GemvHostParams : GemvExpParams, GemvAffFields {};
+struct GemvHostParams : GemvExpParams, GemvAffFields {
+    const uint8_t *w2;
+    int glu;  // 0 none, 1 SwiGLU, 2 GeGLU
+};
 
-template <int FMT, bool EXP>
+// Kernel variants: plain, expert-indexed, gated pair with SwiGLU or GeGLU.
+enum GemvVar : int { kVarPlain = 0, kVarExperts = 1, kVarSwiglu = 2, kVarGeglu = 3 };
+
+template <int FMT, int VAR>
 using GemvParamsOf = typename std::conditional<
     is_affine(FMT), GemvAffParams,
-    typename std::conditional<EXP, GemvExpParams, GemvParams>::type>::type;
+    typename std::conditional<
+        VAR == kVarExperts, GemvExpParams,
+        typename std::conditional<(VAR >= kVarSwiglu), GemvGluParams, GemvParams>::type>::type>::type;
 
-template <int FMT, bool EXP>
-__host__ GemvParamsOf<FMT, EXP> params_of(const GemvHostParams &h) {
+template <int FMT, int VAR>
+__host__ GemvParamsOf<FMT, VAR> params_of(const GemvHostParams &h) {
     if constexpr (is_affine(FMT)) {
         GemvAffParams a;
         static_cast<GemvParams &>(a) = static_cast<const GemvParams &>(h);
         static_cast<GemvAffFields &>(a) = static_cast<const GemvAffFields &>(h);
         return a;
-    } else if constexpr (EXP) {
+    } else if constexpr (VAR == kVarExperts) {
         return static_cast<const GemvExpParams &>(h);
+    } else if constexpr (VAR >= kVarSwiglu) {
+        GemvGluParams gp;
+        static_cast<GemvParams &>(gp) = static_cast<const GemvParams &>(h);
+        gp.w2 = h.w2;
+        return gp;
     } else {
         return static_cast<const GemvParams &>(h);
     }
 }
+
+
 
 // Weights per unit: a 16-byte chunk for 16-bit formats (lane-contiguous in
 // shared memory), a 32-weight block for Q4_0, a 32-weight sub-block for Q4_K
@@ -436,16 +458,19 @@ struct SliceSel<true> {
     __device__ __forceinline__ int64_t w_off() const { return off; }
 };
 
-template <int FMT, int UPT, bool EXP>
-__global__ void __maxnreg__(96) gemv_kernel(const GemvParamsOf<FMT, EXP> p) {
+template <int FMT, int UPT, int VAR>
+__global__ void __maxnreg__(96) gemv_kernel(const GemvParamsOf<FMT, VAR> p) {
     constexpr bool kChunked = (FMT == F_BF16 || FMT == F_F16);  // warp-reduced 16-byte chunks
+    constexpr bool EXP = VAR == kVarExperts, GLU = VAR >= kVarSwiglu;
     extern __shared__ __align__(128) uint8_t smem[];
     const int NS = p.NS, SR = p.SR, SB = p.SB, PU = p.PU;
     const uint32_t bar0 = smem_addr(smem);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 16 * NS);
     float *part = reinterpret_cast<float *>(smem + 16 * NS + 16);
     const int part_bytes = 4 * p.RPF * PU;
-    const int xs_off = (16 * NS + 16 + part_bytes + 127) & ~127;
+    // gated pairs: a second set of partials (the up rows) after the first
+    float *part_up = part + p.RPF * PU;
+    const int xs_off = (16 * NS + 16 + (GLU ? 2 : 1) * part_bytes + 127) & ~127;
     float *xs = reinterpret_cast<float *>(smem + xs_off);
     // 16-bit formats read their x slices straight from global memory (each
     // thread's units are contiguous 32-byte runs): no staging area
@@ -476,8 +501,16 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParamsOf<FMT, EXP> p) {
     }
     const int64_t r0 = p.j0 + (int64_t)cta * p.rows_base + (cta < p.rows_rem ? cta : p.rows_rem);
     const int64_t nrows = p.rows_base + (cta < p.rows_rem ? 1 : 0);
-    const int nst = (int)((nrows + SR - 1) / SR);
+    // gated pairs: stage 2i streams row block i of the gate matrix, stage
+    // 2i + 1 the same rows of the up matrix
+    const int nst_half = (int)((nrows + SR - 1) / SR);
+    const int nst = GLU ? 2 * nst_half : nst_half;
     const int64_t R = p.row_bytes;
+    auto stage_rows = [&](int s, int64_t &ra, int64_t &rb) {
+        const int sl = GLU ? s >> 1 : s;
+        ra = r0 + (int64_t)sl * SR;
+        rb = min(ra + SR, r0 + nrows);
+    };
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -504,14 +537,18 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParamsOf<FMT, EXP> p) {
                 *abort_flag = 1;
                 break;
             }
-            const int64_t ra = r0 + (int64_t)s * SR;
-            const int64_t rb = min(ra + SR, r0 + nrows);
+            int64_t ra, rb;
+            stage_rows(s, ra, rb);
+            const uint8_t *wsrc = p.w;
+            if constexpr (GLU) {
+                if (s & 1) wsrc = p.w2;
+            }
             const int64_t A = sel.w_off() + ra * R, B = sel.w_off() + rb * R;
             const int64_t a16 = A & ~(int64_t)15, b16 = (B + 15) & ~(int64_t)15;
             const int64_t tend = min(b16, lim);
             if (B > lim) {  // bytes after the last whole 16-byte chunk of W
                 for (int64_t q = max(a16, lim); q < B; ++q)
-                    stages[(int64_t)slot * SB + (q - a16)] = p.w[q];
+                    stages[(int64_t)slot * SB + (q - a16)] = wsrc[q];
             }
             const uint32_t tx = tend > a16 ? (uint32_t)(tend - a16) : 0u;
             if constexpr (is_affine(FMT)) {
@@ -529,14 +566,14 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParamsOf<FMT, EXP> p) {
                 }
                 const uint32_t atx = send > s16 ? (uint32_t)(send - s16) : 0u;
                 mbar_arrive_expect_tx(full(slot), tx + 2u * atx);
-                if (tx) bulk_g2s(stage0 + (uint32_t)slot * SB, p.w + a16, tx, full(slot));
+                if (tx) bulk_g2s(stage0 + (uint32_t)slot * SB, wsrc + a16, tx, full(slot));
                 if (atx) {
                     bulk_g2s(stage0 + (uint32_t)sdst, p.sc + s16, atx, full(slot));
                     bulk_g2s(stage0 + (uint32_t)(sdst + p.aux_sb), p.bi + s16, atx, full(slot));
                 }
             } else {
                 mbar_arrive_expect_tx(full(slot), tx);
-                if (tx) bulk_g2s(stage0 + (uint32_t)slot * SB, p.w + a16, tx, full(slot));
+                if (tx) bulk_g2s(stage0 + (uint32_t)slot * SB, wsrc + a16, tx, full(slot));
             }
             ++issued;
         }
@@ -605,12 +642,12 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParamsOf<FMT, EXP> p) {
             *abort_flag = 1;
             record_error(p.err, DERR_GEMV_FULL);
         }
-        const int64_t ra = r0 + (int64_t)s * SR;
-        const int64_t rb = min(ra + SR, r0 + nrows);
+        int64_t ra, rb;
+        stage_rows(s, ra, rb);
         const int rows_in = (int)(rb - ra);
         const int64_t a16 = (sel.w_off() + ra * R) & ~(int64_t)15;
         const uint32_t sbase = stage0 + (uint32_t)slot * SB;
-        float *pb = part + (ra - fbase) * PU;
+        float *pb = ((GLU && (s & 1)) ? part_up : part) + (ra - fbase) * PU;
         if (!failed && active) {
             // same trip count for every lane of a warp (segments of one warp may
             // belong to different row groups), so the shuffles stay convergent
@@ -648,17 +685,24 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParamsOf<FMT, EXP> p) {
         if (lane == 0) mbar_arrive(empty(slot));
         __syncwarp();
         // block-wide reduction once the window is full, and at the end
-        if (rb - fbase >= p.RPF || s == nst - 1) {
+        if ((!GLU || (s & 1)) && (rb - fbase >= p.RPF || s == nst - 1)) {
             if (p.x_ready) pdl_wait_prev();  // y may still be in use by the preceding kernel
             named_barrier(1, kCons);
             if (!failed) {
                 const int wrows = (int)(rb - fbase);
                 for (int rr = warp; rr < wrows; rr += kConsWarps) {
-                    float v = 0.0f;
-                    for (int i = lane; i < PU; i += 32) v += part[rr * PU + i];
+                    float v = 0.0f, vu = 0.0f;
+                    for (int i = lane; i < PU; i += 32) {
+                        v += part[rr * PU + i];
+                        if (GLU) vu += part_up[rr * PU + i];
+                    }
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                    for (int o = 16; o > 0; o >>= 1) {
+                        v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                        if (GLU) vu += __shfl_xor_sync(0xFFFFFFFFu, vu, o);
+                    }
                     if (lane == 0) {
+                        if (GLU) v = glu_act<VAR - kVarSwiglu + 1>(v) * vu;
                         float *yp = sel.y(p) + fbase + rr;
                         *yp = p.accumulate ? *yp + v : v;
                     }
@@ -684,19 +728,19 @@ bool gemv_supports(int fmt, int64_t k) {
     return U <= (int64_t)kCons * max_upt(fmt);
 }
 
-template <int FMT, int UPT, bool EXP>
+template <int FMT, int UPT, int VAR>
 static cudaError_t launch_e(const GemvHostParams &h, dim3 grid, size_t smem, cudaStream_t s,
                             bool overlap) {
-    const GemvParamsOf<FMT, EXP> p = params_of<FMT, EXP>(h);
+    const GemvParamsOf<FMT, VAR> p = params_of<FMT, VAR>(h);
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(gemv_kernel<FMT, UPT, EXP>,
+        attr_err = cudaFuncSetAttribute(gemv_kernel<FMT, UPT, VAR>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (!overlap) {
-        gemv_kernel<FMT, UPT, EXP><<<grid, kGemvThreads, smem, s>>>(p);
+        gemv_kernel<FMT, UPT, VAR><<<grid, kGemvThreads, smem, s>>>(p);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -709,7 +753,7 @@ static cudaError_t launch_e(const GemvHostParams &h, dim3 grid, size_t smem, cud
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<FMT, UPT, EXP>, p);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<FMT, UPT, VAR>, p);
 }
 
 // the expert-indexed kernels are separate instances: the plain GEMV carries
@@ -718,11 +762,14 @@ template <int FMT, int UPT>
 static cudaError_t launch_t(const GemvHostParams &p, dim3 grid, size_t smem, cudaStream_t s,
                             bool overlap) {
     if constexpr (is_affine(FMT)) {
-        if (p.ids) return cudaErrorNotSupported;  // no expert-indexed affine matrices
-        return launch_e<FMT, UPT, false>(p, grid, smem, s, overlap);
+        // no expert-indexed or gated affine matrices
+        if (p.ids || p.glu) return cudaErrorNotSupported;
+        return launch_e<FMT, UPT, kVarPlain>(p, grid, smem, s, overlap);
     } else {
-        return p.ids ? launch_e<FMT, UPT, true>(p, grid, smem, s, overlap)
-                     : launch_e<FMT, UPT, false>(p, grid, smem, s, overlap);
+        if (p.ids) return launch_e<FMT, UPT, kVarExperts>(p, grid, smem, s, overlap);
+        if (p.glu == 1) return launch_e<FMT, UPT, kVarSwiglu>(p, grid, smem, s, overlap);
+        if (p.glu == 2) return launch_e<FMT, UPT, kVarGeglu>(p, grid, smem, s, overlap);
+        return launch_e<FMT, UPT, kVarPlain>(p, grid, smem, s, overlap);
     }
 }
 
@@ -775,8 +822,9 @@ cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t
     auto code_bytes = [&](int64_t sr) { return ((sr * R + 32) + 127) & ~(int64_t)127; };
     auto aux_bytes = [&](int64_t sr) { return aff ? ((sr * AR + 32) + 127) & ~(int64_t)127 : 0; };
     auto stage_bytes = [&](int64_t sr) { return code_bytes(sr) + 2 * aux_bytes(sr); };
+    // gated pairs keep a second set of partials
     auto smem_for = [&](int ns, int64_t sr, int64_t rpf) {
-        const size_t part_bytes = (size_t)4 * rpf * PU;
+        const size_t part_bytes = (size_t)4 * rpf * PU * (g.glu ? 2 : 1);
         const size_t sb = (size_t)stage_bytes(sr);
         return (size_t)((((16 * ns + 16 + part_bytes + 127) & ~(size_t)127) + xs_bytes + 127) &
                         ~(size_t)127) +
@@ -792,11 +840,12 @@ cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t
     int64_t SR, RPF;
     int NS;
     const int64_t half = G * (((per_cta + 1) / 2 + G - 1) / G);
-    if (smem_for(2, half, 2 * half) <= two_cta_limit) {
-        // the CTA's whole share fits in two stages: all of it is requested at
-        // once, one memory round trip per CTA
+    const int ns_whole = g.glu ? 4 : 2;  // gated pairs: both matrices' rows
+    if (smem_for(ns_whole, half, 2 * half) <= two_cta_limit) {
+        // the CTA's whole share fits in two stages (per matrix): all of it is
+        // requested at once, one memory round trip per CTA
         SR = half;
-        NS = 2;
+        NS = ns_whole;
         RPF = 2 * half;
     } else {
         // rows per stage: ~32 KB of weights, a multiple of the row groups, and
@@ -807,6 +856,13 @@ cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t
         // partial-sum window: ~24 KB, whole stages, no more than a CTA's rows
         RPF = std::max<int64_t>(SR, (6144 / PU) / SR * SR);
         RPF = std::min<int64_t>(RPF, std::max<int64_t>(SR, (per_cta + SR - 1) / SR * SR));
+        // gated pairs: two sets of partials; the window is as many stages as
+        // fit beside a two-stage ring with two CTAs per SM (fewer flushes)
+        if (g.glu) {
+            const int64_t cap = std::max<int64_t>(SR, (per_cta + SR - 1) / SR * SR);
+            RPF = SR;
+            while (RPF + SR <= cap && smem_for(2, SR, RPF + SR) <= two_cta_limit) RPF += SR;
+        }
         NS = 8;
         while (NS > 2 && smem_for(NS, SR, RPF) > two_cta_limit) --NS;
         if (smem_for(NS, SR, RPF) > two_cta_limit) {  // one CTA per SM, up to 8 stages
@@ -829,6 +885,8 @@ cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t
     p.aux_total = AR * g.n;
     p.aux_off = (int)code_bytes(SR);
     p.aux_sb = (int)aux_bytes(SR);
+    p.w2 = g.w2;
+    p.glu = g.glu;
     p.k = g.k; p.row_bytes = R;
     p.w_total = R * g.n * (g.ids ? g.n_experts : 1);
     p.ids = g.ids;

@@ -32,6 +32,10 @@ struct GemvLaunch {
     int n_experts = 0, top_k = 1, pairs = 1;
     // affine formats: bf16 scale and bias arrays [n][k/64]
     const uint8_t *sc = nullptr, *bi = nullptr;
+    // gated pair (glu 1: SwiGLU, 2: GeGLU): w is the gate matrix, w2 the up
+    // matrix; y = act(x Wg) * (x Wu)
+    const uint8_t *w2 = nullptr;
+    int glu = 0;
 };
 // Returns cudaSuccess or the launch error; cudaErrorNotSupported when no
 // GEMV variant takes the shape (the caller then uses the tensor-core path).
@@ -82,6 +86,11 @@ cudaError_t launch_dequant(int fmt, const uint8_t *w, int64_t k, int64_t n, int6
 cudaError_t launch_zero_cols(float *y, int64_t n_tokens, int64_t n, int64_t j0, int64_t j1,
                              cudaStream_t s);
 
+// y[t][j] (+)= act(g[t][j]) * u[t][j] over [j0, j1) (act 1 SwiGLU, 2 GeGLU;
+// g, u and y share the row stride n).
+cudaError_t launch_glu_combine(const float *g, const float *u, float *y, int64_t n_tokens,
+                               int64_t n, int64_t j0, int64_t j1, int act, int accumulate,
+                               cudaStream_t s);
 // Record a status and message for qmm_last_error() on this host thread; returns status.
 int set_error(int status, const char *fmt, ...);
 

@@ -178,6 +178,52 @@ __device__ __forceinline__ void to_half_words<F_Q4_K>(const Raw32<F_Q4_K> &raw,
     }
 }
 
+// Affine 4-bit: w = q s + b as (256 s) (0.5 + q/256) + (b - 128 s), the
+// code riding the exact byte carrier, two weights per packed fp32 fma, then
+// RN to fp16 (b - 128 s rounds in fp32, far below the fp16 rounding of w).
+// Word i holds elements 8i .. 8i+7, lowest nibble first: byte j of the
+// low-nibble mask is element 8i + 2j, of the high-nibble mask 8i + 2j + 1,
+// so each (low, high) byte pair is one fp16x2 word of consecutive k.
+template <>
+__device__ __forceinline__ void to_half_words<F_AFF4>(const Raw32<F_AFF4> &raw,
+                                                      uint32_t (&hw)[16]) {
+    const float sc = __uint_as_float(raw.sbits << 16), bi = __uint_as_float(raw.bbits << 16);
+    const float a = 256.0f * sc, c = fmaf(-128.0f, sc, bi);
+    const float2 av = make_float2(a, a), cv = make_float2(c, c);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = raw.qw[i] & 0x0F0F0F0Fu, hi = (raw.qw[i] >> 4) & 0x0F0F0F0Fu;
+        float2 f;
+        f = ffma2(make_float2(byte_half_plus<0>(lo), byte_half_plus<0>(hi)), av, cv);
+        hw[4 * i] = pack_half2(f.x, f.y);
+        f = ffma2(make_float2(byte_half_plus<1>(lo), byte_half_plus<1>(hi)), av, cv);
+        hw[4 * i + 1] = pack_half2(f.x, f.y);
+        f = ffma2(make_float2(byte_half_plus<2>(lo), byte_half_plus<2>(hi)), av, cv);
+        hw[4 * i + 2] = pack_half2(f.x, f.y);
+        f = ffma2(make_float2(byte_half_plus<3>(lo), byte_half_plus<3>(hi)), av, cv);
+        hw[4 * i + 3] = pack_half2(f.x, f.y);
+    }
+}
+
+// Affine 8-bit: q exactly as (2^23 + q) - 2^23, then fma(q, s, b) two weights
+// at a time and RN to fp16; byte j of word i is element 4i + j.
+template <>
+__device__ __forceinline__ void to_half_words<F_AFF8>(const Raw32<F_AFF8> &raw,
+                                                      uint32_t (&hw)[16]) {
+    const float sc = __uint_as_float(raw.sbits << 16), bi = __uint_as_float(raw.bbits << 16);
+    const float2 sv = make_float2(sc, sc), bv = make_float2(bi, bi);
+    const float2 zp = make_float2(-8388608.0f, -8388608.0f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t w = raw.qw[i];
+        const float2 q01 = fadd2(make_float2(byte_magic23<0>(w), byte_magic23<1>(w)), zp);
+        const float2 q23 = fadd2(make_float2(byte_magic23<2>(w), byte_magic23<3>(w)), zp);
+        const float2 f01 = ffma2(q01, sv, bv), f23 = ffma2(q23, sv, bv);
+        hw[2 * i] = pack_half2(f01.x, f01.y);
+        hw[2 * i + 1] = pack_half2(f23.x, f23.y);
+    }
+}
+
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t v) {
     return *reinterpret_cast<const __half2 *>(&v);
 }

@@ -245,3 +245,31 @@ def test_affine_dequant_rejected_on_host(lib):
 
 def test_affine_empty_work_needs_no_device(lib):
     assert q.qmm_matmul_affine(_args(fmt="affine4", k=128, j_start=3, j_end=3), None, None) == 0
+
+
+# ------------------------------------------------------------ gated pairs ----
+
+@pytest.mark.parametrize("kw,wu,act,status", [
+    (dict(), 16 * 900, 0, 1),                 # unknown activation
+    (dict(), 16 * 900, 3, 1),
+    (dict(fmt="affine4", k=128), 16 * 900, 1, 1),
+    (dict(k=300), 16 * 900, 1, 2),
+    (dict(w_len=10), 16 * 900, 2, 3),
+    (dict(j_start=4, j_end=2), 16 * 900, 1, 4),
+    (dict(), None, 1, 5),
+    (dict(), 16 * 900 + 4, 2, 6),
+    (dict(k=16384 * 4, path=q.PATH_GEMV), 16 * 900, 1, 10),
+])
+def test_glu_rejected_on_host(lib, kw, wu, act, status):
+    with pytest.raises(q.QmmError) as ei:
+        q.qmm_matmul_glu(_args(**kw), wu, act)
+    assert ei.value.status == status, q.qmm_last_error()
+
+
+def test_glu_workspace_and_empty_work(lib):
+    assert q.qmm_glu_workspace_bytes(_args(k=4096, n=14336)) == 0          # fused GEMV
+    a = _args(k=4096, n=1000, n_tokens=8)
+    one = (8 * 1000 * 4 + 255) // 256 * 256
+    assert q.qmm_glu_workspace_bytes(a) == 2 * one + 8 * 4096 * 2 + 256
+    assert q.qmm_glu_workspace_bytes(_args(fmt="affine4", k=128)) == 0
+    assert q.qmm_matmul_glu(_args(j_start=3, j_end=3), None, 1) == 0

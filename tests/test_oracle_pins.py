@@ -697,6 +697,31 @@ def test_gelu_tanh_form_against_erf_gelu_and_sigmoid_identity():
     assert abs(oracle.act("geglu", 1.0) - 0.8411919906) < 1e-10
 
 
+def test_gelu_stable_form_matches_the_literal_tanh_form():
+    """Where 0.5 g (1 + tanh z) is still accurate in double (|z| < 3), it and
+    the oracle's g / (1 + e^(-2z)) agree to rounding; far into the negative
+    tail the oracle keeps relative precision (it equals g e^(2z) to first order)."""
+    c = np.sqrt(2.0 / np.pi)
+    for g in np.linspace(-2.5, 2.5, 101):
+        z = c * (g + 0.044715 * g ** 3)
+        assert abs(oracle.act("geglu", g) - 0.5 * g * (1 + np.tanh(z))) <= 1e-15
+    for g in (-8.0, -12.0, -20.0):
+        z = c * (g + 0.044715 * g ** 3)
+        v = oracle.act("geglu", g)
+        assert v < 0 and abs(v / (g * np.exp(2 * z)) - 1) < 1e-6
+
+
+def test_checker_absolute_floor():
+    y_ref = np.array([[1e-40, 1.0]])
+    s_ref = np.array([[1e-41, 1.0]])
+    ok, *_ = oracle.check(np.array([[0.0, 1.0]]), y_ref, s_ref)
+    assert not ok
+    ok, *_ = oracle.check(np.array([[0.0, 1.0]]), y_ref, s_ref, atol=oracle.FLT_MIN)
+    assert ok
+    ok, *_ = oracle.check(np.array([[0.0, 1.001]]), y_ref, s_ref, atol=oracle.FLT_MIN)
+    assert not ok
+
+
 def test_activation_derivatives_by_central_differences():
     for name in ("swiglu", "geglu"):
         for g in (-6.0, -1.3, -0.2, 0.0, 0.4, 1.7, 5.0):
