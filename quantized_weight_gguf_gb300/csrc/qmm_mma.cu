@@ -96,6 +96,9 @@ static size_t round256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 int mma_mode(int fmt, int64_t k) {
     if (fmt == F_BF16 || fmt == F_F16) return 2;  // W is fp16-exact: split x only
+    // affine rows take the raw-tile path in whole 256-wide slices; other k
+    // decode from registers with both operands split
+    if (is_affine(fmt) && k % 256 != 0) return 3;
     if (k >= 4096) return 1;
     if (k >= 1024) return 2;
     return 3;
@@ -193,13 +196,18 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
     // raw Q4_K weight tiles: the packed rows as a 2-D byte tensor [n][row_bytes],
     // boxes of 128 rows x one 144-byte super-block
     tw = tm;
-    if (m.fmt == F_Q4_K && mode != 3) {
+    if (raw_slice_bytes(m.fmt, mode) > 0) {
+        // raw W tiles: Q4_K boxes of 128 rows x one 144-byte super-block;
+        // affine code boxes of 128 rows x 128 bytes, 128-byte swizzled (the
+        // dequant warps read 16-byte chunks of 32 consecutive rows)
+        const bool aff = is_affine(m.fmt);
         const cuuint64_t dims[2] = {(cuuint64_t)m.row_bytes, (cuuint64_t)m.n};
         const cuuint64_t strides[1] = {(cuuint64_t)m.row_bytes};
-        const cuuint32_t box[2] = {144u, (cuuint32_t)kBM};
+        const cuuint32_t box[2] = {aff ? 128u : 144u, (cuuint32_t)kBM};
         const cuuint32_t estr[2] = {1, 1};
         if (encode(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(m.w), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   aff ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;

@@ -81,6 +81,14 @@ using MmaParamsOf = typename std::conditional<is_affine(FMT), MmaAffParams, MmaP
 // 256-wide slice of k), then decoded from shared memory.
 constexpr int kRawBytes = kBM * 144;
 
+// Raw W tiles staged by TMA (one box of 128 rows x the bytes of a 256-wide k
+// slice): Q4_K super-blocks (144 B) and affine code words (128 B at 4 bits,
+// 256 B at 8; their scales and biases come from global memory per thread).
+// MODE 3 (rows split into hi / lo halves) decodes from registers instead.
+__host__ __device__ constexpr int raw_slice_bytes(int fmt, int mode) {
+    return mode == 3 ? 0 : fmt == F_Q4_K ? 144 : fmt == F_AFF4 ? 128 : fmt == F_AFF8 ? 256 : 0;
+}
+
 // Tensor memory (512 columns x 128 lanes of 32 bits, all taken by the one CTA
 // on the SM): the fp32 accumulator(s) first, then a ring of NA dequantized W
 // stages (A operand: row r on lane r, k pairs packed per column, 32 columns
@@ -91,8 +99,9 @@ constexpr int kRawBytes = kBM * 144;
 // then pays one raw-tile wait, one slot wait and one arrival per two decoded
 // chunks. An x stage is KB k-steps, 32 KB at most (the x tile of 256 tokens
 // is 32 KB per k-step).
-template <int BN, bool RAW>
+template <int BN, int RAWB>  // RAWB: bytes of one raw W tile (0: no raw ring)
 struct MmaCfg {
+    static constexpr bool RAW = RAWB > 0;
     static constexpr int KA = 4;
     static constexpr int KB = BN >= 256 ? 1 : (BN >= 128 ? 2 : 4);
     static constexpr int kBBytes = BN * kBK * 2;            // one k-step of x
@@ -110,13 +119,13 @@ struct MmaCfg {
     // raw W stages: as many as fit, up to 4, next to a minimum x ring of four
     // k-steps; HBM latency is hidden by the raw ring, L2 latency by the x ring
     static constexpr int kNBMin = (4 + KB - 1) / KB;
-    static constexpr int kRawFit = (212 * 1024 - kNBMin * kBStage) / kRawBytes;
+    static constexpr int kRawFit = RAW ? (212 * 1024 - kNBMin * kBStage) / RAWB : 0;
     static constexpr int kNR = RAW ? (kRawFit > 4 ? 4 : kRawFit) : 1;
     static_assert(!RAW || kNR >= 2, "raw W ring too shallow");
-    static constexpr int kAvail = 212 * 1024 - (RAW ? kNR * kRawBytes : 0);
+    static constexpr int kAvail = 212 * 1024 - (RAW ? kNR * RAWB : 0);
     static constexpr int NB = (kAvail / kBStage) > 8 ? 8 : (kAvail / kBStage);
     static constexpr size_t kSmemUsed = (size_t)NB * kBStage +
-                                        (RAW ? (size_t)kNR * kRawBytes : 0) + 1024 /*align*/ +
+                                        (RAW ? (size_t)kNR * RAWB : 0) + 1024 /*align*/ +
                                         512 /*barriers*/ + 2048 /*token scales*/;
     // at least half of the SM's shared memory, so that no second CTA can be
     // resident and block in its TMEM allocation (every CTA takes all 512
@@ -304,15 +313,17 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                const __grid_constant__ CUtensorMap tmw, const MmaParamsOf<FMT> p) {
     constexpr int kRowsOut = MODE == 3 ? 64 : kBM;   // output rows per CTA
     constexpr int kTokOut = MODE == 1 ? BN : BN / 2;  // tokens per CTA
-    constexpr bool kRaw = FMT == F_Q4_K && MODE != 3;  // raw W tiles by TMA
-    using C = MmaCfg<BN, kRaw>;
+    constexpr int kSliceB = raw_slice_bytes(FMT, MODE);  // raw W tiles by TMA
+    constexpr bool kRaw = kSliceB > 0;
+    constexpr int kRawB = kBM * kSliceB;
+    using C = MmaCfg<BN, kRawB>;
     constexpr int NA = C::NA, NB = C::NB, kNR = C::kNR, KA = C::KA, KB = C::KB;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
     const uint32_t B0 = sbase;                                     // x ring
     const uint32_t W0 = B0 + NB * C::kBStage;                      // raw W stages (kRaw)
-    const uint32_t bar0 = W0 + (kRaw ? kNR * kRawBytes : 0);
+    const uint32_t bar0 = W0 + (kRaw ? kNR * kRawB : 0);
     auto fullA = [&](int s) { return bar0 + 8u * s; };
     auto emptyA = [&](int s) { return bar0 + 8u * (NA + s); };
     auto fullB = [&](int s) { return bar0 + 8u * (2 * NA + s); };
@@ -570,9 +581,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(rawFull(rs), kRawBytes);
-                    tma_load_2d(W0 + rs * kRawBytes, &tmw, 144 * (kx(t, 4 * b) >> 2),
-                                (int)t.m0, rawFull(rs));
+                    // boxes of at most 128 bytes a row when swizzled (8-bit
+                    // affine rows take two)
+                    constexpr int kBoxes = FMT == F_AFF8 ? 2 : 1;
+                    mbar_arrive_expect_tx(rawFull(rs), kRawB);
+#pragma unroll
+                    for (int bx = 0; bx < kBoxes; ++bx)
+                        tma_load_2d(W0 + rs * kRawB + (uint32_t)bx * (kRawB / kBoxes), &tmw,
+                                    kSliceB * (kx(t, 4 * b) >> 2) + bx * (kSliceB / kBoxes),
+                                    (int)t.m0, rawFull(rs));
                 }
                 if (!ok) break;
             }
@@ -642,12 +659,42 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                         *abort_flag = 1;
                         break;
                     }
-                    uint4 hdr = make_uint4(0u, 0u, 0u, 0u), qv[4];
-                    const uint32_t rb = W0 + rs * kRawBytes + (uint32_t)r * 144u;
-                    if (row_ok) {
-                        hdr = lds128(rb);
+                    // Q4_K: the super-block header and this half of each chunk;
+                    // affine: this half of each k-step's codes (128-byte swizzled
+                    // rows: 16-byte chunk q of row r sits at chunk q ^ (r & 7) of
+                    // its 128-byte line) and the row's four scales and biases
+                    uint4 hdr = make_uint4(0u, 0u, 0u, 0u), qv[4], qv2[4];
+                    uint2 sc4 = make_uint2(0u, 0u), bi4 = make_uint2(0u, 0u);
+                    if constexpr (FMT == F_Q4_K) {
+                        const uint32_t rb = W0 + rs * kRawB + (uint32_t)r * 144u;
+                        if (row_ok) {
+                            hdr = lds128(rb);
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) qv[c] = lds128(rb + 16u + 32u * c + 16u * h);
+                            for (int c = 0; c < 4; ++c) qv[c] = lds128(rb + 16u + 32u * c + 16u * h);
+                        }
+                    } else {
+                        const uint32_t sw = (uint32_t)(r & 7);
+                        if (row_ok) {
+                            // the unit's super-block b is k-step t.k_lo + 4 b (before rotation)
+                            const int64_t ao = (t.m0 + r) * p.aux_row_bytes +
+                                               8 * (kx(t, t.k_lo + 4 * b) >> 2);
+                            sc4 = __ldg(reinterpret_cast<const uint2 *>(p.sc + ao));
+                            bi4 = __ldg(reinterpret_cast<const uint2 *>(p.bi + ao));
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                if (FMT == F_AFF4) {
+                                    const uint32_t rb = W0 + rs * kRawB + (uint32_t)r * 128u;
+                                    qv[c] = lds128(rb + 16u * (((uint32_t)(2 * c + h)) ^ sw));
+                                } else {
+                                    // 256-byte rows as two 128-byte sub-tiles
+                                    const uint32_t rb = W0 + rs * kRawB + (uint32_t)(c >> 1) * (kBM * 128u) +
+                                                        (uint32_t)r * 128u;
+                                    const uint32_t q0 = (uint32_t)(4 * (c & 1) + 2 * h);
+                                    qv[c] = lds128(rb + 16u * (q0 ^ sw));
+                                    qv2[c] = lds128(rb + 16u * ((q0 + 1u) ^ sw));
+                                }
+                            }
+                        }
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(rawEmpty(rs));  // raw tile read
@@ -667,16 +714,31 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t hw[16];
-                        if (row_ok) {
-                            q4k_half_chunk_to_half(hdr, qv[c], c, hw);
-                        } else {
+                        if (!row_ok) {
 #pragma unroll
                             for (int e = 0; e < 16; ++e) hw[e] = 0u;
+                        } else if constexpr (FMT == F_Q4_K) {
+                            q4k_half_chunk_to_half(hdr, qv[c], c, hw);
+                        } else {
+                            Raw32<FMT> ra;
+                            ra.qw[0] = qv[c].x; ra.qw[1] = qv[c].y; ra.qw[2] = qv[c].z; ra.qw[3] = qv[c].w;
+                            if constexpr (FMT == F_AFF8) {
+                                ra.qw[4] = qv2[c].x; ra.qw[5] = qv2[c].y;
+                                ra.qw[6] = qv2[c].z; ra.qw[7] = qv2[c].w;
+                            }
+                            ra.sbits = ((c < 2 ? sc4.x : sc4.y) >> (16 * (c & 1))) & 0xFFFFu;
+                            ra.bbits = ((c < 2 ? bi4.x : bi4.y) >> (16 * (c & 1))) & 0xFFFFu;
+                            to_half_words<FMT>(ra, hw);
                         }
-                        // chunk c = k-step c of the stage: weights 16h + 0..15 ->
-                        // columns 8h..8h+7, 32 + 16h + 0..15 -> 16 + 8h..
-                        tmem_st8(ta + 32u * c + 8u * h, hw);
-                        tmem_st8(ta + 32u * c + 16u + 8u * h, hw + 8);
+                        if constexpr (FMT == F_Q4_K) {
+                            // chunk c = k-step c of the stage: weights 16h + 0..15 ->
+                            // columns 8h..8h+7, 32 + 16h + 0..15 -> 16 + 8h..
+                            tmem_st8(ta + 32u * c + 8u * h, hw);
+                            tmem_st8(ta + 32u * c + 16u + 8u * h, hw + 8);
+                        } else {
+                            // k-step c, weights 32h + 0..31 -> columns 16h..
+                            tmem_st16(ta + 32u * c + 16u * h, hw);
+                        }
                     }
                     tmem_st_wait();
                     tc_fence_before();
@@ -888,7 +950,7 @@ template <int FMT, int BN, int MODE>
 static cudaError_t launch_t(const Maps &mp, const MmaAffParams &h, const DeviceInfo &dev,
                             cudaStream_t s) {
     const MmaParamsOf<FMT> p = h;
-    using C = MmaCfg<BN, FMT == F_Q4_K && MODE != 3>;
+    using C = MmaCfg<BN, kBM * raw_slice_bytes(FMT, MODE)>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     static int max_clusters = 0;
