@@ -532,6 +532,7 @@ def measure_other_workloads(torch, q, lib, r, stream, hbm_peak, tc_peak):
     out["affine4_gemv"] = affine_case("affine4_gemv")
     out["affine8_gemv"] = affine_case("affine8_gemv")
     out["affine4_prefill_512"] = affine_case("affine4_prefill", reps=20)
+    out["affine8_prefill_512"] = affine_case("affine8_prefill", reps=20)
 
     # backward with respect to the input, dx = W^T dy: the output head in 8
     # sum-axis tiles (first writes, the rest accumulate), and the Q4_K FFN shape

@@ -163,6 +163,7 @@ AFFINE_WORKLOADS = {
     "affine4_gemv": (4, 4096, 14336, 1, 10),
     "affine8_gemv": (8, 4096, 14336, 1, 11),
     "affine4_prefill": (4, 4096, 14336, 512, 12),
+    "affine8_prefill": (8, 4096, 14336, 512, 13),
 }
 
 
