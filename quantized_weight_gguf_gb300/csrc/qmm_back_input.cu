@@ -363,6 +363,9 @@ __global__ void __launch_bounds__(kBwThreads, 2) back_input_kernel(const BackPar
                 unit_axpy<FMT>(rowa, u, dys[ra - r0 + rr], st);
             }
         }
+        // the stage is refilled by a bulk copy (the async proxy) once every
+        // consumer warp has arrived: order this thread's reads of it first
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(empty(slot));
     }

@@ -164,8 +164,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     return true;
 }
 
-// Make this thread's generic-proxy shared-memory writes visible to the async
-// proxy (tensor-core operand reads, bulk copies).
+// Order this thread's generic-proxy shared-memory accesses before later
+// async-proxy ones (tensor-core operand reads, bulk and tensor copies): its
+// writes become visible to them, and its reads of a buffer that a copy will
+// refill complete first (without it a refill released by an mbarrier arrival
+// was seen to overwrite data still being read).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

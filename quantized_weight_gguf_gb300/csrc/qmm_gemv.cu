@@ -681,6 +681,9 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParamsOf<FMT, VAR> p) {
                 if (writer && has) pb[rr * PU + pslot] = acc;
             }
         }
+        // the stage is refilled by a bulk copy (the async proxy) once every
+        // consumer warp has arrived: order this thread's reads of it first
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(empty(slot));
         __syncwarp();

@@ -696,6 +696,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                             }
                         }
                     }
+                    // the raw slot is refilled by TMA (the async proxy) once every
+                    // reader has arrived: order this thread's reads of it first
+                    fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(rawEmpty(rs));  // raw tile read
                     // the stage's slot, once the MMAs that read it last are done

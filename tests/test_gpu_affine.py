@@ -164,3 +164,26 @@ def test_repeatable_bits():
     a = _run(4, w, sc, bi, x, k, n)
     b = _run(4, w, sc, bi, x, k, n)
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_tensor_core_path_repeatable_bits(bits):
+    """N = 512 on the raw-tile path, several calls into poisoned outputs: every
+    call gives the same bits (the raw-tile ring is refilled only after its
+    readers are done)."""
+    rng = np.random.default_rng(40 + bits)
+    k, n, nt = 4096, 4096, 512
+    w, sc, bi = qmm_synth.gen_affine(bits, k, n, rng)
+    x = qmm_synth.gen_x(nt, k, rng)
+    wd, scd, bid, xd = _dev(w), _dev(sc), _dev(bi), _dev(x)
+    ref = None
+    for it in range(8):
+        y = torch.full((nt, n), float(it + 1), device=DEV)
+        q.matmul_affine(FMT[bits], wd, scd, bid, xd, k, n, y=y)
+        torch.cuda.synchronize()
+        q.qmm_device_status()
+        got = y.cpu().numpy()
+        if ref is None:
+            ref = got
+        else:
+            assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), f"call {it}"
