@@ -5,7 +5,12 @@
  * The operation (rullama 0.5.0, src/backend/matmul.rs, module doc and the
  * `matmul_bf16` / `matmul_f16` / `matmul_q4_0` / `matmul_q4_k` /
  * `matmul_q6_k` dispatchers): W is n rows of k weights, row-major; row j
- * holds the k weights of output column j, packed in one of five formats.
+ * holds the k weights of output column j, packed in one of the formats
+ * below (the five GGUF formats of those dispatchers, Q8_0 and Q5_0 from the
+ * expert-matmul tests of rullama src/backend/dispatch/mod.rs, and the
+ * MLX-style affine matrices of moeflux tests/graph_diff_oracle.rs). Further
+ * entry points: the backward with respect to the input, the expert-indexed
+ * product, gated FFN pairs (SwiGLU / GeGLU) and the affine products.
  * x holds n_tokens rows of k fp32 activations (the batched tests of the same
  * page stack tokens as X[N x k] -> Y[N x n]); y[t][j] = sum_i x[t][i] *
  * w[j][i], fp32. Output-axis tiling follows `MatmulBackInputParams` in

@@ -16,6 +16,11 @@
 // sum q x = 256 * sum (0.5 + q/256) x - 128 * sum x, with sum x over each
 // unit's sub-blocks computed once per thread. Q4_0 subtracts its zero point
 // exactly instead (2^23 + q - (2^23 + 8)), so an all-zero-point block gives 0.
+//
+// Kernel variants (template VAR): the plain GEMV; expert-indexed (grid.y runs
+// one GEMV per (position, slot) on the selected expert slice); gated pairs
+// (stages alternate gate and up rows, the flush writes act(gate) * up).
+// Affine formats stage their scale and bias rows beside the codes.
 #include "qmm_device.cuh"
 #include "qmm_internal.h"
 

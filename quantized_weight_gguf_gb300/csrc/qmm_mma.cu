@@ -193,8 +193,7 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
     }
     CUtensorMap &tm = mp.x;
     CUtensorMap &tw = mp.w;
-    // raw Q4_K weight tiles: the packed rows as a 2-D byte tensor [n][row_bytes],
-    // boxes of 128 rows x one 144-byte super-block
+    // raw W tiles: the packed rows as a 2-D byte tensor [n][row_bytes]
     tw = tm;
     if (raw_slice_bytes(m.fmt, mode) > 0) {
         // raw W tiles: Q4_K boxes of 128 rows x one 144-byte super-block;

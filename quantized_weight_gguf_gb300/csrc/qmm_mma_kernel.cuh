@@ -14,7 +14,9 @@
 //               k-steps: thread (r, h) turns 32 weights of row r per k-step
 //               into fp16 and stores them in the same swizzled K-major layout
 //               the MMA descriptor describes; after the k-loop all 16 warps
-//               drain the accumulator TMEM -> registers -> y.
+//               drain the accumulator TMEM -> registers -> y;
+//   warp 18     Q4_K and affine formats: streams raw W tiles (128 rows x a
+//               256-wide k slice) by TMA ahead of the dequant warps.
 // X is converted to fp16 once per call by a small kernel that also scales each
 // token row by a power of two (exact) so it fits fp16's range; the epilogue
 // multiplies by the inverse power.
@@ -45,7 +47,7 @@
 namespace qmm {
 
 constexpr int kDeqWarps = 16;                     // two groups of 8, alternate k-steps
-constexpr int kRawWarp = 2 + kDeqWarps;             // streams raw Q4_K tiles
+constexpr int kRawWarp = 2 + kDeqWarps;             // streams raw W tiles
 constexpr int kMmaThreads = 32 * (kRawWarp + 1);
 constexpr int kBM = 128;
 constexpr int kBK = 64;
@@ -93,7 +95,7 @@ __host__ __device__ constexpr int raw_slice_bytes(int fmt, int mode) {
 // on the SM): the fp32 accumulator(s) first, then a ring of NA dequantized W
 // stages (A operand: row r on lane r, k pairs packed per column, 32 columns
 // per 64-wide k-step). Shared memory: a ring of NB x stages (streamed from
-// L2 by TMA) and, for Q4_K, kNR raw super-block tiles of 128 rows.
+// L2 by TMA) and, for the raw-tile formats, kNR raw W tiles of 128 rows.
 //
 // A stage is KA = 4 k-steps (one 256-wide super-block): each dequant thread
 // then pays one raw-tile wait, one slot wait and one arrival per two decoded
@@ -345,7 +347,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // Two groups of 8 dequant warps take alternate k-steps; an A stage (KA = 4
     // k-steps) is done when both groups have arrived.
     constexpr int kGroups = 2;
-    // Q4_K raw tiles: one group fills a whole stage; otherwise both groups
+    // raw W tiles: one group fills a whole stage; otherwise both groups
     constexpr int kFullACount = kRaw ? kDeqWarps / kGroups : kDeqWarps;
     static_assert(KA % kGroups == 0, "every group needs a k-step in every A stage");
 
@@ -562,7 +564,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             bbase += nsb(t);
         }
     } else if (warp == kRawWarp) {
-        // ------------------------------ raw Q4_K tiles via TMA ------------------------------
+        // ------------------------- raw W tiles (Q4_K, affine codes) via TMA -------------------------
         // its own warp, so that the raw ring runs as far ahead of the dequant
         // warps as it is deep (into the next tile), whatever the x ring does
         if (kRaw && lane == 0) {
