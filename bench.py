@@ -625,6 +625,8 @@ def run_case(args):
         base = name
     if name.endswith("_backward_input"):
         return run_case_backward(args, torch, q, lib, r, name[:-len("_backward_input")])
+    if name in qmm_synth.AFFINE_WORKLOADS:
+        return run_case_affine(args, torch, q, lib, r, name)
     fmt, k, n, w, x = qmm_synth.workload(base, n_tokens=nt)
     ncop = 1 if args.no_rotate else r.copies_for(w.size)
     wc = r.weights(w, ncop)
@@ -648,6 +650,40 @@ def run_case(args):
     q.qmm_device_status(stream)
     print(json.dumps({"case": name, "overlap": not args.no_overlap, "us_per_call": dt * 1e6, "weight_gbs": w.size / dt / 1e9,
                       "tflops": 2.0 * x.shape[0] * k * n / dt / 1e12, "copies": ncop,
+                      "clocks": clk.summary()}), flush=True)
+    return 0
+
+
+def run_case_affine(args, torch, q, lib, r, name):
+    """An affine workload alone (codes + bf16 scales and biases)."""
+    import ctypes
+    bits, k, n, w, sc, bi, x = qmm_synth.affine_workload(name)
+    dev = r.dev
+    nt = x.shape[0]
+    total = w.size + sc.nbytes + bi.nbytes
+    ncop = 1 if args.no_rotate else r.copies_for(total)
+    wc = r.weights(w, ncop)
+    sc_c = r.weights(sc.view(np.int16), ncop)
+    bi_c = r.weights(bi.view(np.int16), ncop)
+    xd = torch.from_numpy(x).to(dev)
+    yd = torch.empty((nt, n), device=dev)
+    fl = (q.FLAG_OVERLAP_PREV | q.FLAG_X_READY) if nt == 1 and not args.no_overlap else 0
+    a0 = q.make_args(f"affine{bits}", wc[0], xd, yd, k, n, nt, stream=r.stream, flags=fl)
+    need = q.qmm_workspace_bytes(a0)
+    wsb = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    al = [q.make_args(f"affine{bits}", wc[c], xd, yd, k, n, nt, stream=r.stream, flags=fl,
+                      workspace=wsb if need else None, workspace_bytes=need) for c in range(ncop)]
+    refs = [(ctypes.byref(al[c]), ctypes.c_void_p(sc_c[c].data_ptr()),
+             ctypes.c_void_p(bi_c[c].data_ptr())) for c in range(ncop)]
+
+    def launch(c):
+        if lib.qmm_matmul_affine(*refs[c]):
+            raise RuntimeError(q.qmm_last_error())
+    with ClockSampler(0) as clk:
+        dt = time_loop(torch, launch, args.steps, args.warmup, ncop, r.stream)
+    q.qmm_device_status(r.stream)
+    print(json.dumps({"case": name, "us_per_call": dt * 1e6, "weight_gbs": total / dt / 1e9,
+                      "tflops": 2.0 * nt * k * n / dt / 1e12, "copies": ncop,
                       "clocks": clk.summary()}), flush=True)
     return 0
 
