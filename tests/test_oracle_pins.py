@@ -749,3 +749,63 @@ def test_glu_product_composes_the_plain_products(name):
     # swapping gate and up changes the result (the gate is the activated one)
     y2, _ = oracle.matmul_glu(name, fmt, wu, wg, x, k, n)
     assert not np.allclose(y, y2)
+
+
+# ------------------------------------- a second, per-element decoder ----
+
+def _f16(lo, hi):
+    return np.array([lo | (hi << 8)], np.uint16).view(np.float16).astype(np.float64)[0]
+
+
+def _element_decoder(fmt, blk, e):
+    """Weight e of one block, from an index formula per element (written
+    independently of the oracle's block loops); f64, rounded to f32 once."""
+    b = [int(v) for v in blk]
+    if fmt == "q4_0":
+        q = (b[2 + e % 16] >> (4 * (e // 16))) & 15
+        return np.float32((q - 8) * _f16(b[0], b[1]))
+    if fmt == "q8_0":
+        q = b[2 + e] - 256 * (b[2 + e] >= 128)
+        return np.float32(q * _f16(b[0], b[1]))
+    if fmt == "q5_0":
+        qh = b[2] | (b[3] << 8) | (b[4] << 16) | (b[5] << 24)
+        q = ((b[6 + e % 16] >> (4 * (e // 16))) & 15) | (((qh >> e) & 1) << 4)
+        return np.float32((q - 16) * _f16(b[0], b[1]))
+    if fmt == "q4_k":
+        s = e // 32
+        sc_b = b[4:16]
+        if s < 4:
+            sc, m = sc_b[s] & 63, sc_b[s + 4] & 63
+        else:
+            sc = (sc_b[s + 4] & 15) | ((sc_b[s - 4] >> 6) << 4)
+            m = (sc_b[s + 4] >> 4) | ((sc_b[s] >> 6) << 4)
+        q = (b[16 + 32 * (e // 64) + e % 32] >> (4 * (s % 2))) & 15
+        return np.float32(_f16(b[0], b[1]) * sc * q - _f16(b[2], b[3]) * m)
+    if fmt == "q6_k":
+        h, rem = e // 128, e % 128
+        r, l = rem // 32, rem % 32
+        lo = b[64 * h + l + 32 * (r % 2)]
+        lo = (lo >> 4) if r >= 2 else (lo & 15)
+        hi = (b[128 + 32 * h + l] >> (2 * r)) & 3
+        q = lo | (hi << 4)
+        sc = b[192 + e // 16] - 256 * (b[192 + e // 16] >= 128)
+        return np.float32(_f16(b[208], b[209]) * sc * (q - 32))
+    raise ValueError(fmt)
+
+
+@pytest.mark.parametrize("fmt,elems,nbytes", [("q4_0", 32, 18), ("q8_0", 32, 34), ("q5_0", 32, 22),
+                                              ("q4_k", 256, 144), ("q6_k", 256, 210)])
+def test_per_element_decoder_agrees_bit_for_bit(fmt, elems, nbytes):
+    """Random blocks (every byte uniform: NaN, Inf and subnormal scales
+    included): the oracle's block decoder and the per-element index formula
+    give the same bits for every weight."""
+    rng = np.random.default_rng(elems + nbytes)
+    nblk = 24
+    w = rng.integers(0, 256, size=nblk * nbytes, dtype=np.uint8)
+    got = oracle.dequant(fmt, w, elems * nblk, 1)[0]
+    with np.errstate(invalid="ignore", over="ignore"):   # Inf * 0 scales give NaN on both sides
+        want = np.array([_element_decoder(fmt, w[nbytes * (i // elems):nbytes * (i // elems + 1)],
+                                          i % elems) for i in range(elems * nblk)], np.float32)
+    na, nb = np.isnan(got), np.isnan(want)
+    assert np.array_equal(na, nb)
+    assert np.array_equal(got.view(np.uint32)[~na], want.view(np.uint32)[~na])
