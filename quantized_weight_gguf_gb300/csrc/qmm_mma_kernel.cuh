@@ -654,6 +654,18 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 for (int b = (g - rbase) & 1; b < NSBLK && !failed; b += 2) {
                     const int rc = rbase + b;
                     const int rs = rc % kNR;
+                    // affine: the row's four scales and biases of this slice come
+                    // from global memory; their loads overlap the raw-tile wait
+                    uint2 sc4 = make_uint2(0u, 0u), bi4 = make_uint2(0u, 0u);
+                    if constexpr (FMT != F_Q4_K) {
+                        if (row_ok) {
+                            // the unit's super-block b is k-step t.k_lo + 4 b (before rotation)
+                            const int64_t ao = (t.m0 + r) * p.aux_row_bytes +
+                                               8 * (kx(t, t.k_lo + 4 * b) >> 2);
+                            sc4 = __ldg(reinterpret_cast<const uint2 *>(p.sc + ao));
+                            bi4 = __ldg(reinterpret_cast<const uint2 *>(p.bi + ao));
+                        }
+                    }
                     const bool ok = wait_abortable(rawFull(rs), (rc / kNR) & 1, abort_flag);
                     if (__all_sync(0xFFFFFFFFu, ok) == 0) {
                         record_error(p.err, DERR_MMA_A);
@@ -664,9 +676,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                     // Q4_K: the super-block header and this half of each chunk;
                     // affine: this half of each k-step's codes (128-byte swizzled
                     // rows: 16-byte chunk q of row r sits at chunk q ^ (r & 7) of
-                    // its 128-byte line) and the row's four scales and biases
+                    // its 128-byte line)
                     uint4 hdr = make_uint4(0u, 0u, 0u, 0u), qv[4], qv2[4];
-                    uint2 sc4 = make_uint2(0u, 0u), bi4 = make_uint2(0u, 0u);
                     if constexpr (FMT == F_Q4_K) {
                         const uint32_t rb = W0 + rs * kRawB + (uint32_t)r * 144u;
                         if (row_ok) {
@@ -677,11 +688,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                     } else {
                         const uint32_t sw = (uint32_t)(r & 7);
                         if (row_ok) {
-                            // the unit's super-block b is k-step t.k_lo + 4 b (before rotation)
-                            const int64_t ao = (t.m0 + r) * p.aux_row_bytes +
-                                               8 * (kx(t, t.k_lo + 4 * b) >> 2);
-                            sc4 = __ldg(reinterpret_cast<const uint2 *>(p.sc + ao));
-                            bi4 = __ldg(reinterpret_cast<const uint2 *>(p.bi + ao));
 #pragma unroll
                             for (int c = 0; c < 4; ++c) {
                                 if (FMT == F_AFF4) {
