@@ -5,7 +5,9 @@ Argument marshalling only: every step of the product runs in the CUDA
 kernels of ``libqmm.so``. PyTorch supplies device memory and streams. The
 functions carry the C names (``qmm_matmul``, ``qmm_matmul_ex``,
 ``qmm_dequant`` ...) and take plain integers / device pointers or torch
-tensors; ``matmul`` and ``dequant`` are tensor-level conveniences over them.
+tensors; ``matmul``, ``dequant``, ``matmul_backward_input``,
+``matmul_experts``, ``matmul_affine``, ``dequant_affine`` and ``matmul_glu``
+are tensor-level conveniences over them.
 If ``libqmm.so`` has not been built, every call raises: there is no fallback.
 """
 from __future__ import annotations
