@@ -546,7 +546,9 @@ def measure_other_workloads(torch, q, lib, r, stream, hbm_peak, tc_peak):
         dxd = torch.empty(k, device=dev)
         tile = n // tiles
         al = [[q.make_args(fmt, wc[c], dyd, dxd, k, n, 1, j_start=t * tile, j_end=(t + 1) * tile,
-                           accumulate=t > 0, stream=stream) for t in range(tiles)] for c in range(ncop)]
+                           accumulate=t > 0, stream=stream,
+                           flags=q.FLAG_OVERLAP_PREV | q.FLAG_X_READY)
+               for t in range(tiles)] for c in range(ncop)]
         need = max(q.qmm_backward_input_workspace_bytes(a) for a in al[0])
         wsb = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
         for row in al:
@@ -698,7 +700,9 @@ def run_case_backward(args, torch, q, lib, r, base):
     wc = r.weights(w, ncop)
     dyd = torch.from_numpy(np.random.default_rng(4).standard_normal(n).astype(np.float32)).to(dev)
     dxd = torch.empty(k, device=dev)
-    al = [q.make_args(fmt, wc[c], dyd, dxd, k, n, 1, stream=stream) for c in range(ncop)]
+    flags = 0 if args.no_overlap else (q.FLAG_OVERLAP_PREV | q.FLAG_X_READY)
+    al = [q.make_args(fmt, wc[c], dyd, dxd, k, n, 1, stream=stream, flags=flags)
+          for c in range(ncop)]
     need = q.qmm_backward_input_workspace_bytes(al[0])
     wsb = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     for a in al:

@@ -183,8 +183,12 @@ int qmm_matmul_host(const qmm_args *a, void *dev_w, float *dev_x, float *dev_y);
  * (accumulate = 1); j_start == j_end == 0 means all n rows, and an empty
  * range writes zeros (or leaves dx when accumulating). Fields: a->x is dy
  * (device, n floats), a->y is dx (device, k floats), a->n_tokens must be 1,
- * a->path and a->flags must be 0; fmt, w, w_len, k, n, workspace, stream as
- * for qmm_matmul_ex. Units of k are 32 weights (8 for 16-bit formats) and at
+ * a->path is ignored; fmt, w, w_len, k, n, workspace, stream as for
+ * qmm_matmul_ex. a->flags as for qmm_matmul_ex with dy in the role of x:
+ * under QMM_FLAG_OVERLAP_PREV the partial-sum kernel starts streaming W
+ * while the preceding kernel finishes, reads dy after it (unless
+ * QMM_FLAG_X_READY) and always writes its partials after it. Within a call
+ * the summing kernel is always launched as a programmatic dependent. Units of k are 32 weights (8 for 16-bit formats) and at
  * most 256 per row: k <= 8192 for the block formats, k <= 2048 for BF16/F16
  * (QMM_ERR_UNSUPPORTED beyond). The result is the same on every call (the
  * per-CTA partial sums are added in a fixed order). Stream-ordered, no

@@ -239,7 +239,7 @@ def matmul(fmt, w, x, k: int, n: int, *, y=None, j_start=0, j_end=0, accumulate=
 
 
 def matmul_backward_input(fmt, w, dy, k: int, n: int, *, dx=None, j_start=0, j_end=0,
-                          accumulate=False, stream=None):
+                          accumulate=False, stream=None, flags=0):
     """dx = W^T dy over the rows [j_start, j_end) for torch CUDA tensors: w
     uint8 packed bytes, dy float32 [n]. Returns dx float32 [k] (the given dx
     when passed). Scratch is the library's own buffer."""
@@ -247,7 +247,7 @@ def matmul_backward_input(fmt, w, dy, k: int, n: int, *, dx=None, j_start=0, j_e
     if dx is None:
         dx = torch.empty(k, dtype=torch.float32, device=dy.device)
     a = make_args(fmt, w, dy, dx, k, n, 1, w_len=w.numel() * w.element_size(), j_start=j_start,
-                  j_end=j_end, accumulate=accumulate, stream=stream)
+                  j_end=j_end, accumulate=accumulate, stream=stream, flags=flags)
     qmm_matmul_backward_input(a)
     return dx
 

@@ -354,7 +354,6 @@ int qmm_matmul_backward_input(const qmm_args *a) {
     if (a->n_tokens != 1)
         return fail(QMM_ERR_SHAPE, "backward-input takes one dy vector (n_tokens %lld != 1)",
                     (long long)a->n_tokens);
-    if (a->flags != 0) return fail(QMM_ERR_SHAPE, "backward-input takes no flags");
     if (affine_fmt(a->fmt))
         return fail(QMM_ERR_FORMAT, "backward-input takes single-stream (GGUF) formats");
     int64_t j0, j1, rb;
@@ -398,6 +397,8 @@ int qmm_matmul_backward_input(const qmm_args *a) {
     b.j0 = j0; b.j1 = j1;
     b.accumulate = a->accumulate;
     b.workspace = ws;
+    b.overlap_prev = (a->flags & QMM_FLAG_OVERLAP_PREV) != 0;
+    b.x_ready = b.overlap_prev && (a->flags & QMM_FLAG_X_READY) != 0;
     cudaError_t e = qmm::launch_back_input(b, *dev, s);
     return e == cudaSuccess ? QMM_OK : cuda_fail(e, "backward-input launch");
 }

@@ -43,6 +43,7 @@ struct BackParams {
     int SB;   // bytes per stage buffer (multiple of 128)
     int NS;   // stage buffers
     int dy_cap;  // rows of dy staged (>= rows per CTA)
+    int x_ready; // dy may be read before the preceding kernel completes
     unsigned int *err;
 };
 
@@ -298,6 +299,8 @@ __global__ void __launch_bounds__(kBwThreads, 2) back_input_kernel(const BackPar
         fence_barrier_init();
     }
     __syncthreads();
+    // the sum kernel that follows may start launching; it waits for this grid
+    pdl_launch_dependents();
 
     if (warp == kBwWarps) {
         // ---------------- producer: one lane streams the weight bytes ----------------
@@ -333,6 +336,10 @@ __global__ void __launch_bounds__(kBwThreads, 2) back_input_kernel(const BackPar
     }
 
     // ---------------- consumers ----------------
+    // Under programmatic launch the weight stream starts while the preceding
+    // kernel finishes; dy is read after it unless the caller vouched that it
+    // does not write dy.
+    if (!p.x_ready) pdl_wait_prev();
     for (int64_t i = tid; i < nrows; i += kBwCons) dys[i] = __ldg(p.dy + r0 + i);
     named_barrier(1, kBwCons);
     const int U = p.U, G = p.G;
@@ -387,6 +394,8 @@ __global__ void __launch_bounds__(kBwThreads, 2) back_input_kernel(const BackPar
         }
     }
     named_barrier(1, kBwCons);
+    // the partials' workspace may still be read by the preceding call's sum
+    pdl_wait_prev();
     float *out = p.part + (int64_t)cta * k;
     for (int64_t i = tid; i < k; i += kBwCons) {
         float v = 0.0f;
@@ -402,6 +411,10 @@ __global__ void __launch_bounds__(256) back_input_sum_kernel(const float *__rest
                                                              int parts, int64_t k, float *dx,
                                                              int accumulate) {
     __shared__ float ws[8][33];
+    // launched as a programmatic dependent of the partials' kernel: wait for
+    // it before reading; a following call's kernels may start streaming now
+    pdl_wait_prev();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t i = (int64_t)blockIdx.x * 32 + lane;
     float v = 0.0f;
@@ -429,7 +442,7 @@ __global__ void __launch_bounds__(256) back_input_sum_kernel(const float *__rest
 }
 
 template <int FMT>
-cudaError_t launch_bw_t(const BackParams &p, int grid, size_t smem, cudaStream_t s) {
+cudaError_t launch_bw_t(const BackParams &p, int grid, size_t smem, cudaStream_t s, bool overlap) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
@@ -437,8 +450,21 @@ cudaError_t launch_bw_t(const BackParams &p, int grid, size_t smem, cudaStream_t
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    back_input_kernel<FMT><<<grid, kBwThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    if (!overlap) {
+        back_input_kernel<FMT><<<grid, kBwThreads, smem, s>>>(p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kBwThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, back_input_kernel<FMT>, p);
 }
 
 int unit_k_of(int fmt) { return (fmt == F_BF16 || fmt == F_F16) ? 8 : 32; }
@@ -517,22 +543,36 @@ cudaError_t launch_back_input(const BackLaunch &b, const DeviceInfo &dev, cudaSt
     p.SB = SB;
     p.NS = NS;
     p.dy_cap = dy_cap;
+    p.x_ready = b.x_ready ? 1 : 0;
     p.err = dev.err;
     cudaError_t e;
     switch (b.fmt) {
-    case F_BF16: e = launch_bw_t<F_BF16>(p, grid, smem, s); break;
-    case F_F16: e = launch_bw_t<F_F16>(p, grid, smem, s); break;
-    case F_Q4_0: e = launch_bw_t<F_Q4_0>(p, grid, smem, s); break;
-    case F_Q4_K: e = launch_bw_t<F_Q4_K>(p, grid, smem, s); break;
-    case F_Q6_K: e = launch_bw_t<F_Q6_K>(p, grid, smem, s); break;
-    case F_Q8_0: e = launch_bw_t<F_Q8_0>(p, grid, smem, s); break;
-    case F_Q5_0: e = launch_bw_t<F_Q5_0>(p, grid, smem, s); break;
+    case F_BF16: e = launch_bw_t<F_BF16>(p, grid, smem, s, b.overlap_prev); break;
+    case F_F16: e = launch_bw_t<F_F16>(p, grid, smem, s, b.overlap_prev); break;
+    case F_Q4_0: e = launch_bw_t<F_Q4_0>(p, grid, smem, s, b.overlap_prev); break;
+    case F_Q4_K: e = launch_bw_t<F_Q4_K>(p, grid, smem, s, b.overlap_prev); break;
+    case F_Q6_K: e = launch_bw_t<F_Q6_K>(p, grid, smem, s, b.overlap_prev); break;
+    case F_Q8_0: e = launch_bw_t<F_Q8_0>(p, grid, smem, s, b.overlap_prev); break;
+    case F_Q5_0: e = launch_bw_t<F_Q5_0>(p, grid, smem, s, b.overlap_prev); break;
     default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
-    back_input_sum_kernel<<<(unsigned)((b.k + 31) / 32), 256, 0, s>>>(p.part, grid, b.k, b.dx,
-                                                                      b.accumulate);
-    return cudaGetLastError();
+    // the sum: a programmatic dependent of the partials' kernel (it waits for it)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((b.k + 31) / 32));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const float *part = p.part;
+    const int parts = grid;
+    const int64_t kk = b.k;
+    float *dx = b.dx;
+    const int acc = b.accumulate;
+    return cudaLaunchKernelEx(&cfg, back_input_sum_kernel, part, parts, kk, dx, acc);
 }
 
 }  // namespace qmm

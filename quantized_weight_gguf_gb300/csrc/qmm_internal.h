@@ -70,6 +70,8 @@ struct BackLaunch {
     int64_t j0, j1;         // rows of the sum axis
     int accumulate;
     void *workspace;        // >= back_input_workspace_bytes(...): per-CTA partials
+    bool overlap_prev = false;  // programmatic launch (W is not written by the previous kernel)
+    bool x_ready = false;       // dy is not written by the previous kernel either
 };
 bool back_input_supports(int fmt, int64_t k);
 size_t back_input_workspace_bytes(int fmt, int64_t k, int64_t n, int64_t j0, int64_t j1,

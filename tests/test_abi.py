@@ -144,7 +144,7 @@ def test_empty_work_needs_no_device(lib):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(n_tokens=2), 2),                 # one dy vector only
-    (dict(flags=q.FLAG_OVERLAP_PREV), 2),  # no launch flags
+    (dict(flags=8), 2),                    # unknown flag
     (dict(k=300), 2),
     (dict(fmt=9), 1),
     (dict(w_len=10), 3),

@@ -143,3 +143,31 @@ def test_back_input_q6_k_head_tiles_full_size():
     q.qmm_device_status()
     ref, s = oracle.matmul_back_input(fmt, w, dy, k, n)
     _assert(dx.cpu().numpy(), ref, s, "head, 8 tiles")
+
+
+def test_back_input_overlapped_tiles():
+    """Sum-axis tiles under programmatic launch: with OVERLAP_PREV | X_READY
+    (dy not written by the preceding kernels) and with OVERLAP_PREV alone
+    after a kernel that rewrites dy, the result matches the whole-range
+    oracle."""
+    fmt, k, n = "q4_k", 4096, 14336
+    rng = np.random.default_rng(8)
+    w = qmm_synth.gen_weights(fmt, k, n, rng)
+    dy = rng.standard_normal(n).astype(np.float32)
+    ref, s = oracle.matmul_back_input(fmt, w, dy, k, n)
+    wd, dyd = _dev(w), _dev(dy)
+    tiles = [(0, 3000), (3000, 3001), (3001, 9000), (9000, n)]
+    for flags in (q.FLAG_OVERLAP_PREV | q.FLAG_X_READY, q.FLAG_OVERLAP_PREV):
+        dx = torch.full((k,), 5.0, device=DEV)
+        src = torch.zeros(n, device=DEV)
+        for t, (a, b) in enumerate(tiles):
+            if flags == q.FLAG_OVERLAP_PREV:
+                src.copy_(dyd)          # the preceding kernel writes dy
+                dyt = src
+            else:
+                dyt = dyd
+            q.matmul_backward_input(fmt, wd, dyt, k, n, dx=dx, j_start=a, j_end=b,
+                                    accumulate=t > 0, flags=flags)
+        torch.cuda.synchronize()
+        q.qmm_device_status()
+        _assert(dx.cpu().numpy(), ref, s, f"overlapped tiles flags={flags}")
