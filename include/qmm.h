@@ -260,6 +260,13 @@ int qmm_matmul_affine(const qmm_args *a, const void *scales, const void *biases)
 int qmm_dequant_affine(int fmt, const void *w, const void *scales, const void *biases, int64_t k,
                        int64_t n, float *out, void *stream);
 
+/* Health check of the device-side bounded waits: enqueues one small kernel
+ * that waits on a barrier nothing satisfies; after about 50 ms the wait
+ * gives up and the kernel records the fault and returns (no GPU fault, no
+ * hang). The next qmm_device_status(stream) must then report
+ * QMM_ERR_DEVICE_TIMEOUT (and clear it); the context stays usable. */
+int qmm_check_bounded_wait(void *stream);
+
 /* Synchronizes `stream`, then reports whether any kernel enqueued so far
  * timed out on a pipeline barrier (QMM_ERR_DEVICE_TIMEOUT) or met an expert
  * id out of range (QMM_ERR_BAD_ID), and clears the flag; QMM_OK otherwise,

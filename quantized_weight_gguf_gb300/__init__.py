@@ -32,7 +32,7 @@ EXPORTS = ("qmm_weight_bytes", "qmm_matmul", "qmm_set_stream", "qmm_matmul_ex",
            "qmm_device_status", "qmm_last_error", "qmm_version", "qmm_matmul_noalloc",
            "qmm_matmul_backward_input", "qmm_backward_input_workspace_bytes",
            "qmm_matmul_experts", "qmm_matmul_affine", "qmm_dequant_affine", "qmm_matmul_glu",
-           "qmm_glu_workspace_bytes")
+           "qmm_glu_workspace_bytes", "qmm_check_bounded_wait")
 
 
 class QmmError(RuntimeError):
@@ -83,6 +83,7 @@ def load(path: str = LIB_PATH):
         "qmm_matmul_affine": (i, [pa, vp, vp]),
         "qmm_matmul_glu": (i, [pa, vp, i]),
         "qmm_glu_workspace_bytes": (sz, [pa]),
+        "qmm_check_bounded_wait": (i, [vp]),
         "qmm_dequant_affine": (i, [i, vp, vp, vp, i64, i64, vp, vp]),
     }
     for name, (res, args) in sig.items():
@@ -199,6 +200,10 @@ def qmm_matmul_host(args: qmm_args, dev_w, dev_x, dev_y) -> int:
 
 def qmm_dequant(fmt, w, k: int, n: int, out, stream=None) -> int:
     return _check(load().qmm_dequant(_fmt(fmt), _ptr(w), k, n, _ptr(out), _stream(stream)))
+
+
+def qmm_check_bounded_wait(stream=None) -> int:
+    return _check(load().qmm_check_bounded_wait(_stream(stream)))
 
 
 def qmm_device_status(stream=None) -> int:

@@ -605,6 +605,16 @@ int qmm_dequant_affine(int fmt, const void *w, const void *scales, const void *b
     return e == cudaSuccess ? QMM_OK : cuda_fail(e, "dequant launch");
 }
 
+int qmm_check_bounded_wait(void *stream) {
+    t_err[0] = 0;
+    qmm::DeviceInfo *dev = nullptr;
+    int st = device_info(&dev);
+    if (st != QMM_OK) return st;
+    cudaError_t e = qmm::launch_bounded_wait_probe(dev->err, 50000000ull /* 50 ms */,
+                                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QMM_OK : cuda_fail(e, "bounded-wait check launch");
+}
+
 int qmm_device_status(void *stream) {
     t_err[0] = 0;
     qmm::DeviceInfo *dev = nullptr;

@@ -86,6 +86,26 @@ cudaError_t launch_zero_cols(float *y, int64_t n_tokens, int64_t n, int64_t j0, 
     return cudaGetLastError();
 }
 
+// Check of the bounded waits every pipeline relies on: one thread waits on an
+// mbarrier that nothing ever arrives on. The wait gives up after limit_ns,
+// the kernel records DERR_WAIT_PROBE and returns: no fault and no hang, and
+// the context stays usable.
+__global__ void bounded_wait_probe_kernel(unsigned int *err, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_addr(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(b, 0, limit_ns)) record_error(err, DERR_WAIT_PROBE);
+}
+
+cudaError_t launch_bounded_wait_probe(unsigned int *err, uint64_t limit_ns, cudaStream_t s) {
+    bounded_wait_probe_kernel<<<1, 32, 0, s>>>(err, limit_ns);
+    return cudaGetLastError();
+}
+
 // y[t][j] (+)= act(g[t][j]) * u[t][j] for j in [j0, j1) (row stride n).
 template <int ACT>
 __global__ void glu_combine_kernel(const float *__restrict__ gt, const float *__restrict__ up,

@@ -28,7 +28,8 @@ enum DevErr : unsigned int {
     DERR_MMA_EMPTY = 5,    // a producer gave up waiting for a free stage
     DERR_MMA_ACC = 6,      // epilogue gave up waiting for the accumulator
     DERR_TEARDOWN = 7,     // copies still in flight at exit after a fault
-    DERR_BAD_ID = 8        // an expert id outside [0, n_experts)
+    DERR_BAD_ID = 8,       // an expert id outside [0, n_experts)
+    DERR_WAIT_PROBE = 9    // the bounded-wait check gave up, as it must
 };
 
 // Block geometry (elements per block, bytes per block) of each format.
@@ -154,12 +155,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Wait for the phase with parity `parity` to complete; false after ~2 s.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for the phase with parity `parity` to complete; false after
+// `limit_ns` (2 s unless a caller asks otherwise).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
     return true;
 }

@@ -93,6 +93,9 @@ cudaError_t launch_zero_cols(float *y, int64_t n_tokens, int64_t n, int64_t j0, 
 cudaError_t launch_glu_combine(const float *g, const float *u, float *y, int64_t n_tokens,
                                int64_t n, int64_t j0, int64_t j1, int act, int accumulate,
                                cudaStream_t s);
+// One block waiting on a barrier nothing satisfies; it gives up after
+// limit_ns and records an error in *err (see qmm_check_bounded_wait).
+cudaError_t launch_bounded_wait_probe(unsigned int *err, uint64_t limit_ns, cudaStream_t s);
 // Record a status and message for qmm_last_error() on this host thread; returns status.
 int set_error(int status, const char *fmt, ...);
 
