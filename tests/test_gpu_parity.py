@@ -361,3 +361,29 @@ def test_north_star_signature_and_host_variant():
     torch.cuda.synchronize()
     assert_parity(yh.numpy(), y_ref, s_ref, "qmm_matmul_host")
     assert lib is q.load()
+
+
+@pytest.mark.parametrize("fmt,k,n,nt", [("q4_k", 256, 384, 2048), ("q8_0", 512, 200, 1500),
+                                        ("bf16", 256, 130, 777)])
+def test_mma_many_token_tiles(fmt, k, n, nt):
+    """Many token tiles (up to 8 of 256) over few row pairs, ragged rows and
+    tokens: the persistent schedule walks several rounds."""
+    rng = np.random.default_rng(nt + n)
+    w = qmm_synth.gen_weights(fmt, k, n, rng)
+    x = qmm_synth.gen_x(nt, k, rng)
+    y = run(fmt, w, x, k, n, path=q.PATH_MMA)
+    y_ref, s_ref = oracle.matmul(fmt, w, x, k, n)
+    assert_parity(y, y_ref, s_ref, f"mma {fmt} k={k} n={n} N={nt}")
+
+
+@pytest.mark.parametrize("fmt,k", [("bf16", 16384), ("f16", 16384), ("q4_0", 16384),
+                                   ("q8_0", 16384), ("q5_0", 16384)])
+def test_gemv_largest_k(fmt, k):
+    """The largest k the one-token kernel takes for each unit width."""
+    rng = np.random.default_rng(k // 7)
+    n = 96
+    w = qmm_synth.gen_weights(fmt, k, n, rng)
+    x = qmm_synth.gen_x(1, k, rng)
+    y = run(fmt, w, x, k, n, path=q.PATH_GEMV)
+    y_ref, s_ref = oracle.matmul(fmt, w, x, k, n)
+    assert_parity(y, y_ref, s_ref, f"gemv {fmt} k={k}")
