@@ -149,7 +149,11 @@ void qmm_set_stream(void *stream);
 
 /* Full form: column tile, accumulate, path, workspace and stream.
  * k == 0 writes zeros to the tile's columns (or leaves them when
- * accumulating); n == 0 or an empty tile enqueues nothing. */
+ * accumulating); n == 0 or an empty tile enqueues nothing.
+ * Scratch: with a->workspace NULL the tensor-core path uses one grow-only
+ * buffer per device owned by the library (growing it synchronizes the
+ * device once); calls that may run concurrently on different streams, or
+ * that are captured into a CUDA graph, pass their own workspace. */
 int qmm_matmul_ex(const qmm_args *a);
 
 /* Device scratch bytes qmm_matmul_ex needs for *a (0 for the GEMV path).
