@@ -218,6 +218,26 @@ def _oracle_share(job):
     return done, time.perf_counter() - t0
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
 def cpu_baseline(seconds: float = 10.0):
     """The oracle as it stands on the host: single-threaded, and row-partitioned
     over every core (one spawned process per core; spawn, since the CUDA
@@ -246,6 +266,7 @@ def cpu_baseline(seconds: float = 10.0):
                 "sample": f"oracle (plain C, f64 sums) on the bf16+f16 4096x4096 GEMVs, rows split "
                           f"over {cores} processes, repeated for {wall:.1f} s "
                           f"({total / 1e6:.0f} MB of weights)",
+                "cpu_model": cpu_model(),
                 "single_core": single}
     except Exception as e:  # a pool that cannot start: report the single-core figure
         single.update({"kind": "oracle", "note": f"all-core run unavailable: {e}"})
@@ -463,7 +484,8 @@ def measure_other_workloads(torch, q, lib, r, stream, hbm_peak, tc_peak):
                 "weight_bytes": int(w.size), "launches_per_call": tiles}
 
     out["q4_0_gemv"] = gemv_case("q4_0_gemv", reps=200)
-    out["q4_0_gemv"]["note"] = "73,728 weight bytes: launch-latency bound; fraction not meaningful"
+    out["q4_0_gemv"]["note"] = ("73,728 weight bytes: every rotated copy fits in L2, so this is the "
+                                "L2-resident figure; launch-latency bound, fraction not meaningful")
     out["q4_k_gemv"] = gemv_case("q4_k_gemv")
     out["q6_k_head_8_tiles"] = gemv_case("q6_k_head", tiles=8, reps=20)
     out["q6_k_head_untiled"] = gemv_case("q6_k_head", tiles=1, reps=20)
