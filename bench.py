@@ -7,13 +7,16 @@ GB/s = weight bytes / time (x and y bytes excluded). Inputs are resident in
 HBM; every step reads a different one of several distinct weight copies whose
 total is > 3x the L2 size, so each step streams W from HBM.
 
-The JSON line also carries the other workloads of the path measured the same
-way (Q4_0 / Q4_K / Q6_K GEMV, and the Q4_K N-token product in TFLOP/s at
-N = 1, 8, 64, 512 on both paths), the roofline of the dominant kernel against
-the measured HBM copy bandwidth, an end-to-end figure through the host-buffer
-C entry point (qmm_matmul_host: W and x copied in, y copied out, every step),
-SM clocks sampled during the timed region, and the oracle timed on the host
-as a CPU baseline.
+The JSON line also carries the other workloads measured the same way
+(Q4_0 / Q4_K / Q6_K / Q8_0 / Q5_0 GEMVs, the expert-indexed products, the
+gated pairs, the affine GEMVs and N = 512 products, the backward-input cases,
+and the Q4_K N-token product in TFLOP/s at N = 1, 8, 64, 512 on both paths),
+the roofline of the dominant kernel against the measured HBM copy bandwidth,
+an end-to-end figure through the host-buffer C entry point (qmm_matmul_host:
+W and x copied in, y copied out, every step), SM clocks sampled during the
+timed region, and the oracle timed on the host's cores as a CPU baseline.
+
+--case <workload> times one workload alone (for profiling one kernel).
 
 --impl reference times the oracle (plain C, one host core) on the same
 workload: each step is the full oracle product of both weight matrices.
