@@ -256,8 +256,11 @@ def check(y: np.ndarray, y_ref: np.ndarray, s_ref: np.ndarray, tol: float = TOL_
     finite = ~np.isnan(y_ref)
     bad = (err > bound) & finite
     bad |= nan_mismatch
+    # err / S, with S raised to the absolute floor's equivalent (atol / tol) so
+    # that the worst ratio is comparable with tol whichever bound applies
+    s_eff = np.maximum(s_ref, atol / tol) if atol > 0 else s_ref
     with np.errstate(divide="ignore", invalid="ignore"):
-        ratio = np.where(s_ref > 0, err / np.where(s_ref > 0, s_ref, 1.0), np.where(err > 0, np.inf, 0.0))
+        ratio = np.where(s_eff > 0, err / np.where(s_eff > 0, s_eff, 1.0), np.where(err > 0, np.inf, 0.0))
     worst = float(np.nanmax(ratio[finite])) if finite.any() else 0.0
     cos = cosine(np.where(finite, y, 0.0), np.where(finite, y_ref, 0.0))
     ok = (not bad.any()) and cos >= COSINE_FLOOR
