@@ -528,6 +528,42 @@ def measure_other_workloads(torch, q, lib, r, stream, hbm_peak, tc_peak):
         out[f"{name}_pos1"] = expert_case(name, 1)
         out[f"{name}_pos4"] = expert_case(name, 4)
 
+    exa = lib.qmm_matmul_experts_affine
+
+    def expert_affine_case(bits, n_pos, reps=50):
+        # affine experts of the same shape: k=2048, n=768, 64 experts, top 8
+        k, n, n_exp, top_k = 2048, 768, 64, 8
+        rng = np.random.default_rng(20 + bits)
+        w, sc, bi = qmm_synth.gen_affine(bits, k, n * n_exp, rng)
+        x = qmm_synth.gen_x(n_pos, k, rng)
+        ids = qmm_synth.gen_ids(n_pos, top_k, n_exp, rng)
+        slice_bytes = (w.size + sc.nbytes + bi.nbytes) // n_exp
+        pairs = ids.size
+        ncop = r.copies_for(len(np.unique(ids)) * slice_bytes)
+        wc = r.weights(w, ncop)
+        scd = torch.from_numpy(sc.view(np.int16)).to(dev)
+        bid = torch.from_numpy(bi.view(np.int16)).to(dev)
+        xd = torch.from_numpy(x).to(dev)
+        idd = torch.from_numpy(ids).to(dev)
+        yd = torch.empty((pairs, n), device=dev)
+        al = [ctypes.byref(q.make_args(f"affine{bits}", wc[c], xd, yd, k, n, n_pos, stream=stream,
+                                       flags=q.FLAG_OVERLAP_PREV | q.FLAG_X_READY))
+              for c in range(ncop)]
+        ip, sp, bp = (ctypes.c_void_p(t.data_ptr()) for t in (idd, scd, bid))
+
+        def launch(c):
+            if exa(al[c], ip, n_exp, top_k, sp, bp):
+                raise RuntimeError(q.qmm_last_error())
+        dt = time_loop(torch, launch, reps, 5, ncop, stream)
+        q.qmm_device_status(stream)
+        gbs = pairs * slice_bytes / dt / 1e9
+        return {"us": dt * 1e6, "weight_gbs": gbs, "frac_hbm": gbs / hbm_peak,
+                "weight_bytes": int(pairs * slice_bytes), "pairs": int(pairs),
+                "note": "scale and bias arrays of the code words rotate with one copy (L2-resident)",
+                "launches_per_call": 1}
+
+    out["affine4_experts_pos1"] = expert_affine_case(4, 1)
+
     # MLX-style affine matrices: bytes = codes + bf16 scales + bf16 biases
     aff = lib.qmm_matmul_affine
 

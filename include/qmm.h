@@ -224,6 +224,14 @@ size_t qmm_backward_input_workspace_bytes(const qmm_args *a);
  * qmm_device_status reports as QMM_ERR_BAD_ID. Same formats and k limits as the one-token path. */
 int qmm_matmul_experts(const qmm_args *a, const int32_t *ids, int64_t n_experts, int64_t top_k);
 
+/* The expert-indexed product for affine matrices (a->fmt = QMM_AFFINE4 or
+ * QMM_AFFINE8; mixture-of-experts layers of MLX-style models): the code
+ * words are stacked as above, and `scales` / `biases` stack the experts'
+ * bf16 arrays the same way ([n_experts][n][k/64] each; device, 16-byte
+ * aligned). Everything else as qmm_matmul_experts. */
+int qmm_matmul_experts_affine(const qmm_args *a, const int32_t *ids, int64_t n_experts,
+                              int64_t top_k, const void *scales, const void *biases);
+
 /* Standalone dequantization: out[j][i] = the fp32 value of weight i of row
  * j, bit-identical to the exact value rounded once to fp32 (only Q4_K's
  * d*sc*q - dmin*m rounds; every other product is exact). out is device

@@ -32,7 +32,7 @@ EXPORTS = ("qmm_weight_bytes", "qmm_matmul", "qmm_set_stream", "qmm_matmul_ex",
            "qmm_device_status", "qmm_last_error", "qmm_version", "qmm_matmul_noalloc",
            "qmm_matmul_backward_input", "qmm_backward_input_workspace_bytes",
            "qmm_matmul_experts", "qmm_matmul_affine", "qmm_dequant_affine", "qmm_matmul_glu",
-           "qmm_glu_workspace_bytes", "qmm_check_bounded_wait")
+           "qmm_glu_workspace_bytes", "qmm_check_bounded_wait", "qmm_matmul_experts_affine")
 
 
 class QmmError(RuntimeError):
@@ -84,6 +84,7 @@ def load(path: str = LIB_PATH):
         "qmm_matmul_glu": (i, [pa, vp, i]),
         "qmm_glu_workspace_bytes": (sz, [pa]),
         "qmm_check_bounded_wait": (i, [vp]),
+        "qmm_matmul_experts_affine": (i, [pa, vp, i64, i64, vp, vp]),
         "qmm_dequant_affine": (i, [i, vp, vp, vp, i64, i64, vp, vp]),
     }
     for name, (res, args) in sig.items():
@@ -178,6 +179,12 @@ def qmm_dequant_affine(fmt, w, scales, biases, k: int, n: int, out, stream=None)
                                             _ptr(out), _stream(stream)))
 
 
+def qmm_matmul_experts_affine(args: qmm_args, ids, n_experts: int, top_k: int, scales,
+                              biases) -> int:
+    return _check(load().qmm_matmul_experts_affine(ctypes.byref(args), _ptr(ids), n_experts, top_k,
+                                                   _ptr(scales), _ptr(biases)))
+
+
 def qmm_matmul_experts(args: qmm_args, ids, n_experts: int, top_k: int) -> int:
     return _check(load().qmm_matmul_experts(ctypes.byref(args), _ptr(ids), n_experts, top_k))
 
@@ -258,7 +265,7 @@ def matmul_backward_input(fmt, w, dy, k: int, n: int, *, dx=None, j_start=0, j_e
 
 
 def matmul_experts(fmt, w, x, ids, k: int, n: int, n_experts: int, *, y=None, j_start=0,
-                   j_end=0, accumulate=False, stream=None, flags=0):
+                   j_end=0, accumulate=False, stream=None, flags=0, scales=None, biases=None):
     """Expert-indexed product for torch CUDA tensors: w uint8 (n_experts
     stacked slices of n rows), x float32 [n_pos, k], ids int32 [n_pos, top_k]
     on the device. Returns y float32 [n_pos * top_k, n] (the given y when passed)."""
@@ -272,7 +279,10 @@ def matmul_experts(fmt, w, x, ids, k: int, n: int, n_experts: int, *, y=None, j_
         y = torch.empty((n_pos * top_k, n), dtype=torch.float32, device=x.device)
     a = make_args(fmt, w, x, y, k, n, n_pos, w_len=w.numel() * w.element_size(), j_start=j_start,
                   j_end=j_end, accumulate=accumulate, stream=stream, flags=flags)
-    qmm_matmul_experts(a, ids, n_experts, top_k)
+    if scales is not None or biases is not None:
+        qmm_matmul_experts_affine(a, ids, n_experts, top_k, scales, biases)
+    else:
+        qmm_matmul_experts(a, ids, n_experts, top_k)
     return y
 
 

@@ -263,6 +263,73 @@ size_t glu_scratch_bytes(const qmm_args *a) {
     const size_t one = round256_bytes((size_t)a->n_tokens * (size_t)a->n * 4);
     return 2 * one + qmm::mma_workspace_bytes(a->fmt, a->n_tokens, a->k);
 }
+// The expert-indexed product of both entry points; affine matrices come with
+// their stacked scale and bias arrays (affine_entry).
+int experts_impl(const qmm_args *a, const int32_t *ids, int64_t n_experts, int64_t top_k,
+                 const void *sc, const void *bi, bool affine_entry) {
+    if (!a) return fail(QMM_ERR_NULL, "args is NULL");
+    if (n_experts < 1 || top_k < 1)
+        return fail(QMM_ERR_SHAPE, "n_experts %lld and top_k %lld must be >= 1",
+                    (long long)n_experts, (long long)top_k);
+    if (a->path == QMM_PATH_MMA) return fail(QMM_ERR_UNSUPPORTED, "expert products run as GEMVs");
+    if (affine_fmt(a->fmt) != affine_entry)
+        return fail(QMM_ERR_FORMAT, affine_entry
+                                        ? "qmm_matmul_experts_affine takes QMM_AFFINE4 or QMM_AFFINE8"
+                                        : "affine experts need their scales and biases: use "
+                                          "qmm_matmul_experts_affine");
+    // shape checks of one expert slice (w_len is checked against all slices below)
+    qmm_args one = *a;
+    one.w_len = 0;
+    int64_t j0, j1, rb;
+    int st = validate(&one, &j0, &j1, &rb, true);
+    if (st != QMM_OK) return st;
+    const int64_t slice = rb * a->n;
+    if (a->w_len != 0 && a->w_len != (size_t)(slice * n_experts))
+        return fail(QMM_ERR_SIZE, "%s W bytes %zu != n_experts*row_bytes*n = %lld",
+                    fmt_name(a->fmt), a->w_len, (long long)(slice * n_experts));
+    const int64_t pairs = a->n_tokens * top_k;
+    if (pairs > 65535)
+        return fail(QMM_ERR_SHAPE, "n_tokens * top_k = %lld exceeds 65535", (long long)pairs);
+    if (j1 <= j0) return QMM_OK;
+    if (!ids) return fail(QMM_ERR_NULL, "ids is NULL");
+    if (reinterpret_cast<uintptr_t>(ids) & 3u) return fail(QMM_ERR_ALIGN, "ids must be 4-byte aligned");
+    if (affine_entry && a->k > 0) {
+        if (!sc || !bi) return fail(QMM_ERR_NULL, "scales or biases is NULL");
+        if ((reinterpret_cast<uintptr_t>(sc) & 15u) || (reinterpret_cast<uintptr_t>(bi) & 15u))
+            return fail(QMM_ERR_ALIGN, "scales and biases must be 16-byte aligned");
+    }
+    if (a->k > 0 && !qmm::gemv_supports(a->fmt, a->k))
+        return fail(QMM_ERR_UNSUPPORTED, "expert GEMV cannot take %s with k=%lld", fmt_name(a->fmt),
+                    (long long)a->k);
+    qmm::DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != QMM_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(a->stream);
+    if (a->k == 0) {
+        if (a->accumulate) return QMM_OK;
+        cudaError_t e = qmm::launch_zero_cols(a->y, pairs, a->n, j0, j1, s);
+        return e == cudaSuccess ? QMM_OK : cuda_fail(e, "zero-fill launch");
+    }
+    qmm::GemvLaunch g;
+    g.fmt = a->fmt;
+    g.w = static_cast<const uint8_t *>(a->w);
+    g.x = a->x;
+    g.y = a->y;
+    g.k = a->k; g.n = a->n; g.row_bytes = rb;
+    g.j0 = j0; g.j1 = j1;
+    g.accumulate = a->accumulate;
+    g.overlap_prev = (a->flags & QMM_FLAG_OVERLAP_PREV) != 0;
+    g.x_ready = g.overlap_prev && (a->flags & QMM_FLAG_X_READY) != 0;
+    g.ids = ids;
+    g.sc = static_cast<const uint8_t *>(sc);
+    g.bi = static_cast<const uint8_t *>(bi);
+    g.n_experts = (int)n_experts;
+    g.top_k = (int)top_k;
+    g.pairs = (int)pairs;
+    cudaError_t e = qmm::launch_gemv(g, *dev, s);
+    return e == cudaSuccess ? QMM_OK : cuda_fail(e, "expert GEMV launch");
+}
+
 }  // namespace
 
 namespace qmm {
@@ -405,57 +472,13 @@ int qmm_matmul_backward_input(const qmm_args *a) {
 
 int qmm_matmul_experts(const qmm_args *a, const int32_t *ids, int64_t n_experts, int64_t top_k) {
     t_err[0] = 0;
-    if (!a) return fail(QMM_ERR_NULL, "args is NULL");
-    if (n_experts < 1 || top_k < 1)
-        return fail(QMM_ERR_SHAPE, "n_experts %lld and top_k %lld must be >= 1",
-                    (long long)n_experts, (long long)top_k);
-    if (a->path == QMM_PATH_MMA) return fail(QMM_ERR_UNSUPPORTED, "expert products run as GEMVs");
-    if (affine_fmt(a->fmt))
-        return fail(QMM_ERR_FORMAT, "expert products take single-stream (GGUF) formats");
-    // shape checks of one expert slice (w_len is checked against all slices below)
-    qmm_args one = *a;
-    one.w_len = 0;
-    int64_t j0, j1, rb;
-    int st = validate(&one, &j0, &j1, &rb, true);
-    if (st != QMM_OK) return st;
-    const int64_t slice = rb * a->n;
-    if (a->w_len != 0 && a->w_len != (size_t)(slice * n_experts))
-        return fail(QMM_ERR_SIZE, "%s W bytes %zu != n_experts*row_bytes*n = %lld",
-                    fmt_name(a->fmt), a->w_len, (long long)(slice * n_experts));
-    const int64_t pairs = a->n_tokens * top_k;
-    if (pairs > 65535)
-        return fail(QMM_ERR_SHAPE, "n_tokens * top_k = %lld exceeds 65535", (long long)pairs);
-    if (j1 <= j0) return QMM_OK;
-    if (!ids) return fail(QMM_ERR_NULL, "ids is NULL");
-    if (reinterpret_cast<uintptr_t>(ids) & 3u) return fail(QMM_ERR_ALIGN, "ids must be 4-byte aligned");
-    if (a->k > 0 && !qmm::gemv_supports(a->fmt, a->k))
-        return fail(QMM_ERR_UNSUPPORTED, "expert GEMV cannot take %s with k=%lld", fmt_name(a->fmt),
-                    (long long)a->k);
-    qmm::DeviceInfo *dev = nullptr;
-    st = device_info(&dev);
-    if (st != QMM_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(a->stream);
-    if (a->k == 0) {
-        if (a->accumulate) return QMM_OK;
-        cudaError_t e = qmm::launch_zero_cols(a->y, pairs, a->n, j0, j1, s);
-        return e == cudaSuccess ? QMM_OK : cuda_fail(e, "zero-fill launch");
-    }
-    qmm::GemvLaunch g;
-    g.fmt = a->fmt;
-    g.w = static_cast<const uint8_t *>(a->w);
-    g.x = a->x;
-    g.y = a->y;
-    g.k = a->k; g.n = a->n; g.row_bytes = rb;
-    g.j0 = j0; g.j1 = j1;
-    g.accumulate = a->accumulate;
-    g.overlap_prev = (a->flags & QMM_FLAG_OVERLAP_PREV) != 0;
-    g.x_ready = g.overlap_prev && (a->flags & QMM_FLAG_X_READY) != 0;
-    g.ids = ids;
-    g.n_experts = (int)n_experts;
-    g.top_k = (int)top_k;
-    g.pairs = (int)pairs;
-    cudaError_t e = qmm::launch_gemv(g, *dev, s);
-    return e == cudaSuccess ? QMM_OK : cuda_fail(e, "expert GEMV launch");
+    return experts_impl(a, ids, n_experts, top_k, nullptr, nullptr, false);
+}
+
+int qmm_matmul_experts_affine(const qmm_args *a, const int32_t *ids, int64_t n_experts,
+                              int64_t top_k, const void *scales, const void *biases) {
+    t_err[0] = 0;
+    return experts_impl(a, ids, n_experts, top_k, scales, biases, true);
 }
 
 size_t qmm_backward_input_workspace_bytes(const qmm_args *a) {

@@ -74,6 +74,9 @@ struct GemvAffFields {
     int aux_off, aux_sb;
 };
 struct GemvAffParams : GemvParams, GemvAffFields {};
+// expert-indexed affine matrices: the scale and bias arrays are stacked like
+// the codes ([n_experts][n][k/64] each)
+struct GemvAffExpParams : GemvExpParams, GemvAffFields {};
 // Gated pairs: w is the gate matrix, w2 the up matrix (same format and
 // shape); y = act(x Wg) * (x Wu). A CTA's stages alternate between a block
 // of rows of Wg and the same rows of Wu; each window of rows keeps two sets
@@ -92,14 +95,20 @@ enum GemvVar : int { kVarPlain = 0, kVarExperts = 1, kVarSwiglu = 2, kVarGeglu =
 
 template <int FMT, int VAR>
 using GemvParamsOf = typename std::conditional<
-    is_affine(FMT), GemvAffParams,
+    is_affine(FMT),
+    typename std::conditional<VAR == kVarExperts, GemvAffExpParams, GemvAffParams>::type,
     typename std::conditional<
         VAR == kVarExperts, GemvExpParams,
         typename std::conditional<(VAR >= kVarSwiglu), GemvGluParams, GemvParams>::type>::type>::type;
 
 template <int FMT, int VAR>
 __host__ GemvParamsOf<FMT, VAR> params_of(const GemvHostParams &h) {
-    if constexpr (is_affine(FMT)) {
+    if constexpr (is_affine(FMT) && VAR == kVarExperts) {
+        GemvAffExpParams a;
+        static_cast<GemvExpParams &>(a) = static_cast<const GemvExpParams &>(h);
+        static_cast<GemvAffFields &>(a) = static_cast<const GemvAffFields &>(h);
+        return a;
+    } else if constexpr (is_affine(FMT)) {
         GemvAffParams a;
         static_cast<GemvParams &>(a) = static_cast<const GemvParams &>(h);
         static_cast<GemvAffFields &>(a) = static_cast<const GemvAffFields &>(h);
@@ -452,15 +461,18 @@ struct SliceSel {
     __device__ __forceinline__ const float *x(const GemvParams &p) const { return p.x; }
     __device__ __forceinline__ float *y(const GemvParams &p) const { return p.y; }
     __device__ __forceinline__ int64_t w_off() const { return 0; }
+    __device__ __forceinline__ int64_t a_off() const { return 0; }
 };
 template <>
 struct SliceSel<true> {
     const float *xg;
     float *yg;
     int64_t off;
+    int64_t aoff = 0;  // affine formats: the slice's offset in the scale and bias arrays
     __device__ __forceinline__ const float *x(const GemvParams &) const { return xg; }
     __device__ __forceinline__ float *y(const GemvParams &) const { return yg; }
     __device__ __forceinline__ int64_t w_off() const { return off; }
+    __device__ __forceinline__ int64_t a_off() const { return aoff; }
 };
 
 template <int FMT, int UPT, int VAR>
@@ -503,6 +515,7 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParamsOf<FMT, VAR> p) {
         sel.off = (int64_t)e * p.slice_bytes;
         sel.xg = p.x + (int64_t)(pair / p.top_k) * p.k;
         sel.yg = p.y + (int64_t)pair * p.n;
+        if constexpr (is_affine(FMT)) sel.aoff = (int64_t)e * p.n * p.aux_row_bytes;
     }
     const int64_t r0 = p.j0 + (int64_t)cta * p.rows_base + (cta < p.rows_rem ? cta : p.rows_rem);
     const int64_t nrows = p.rows_base + (cta < p.rows_rem ? 1 : 0);
@@ -559,7 +572,7 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParamsOf<FMT, VAR> p) {
             if constexpr (is_affine(FMT)) {
                 // the stage's rows of the scale and bias arrays, the same way
                 const int64_t AR = p.aux_row_bytes, alim = p.aux_total & ~(int64_t)15;
-                const int64_t SA = ra * AR, SE = rb * AR;
+                const int64_t SA = sel.a_off() + ra * AR, SE = sel.a_off() + rb * AR;
                 const int64_t s16 = SA & ~(int64_t)15;
                 const int64_t send = min((SE + 15) & ~(int64_t)15, alim);
                 const int64_t sdst = (int64_t)slot * SB + p.aux_off;
@@ -664,8 +677,9 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParamsOf<FMT, VAR> p) {
                     const uint32_t rowa = sbase + (uint32_t)(sel.w_off() + (ra + rr) * R - a16);
                     if constexpr (is_affine(FMT)) {
                         const int64_t AR = p.aux_row_bytes;
+                        const int64_t a0 = sel.a_off() + ra * AR;
                         const uint32_t auxa = sbase + (uint32_t)p.aux_off +
-                                              (uint32_t)((ra + rr) * AR - ((ra * AR) & ~(int64_t)15));
+                                              (uint32_t)(a0 + rr * AR - (a0 & ~(int64_t)15));
 #pragma unroll
                         for (int q = 0; q < UPT; ++q) {
                             const int u = u0 + q * kCons;
@@ -770,9 +784,9 @@ template <int FMT, int UPT>
 static cudaError_t launch_t(const GemvHostParams &p, dim3 grid, size_t smem, cudaStream_t s,
                             bool overlap) {
     if constexpr (is_affine(FMT)) {
-        // no expert-indexed or gated affine matrices
-        if (p.ids || p.glu) return cudaErrorNotSupported;
-        return launch_e<FMT, UPT, kVarPlain>(p, grid, smem, s, overlap);
+        if (p.glu) return cudaErrorNotSupported;  // no gated affine pairs
+        return p.ids ? launch_e<FMT, UPT, kVarExperts>(p, grid, smem, s, overlap)
+                     : launch_e<FMT, UPT, kVarPlain>(p, grid, smem, s, overlap);
     } else {
         if (p.ids) return launch_e<FMT, UPT, kVarExperts>(p, grid, smem, s, overlap);
         if (p.glu == 1) return launch_e<FMT, UPT, kVarSwiglu>(p, grid, smem, s, overlap);
@@ -890,7 +904,7 @@ cudaError_t launch_gemv(const GemvLaunch &g, const DeviceInfo &dev, cudaStream_t
     p.sc = g.sc;
     p.bi = g.bi;
     p.aux_row_bytes = AR;
-    p.aux_total = AR * g.n;
+    p.aux_total = AR * g.n * (g.ids ? g.n_experts : 1);
     p.aux_off = (int)code_bytes(SR);
     p.aux_sb = (int)aux_bytes(SR);
     p.w2 = g.w2;

@@ -217,6 +217,10 @@ def test_affine_sizes_and_policy(lib):
     ("aff", dict(fmt="affine8", k=128), (16 * 700 + 2, 16 * 800), 6),
     ("aff", dict(fmt="affine4", k=128, w_len=10), (16 * 700, 16 * 800), 3),
     ("experts", dict(fmt="affine4", k=128), None, 1),
+    ("experts_aff", dict(fmt="q4_k"), (16 * 700, 16 * 800), 1),
+    ("experts_aff", dict(fmt="affine4", k=128), (None, 16 * 800), 5),
+    ("experts_aff", dict(fmt="affine4", k=128), (16 * 700 + 2, 16 * 800), 6),
+    ("experts_aff", dict(fmt="affine8", k=128, w_len=128 * 8 * 3), (16 * 700, 16 * 800), 3),
     ("back", dict(fmt="affine4", k=128), None, 1),
 ])
 def test_affine_rejected_on_host(lib, fn, kw, sb, status):
@@ -228,6 +232,8 @@ def test_affine_rejected_on_host(lib, fn, kw, sb, status):
             q.qmm_matmul_affine(a, *sb)
         elif fn == "experts":
             q.qmm_matmul_experts(a, 16 * 500, 4, 2)
+        elif fn == "experts_aff":
+            q.qmm_matmul_experts_affine(a, 16 * 500, 4, 2, *sb)
         else:
             q.qmm_matmul_backward_input(a)
     assert ei.value.status == status, q.qmm_last_error()

@@ -187,3 +187,54 @@ def test_tensor_core_path_repeatable_bits(bits):
             ref = got
         else:
             assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), f"call {it}"
+
+
+@pytest.mark.parametrize("bits,k,n,n_exp,top_k,n_pos", [(4, 1024, 300, 6, 3, 2), (8, 4096, 768, 16, 4, 3),
+                                                       (4, 64, 7, 3, 2, 1)])
+def test_affine_experts(bits, k, n, n_exp, top_k, n_pos):
+    """Expert-indexed affine product: row p * top_k + s equals the plain affine
+    product of x[p] with the slice ids[p, s] of the stacked codes, scales and
+    biases (cut by hand)."""
+    rng = np.random.default_rng(bits * 100 + k + n)
+    w, sc, bi = qmm_synth.gen_affine(bits, k, n * n_exp, rng)
+    x = qmm_synth.gen_x(n_pos, k, rng)
+    ids = qmm_synth.gen_ids(n_pos, top_k, n_exp, rng)
+    y = q.matmul_experts(FMT[bits], _dev(w), _dev(x), _dev(ids), k, n, n_exp, scales=_dev(sc),
+                         biases=_dev(bi))
+    torch.cuda.synchronize()
+    q.qmm_device_status()
+    y = y.cpu().numpy()
+    rb = k * bits // 8
+    for p in range(n_pos):
+        for s in range(top_k):
+            e = int(ids[p, s])
+            yr, sr = oracle.matmul_affine(bits, w[e * n * rb:(e + 1) * n * rb], sc[e * n:(e + 1) * n],
+                                          bi[e * n:(e + 1) * n], x[p], k, n)
+            _assert(y[p * top_k + s][None, :], yr, sr, f"affine{bits} expert {e} pos {p} slot {s}")
+
+
+def test_affine_experts_tile_accumulate_and_bad_id():
+    rng = np.random.default_rng(61)
+    bits, k, n, n_exp = 4, 512, 400, 4
+    w, sc, bi = qmm_synth.gen_affine(bits, k, n * n_exp, rng)
+    x = qmm_synth.gen_x(2, k, rng)
+    ids = np.array([[3, 0], [-1, 2]], np.int32)
+    y_in = rng.normal(0, 1, (4, n)).astype(np.float32)
+    j0, j1 = 33, 301
+    y = q.matmul_experts(FMT[bits], _dev(w), _dev(x), _dev(ids), k, n, n_exp, scales=_dev(sc),
+                         biases=_dev(bi), y=_dev(y_in), j_start=j0, j_end=j1, accumulate=True)
+    torch.cuda.synchronize()
+    with pytest.raises(q.QmmError) as ei:
+        q.qmm_device_status()
+    assert ei.value.status == 11
+    y = y.cpu().numpy()
+    assert np.array_equal(y[2].view(np.uint32), y_in[2].view(np.uint32))   # bad id: row untouched
+    outside = np.ones(n, bool)
+    outside[j0:j1] = False
+    assert np.array_equal(y[:, outside].view(np.uint32), y_in[:, outside].view(np.uint32))
+    rb = k * bits // 8
+    for row, (p, e) in ((0, (0, 3)), (1, (0, 0)), (3, (1, 2))):
+        yr, sr = oracle.matmul_affine(bits, w[e * n * rb:(e + 1) * n * rb], sc[e * n:(e + 1) * n],
+                                      bi[e * n:(e + 1) * n], x[p], k, n)
+        ye, se = oracle.tiled(yr, sr, j0, j1, True, y_in[row][None, :])
+        _assert(y[row][None, j0:j1], ye[:, j0:j1], se[:, j0:j1], f"row {row}")
