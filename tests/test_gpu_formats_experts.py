@@ -234,3 +234,17 @@ def test_experts_overlapped_launches():
     torch.cuda.synchronize()
     q.qmm_device_status()
     _assert(y.cpu().numpy(), 4 * y_ref, 4 * s_ref, "accumulating chain")
+
+
+def test_experts_many_pairs():
+    """A prefill-sized routing (64 positions x top 8 = 512 pairs, each pair
+    one CTA's GEMV over its slice), ids repeating across positions."""
+    fmt, k, n, n_exp = "q4_k", 256, 64, 16
+    rng = np.random.default_rng(91)
+    w = qmm_synth.gen_weights(fmt, k, n * n_exp, rng)
+    x = qmm_synth.gen_x(64, k, rng)
+    ids = qmm_synth.gen_ids(64, 8, n_exp, rng)
+    y = _experts(fmt, w, x, ids, k, n, n_exp)
+    q.qmm_device_status()
+    y_ref, s_ref = oracle.matmul_experts(fmt, w, x, k, n, n_exp, ids)
+    _assert(y.cpu().numpy(), y_ref, s_ref, "512 pairs")
