@@ -61,8 +61,9 @@ extern "C" {
  *       per row: little-endian 32-bit words of 8 four-bit or 4 eight-bit codes,
  *       lowest bits first), and a bf16 scale and a bf16 bias per group of 64
  *       consecutive weights of a row ([n][k/64] each); weight = code * scale +
- *       bias, rounded once to fp32; k % 64 == 0. Only qmm_matmul_affine and
- *       qmm_dequant_affine take them; qmm_weight_bytes counts the code bytes. */
+ *       bias, rounded once to fp32; k % 64 == 0. Only qmm_matmul_affine,
+ *       qmm_matmul_experts_affine and qmm_dequant_affine take them;
+ *       qmm_weight_bytes counts the code bytes. */
 typedef enum qmm_format {
     QMM_BF16 = 0,
     QMM_F16 = 1,
@@ -132,9 +133,11 @@ typedef enum qmm_flags {
     QMM_FLAG_X_READY = 2
 } qmm_flags;
 
-/* Bytes of n packed rows of k weights: (k/32)*18*n, (k/256)*144*n,
- * (k/256)*210*n or 2*k*n (rullama matmul.rs shape checks). 0 when fmt is
- * unknown, k does not fit the format, or k/n is negative. Host only. */
+/* Bytes of n packed rows of k weights: (k/32)*18*n (Q4_0), (k/256)*144*n
+ * (Q4_K), (k/256)*210*n (Q6_K), 2*k*n (BF16 / F16) as in the rullama
+ * matmul.rs shape checks; (k/32)*34*n (Q8_0), (k/32)*22*n (Q5_0); the code
+ * bytes k*n/2 or k*n of the affine formats. 0 when fmt is unknown, k does
+ * not fit the format, or k/n is negative. Host only. */
 size_t qmm_weight_bytes(int fmt, int64_t k, int64_t n);
 
 /* y = x @ W over the whole output axis, on the stream last given to
