@@ -66,6 +66,8 @@ def test_golden_page_constants():
             oracle.dequant_affine(bits, w, sb, sb, k, 1)
             with pytest.raises(ValueError):
                 oracle.dequant_affine(bits, w, sb[:-1], sb[:-1], k, 1)
+        elif kind == "floor":
+            assert row[1] == "cosine" and oracle.COSINE_FLOOR == float(row[2])
         else:
             raise AssertionError(f"unknown golden kind {kind}")
 
@@ -395,6 +397,32 @@ def test_cosine_zero_vectors():
     z = np.zeros(5)
     assert oracle.cosine(z, z) == 1.0
     assert oracle.cosine(z, np.ones(5)) == 0.0
+
+
+def test_checker_cosine_floor_between_0_999_and_0_9999():
+    """Errors inside the elementwise bar (S large against y) still fail when
+    the direction drifts: cosine 0.99953 is below the 0.9999 floor, cosine
+    0.999950 above it (both in closed form: (1 + a) / sqrt(2 (1 + a^2)))."""
+    y_ref = np.array([[1.0, 1.0]])
+    s_ref = np.full_like(y_ref, 1e4)  # bar 1.0 per element
+    for a, want_ok in ((1.063, False), (1.02, True)):
+        cos_exact = (1 + a) / np.sqrt(2 * (1 + a * a))
+        ok, _, cos, _ = oracle.check(np.array([[1.0, a]]), y_ref, s_ref)
+        assert abs(cos - cos_exact) < 1e-12
+        assert ok == want_ok, (a, cos)
+    assert 0.999 < (1 + 1.063) / np.sqrt(2 * (1 + 1.063 ** 2)) < 0.9999
+
+
+def test_checker_nan_positions_must_agree():
+    """A NaN reference (a NaN weight) must come out NaN, at the same place."""
+    y_ref = np.array([[np.nan, 1.0, 2.0]])
+    s_ref = np.array([[1.0, 1.0, 2.0]])
+    ok, *_ = oracle.check(np.array([[np.nan, 1.0, 2.0]]), y_ref, s_ref)
+    assert ok
+    ok, *_ = oracle.check(np.array([[0.0, 1.0, 2.0]]), y_ref, s_ref)
+    assert not ok
+    ok, *_ = oracle.check(np.array([[1.0, np.nan, 2.0]]), np.array([[1.0, 1.0, 2.0]]), s_ref)
+    assert not ok
 
 
 def test_tiled_semantics():
