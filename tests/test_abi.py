@@ -279,3 +279,40 @@ def test_glu_workspace_and_empty_work(lib):
     assert q.qmm_glu_workspace_bytes(a) == 2 * one + 8 * 4096 * 2 + 256
     assert q.qmm_glu_workspace_bytes(_args(fmt="affine4", k=128)) == 0
     assert q.qmm_matmul_glu(_args(j_start=3, j_end=3), None, 1) == 0
+
+
+def _fresh_python(code):
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    return subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                          timeout=300)
+
+
+def test_missing_library_fails_loudly():
+    """No fallback: without libqmm.so the binding raises instead of computing
+    anything another way."""
+    r = _fresh_python("import quantized_weight_gguf_gb300 as q\n"
+                      "try:\n"
+                      "    q.load('no_such_dir/libqmm.so')\n"
+                      "except RuntimeError as e:\n"
+                      "    print('raised:', e)\n"
+                      "else:\n"
+                      "    raise SystemExit('loaded')\n")
+    assert r.returncode == 0 and "raised: libqmm.so is not built" in r.stdout, r.stdout + r.stderr
+
+
+def test_product_package_never_reaches_the_oracle(lib):
+    """The package neither imports the oracle nor mentions it in code."""
+    r = _fresh_python("import sys\n"
+                      "import quantized_weight_gguf_gb300 as q\n"
+                      "q.load()\n"
+                      "print(sorted(m for m in sys.modules if m == 'oracle' or m.startswith('oracle.')))\n")
+    assert r.returncode == 0 and r.stdout.strip() == "[]", r.stdout + r.stderr
+    pkg = os.path.dirname(q.__file__)
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), f
+                assert "qmm_oracle" not in src and "liboracle" not in src, f
