@@ -75,3 +75,33 @@ def test_reference_arm_only_rank0_works(monkeypatch, capsys):
     args = argparse.Namespace(gpus=2, steps=1, warmup=1)
     assert bench.run_reference(args) == 0
     assert capsys.readouterr().out == ""  # rank 1 prints nothing and does no work
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` at world size 1: one JSON line with the
+    contract's keys, the oracle timed on host cores, no device bytes moved."""
+    import json
+    import subprocess
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "3",
+                        "--warmup", "3"], cwd=ROOT, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["n_gpus"] == 1
+    assert (d["steps"], d["warmup"]) == (3, 3)
+    assert d["value"] > 0 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert "workload" in d["config"]
+    # value is weight bytes per second: bytes per step / seconds per step
+    assert abs(d["value"] - d["config"]["weight_bytes_per_step"] / (d["ms_per_step"] * 1e6)) \
+        < 1e-6 * d["value"]
