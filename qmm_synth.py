@@ -29,6 +29,14 @@ stand-ins for the real-model shapes that the rullama ``matmul.rs`` tests use
                     Q8_0 d ~ U[0.002, 0.02] with uniform int8 codes, Q5_0
                     d ~ U[0.005, 0.05] with uniform high-bit words and nibbles;
                     ids drawn without repetition per position; x ~ N(0, 1); seeds 6, 7.
+* ``q8_0_gemv`` / ``q5_0_gemv``
+                    k=4096, n=14336, one token; the expert workloads' value
+                    distributions; x ~ N(0, 1); seeds 8, 9.
+* ``affine4_gemv`` / ``affine8_gemv`` / ``affine4_prefill`` / ``affine8_prefill``
+                    MLX-style affine matrices, k=4096, n=14336, 1 or 512 tokens:
+                    uniform code words, bf16 scales U[0.01, 0.06) and biases
+                    U[-0.1, 0.1) per 64 weights (fp32 draws truncated to bf16);
+                    x ~ N(0, 1); seeds 10-13.
 
 Byte layouts written here (little-endian): Q4_0 block = f16 d then 16 quant
 bytes (18 B); Q8_0 block = f16 d then 32 code bytes (34 B); Q5_0 block = f16 d,
