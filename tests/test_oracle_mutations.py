@@ -102,6 +102,18 @@ MUTATIONS = [
      "const double a = oracle_act(act, gu[0]);\n            y[t * n + j] = a * gu[1];",
      "const double a = oracle_act(act, gu[1]);\n            y[t * n + j] = a * gu[0];"),
     ("gated error bar drops the up term", C, "* su[0] + fabs(a) * su[1];", "* su[0];"),
+    # numpy-product helpers and the tile rule of the wrapper
+    ("blas product transposed weights", PY, "    return x64 @ deq.T, np.abs(x64) @ np.abs(deq).T\n\n\ndef matmul_sampled",
+     "    return x64 @ deq.T[::-1], np.abs(x64) @ np.abs(deq).T\n\n\ndef matmul_sampled"),
+    ("blas back-input magnitude without abs", PY, "    return d @ deq, np.abs(d) @ np.abs(deq)",
+     "    return d @ deq, np.abs(d @ deq)"),
+    ("blas back-input tile ignored", PY, "    d = np.asarray(dy, np.float64).reshape(-1)[j_start:j_end]",
+     "    d = np.asarray(dy, np.float64).reshape(-1)[:j_end - j_start]"),
+    ("affine blas without abs", PY, "    deq = dequant_affine(bits, w, scales, biases, k, n).astype(np.float64)\n    x64 = np.atleast_2d(np.asarray(x, np.float64))\n    return x64 @ deq.T, np.abs(x64) @ np.abs(deq).T",
+     "    deq = dequant_affine(bits, w, scales, biases, k, n).astype(np.float64)\n    x64 = np.atleast_2d(np.asarray(x, np.float64))\n    return x64 @ deq.T, np.abs(x64 @ deq.T)"),
+    ("tile bar without |y_in|", PY, "        s[:, sl] = s_ref[:, sl] + np.abs(np.asarray(y_in, np.float64)[:, sl])",
+     "        s[:, sl] = s_ref[:, sl]"),
+    ("tile accumulate overwrites", PY, "        y[:, sl] = y[:, sl] + y_ref[:, sl]", "        y[:, sl] = y_ref[:, sl]"),
     # acceptance check
     ("bar 1e-3 instead of 1e-4", PY, "TOL_REL = 1e-4", "TOL_REL = 1e-3"),
     ("cosine floor 0.999", PY, "COSINE_FLOOR = 0.9999", "COSINE_FLOOR = 0.999"),

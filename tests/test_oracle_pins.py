@@ -503,6 +503,7 @@ def test_back_input_sum_axis_tiles_add_up():
     assert not z.any() and not sz.any()
     c, sc = oracle.matmul_back_input_blas(fmt, w, dy, k, n, 13, n)
     np.testing.assert_allclose(c, b, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(sc, sb, rtol=1e-12)
     with pytest.raises(ValueError):
         oracle.matmul_back_input(fmt, w, dy, k, n, 10, 5)
 
@@ -692,6 +693,10 @@ def test_affine_product_matches_numpy_and_sampled():
     ti, ji = np.array([0, 2, 1]), np.array([10, 0, 5])
     ys, ss = oracle.matmul_affine_sampled(4, w, scales, biases, x, k, n, ti, ji)
     assert np.array_equal(ys, y[ti, ji]) and np.array_equal(ss, s[ti, ji])
+    # the library-product variant used for full-size checks gives the same (y, S)
+    yb, sb = oracle.matmul_affine_blas(4, w, scales, biases, x, k, n)
+    np.testing.assert_allclose(yb, y, rtol=1e-12, atol=1e-12 * float(np.max(s)))
+    np.testing.assert_allclose(sb, s, rtol=1e-12)
 
 
 
