@@ -102,6 +102,12 @@ MUTATIONS = [
      "const double a = oracle_act(act, gu[0]);\n            y[t * n + j] = a * gu[1];",
      "const double a = oracle_act(act, gu[1]);\n            y[t * n + j] = a * gu[0];"),
     ("gated error bar drops the up term", C, "* su[0] + fabs(a) * su[1];", "* su[0];"),
+    ("gated error bar with a signed derivative", C, "fabs(oracle_act_deriv(act, gu[0]))", "oracle_act_deriv(act, gu[0])"),
+    ("gated act selector ignored", C, "if (act == 0) return g / (1.0 + exp(-g));",
+     "if (act >= 0) return g / (1.0 + exp(-g));"),
+    # cosine
+    ("cosine of zero vectors 0", PY, "    if na == 0.0 and nb == 0.0:\n        return 1.0", "    if na == 0.0 and nb == 0.0:\n        return 0.0"),
+    ("cosine without the norm of b", PY, "np.dot(a, b) / (np.sqrt(na) * np.sqrt(nb))", "np.dot(a, b) / (np.sqrt(na) * np.sqrt(na))"),
     # numpy-product helpers and the tile rule of the wrapper
     ("blas product transposed weights", PY, "    return x64 @ deq.T, np.abs(x64) @ np.abs(deq).T\n\n\ndef matmul_sampled",
      "    return x64 @ deq.T[::-1], np.abs(x64) @ np.abs(deq).T\n\n\ndef matmul_sampled"),
