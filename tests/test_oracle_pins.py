@@ -386,6 +386,51 @@ def test_checker_catches_a_dropped_term():
     assert not ok and worst > 1e-4
 
 
+def test_checker_catches_plausible_kernel_mistakes():
+    """Outputs a faulty kernel would plausibly produce, built from the oracle's
+    own weights, must each fail the acceptance check at the configs' k: one
+    32-weight unit skipped, output columns shifted by one, two tokens swapped,
+    a ragged last tile left unwritten, sub-block 2 of every super-block read
+    with scale sc + 1 (a decoder slip repeats in every row), and zero point 7
+    instead of 8 in the Q4_0 blocks at one position of every row. A slip
+    confined to one sub-block of one row is below the bar's resolution (it
+    moves one output by about 1e-5 of S here): the bit-exact dequant tests are
+    what see those."""
+    rng = np.random.default_rng(17)
+    k, n, nt = 4096, 64, 3
+    w = qmm_synth.gen_weights("q4_k", k, n, rng)
+    x = qmm_synth.gen_x(nt, k, rng).astype(np.float64)
+    y, s = oracle.matmul("q4_k", w, x.astype(np.float32), k, n)
+    deq = oracle.dequant("q4_k", w, k, n).astype(np.float64)
+    assert oracle.check(y, y, s)[0]
+    bad = []
+    u = int(np.argmax(np.abs((x[0].reshape(-1, 32) * deq[5].reshape(-1, 32)).sum(1))))
+    b = y.copy(); b[0, 5] -= x[0, 32 * u:32 * u + 32] @ deq[5, 32 * u:32 * u + 32]; bad.append(b)
+    b = y.copy(); b[:, 1:] = y[:, :-1]; bad.append(b)
+    b = y.copy(); b[[0, 1]] = y[[1, 0]]; bad.append(b)
+    b = y.copy(); b[:, 60:] = 0.0; bad.append(b)
+    # d * q of sub-block 2 (low nibbles of quant bytes 32..63, quant bytes at 16)
+    blk = w.reshape(n, k // 256, 144)
+    dsb = np.ascontiguousarray(blk[:, :, 0:2]).view("<f2")[..., 0].astype(np.float64)
+    q2 = (blk[:, :, 16 + 32:16 + 64] & 15).astype(np.float64)
+    d2 = deq.copy().reshape(n, k // 256, 256)
+    d2[:, :, 64:96] += dsb[:, :, None] * q2                # sc read as sc + 1
+    b = x @ d2.reshape(n, k).T; bad.append(b)
+    for i, yb in enumerate(bad):
+        ok, worst, cos, msg = oracle.check(yb, y, s)
+        assert not ok, (i, msg)
+    w0 = qmm_synth.gen_weights("q4_0", k, n, rng)
+    y0, s0 = oracle.matmul("q4_0", w0, x.astype(np.float32), k, n)
+    dq0 = oracle.dequant("q4_0", w0, k, n).astype(np.float64)
+    dblk = np.ascontiguousarray(w0.reshape(n, -1, 18)[:, 10, 0:2]).view("<f2")[:, 0]
+    d3 = dq0.copy(); d3[:, 320:352] += dblk.astype(np.float64)[:, None]  # (q - 7) d
+    assert not oracle.check(x @ d3.T, y0, s0)[0]
+    # the resolution limit stated above
+    d4 = deq.copy(); d4[7, 64:96] *= 1.0 + 1.0 / 32.0
+    b = y.copy(); b[:, 7] = x @ d4[7]
+    assert oracle.check(b, y, s)[0]
+
+
 def test_checker_catches_sign_flip_by_cosine():
     y = np.linspace(-1, 1, 101)[None, :]
     s = np.full_like(y, 1e9)  # elementwise bar loose: cosine must catch it
