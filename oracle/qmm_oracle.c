@@ -59,7 +59,9 @@
  *
  * Parity pins live in tests/test_oracle_pins.py (hand-packed blocks with
  * known values, closed-form sizes, exhaustive f16 decode against numpy,
- * identity / one-hot products, brute-force tiny products).
+ * identity / one-hot products, brute-force tiny products);
+ * tests/test_oracle_mutations.py plants plausible mistakes in private copies
+ * of this file and requires every one of them to fail a pin.
  */
 #include <math.h>
 #include <stdint.h>
