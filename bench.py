@@ -42,6 +42,8 @@ sys.path.insert(0, ROOT)
 
 import qmm_synth  # noqa: E402
 
+# the workload every arm of the bench reports (the same string in each line)
+HEADLINE_WORKLOAD = "bf16+f16 GEMV k=n=4096, 1 token (one step = both GEMVs)"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES_DEFAULT = 129 * 1024 * 1024
@@ -190,8 +192,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "bf16+f16 GEMV k=n=4096, 1 token (one step = both)",
-                       "weight_bytes_per_step": wbytes},
+            "config": {"workload": HEADLINE_WORKLOAD, "weight_bytes_per_step": wbytes},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": "full oracle product of both 4096x4096 weight matrices per step"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -376,6 +377,20 @@ def run_native(args):
                 raise RuntimeError(q.qmm_last_error())
         r1.record(stream)
         r1.synchronize()
+        # the same kernel as plain stream-ordered launches (no programmatic
+        # overlap: what a dependent chain of products gets)
+        fmt0, k0, n0 = work[0][:3]
+        plain = [q.make_args(fmt0, wcopies[0][c], xs[0], ys[0], k0, n0, 1, stream=stream, flags=0)
+                 for c in range(ncop)]
+        prefs = [ctypes.byref(a) for a in plain]
+        p0 = torch.cuda.Event(enable_timing=True)
+        p1 = torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        for i in range(KR):
+            if mm(prefs[i % ncop]):
+                raise RuntimeError(q.qmm_last_error())
+        p1.record(stream)
+        p1.synchronize()
         time.sleep(0.25)
     torch.cuda.synchronize()
     barrier(ws)
@@ -383,6 +398,7 @@ def run_native(args):
     elapsed = max_over_ranks(elapsed, ws, device)
     q.qmm_device_status(stream)
     t_bf16 = r0.elapsed_time(r1) / 1e3 / KR
+    t_bf16_plain = p0.elapsed_time(p1) / 1e3 / KR
     ms_per_step = elapsed / K * 1e3
     value = ws * 2 * wbytes_each / (elapsed / K) / 1e9
     clocks = clk.summary()
@@ -420,7 +436,9 @@ def run_native(args):
 
     # ---------------- other workloads of the path ----------------
     others = {}
-    if rank == 0 and not args.quick:
+    if ws == 1 and not args.quick:
+        # single-GPU runs only: the tensor-core cases use cluster-shared x
+        # tile copies, which stay within one GPU's own memory
         others = measure_other_workloads(torch, q, lib, r, stream, hbm_peak, tc_peak)
 
     # roofline of the dominant kernel (bf16 GEMV)
@@ -429,13 +447,18 @@ def run_native(args):
             "frac": achieved / hbm_peak, "traffic": recorded_traffic("gemv_bf16_4096x4096"),
             "kernel": "gemv_kernel<BF16> (k=n=4096)", "peak_source": f"{peak_src} hbm_gbs",
             "duration_us": t_bf16 * 1e6,
-            "duration_from": f"CUDA events around {KR} back-to-back launches of this kernel alone"}
+            "duration_from": f"CUDA events around {KR} back-to-back launches of this kernel alone",
+            "stream_ordered": {"duration_us": t_bf16_plain * 1e6,
+                               "achieved": wbytes_each / t_bf16_plain / 1e9,
+                               "frac": wbytes_each / t_bf16_plain / 1e9 / hbm_peak,
+                               "note": "the same kernel launched without QMM_FLAG_OVERLAP_PREV "
+                                       "(each launch waits for the previous one to finish)"}}
 
     line = {"metric": "effective weight GB/s", "value": value, "unit": "GB/s", "n_gpus": ws,
             "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
             "data": "synthetic",
-            "config": {"workload": "bf16+f16 GEMV k=n=4096, 1 token (one step = both GEMVs)",
+            "config": {"workload": HEADLINE_WORKLOAD,
                        "launch": ("stream-ordered" if args.no_overlap else
                                   "programmatic dependent launch (QMM_FLAG_OVERLAP_PREV | "
                                   "QMM_FLAG_X_READY): consecutive GEMVs on the same x; each streams "

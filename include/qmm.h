@@ -87,7 +87,8 @@ typedef enum qmm_status {
     QMM_ERR_CUDA = 7,            /* a CUDA runtime call failed (message has the CUDA error) */
     QMM_ERR_DEVICE_TIMEOUT = 8,  /* a kernel gave up waiting on a pipeline barrier (reported by qmm_device_status) */
     QMM_ERR_WORKSPACE = 9,       /* workspace given but smaller than qmm_workspace_bytes() */
-    QMM_ERR_UNSUPPORTED = 10,    /* current device is not compute capability 10.3, or the path cannot take the shape */
+    QMM_ERR_UNSUPPORTED = 10,    /* current device is not compute capability 10.3, the path cannot take the shape,
+                                    or a caller workspace is not device memory of the current device */
     QMM_ERR_BAD_ID = 11          /* an expert id outside [0, n_experts) (reported by qmm_device_status) */
 } qmm_status;
 
@@ -147,7 +148,11 @@ size_t qmm_weight_bytes(int fmt, int64_t k, int64_t n);
 int qmm_matmul(int fmt, const void *w, const float *x, int64_t k, int64_t n,
                int64_t n_tokens, float *y);
 
-/* Stream used by qmm_matmul on the calling host thread (a cudaStream_t). */
+/* Stream used by qmm_matmul on the calling host thread (a cudaStream_t).
+ * This is the chained model of rullama src/backend/dispatch/mod.rs
+ * ("Chained dispatchers"): work is appended to a stream that the caller
+ * owns and nothing waits for it; NULL selects the legacy default stream.
+ * The library keeps the handle only as this thread's setting. */
 void qmm_set_stream(void *stream);
 
 /* Full form: column tile, accumulate, path, workspace and stream.
@@ -156,15 +161,18 @@ void qmm_set_stream(void *stream);
  * Scratch: with a->workspace NULL the tensor-core path uses one grow-only
  * buffer per device owned by the library (growing it synchronizes the
  * device once); calls that may run concurrently on different streams, or
- * that are captured into a CUDA graph, pass their own workspace. */
+ * that are captured into a CUDA graph, pass their own workspace. A caller
+ * workspace must be 256-byte aligned device memory of the current device
+ * (checked with cudaPointerGetAttributes: QMM_ERR_UNSUPPORTED otherwise),
+ * since the tensor-core kernel reads its x tiles from it with copies that
+ * each pair of CTAs shares. */
 int qmm_matmul_ex(const qmm_args *a);
 
 /* Device scratch bytes qmm_matmul_ex needs for *a (0 for the GEMV path).
- * The MMA path keeps an fp16 copy of x (k padded to a multiple of 64) plus
- * one power-of-two scale per token; where it splits x into two fp16 terms
- * (16-bit weight formats, and K-quant / Q4_0 weights with k < 4096) it keeps
- * two copies: c * round256(n_tokens * kp * 2) + round256(n_tokens * 4) with
- * c = 1 or 2. Host only. */
+ * The MMA path splits x into two fp16 terms (high part and rounding
+ * remainder, k padded to a multiple of 64) scaled by one power of two per
+ * token: 2 * round256(n_tokens * kp * 2) + round256(n_tokens * 4) bytes.
+ * Host only. */
 size_t qmm_workspace_bytes(const qmm_args *a);
 
 /* Which kernel path qmm_matmul_ex would run for *a (a qmm_path value other
@@ -235,10 +243,17 @@ int qmm_matmul_experts(const qmm_args *a, const int32_t *ids, int64_t n_experts,
 int qmm_matmul_experts_affine(const qmm_args *a, const int32_t *ids, int64_t n_experts,
                               int64_t top_k, const void *scales, const void *biases);
 
-/* Standalone dequantization: out[j][i] = the fp32 value of weight i of row
- * j, bit-identical to the exact value rounded once to fp32 (only Q4_K's
- * d*sc*q - dmin*m rounds; every other product is exact). out is device
- * [n][k] fp32. Stream-ordered. */
+/* Standalone dequantization, the GPU counterpart of the ggml-exact CPU
+ * routines (`crate::gguf::quant::dequant_q4_0`, `dequant_q4_k`,
+ * `dequant_q6_k`, `dequant_q8_0`, `dequant_q5_0`) that the tests of rullama
+ * src/backend/matmul.rs and dispatch/mod.rs use as their reference:
+ * out[j][i] = the fp32 value of weight i of row j, bit-identical to the
+ * exact value rounded once to fp32 (only Q4_K's d*sc*q - dmin*m rounds;
+ * every other product is exact). w is device memory (16-byte aligned), n
+ * rows of qmm_weight_bytes(fmt, k, 1) bytes; out is caller-owned device
+ * [n][k] fp32 (4-byte aligned). Errors as for qmm_matmul_ex (affine formats:
+ * QMM_ERR_FORMAT, use qmm_dequant_affine); k == 0 or n == 0 enqueues
+ * nothing. Stream-ordered, no host synchronization. */
 int qmm_dequant(int fmt, const void *w, int64_t k, int64_t n, float *out, void *stream);
 
 /* Gate activations of gated FFN pairs. */
@@ -311,7 +326,11 @@ int qmm_device_status(void *stream);
  * between them) race on it. */
 int qmm_matmul_noalloc(const qmm_args *a);
 
-/* Message for the last non-OK status on this host thread ("" if none). */
+/* Message for the last non-OK status on this host thread ("" if none): the
+ * text that the rullama matmul_* dispatchers (src/backend/matmul.rs) carry
+ * in their `Err(RullamaError::Inference(..))` returns, here beside the
+ * numeric qmm_status. The string is owned by the library and stays valid
+ * until the next call on the same thread. */
 const char *qmm_last_error(void);
 
 /* ABI version (major * 100 + minor). */

@@ -74,10 +74,16 @@ def _bf16_bits_rne(values: np.ndarray) -> np.ndarray:
 
 
 def gen_weights(fmt: str, k: int, n: int, rng: np.random.Generator, **dist) -> np.ndarray:
-    """Packed weight bytes, shape [n * row_bytes(fmt, k)] uint8, row-major (row j = column j of W)."""
+    """Packed weight bytes, shape [n * row_bytes(fmt, k)] uint8, row-major (row j = column j of W).
+
+    Structure options: ``nonneg=True`` (bf16 / f16) draws |N(0, std)|;
+    ``dmin_zero=True`` (q4_k) stores dmin = +0, so every min term vanishes and
+    every weight is >= 0 (d and the codes stay as drawn)."""
     if fmt in ("bf16", "f16"):
         std = dist.get("std", 0.02)
         w = rng.normal(0.0, std, size=(n, k)).astype(np.float32)
+        if dist.get("nonneg"):
+            w = np.abs(w)
         if fmt == "bf16":
             bits = _bf16_bits_rne(w).astype("<u2")
         else:
@@ -97,6 +103,8 @@ def gen_weights(fmt: str, k: int, n: int, rng: np.random.Generator, **dist) -> n
         blk[..., 0:2] = _f16_bytes(rng.uniform(lo, hi, size=(n, nb)))
         blk[..., 2:4] = _f16_bytes(rng.uniform(lo, hi, size=(n, nb)))
         blk[..., 4:144] = rng.integers(0, 256, size=(n, nb, 140), dtype=np.uint8)
+        if dist.get("dmin_zero"):
+            blk[..., 2:4] = 0
         return blk.reshape(-1)
     if fmt == "q6_k":
         lo, hi = dist.get("d_range", (0.0005, 0.01))
@@ -122,6 +130,55 @@ def gen_weights(fmt: str, k: int, n: int, rng: np.random.Generator, **dist) -> n
         blk[..., 2:22] = rng.integers(0, 256, size=(n, nb, 20), dtype=np.uint8)
         return blk.reshape(-1)
     raise ValueError(f"unknown format {fmt!r}")
+
+
+# Byte values that put every code of a block at its format's zero point (the
+# code whose weight is 0 whatever the block's scale): Q4_0 nibbles 8 (0x88
+# bytes); Q8_0 codes 0; Q5_0 code 16 = nibble 0 with its fifth bit set (the
+# 4-byte high-bit word all ones); Q6_K code 32 = low nibble 0 with high bits
+# 0b10 (ql bytes 0x00, qh bytes 0xAA). Q4_K has no zero point (its codes are
+# unsigned with a separate min): there, codes 0 with dmin = +0 give weights
+# that are exactly 0 while d and the 6-bit scales stay nonzero.
+# (byte range within the block, value) per format; bf16 / f16 rows become +0.
+_ZERO_POINT_BYTES = {
+    "q4_0": [((2, 18), 0x88)],
+    "q8_0": [((2, 34), 0x00)],
+    "q5_0": [((2, 6), 0xFF), ((6, 22), 0x00)],
+    "q6_k": [((0, 128), 0x00), ((128, 192), 0xAA)],
+    "q4_k": [((2, 4), 0x00), ((16, 144), 0x00)],
+}
+
+
+def set_zero_point_rows(fmt: str, w: np.ndarray, k: int, rows) -> np.ndarray:
+    """Copy of packed weights w in which every code of the given rows sits at
+    the zero point (see _ZERO_POINT_BYTES); the rows' scales keep their drawn,
+    nonzero values, so those rows' weights are all exactly 0."""
+    rb = row_bytes(fmt, k)
+    out = np.array(w, dtype=np.uint8, copy=True).reshape(-1, rb)
+    rows = np.asarray(rows, dtype=np.int64)
+    if fmt in ("bf16", "f16"):
+        out[rows] = 0
+        return out.reshape(-1)
+    nb = BLOCK_BYTES[fmt]
+    blk = out.reshape(out.shape[0], -1, nb)
+    for (b0, b1), v in _ZERO_POINT_BYTES[fmt]:
+        blk[rows, :, b0:b1] = v
+    return blk.reshape(-1)
+
+
+def set_affine_zero_rows(bits: int, w: np.ndarray, scales: np.ndarray, biases: np.ndarray,
+                         k: int, rows):
+    """Copies of an affine matrix's arrays in which the given rows are what an
+    MLX-style quantizer stores for all-zero groups: codes 0, bias +0 and the
+    floor scale -1e-7 (as bf16 bits). Returns (w, scales, biases)."""
+    rows = np.asarray(rows, dtype=np.int64)
+    w = np.array(w, dtype=np.uint8, copy=True).reshape(scales.shape[0], -1)
+    sc = np.array(scales, dtype=np.uint16, copy=True)
+    bi = np.array(biases, dtype=np.uint16, copy=True)
+    w[rows] = 0
+    sc[rows] = _bf16_trunc(np.float32(-1e-7))
+    bi[rows] = 0
+    return w.reshape(-1), sc, bi
 
 
 def gen_ids(n_pos: int, top_k: int, n_experts: int, rng: np.random.Generator) -> np.ndarray:
@@ -186,10 +243,21 @@ def affine_workload(name: str, n_tokens: int | None = None, n: int | None = None
     return bits, k, n, w, scales, biases, x
 
 
-def gen_x(n_tokens: int, k: int, rng: np.random.Generator, dist: str = "normal") -> np.ndarray:
-    """Activations [n_tokens, k] fp32."""
+def gen_x(n_tokens: int, k: int, rng: np.random.Generator, dist: str = "normal",
+          value: float = 0.1) -> np.ndarray:
+    """Activations [n_tokens, k] fp32: "normal" N(0, 1), "uniform" U[-1, 1],
+    "abs_normal" |N(0, 1)| (every element positive), "constant" (every
+    element the fp32 nearest `value`), "constant_rows" (row t constant at
+    the fp32 nearest value * (t + 1))."""
     if dist == "uniform":
         return rng.uniform(-1.0, 1.0, size=(n_tokens, k)).astype(np.float32)
+    if dist == "abs_normal":
+        return np.abs(rng.normal(0.0, 1.0, size=(n_tokens, k))).astype(np.float32)
+    if dist == "constant":
+        return np.full((n_tokens, k), value, dtype=np.float32)
+    if dist == "constant_rows":
+        return (np.arange(1, n_tokens + 1, dtype=np.float64)[:, None] * value
+                * np.ones((1, k))).astype(np.float32)
     return rng.normal(0.0, 1.0, size=(n_tokens, k)).astype(np.float32)
 
 

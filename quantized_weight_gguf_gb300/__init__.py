@@ -117,6 +117,19 @@ def _check(status: int):
     return status
 
 
+def _keep_until_done(buf, stream):
+    """A per-call scratch tensor allocated on torch's current stream but used
+    by kernels on another stream: tell the caching allocator, so the memory
+    is not handed out again before that stream's work is done."""
+    if buf is None or stream is None or stream == 0:
+        return
+    import torch
+    s = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.ExternalStream(
+        int(getattr(stream, "cuda_stream", stream)), device=buf.device)
+    if s.cuda_stream != torch.cuda.current_stream(buf.device).cuda_stream:
+        buf.record_stream(s)
+
+
 def _stream(stream):
     if stream is None:
         import torch
@@ -247,6 +260,7 @@ def matmul(fmt, w, x, k: int, n: int, *, y=None, j_start=0, j_end=0, accumulate=
         a.workspace = ws.data_ptr()
         a.workspace_bytes = need
     qmm_matmul_ex(a)
+    _keep_until_done(ws, stream)
     return y
 
 
@@ -308,14 +322,16 @@ def matmul_affine(fmt, w, scales, biases, x, k: int, n: int, *, y=None, j_start=
         y = torch.empty((nt, n), dtype=torch.float32, device=x.device)
     a = make_args(fmt, w, x, y, k, n, nt, w_len=w.numel() * w.element_size(), j_start=j_start,
                   j_end=j_end, accumulate=accumulate, path=path, stream=stream, flags=flags)
+    own = None
     if workspace is None:
         need = qmm_workspace_bytes(a)
         if need:
-            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+            own = workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
             workspace_bytes = need
     if workspace is not None:
         a.workspace, a.workspace_bytes = _ptr(workspace), workspace_bytes
     qmm_matmul_affine(a, scales, biases)
+    _keep_until_done(own, stream)
     return y
 
 
@@ -346,4 +362,5 @@ def matmul_glu(act, fmt, w_gate, w_up, x, k: int, n: int, *, y=None, j_start=0, 
         ws = torch.empty(need, dtype=torch.uint8, device=x.device)
         a.workspace, a.workspace_bytes = ws.data_ptr(), need
     qmm_matmul_glu(a, w_up, act)
+    _keep_until_done(ws, stream)
     return y

@@ -173,6 +173,34 @@ int library_workspace(size_t need, void **out) {
 
 bool affine_fmt(int fmt) { return fmt == QMM_AFFINE4 || fmt == QMM_AFFINE8; }
 
+// A caller workspace for the tensor-core path: large enough, 256-byte
+// aligned, and device memory of the current device. The kernel reads its x
+// tiles from it with tensor copies that the two CTAs of a cluster share, so
+// the tensor map must cover this GPU's own memory only (not host, managed
+// or another device's memory).
+int check_mma_workspace(const void *ws, size_t have, size_t need) {
+    if (have < need)
+        return fail(QMM_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", have, need);
+    if (reinterpret_cast<uintptr_t>(ws) & 255u)
+        return fail(QMM_ERR_ALIGN, "workspace must be 256-byte aligned");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(QMM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    cudaPointerAttributes at;
+    e = cudaPointerGetAttributes(&at, ws);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return fail(QMM_ERR_UNSUPPORTED, "workspace is not CUDA device memory (%s)",
+                    cudaGetErrorString(e));
+    }
+    if (at.type != cudaMemoryTypeDevice || at.device != dev)
+        return fail(QMM_ERR_UNSUPPORTED,
+                    "workspace must be device memory of the current device %d (memory type %d, "
+                    "device %d)",
+                    dev, (int)at.type, at.device);
+    return QMM_OK;
+}
+
 // The product of every entry point. Affine formats come with their scale and
 // bias arrays (sc, bi), which only qmm_matmul_affine passes (affine_entry).
 int run(const qmm_args *a, const void *sc = nullptr, const void *bi = nullptr,
@@ -226,11 +254,8 @@ int run(const qmm_args *a, const void *sc = nullptr, const void *bi = nullptr,
     const size_t need = qmm::mma_workspace_bytes(a->fmt, a->n_tokens, a->k);
     void *ws = a->workspace;
     if (ws) {
-        if (a->workspace_bytes < need)
-            return fail(QMM_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", a->workspace_bytes,
-                        need);
-        if (reinterpret_cast<uintptr_t>(ws) & 255u)
-            return fail(QMM_ERR_ALIGN, "workspace must be 256-byte aligned");
+        st = check_mma_workspace(ws, a->workspace_bytes, need);
+        if (st != QMM_OK) return st;
     } else {
         st = library_workspace(need, &ws);
         if (st != QMM_OK) return st;
@@ -566,11 +591,8 @@ int qmm_matmul_glu(const qmm_args *a, const void *w_up, int act) {
     const size_t need = glu_scratch_bytes(a);
     void *ws = a->workspace;
     if (ws) {
-        if (a->workspace_bytes < need)
-            return fail(QMM_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", a->workspace_bytes,
-                        need);
-        if (reinterpret_cast<uintptr_t>(ws) & 255u)
-            return fail(QMM_ERR_ALIGN, "workspace must be 256-byte aligned");
+        st = check_mma_workspace(ws, a->workspace_bytes, need);
+        if (st != QMM_OK) return st;
     } else {
         st = library_workspace(need, &ws);
         if (st != QMM_OK) return st;

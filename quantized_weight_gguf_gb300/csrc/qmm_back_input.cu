@@ -8,10 +8,14 @@
 // threads owns a fixed unit of k (8 weights for 16-bit formats, one 32-weight
 // block / sub-block / quarter-half otherwise) and keeps that unit's dx partial
 // sums in registers; for every row it decodes the unit and adds dy[j] times
-// the weights. Codes stay exact: a byte permute builds 0.5 + q/256, so a unit
-// accumulates sum_j a_j (0.5 + q/256) with a_j = dy[j] * scale, plus the
-// per-unit sums of a_j that remove the carrier and the zero point / min
-// (e.g. Q4_K: dx = 256 acc - 128 sum a - sum dy dmin m).
+// the weights. Codes stay exact. Formats with a zero point z (Q4_0, Q5_0,
+// Q6_K, Q8_0) turn each code into q - z exactly (2^23 + q - (2^23 + z)) and
+// accumulate sum_j a_j (q - z) with a_j = dy[j] * scale, so rows whose codes
+// sit at the zero point add exactly 0. Q4_K codes ride the float 0.5 + q/256
+// that a byte permute builds, and the per-unit sums of a_j (accumulated in
+// the same order) remove the carrier and the min:
+// dx = 256 acc - (128 sum a + sum dy dmin m), exactly 0 for zero codes and
+// zero mins.
 // At the end the row groups of a CTA are summed in shared memory and the CTA
 // writes its partial dx; a second small kernel adds the partials of all CTAs in
 // a fixed order (deterministic) into dx.
@@ -55,7 +59,7 @@ struct BUnitK {
 template <int FMT>
 struct BAcc {
     float a[BUnitK<FMT>::value];
-    float s0, s1, s2, s3;  // carrier sums (per scale group) and Q4_K's min term
+    float s0, s1;  // Q4_K: sum of dy * d * sc (the carrier's offset) and of dy * dmin * m
 };
 
 __device__ __forceinline__ uint32_t bw_bfe(uint32_t a, uint32_t pos, uint32_t len) {
@@ -90,25 +94,25 @@ __device__ __forceinline__ void unit_axpy(uint32_t rowa, int u, float dyj, BAcc<
         uint32_t qw[4];
         lds_words_a2<4>(base + 2, qw);
         const float2 aa = make_float2(a, a);
+        const float2 zp = make_float2(-8388616.0f, -8388616.0f);  // -(2^23 + 8)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint32_t lo = qw[i] & 0x0F0F0F0Fu, hi = (qw[i] >> 4) & 0x0F0F0F0Fu;
             // element 4i + b: low nibble of byte 4i + b; element 16 + 4i + b: its high nibble
-            float2 r;
-            r = ffma2(make_float2(byte_half_plus<0>(lo), byte_half_plus<1>(lo)), aa,
-                      make_float2(st.a[4 * i], st.a[4 * i + 1]));
+            float2 r, f;
+            f = fadd2(make_float2(byte_magic23<0>(lo), byte_magic23<1>(lo)), zp);
+            r = ffma2(f, aa, make_float2(st.a[4 * i], st.a[4 * i + 1]));
             st.a[4 * i] = r.x; st.a[4 * i + 1] = r.y;
-            r = ffma2(make_float2(byte_half_plus<2>(lo), byte_half_plus<3>(lo)), aa,
-                      make_float2(st.a[4 * i + 2], st.a[4 * i + 3]));
+            f = fadd2(make_float2(byte_magic23<2>(lo), byte_magic23<3>(lo)), zp);
+            r = ffma2(f, aa, make_float2(st.a[4 * i + 2], st.a[4 * i + 3]));
             st.a[4 * i + 2] = r.x; st.a[4 * i + 3] = r.y;
-            r = ffma2(make_float2(byte_half_plus<0>(hi), byte_half_plus<1>(hi)), aa,
-                      make_float2(st.a[16 + 4 * i], st.a[16 + 4 * i + 1]));
+            f = fadd2(make_float2(byte_magic23<0>(hi), byte_magic23<1>(hi)), zp);
+            r = ffma2(f, aa, make_float2(st.a[16 + 4 * i], st.a[16 + 4 * i + 1]));
             st.a[16 + 4 * i] = r.x; st.a[16 + 4 * i + 1] = r.y;
-            r = ffma2(make_float2(byte_half_plus<2>(hi), byte_half_plus<3>(hi)), aa,
-                      make_float2(st.a[16 + 4 * i + 2], st.a[16 + 4 * i + 3]));
+            f = fadd2(make_float2(byte_magic23<2>(hi), byte_magic23<3>(hi)), zp);
+            r = ffma2(f, aa, make_float2(st.a[16 + 4 * i + 2], st.a[16 + 4 * i + 3]));
             st.a[16 + 4 * i + 2] = r.x; st.a[16 + 4 * i + 3] = r.y;
         }
-        st.s0 += a;
     } else if (FMT == F_Q4_K) {
         // unit u = sub-block s of super-block b; its 32 codes are the low
         // (s even) or high (s odd) nibbles of quant bytes 32 (s / 2) ..
@@ -169,27 +173,27 @@ __device__ __forceinline__ void unit_axpy(uint32_t rowa, int u, float dyj, BAcc<
         lds_words_a2<1>(base + 2, qh);
         lds_words_a2<4>(base + 6, qw);
         const float2 aa = make_float2(a, a);
+        const float2 zp = make_float2(-8388624.0f, -8388624.0f);  // -(2^23 + 16)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             // bits j of a 4-bit field of qh -> bit 4 of byte j
             const uint32_t hl = (((qh[0] >> (4 * i)) & 15u) * 0x02040810u) & 0x10101010u;
             const uint32_t hh = (((qh[0] >> (16 + 4 * i)) & 15u) * 0x02040810u) & 0x10101010u;
             const uint32_t lo = (qw[i] & 0x0F0F0F0Fu) | hl, hi = ((qw[i] >> 4) & 0x0F0F0F0Fu) | hh;
-            float2 r;
-            r = ffma2(make_float2(byte_half_plus<0>(lo), byte_half_plus<1>(lo)), aa,
-                      make_float2(st.a[4 * i], st.a[4 * i + 1]));
+            float2 r, f;
+            f = fadd2(make_float2(byte_magic23<0>(lo), byte_magic23<1>(lo)), zp);
+            r = ffma2(f, aa, make_float2(st.a[4 * i], st.a[4 * i + 1]));
             st.a[4 * i] = r.x; st.a[4 * i + 1] = r.y;
-            r = ffma2(make_float2(byte_half_plus<2>(lo), byte_half_plus<3>(lo)), aa,
-                      make_float2(st.a[4 * i + 2], st.a[4 * i + 3]));
+            f = fadd2(make_float2(byte_magic23<2>(lo), byte_magic23<3>(lo)), zp);
+            r = ffma2(f, aa, make_float2(st.a[4 * i + 2], st.a[4 * i + 3]));
             st.a[4 * i + 2] = r.x; st.a[4 * i + 3] = r.y;
-            r = ffma2(make_float2(byte_half_plus<0>(hi), byte_half_plus<1>(hi)), aa,
-                      make_float2(st.a[16 + 4 * i], st.a[16 + 4 * i + 1]));
+            f = fadd2(make_float2(byte_magic23<0>(hi), byte_magic23<1>(hi)), zp);
+            r = ffma2(f, aa, make_float2(st.a[16 + 4 * i], st.a[16 + 4 * i + 1]));
             st.a[16 + 4 * i] = r.x; st.a[16 + 4 * i + 1] = r.y;
-            r = ffma2(make_float2(byte_half_plus<2>(hi), byte_half_plus<3>(hi)), aa,
-                      make_float2(st.a[16 + 4 * i + 2], st.a[16 + 4 * i + 3]));
+            f = fadd2(make_float2(byte_magic23<2>(hi), byte_magic23<3>(hi)), zp);
+            r = ffma2(f, aa, make_float2(st.a[16 + 4 * i + 2], st.a[16 + 4 * i + 3]));
             st.a[16 + 4 * i + 2] = r.x; st.a[16 + 4 * i + 3] = r.y;
         }
-        st.s0 += a;
     } else {  // F_Q6_K
         // unit u: super-block b, half h, byte group gq; element 8 r + i is
         // weight 128 h + 32 r + 8 gq + i, with scale scales[8 h + 2 r + gq / 2]
@@ -220,19 +224,17 @@ __device__ __forceinline__ void unit_axpy(uint32_t rowa, int u, float dyj, BAcc<
             for (int r = 0; r < 4; ++r) {
                 const float2 aa = make_float2(ar[r], ar[r]);
                 const int e = 8 * r + 4 * wi;
-                float2 v;
-                v = ffma2(make_float2(byte_half_plus<0>(q[r]), byte_half_plus<1>(q[r])), aa,
-                          make_float2(st.a[e], st.a[e + 1]));
+                // q - 32 exactly as 2^23 + q - (2^23 + 32)
+                const float2 zp = make_float2(-8388640.0f, -8388640.0f);
+                float2 v, f;
+                f = fadd2(make_float2(byte_magic23<0>(q[r]), byte_magic23<1>(q[r])), zp);
+                v = ffma2(f, aa, make_float2(st.a[e], st.a[e + 1]));
                 st.a[e] = v.x; st.a[e + 1] = v.y;
-                v = ffma2(make_float2(byte_half_plus<2>(q[r]), byte_half_plus<3>(q[r])), aa,
-                          make_float2(st.a[e + 2], st.a[e + 3]));
+                f = fadd2(make_float2(byte_magic23<2>(q[r]), byte_magic23<3>(q[r])), zp);
+                v = ffma2(f, aa, make_float2(st.a[e + 2], st.a[e + 3]));
                 st.a[e + 2] = v.x; st.a[e + 3] = v.y;
             }
         }
-        st.s0 += ar[0];
-        st.s1 += ar[1];
-        st.s2 += ar[2];
-        st.s3 += ar[3];
     }
 }
 
@@ -243,16 +245,8 @@ __device__ __forceinline__ void unit_result(const BAcc<FMT> &st, int u, int e, f
     if (FMT == F_BF16 || FMT == F_F16) {
         v = st.a[e];
         kidx = 8 * (int64_t)u + e;
-    } else if (FMT == F_Q4_0) {
-        // sum a (q - 8) = 256 sum a (0.5 + q/256) - 136 sum a
-        v = fmaf(256.0f, st.a[e], -136.0f * st.s0);
-        kidx = 32 * (int64_t)u + e;
-    } else if (FMT == F_Q8_0) {
-        v = st.a[e];  // exact codes: no carrier
-        kidx = 32 * (int64_t)u + e;
-    } else if (FMT == F_Q5_0) {
-        // sum a (q - 16) = 256 sum a (0.5 + q/256) - 144 sum a
-        v = fmaf(256.0f, st.a[e], -144.0f * st.s0);
+    } else if (FMT == F_Q4_0 || FMT == F_Q8_0 || FMT == F_Q5_0) {
+        v = st.a[e];  // exact q - z: no carrier
         kidx = 32 * (int64_t)u + e;
     } else if (FMT == F_Q4_K) {
         // sum (a q - dy dm) = 256 sum a (0.5 + q/256) - 128 sum a - sum dy dm
@@ -260,9 +254,7 @@ __device__ __forceinline__ void unit_result(const BAcc<FMT> &st, int u, int e, f
         kidx = 32 * (int64_t)u + e;
     } else {
         const int r = e >> 3, i = e & 7;
-        const float sr = r == 0 ? st.s0 : (r == 1 ? st.s1 : (r == 2 ? st.s2 : st.s3));
-        // sum a (q - 32) = 256 sum a (0.5 + q/256) - 160 sum a
-        v = fmaf(256.0f, st.a[e], -160.0f * sr);
+        v = st.a[e];  // exact q - 32
         const int b = u >> 3, h = (u >> 2) & 1, gq = u & 3;
         kidx = 256 * (int64_t)b + 128 * h + 32 * r + 8 * gq + i;
     }
@@ -350,7 +342,7 @@ __global__ void __launch_bounds__(kBwThreads, 2) back_input_kernel(const BackPar
     BAcc<FMT> st;
 #pragma unroll
     for (int e = 0; e < UK; ++e) st.a[e] = 0.0f;
-    st.s0 = st.s1 = st.s2 = st.s3 = 0.0f;
+    st.s0 = st.s1 = 0.0f;
     bool failed = false;
     for (int s = 0; s < nst; ++s) {
         const int slot = s % NS;

@@ -11,11 +11,15 @@
 // memory and one warp per row reduces them in a fixed order (deterministic).
 //
 // Decoding keeps the integer codes exact and out of the fp pipe as far as
-// possible: a byte permute builds the float 0.5 + q/256 from a code q < 128
-// (q lands in mantissa bits 16..22), so the dot over a sub-block is
-// sum q x = 256 * sum (0.5 + q/256) x - 128 * sum x, with sum x over each
-// unit's sub-blocks computed once per thread. Q4_0 subtracts its zero point
-// exactly instead (2^23 + q - (2^23 + 8)), so an all-zero-point block gives 0.
+// possible. Codes with no zero point (Q4_K, affine 4-bit) ride the float
+// 0.5 + q/256 that a byte permute builds from q < 128 (q lands in mantissa
+// bits 16..22), so the dot over a sub-block is
+// sum q x = 256 * (sum (0.5 + q/256) x - 0.5 * sum x), where sum x is summed
+// once per thread in exactly the order and pairing of the carrier's fmas:
+// with every code 0 the carrier sum is then exactly half of it and the unit
+// gives exactly 0. Codes with a zero point z (Q4_0, Q5_0, Q6_K, Q8_0) become
+// q - z exactly (2^23 + q - (2^23 + z)), so a block whose codes all sit at
+// the zero point gives exactly 0 as well.
 //
 // Kernel variants (template VAR): the plain GEMV; expert-indexed (grid.y runs
 // one GEMV per (position, slot) on the selected expert slice); gated pairs
@@ -168,10 +172,25 @@ __device__ __forceinline__ int x_slot(int k, int U) {
 template <int FMT>
 struct UnitState {
     float xr[UnitK<FMT>::value];
-    float c0, c1, c2, c3;      // format-specific sums of x
+    float c0;                  // sum of the unit's x (carrier and affine formats)
     uint32_t p0, p1, p2, p3;   // format-specific bit positions
     uint32_t la, lb, lowgrp;
 };
+
+// sum of the unit's 32 x values in the order and pairing of a carrier dot:
+// the packed fmas accumulate elements 4m, 4m+1, 4m+2, 4m+3 (m = 0..7) in four
+// chains that are then added as (c0 + c1) + (c2 + c3). A carrier dot whose
+// codes are all 0 (every carrier 0.5) then equals exactly half of this sum.
+__device__ __forceinline__ float carrier_order_sum(const float (&xr)[32]) {
+    float c[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        c[r] = xr[r];
+#pragma unroll
+        for (int m = 1; m < 8; ++m) c[r] += xr[4 * m + r];
+    }
+    return (c[0] + c[1]) + (c[2] + c[3]);
+}
 
 template <int FMT>
 __device__ __forceinline__ void unit_init(UnitState<FMT> &st, const float *xs, int U, int u,
@@ -180,31 +199,20 @@ __device__ __forceinline__ void unit_init(UnitState<FMT> &st, const float *xs, i
     // element e of unit u sits at xs[e * (U + 1) + u]
 #pragma unroll
     for (int e = 0; e < UK; ++e) st.xr[e] = valid ? xs[e * (U + 1) + u] : 0.0f;
-    if (FMT == F_Q6_K) {
+    if constexpr (FMT == F_Q6_K) {
         const int gq = u & 3;
-        float s[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            s[r] = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) s[r] += st.xr[8 * r + i];
-        }
-        // sum (q - 32) x = 256 * sum (0.5 + q/256) x - 160 * sum x
-        st.c0 = -160.0f * s[0]; st.c1 = -160.0f * s[1];
-        st.c2 = -160.0f * s[2]; st.c3 = -160.0f * s[3];
         // scale byte of quarter r sits at byte 2r + (gq >> 1) of scales[8h .. 8h+7]
         st.p0 = 8 * (0 + (gq >> 1)); st.p1 = 8 * (2 + (gq >> 1));
         st.p2 = st.p0; st.p3 = st.p1;
-    } else if (FMT == F_Q5_0 || is_affine(FMT)) {
+    } else if constexpr (FMT == F_AFF8) {
         float sx = 0.0f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) sx += st.xr[i];
         st.c0 = sx;
-    } else if (FMT == F_Q4_K) {
-        float sx = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sx += st.xr[i];
-        st.c0 = sx;
+    } else if constexpr (FMT == F_Q4_K || FMT == F_AFF4) {
+        st.c0 = carrier_order_sum(st.xr);
+    }
+    if constexpr (FMT == F_Q4_K) {
         const int sb = u & 7;  // sub-block within the super-block
         st.lowgrp = sb < 4;
         const int t = sb >= 4 ? sb - 4 : 0;
@@ -306,8 +314,10 @@ __device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<
         }
         const float a = (a0.x + a0.y) + (a1.x + a1.y);
         const float ds = d * (float)sc, dm = dmin * (float)m;
-        // ds * sum q x - dm * sum x, with sum q x = 256 * a - 128 * sum x
-        return fmaf(256.0f * ds, a, -fmaf(128.0f, ds, dm) * st.c0);
+        // ds * sum q x - dm * sum x, with sum q x = 256 * (a - sum x / 2);
+        // a - sum x / 2 is exactly 0 when every code is 0
+        const float t = fmaf(-0.5f, st.c0, a);
+        return fmaf(256.0f * ds, t, -dm * st.c0);
     } else if (FMT == F_Q8_0) {
         // codes are signed bytes: flipping the top bit gives q + 128 unsigned,
         // 2^23 + (q + 128) - (2^23 + 128) = q exactly
@@ -327,13 +337,14 @@ __device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<
         }
         return d * ((a0.x + a0.y) + (a1.x + a1.y));
     } else if (FMT == F_Q5_0) {
-        // 5-bit codes (< 128): nibble | fifth bit spread to bit 4 of each byte,
-        // then the 0.5 + q/256 permute; sum (q - 16) x = 256 a - 144 sum x
+        // 5-bit codes: nibble | fifth bit spread to bit 4 of each byte, then
+        // q - 16 exactly as 2^23 + q - (2^23 + 16)
         const uint32_t base = rowa + 22u * u;
         const float d = f16_bits_to_f32(lds16(base));
         uint32_t qh[1], qw[4];
         lds_words_a2<1>(base + 2, qh);
         lds_words_a2<4>(base + 6, qw);
+        const float2 zp = make_float2(-8388624.0f, -8388624.0f);  // -(2^23 + 16)
         float2 a0 = make_float2(0.f, 0.f), a1 = a0;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -341,17 +352,17 @@ __device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<
             const uint32_t hl = (((qh[0] >> (4 * i)) & 15u) * 0x02040810u) & 0x10101010u;
             const uint32_t hh = (((qh[0] >> (16 + 4 * i)) & 15u) * 0x02040810u) & 0x10101010u;
             const uint32_t lo = (qw[i] & 0x0F0F0F0Fu) | hl, hi = ((qw[i] >> 4) & 0x0F0F0F0Fu) | hh;
-            a0 = ffma2(make_float2(byte_half_plus<0>(lo), byte_half_plus<1>(lo)),
-                       make_float2(st.xr[4 * i], st.xr[4 * i + 1]), a0);
-            a1 = ffma2(make_float2(byte_half_plus<2>(lo), byte_half_plus<3>(lo)),
-                       make_float2(st.xr[4 * i + 2], st.xr[4 * i + 3]), a1);
-            a0 = ffma2(make_float2(byte_half_plus<0>(hi), byte_half_plus<1>(hi)),
-                       make_float2(st.xr[16 + 4 * i], st.xr[16 + 4 * i + 1]), a0);
-            a1 = ffma2(make_float2(byte_half_plus<2>(hi), byte_half_plus<3>(hi)),
-                       make_float2(st.xr[16 + 4 * i + 2], st.xr[16 + 4 * i + 3]), a1);
+            float2 f;
+            f = fadd2(make_float2(byte_magic23<0>(lo), byte_magic23<1>(lo)), zp);
+            a0 = ffma2(f, make_float2(st.xr[4 * i], st.xr[4 * i + 1]), a0);
+            f = fadd2(make_float2(byte_magic23<2>(lo), byte_magic23<3>(lo)), zp);
+            a1 = ffma2(f, make_float2(st.xr[4 * i + 2], st.xr[4 * i + 3]), a1);
+            f = fadd2(make_float2(byte_magic23<0>(hi), byte_magic23<1>(hi)), zp);
+            a0 = ffma2(f, make_float2(st.xr[16 + 4 * i], st.xr[16 + 4 * i + 1]), a0);
+            f = fadd2(make_float2(byte_magic23<2>(hi), byte_magic23<3>(hi)), zp);
+            a1 = ffma2(f, make_float2(st.xr[16 + 4 * i + 2], st.xr[16 + 4 * i + 3]), a1);
         }
-        const float a = (a0.x + a0.y) + (a1.x + a1.y);
-        return d * fmaf(256.0f, a, -144.0f * st.c0);
+        return d * ((a0.x + a0.y) + (a1.x + a1.y));
     } else {  // F_Q6_K
         const int b = u >> 3, h = (u >> 2) & 1, gq = u & 3;
         const uint32_t sb = rowa + 210u * b;
@@ -361,6 +372,8 @@ __device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<
         lds_words_a2<2>(sb + 128u + 32u * h + 8u * gq, H);
         lds_words_a2<2>(sb + 192u + 8u * h, S);
         const float d = f16_bits_to_f32(lds16(sb + 208u));
+        // codes q - 32 exactly as 2^23 + q - (2^23 + 32)
+        const float2 zp = make_float2(-8388640.0f, -8388640.0f);
         float2 acc[4][2];
 #pragma unroll
         for (int r = 0; r < 4; ++r) acc[r][0] = acc[r][1] = make_float2(0.f, 0.f);
@@ -373,22 +386,21 @@ __device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<
                 ((B[wi] >> 4) & 0x0F0F0F0Fu) | ((H[wi] >> 2) & 0x30303030u)};
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
-                acc[r][0] = ffma2(make_float2(byte_half_plus<0>(q[r]), byte_half_plus<1>(q[r])),
-                                  make_float2(st.xr[8 * r + 4 * wi], st.xr[8 * r + 4 * wi + 1]),
+                const float2 f0 = fadd2(make_float2(byte_magic23<0>(q[r]), byte_magic23<1>(q[r])), zp);
+                const float2 f1 = fadd2(make_float2(byte_magic23<2>(q[r]), byte_magic23<3>(q[r])), zp);
+                acc[r][0] = ffma2(f0, make_float2(st.xr[8 * r + 4 * wi], st.xr[8 * r + 4 * wi + 1]),
                                   acc[r][0]);
-                acc[r][1] = ffma2(make_float2(byte_half_plus<2>(q[r]), byte_half_plus<3>(q[r])),
-                                  make_float2(st.xr[8 * r + 4 * wi + 2], st.xr[8 * r + 4 * wi + 3]),
+                acc[r][1] = ffma2(f1, make_float2(st.xr[8 * r + 4 * wi + 2], st.xr[8 * r + 4 * wi + 3]),
                                   acc[r][1]);
             }
         }
-        const float cr[4] = {st.c0, st.c1, st.c2, st.c3};
         const uint32_t pr[4] = {st.p0, st.p1, st.p2, st.p3};
         float sum = 0.0f;
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const float a = (acc[r][0].x + acc[r][0].y) + (acc[r][1].x + acc[r][1].y);
             const float sc = (float)bfe_s(S[r >> 1], pr[r]);
-            sum = fmaf(sc, fmaf(256.0f, a, cr[r]), sum);
+            sum = fmaf(sc, a, sum);
         }
         return d * sum;
     }
@@ -407,8 +419,9 @@ __device__ __forceinline__ float unit_dot_aff(uint32_t rowa, uint32_t auxa, uint
     if (FMT == F_AFF4) {
         // word i holds elements 8i .. 8i+7, lowest nibble first: byte j of the
         // low-nibble mask is element 8i + 2j, of the high-nibble mask 8i + 2j + 1;
-        // codes ride the exact carrier 0.5 + q/256 and
-        // sum q x = 256 * sum (0.5 + q/256) x - 128 * sum x
+        // codes ride the exact carrier 0.5 + q/256 (element 4m + r lands in
+        // chain r, as in carrier_order_sum) and
+        // sum q x = 256 * (sum (0.5 + q/256) x - sum x / 2)
         const uint4 v = lds128(rowa + 16u * u);
         const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -424,7 +437,9 @@ __device__ __forceinline__ float unit_dot_aff(uint32_t rowa, uint32_t auxa, uint
                        make_float2(st.xr[8 * i + 6], st.xr[8 * i + 7]), a1);
         }
         const float a = (a0.x + a0.y) + (a1.x + a1.y);
-        return fmaf(256.0f * sc, a, fmaf(-128.0f, sc, bi) * st.c0);
+        // exactly 0 for a group of zero codes with a zero bias
+        const float t = fmaf(-0.5f, st.c0, a);
+        return fmaf(256.0f * sc, t, bi * st.c0);
     } else {
         // 8-bit codes: element 4i + j is byte j of word i; 2^23 + q - 2^23 = q exactly
         const uint4 v0 = lds128(rowa + 32u * u), v1 = lds128(rowa + 32u * u + 16u);

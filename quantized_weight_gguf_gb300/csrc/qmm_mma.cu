@@ -94,12 +94,17 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const float *__restrict__
 static int64_t kpad(int64_t k) { return (k + kBK - 1) / kBK * kBK; }
 static size_t round256(size_t v) { return (v + 255) & ~(size_t)255; }
 
+// Precision mode of a call. x is always split into two fp16 terms (about 22
+// significant bits), so its rounding cannot add up over k whatever x holds
+// (a single fp16 copy errs by up to 2^-12 per element, coherently for
+// constant or repeated activations: 2.4e-4 of sum |x w| for x = 0.1). W is
+// rounded once to fp16 (16-bit formats are exact in fp16 within its range);
+// for k < 1024 it is split too, since fewer products average its rounding.
 int mma_mode(int fmt, int64_t k) {
-    if (fmt == F_BF16 || fmt == F_F16) return 2;  // W is fp16-exact: split x only
+    if (fmt == F_BF16 || fmt == F_F16) return 2;
     // affine rows take the raw-tile path in whole 256-wide slices; other k
     // decode from registers with both operands split
     if (is_affine(fmt) && k % 256 != 0) return 3;
-    if (k >= 4096) return 1;
     if (k >= 1024) return 2;
     return 3;
 }

@@ -21,10 +21,10 @@ int mma_clusters(const DeviceInfo &dev) {
         q.attrs = attr;
         q.numAttrs = 1;
         int v = 0;
-        if (cudaFuncSetAttribute(mma_kernel<F_Q4_K, 256, 1>,
+        if (cudaFuncSetAttribute(mma_kernel<F_Q4_K, 256, 2>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)MmaCfg<256, kRawBytes>::kSmem) != cudaSuccess ||
-            cudaOccupancyMaxActiveClusters(&v, mma_kernel<F_Q4_K, 256, 1>, &q) != cudaSuccess ||
+            cudaOccupancyMaxActiveClusters(&v, mma_kernel<F_Q4_K, 256, 2>, &q) != cudaSuccess ||
             v <= 0) {
             (void)cudaGetLastError();
             v = dev.sm_count / 2;

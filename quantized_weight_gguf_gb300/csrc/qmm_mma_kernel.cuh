@@ -1022,7 +1022,6 @@ cudaError_t launch_fmt(int mode, int bn, const Maps &mp, const MmaAffParams &p,
                        const DeviceInfo &dev, cudaStream_t s) {
     constexpr bool quant = FMT != F_BF16 && FMT != F_F16;
     if (mode == 2) return launch_bn<FMT, 2>(bn, mp, p, dev, s);
-    if (quant && mode == 1) return launch_bn<FMT, quant ? 1 : 2>(bn, mp, p, dev, s);
     if (quant && mode == 3) return launch_bn<FMT, quant ? 3 : 2>(bn, mp, p, dev, s);
     return cudaErrorInvalidValue;
 }

@@ -111,7 +111,8 @@ def test_path_policy_and_workspace(lib):
     assert q.qmm_workspace_bytes(a) == 0
     a = _args(k=4096, n=14336, n_tokens=512)
     assert q.qmm_select_path(a) == q.PATH_MMA
-    assert q.qmm_workspace_bytes(a) == 512 * 4096 * 2 + 2048
+    # x is always split into two fp16 terms (high part and remainder)
+    assert q.qmm_workspace_bytes(a) == 2 * 512 * 4096 * 2 + 2048
     # 16-bit weights split x into two fp16 terms; k is padded to 64 in the copies
     a = _args(fmt="bf16", k=40, n=8, n_tokens=3)
     assert q.qmm_workspace_bytes(a) == 2 * ((3 * 64 * 2 + 255) // 256) * 256 + 256
@@ -206,7 +207,7 @@ def test_affine_sizes_and_policy(lib):
     assert q.qmm_select_path(a) == q.PATH_GEMV and q.qmm_workspace_bytes(a) == 0
     a = _args(fmt="affine8", k=4096, n=14336, n_tokens=64)
     assert q.qmm_select_path(a) == q.PATH_MMA
-    assert q.qmm_workspace_bytes(a) == 64 * 4096 * 2 + 256
+    assert q.qmm_workspace_bytes(a) == 2 * 64 * 4096 * 2 + 256
 
 
 @pytest.mark.parametrize("fn,kw,sb,status", [
@@ -276,7 +277,7 @@ def test_glu_workspace_and_empty_work(lib):
     assert q.qmm_glu_workspace_bytes(_args(k=4096, n=14336)) == 0          # fused GEMV
     a = _args(k=4096, n=1000, n_tokens=8)
     one = (8 * 1000 * 4 + 255) // 256 * 256
-    assert q.qmm_glu_workspace_bytes(a) == 2 * one + 8 * 4096 * 2 + 256
+    assert q.qmm_glu_workspace_bytes(a) == 2 * one + 2 * 8 * 4096 * 2 + 256
     assert q.qmm_glu_workspace_bytes(_args(fmt="affine4", k=128)) == 0
     assert q.qmm_matmul_glu(_args(j_start=3, j_end=3), None, 1) == 0
 

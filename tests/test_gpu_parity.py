@@ -387,3 +387,34 @@ def test_gemv_largest_k(fmt, k):
     y = run(fmt, w, x, k, n, path=q.PATH_GEMV)
     y_ref, s_ref = oracle.matmul(fmt, w, x, k, n)
     assert_parity(y, y_ref, s_ref, f"gemv {fmt} k={k}")
+
+
+def test_workspace_must_be_device_memory_of_this_gpu():
+    """The tensor-core path reads its x tiles from the workspace with copies
+    shared by a pair of CTAs: a caller workspace in host memory (pinned or
+    pageable) is rejected on the host with QMM_ERR_UNSUPPORTED, nothing
+    enqueued; device memory of the current GPU is taken."""
+    import ctypes
+    fmt, k, n, nt = "q4_k", 1024, 256, 8
+    rng = np.random.default_rng(17)
+    w = qmm_synth.gen_weights(fmt, k, n, rng)
+    x = qmm_synth.gen_x(nt, k, rng)
+    wd, xd = _dev(w), _dev(x)
+    y = torch.zeros((nt, n), device=DEV)
+    a = q.make_args(fmt, wd, xd, y, k, n, nt, path=q.PATH_MMA)
+    need = q.qmm_workspace_bytes(a)
+    pinned = torch.empty(need + 256, dtype=torch.uint8).pin_memory()
+    pageable = np.empty(need + 256, np.uint8)
+    for base in (pinned.data_ptr(), pageable.ctypes.data):
+        a.workspace, a.workspace_bytes = (base + 255) // 256 * 256, need
+        assert q.load().qmm_matmul_ex(ctypes.byref(a)) == 10
+        assert "device memory" in q.qmm_last_error()
+    torch.cuda.synchronize()
+    assert (y == 0).all()
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), need
+    q.qmm_matmul_ex(a)
+    torch.cuda.synchronize()
+    q.qmm_device_status()
+    y_ref, s_ref = oracle.matmul(fmt, w, x, k, n)
+    assert_parity(y.cpu().numpy(), y_ref, s_ref, "device workspace")

@@ -1,0 +1,141 @@
+"""GPU parity of the tensor-core (N-token) path on structured activations and
+weights, through the C ABI, against the oracle element by element: per
+output |y - y_ref| <= 1e-4 * sum_i |x_i w_ij| and cosine >= 0.9999.
+
+Random N(0, 1) activations let fp16 rounding errors cancel over k; these
+cases do not. A constant row of x (0.1, 1/3) rounds every element the same
+way, so a single fp16 copy of x would err coherently by up to 2^-12 of
+sum |x w| (2.4e-4 for x = 0.1 after the per-token power-of-two scaling),
+above the bar at any k. All-positive x with all-nonnegative weights (Q4_K
+with every min 0, BF16 with |w|) makes every product the same sign. The
+path splits x into two fp16 terms, so these must pass like random inputs
+(the same guard against easy passes as the structured cases of moeflux
+tests/graph_diff_oracle.rs and rullama matmul.rs `f16_matmul_3x4_eye`)."""
+import numpy as np
+import pytest
+
+import oracle
+import qmm_synth
+
+torch = pytest.importorskip("torch")
+import quantized_weight_gguf_gb300 as q  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from quantized_weight_gguf_gb300 import build_lib
+    build_lib.build()
+    q.load()
+    oracle.build()
+    yield
+    q.qmm_device_status()
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _mma(fmt, w, x, k, n):
+    out = q.matmul(fmt, _dev(w), _dev(x), k, n, path=q.PATH_MMA)
+    torch.cuda.synchronize()
+    q.qmm_device_status()
+    return out.cpu().numpy()
+
+
+def _assert(y, y_ref, s_ref, what):
+    ok, worst, cos, msg = oracle.check(y, y_ref, s_ref)
+    assert ok, f"{what}: {msg}"
+    return worst
+
+
+@pytest.mark.parametrize("nt", [8, 64, 512])
+@pytest.mark.parametrize("k,value", [(4096, 0.1), (16384, 1.0 / 3.0)])
+def test_q4_k_constant_activations(k, value, nt):
+    """Every element of every token row equal: the coherent case."""
+    n = 320
+    rng = np.random.default_rng(k + nt)
+    w = qmm_synth.gen_weights("q4_k", k, n, rng)
+    x = qmm_synth.gen_x(nt, k, rng, "constant", value)
+    y = _mma("q4_k", w, x, k, n)
+    y_ref, s_ref = oracle.matmul_blas("q4_k", w, x, k, n)
+    _assert(y, y_ref, s_ref, f"q4_k k={k} N={nt} x={value}")
+
+
+@pytest.mark.parametrize("nt", [8, 64])
+def test_q4_k_constant_rows_of_different_values(nt):
+    """Row t constant at 0.1 (t + 1): every token's own scale and rounding."""
+    k, n = 4096, 300
+    rng = np.random.default_rng(91 + nt)
+    w = qmm_synth.gen_weights("q4_k", k, n, rng)
+    x = qmm_synth.gen_x(nt, k, rng, "constant_rows", 0.1)
+    y = _mma("q4_k", w, x, k, n)
+    y_ref, s_ref = oracle.matmul_blas("q4_k", w, x, k, n)
+    _assert(y, y_ref, s_ref, f"q4_k constant rows N={nt}")
+
+
+@pytest.mark.parametrize("nt", [8, 64, 512])
+def test_q4_k_nonnegative_weights_and_activations(nt):
+    """dmin = 0 (w = d sc q >= 0) and x = |N(0, 1)|: no sign cancellation."""
+    k, n = 4096, 320
+    rng = np.random.default_rng(7 * nt)
+    w = qmm_synth.gen_weights("q4_k", k, n, rng, dmin_zero=True)
+    x = qmm_synth.gen_x(nt, k, rng, "abs_normal")
+    y = _mma("q4_k", w, x, k, n)
+    y_ref, s_ref = oracle.matmul_blas("q4_k", w, x, k, n)
+    assert (y_ref >= 0).all()
+    _assert(y, y_ref, s_ref, f"q4_k nonneg N={nt}")
+
+
+@pytest.mark.parametrize("nt", [8, 64])
+def test_bf16_nonnegative_weights_and_activations(nt):
+    k, n = 4096, 300
+    rng = np.random.default_rng(11 * nt)
+    w = qmm_synth.gen_weights("bf16", k, n, rng, nonneg=True)
+    x = qmm_synth.gen_x(nt, k, rng, "abs_normal")
+    y = _mma("bf16", w, x, k, n)
+    y_ref, s_ref = oracle.matmul_blas("bf16", w, x, k, n)
+    _assert(y, y_ref, s_ref, f"bf16 nonneg N={nt}")
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0", "q5_0", "q6_k", "f16"])
+@pytest.mark.parametrize("k", [1024, 4096])
+def test_other_formats_constant_activations(fmt, k):
+    n, nt = 300, 64
+    rng = np.random.default_rng(k + len(fmt))
+    w = qmm_synth.gen_weights(fmt, k, n, rng)
+    x = qmm_synth.gen_x(nt, k, rng, "constant", 1.0 / 3.0)
+    y = _mma(fmt, w, x, k, n)
+    y_ref, s_ref = oracle.matmul_blas(fmt, w, x, k, n)
+    _assert(y, y_ref, s_ref, f"{fmt} k={k} constant x")
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_affine_constant_activations(bits):
+    k, n, nt = 4096, 300, 64
+    rng = np.random.default_rng(40 + bits)
+    w, sc, bi = qmm_synth.gen_affine(bits, k, n, rng)
+    x = qmm_synth.gen_x(nt, k, rng, "constant", 0.1)
+    y = q.matmul_affine(f"affine{bits}", _dev(w), _dev(sc.view(np.int16)), _dev(bi.view(np.int16)),
+                        _dev(x), k, n, path=q.PATH_MMA)
+    torch.cuda.synchronize()
+    q.qmm_device_status()
+    y_ref, s_ref = oracle.matmul_affine_blas(bits, w, sc, bi, x, k, n)
+    _assert(y.cpu().numpy(), y_ref, s_ref, f"affine{bits} constant x")
+
+
+@pytest.mark.parametrize("fmt", ["q4_k", "q6_k"])
+def test_gemv_constant_activations(fmt):
+    """The one-token path accumulates in fp32 from exact codes: constant x
+    holds the bar too."""
+    k, n = 4096, 1000
+    rng = np.random.default_rng(3 + len(fmt))
+    w = qmm_synth.gen_weights(fmt, k, n, rng)
+    x = qmm_synth.gen_x(1, k, rng, "constant", 0.1)
+    y = q.matmul(fmt, _dev(w), _dev(x), k, n, path=q.PATH_GEMV)
+    torch.cuda.synchronize()
+    q.qmm_device_status()
+    y_ref, s_ref = oracle.matmul(fmt, w, x, k, n)
+    _assert(y.cpu().numpy(), y_ref, s_ref, f"gemv {fmt} constant x")
