@@ -132,18 +132,13 @@ __host__ GemvParamsOf<FMT, VAR> params_of(const GemvHostParams &h) {
 
 
 // Weights per unit: a 16-byte chunk for 16-bit formats (lane-contiguous in
-// shared memory), a 32-weight block for Q4_0, a 32-weight sub-block for Q4_K
-// and a 32-weight quarter-half for Q6_K.
+// shared memory), a 32-weight block for Q4_0, Q8_0 and Q5_0, a 32-weight
+// sub-block for Q4_K and a 32-weight quarter-half for Q6_K.
 template <int FMT>
 struct UnitK {
     static constexpr int value = (FMT == F_BF16 || FMT == F_F16) ? 8 : 32;
 };
 
-__device__ __forceinline__ uint32_t bfe(uint32_t a, uint32_t pos, uint32_t len) {
-    uint32_t d;
-    asm("bfe.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(pos), "r"(len));
-    return d;
-}
 __device__ __forceinline__ int32_t bfe_s(uint32_t a, uint32_t pos) {
     int32_t d;
     asm("bfe.s32 %0, %1, %2, 8;" : "=r"(d) : "r"(a), "r"(pos));
@@ -173,21 +168,22 @@ template <int FMT>
 struct UnitState {
     float xr[UnitK<FMT>::value];
     float c0;                  // sum of the unit's x (carrier and affine formats)
-    uint32_t p0, p1, p2, p3;   // format-specific bit positions
-    uint32_t la, lb, lowgrp;
+    uint32_t p0, p1, p2, p3;   // format-specific bit positions / byte selectors
+    uint32_t lowgrp;
 };
 
 // sum of the unit's 32 x values in the order and pairing of a carrier dot:
 // the packed fmas accumulate elements 4m, 4m+1, 4m+2, 4m+3 (m = 0..7) in four
 // chains that are then added as (c0 + c1) + (c2 + c3). A carrier dot whose
 // codes are all 0 (every carrier 0.5) then equals exactly half of this sum.
-__device__ __forceinline__ float carrier_order_sum(const float (&xr)[32]) {
+template <int N>
+__device__ __forceinline__ float carrier_order_sum(const float (&xr)[N], int off = 0) {
     float c[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        c[r] = xr[r];
+        c[r] = xr[off + r];
 #pragma unroll
-        for (int m = 1; m < 8; ++m) c[r] += xr[4 * m + r];
+        for (int m = 1; m < 8; ++m) c[r] += xr[off + 4 * m + r];
     }
     return (c[0] + c[1]) + (c[2] + c[3]);
 }
@@ -209,22 +205,23 @@ __device__ __forceinline__ void unit_init(UnitState<FMT> &st, const float *xs, i
 #pragma unroll
         for (int i = 0; i < 32; ++i) sx += st.xr[i];
         st.c0 = sx;
-    } else if constexpr (FMT == F_Q4_K || FMT == F_AFF4) {
+    } else if constexpr (FMT == F_AFF4) {
         st.c0 = carrier_order_sum(st.xr);
-    }
-    if constexpr (FMT == F_Q4_K) {
+    } else if constexpr (FMT == F_Q4_K) {
+        st.c0 = carrier_order_sum(st.xr);
+        // 6-bit scale and min of sub-block s gathered into bytes 0, 1 of a
+        // word from the header words y (scales[0..3]), z (scales[4..7]) and
+        // w (scales[8..11]):
+        //   s < 4:  sc = y byte s & 63, m = z byte s & 63;
+        //   s >= 4 (t = s - 4): sc = w byte t & 15 | (y byte t >> 6) << 4,
+        //                       m = w byte t >> 4 | (z byte t >> 6) << 4.
         const int sb = u & 7;  // sub-block within the super-block
         st.lowgrp = sb < 4;
-        const int t = sb >= 4 ? sb - 4 : 0;
-        // sub-block s < 4: scale = bits 8s..8s+5 of word 0, min = same bits of word 1;
-        // s >= 4 (t = s - 4): scale = bits 8t..8t+3 of word 2 | (bits 8t+6..8t+7 of word 0) << 4,
-        //                     min = bits 8t+4..8t+7 of word 2 | (bits 8t+6..8t+7 of word 1) << 4.
-        st.la = st.lowgrp ? 6u : 4u;
-        st.lb = st.lowgrp ? 0u : 2u;
-        st.p0 = st.lowgrp ? 8 * sb : 8 * t;       // scale, field A
-        st.p1 = st.lowgrp ? 8 * sb : 8 * t + 4;   // min, field A
-        st.p2 = 8 * t + 6;                        // top bits, field B
-        st.p3 = (sb & 1) ? 4u : 0u;               // nibble of the quant bytes
+        const uint32_t t = st.lowgrp ? (uint32_t)sb : (uint32_t)sb - 4u;
+        st.p0 = t | ((t + 4u) << 4);                  // byte selector (field A, top bits)
+        st.p1 = st.lowgrp ? 0x3F3Fu : 0x0F0Fu;       // mask of field A
+        st.p2 = st.lowgrp ? 0u : 0x3030u;            // mask of the top bits
+        st.p3 = (sb & 1) ? 4u : 0u;                  // nibble of the quant bytes
     }
 }
 
@@ -296,12 +293,16 @@ __device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<
         const uint4 hdr = lds128(sb);
         const uint4 q0 = lds128(sb + 16u + 32u * c);
         const uint4 q1 = lds128(sb + 32u + 32u * c);
-        const float d = f16_bits_to_f32(hdr.x & 0xFFFFu);
-        const float dmin = f16_bits_to_f32(hdr.x >> 16);
-        const uint32_t srcA_sc = st.lowgrp ? hdr.y : hdr.w;
-        const uint32_t srcA_m = st.lowgrp ? hdr.z : hdr.w;
-        const uint32_t sc = bfe(srcA_sc, st.p0, st.la) | (bfe(hdr.y, st.p2, st.lb) << 4);
-        const uint32_t m = bfe(srcA_m, st.p1, st.la) | (bfe(hdr.z, st.p2, st.lb) << 4);
+        // [sc, m] in bytes 0 and 1 (see unit_init)
+        const uint32_t fa = prmt(st.lowgrp ? hdr.y : hdr.w, st.lowgrp ? hdr.z : hdr.w >> 4, st.p0);
+        const uint32_t fb = prmt(hdr.y, hdr.z, st.p0) >> 2;
+        const uint32_t scm = (fa & st.p1) | (fb & st.p2);
+        // v as the float 2^23 + v, then (2^23 + v) s - 2^23 s = v s exactly
+        // (at most 17 significant bits): (256 d sc, dmin m) in one packed fma
+        const float2 sd = make_float2(256.0f * f16_bits_to_f32(hdr.x & 0xFFFFu),
+                                      f16_bits_to_f32(hdr.x >> 16));
+        const float2 dsm = ffma2(make_float2(byte_magic23<0>(scm), byte_magic23<1>(scm)), sd,
+                                 make_float2(-8388608.0f * sd.x, -8388608.0f * sd.y));
         const uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
         float2 a0 = make_float2(0.f, 0.f), a1 = a0;
 #pragma unroll
@@ -313,11 +314,10 @@ __device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<
                        make_float2(st.xr[4 * i + 2], st.xr[4 * i + 3]), a1);
         }
         const float a = (a0.x + a0.y) + (a1.x + a1.y);
-        const float ds = d * (float)sc, dm = dmin * (float)m;
-        // ds * sum q x - dm * sum x, with sum q x = 256 * (a - sum x / 2);
+        // d sc * sum q x - dmin m * sum x, with sum q x = 256 * (a - sum x / 2);
         // a - sum x / 2 is exactly 0 when every code is 0
         const float t = fmaf(-0.5f, st.c0, a);
-        return fmaf(256.0f * ds, t, -dm * st.c0);
+        return fmaf(dsm.x, t, -dsm.y * st.c0);
     } else if (FMT == F_Q8_0) {
         // codes are signed bytes: flipping the top bit gives q + 128 unsigned,
         // 2^23 + (q + 128) - (2^23 + 128) = q exactly
@@ -682,37 +682,58 @@ __global__ void __maxnreg__(96) gemv_kernel(const GemvParamsOf<FMT, VAR> p) {
         const uint32_t sbase = stage0 + (uint32_t)slot * SB;
         float *pb = ((GLU && (s & 1)) ? part_up : part) + (ra - fbase) * PU;
         if (!failed && active) {
-            // same trip count for every lane of a warp (segments of one warp may
-            // belong to different row groups), so the shuffles stay convergent
-            for (int base = 0; base < rows_in; base += G) {
-                const int rr = base + g;
-                const bool has = rr < rows_in;
+            // this thread's rows g, g + G, ... of the stage: shared addresses of
+            // the row (and of its affine scales) and its partial slot advance
+            // by fixed 32-bit steps
+            const uint32_t Rb = (uint32_t)R;
+            uint32_t rowa = sbase + (uint32_t)(sel.w_off() + ra * R - a16) + (uint32_t)g * Rb;
+            const uint32_t rstep = (uint32_t)G * Rb;
+            uint32_t auxa = 0, astep = 0;
+            if constexpr (is_affine(FMT)) {
+                const int64_t AR = p.aux_row_bytes;
+                const int64_t a0 = sel.a_off() + ra * AR;
+                auxa = sbase + (uint32_t)p.aux_off + (uint32_t)(a0 - (a0 & ~(int64_t)15)) +
+                       (uint32_t)g * (uint32_t)AR;
+                astep = (uint32_t)G * (uint32_t)AR;
+            }
+            float *pp = pb + g * PU + pslot;
+            const int pstep = G * PU;
+            auto row_dot = [&](uint32_t ra_, uint32_t aa_) {
                 float acc = 0.0f;
-                if (has) {
-                    const uint32_t rowa = sbase + (uint32_t)(sel.w_off() + (ra + rr) * R - a16);
+#pragma unroll
+                for (int q = 0; q < UPT; ++q) {
+                    const int u = u0 + q * kCons;
                     if constexpr (is_affine(FMT)) {
-                        const int64_t AR = p.aux_row_bytes;
-                        const int64_t a0 = sel.a_off() + ra * AR;
-                        const uint32_t auxa = sbase + (uint32_t)p.aux_off +
-                                              (uint32_t)(a0 + rr * AR - (a0 & ~(int64_t)15));
-#pragma unroll
-                        for (int q = 0; q < UPT; ++q) {
-                            const int u = u0 + q * kCons;
-                            if (UPT == 1 || u < p.U)
-                                acc += unit_dot_aff<FMT>(rowa, auxa, (uint32_t)p.aux_sb, u, st[q]);
-                        }
+                        if (UPT == 1 || u < p.U)
+                            acc += unit_dot_aff<FMT>(ra_, aa_, (uint32_t)p.aux_sb, u, st[q]);
                     } else {
-#pragma unroll
-                        for (int q = 0; q < UPT; ++q) {
-                            const int u = u0 + q * kCons;
-                            if ((UPT == 1 && !kChunked) || u < p.U) acc += unit_dot<FMT>(rowa, u, st[q]);
-                        }
+                        if ((UPT == 1 && !kChunked) || u < p.U) acc += unit_dot<FMT>(ra_, u, st[q]);
                     }
                 }
-                if (SEG) {
-                    for (int o = SEG >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+                return acc;
+            };
+            if (SEG == 0) {
+                // one partial per thread and row: no cross-lane traffic, each
+                // thread runs its own trip count
+                for (int rr = g; rr < rows_in; rr += G) {
+                    *pp = row_dot(rowa, auxa);
+                    rowa += rstep;
+                    auxa += astep;
+                    pp += pstep;
                 }
-                if (writer && has) pb[rr * PU + pslot] = acc;
+            } else {
+                // same trip count for every lane of a warp (segments of one warp
+                // may belong to different row groups), so the shuffles stay
+                // convergent
+                for (int base = 0; base < rows_in; base += G) {
+                    const bool has = base + g < rows_in;
+                    float acc = has ? row_dot(rowa, auxa) : 0.0f;
+                    for (int o = SEG >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+                    if (writer && has) *pp = acc;
+                    rowa += rstep;
+                    auxa += astep;
+                    pp += pstep;
+                }
             }
         }
         // the stage is refilled by a bulk copy (the async proxy) once every

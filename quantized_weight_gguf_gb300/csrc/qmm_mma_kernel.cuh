@@ -119,8 +119,10 @@ struct MmaCfg {
     static constexpr int NA = kNAFit > 3 ? 3 : kNAFit;
     static constexpr int kCols = 512;
     // raw W stages: as many as fit, up to 4, next to a minimum x ring of four
-    // k-steps; HBM latency is hidden by the raw ring, L2 latency by the x ring
-    static constexpr int kNBMin = (4 + KB - 1) / KB;
+    // k-steps (two stages at least); HBM latency is hidden by the raw ring, L2
+    // latency by the x ring (8 raw stages at small token tiles measured no
+    // faster at N <= 32 and slower at N = 64)
+    static constexpr int kNBMin = (4 + KB - 1) / KB < 2 ? 2 : (4 + KB - 1) / KB;
     static constexpr int kRawFit = RAW ? (212 * 1024 - kNBMin * kBStage) / RAWB : 0;
     static constexpr int kNR = RAW ? (kRawFit > 4 ? 4 : kRawFit) : 1;
     static_assert(!RAW || kNR >= 2, "raw W ring too shallow");
@@ -242,7 +244,45 @@ __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// Half h of a Q4_K 64-weight chunk c: quant bytes 16h .. 16h+15 of the chunk (q),
+// Q4_K, per super-block: the fp16x2 constants of its four 64-weight chunks
+// (chunk c holds sub-block 2c in the low nibbles, 2c + 1 in the high ones).
+// The 6-bit scales sc[0..7] and mins m[0..7] are first gathered as bytes of
+// four words from the header words y (scales[0..3]), z (scales[4..7]) and
+// w (scales[8..11]): sc[s] = y byte s & 63 and m[s] = z byte s & 63 for
+// s < 4; for s = 4 + t, the low / high nibble of w byte t below the top two
+// bits of y / z byte t.
+struct Q4KChunk {
+    __half2 s0, n0, s1, n1, e0, e1;
+};
+
+__device__ __forceinline__ void q4k_superblock_consts(const uint4 &hdr, __half2 &d2,
+                                                      Q4KChunk (&cc)[4]) {
+    const uint32_t sc_lo = hdr.y & 0x3F3F3F3Fu, m_lo = hdr.z & 0x3F3F3F3Fu;
+    const uint32_t sc_hi = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+    const uint32_t m_hi = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+    d2 = u32_as_h2((hdr.x & 0xFFFFu) * 0x10001u);
+    const __half2 ndmin2 = __hneg2(u32_as_h2((hdr.x >> 16) * 0x10001u));
+    const __half2 k1024 = u32_as_h2(0x64006400u);
+    // byte j of v (< 64) as the exact fp16 pair (v, v): (1024 + v) - 1024
+    auto byte_h2 = [&](uint32_t v, uint32_t j) {
+        return __hsub2(u32_as_h2(prmt(v, 0x64646464u, j | 0x40u | (j << 8) | 0x4000u)), k1024);
+    };
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t scw = c < 2 ? sc_lo : sc_hi, mw = c < 2 ? m_lo : m_hi;
+        const uint32_t j = 2u * (uint32_t)(c & 1);
+        const __half2 sa = byte_h2(scw, j), sb = byte_h2(scw, j + 1);
+        cc[c].s0 = sa;
+        cc[c].n0 = __hmul2(sa, u32_as_h2(0xE400E400u));   // * -1024
+        cc[c].s1 = __hmul2(sb, u32_as_h2(0x2C002C00u));   // / 16
+        cc[c].n1 = __hmul2(sb, u32_as_h2(0xD400D400u));   // * -64
+        // -fp16(dmin m): the exact product rounded once
+        cc[c].e0 = __hmul2(ndmin2, byte_h2(mw, j));
+        cc[c].e1 = __hmul2(ndmin2, byte_h2(mw, j + 1));
+    }
+}
+
+// Half h of a Q4_K 64-weight chunk: quant bytes 16h .. 16h+15 of the chunk (q),
 // i.e. weights 16h + 0..15 (low nibbles, sub-block 2c) and 32 + 16h + 0..15
 // (high nibbles, sub-block 2c+1) -> 16 fp16x2 words: 0..7 low, 8..15 high.
 //
@@ -254,25 +294,8 @@ __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) {
 //   w = d * (sc q) - fp16(dmin m) is then rounded once.
 // Only dmin * m picks up an extra fp16 rounding against RN(ds q - dm); the
 // error stays at the level of rounding w itself.
-__device__ __forceinline__ void q4k_half_chunk_to_half(const uint4 &hdr, const uint4 &q, int c,
-                                                       uint32_t (&hw)[16]) {
-    uint32_t sc0, m0, sc1, m1;
-    q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * c, sc0, m0);
-    q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * c + 1, sc1, m1);
-    // small integers v < 1024 as exact fp16 pairs: (1024 + v) - 1024
-    auto int_h2 = [](uint32_t v) {
-        return __hsub2(u32_as_h2((0x6400u | v) * 0x10001u), u32_as_h2(0x64006400u));
-    };
-    const __half2 d2 = u32_as_h2((hdr.x & 0xFFFFu) * 0x10001u);
-    const __half2 dmin2 = u32_as_h2((hdr.x >> 16) * 0x10001u);
-    const __half2 s0 = int_h2(sc0);
-    const __half2 n0 = __hmul2(s0, u32_as_h2(0xE400E400u));                   // * -1024
-    const __half2 sc1h = int_h2(sc1);
-    const __half2 s1 = __hmul2(sc1h, u32_as_h2(0x2C002C00u));                 // / 16
-    const __half2 n1 = __hmul2(sc1h, u32_as_h2(0xD400D400u));                 // * -64
-    // -fp16(dmin m): the exact product rounded once
-    const __half2 e0 = __hneg2(__hmul2(dmin2, int_h2(m0)));
-    const __half2 e1 = __hneg2(__hmul2(dmin2, int_h2(m1)));
+__device__ __forceinline__ void q4k_half_chunk_to_half(const Q4KChunk &k, const __half2 d2,
+                                                       const uint4 &q, uint32_t (&hw)[16]) {
     const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -284,16 +307,17 @@ __device__ __forceinline__ void q4k_half_chunk_to_half(const uint4 &hdr, const u
         const __half2 l23 = u32_as_h2((u & 0x000F000Fu) | 0x64006400u);
         const __half2 h01 = u32_as_h2((t & 0x00F000F0u) | 0x64006400u);
         const __half2 h23 = u32_as_h2((u & 0x00F000F0u) | 0x64006400u);
-        hw[2 * i] = h2_as_u32(__hfma2(__hfma2(l01, s0, n0), d2, e0));
-        hw[2 * i + 1] = h2_as_u32(__hfma2(__hfma2(l23, s0, n0), d2, e0));
-        hw[8 + 2 * i] = h2_as_u32(__hfma2(__hfma2(h01, s1, n1), d2, e1));
-        hw[8 + 2 * i + 1] = h2_as_u32(__hfma2(__hfma2(h23, s1, n1), d2, e1));
+        hw[2 * i] = h2_as_u32(__hfma2(__hfma2(l01, k.s0, k.n0), d2, k.e0));
+        hw[2 * i + 1] = h2_as_u32(__hfma2(__hfma2(l23, k.s0, k.n0), d2, k.e0));
+        hw[8 + 2 * i] = h2_as_u32(__hfma2(__hfma2(h01, k.s1, k.n1), d2, k.e1));
+        hw[8 + 2 * i + 1] = h2_as_u32(__hfma2(__hfma2(h23, k.s1, k.n1), d2, k.e1));
     }
 }
 
 template <int FMT>
 struct Prefetch {
-    static constexpr int value = (FMT == F_Q4_K || FMT == F_Q4_0) ? 4 : (FMT == F_Q6_K ? 2 : 3);
+    static constexpr int value = (FMT == F_Q4_K || FMT == F_Q4_0) ? 4
+                                 : (FMT == F_Q6_K || FMT == F_BF16 || FMT == F_F16) ? 2 : 3;
 };
 
 __device__ __forceinline__ void split_half_words(const float (&v)[32], bool lo, uint32_t (&hw)[16]) {
@@ -722,6 +746,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                         tc_fence_after();
                     }
                     const uint32_t ta = tlane + (uint32_t)(C::kACol0 + slot * C::kAStageCols);
+                    Q4KChunk kc[4];
+                    __half2 d2;
+                    if constexpr (FMT == F_Q4_K) q4k_superblock_consts(hdr, d2, kc);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t hw[16];
@@ -729,7 +756,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 #pragma unroll
                             for (int e = 0; e < 16; ++e) hw[e] = 0u;
                         } else if constexpr (FMT == F_Q4_K) {
-                            q4k_half_chunk_to_half(hdr, qv[c], c, hw);
+                            q4k_half_chunk_to_half(kc[c], d2, qv[c], hw);
                         } else {
                             Raw32<FMT> ra;
                             ra.qw[0] = qv[c].x; ra.qw[1] = qv[c].y; ra.qw[2] = qv[c].z; ra.qw[3] = qv[c].w;
@@ -862,24 +889,28 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             // the two accumulators (even / odd k-steps) are summed here; KS == 1
             // leaves the odd one unwritten
             const bool two_acc = C::kNAcc == 2 && KSu > 1;
+            // (one accumulator's hi and lo columns at a time: 32 registers live)
             auto load_acc = [&](int col, float (&acc)[16]) {
                 uint32_t v[16], v2[16];
                 tmem_ld16(tlane + (uint32_t)col, v);
-                if (two_acc) tmem_ld16(tlane + (uint32_t)(C::kAccCols + col), v2);
                 if (MODE == 1) {
+                    if (two_acc) tmem_ld16(tlane + (uint32_t)(C::kAccCols + col), v2);
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         acc[i] = __uint_as_float(v[i]) + (two_acc ? __uint_as_float(v2[i]) : 0.0f);
                 } else {
-                    uint32_t w2[16], w3[16];
-                    tmem_ld16(tlane + (uint32_t)(col + BN / 2), w2);
-                    if (two_acc) tmem_ld16(tlane + (uint32_t)(C::kAccCols + col + BN / 2), w3);
+                    tmem_ld16(tlane + (uint32_t)(col + BN / 2), v2);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        acc[i] = __uint_as_float(v[i]) + __uint_as_float(w2[i]);
-                        if (two_acc) acc[i] += __uint_as_float(v2[i]) + __uint_as_float(w3[i]);
+                    for (int i = 0; i < 16; ++i) acc[i] = __uint_as_float(v[i]) + __uint_as_float(v2[i]);
+                    if (two_acc) {
+                        tmem_ld16(tlane + (uint32_t)(C::kAccCols + col), v);
+                        tmem_ld16(tlane + (uint32_t)(C::kAccCols + col + BN / 2), v2);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            acc[i] += __uint_as_float(v[i]) + __uint_as_float(v2[i]);
                     }
                 }
             };
