@@ -522,7 +522,7 @@ def measure_other_workloads(torch, q, lib, r, stream, hbm_peak, tc_peak):
     # id selects; the bytes are the selected slices (one read per pair)
     ex = lib.qmm_matmul_experts
 
-    def expert_case(name, n_pos, reps=50):
+    def expert_case(name, n_pos, reps=50, path=q.PATH_AUTO):
         fmt, k, n, n_exp, w, x, ids = qmm_synth.expert_workload(name, n_pos=n_pos)
         slice_bytes = w.size // n_exp
         pairs = ids.size
@@ -532,9 +532,14 @@ def measure_other_workloads(torch, q, lib, r, stream, hbm_peak, tc_peak):
         xd = torch.from_numpy(x).to(dev)
         idd = torch.from_numpy(ids).to(dev)
         yd = torch.empty((pairs, n), device=dev)
-        al = [ctypes.byref(q.make_args(fmt, wc[c], xd, yd, k, n, n_pos, stream=stream,
-                                       flags=q.FLAG_OVERLAP_PREV | q.FLAG_X_READY))
-              for c in range(ncop)]
+        args = [q.make_args(fmt, wc[c], xd, yd, k, n, n_pos, stream=stream, path=path,
+                            flags=q.FLAG_OVERLAP_PREV | q.FLAG_X_READY) for c in range(ncop)]
+        need = q.qmm_experts_workspace_bytes(args[0], n_exp, ids.shape[1])
+        wsb = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        if need:
+            for a in args:
+                a.workspace, a.workspace_bytes = wsb.data_ptr(), need
+        al = [ctypes.byref(a) for a in args]
         ip = ctypes.c_void_p(idd.data_ptr())
 
         def launch(c):
@@ -542,14 +547,24 @@ def measure_other_workloads(torch, q, lib, r, stream, hbm_peak, tc_peak):
                 raise RuntimeError(q.qmm_last_error())
         dt = time_loop(torch, launch, reps, 5, ncop, stream)
         q.qmm_device_status(stream)
-        gbs = pairs * slice_bytes / dt / 1e9
-        return {"us": dt * 1e6, "weight_gbs": gbs, "frac_hbm": gbs / hbm_peak,
-                "weight_bytes": int(pairs * slice_bytes), "distinct_bytes": int(touched),
-                "pairs": int(pairs), "launches_per_call": 1}
+        res = {"us": dt * 1e6, "pairs": int(pairs), "distinct_bytes": int(touched),
+               "form": "grouped tensor-core" if need else "one GEMV per pair"}
+        if need:
+            # grouped: each selected slice is decoded once per token tile
+            fl = 2.0 * pairs * k * n
+            res.update({"tflops": fl / dt / 1e12, "frac_bf16_peak": fl / dt / 1e12 / tc_peak,
+                        "distinct_weight_gbs": touched / dt / 1e9, "launches_per_call": 3})
+        else:
+            gbs = pairs * slice_bytes / dt / 1e9
+            res.update({"weight_gbs": gbs, "frac_hbm": gbs / hbm_peak,
+                        "weight_bytes": int(pairs * slice_bytes), "launches_per_call": 1})
+        return res
 
     for name in sorted(qmm_synth.EXPERT_WORKLOADS):
         out[f"{name}_pos1"] = expert_case(name, 1)
         out[f"{name}_pos4"] = expert_case(name, 4)
+        out[f"{name}_pos64_gemv"] = expert_case(name, 64, reps=20, path=q.PATH_GEMV)
+        out[f"{name}_pos64_grouped"] = expert_case(name, 64, reps=20, path=q.PATH_MMA)
 
     exa = lib.qmm_matmul_experts_affine
 
@@ -650,6 +665,35 @@ def measure_other_workloads(torch, q, lib, r, stream, hbm_peak, tc_peak):
 
     out["q4_k_swiglu_pair"] = glu_case("q4_k_gemv", q.ACT_SWIGLU)
     out["q8_0_geglu_pair"] = glu_case("q8_0_gemv", q.ACT_GEGLU)
+
+    def glu_tokens_case(nt, act, reps=20):
+        # several tokens: the gate product into scratch, then the up product
+        # whose epilogue writes act(gate) * up
+        fmt, k, n, w, x = qmm_synth.workload("q4_k_prefill", n_tokens=nt)
+        w2 = qmm_synth.gen_weights(fmt, k, n, np.random.default_rng(78))
+        ncop = r.copies_for(2 * w.size)
+        wg, wu = r.weights(w, ncop), r.weights(w2, ncop)
+        xd = torch.from_numpy(x).to(dev)
+        yd = torch.empty((nt, n), device=dev)
+        a0 = q.make_args(fmt, wg[0], xd, yd, k, n, nt, stream=stream)
+        need = q.qmm_glu_workspace_bytes(a0)
+        wsb = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        al = [ctypes.byref(q.make_args(fmt, wg[c], xd, yd, k, n, nt, stream=stream, workspace=wsb,
+                                       workspace_bytes=need)) for c in range(ncop)]
+        ups = [ctypes.c_void_p(wu[c].data_ptr()) for c in range(ncop)]
+
+        def launch(c):
+            if glu(al[c], ups[c], act):
+                raise RuntimeError(q.qmm_last_error())
+        dt = time_loop(torch, launch, reps, 3, ncop, stream)
+        q.qmm_device_status(stream)
+        fl = 4.0 * nt * k * n
+        return {"us": dt * 1e6, "tflops": fl / dt / 1e12, "frac_bf16_peak": fl / dt / 1e12 / tc_peak,
+                "launches_per_call": 4,
+                "note": "gate product into scratch; the up product's epilogue applies act(gate)"}
+
+    out["q4_k_swiglu_pair_N64"] = glu_tokens_case(64, q.ACT_SWIGLU)
+    out["q4_k_swiglu_pair_N512"] = glu_tokens_case(512, q.ACT_SWIGLU)
 
     out["affine4_gemv"] = affine_case("affine4_gemv")
     out["affine8_gemv"] = affine_case("affine8_gemv")

@@ -224,16 +224,35 @@ size_t qmm_backward_input_workspace_bytes(const qmm_args *a);
  * array [n_pos x top_k]; a->y is [n_pos * top_k x n]:
  *     y[p * top_k + s][j] (+)= sum_i x[p][i] * w_{ids[p * top_k + s]}[j][i]
  * for j in [j_start, j_end). a->w_len, when nonzero, must be n_experts times
- * the slice bytes; n_pos * top_k <= 65535; a->path AUTO or GEMV (each
- * (position, slot) runs as one GEMV of the one-token path, side by side in
- * one launch; the ids are read on the device, nothing synchronizes).
- * a->flags as for qmm_matmul_ex, with ids counted as input: under
- * QMM_FLAG_OVERLAP_PREV alone the kernel waits for the preceding one before
- * it reads ids (so no weight byte moves before then); QMM_FLAG_X_READY
- * vouches that neither x nor ids is written by the preceding kernel. An id
- * outside [0, n_experts) leaves that y row untouched and records an error that
- * qmm_device_status reports as QMM_ERR_BAD_ID. Same formats and k limits as the one-token path. */
+ * the slice bytes; n_pos * top_k <= 65535. Two forms, both reading the ids
+ * on the device (nothing synchronizes):
+ *  - GEMV form: each (position, slot) runs as one GEMV of the one-token
+ *    path, side by side in one launch. a->flags as for qmm_matmul_ex, with
+ *    ids counted as input: under QMM_FLAG_OVERLAP_PREV alone the kernel waits
+ *    for the preceding one before it reads ids (so no weight byte moves
+ *    before then); QMM_FLAG_X_READY vouches that neither x nor ids is written
+ *    by the preceding kernel. Same formats and k limits as the one-token path.
+ *  - grouped form (the batched expert matmul of the same page): a routing
+ *    kernel sorts the pairs by expert on the device, then one tensor-core
+ *    pass multiplies each expert's rows by its slice, so a slice chosen by
+ *    many positions is decoded once per token tile instead of once per pair.
+ *    GGUF formats with k >= 1024 (the split-x mode), n_experts <= 4096;
+ *    scratch from a->workspace (qmm_experts_workspace_bytes) or the
+ *    library's buffer; flags are not used.
+ * a->path GEMV or MMA forces a form (MMA: QMM_ERR_UNSUPPORTED where the
+ * grouped form cannot take the call); AUTO takes the grouped form for Q4_K
+ * (whose W tiles the tensor-core path streams by TMA) when n_pos > 1 and
+ * n_pos * top_k >= 2 * n_experts, the GEMV form otherwise. An id outside [0, n_experts)
+ * leaves that y row untouched and records an error that qmm_device_status
+ * reports as QMM_ERR_BAD_ID. */
 int qmm_matmul_experts(const qmm_args *a, const int32_t *ids, int64_t n_experts, int64_t top_k);
+
+/* Device scratch bytes qmm_matmul_experts needs for these arguments: 0 for
+ * the GEMV form; for the grouped form the split fp16 copies of the routed x
+ * rows, a scale per row, the routing tables and the row order
+ * (2 * round256(P * kp * 2) + round256(P * 4) + 2 * round256((n_experts + 1) * 4)
+ * + round256(P * 4) with P = n_pos * top_k, kp = k padded to 64). Host only. */
+size_t qmm_experts_workspace_bytes(const qmm_args *a, int64_t n_experts, int64_t top_k);
 
 /* The expert-indexed product for affine matrices (a->fmt = QMM_AFFINE4 or
  * QMM_AFFINE8; mixture-of-experts layers of MLX-style models): the code
@@ -268,11 +287,14 @@ typedef enum qmm_act {
  * a->w is the gate matrix, w_up the up matrix (same format, k, n and w_len;
  * device, 16-byte aligned). One token on the GEMV path: one fused launch
  * that streams a CTA's rows of Wg, keeps the gate values on chip, streams
- * the same rows of Wu and writes only y. Several tokens: the two products
- * go through the tensor-core path into scratch (a->workspace of at least
- * qmm_glu_workspace_bytes(a) bytes, else the library's) and one
- * elementwise launch combines them. GGUF formats only (QMM_ERR_FORMAT for
- * affine ones or an unknown act); flags as for qmm_matmul_ex. */
+ * the same rows of Wu and writes only y. Several tokens: the gate product
+ * goes through the tensor-core path into scratch (a->workspace of at least
+ * qmm_glu_workspace_bytes(a) bytes, else the library's: the gate values
+ * [n_tokens][n] fp32 plus qmm_workspace_bytes of the product), then the up
+ * product's epilogue reads each gate value and writes act(gate) * up (or
+ * adds it) to y; no up vector is stored and no combine kernel runs. GGUF
+ * formats only (QMM_ERR_FORMAT for affine ones or an unknown act); flags as
+ * for qmm_matmul_ex. */
 int qmm_matmul_glu(const qmm_args *a, const void *w_up, int act);
 size_t qmm_glu_workspace_bytes(const qmm_args *a);
 

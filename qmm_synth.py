@@ -23,12 +23,13 @@ stand-ins for the real-model shapes that the rullama ``matmul.rs`` tests use
                     seed 4; run as 8 output tiles of 32768 columns.
 * ``q4_k_prefill``  Q4_K with the q4_k_gemv value distribution, N=512 tokens,
                     k=4096, n=14336; X ~ N(0, 1) [N x k]; seed 5 (also N=1, 8, 64).
-* ``q8_0_experts`` / ``q5_0_experts``
+* ``q8_0_experts`` / ``q5_0_experts`` / ``q4_k_experts``
                     expert-indexed decode: 64 stacked experts of n=768 rows,
-                    k=2048, top_k = 8 experts per position, 1 position (also 4);
-                    Q8_0 d ~ U[0.002, 0.02] with uniform int8 codes, Q5_0
-                    d ~ U[0.005, 0.05] with uniform high-bit words and nibbles;
-                    ids drawn without repetition per position; x ~ N(0, 1); seeds 6, 7.
+                    k=2048, top_k = 8 experts per position, 1 position (also 4
+                    and 64); Q8_0 d ~ U[0.002, 0.02] with uniform int8 codes,
+                    Q5_0 d ~ U[0.005, 0.05] with uniform high-bit words and
+                    nibbles, Q4_K with the q4_k_gemv distribution; ids drawn
+                    without repetition per position; x ~ N(0, 1); seeds 6, 7, 14.
 * ``q8_0_gemv`` / ``q5_0_gemv``
                     k=4096, n=14336, one token; the expert workloads' value
                     distributions; x ~ N(0, 1); seeds 8, 9.
@@ -191,6 +192,7 @@ def gen_ids(n_pos: int, top_k: int, n_experts: int, rng: np.random.Generator) ->
 EXPERT_WORKLOADS = {
     "q8_0_experts": ("q8_0", 2048, 768, 64, 8, 1, 6),
     "q5_0_experts": ("q5_0", 2048, 768, 64, 8, 1, 7),
+    "q4_k_experts": ("q4_k", 2048, 768, 64, 8, 1, 14),
 }
 
 

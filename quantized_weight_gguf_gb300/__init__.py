@@ -32,7 +32,8 @@ EXPORTS = ("qmm_weight_bytes", "qmm_matmul", "qmm_set_stream", "qmm_matmul_ex",
            "qmm_device_status", "qmm_last_error", "qmm_version", "qmm_matmul_noalloc",
            "qmm_matmul_backward_input", "qmm_backward_input_workspace_bytes",
            "qmm_matmul_experts", "qmm_matmul_affine", "qmm_dequant_affine", "qmm_matmul_glu",
-           "qmm_glu_workspace_bytes", "qmm_check_bounded_wait", "qmm_matmul_experts_affine")
+           "qmm_glu_workspace_bytes", "qmm_check_bounded_wait", "qmm_matmul_experts_affine",
+           "qmm_experts_workspace_bytes")
 
 
 class QmmError(RuntimeError):
@@ -80,6 +81,7 @@ def load(path: str = LIB_PATH):
         "qmm_matmul_backward_input": (i, [pa]),
         "qmm_backward_input_workspace_bytes": (sz, [pa]),
         "qmm_matmul_experts": (i, [pa, vp, i64, i64]),
+        "qmm_experts_workspace_bytes": (sz, [pa, i64, i64]),
         "qmm_matmul_affine": (i, [pa, vp, vp]),
         "qmm_matmul_glu": (i, [pa, vp, i]),
         "qmm_glu_workspace_bytes": (sz, [pa]),
@@ -202,6 +204,10 @@ def qmm_matmul_experts(args: qmm_args, ids, n_experts: int, top_k: int) -> int:
     return _check(load().qmm_matmul_experts(ctypes.byref(args), _ptr(ids), n_experts, top_k))
 
 
+def qmm_experts_workspace_bytes(args: qmm_args, n_experts: int, top_k: int) -> int:
+    return load().qmm_experts_workspace_bytes(ctypes.byref(args), n_experts, top_k)
+
+
 def qmm_backward_input_workspace_bytes(args: qmm_args) -> int:
     return load().qmm_backward_input_workspace_bytes(ctypes.byref(args))
 
@@ -279,10 +285,12 @@ def matmul_backward_input(fmt, w, dy, k: int, n: int, *, dx=None, j_start=0, j_e
 
 
 def matmul_experts(fmt, w, x, ids, k: int, n: int, n_experts: int, *, y=None, j_start=0,
-                   j_end=0, accumulate=False, stream=None, flags=0, scales=None, biases=None):
+                   j_end=0, accumulate=False, path=PATH_AUTO, stream=None, flags=0, scales=None,
+                   biases=None):
     """Expert-indexed product for torch CUDA tensors: w uint8 (n_experts
     stacked slices of n rows), x float32 [n_pos, k], ids int32 [n_pos, top_k]
-    on the device. Returns y float32 [n_pos * top_k, n] (the given y when passed)."""
+    on the device. Returns y float32 [n_pos * top_k, n] (the given y when
+    passed). Scratch of the grouped form is a torch allocation on x's device."""
     import torch
     if x.dim() == 1:
         x = x.unsqueeze(0)
@@ -292,11 +300,17 @@ def matmul_experts(fmt, w, x, ids, k: int, n: int, n_experts: int, *, y=None, j_
     if y is None:
         y = torch.empty((n_pos * top_k, n), dtype=torch.float32, device=x.device)
     a = make_args(fmt, w, x, y, k, n, n_pos, w_len=w.numel() * w.element_size(), j_start=j_start,
-                  j_end=j_end, accumulate=accumulate, stream=stream, flags=flags)
+                  j_end=j_end, accumulate=accumulate, path=path, stream=stream, flags=flags)
     if scales is not None or biases is not None:
         qmm_matmul_experts_affine(a, ids, n_experts, top_k, scales, biases)
-    else:
-        qmm_matmul_experts(a, ids, n_experts, top_k)
+        return y
+    need = qmm_experts_workspace_bytes(a, n_experts, top_k)
+    ws = None
+    if need:
+        ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+        a.workspace, a.workspace_bytes = ws.data_ptr(), need
+    qmm_matmul_experts(a, ids, n_experts, top_k)
+    _keep_until_done(ws, stream)
     return y
 
 

@@ -16,6 +16,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqmm.so")
 # the tensor-core kernel instances come first: they take longest to compile
 SOURCES = ["qmm_mma_inst_q4k.cu", "qmm_mma_inst_16.cu", "qmm_mma_inst_q.cu", "qmm_mma_inst_aff.cu",
+           "qmm_mma_inst_grp.cu",
            "qmm_api.cu", "qmm_gemv.cu", "qmm_mma.cu", "qmm_dequant.cu", "qmm_noalloc.cu",
            "qmm_back_input.cu"]
 GENCODE = "arch=compute_103a,code=sm_103a"

@@ -278,16 +278,34 @@ int run(const qmm_args *a, const void *sc = nullptr, const void *bi = nullptr,
 
 size_t round256_bytes(size_t v) { return (v + 255) & ~(size_t)255; }
 
-// One token on the GEMV path: the fused gated GEMV; otherwise two products
-// into scratch and an elementwise combine.
+// One token on the GEMV path: the fused gated GEMV; otherwise the gate
+// product into scratch, then the up product whose epilogue applies the
+// activation to the gate values and writes y.
 bool glu_fused(const qmm_args *a) {
     return a->n_tokens == 1 && a->path != QMM_PATH_MMA && qmm::gemv_supports(a->fmt, a->k);
 }
 
 size_t glu_scratch_bytes(const qmm_args *a) {
     const size_t one = round256_bytes((size_t)a->n_tokens * (size_t)a->n * 4);
-    return 2 * one + qmm::mma_workspace_bytes(a->fmt, a->n_tokens, a->k);
+    return one + qmm::mma_workspace_bytes(a->fmt, a->n_tokens, a->k);
 }
+// Whether an expert-indexed call runs as the grouped tensor-core product
+// (pairs routed by expert on the device, one pass over the sorted rows) or
+// as one GEMV per (position, slot). The grouped form takes GGUF formats whose
+// k the split-x tensor-core mode takes. AUTO groups Q4_K (its W tiles stream
+// by TMA) once there are several positions and on average at least two
+// pairs per expert; the other formats decode W rows with per-thread loads on
+// the tensor-core path, which measured no faster than one GEMV per pair.
+bool experts_grouped_ok(const qmm_args *a, int64_t n_experts) {
+    return !affine_fmt(a->fmt) && a->k > 0 && qmm::mma_mode(a->fmt, a->k) == 2 &&
+           n_experts <= qmm::kMaxGroupedExperts;
+}
+bool experts_grouped(const qmm_args *a, int64_t n_experts, int64_t top_k) {
+    if (a->path == QMM_PATH_GEMV || !experts_grouped_ok(a, n_experts)) return false;
+    if (a->path == QMM_PATH_MMA) return true;
+    return a->fmt == QMM_Q4_K && a->n_tokens > 1 && a->n_tokens * top_k >= 2 * n_experts;
+}
+
 // The expert-indexed product of both entry points; affine matrices come with
 // their stacked scale and bias arrays (affine_entry).
 int experts_impl(const qmm_args *a, const int32_t *ids, int64_t n_experts, int64_t top_k,
@@ -296,7 +314,10 @@ int experts_impl(const qmm_args *a, const int32_t *ids, int64_t n_experts, int64
     if (n_experts < 1 || top_k < 1)
         return fail(QMM_ERR_SHAPE, "n_experts %lld and top_k %lld must be >= 1",
                     (long long)n_experts, (long long)top_k);
-    if (a->path == QMM_PATH_MMA) return fail(QMM_ERR_UNSUPPORTED, "expert products run as GEMVs");
+    if (a->path == QMM_PATH_MMA && !experts_grouped_ok(a, n_experts))
+        return fail(QMM_ERR_UNSUPPORTED,
+                    "the grouped tensor-core expert product takes GGUF formats with k >= 1024 "
+                    "and at most %d experts", qmm::kMaxGroupedExperts);
     if (affine_fmt(a->fmt) != affine_entry)
         return fail(QMM_ERR_FORMAT, affine_entry
                                         ? "qmm_matmul_experts_affine takes QMM_AFFINE4 or QMM_AFFINE8"
@@ -323,7 +344,7 @@ int experts_impl(const qmm_args *a, const int32_t *ids, int64_t n_experts, int64
         if ((reinterpret_cast<uintptr_t>(sc) & 15u) || (reinterpret_cast<uintptr_t>(bi) & 15u))
             return fail(QMM_ERR_ALIGN, "scales and biases must be 16-byte aligned");
     }
-    if (a->k > 0 && !qmm::gemv_supports(a->fmt, a->k))
+    if (a->k > 0 && !experts_grouped(a, n_experts, top_k) && !qmm::gemv_supports(a->fmt, a->k))
         return fail(QMM_ERR_UNSUPPORTED, "expert GEMV cannot take %s with k=%lld", fmt_name(a->fmt),
                     (long long)a->k);
     qmm::DeviceInfo *dev = nullptr;
@@ -334,6 +355,30 @@ int experts_impl(const qmm_args *a, const int32_t *ids, int64_t n_experts, int64
         if (a->accumulate) return QMM_OK;
         cudaError_t e = qmm::launch_zero_cols(a->y, pairs, a->n, j0, j1, s);
         return e == cudaSuccess ? QMM_OK : cuda_fail(e, "zero-fill launch");
+    }
+    if (experts_grouped(a, n_experts, top_k)) {
+        const size_t need = qmm::mma_grouped_workspace_bytes(a->fmt, pairs, a->k, n_experts);
+        void *ws = a->workspace;
+        if (ws) {
+            st = check_mma_workspace(ws, a->workspace_bytes, need);
+            if (st != QMM_OK) return st;
+        } else {
+            st = library_workspace(need, &ws);
+            if (st != QMM_OK) return st;
+        }
+        qmm::MmaGroupedLaunch m;
+        m.fmt = a->fmt;
+        m.w = static_cast<const uint8_t *>(a->w);
+        m.x = a->x;
+        m.ids = ids;
+        m.y = a->y;
+        m.k = a->k; m.n = a->n; m.n_pos = a->n_tokens; m.top_k = top_k;
+        m.n_experts = n_experts; m.row_bytes = rb;
+        m.j0 = j0; m.j1 = j1;
+        m.accumulate = a->accumulate;
+        m.workspace = ws;
+        cudaError_t e = qmm::launch_mma_grouped(m, *dev, s);
+        return e == cudaSuccess ? QMM_OK : cuda_fail(e, "grouped expert launch");
     }
     qmm::GemvLaunch g;
     g.fmt = a->fmt;
@@ -500,6 +545,16 @@ int qmm_matmul_experts(const qmm_args *a, const int32_t *ids, int64_t n_experts,
     return experts_impl(a, ids, n_experts, top_k, nullptr, nullptr, false);
 }
 
+size_t qmm_experts_workspace_bytes(const qmm_args *a, int64_t n_experts, int64_t top_k) {
+    if (!a || n_experts < 1 || top_k < 1) return 0;
+    qmm_args one = *a;
+    one.w_len = 0;
+    int64_t j0, j1, rb;
+    if (validate(&one, &j0, &j1, &rb, false) != QMM_OK || a->k == 0 || j1 <= j0) return 0;
+    if (!experts_grouped(a, n_experts, top_k)) return 0;
+    return qmm::mma_grouped_workspace_bytes(a->fmt, a->n_tokens * top_k, a->k, n_experts);
+}
+
 int qmm_matmul_experts_affine(const qmm_args *a, const int32_t *ids, int64_t n_experts,
                               int64_t top_k, const void *scales, const void *biases) {
     t_err[0] = 0;
@@ -599,24 +654,27 @@ int qmm_matmul_glu(const qmm_args *a, const void *w_up, int act) {
     }
     const size_t one = round256_bytes((size_t)a->n_tokens * (size_t)a->n * 4);
     float *gbuf = static_cast<float *>(ws);
-    float *ubuf = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + one);
-    void *mws = static_cast<uint8_t *>(ws) + 2 * one;
+    void *mws = static_cast<uint8_t *>(ws) + one;
+    // gate = x Wg into scratch; then y (+)= act(gate) * (x Wu) in the up
+    // product's epilogue (no up vector is stored, no combine launch)
     for (int m = 0; m < 2; ++m) {
         qmm::MmaLaunch ml;
         ml.fmt = a->fmt;
         ml.w = static_cast<const uint8_t *>(m ? w_up : a->w);
         ml.x = a->x;
-        ml.y = m ? ubuf : gbuf;
+        ml.y = m ? a->y : gbuf;
         ml.k = a->k; ml.n = a->n; ml.n_tokens = a->n_tokens; ml.row_bytes = rb;
         ml.j0 = j0; ml.j1 = j1;
-        ml.accumulate = 0;
+        ml.accumulate = m ? a->accumulate : 0;
         ml.workspace = mws;
+        if (m) {
+            ml.gate = gbuf;
+            ml.glu = act;
+        }
         cudaError_t e = qmm::launch_mma(ml, *dev, s);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core launch");
     }
-    cudaError_t e = qmm::launch_glu_combine(gbuf, ubuf, a->y, a->n_tokens, a->n, j0, j1, act,
-                                            a->accumulate, s);
-    return e == cudaSuccess ? QMM_OK : cuda_fail(e, "gated combine launch");
+    return QMM_OK;
 }
 
 int qmm_matmul_affine(const qmm_args *a, const void *scales, const void *biases) {

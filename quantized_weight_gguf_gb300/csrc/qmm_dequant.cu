@@ -106,34 +106,4 @@ cudaError_t launch_bounded_wait_probe(unsigned int *err, uint64_t limit_ns, cuda
     return cudaGetLastError();
 }
 
-// y[t][j] (+)= act(g[t][j]) * u[t][j] for j in [j0, j1) (row stride n).
-template <int ACT>
-__global__ void glu_combine_kernel(const float *__restrict__ gt, const float *__restrict__ up,
-                                   float *y, int64_t n_tokens, int64_t n, int64_t j0, int64_t j1,
-                                   int accumulate) {
-    const int64_t width = j1 - j0;
-    const int64_t total = width * n_tokens;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t t = i / width;
-        const int64_t o = t * n + j0 + (i - t * width);
-        const float h = glu_act<ACT>(gt[o]) * up[o];
-        y[o] = accumulate ? y[o] + h : h;
-    }
-}
-
-cudaError_t launch_glu_combine(const float *g, const float *u, float *y, int64_t n_tokens,
-                               int64_t n, int64_t j0, int64_t j1, int act, int accumulate,
-                               cudaStream_t s) {
-    const int64_t total = (j1 - j0) * n_tokens;
-    if (total <= 0) return cudaSuccess;
-    int64_t blocks = (total + 255) / 256;
-    if (blocks > 8192) blocks = 8192;
-    if (act == 1)
-        glu_combine_kernel<1><<<(unsigned)blocks, 256, 0, s>>>(g, u, y, n_tokens, n, j0, j1, accumulate);
-    else
-        glu_combine_kernel<2><<<(unsigned)blocks, 256, 0, s>>>(g, u, y, n_tokens, n, j0, j1, accumulate);
-    return cudaGetLastError();
-}
-
 }  // namespace qmm

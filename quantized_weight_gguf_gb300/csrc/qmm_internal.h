@@ -54,10 +54,32 @@ struct MmaLaunch {
     void *workspace;        // >= mma_workspace_bytes(fmt, n_tokens, k)
     // affine formats: bf16 scale and bias arrays [n][k/64]
     const uint8_t *sc = nullptr, *bi = nullptr;
+    // gated pairs (glu 1: SwiGLU, 2: GeGLU): this is the up product, and the
+    // epilogue writes act(gate[t][j]) * (x Wu)[t][j] (gate: [N][n], row stride n)
+    const float *gate = nullptr;
+    int glu = 0;
 };
 size_t mma_workspace_bytes(int fmt, int64_t n_tokens, int64_t k);
 int mma_mode(int fmt, int64_t k);  // 1: W16.X16, 2: x split, 3: w and x split
 cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s);
+
+// Expert-grouped N-token product: the (position, slot) pairs are routed on
+// the device into expert-sorted rows, then one tensor-core pass multiplies
+// each expert's rows by its slice; y row p * top_k + s as for the GEMV form.
+constexpr int kMaxGroupedExperts = 4096;
+struct MmaGroupedLaunch {
+    int fmt;
+    const uint8_t *w;           // n_experts stacked slices of n rows
+    const float *x;             // [n_pos][k]
+    const int32_t *ids;         // [n_pos][top_k], device
+    float *y;                   // [n_pos * top_k][n]
+    int64_t k, n, n_pos, top_k, n_experts, row_bytes;
+    int64_t j0, j1;
+    int accumulate;
+    void *workspace;            // >= mma_grouped_workspace_bytes(...)
+};
+size_t mma_grouped_workspace_bytes(int fmt, int64_t pairs, int64_t k, int64_t n_experts);
+cudaError_t launch_mma_grouped(const MmaGroupedLaunch &m, const DeviceInfo &dev, cudaStream_t s);
 
 // Backward with respect to the input, one vector:
 // dx[i] (+)= sum_{j in [j0, j1)} dy[j] w[j][i].
@@ -88,11 +110,6 @@ cudaError_t launch_dequant(int fmt, const uint8_t *w, int64_t k, int64_t n, int6
 cudaError_t launch_zero_cols(float *y, int64_t n_tokens, int64_t n, int64_t j0, int64_t j1,
                              cudaStream_t s);
 
-// y[t][j] (+)= act(g[t][j]) * u[t][j] over [j0, j1) (act 1 SwiGLU, 2 GeGLU;
-// g, u and y share the row stride n).
-cudaError_t launch_glu_combine(const float *g, const float *u, float *y, int64_t n_tokens,
-                               int64_t n, int64_t j0, int64_t j1, int act, int accumulate,
-                               cudaStream_t s);
 // One block waiting on a barrier nothing satisfies; it gives up after
 // limit_ns and records an error in *err (see qmm_check_bounded_wait).
 cudaError_t launch_bounded_wait_probe(unsigned int *err, uint64_t limit_ns, cudaStream_t s);

@@ -7,24 +7,35 @@
 
 namespace qmm {
 
-extern template cudaError_t launch_fmt<F_BF16>(int, int, const Maps &, const MmaAffParams &,
+extern template cudaError_t launch_fmt<F_BF16>(int, int, const Maps &, const MmaHostParams &,
                                             const DeviceInfo &, cudaStream_t);
-extern template cudaError_t launch_fmt<F_F16>(int, int, const Maps &, const MmaAffParams &,
+extern template cudaError_t launch_fmt<F_F16>(int, int, const Maps &, const MmaHostParams &,
                                             const DeviceInfo &, cudaStream_t);
-extern template cudaError_t launch_fmt<F_Q4_0>(int, int, const Maps &, const MmaAffParams &,
+extern template cudaError_t launch_fmt<F_Q4_0>(int, int, const Maps &, const MmaHostParams &,
                                             const DeviceInfo &, cudaStream_t);
-extern template cudaError_t launch_fmt<F_Q4_K>(int, int, const Maps &, const MmaAffParams &,
+extern template cudaError_t launch_fmt<F_Q4_K>(int, int, const Maps &, const MmaHostParams &,
                                             const DeviceInfo &, cudaStream_t);
-extern template cudaError_t launch_fmt<F_Q6_K>(int, int, const Maps &, const MmaAffParams &,
+extern template cudaError_t launch_fmt<F_Q6_K>(int, int, const Maps &, const MmaHostParams &,
                                             const DeviceInfo &, cudaStream_t);
-extern template cudaError_t launch_fmt<F_Q8_0>(int, int, const Maps &, const MmaAffParams &,
+extern template cudaError_t launch_fmt<F_Q8_0>(int, int, const Maps &, const MmaHostParams &,
                                             const DeviceInfo &, cudaStream_t);
-extern template cudaError_t launch_fmt<F_Q5_0>(int, int, const Maps &, const MmaAffParams &,
+extern template cudaError_t launch_fmt<F_Q5_0>(int, int, const Maps &, const MmaHostParams &,
                                             const DeviceInfo &, cudaStream_t);
-extern template cudaError_t launch_fmt<F_AFF4>(int, int, const Maps &, const MmaAffParams &,
+extern template cudaError_t launch_fmt<F_AFF4>(int, int, const Maps &, const MmaHostParams &,
                                             const DeviceInfo &, cudaStream_t);
-extern template cudaError_t launch_fmt<F_AFF8>(int, int, const Maps &, const MmaAffParams &,
+extern template cudaError_t launch_fmt<F_AFF8>(int, int, const Maps &, const MmaHostParams &,
                                             const DeviceInfo &, cudaStream_t);
+#define QMM_EXTERN_GROUPED(F)                                                                \
+    extern template cudaError_t launch_fmt_grouped<F>(int, const Maps &, const MmaHostParams &, \
+                                                      const DeviceInfo &, cudaStream_t)
+QMM_EXTERN_GROUPED(F_BF16);
+QMM_EXTERN_GROUPED(F_F16);
+QMM_EXTERN_GROUPED(F_Q4_0);
+QMM_EXTERN_GROUPED(F_Q4_K);
+QMM_EXTERN_GROUPED(F_Q6_K);
+QMM_EXTERN_GROUPED(F_Q8_0);
+QMM_EXTERN_GROUPED(F_Q5_0);
+#undef QMM_EXTERN_GROUPED
 
 // y columns that split tiles add into: zeroed per token by the conversion kernel
 struct SplitZero {
@@ -34,6 +45,14 @@ struct SplitZero {
     int pairs, tiles_n, tok, rows;
 };
 
+// Rows of x in another order (expert-grouped products): x16 row t is x row
+// src[t] / top_k for t < *count, zeros beyond.
+struct XGather {
+    const int *src;     // null: row t is x row t
+    const int *count;
+    int top_k;
+};
+
 // X [N][k] fp32 -> X16 [N][kp] fp16 (zero padded) scaled by 2^-e per row so the
 // row's largest magnitude lands in [2^14, 2^15); xscale[t] = 2^e. With x16lo,
 // also the fp16 rounding of what X16 missed (x = hi + lo to ~22 bits).
@@ -41,9 +60,22 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const float *__restrict__
                                                        int64_t kp, __half *__restrict__ x16,
                                                        __half *__restrict__ x16lo,
                                                        float *__restrict__ xscale,
-                                                       const SplitZero z) {
+                                                       const SplitZero z, const XGather gx) {
     __shared__ float red[8];
     pdl_launch_dependents();  // the product kernel may start its W pipeline now
+    int64_t src_row = blockIdx.x;
+    if (gx.src) {
+        const int64_t t = blockIdx.x;
+        if (t >= *gx.count) {  // past the routed rows (block-uniform)
+            for (int64_t i = threadIdx.x; i < kp; i += blockDim.x) {
+                x16[t * kp + i] = __float2half_rn(0.0f);
+                x16lo[t * kp + i] = __float2half_rn(0.0f);
+            }
+            if (threadIdx.x == 0) xscale[t] = 1.0f;
+            return;
+        }
+        src_row = gx.src[t] / gx.top_k;
+    }
     if (z.y) {
         // split pair-tiles v >= first (v = q * tiles_n + nt) of this token's
         // token tile start at the first such v; they run to the last row tile
@@ -56,7 +88,7 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const float *__restrict__
         }
     }
     const int64_t t = blockIdx.x;
-    const float *xt = x + t * k;
+    const float *xt = x + src_row * k;
     float m = 0.0f;
     for (int64_t i = threadIdx.x; i < k; i += blockDim.x) m = fmaxf(m, fabsf(__ldg(xt + i)));
 #pragma unroll
@@ -173,7 +205,10 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
     const int P = pairs * tiles_n, NC = mma_clusters(dev);
     const int R = P % NC;
     const int KS = (int)(kp / kBK);
-    const bool split = mode != 3 && !m.accumulate && R > 0 && 2 * R <= NC && (KS + 3) / 4 >= 2;
+    // (not for the gated up product: a saturated gate makes act(g) * u_half
+    // subnormal, and fp32 atomic adds flush subnormals to zero)
+    const bool split = mode != 3 && !m.accumulate && !m.glu && R > 0 && 2 * R <= NC &&
+                       (KS + 3) / 4 >= 2;
     SplitZero z = {};
     if (split) {
         z.y = m.y;
@@ -182,7 +217,8 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
         z.pairs = pairs; z.tiles_n = tiles_n; z.tok = mode == 1 ? tok : tok;
         z.rows = rows_out;
     }
-    x_to_f16_kernel<<<(unsigned)m.n_tokens, 256, 0, s>>>(m.x, m.k, kp, x16, x16lo, xscale, z);
+    x_to_f16_kernel<<<(unsigned)m.n_tokens, 256, 0, s>>>(m.x, m.k, kp, x16, x16lo, xscale, z,
+                                                          XGather{});
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int bn = mode == 1 ? tok : 2 * tok;
@@ -216,7 +252,7 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    MmaAffParams p;
+    MmaHostParams p = {};
     p.w = m.w; p.y = m.y; p.xscale = xscale;
     p.sc = m.sc;
     p.bi = m.bi;
@@ -226,6 +262,8 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
     p.KS = (int)(kp / kBK);
     p.accumulate = m.accumulate;
     p.err = dev.err;
+    p.gate = m.gate;
+    p.glu = m.glu;
     p.pairs = pairs;
     p.tiles_n = tiles_n;
     p.full_units = split ? P - R : P;
@@ -242,6 +280,183 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
     case F_AFF4: return launch_fmt<F_AFF4>(mode, bn, mp, p, dev, s);
     case F_AFF8: return launch_fmt<F_AFF8>(mode, bn, mp, p, dev, s);
     default: return cudaErrorInvalidValue;
+    }
+}
+
+// ------------------------------------------------ expert-grouped products ----
+
+// One block: counts the valid (position, slot) pairs of each expert, lays the
+// experts' rows out one after another (row_off[e] .. row_off[e + 1]), gives
+// expert e ceil(count / tok) token tiles times `row_pairs` row pairs of
+// schedule units (unit_off), and scatters each pair's index to a row of its
+// expert (perm). The order within an expert is whatever the atomics give:
+// each output row is computed from its own x row alone, so the results do not
+// depend on it. Ids outside [0, E) are left out (their y rows untouched) and
+// reported through the device error word.
+constexpr int kRouteThreads = 1024;
+
+__global__ void __launch_bounds__(kRouteThreads)
+    expert_route_kernel(const int32_t *__restrict__ ids, int pairs, int E, int tok, int row_pairs,
+                        int *__restrict__ row_off, int *__restrict__ unit_off,
+                        int *__restrict__ perm, unsigned int *err) {
+    __shared__ int cnt[kMaxGroupedExperts];
+    __shared__ int wr[32], wu[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int e = tid; e < E; e += kRouteThreads) cnt[e] = 0;
+    __syncthreads();
+    for (int i = tid; i < pairs; i += kRouteThreads) {
+        const int e = ids[i];
+        if (e >= 0 && e < E)
+            atomicAdd(&cnt[e], 1);
+        else
+            record_error(err, DERR_BAD_ID);
+    }
+    __syncthreads();
+    // exclusive scans of rows and units: thread t takes experts [t * per, +per)
+    const int per = (E + kRouteThreads - 1) / kRouteThreads;
+    const int e0 = tid * per;
+    int sr = 0, su = 0;
+    for (int j = 0; j < per; ++j) {
+        const int e = e0 + j;
+        if (e < E) {
+            sr += cnt[e];
+            su += (cnt[e] + tok - 1) / tok * row_pairs;
+        }
+    }
+    int ir = sr, iu = su;  // inclusive within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(0xFFFFFFFFu, ir, o), b = __shfl_up_sync(0xFFFFFFFFu, iu, o);
+        if (lane >= o) { ir += a; iu += b; }
+    }
+    if (lane == 31) { wr[warp] = ir; wu[warp] = iu; }
+    __syncthreads();
+    if (warp == 0) {
+        int a = wr[lane], b = wu[lane];  // 32 warps of 32 threads
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int c = __shfl_up_sync(0xFFFFFFFFu, a, o), d = __shfl_up_sync(0xFFFFFFFFu, b, o);
+            if (lane >= o) { a += c; b += d; }
+        }
+        wr[lane] = a;
+        wu[lane] = b;
+    }
+    __syncthreads();
+    int br = (warp ? wr[warp - 1] : 0) + ir - sr, bu = (warp ? wu[warp - 1] : 0) + iu - su;
+    for (int j = 0; j < per; ++j) {
+        const int e = e0 + j;
+        if (e < E) {
+            const int c = cnt[e];
+            row_off[e] = br;
+            unit_off[e] = bu;
+            cnt[e] = br;  // becomes the expert's scatter cursor
+            br += c;
+            bu += (c + tok - 1) / tok * row_pairs;
+        }
+    }
+    if (tid == kRouteThreads - 1) {
+        row_off[E] = wr[31];
+        unit_off[E] = wu[31];
+    }
+    __syncthreads();
+    for (int i = tid; i < pairs; i += kRouteThreads) {
+        const int e = ids[i];
+        if (e >= 0 && e < E) perm[atomicAdd(&cnt[e], 1)] = i;
+    }
+}
+
+int grouped_token_tile(int64_t pairs, int64_t n_experts) {
+    const int64_t avg = (pairs + n_experts - 1) / n_experts;
+    int tok = 16;
+    while (tok < avg && tok < 128) tok <<= 1;
+    return tok;
+}
+
+size_t mma_grouped_workspace_bytes(int fmt, int64_t pairs, int64_t k, int64_t n_experts) {
+    return mma_workspace_bytes(fmt, pairs, k) + 2 * round256((size_t)(n_experts + 1) * 4) +
+           round256((size_t)pairs * 4);
+}
+
+cudaError_t launch_mma_grouped(const MmaGroupedLaunch &m, const DeviceInfo &dev, cudaStream_t s) {
+    const int64_t M = m.j1 - m.j0;
+    const int64_t P = m.n_pos * m.top_k;
+    if (M <= 0 || P <= 0) return cudaSuccess;
+    if (mma_mode(m.fmt, m.k) != 2 || is_affine(m.fmt) || m.n_experts > kMaxGroupedExperts)
+        return cudaErrorNotSupported;
+    EncodeTiledFn encode = get_encode_fn();
+    if (!encode) return cudaErrorNotSupported;
+    const int64_t kp = kpad(m.k);
+    const size_t one = round256((size_t)P * kp * 2);
+    uint8_t *ws = reinterpret_cast<uint8_t *>(m.workspace);
+    __half *x16 = reinterpret_cast<__half *>(ws);
+    __half *x16lo = reinterpret_cast<__half *>(ws + one);
+    float *xscale = reinterpret_cast<float *>(ws + 2 * one);
+    uint8_t *tail = ws + 2 * one + round256((size_t)P * 4);
+    const size_t eb = round256((size_t)(m.n_experts + 1) * 4);
+    int *row_off = reinterpret_cast<int *>(tail);
+    int *unit_off = reinterpret_cast<int *>(tail + eb);
+    int *perm = reinterpret_cast<int *>(tail + 2 * eb);
+    const int tok = grouped_token_tile(P, m.n_experts);
+    const int bn = 2 * tok;
+    const int64_t tiles_m = (M + kBM - 1) / kBM;
+    const int row_pairs = (int)((tiles_m + 1) / 2);
+    expert_route_kernel<<<1, kRouteThreads, 0, s>>>(m.ids, (int)P, (int)m.n_experts, tok,
+                                                     row_pairs, row_off, unit_off, perm, dev.err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    XGather gx;
+    gx.src = perm;
+    gx.count = row_off + m.n_experts;
+    gx.top_k = (int)m.top_k;
+    x_to_f16_kernel<<<(unsigned)P, 256, 0, s>>>(m.x, m.k, kp, x16, x16lo, xscale, SplitZero{}, gx);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    Maps mp;
+    if (!encode_x_map(encode, &mp.x, x16, kp, P, bn / 2) ||
+        !encode_x_map(encode, &mp.xlo, x16lo, kp, P, bn / 2))
+        return cudaErrorInvalidValue;
+    mp.w = mp.x;
+    if (raw_slice_bytes(m.fmt, 2) > 0) {
+        // the stacked slices as one 2-D byte tensor [n_experts * n][row_bytes]
+        const cuuint64_t dims[2] = {(cuuint64_t)m.row_bytes, (cuuint64_t)(m.n * m.n_experts)};
+        const cuuint64_t strides[1] = {(cuuint64_t)m.row_bytes};
+        const cuuint32_t box[2] = {144u, (cuuint32_t)kBM};
+        const cuuint32_t estr[2] = {1, 1};
+        if (encode(&mp.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(m.w), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    MmaHostParams p = {};
+    p.w = m.w; p.y = m.y; p.xscale = xscale;
+    p.k = m.k; p.n = m.n; p.n_tokens = P; p.row_bytes = m.row_bytes;
+    p.j0 = m.j0; p.j1 = m.j1;
+    p.KS = (int)(kp / kBK);
+    p.accumulate = m.accumulate;
+    p.err = dev.err;
+    p.pairs = row_pairs;
+    p.tiles_n = 1;
+    p.split = 1;
+    // an upper bound on the routed units (each expert with rows adds at most
+    // one partial token tile): the grid size; the kernel reads the count
+    const int64_t bound = (int64_t)row_pairs * ((P + tok - 1) / tok + std::min<int64_t>(m.n_experts, P));
+    p.n_units = (int)std::min<int64_t>(bound, 1 << 30);
+    p.full_units = p.n_units;
+    p.row_off = row_off;
+    p.unit_off = unit_off;
+    p.perm = perm;
+    p.n_experts = (int)m.n_experts;
+    p.slice_rows = m.n;
+    switch (m.fmt) {
+    case F_BF16: return launch_fmt_grouped<F_BF16>(bn, mp, p, dev, s);
+    case F_F16: return launch_fmt_grouped<F_F16>(bn, mp, p, dev, s);
+    case F_Q4_0: return launch_fmt_grouped<F_Q4_0>(bn, mp, p, dev, s);
+    case F_Q4_K: return launch_fmt_grouped<F_Q4_K>(bn, mp, p, dev, s);
+    case F_Q6_K: return launch_fmt_grouped<F_Q6_K>(bn, mp, p, dev, s);
+    case F_Q8_0: return launch_fmt_grouped<F_Q8_0>(bn, mp, p, dev, s);
+    case F_Q5_0: return launch_fmt_grouped<F_Q5_0>(bn, mp, p, dev, s);
+    default: return cudaErrorNotSupported;
     }
 }
 

@@ -66,6 +66,9 @@ struct MmaParams {
     int split;       // the remaining pair-tiles are computed as `split` k-ranges each
     int n_units;     // full_units + (pairs * tiles_n - full_units) * split
     unsigned int *err;
+    // gated pairs: y = act(gate) * (this product); act 1 SwiGLU, 2 GeGLU, 0 none
+    const float *gate;
+    int glu;
 };
 
 // Affine formats also read a bf16 scale and bias per group of 64 from two
@@ -76,8 +79,25 @@ struct MmaAffFields {
     int64_t aux_row_bytes;
 };
 struct MmaAffParams : MmaParams, MmaAffFields {};
-template <int FMT>
-using MmaParamsOf = typename std::conditional<is_affine(FMT), MmaAffParams, MmaParams>::type;
+
+// Expert-grouped products (mixture of experts over many positions): the
+// (position, slot) pairs are routed on the device into expert-sorted rows of
+// x; x row i of the sorted order goes to y row perm[i]. Expert e owns the
+// sorted rows [row_off[e], row_off[e + 1]) and the units
+// [unit_off[e], unit_off[e + 1]) of the schedule (its token tiles times the
+// row pairs), and W rows e * slice_rows + j. GGUF formats only.
+struct MmaGrpFields {
+    const int *row_off, *unit_off, *perm;
+    int n_experts;
+    int64_t slice_rows;
+};
+struct MmaGrpParams : MmaParams, MmaGrpFields {};
+// everything the host fills in
+struct MmaHostParams : MmaAffParams, MmaGrpFields {};
+template <int FMT, bool GRP = false>
+using MmaParamsOf = typename std::conditional<
+    GRP, MmaGrpParams,
+    typename std::conditional<is_affine(FMT), MmaAffParams, MmaParams>::type>::type;
 
 // Q4_K super-blocks of 128 rows staged raw by TMA (one 128 x 144-byte box per
 // 256-wide slice of k), then decoded from shared memory.
@@ -333,10 +353,11 @@ __device__ __forceinline__ void split_half_words(const float (&v)[32], bool lo, 
     }
 }
 
-template <int FMT, int BN, int MODE>
+template <int FMT, int BN, int MODE, bool GRP = false>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     mma_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmx_lo,
-               const __grid_constant__ CUtensorMap tmw, const MmaParamsOf<FMT> p) {
+               const __grid_constant__ CUtensorMap tmw, const MmaParamsOf<FMT, GRP> p) {
+    static_assert(!GRP || (!is_affine(FMT) && MODE == 2), "grouped products: GGUF formats, x split");
     constexpr int kRowsOut = MODE == 3 ? 64 : kBM;   // output rows per CTA
     constexpr int kTokOut = MODE == 1 ? BN : BN / 2;  // tokens per CTA
     constexpr int kSliceB = raw_slice_bytes(FMT, MODE);  // raw W tiles by TMA
@@ -387,24 +408,55 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // conversion kernel zeroed (0 + a + b is the same in either order, so the
     // result does not depend on which half lands first). Cluster c of C takes
     // units c, c + C, ...
+    //
+    // Grouped products take units expert by expert (unit_off, written by the
+    // routing kernel before this grid started): unit u of expert e is row
+    // pair q and token tile nt of e's sorted rows, never split.
     const int c0 = (int)(blockIdx.x >> 1), cstep = (int)(gridDim.x >> 1);
     struct Tile {
-        int64_t m0;
-        int n0, rot;
+        int64_t m0;      // first output column (row of W within its slice)
+        int64_t wrow;    // first row of W in the stacked weights
+        int n0, rot;     // first x row (sorted order for grouped products)
+        int tok_end;     // end of this tile's valid x rows
         int k_lo, k_hi;  // k-steps of this unit
         int part;        // k-range index, or -1 for a whole tile
     };
+    int n_units = p.n_units;
+    if constexpr (GRP) n_units = __ldg(p.unit_off + p.n_experts);
     auto tile_of = [&](int u) {
         int v = u, part = -1;
-        if (u >= p.full_units) {
-            const int w = u - p.full_units;
-            v = p.full_units + w / p.split;
-            part = w % p.split;
-        }
-        const int q = v / p.tiles_n, nt = v - q * p.tiles_n;
+        int q, nt;
         Tile t;
-        t.m0 = p.j0 + (int64_t)(2 * q + (int)crank) * kRowsOut;
-        t.n0 = nt * kTokOut;
+        if constexpr (GRP) {
+            // expert e: the last with unit_off[e] <= u (experts without rows
+            // own no units)
+            int lo = 0, hi = p.n_experts;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (__ldg(p.unit_off + mid) <= u) lo = mid; else hi = mid;
+            }
+            const int r0 = __ldg(p.row_off + lo), r1 = __ldg(p.row_off + lo + 1);
+            const int ntile = (r1 - r0 + kTokOut - 1) / kTokOut;
+            const int local = u - __ldg(p.unit_off + lo);
+            q = local / ntile;
+            nt = local - q * ntile;
+            t.n0 = r0 + nt * kTokOut;
+            t.tok_end = r1;
+            t.m0 = p.j0 + (int64_t)(2 * q + (int)crank) * kRowsOut;
+            t.wrow = (int64_t)lo * p.slice_rows + t.m0;
+        } else {
+            if (u >= p.full_units) {
+                const int w = u - p.full_units;
+                v = p.full_units + w / p.split;
+                part = w % p.split;
+            }
+            q = v / p.tiles_n;
+            nt = v - q * p.tiles_n;
+            t.n0 = nt * kTokOut;
+            t.tok_end = (int)p.n_tokens;
+            t.m0 = p.j0 + (int64_t)(2 * q + (int)crank) * kRowsOut;
+            t.wrow = t.m0;
+        }
         t.part = part;
         if (part < 0) {
             t.k_lo = 0;
@@ -471,7 +523,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
         int bcount = 0;  // x stages issued so far (all tiles)
         int it = 0;
-        for (int u = c0; u < p.n_units; u += cstep, ++it) {
+        for (int u = c0; u < n_units; u += cstep, ++it) {
             if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
             const Tile t = tile_of(u);
             // the tile's token scales (2^e of each token's fp16 conversion) for
@@ -485,7 +537,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 }
             }
             for (int i = lane; i < kTokOut; i += 32)
-                xs_s[xb * kTokOut + i] = t.n0 + i < p.n_tokens ? __ldg(p.xscale + t.n0 + i) : 0.0f;
+                xs_s[xb * kTokOut + i] = t.n0 + i < t.tok_end ? __ldg(p.xscale + t.n0 + i) : 0.0f;
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(xsFull(xb));
@@ -534,7 +586,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         int abase = 0, bbase = 0;  // A / x stages consumed by earlier tiles
         int it = 0;
         bool failed = false;
-        for (int u = c0; u < p.n_units && !failed; u += cstep, ++it) {
+        for (int u = c0; u < n_units && !failed; u += cstep, ++it) {
             const Tile t = tile_of(u);
             const int KSu = nks(t);
             if (it > 0) {  // the epilogue has drained the accumulator
@@ -594,7 +646,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         if (kRaw && lane == 0) {
             prefetch_tmap(&tmw);
             int rcount = 0;
-            for (int u = c0; u < p.n_units; u += cstep) {
+            for (int u = c0; u < n_units; u += cstep) {
                 if (*abort_flag) break;
                 const Tile t = tile_of(u);
                 bool ok = true;
@@ -615,7 +667,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                     for (int bx = 0; bx < kBoxes; ++bx)
                         tma_load_2d(W0 + rs * kRawB + (uint32_t)bx * (kRawB / kBoxes), &tmw,
                                     kSliceB * (kx(t, 4 * b) >> 2) + bx * (kSliceB / kBoxes),
-                                    (int)t.m0, rawFull(rs));
+                                    (int)t.wrow, rawFull(rs));
                 }
                 if (!ok) break;
             }
@@ -664,7 +716,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             }
         };
         int it = 0;
-        for (int u = c0; u < p.n_units && !failed; u += cstep, ++it) {
+        for (int u = c0; u < n_units && !failed; u += cstep, ++it) {
             const Tile t = tile_of(u);
             const int KSu = nks(t);
             if constexpr (kRaw) {
@@ -684,7 +736,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                     if constexpr (FMT != F_Q4_K) {
                         if (row_ok) {
                             // the unit's super-block b is k-step t.k_lo + 4 b (before rotation)
-                            const int64_t ao = (t.m0 + r) * p.aux_row_bytes +
+                            const int64_t ao = (t.wrow + r) * p.aux_row_bytes +
                                                8 * (kx(t, t.k_lo + 4 * b) >> 2);
                             sc4 = __ldg(reinterpret_cast<const uint2 *>(p.sc + ao));
                             bi4 = __ldg(reinterpret_cast<const uint2 *>(p.bi + ao));
@@ -786,13 +838,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 rcount = rbase + NSBLK;
             } else {
                 const bool lo_part = MODE == 3 && r >= 64;  // MODE 3: rows 64..127 hold W_lo
-                const int64_t j = t.m0 + (MODE == 3 ? (r & 63) : r);
+                const int64_t rj = MODE == 3 ? (r & 63) : r;
+                const int64_t j = t.m0 + rj;
                 const bool row_ok = j < p.j1;
-                const uint8_t *rowp = p.w + (row_ok ? j : 0) * p.row_bytes;
+                const uint8_t *rowp = p.w + (row_ok ? t.wrow + rj : 0) * p.row_bytes;
                 // 32 weights of this row at k0 (affine: with the group's scale and bias)
                 auto load_raw = [&](Raw32<FMT> &r, int64_t k0, int nv) {
                     if constexpr (is_affine(FMT)) {
-                        const int64_t ao = (row_ok ? j : 0) * p.aux_row_bytes;
+                        const int64_t ao = (row_ok ? t.wrow + rj : 0) * p.aux_row_bytes;
                         r.load(rowp, p.sc + ao, p.bi + ao, k0);
                     } else {
                         r.load(rowp, k0, nv);
@@ -943,12 +996,19 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                     }
                     if (store_ok) {
                         const int64_t t0 = t.n0 + col;
-                        float *yp = p.y + t0 * p.n + je;
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            if (t0 + i < p.n_tokens) {
-                                const float val = acc[i] * xsc[col + i];
-                                float *yq = yp + (int64_t)i * p.n;
+                            if (t0 + i < t.tok_end) {
+                                float val = acc[i] * xsc[col + i];
+                                // grouped products: sorted x row -> its y row
+                                int64_t yrow = t0 + i;
+                                if constexpr (GRP) yrow = __ldg(p.perm + t0 + i);
+                                if (p.glu) {
+                                    // act(g) u is linear in u: split k-halves add their share
+                                    const float g = __ldg(p.gate + yrow * p.n + je);
+                                    val *= p.glu == 1 ? glu_act<1>(g) : glu_act<2>(g);
+                                }
+                                float *yq = p.y + yrow * p.n + je;
                                 if (split)
                                     atomicAdd(yq, val);
                                 else
@@ -988,10 +1048,16 @@ int mma_clusters(const DeviceInfo &dev);
 // Persistent grid: clusters of two CTAs, as many as can be resident at once
 // (one CTA per SM), capped by the number of row-tile pairs x token tiles.
 // MODE 3 keeps one tile per CTA (its epilogue scratch lives in the x ring).
-template <int FMT, int BN, int MODE>
-static cudaError_t launch_t(const Maps &mp, const MmaAffParams &h, const DeviceInfo &dev,
+template <int FMT, int BN, int MODE, bool GRP = false>
+static cudaError_t launch_t(const Maps &mp, const MmaHostParams &h, const DeviceInfo &dev,
                             cudaStream_t s) {
-    const MmaParamsOf<FMT> p = h;
+    MmaParamsOf<FMT, GRP> p;
+    if constexpr (GRP) {
+        static_cast<MmaParams &>(p) = static_cast<const MmaParams &>(h);
+        static_cast<MmaGrpFields &>(p) = static_cast<const MmaGrpFields &>(h);
+    } else {
+        p = static_cast<const MmaParamsOf<FMT> &>(static_cast<const MmaAffParams &>(h));
+    }
     using C = MmaCfg<BN, kBM * raw_slice_bytes(FMT, MODE)>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -1008,13 +1074,13 @@ static cudaError_t launch_t(const Maps &mp, const MmaAffParams &h, const DeviceI
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(mma_kernel<FMT, BN, MODE>,
+        attr_err = cudaFuncSetAttribute(mma_kernel<FMT, BN, MODE, GRP>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
         if (attr_err != cudaSuccess) return;
         cudaLaunchConfig_t q = cfg;
         q.gridDim = dim3(2 * (unsigned)(dev.sm_count / 2));
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<FMT, BN, MODE>, &q) != cudaSuccess ||
+        if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<FMT, BN, MODE, GRP>, &q) != cudaSuccess ||
             n <= 0) {
             (void)cudaGetLastError();
             n = dev.sm_count / 2;
@@ -1023,24 +1089,27 @@ static cudaError_t launch_t(const Maps &mp, const MmaAffParams &h, const DeviceI
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int P = p.pairs * p.tiles_n;
+    // grouped products: n_units is an upper bound (the routed count is on the device)
     const int clusters = MODE == 3 ? P : std::min(p.n_units, max_clusters);
     cfg.gridDim = dim3(2 * (unsigned)clusters);
     // programmatic launch after the x conversion kernel (see pdl_wait_prev)
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, mma_kernel<FMT, BN, MODE>, mp.x, mp.xlo, mp.w, p);
+    return cudaLaunchKernelEx(&cfg, mma_kernel<FMT, BN, MODE, GRP>, mp.x, mp.xlo, mp.w, p);
 }
 
-template <int FMT, int MODE>
-static cudaError_t launch_bn(int bn, const Maps &mp, const MmaAffParams &p, const DeviceInfo &dev,
+template <int FMT, int MODE, bool GRP = false>
+static cudaError_t launch_bn(int bn, const Maps &mp, const MmaHostParams &p, const DeviceInfo &dev,
                              cudaStream_t s) {
     switch (bn) {
-    case 16: if (MODE == 1) return launch_t<FMT, 16, MODE>(mp, p, dev, s); break;
-    case 32: return launch_t<FMT, 32, MODE>(mp, p, dev, s);
-    case 64: return launch_t<FMT, 64, MODE>(mp, p, dev, s);
-    case 128: return launch_t<FMT, 128, MODE>(mp, p, dev, s);
-    case 256: return launch_t<FMT, 256, MODE>(mp, p, dev, s);
+    case 16:
+        if constexpr (MODE == 1) return launch_t<FMT, 16, MODE, GRP>(mp, p, dev, s);
+        break;
+    case 32: return launch_t<FMT, 32, MODE, GRP>(mp, p, dev, s);
+    case 64: return launch_t<FMT, 64, MODE, GRP>(mp, p, dev, s);
+    case 128: return launch_t<FMT, 128, MODE, GRP>(mp, p, dev, s);
+    case 256: return launch_t<FMT, 256, MODE, GRP>(mp, p, dev, s);
     default: break;
     }
     return cudaErrorInvalidValue;
@@ -1049,7 +1118,7 @@ static cudaError_t launch_bn(int bn, const Maps &mp, const MmaAffParams &p, cons
 // Instantiated (explicitly) by the qmm_mma_inst_*.cu units, one group of
 // formats each.
 template <int FMT>
-cudaError_t launch_fmt(int mode, int bn, const Maps &mp, const MmaAffParams &p,
+cudaError_t launch_fmt(int mode, int bn, const Maps &mp, const MmaHostParams &p,
                        const DeviceInfo &dev, cudaStream_t s) {
     constexpr bool quant = FMT != F_BF16 && FMT != F_F16;
     if (mode == 2) return launch_bn<FMT, 2>(bn, mp, p, dev, s);
@@ -1057,8 +1126,22 @@ cudaError_t launch_fmt(int mode, int bn, const Maps &mp, const MmaAffParams &p,
     return cudaErrorInvalidValue;
 }
 
+// The expert-grouped instances (split x only), in units of their own.
+template <int FMT>
+cudaError_t launch_fmt_grouped(int bn, const Maps &mp, const MmaHostParams &p,
+                               const DeviceInfo &dev, cudaStream_t s) {
+    if constexpr (is_affine(FMT)) {
+        return cudaErrorNotSupported;
+    } else {
+        return launch_bn<FMT, 2, true>(bn, mp, p, dev, s);
+    }
+}
+
 #define QMM_MMA_INSTANTIATE(F)                                                               \
-    template cudaError_t launch_fmt<F>(int, int, const Maps &, const MmaAffParams &,          \
+    template cudaError_t launch_fmt<F>(int, int, const Maps &, const MmaHostParams &,         \
                                        const DeviceInfo &, cudaStream_t)
+#define QMM_MMA_INSTANTIATE_GROUPED(F)                                                       \
+    template cudaError_t launch_fmt_grouped<F>(int, const Maps &, const MmaHostParams &,      \
+                                               const DeviceInfo &, cudaStream_t)
 
 }  // namespace qmm

@@ -277,7 +277,7 @@ def test_glu_workspace_and_empty_work(lib):
     assert q.qmm_glu_workspace_bytes(_args(k=4096, n=14336)) == 0          # fused GEMV
     a = _args(k=4096, n=1000, n_tokens=8)
     one = (8 * 1000 * 4 + 255) // 256 * 256
-    assert q.qmm_glu_workspace_bytes(a) == 2 * one + 2 * 8 * 4096 * 2 + 256
+    assert q.qmm_glu_workspace_bytes(a) == one + 2 * 8 * 4096 * 2 + 256
     assert q.qmm_glu_workspace_bytes(_args(fmt="affine4", k=128)) == 0
     assert q.qmm_matmul_glu(_args(j_start=3, j_end=3), None, 1) == 0
 

@@ -22,6 +22,7 @@ RECIPES = {
 EXPERT_RECIPES = {  # (fmt, k, n, n_experts, top_k, n_pos, seed)
     "q8_0_experts": ("q8_0", 2048, 768, 64, 8, 1, 6),
     "q5_0_experts": ("q5_0", 2048, 768, 64, 8, 1, 7),
+    "q4_k_experts": ("q4_k", 2048, 768, 64, 8, 1, 14),
 }
 AFFINE_RECIPES = {  # (bits, k, n, n_tokens, seed)
     "affine4_gemv": (4, 4096, 14336, 1, 10),
