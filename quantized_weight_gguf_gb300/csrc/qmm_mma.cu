@@ -252,7 +252,26 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
+    // y through shared memory and tensor stores: split-x mode, no gated
+    // epilogue, rows of y 16-byte aligned (n % 4 == 0) and the column tile
+    // starting on a 16-byte boundary; the map's columns end at j1, so the
+    // stores never touch columns outside the tile
+    const bool tma_epi = mode == 2 && !m.glu && m.n % 4 == 0 && m.j0 % 4 == 0 &&
+                         (reinterpret_cast<uintptr_t>(m.y) & 15u) == 0;
+    mp.y = mp.x;
+    if (tma_epi) {
+        const cuuint64_t dims[2] = {(cuuint64_t)m.j1, (cuuint64_t)m.n_tokens};
+        const cuuint64_t strides[1] = {(cuuint64_t)m.n * 4};
+        const cuuint32_t box[2] = {32u, 16u};
+        const cuuint32_t estr[2] = {1, 1};
+        if (encode(&mp.y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, m.y, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     MmaHostParams p = {};
+    p.tma_epi = tma_epi ? 1 : 0;
     p.w = m.w; p.y = m.y; p.xscale = xscale;
     p.sc = m.sc;
     p.bi = m.bi;
@@ -416,6 +435,7 @@ cudaError_t launch_mma_grouped(const MmaGroupedLaunch &m, const DeviceInfo &dev,
         !encode_x_map(encode, &mp.xlo, x16lo, kp, P, bn / 2))
         return cudaErrorInvalidValue;
     mp.w = mp.x;
+    mp.y = mp.x;  // rows of y are scattered: stored from registers
     if (raw_slice_bytes(m.fmt, 2) > 0) {
         // the stacked slices as one 2-D byte tensor [n_experts * n][row_bytes]
         const cuuint64_t dims[2] = {(cuuint64_t)m.row_bytes, (cuuint64_t)(m.n * m.n_experts)};

@@ -12,7 +12,7 @@ int mma_clusters(const DeviceInfo &dev) {
         cudaLaunchConfig_t q = {};
         q.gridDim = dim3(2 * (unsigned)(dev.sm_count / 2));
         q.blockDim = dim3(kMmaThreads);
-        q.dynamicSmemBytes = MmaCfg<256, kRawBytes>::kSmem;
+        q.dynamicSmemBytes = MmaCfg<256, kRawBytes, kEpiStageBytes>::kSmem;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
@@ -23,7 +23,7 @@ int mma_clusters(const DeviceInfo &dev) {
         int v = 0;
         if (cudaFuncSetAttribute(mma_kernel<F_Q4_K, 256, 2>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)MmaCfg<256, kRawBytes>::kSmem) != cudaSuccess ||
+                                 (int)MmaCfg<256, kRawBytes, kEpiStageBytes>::kSmem) != cudaSuccess ||
             cudaOccupancyMaxActiveClusters(&v, mma_kernel<F_Q4_K, 256, 2>, &q) != cudaSuccess ||
             v <= 0) {
             (void)cudaGetLastError();

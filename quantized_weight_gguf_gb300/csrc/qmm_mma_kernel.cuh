@@ -69,6 +69,7 @@ struct MmaParams {
     // gated pairs: y = act(gate) * (this product); act 1 SwiGLU, 2 GeGLU, 0 none
     const float *gate;
     int glu;
+    int tma_epi;  // y written through shared memory by tensor stores (map tmy)
 };
 
 // Affine formats also read a bf16 scale and bias per group of 64 from two
@@ -121,7 +122,14 @@ __host__ __device__ constexpr int raw_slice_bytes(int fmt, int mode) {
 // then pays one raw-tile wait, one slot wait and one arrival per two decoded
 // chunks. An x stage is KB k-steps, 32 KB at most (the x tile of 256 tokens
 // is 32 KB per k-step).
-template <int BN, int RAWB>  // RAWB: bytes of one raw W tile (0: no raw ring)
+// The epilogue stages y in shared memory and writes it with tensor stores
+// (split x mode, ungrouped products): each of the 16 dequant warps owns
+// 2 KB, 32 rows x 16 tokens of fp32.
+constexpr int kEpiStageBytes = 16 * 2048;
+__host__ __device__ constexpr bool mma_tma_epilogue(int mode, bool grp) { return mode == 2 && !grp; }
+
+// EPI: bytes of the epilogue's staging area (0: y stored from registers).
+template <int BN, int RAWB, int EPI = 0>  // RAWB: bytes of one raw W tile (0: no raw ring)
 struct MmaCfg {
     static constexpr bool RAW = RAWB > 0;
     static constexpr int KA = 4;
@@ -129,9 +137,13 @@ struct MmaCfg {
     static constexpr int kBBytes = BN * kBK * 2;            // one k-step of x
     static constexpr int kBStage = KB * kBBytes;
     static constexpr int kAccCols = BN < 32 ? 32 : BN;      // one accumulator
-    // two accumulators (even k-steps into one, odd into the other, summed at
-    // the end) where TMEM has room: back-to-back MMAs then do not wait on
-    // each other's result
+    // Two accumulators where TMEM has room: the K = 16 steps of a k-step go
+    // to them in turn (summed in the epilogue), so back-to-back MMAs do not
+    // wait on each other's result. An MMA into the accumulator the one before
+    // it wrote waits for that result (a k-step of four such MMAs measured
+    // about 290 cycles at N = 32, where each MMA's work is 16 cycles); at
+    // BN = 256 an MMA's own 128 cycles cover it and one accumulator leaves
+    // TMEM to the A ring.
     static constexpr int kNAcc = BN >= 256 ? 1 : 2;
     static constexpr int kACol0 = kNAcc * kAccCols;         // first A column
     static constexpr int kAStageCols = KA * 32;
@@ -142,21 +154,31 @@ struct MmaCfg {
     // k-steps (two stages at least); HBM latency is hidden by the raw ring, L2
     // latency by the x ring (8 raw stages at small token tiles measured no
     // faster at N <= 32 and slower at N = 64)
-    static constexpr int kNBMin = (4 + KB - 1) / KB < 2 ? 2 : (4 + KB - 1) / KB;
-    static constexpr int kRawFit = RAW ? (212 * 1024 - kNBMin * kBStage) / RAWB : 0;
+    // The rings and the epilogue staging area share kBudget bytes (the rest
+    // of the 227 KB goes to alignment, barriers and token scales). At
+    // BN = 256 the x ring keeps four one-k-step stages (three measured 50 %
+    // slower k-loops: L2 latency is no longer covered); the raw ring then
+    // gets what is left, three or four stages (two x stages fewer only when
+    // a raw tile is so large that fewer than two would fit).
+    static constexpr int kBudget = 220 * 1024;
+    static constexpr int kNBWant = (4 + KB - 1) / KB < 2 ? 2 : (4 + KB - 1) / KB;
+    static constexpr bool kShrinkX =
+        RAW && KB == 1 && (kBudget - kNBWant * kBStage - EPI) / RAWB < 2;
+    static constexpr int kNBMin = kShrinkX ? kNBWant - 1 : kNBWant;
+    static constexpr int kRawFit = RAW ? (kBudget - kNBMin * kBStage - EPI) / RAWB : 0;
     static constexpr int kNR = RAW ? (kRawFit > 4 ? 4 : kRawFit) : 1;
     static_assert(!RAW || kNR >= 2, "raw W ring too shallow");
-    static constexpr int kAvail = 212 * 1024 - (RAW ? kNR * RAWB : 0);
+    static constexpr int kAvail = kBudget - (RAW ? kNR * RAWB : 0) - EPI;
     static constexpr int NB = (kAvail / kBStage) > 8 ? 8 : (kAvail / kBStage);
     static constexpr size_t kSmemUsed = (size_t)NB * kBStage +
-                                        (RAW ? (size_t)kNR * RAWB : 0) + 1024 /*align*/ +
+                                        (RAW ? (size_t)kNR * RAWB : 0) + EPI + 1024 /*align*/ +
                                         512 /*barriers*/ + 2048 /*token scales*/;
     // at least half of the SM's shared memory, so that no second CTA can be
     // resident and block in its TMEM allocation (every CTA takes all 512
     // columns) while holding resources its cluster peer waits for
     static constexpr size_t kSmem = kSmemUsed < 120 * 1024 ? 120 * 1024 : kSmemUsed;
-    // the output tile (rows x tokens fp32) is staged over the x ring
-    static_assert(NB * kBStage >= kBM * BN * 4, "x ring too small for the output tile");
+    // MODE 3 parks its low rows' sums ([BN/2 tokens][64 rows] fp32) over the x ring
+    static_assert(NB * kBStage >= BN * 128, "x ring too small for the MODE 3 epilogue");
     static_assert(NB >= 2 && NA >= 2, "rings too shallow");
 };
 
@@ -356,21 +378,26 @@ __device__ __forceinline__ void split_half_words(const float (&v)[32], bool lo, 
 template <int FMT, int BN, int MODE, bool GRP = false>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     mma_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmx_lo,
-               const __grid_constant__ CUtensorMap tmw, const MmaParamsOf<FMT, GRP> p) {
+               const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmy,
+               const MmaParamsOf<FMT, GRP> p) {
     static_assert(!GRP || (!is_affine(FMT) && MODE == 2), "grouped products: GGUF formats, x split");
     constexpr int kRowsOut = MODE == 3 ? 64 : kBM;   // output rows per CTA
     constexpr int kTokOut = MODE == 1 ? BN : BN / 2;  // tokens per CTA
     constexpr int kSliceB = raw_slice_bytes(FMT, MODE);  // raw W tiles by TMA
     constexpr bool kRaw = kSliceB > 0;
     constexpr int kRawB = kBM * kSliceB;
-    using C = MmaCfg<BN, kRawB>;
+    // y through shared memory and tensor stores (the host enables it per call)
+    constexpr bool kTmaEpi = mma_tma_epilogue(MODE, GRP);
+    constexpr int kEpiB = kTmaEpi ? kEpiStageBytes : 0;
+    using C = MmaCfg<BN, kRawB, kEpiB>;
     constexpr int NA = C::NA, NB = C::NB, kNR = C::kNR, KA = C::KA, KB = C::KB;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
     const uint32_t B0 = sbase;                                     // x ring
     const uint32_t W0 = B0 + NB * C::kBStage;                      // raw W stages (kRaw)
-    const uint32_t bar0 = W0 + (kRaw ? kNR * kRawB : 0);
+    const uint32_t E0 = W0 + (kRaw ? kNR * kRawB : 0);              // epilogue staging (kTmaEpi)
+    const uint32_t bar0 = E0 + kEpiB;
     auto fullA = [&](int s) { return bar0 + 8u * s; };
     auto emptyA = [&](int s) { return bar0 + 8u * (NA + s); };
     auto fullB = [&](int s) { return bar0 + 8u * (2 * NA + s); };
@@ -536,11 +563,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                     break;
                 }
             }
-            for (int i = lane; i < kTokOut; i += 32)
-                xs_s[xb * kTokOut + i] = t.n0 + i < t.tok_end ? __ldg(p.xscale + t.n0 + i) : 0.0f;
-            __syncwarp();
+            // the scale loads are issued now and stored after the tile's x
+            // stages have gone out (the epilogue needs them only at the end)
+            constexpr int kScl = (kTokOut + 31) / 32;
+            float scl[kScl];
+#pragma unroll
+            for (int j = 0; j < kScl; ++j) {
+                const int i = lane + 32 * j;
+                scl[j] = i < kTokOut && t.n0 + i < t.tok_end ? __ldg(p.xscale + t.n0 + i) : 0.0f;
+            }
             if (lane == 0) {
-                mbar_arrive(xsFull(xb));
                 const int NSB = nsb(t);
                 for (int st = 0; st < NSB; ++st, ++bcount) {
                     const int slot = bcount % NB;
@@ -572,6 +604,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 }
             }
             __syncwarp();
+#pragma unroll
+            for (int j = 0; j < kScl; ++j)
+                if (lane + 32 * j < kTokOut) xs_s[xb * kTokOut + lane + 32 * j] = scl[j];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xsFull(xb));
         }
         // no copy may land after this CTA exits
         if (lane == 0)
@@ -622,12 +659,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                         tmem + (uint32_t)(C::kACol0 + sa * C::kAStageCols + (ks % KA) * 32);
                     const uint64_t bd =
                         sdesc_sw128(B0 + sb * C::kBStage + (ks % KB) * C::kBBytes);
-                    const uint32_t dacc =
-                        tmem + (uint32_t)((C::kNAcc == 2 ? (ks & 1) : 0) * C::kAccCols);
-                    const bool acc0 = C::kNAcc == 2 ? ks > 1 : ks > 0;
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16: 8 A columns, 32 B bytes
-                        tc_mma_f16_ts(dacc, at + 8 * kk, bd + 2 * kk, idesc, acc0 || kk != 0);
+                    for (int kk = 0; kk < kBK / 16; ++kk) {  // K = 16: 8 A columns, 32 B bytes
+                        // K step kk goes to accumulator kk % kNAcc; the tile's
+                        // first MMA into each accumulator overwrites it
+                        const int a = kk % C::kNAcc;
+                        tc_mma_f16_ts(tmem + (uint32_t)(a * C::kAccCols), at + 8 * kk, bd + 2 * kk,
+                                      idesc, ks > 0 || kk >= C::kNAcc);
+                    }
                     const bool last = ks == KSu - 1;
                     if (ks % KB == KB - 1 || last)
                         tc_commit_multicast(emptyB(sb), (uint16_t)3);  // both CTAs may refill
@@ -939,31 +978,22 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             // MODE 3 row-pair scratch [col][64] over the x ring (MODE 3 CTAs
             // take one tile each: nothing is prefetched into the ring)
             float *scratch = reinterpret_cast<float *>(smem_raw + (B0 - raw_addr));
-            // the two accumulators (even / odd k-steps) are summed here; KS == 1
-            // leaves the odd one unwritten
-            const bool two_acc = C::kNAcc == 2 && KSu > 1;
-            // (one accumulator's hi and lo columns at a time: 32 registers live)
+            // the accumulators are summed here (every one was written: a
+            // k-step has four K steps); one accumulator's hi and lo columns at
+            // a time, 32 registers live
             auto load_acc = [&](int col, float (&acc)[16]) {
-                uint32_t v[16], v2[16];
-                tmem_ld16(tlane + (uint32_t)col, v);
-                if (MODE == 1) {
-                    if (two_acc) tmem_ld16(tlane + (uint32_t)(C::kAccCols + col), v2);
+#pragma unroll
+                for (int a = 0; a < C::kNAcc; ++a) {
+                    uint32_t v[16], v2[16];
+                    const uint32_t base = tlane + (uint32_t)(a * C::kAccCols + col);
+                    tmem_ld16(base, v);
+                    if (MODE != 1) tmem_ld16(base + (uint32_t)(BN / 2), v2);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        acc[i] = __uint_as_float(v[i]) + (two_acc ? __uint_as_float(v2[i]) : 0.0f);
-                } else {
-                    tmem_ld16(tlane + (uint32_t)(col + BN / 2), v2);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[i] = __uint_as_float(v[i]) + __uint_as_float(v2[i]);
-                    if (two_acc) {
-                        tmem_ld16(tlane + (uint32_t)(C::kAccCols + col), v);
-                        tmem_ld16(tlane + (uint32_t)(C::kAccCols + col + BN / 2), v2);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            acc[i] += __uint_as_float(v[i]) + __uint_as_float(v2[i]);
+                    for (int i = 0; i < 16; ++i) {
+                        const float d = MODE != 1 ? __uint_as_float(v[i]) + __uint_as_float(v2[i])
+                                                  : __uint_as_float(v[i]);
+                        acc[i] = a == 0 ? d : acc[i] + d;
                     }
                 }
             };
@@ -986,7 +1016,34 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                     *abort_flag = 1;
                 }
             }
-            if ((MODE != 3 || quarter < 2) && scr_ok) {
+            if (kTmaEpi && p.tma_epi) {
+                // each warp: its 32 rows x 16 tokens through its 2 KB staging
+                // area (token-major: the layout of y) and one tensor store (or
+                // add); the stores run on while the warps decode the next
+                // tile. Tokens past n_tokens and columns past j1 fall outside
+                // the tensor map and are not written.
+                const uint32_t ereg = E0 + (uint32_t)(warp - 2) * 2048u;
+                const bool add = p.accumulate || split;
+                for (int col = c_lo; col < c_hi; col += 16) {
+                    float acc[16];
+                    load_acc(col, acc);
+                    if (lane == 0) bulk_wait_group_read0();  // the area's last store has read it
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        sts32f(ereg + (uint32_t)(128 * i + 4 * lane), acc[i] * xsc[col + i]);
+                    fence_proxy_async_smem();  // visible to the tensor store
+                    __syncwarp();
+                    if (lane == 0 && !*abort_flag) {
+                        const int cx = (int)(t.m0 + 32 * quarter), cy = t.n0 + col;
+                        if (add)
+                            tma_reduce_add_2d(&tmy, cx, cy, ereg);
+                        else
+                            tma_store_2d(&tmy, cx, cy, ereg);
+                        bulk_commit_group();
+                    }
+                }
+            } else if ((MODE != 3 || quarter < 2) && scr_ok) {
                 for (int col = c_lo; col < c_hi; col += 16) {
                     float acc[16];
                     load_acc(col, acc);
@@ -1026,6 +1083,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 mbar_arrive(xsFree(xb));
             }
         }
+        // this warp's tensor stores of y complete before the CTA exits
+        if (kTmaEpi && p.tma_epi && lane == 0) bulk_wait_group0();
     }
     tc_fence_before();
     __syncthreads();
@@ -1038,7 +1097,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 }
 
 struct Maps {
-    CUtensorMap x, xlo, w;
+    CUtensorMap x, xlo, w, y;
 };
 
 // Clusters of two CTAs that can be resident at once (defined beside the Q4_K
@@ -1058,7 +1117,8 @@ static cudaError_t launch_t(const Maps &mp, const MmaHostParams &h, const Device
     } else {
         p = static_cast<const MmaParamsOf<FMT> &>(static_cast<const MmaAffParams &>(h));
     }
-    using C = MmaCfg<BN, kBM * raw_slice_bytes(FMT, MODE)>;
+    using C = MmaCfg<BN, kBM * raw_slice_bytes(FMT, MODE),
+                     mma_tma_epilogue(MODE, GRP) ? kEpiStageBytes : 0>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     static int max_clusters = 0;
@@ -1096,7 +1156,7 @@ static cudaError_t launch_t(const Maps &mp, const MmaHostParams &h, const Device
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, mma_kernel<FMT, BN, MODE, GRP>, mp.x, mp.xlo, mp.w, p);
+    return cudaLaunchKernelEx(&cfg, mma_kernel<FMT, BN, MODE, GRP>, mp.x, mp.xlo, mp.w, mp.y, p);
 }
 
 template <int FMT, int MODE, bool GRP = false>
