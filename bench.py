@@ -793,6 +793,8 @@ def run_case(args):
         base = name
     if name.endswith("_backward_input"):
         return run_case_backward(args, torch, q, lib, r, name[:-len("_backward_input")])
+    if "_experts_pos" in name:
+        return run_case_experts(args, torch, q, lib, r, name)
     if name in qmm_synth.AFFINE_WORKLOADS:
         return run_case_affine(args, torch, q, lib, r, name)
     fmt, k, n, w, x = qmm_synth.workload(base, n_tokens=nt)
@@ -856,6 +858,41 @@ def run_case_affine(args, torch, q, lib, r, name):
     return 0
 
 
+def run_case_experts(args, torch, q, lib, r, name):
+    """An expert workload at some positions: <workload>_pos<N>[_gemv|_grouped]."""
+    import ctypes
+    base, rest = name.split("_pos")
+    parts = rest.split("_")
+    n_pos = int(parts[0])
+    path = {"gemv": q.PATH_GEMV, "grouped": q.PATH_MMA}.get(parts[1] if len(parts) > 1 else "",
+                                                           q.PATH_AUTO)
+    fmt, k, n, n_exp, w, x, ids = qmm_synth.expert_workload(base, n_pos=n_pos)
+    dev, stream = r.dev, r.stream
+    ncop = 1 if args.no_rotate else r.copies_for(w.size)
+    wc = r.weights(w, ncop)
+    xd = torch.from_numpy(x).to(dev)
+    idd = torch.from_numpy(ids).to(dev)
+    yd = torch.empty((ids.size, n), device=dev)
+    al = [q.make_args(fmt, wc[c], xd, yd, k, n, n_pos, path=path, stream=stream)
+          for c in range(ncop)]
+    need = q.qmm_experts_workspace_bytes(al[0], n_exp, ids.shape[1])
+    wsb = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    if need:
+        for a in al:
+            a.workspace, a.workspace_bytes = wsb.data_ptr(), need
+    refs = [ctypes.byref(a) for a in al]
+    ip = ctypes.c_void_p(idd.data_ptr())
+
+    def launch(c):
+        if lib.qmm_matmul_experts(refs[c], ip, n_exp, ids.shape[1]):
+            raise RuntimeError(q.qmm_last_error())
+    dt = time_loop(torch, launch, args.steps, args.warmup, ncop, stream)
+    q.qmm_device_status(stream)
+    print(json.dumps({"case": name, "form": "grouped" if need else "gemv", "us_per_call": dt * 1e6,
+                      "tflops": 2.0 * ids.size * k * n / dt / 1e12, "copies": ncop}), flush=True)
+    return 0
+
+
 def run_case_backward(args, torch, q, lib, r, base):
     """dx = W^T dy over all rows of a workload's weights, timed alone."""
     import ctypes
@@ -889,7 +926,8 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
                     help="profile one workload alone (bf16_gemv, f16_gemv, q4_0_gemv, q4_k_gemv, "
-                         "q6_k_head, q4_k_prefill_N<tokens>[_gemv], <gemv workload>_backward_input)")
+                         "q6_k_head, q4_k_prefill_N<tokens>[_gemv], <gemv workload>_backward_input, "
+                         "<expert workload>_pos<N>[_gemv|_grouped])")
     ap.add_argument("--no-rotate", action="store_true")
     ap.add_argument("--x-wait", action="store_true",
                     help="overlap only the weight stream with the previous kernel (x read after it)")

@@ -653,7 +653,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                         break;
                     }
                 }
-                tc_fence_after();
+                // order the MMAs after the barrier waits of this k-step (a
+                // k-step without one has nothing new to order against)
+                if (ks % KA == 0 || ks % KB == 0) tc_fence_after();
                 if (leader) {
                     const uint32_t at =
                         tmem + (uint32_t)(C::kACol0 + sa * C::kAStageCols + (ks % KA) * 32);

@@ -109,6 +109,11 @@ def test_path_policy_and_workspace(lib):
     a = _args(k=4096, n=14336, n_tokens=1)
     assert q.qmm_select_path(a) == q.PATH_GEMV
     assert q.qmm_workspace_bytes(a) == 0
+    # two tokens: two GEMVs (2 x 11.0 us) beat one tensor-core call (24.7 us)
+    a = _args(k=4096, n=14336, n_tokens=2)
+    assert q.qmm_select_path(a) == q.PATH_GEMV
+    a = _args(k=4096, n=14336, n_tokens=3)
+    assert q.qmm_select_path(a) == q.PATH_MMA
     a = _args(k=4096, n=14336, n_tokens=512)
     assert q.qmm_select_path(a) == q.PATH_MMA
     # x is always split into two fp16 terms (high part and remainder)
