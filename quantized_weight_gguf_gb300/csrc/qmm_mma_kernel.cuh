@@ -21,9 +21,11 @@
 // token row by a power of two (exact) so it fits fp16's range; the epilogue
 // multiplies by the inverse power.
 //
-// Precision modes (fp16 operands round each product's inputs to 11 bits; the
-// resulting error relative to sum |x w| shrinks like 1/sqrt(k)):
-//   MODE 1  W16 . X16                      one product per output
+// Precision modes (fp16 operands round each product's inputs to 11 bits):
+//   MODE 1  W16 . X16                      one product per output; the
+//           templates keep it but nothing instantiates it: a single fp16 copy
+//           of a structured x (a constant row, all-positive terms) errs
+//           coherently by up to 2^-12 of sum |x w| at any k
 //   MODE 2  W16 . (X_hi + X_lo)            x split into two fp16 terms: the B
 //           tile holds BN/2 tokens' hi rows then their lo rows, and the
 //           epilogue adds column c and c + BN/2 (exact for fp16-exact W)
@@ -616,70 +618,75 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 if (!mbar_wait(fullB(s % NB), (s / NB) & 1)) record_error(p.err, DERR_TEARDOWN);
     } else if (warp == 1) {
         // ------------------------------ MMA issue ------------------------------
-        // The whole warp runs the loop (so that descriptors and addresses stay
-        // warp-uniform); one elected lane issues the MMAs and their commits.
+        // One elected lane runs the whole loop: its waits, the MMAs and their
+        // commits (the other lanes wait at the end). The loop goes A stage by
+        // A stage: an x stage (KB k-steps, KB | KA) starts at a multiple of KB
+        // inside it, so every wait and commit sits at a position known at
+        // compile time, and ring slots and phases are running counters. The
+        // lane's instructions per k-step set the pace of small token tiles (a
+        // k-step of 4 MMAs at 32 columns is 64 cycles of tensor work): a loop
+        // that the whole warp ran, converging at every k-step, measured about
+        // 500 cycles a k-step at 32 columns.
         constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
-        const bool leader = elect_one();
-        int abase = 0, bbase = 0;  // A / x stages consumed by earlier tiles
-        int it = 0;
-        bool failed = false;
-        for (int u = c0; u < n_units && !failed; u += cstep, ++it) {
-            const Tile t = tile_of(u);
-            const int KSu = nks(t);
-            if (it > 0) {  // the epilogue has drained the accumulator
-                const bool ok = wait_abortable(accEmpty, (it - 1) & 1, abort_flag);
-                if (__all_sync(0xFFFFFFFFu, ok) == 0) {
-                    if (leader) { record_error(p.err, DERR_MMA_ACC); *abort_flag = 1; }
-                    break;
+        if (elect_one()) {
+            int sa = 0, sb = 0;        // A / x ring slots
+            uint32_t pha = 0, phb = 0; // their phase parities
+            int it = 0;
+            bool failed = false;
+            for (int u = c0; u < n_units && !failed; u += cstep, ++it) {
+                const Tile t = tile_of(u);
+                const int KSu = nks(t);
+                if (it > 0) {  // the epilogue has drained the accumulator
+                    if (!wait_abortable(accEmpty, (it - 1) & 1, abort_flag)) {
+                        record_error(p.err, DERR_MMA_ACC);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    tc_fence_after();
                 }
-                tc_fence_after();
-            }
-            for (int ks = 0; ks < KSu; ++ks) {
-                const int st = abase + ks / KA, sa = st % NA;
-                const int bt = bbase + ks / KB, sb = bt % NB;
-                if (ks % KA == 0) {
-                    const bool ok = wait_abortable(fullA(sa), (st / NA) & 1, abort_flag);
-                    if (__all_sync(0xFFFFFFFFu, ok) == 0) {
-                        if (leader) { record_error(p.err, DERR_MMA_A); *abort_flag = 1; }
+                for (int ks0 = 0; ks0 < KSu; ks0 += KA) {
+                    if (!wait_abortable(fullA(sa), pha, abort_flag)) {
+                        record_error(p.err, DERR_MMA_A);
+                        *abort_flag = 1;
                         failed = true;
                         break;
                     }
-                }
-                if (ks % KB == 0) {
-                    const bool ok = wait_abortable(fullB(sb), (bt / NB) & 1, abort_flag);
-                    if (__all_sync(0xFFFFFFFFu, ok) == 0) {
-                        if (leader) { record_error(p.err, DERR_MMA_B); *abort_flag = 1; }
-                        failed = true;
-                        break;
-                    }
-                }
-                // order the MMAs after the barrier waits of this k-step (a
-                // k-step without one has nothing new to order against)
-                if (ks % KA == 0 || ks % KB == 0) tc_fence_after();
-                if (leader) {
-                    const uint32_t at =
-                        tmem + (uint32_t)(C::kACol0 + sa * C::kAStageCols + (ks % KA) * 32);
-                    const uint64_t bd =
-                        sdesc_sw128(B0 + sb * C::kBStage + (ks % KB) * C::kBBytes);
+                    const uint32_t at0 = tmem + (uint32_t)(C::kACol0 + sa * C::kAStageCols);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {  // K = 16: 8 A columns, 32 B bytes
-                        // K step kk goes to accumulator kk % kNAcc; the tile's
-                        // first MMA into each accumulator overwrites it
-                        const int a = kk % C::kNAcc;
-                        tc_mma_f16_ts(tmem + (uint32_t)(a * C::kAccCols), at + 8 * kk, bd + 2 * kk,
-                                      idesc, ks > 0 || kk >= C::kNAcc);
+                    for (int j = 0; j < KA; ++j) {
+                        const int ks = ks0 + j;
+                        if (ks >= KSu) break;  // a padded last A stage
+                        if (j % KB == 0 && !wait_abortable(fullB(sb), phb, abort_flag)) {
+                            record_error(p.err, DERR_MMA_B);
+                            *abort_flag = 1;
+                            failed = true;
+                            break;
+                        }
+                        // order the MMAs after this stage's barrier waits
+                        if (j % KB == 0) tc_fence_after();
+                        const bool last = ks == KSu - 1;
+                        const uint64_t bd = sdesc_sw128(B0 + sb * C::kBStage + (j % KB) * C::kBBytes);
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk) {  // K = 16: 8 A columns, 32 B bytes
+                            // K step kk goes to accumulator kk % kNAcc; the tile's
+                            // first MMA into each accumulator overwrites it
+                            const int a = kk % C::kNAcc;
+                            tc_mma_f16_ts(tmem + (uint32_t)(a * C::kAccCols), at0 + 32 * j + 8 * kk,
+                                          bd + 2 * kk, idesc, ks > 0 || kk >= C::kNAcc);
+                        }
+                        if (j % KB == KB - 1 || last) {
+                            tc_commit_multicast(emptyB(sb), (uint16_t)3);  // both CTAs may refill
+                            if (++sb == NB) { sb = 0; phb ^= 1u; }
+                        }
+                        if (j == KA - 1 || last) tc_commit(emptyA(sa));
+                        if (last) tc_commit(accFull);  // the tile's product is complete
                     }
-                    const bool last = ks == KSu - 1;
-                    if (ks % KB == KB - 1 || last)
-                        tc_commit_multicast(emptyB(sb), (uint16_t)3);  // both CTAs may refill
-                    if (ks % KA == KA - 1 || last) tc_commit(emptyA(sa));
-                    if (last) tc_commit(accFull);  // the tile's product is complete
+                    if (failed) break;
+                    if (++sa == NA) { sa = 0; pha ^= 1u; }
                 }
-                __syncwarp();
             }
-            abase += nsa(t);
-            bbase += nsb(t);
         }
+        __syncwarp();
     } else if (warp == kRawWarp) {
         // ------------------------- raw W tiles (Q4_K, affine codes) via TMA -------------------------
         // its own warp, so that the raw ring runs as far ahead of the dequant
