@@ -622,11 +622,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         // commits (the other lanes wait at the end). The loop goes A stage by
         // A stage: an x stage (KB k-steps, KB | KA) starts at a multiple of KB
         // inside it, so every wait and commit sits at a position known at
-        // compile time, and ring slots and phases are running counters. The
-        // lane's instructions per k-step set the pace of small token tiles (a
-        // k-step of 4 MMAs at 32 columns is 64 cycles of tensor work): a loop
-        // that the whole warp ran, converging at every k-step, measured about
-        // 500 cycles a k-step at 32 columns.
+        // compile time, and ring slots and phases are running counters.
+        // Measured at 32 columns (a k-step of 4 MMAs is 64 cycles of tensor
+        // work): issuing a k-step takes about 106 cycles this way against 230
+        // for a loop that the whole warp ran and converged at every k-step;
+        // either way small token tiles are paced by the decode (about 2300
+        // cycles per super-block and group, the two groups overlapping).
         constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
         if (elect_one()) {
             int sa = 0, sb = 0;        // A / x ring slots
