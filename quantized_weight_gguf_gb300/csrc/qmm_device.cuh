@@ -64,6 +64,24 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     return d;
 }
 
+// A pair of fp32 values as one 64-bit register (the packed instructions'
+// operand form).
+__device__ __forceinline__ uint64_t pack_f2(float x, float y) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+// As above with b already packed.
+__device__ __forceinline__ float2 ffma2(float2 a, uint64_t b, float2 c) {
+    uint64_t ra, rc, rd;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(b), "l"(rc));
+    float2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+    return d;
+}
+
 // Two fp32 additions in one packed instruction.
 __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
     uint64_t ra, rb, rd;

@@ -166,7 +166,9 @@ __device__ __forceinline__ int x_slot(int k, int U) {
 // Per-thread constants of one unit (x slice and what is derived from it).
 template <int FMT>
 struct UnitState {
-    float xr[UnitK<FMT>::value];
+    // the unit's x as pairs (elements 2i, 2i + 1) in 64-bit registers, the
+    // operand form of the packed fmas (no register moves per use)
+    uint64_t xp[UnitK<FMT>::value / 2];
     float c0;                  // sum of the unit's x (carrier and affine formats)
     uint32_t p0, p1, p2, p3;   // format-specific bit positions / byte selectors
     uint32_t lowgrp;
@@ -193,8 +195,11 @@ __device__ __forceinline__ void unit_init(UnitState<FMT> &st, const float *xs, i
                                           bool valid) {
     constexpr int UK = UnitK<FMT>::value;
     // element e of unit u sits at xs[e * (U + 1) + u]
+    float xr[UK];
 #pragma unroll
-    for (int e = 0; e < UK; ++e) st.xr[e] = valid ? xs[e * (U + 1) + u] : 0.0f;
+    for (int e = 0; e < UK; ++e) xr[e] = valid ? xs[e * (U + 1) + u] : 0.0f;
+#pragma unroll
+    for (int i = 0; i < UK / 2; ++i) st.xp[i] = pack_f2(xr[2 * i], xr[2 * i + 1]);
     if constexpr (FMT == F_Q6_K) {
         const int gq = u & 3;
         // scale byte of quarter r sits at byte 2r + (gq >> 1) of scales[8h .. 8h+7]
@@ -203,12 +208,12 @@ __device__ __forceinline__ void unit_init(UnitState<FMT> &st, const float *xs, i
     } else if constexpr (FMT == F_AFF8) {
         float sx = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) sx += st.xr[i];
+        for (int i = 0; i < 32; ++i) sx += xr[i];
         st.c0 = sx;
     } else if constexpr (FMT == F_AFF4) {
-        st.c0 = carrier_order_sum(st.xr);
+        st.c0 = carrier_order_sum(xr);
     } else if constexpr (FMT == F_Q4_K) {
-        st.c0 = carrier_order_sum(st.xr);
+        st.c0 = carrier_order_sum(xr);
         // 6-bit scale and min of sub-block s gathered into bytes 0, 1 of a
         // word from the header words y (scales[0..3]), z (scales[4..7]) and
         // w (scales[8..11]):
@@ -232,18 +237,21 @@ __device__ __forceinline__ void unit_init_direct(UnitState<FMT> &st, const float
                                                  bool valid) {
     static_assert(UnitK<FMT>::value == 8, "16-bit formats only");
     const float *xu = x + 8 * u;
+    float xr[8];
     if (!valid) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) st.xr[e] = 0.0f;
+        for (int e = 0; e < 8; ++e) xr[e] = 0.0f;
     } else if ((reinterpret_cast<uintptr_t>(xu) & 15u) == 0) {
         const float4 a = __ldg(reinterpret_cast<const float4 *>(xu));
         const float4 b = __ldg(reinterpret_cast<const float4 *>(xu) + 1);
-        st.xr[0] = a.x; st.xr[1] = a.y; st.xr[2] = a.z; st.xr[3] = a.w;
-        st.xr[4] = b.x; st.xr[5] = b.y; st.xr[6] = b.z; st.xr[7] = b.w;
+        xr[0] = a.x; xr[1] = a.y; xr[2] = a.z; xr[3] = a.w;
+        xr[4] = b.x; xr[5] = b.y; xr[6] = b.z; xr[7] = b.w;
     } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) st.xr[e] = __ldg(xu + e);
+        for (int e = 0; e < 8; ++e) xr[e] = __ldg(xu + e);
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) st.xp[i] = pack_f2(xr[2 * i], xr[2 * i + 1]);
 }
 
 // Partial dot of one unit of one row; `rowa` is the row's shared address.
@@ -262,7 +270,7 @@ __device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<
             } else {
                 wf = __half22float2(*reinterpret_cast<const __half2 *>(&wd[i]));
             }
-            const float2 xv = make_float2(st.xr[2 * i], st.xr[2 * i + 1]);
+            const uint64_t xv = st.xp[i];
             if (i & 1) a1 = ffma2(wf, xv, a1); else a0 = ffma2(wf, xv, a0);
         }
         return (a0.x + a0.y) + (a1.x + a1.y);
@@ -278,13 +286,13 @@ __device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<
             const uint32_t lo = qw[i] & 0x0F0F0F0Fu, hi = (qw[i] >> 4) & 0x0F0F0F0Fu;
             float2 f;
             f = fadd2(make_float2(byte_magic23<0>(lo), byte_magic23<1>(lo)), zp);
-            a0 = ffma2(f, make_float2(st.xr[4 * i], st.xr[4 * i + 1]), a0);
+            a0 = ffma2(f, st.xp[2 * i], a0);
             f = fadd2(make_float2(byte_magic23<2>(lo), byte_magic23<3>(lo)), zp);
-            a1 = ffma2(f, make_float2(st.xr[4 * i + 2], st.xr[4 * i + 3]), a1);
+            a1 = ffma2(f, st.xp[2 * i + 1], a1);
             f = fadd2(make_float2(byte_magic23<0>(hi), byte_magic23<1>(hi)), zp);
-            a0 = ffma2(f, make_float2(st.xr[16 + 4 * i], st.xr[16 + 4 * i + 1]), a0);
+            a0 = ffma2(f, st.xp[8 + 2 * i], a0);
             f = fadd2(make_float2(byte_magic23<2>(hi), byte_magic23<3>(hi)), zp);
-            a1 = ffma2(f, make_float2(st.xr[16 + 4 * i + 2], st.xr[16 + 4 * i + 3]), a1);
+            a1 = ffma2(f, st.xp[8 + 2 * i + 1], a1);
         }
         return d * ((a0.x + a0.y) + (a1.x + a1.y));
     } else if (FMT == F_Q4_K) {
@@ -309,9 +317,9 @@ __device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<
         for (int i = 0; i < 8; ++i) {
             const uint32_t nib = (wd[i] >> st.p3) & 0x0F0F0F0Fu;
             a0 = ffma2(make_float2(byte_half_plus<0>(nib), byte_half_plus<1>(nib)),
-                       make_float2(st.xr[4 * i], st.xr[4 * i + 1]), a0);
+                       st.xp[2 * i], a0);
             a1 = ffma2(make_float2(byte_half_plus<2>(nib), byte_half_plus<3>(nib)),
-                       make_float2(st.xr[4 * i + 2], st.xr[4 * i + 3]), a1);
+                       st.xp[2 * i + 1], a1);
         }
         const float a = (a0.x + a0.y) + (a1.x + a1.y);
         // d sc * sum q x - dmin m * sum x, with sum q x = 256 * (a - sum x / 2);
@@ -331,9 +339,9 @@ __device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<
         for (int i = 0; i < 8; ++i) {
             const uint32_t v = qw[i] ^ 0x80808080u;
             float2 f = fadd2(make_float2(byte_magic23<0>(v), byte_magic23<1>(v)), zp);
-            a0 = ffma2(f, make_float2(st.xr[4 * i], st.xr[4 * i + 1]), a0);
+            a0 = ffma2(f, st.xp[2 * i], a0);
             f = fadd2(make_float2(byte_magic23<2>(v), byte_magic23<3>(v)), zp);
-            a1 = ffma2(f, make_float2(st.xr[4 * i + 2], st.xr[4 * i + 3]), a1);
+            a1 = ffma2(f, st.xp[2 * i + 1], a1);
         }
         return d * ((a0.x + a0.y) + (a1.x + a1.y));
     } else if (FMT == F_Q5_0) {
@@ -354,13 +362,13 @@ __device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<
             const uint32_t lo = (qw[i] & 0x0F0F0F0Fu) | hl, hi = ((qw[i] >> 4) & 0x0F0F0F0Fu) | hh;
             float2 f;
             f = fadd2(make_float2(byte_magic23<0>(lo), byte_magic23<1>(lo)), zp);
-            a0 = ffma2(f, make_float2(st.xr[4 * i], st.xr[4 * i + 1]), a0);
+            a0 = ffma2(f, st.xp[2 * i], a0);
             f = fadd2(make_float2(byte_magic23<2>(lo), byte_magic23<3>(lo)), zp);
-            a1 = ffma2(f, make_float2(st.xr[4 * i + 2], st.xr[4 * i + 3]), a1);
+            a1 = ffma2(f, st.xp[2 * i + 1], a1);
             f = fadd2(make_float2(byte_magic23<0>(hi), byte_magic23<1>(hi)), zp);
-            a0 = ffma2(f, make_float2(st.xr[16 + 4 * i], st.xr[16 + 4 * i + 1]), a0);
+            a0 = ffma2(f, st.xp[8 + 2 * i], a0);
             f = fadd2(make_float2(byte_magic23<2>(hi), byte_magic23<3>(hi)), zp);
-            a1 = ffma2(f, make_float2(st.xr[16 + 4 * i + 2], st.xr[16 + 4 * i + 3]), a1);
+            a1 = ffma2(f, st.xp[8 + 2 * i + 1], a1);
         }
         return d * ((a0.x + a0.y) + (a1.x + a1.y));
     } else {  // F_Q6_K
@@ -388,9 +396,9 @@ __device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<
             for (int r = 0; r < 4; ++r) {
                 const float2 f0 = fadd2(make_float2(byte_magic23<0>(q[r]), byte_magic23<1>(q[r])), zp);
                 const float2 f1 = fadd2(make_float2(byte_magic23<2>(q[r]), byte_magic23<3>(q[r])), zp);
-                acc[r][0] = ffma2(f0, make_float2(st.xr[8 * r + 4 * wi], st.xr[8 * r + 4 * wi + 1]),
+                acc[r][0] = ffma2(f0, st.xp[4 * r + 2 * wi],
                                   acc[r][0]);
-                acc[r][1] = ffma2(f1, make_float2(st.xr[8 * r + 4 * wi + 2], st.xr[8 * r + 4 * wi + 3]),
+                acc[r][1] = ffma2(f1, st.xp[4 * r + 2 * wi + 1],
                                   acc[r][1]);
             }
         }
@@ -428,13 +436,13 @@ __device__ __forceinline__ float unit_dot_aff(uint32_t rowa, uint32_t auxa, uint
         for (int i = 0; i < 4; ++i) {
             const uint32_t lo = wd[i] & 0x0F0F0F0Fu, hi = (wd[i] >> 4) & 0x0F0F0F0Fu;
             a0 = ffma2(make_float2(byte_half_plus<0>(lo), byte_half_plus<0>(hi)),
-                       make_float2(st.xr[8 * i], st.xr[8 * i + 1]), a0);
+                       st.xp[4 * i], a0);
             a1 = ffma2(make_float2(byte_half_plus<1>(lo), byte_half_plus<1>(hi)),
-                       make_float2(st.xr[8 * i + 2], st.xr[8 * i + 3]), a1);
+                       st.xp[4 * i + 1], a1);
             a0 = ffma2(make_float2(byte_half_plus<2>(lo), byte_half_plus<2>(hi)),
-                       make_float2(st.xr[8 * i + 4], st.xr[8 * i + 5]), a0);
+                       st.xp[4 * i + 2], a0);
             a1 = ffma2(make_float2(byte_half_plus<3>(lo), byte_half_plus<3>(hi)),
-                       make_float2(st.xr[8 * i + 6], st.xr[8 * i + 7]), a1);
+                       st.xp[4 * i + 3], a1);
         }
         const float a = (a0.x + a0.y) + (a1.x + a1.y);
         // exactly 0 for a group of zero codes with a zero bias
@@ -448,9 +456,9 @@ __device__ __forceinline__ float unit_dot_aff(uint32_t rowa, uint32_t auxa, uint
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             float2 f = fadd2(make_float2(byte_magic23<0>(wd[i]), byte_magic23<1>(wd[i])), zp);
-            a0 = ffma2(f, make_float2(st.xr[4 * i], st.xr[4 * i + 1]), a0);
+            a0 = ffma2(f, st.xp[2 * i], a0);
             f = fadd2(make_float2(byte_magic23<2>(wd[i]), byte_magic23<3>(wd[i])), zp);
-            a1 = ffma2(f, make_float2(st.xr[4 * i + 2], st.xr[4 * i + 3]), a1);
+            a1 = ffma2(f, st.xp[2 * i + 1], a1);
         }
         const float a = (a0.x + a0.y) + (a1.x + a1.y);
         return fmaf(sc, a, bi * st.c0);
