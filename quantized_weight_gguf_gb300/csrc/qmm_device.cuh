@@ -114,19 +114,21 @@ __device__ __forceinline__ float byte_magic23(uint32_t v) {
 // Gate activations of gated FFN pairs, out = act(gate) * up: ACT 1 silu,
 // g s(g); ACT 2 GELU in its tanh form, g/2 (1 + tanh z) with z = sqrt(2/pi)
 // (g + 0.044715 g^3), evaluated as g s(2z) (the same function:
-// 1 + tanh z = 2 s(2z)). s(t) = 1 / (1 + e^-t) is taken as e^t / (1 + e^t)
-// for t < 0 (fp32 library exp), so neither tail cancels or overflows early.
+// 1 + tanh z = 2 s(2z)). The logistic s(t) is taken from e = exp(-|t|)
+// (fp32 library exp, never overflows): r = 1 / (1 + e) correctly rounded,
+// s = r for t >= 0 and e r for t < 0, so neither tail cancels and there is
+// no divergent branch.
+__device__ __forceinline__ float glu_arg(int act, float g) {
+    return act == 1 ? g : 1.5957691216057308f * fmaf(0.044715f * g, g * g, g);
+}
+__device__ __forceinline__ float glu_gate(float g, float t) {
+    const float e = expf(-fabsf(t));
+    const float r = __frcp_rn(1.0f + e);
+    return g * (t >= 0.0f ? r : e * r);
+}
 template <int ACT>
 __device__ __forceinline__ float glu_act(float g) {
-    const float t = ACT == 1 ? g : 1.5957691216057308f * fmaf(0.044715f * g, g * g, g);
-    float sig;
-    if (t >= 0.0f) {
-        sig = 1.0f / (1.0f + expf(-t));
-    } else {
-        const float e = expf(t);
-        sig = e / (1.0f + e);
-    }
-    return g * sig;
+    return glu_gate(g, glu_arg(ACT, g));
 }
 
 // ------------------------------------------------------------- timing ----

@@ -252,11 +252,11 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    // y through shared memory and tensor stores: split-x mode, no gated
-    // epilogue, rows of y 16-byte aligned (n % 4 == 0) and the column tile
-    // starting on a 16-byte boundary; the map's columns end at j1, so the
-    // stores never touch columns outside the tile
-    const bool tma_epi = mode == 2 && !m.glu && m.n % 4 == 0 && m.j0 % 4 == 0 &&
+    // y through shared memory and tensor stores: split-x mode, rows of y
+    // 16-byte aligned (n % 4 == 0) and the column tile starting on a 16-byte
+    // boundary; the map's columns end at j1, so the stores never touch
+    // columns outside the tile
+    const bool tma_epi = mode == 2 && m.n % 4 == 0 && m.j0 % 4 == 0 &&
                          (reinterpret_cast<uintptr_t>(m.y) & 15u) == 0;
     mp.y = mp.x;
     if (tma_epi) {

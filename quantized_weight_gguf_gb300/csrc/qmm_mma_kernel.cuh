@@ -139,14 +139,11 @@ struct MmaCfg {
     static constexpr int kBBytes = BN * kBK * 2;            // one k-step of x
     static constexpr int kBStage = KB * kBBytes;
     static constexpr int kAccCols = BN < 32 ? 32 : BN;      // one accumulator
-    // Two accumulators where TMEM has room: the K = 16 steps of a k-step go
-    // to them in turn (summed in the epilogue), so back-to-back MMAs do not
-    // wait on each other's result. An MMA into the accumulator the one before
-    // it wrote waits for that result (a k-step of four such MMAs measured
-    // about 290 cycles at N = 32, where each MMA's work is 16 cycles); at
-    // BN = 256 an MMA's own 128 cycles cover it and one accumulator leaves
-    // TMEM to the A ring.
-    static constexpr int kNAcc = BN >= 256 ? 1 : 2;
+    // Accumulators that the K = 16 steps of a k-step go to in turn (summed
+    // in the epilogue). One: back-to-back MMAs into the same accumulator run
+    // at the full rate (16 cycles each at N = 32, measured alone), and one
+    // accumulator leaves TMEM to a three-stage A ring at every tile width.
+    static constexpr int kNAcc = 1;
     static constexpr int kACol0 = kNAcc * kAccCols;         // first A column
     static constexpr int kAStageCols = KA * 32;
     static constexpr int kNAFit = (512 - kACol0) / kAStageCols;
@@ -1037,6 +1034,20 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 for (int col = c_lo; col < c_hi; col += 16) {
                     float acc[16];
                     load_acc(col, acc);
+                    if (p.glu) {
+                        // gated pair: y (+)= act(gate) * (this product); the
+                        // gate values of rows and tokens outside the tile are
+                        // not read (the tensor store drops those elements)
+                        // all 16 loads are issued before any is used
+                        float gv[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int64_t tt = t.n0 + col + i;
+                            gv[i] = tt < t.tok_end && je < p.j1 ? __ldg(p.gate + tt * p.n + je) : 0.0f;
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[i] *= glu_gate(gv[i], glu_arg(p.glu, gv[i]));
+                    }
                     if (lane == 0) bulk_wait_group_read0();  // the area's last store has read it
                     __syncwarp();
 #pragma unroll
@@ -1073,7 +1084,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                                 if (p.glu) {
                                     // act(g) u is linear in u: split k-halves add their share
                                     const float g = __ldg(p.gate + yrow * p.n + je);
-                                    val *= p.glu == 1 ? glu_act<1>(g) : glu_act<2>(g);
+                                    val *= glu_gate(g, glu_arg(p.glu, g));
                                 }
                                 float *yq = p.y + yrow * p.n + je;
                                 if (split)
