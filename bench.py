@@ -381,7 +381,7 @@ def run_native(args):
         # back-to-back loop of it (same flags, same rotation)
         r0 = torch.cuda.Event(enable_timing=True)
         r1 = torch.cuda.Event(enable_timing=True)
-        KR = max(K, 100)
+        KR = max(K, 500)
         queue_ahead(torch, stream, 0.5 + 0.01 * KR)
         r0.record(stream)
         for i in range(KR):

@@ -60,7 +60,7 @@ struct MmaLaunch {
     int glu = 0;
 };
 size_t mma_workspace_bytes(int fmt, int64_t n_tokens, int64_t k);
-int mma_mode(int fmt, int64_t k);  // 1: W16.X16, 2: x split, 3: w and x split
+int mma_mode(int fmt, int64_t k);  // 2: x split, 3: w and x split
 cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s);
 
 // Expert-grouped N-token product: the (position, slot) pairs are routed on
