@@ -62,7 +62,12 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const float *__restrict__
                                                        float *__restrict__ xscale,
                                                        const SplitZero z, const XGather gx) {
     __shared__ float red[8];
-    pdl_launch_dependents();  // the product kernel may start its W pipeline now
+    // Launched as a programmatic dependent: the product kernel that follows may
+    // start its W pipeline now; everything this kernel reads (x, the routing)
+    // or writes (the workspace, y's split columns) waits for the preceding
+    // grid, which may still be reading the workspace, to complete.
+    pdl_launch_dependents();
+    pdl_wait_prev();
     int64_t src_row = blockIdx.x;
     if (gx.src) {
         const int64_t t = blockIdx.x;
@@ -119,6 +124,23 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const float *__restrict__
         if (ol) ol[i] = __float2half_rn(v - __half2float(hv));
     }
     if (threadIdx.x == 0) xscale[t] = ldexpf(1.0f, e);
+}
+
+// The conversion as a programmatic dependent of the preceding grid (see the
+// kernel's first lines).
+static cudaError_t launch_x_to_f16(unsigned blocks, cudaStream_t s, const float *x, int64_t k,
+                                   int64_t kp, __half *x16, __half *x16lo, float *xscale,
+                                   const SplitZero &z, const XGather &gx) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, x_to_f16_kernel, x, k, kp, x16, x16lo, xscale, z, gx);
 }
 
 // ------------------------------------------------------------------ host ----
@@ -217,9 +239,8 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
         z.pairs = pairs; z.tiles_n = tiles_n; z.tok = mode == 1 ? tok : tok;
         z.rows = rows_out;
     }
-    x_to_f16_kernel<<<(unsigned)m.n_tokens, 256, 0, s>>>(m.x, m.k, kp, x16, x16lo, xscale, z,
-                                                          XGather{});
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_x_to_f16((unsigned)m.n_tokens, s, m.x, m.k, kp, x16, x16lo, xscale, z,
+                                    XGather{});
     if (e != cudaSuccess) return e;
     const int bn = mode == 1 ? tok : 2 * tok;
     // each CTA of a pair fetches half of an x tile: BN/2 token rows
@@ -427,7 +448,11 @@ cudaError_t launch_mma_grouped(const MmaGroupedLaunch &m, const DeviceInfo &dev,
     gx.src = perm;
     gx.count = row_off + m.n_experts;
     gx.top_k = (int)m.top_k;
-    x_to_f16_kernel<<<(unsigned)P, 256, 0, s>>>(m.x, m.k, kp, x16, x16lo, xscale, SplitZero{}, gx);
+    {
+        const cudaError_t ce =
+            launch_x_to_f16((unsigned)P, s, m.x, m.k, kp, x16, x16lo, xscale, SplitZero{}, gx);
+        if (ce != cudaSuccess) return ce;
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     Maps mp;

@@ -537,6 +537,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     cluster_sync();  // the peer's barriers exist before any multicast reaches them
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // The next grid in the stream may begin launching now; whatever it reads
+    // of this product (y, the workspace) it reads after its griddepcontrol.wait,
+    // which returns once this grid has completed (the library's conversion
+    // kernel and programmatic GEMVs do so).
+    pdl_launch_dependents();
 
     if (warp == 0) {
         // ------------------ token scales + x tiles via TMA ------------------
@@ -799,17 +804,19 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                     // affine: this half of each k-step's codes (128-byte swizzled
                     // rows: 16-byte chunk q of row r sits at chunk q ^ (r & 7) of
                     // its 128-byte line)
-                    uint4 hdr = make_uint4(0u, 0u, 0u, 0u), qv[4], qv2[4];
+                    // Rows past j1 are decoded like the others (their raw bytes
+                    // are in the tile, rows past the matrix being the map's zero
+                    // fill; affine scales and biases past j1 stay 0): the
+                    // accumulator rows they feed are never stored.
+                    uint4 hdr, qv[4], qv2[4];
                     if constexpr (FMT == F_Q4_K) {
                         const uint32_t rb = W0 + rs * kRawB + (uint32_t)r * 144u;
-                        if (row_ok) {
-                            hdr = lds128(rb);
+                        hdr = lds128(rb);
 #pragma unroll
-                            for (int c = 0; c < 4; ++c) qv[c] = lds128(rb + 16u + 32u * c + 16u * h);
-                        }
+                        for (int c = 0; c < 4; ++c) qv[c] = lds128(rb + 16u + 32u * c + 16u * h);
                     } else {
                         const uint32_t sw = (uint32_t)(r & 7);
-                        if (row_ok) {
+                        {
 #pragma unroll
                             for (int c = 0; c < 4; ++c) {
                                 if (FMT == F_AFF4) {
@@ -850,10 +857,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t hw[16];
-                        if (!row_ok) {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) hw[e] = 0u;
-                        } else if constexpr (FMT == F_Q4_K) {
+                        if constexpr (FMT == F_Q4_K) {
                             q4k_half_chunk_to_half(kc[c], d2, qv[c], hw);
                         } else {
                             Raw32<FMT> ra;
