@@ -133,6 +133,14 @@ typedef enum qmm_flags {
      * wait for it. */
     QMM_FLAG_X_READY = 2
 } qmm_flags;
+/* Independent of the flags, the tensor-core (N-token) path lets the launches
+ * after it begin early: its x conversion runs as a programmatic dependent of
+ * the preceding kernel (it waits for that kernel to finish before it reads x
+ * or writes anything, so ordinary stream order holds), and the product kernel
+ * allows the next kernel to launch while it runs. A caller's own kernel
+ * launched with programmatic stream serialization after a tensor-core call
+ * must therefore wait (griddepcontrol.wait / cudaGridDependencySynchronize)
+ * before it reads y; ordinary launches are unaffected. */
 
 /* Bytes of n packed rows of k weights: (k/32)*18*n (Q4_0), (k/256)*144*n
  * (Q4_K), (k/256)*210*n (Q6_K), 2*k*n (BF16 / F16) as in the rullama
