@@ -124,7 +124,9 @@ typedef enum qmm_flags {
      * kernel: it may start streaming W into shared memory while the
      * preceding kernel is still running, and waits for that kernel to finish
      * (and its writes to become visible) before it reads x or touches y.
-     * Without the flag the launch is ordinary stream-ordered. */
+     * Without the flag the GEMV is launched the same way but waits for the
+     * preceding kernel before it reads W as well: stream order holds, and only
+     * the launch latency is hidden. */
     QMM_FLAG_OVERLAP_PREV = 1,
     /* With QMM_FLAG_OVERLAP_PREV: x is not written by the preceding kernel
      * either (for instance several projections of the same activations, or
