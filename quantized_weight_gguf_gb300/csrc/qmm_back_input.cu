@@ -60,13 +60,13 @@ template <int FMT>
 struct BAcc {
     float a[BUnitK<FMT>::value];
     float s0, s1;  // Q4_K: sum of dy * d * sc (the carrier's offset) and of dy * dmin * m
+    // Q4_K: the unit's 6-bit scale and min gathered from the header by byte
+    // permutes (selectors fixed per thread, as its unit is): p0 byte
+    // selector, p1 / p2 masks of the low field and of the top bits, sh the
+    // nibble of the quant bytes, lowgrp sub-blocks 0..3
+    uint32_t p0, p1, p2, sh, lowgrp;
 };
 
-__device__ __forceinline__ uint32_t bw_bfe(uint32_t a, uint32_t pos, uint32_t len) {
-    uint32_t d;
-    asm("bfe.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(pos), "r"(len));
-    return d;
-}
 
 // acc += dyj * (unit u of the row at shared address rowa)
 template <int FMT>
@@ -116,23 +116,24 @@ __device__ __forceinline__ void unit_axpy(uint32_t rowa, int u, float dyj, BAcc<
     } else if (FMT == F_Q4_K) {
         // unit u = sub-block s of super-block b; its 32 codes are the low
         // (s even) or high (s odd) nibbles of quant bytes 32 (s / 2) ..
-        const int b = u >> 3, s = u & 7, c = s >> 1;
+        const int b = u >> 3, c = (u & 7) >> 1;
         const uint32_t sb = rowa + 144u * b;
         const uint4 hdr = lds128(sb);
         const uint4 q0 = lds128(sb + 16u + 32u * c);
         const uint4 q1 = lds128(sb + 32u + 32u * c);
-        uint32_t sc, m;
-        if (s < 4) {
-            sc = bw_bfe(hdr.y, 8 * s, 6);
-            m = bw_bfe(hdr.z, 8 * s, 6);
-        } else {
-            const uint32_t t = 8 * (s - 4);
-            sc = bw_bfe(hdr.w, t, 4) | (bw_bfe(hdr.y, t + 6, 2) << 4);
-            m = bw_bfe(hdr.w, t + 4, 4) | (bw_bfe(hdr.z, t + 6, 2) << 4);
-        }
-        const float a = dyj * (f16_bits_to_f32(hdr.x & 0xFFFFu) * (float)sc);
-        const float bm = dyj * (f16_bits_to_f32(hdr.x >> 16) * (float)m);
-        const uint32_t sh = (s & 1) ? 4u : 0u;
+        // [sc, m] in bytes 0 and 1: s < 4: sc = y byte s & 63, m = z byte s & 63;
+        // s = 4 + t: sc = w byte t & 15 | (y byte t >> 6) << 4,
+        //            m = w byte t >> 4 | (z byte t >> 6) << 4
+        const uint32_t fa = prmt(st.lowgrp ? hdr.y : hdr.w, st.lowgrp ? hdr.z : hdr.w >> 4, st.p0);
+        const uint32_t fb = prmt(hdr.y, hdr.z, st.p0) >> 2;
+        const uint32_t scm = (fa & st.p1) | (fb & st.p2);
+        // (d sc, dmin m) exactly: (2^23 + v) s - 2^23 s, one packed fma
+        const float2 sd = make_float2(f16_bits_to_f32(hdr.x & 0xFFFFu), f16_bits_to_f32(hdr.x >> 16));
+        const float2 dsm = ffma2(make_float2(byte_magic23<0>(scm), byte_magic23<1>(scm)), sd,
+                                 make_float2(-8388608.0f * sd.x, -8388608.0f * sd.y));
+        const float a = dyj * dsm.x;
+        const float bm = dyj * dsm.y;
+        const uint32_t sh = st.sh;
         const uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
         const float2 aa = make_float2(a, a);
 #pragma unroll
@@ -343,6 +344,15 @@ __global__ void __launch_bounds__(kBwThreads, 2) back_input_kernel(const BackPar
 #pragma unroll
     for (int e = 0; e < UK; ++e) st.a[e] = 0.0f;
     st.s0 = st.s1 = 0.0f;
+    {
+        const uint32_t sbk = (uint32_t)(u & 7);  // Q4_K: sub-block of the unit
+        st.lowgrp = sbk < 4;
+        const uint32_t t = st.lowgrp ? sbk : sbk - 4u;
+        st.p0 = t | ((t + 4u) << 4);
+        st.p1 = st.lowgrp ? 0x3F3Fu : 0x0F0Fu;
+        st.p2 = st.lowgrp ? 0u : 0x3030u;
+        st.sh = (sbk & 1) ? 4u : 0u;
+    }
     bool failed = false;
     for (int s = 0; s < nst; ++s) {
         const int slot = s % NS;
