@@ -382,9 +382,9 @@ __device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<
         const float d = f16_bits_to_f32(lds16(sb + 208u));
         // codes q - 32 exactly as 2^23 + q - (2^23 + 32)
         const float2 zp = make_float2(-8388640.0f, -8388640.0f);
-        float2 acc[4][2];
+        float2 acc[4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) acc[r][0] = acc[r][1] = make_float2(0.f, 0.f);
+        for (int r = 0; r < 4; ++r) acc[r] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int wi = 0; wi < 2; ++wi) {
             const uint32_t q[4] = {
@@ -396,17 +396,15 @@ __device__ __forceinline__ float unit_dot(uint32_t rowa, int u, const UnitState<
             for (int r = 0; r < 4; ++r) {
                 const float2 f0 = fadd2(make_float2(byte_magic23<0>(q[r]), byte_magic23<1>(q[r])), zp);
                 const float2 f1 = fadd2(make_float2(byte_magic23<2>(q[r]), byte_magic23<3>(q[r])), zp);
-                acc[r][0] = ffma2(f0, st.xp[4 * r + 2 * wi],
-                                  acc[r][0]);
-                acc[r][1] = ffma2(f1, st.xp[4 * r + 2 * wi + 1],
-                                  acc[r][1]);
+                acc[r] = ffma2(f0, st.xp[4 * r + 2 * wi], acc[r]);
+                acc[r] = ffma2(f1, st.xp[4 * r + 2 * wi + 1], acc[r]);
             }
         }
         const uint32_t pr[4] = {st.p0, st.p1, st.p2, st.p3};
         float sum = 0.0f;
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            const float a = (acc[r][0].x + acc[r][0].y) + (acc[r][1].x + acc[r][1].y);
+            const float a = acc[r].x + acc[r].y;
             const float sc = (float)bfe_s(S[r >> 1], pr[r]);
             sum = fmaf(sc, a, sum);
         }
