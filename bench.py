@@ -812,6 +812,8 @@ def run_case(args):
         return run_case_backward(args, torch, q, lib, r, name[:-len("_backward_input")])
     if "_experts_pos" in name:
         return run_case_experts(args, torch, q, lib, r, name)
+    if "_pair" in name:
+        return run_case_glu(args, torch, q, lib, r, name)
     if name in qmm_synth.AFFINE_WORKLOADS:
         return run_case_affine(args, torch, q, lib, r, name)
     fmt, k, n, w, x = qmm_synth.workload(base, n_tokens=nt)
@@ -910,6 +912,48 @@ def run_case_experts(args, torch, q, lib, r, name):
     return 0
 
 
+def run_case_glu(args, torch, q, lib, r, name):
+    """A gated pair: <gemv workload>_swiglu_pair / _geglu_pair (one token, the
+    fused GEMV) or q4_k_swiglu_pair_N<tokens> (gate product, then the up
+    product with the gated epilogue)."""
+    import ctypes
+    import re
+    m = re.fullmatch(r"(\w+?)_(swiglu|geglu)_pair(?:_N(\d+))?", name)
+    if not m:
+        raise SystemExit(f"unknown gated-pair case {name}")
+    act = q.ACT_SWIGLU if m.group(2) == "swiglu" else q.ACT_GEGLU
+    nt = int(m.group(3)) if m.group(3) else 1
+    if nt > 1:
+        fmt, k, n, w, x = qmm_synth.workload("q4_k_prefill", n_tokens=nt)
+        w2 = qmm_synth.gen_weights(fmt, k, n, np.random.default_rng(78))
+    else:
+        fmt, k, n, w, x = qmm_synth.workload(m.group(1) + "_gemv")
+        w2 = qmm_synth.gen_weights(fmt, k, n, np.random.default_rng(77))
+    dev, stream = r.dev, r.stream
+    ncop = 1 if args.no_rotate else r.copies_for(2 * w.size)
+    wg, wu = r.weights(w, ncop), r.weights(w2, ncop)
+    xd = torch.from_numpy(x).to(dev)
+    yd = torch.empty((nt, n), device=dev)
+    flags = 0 if (args.no_overlap or nt > 1) else (q.FLAG_OVERLAP_PREV | q.FLAG_X_READY)
+    al = [q.make_args(fmt, wg[c], xd, yd, k, n, nt, stream=stream, flags=flags) for c in range(ncop)]
+    need = q.qmm_glu_workspace_bytes(al[0])
+    wsb = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    if need:
+        for a in al:
+            a.workspace, a.workspace_bytes = wsb.data_ptr(), need
+    refs = [ctypes.byref(a) for a in al]
+    ups = [ctypes.c_void_p(wu[c].data_ptr()) for c in range(ncop)]
+
+    def launch(c):
+        if lib.qmm_matmul_glu(refs[c], ups[c], act):
+            raise RuntimeError(q.qmm_last_error())
+    dt = time_loop(torch, launch, args.steps, args.warmup, ncop, stream)
+    q.qmm_device_status(stream)
+    print(json.dumps({"case": name, "us_per_call": dt * 1e6, "weight_gbs": 2 * w.size / dt / 1e9,
+                      "tflops": 4.0 * nt * k * n / dt / 1e12, "copies": ncop}), flush=True)
+    return 0
+
+
 def run_case_backward(args, torch, q, lib, r, base):
     """dx = W^T dy over all rows of a workload's weights, timed alone."""
     import ctypes
@@ -944,7 +988,8 @@ def main():
     ap.add_argument("--case", default=None,
                     help="profile one workload alone (bf16_gemv, f16_gemv, q4_0_gemv, q4_k_gemv, "
                          "q6_k_head, q4_k_prefill_N<tokens>[_gemv], <gemv workload>_backward_input, "
-                         "<expert workload>_pos<N>[_gemv|_grouped])")
+                         "<expert workload>_pos<N>[_gemv|_grouped], <format>_swiglu_pair, "
+                         "<format>_geglu_pair, q4_k_swiglu_pair_N<tokens>)")
     ap.add_argument("--no-rotate", action="store_true")
     ap.add_argument("--x-wait", action="store_true",
                     help="overlap only the weight stream with the previous kernel (x read after it)")

@@ -26,6 +26,9 @@ def _case_exists(name):
         return name[:-len("_backward_input")] in qmm_synth.WORKLOADS
     if name.startswith("q4_k_prefill"):
         return re.fullmatch(r"q4_k_prefill(_N\d+)?(_gemv)?", name) is not None
+    m = re.fullmatch(r"(\w+?)_(swiglu|geglu)_pair(_N\d+)?", name)
+    if m:
+        return (m.group(1) + "_gemv") in qmm_synth.WORKLOADS
     m = re.fullmatch(r"(\w+_experts)_pos\d+(_gemv|_grouped)?", name)
     if m:
         return m.group(1) in qmm_synth.EXPERT_WORKLOADS
