@@ -44,6 +44,15 @@ import qmm_synth  # noqa: E402
 
 # the workload every arm of the bench reports (the same string in each line)
 HEADLINE_WORKLOAD = "bf16+f16 GEMV k=n=4096, 1 token (one step = both GEMVs)"
+
+
+def headline_config(ws: int, wbytes_step: int, l2_bytes: int) -> dict:
+    """The `config` of the headline line, the same in both arms."""
+    ncop = max(1, min(64, -(-3 * l2_bytes // max(wbytes_step // 2, 1))))
+    return {"workload": HEADLINE_WORKLOAD, "weight_bytes_per_step": int(wbytes_step),
+            "l2": f"inputs larger than L2: {ncop} distinct copies of each weight matrix rotate "
+                  f"(> 3x L2 of {l2_bytes >> 20} MiB)",
+            "parallelism": f"replicas x{ws}"}
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES_DEFAULT = 129 * 1024 * 1024
@@ -192,7 +201,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": HEADLINE_WORKLOAD, "weight_bytes_per_step": wbytes},
+            "config": headline_config(ws, wbytes, L2_BYTES_DEFAULT),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": "full oracle product of both 4096x4096 weight matrices per step"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -471,19 +480,17 @@ def run_native(args):
             "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
             "data": "synthetic",
-            "config": {"workload": HEADLINE_WORKLOAD,
-                       "launch": ("stream-ordered" if args.no_overlap else
+            "config": headline_config(ws, 2 * wbytes_each, r.l2),
+            "timing": {"launch": ("stream-ordered" if args.no_overlap else
                                   "programmatic dependent launch (QMM_FLAG_OVERLAP_PREV | "
                                   "QMM_FLAG_X_READY): consecutive GEMVs on the same x; each streams "
                                   "its weights and computes while the previous one finishes, and "
                                   "stores y after it"),
-                       "weight_bytes_per_step": 2 * wbytes_each,
                        "queue": "a device-side sleep (torch.cuda._sleep) precedes the start event, "
                                 "so that the K steps are queued before the first one runs: the "
                                 "host's latency to issue them is outside the device-timed region "
                                 "(it is inside e2e)",
-                       "l2": f"rotating {ncop} distinct weight copies per format (> 3x L2 of {r.l2 >> 20} MiB)",
-                       "parallelism": f"replicas x{ws}"},
+                       "rotation": f"{ncop} copies per format"},
             "roofline": roof, "e2e": e2e, "clocks": clocks,
             "gpu_launches": 2 * K,
             "other_workloads": others}
