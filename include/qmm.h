@@ -133,7 +133,24 @@ typedef enum qmm_flags {
      * x produced two kernels back). The GEMV then also stages x and computes
      * its partial sums before that kernel has finished; only its stores to y
      * wait for it. */
-    QMM_FLAG_X_READY = 2
+    QMM_FLAG_X_READY = 2,
+    /* Tensor-core (N-token) calls on a quantized format: W is split into two
+     * fp16 terms as well as x, at every k (precision mode 3; by default W is
+     * one fp16 term for k >= 1024). Each weight is then carried with about 22
+     * significant bits instead of 11. Without the flag the product's error
+     * bound rests on W's fp16 rounding errors not adding up coherently along
+     * k: a row whose weights repeat one value (a constant row, codes at one
+     * level under one scale) times activations of one sign errs by about
+     * 2^-11 of sum_i |x_i w_ij| (measured 4.9e-4), and by more (4.9e-3
+     * measured) on Q4_K rows whose weight d q - dmin m nearly cancels, above
+     * the 1e-4 bar of the problem statement; with the flag such rows hold the
+     * bar. Costs about 5x the
+     * time of the default tensor-core call (Q4_K k=4096 n=14336: 106 against
+     * 22 us at 8 tokens, 411 against 83 us at 512). Expert-indexed calls with
+     * the flag take the one-GEMV-per-pair form (exact fp32 products). The
+     * GEMV path and 16-bit formats are unaffected: their products are exact
+     * in their operand types. */
+    QMM_FLAG_SPLIT_W = 4
 } qmm_flags;
 /* Independent of the flags, the tensor-core (N-token) path lets the launches
  * after it begin early: its x conversion runs as a programmatic dependent of

@@ -167,6 +167,38 @@ def set_zero_point_rows(fmt: str, w: np.ndarray, k: int, rows) -> np.ndarray:
     return blk.reshape(-1)
 
 
+# Rows whose weights all repeat one value: every block of the row becomes a
+# copy of the row's first block (its drawn f16 scales kept) with the codes
+# and sub-block scales below, so every weight of the row is the same number.
+# (byte range within the block, value) per format; Q4_K's twelve scale bytes
+# give every sub-block sc = 1 and m = 45 (with codes 0 every weight is
+# -45 dmin); Q6_K's int8 scales are all 37.
+_CONSTANT_BYTES = {
+    "q4_0": [((2, 18), 0x33)],
+    "q8_0": [((2, 34), 0x5B)],
+    "q6_k": [((0, 128), 0x00), ((128, 192), 0x00), ((192, 208), 37)],
+    "q4_k": [((4, 8), 0x01), ((8, 12), 0xAD), ((12, 16), 0xD1), ((16, 144), 0x00)],
+}
+
+
+def set_constant_rows(fmt: str, w: np.ndarray, k: int, rows, q4_k_code: int = 0) -> np.ndarray:
+    """Copy of packed weights w in which every weight of the given rows has
+    the same value (see _CONSTANT_BYTES). For Q4_K, q4_k_code (0..15) sets
+    every code: 0 gives the weight -dmin m; a nonzero code gives
+    d q - dmin m, two terms of the same order that partly cancel."""
+    rb = row_bytes(fmt, k)
+    out = np.array(w, dtype=np.uint8, copy=True).reshape(-1, rb)
+    rows = np.asarray(rows, dtype=np.int64)
+    nb = BLOCK_BYTES[fmt]
+    blk = out.reshape(out.shape[0], -1, nb)
+    blk[rows] = blk[rows, :1, :]
+    for (b0, b1), v in _CONSTANT_BYTES[fmt]:
+        blk[rows, :, b0:b1] = v
+    if fmt == "q4_k":
+        blk[rows, :, 16:144] = (q4_k_code & 15) * 0x11
+    return blk.reshape(-1)
+
+
 def set_affine_zero_rows(bits: int, w: np.ndarray, scales: np.ndarray, biases: np.ndarray,
                          k: int, rows):
     """Copies of an affine matrix's arrays in which the given rows are what an

@@ -23,6 +23,7 @@ FORMATS = {"bf16": 0, "f16": 1, "q4_0": 2, "q4_k": 3, "q6_k": 4, "q8_0": 5, "q5_
 PATH_AUTO, PATH_GEMV, PATH_MMA = 0, 1, 2
 FLAG_OVERLAP_PREV = 1
 FLAG_X_READY = 2
+FLAG_SPLIT_W = 4
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_FORMAT", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_SIZE",
           4: "QMM_ERR_RANGE", 5: "QMM_ERR_NULL", 6: "QMM_ERR_ALIGN", 7: "QMM_ERR_CUDA",
           8: "QMM_ERR_DEVICE_TIMEOUT", 9: "QMM_ERR_WORKSPACE", 10: "QMM_ERR_UNSUPPORTED",

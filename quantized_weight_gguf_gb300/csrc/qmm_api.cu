@@ -137,7 +137,7 @@ int validate(const qmm_args *a, int64_t *j0, int64_t *j1, int64_t *rb, bool chec
     }
     if (a->path < QMM_PATH_AUTO || a->path > QMM_PATH_MMA)
         return fail(QMM_ERR_SHAPE, "unknown path %d", a->path);
-    if (a->flags & ~(QMM_FLAG_OVERLAP_PREV | QMM_FLAG_X_READY))
+    if (a->flags & ~(QMM_FLAG_OVERLAP_PREV | QMM_FLAG_X_READY | QMM_FLAG_SPLIT_W))
         return fail(QMM_ERR_SHAPE, "unknown flags 0x%x", a->flags);
     return QMM_OK;
 }
@@ -273,6 +273,7 @@ int run(const qmm_args *a, const void *sc = nullptr, const void *bi = nullptr,
     m.workspace = ws;
     m.sc = static_cast<const uint8_t *>(sc);
     m.bi = static_cast<const uint8_t *>(bi);
+    m.split_w = (a->flags & QMM_FLAG_SPLIT_W) != 0;
     cudaError_t e = qmm::launch_mma(m, *dev, s);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core launch");
     return QMM_OK;
@@ -298,9 +299,10 @@ size_t glu_scratch_bytes(const qmm_args *a) {
 // by TMA) once there are several positions and on average at least two
 // pairs per expert; the other formats decode W rows with per-thread loads on
 // the tensor-core path, which measured no faster than one GEMV per pair.
+// With QMM_FLAG_SPLIT_W the pairs take the GEMV (exact fp32 products).
 bool experts_grouped_ok(const qmm_args *a, int64_t n_experts) {
     return !affine_fmt(a->fmt) && a->k > 0 && qmm::mma_mode(a->fmt, a->k) == 2 &&
-           n_experts <= qmm::kMaxGroupedExperts;
+           !(a->flags & QMM_FLAG_SPLIT_W) && n_experts <= qmm::kMaxGroupedExperts;
 }
 bool experts_grouped(const qmm_args *a, int64_t n_experts, int64_t top_k) {
     if (a->path == QMM_PATH_GEMV || !experts_grouped_ok(a, n_experts)) return false;
@@ -669,6 +671,7 @@ int qmm_matmul_glu(const qmm_args *a, const void *w_up, int act) {
         ml.j0 = j0; ml.j1 = j1;
         ml.accumulate = m ? a->accumulate : 0;
         ml.workspace = mws;
+        ml.split_w = (a->flags & QMM_FLAG_SPLIT_W) != 0;
         if (m) {
             ml.gate = gbuf;
             ml.glu = act;

@@ -58,9 +58,13 @@ struct MmaLaunch {
     // epilogue writes act(gate[t][j]) * (x Wu)[t][j] (gate: [N][n], row stride n)
     const float *gate = nullptr;
     int glu = 0;
+    // 1: a quantized W is split into two fp16 terms as well (precision mode 3
+    // at every k); 16-bit formats are exact in the operand type either way
+    int split_w = 0;
 };
 size_t mma_workspace_bytes(int fmt, int64_t n_tokens, int64_t k);
-int mma_mode(int fmt, int64_t k);  // 2: x split, 3: w and x split
+// precision mode: 2 x split into two fp16 terms, 3 w and x split
+int mma_mode(int fmt, int64_t k, bool split_w = false);
 cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s);
 
 // Expert-grouped N-token product: the (position, slot) pairs are routed on

@@ -154,8 +154,9 @@ static size_t round256(size_t v) { return (v + 255) & ~(size_t)255; }
 // constant or repeated activations: 2.4e-4 of sum |x w| for x = 0.1). W is
 // rounded once to fp16 (16-bit formats are exact in fp16 within its range);
 // for k < 1024 it is split too, since fewer products average its rounding.
-int mma_mode(int fmt, int64_t k) {
+int mma_mode(int fmt, int64_t k, bool split_w) {
     if (fmt == F_BF16 || fmt == F_F16) return 2;
+    if (split_w) return 3;
     // affine rows take the raw-tile path in whole 256-wide slices; other k
     // decode from registers with both operands split
     if (is_affine(fmt) && k % 256 != 0) return 3;
@@ -204,7 +205,7 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
     if (M <= 0 || m.n_tokens <= 0) return cudaSuccess;
     EncodeTiledFn encode = get_encode_fn();
     if (!encode) return cudaErrorNotSupported;
-    const int mode = mma_mode(m.fmt, m.k);
+    const int mode = mma_mode(m.fmt, m.k, m.split_w != 0);
     const int64_t kp = kpad(m.k);
     const size_t one = round256((size_t)m.n_tokens * kp * 2);
     uint8_t *ws = reinterpret_cast<uint8_t *>(m.workspace);

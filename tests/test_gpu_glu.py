@@ -137,3 +137,19 @@ def test_k_zero_writes_zeros():
     x = np.zeros((1, 0), np.float32)
     y = _run("swiglu", "q4_k", w, w, x, 0, 8, y0=y_in)
     assert np.all(y == 0.0)
+
+
+@pytest.mark.parametrize("act", ["swiglu", "geglu"])
+def test_several_tokens_constant_rows_with_split_w(act):
+    """Gated pairs on the tensor cores with QMM_FLAG_SPLIT_W: both products
+    carry W as two fp16 terms, so rows whose weights repeat one value (gate
+    and up) hold the bar with activations of one sign."""
+    fmt, k, n, nt = "q4_k", 4096, 256, 16
+    rng = np.random.default_rng(77)
+    rows = np.arange(0, n, 2)
+    wg = qmm_synth.set_constant_rows(fmt, qmm_synth.gen_weights(fmt, k, n, rng), k, rows)
+    wu = qmm_synth.set_constant_rows(fmt, qmm_synth.gen_weights(fmt, k, n, rng), k, rows)
+    x = qmm_synth.gen_x(nt, k, rng, "abs_normal")
+    y = _run(act, fmt, wg, wu, x, k, n, flags=q.FLAG_SPLIT_W)
+    y_ref, s_ref = oracle.matmul_glu(act, fmt, wg, wu, x, k, n)
+    _assert(y, y_ref, s_ref, f"{act} N={nt} split W")

@@ -38,8 +38,8 @@ def _dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
 
 
-def _mma(fmt, w, x, k, n):
-    out = q.matmul(fmt, _dev(w), _dev(x), k, n, path=q.PATH_MMA)
+def _mma(fmt, w, x, k, n, flags=0):
+    out = q.matmul(fmt, _dev(w), _dev(x), k, n, path=q.PATH_MMA, flags=flags)
     torch.cuda.synchronize()
     q.qmm_device_status()
     return out.cpu().numpy()
@@ -139,3 +139,44 @@ def test_gemv_constant_activations(fmt):
     q.qmm_device_status()
     y_ref, s_ref = oracle.matmul(fmt, w, x, k, n)
     _assert(y.cpu().numpy(), y_ref, s_ref, f"gemv {fmt} constant x")
+
+
+
+@pytest.mark.parametrize("fmt", ["q4_k", "q6_k", "q8_0", "q4_0"])
+@pytest.mark.parametrize("nt", [8, 64])
+def test_constant_weight_rows(fmt, nt):
+    """Rows whose weights all repeat one value (every other row; Q4_K codes 0,
+    so each weight is the single term -dmin m), times activations of one
+    sign. Rounded to fp16 once (the default tensor-core mode at k >= 1024)
+    such a weight errs the same way in every product, by up to about 2^-12 of
+    it, plus the rounding of x's two terms and of the fp32 sums: the default
+    call is held to 2^-10 of sum |x w|. With QMM_FLAG_SPLIT_W, W is carried
+    as two fp16 terms and the product holds the 1e-4 bar like any input."""
+    k, n = 4096, 256
+    rng = np.random.default_rng(500 + nt + len(fmt))
+    w = qmm_synth.gen_weights(fmt, k, n, rng)
+    w = qmm_synth.set_constant_rows(fmt, w, k, np.arange(0, n, 2))
+    x = qmm_synth.gen_x(nt, k, rng, "abs_normal")
+    y_ref, s_ref = oracle.matmul_blas(fmt, w, x, k, n)
+    y = _mma(fmt, w, x, k, n)
+    rel = np.abs(y.astype(np.float64) - y_ref) / s_ref
+    assert rel.max() <= 2.0 ** -10, f"default mode: worst |err|/S {rel.max():.3g}"
+    y2 = _mma(fmt, w, x, k, n, flags=q.FLAG_SPLIT_W)
+    _assert(y2, y_ref, s_ref, f"{fmt} N={nt} with QMM_FLAG_SPLIT_W")
+
+
+@pytest.mark.parametrize("code", [3, 5, 9])
+def test_q4_k_cancelling_constant_rows_with_split_w(code):
+    """Constant Q4_K rows whose weight d q - dmin m is a difference of two
+    terms of the same order: the default decode rounds dmin m to fp16 before
+    the difference, so its error is relative to that term, not to the weight
+    (no bound is claimed for the default call here). QMM_FLAG_SPLIT_W holds
+    the bar on them, and on the varied rows between them."""
+    k, n, nt = 4096, 256, 64
+    rng = np.random.default_rng(600 + code)
+    w = qmm_synth.gen_weights("q4_k", k, n, rng)
+    w = qmm_synth.set_constant_rows("q4_k", w, k, np.arange(0, n, 2), q4_k_code=code)
+    x = qmm_synth.gen_x(nt, k, rng, "abs_normal")
+    y_ref, s_ref = oracle.matmul_blas("q4_k", w, x, k, n)
+    y = _mma("q4_k", w, x, k, n, flags=q.FLAG_SPLIT_W)
+    _assert(y, y_ref, s_ref, f"q4_k code {code} with QMM_FLAG_SPLIT_W")

@@ -157,3 +157,22 @@ def test_affine_scales_biases_and_codes():
     for name, (bits, k, n, nt, seed) in AFFINE_RECIPES.items():
         bb, kk, nn, w, sc, bi, x = S.affine_workload(name, n_tokens=2, n=4)
         assert (bb, kk, nn) == (bits, k, 4) and w.size == 4 * k * bits // 8 and x.shape == (2, k)
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0", "q6_k", "q4_k"])
+def test_constant_rows_repeat_one_weight(fmt):
+    """set_constant_rows: every weight of a chosen row is the same value (read
+    through the oracle's decoder), other rows are untouched."""
+    import oracle
+    oracle.build()
+    k, n = 512, 7
+    rng = np.random.default_rng(17)
+    w = S.gen_weights(fmt, k, n, rng)
+    rows = [1, 4, 6]
+    w2 = S.set_constant_rows(fmt, w, k, rows)
+    f, f2 = oracle.dequant(fmt, w, k, n), oracle.dequant(fmt, w2, k, n)
+    for j in range(n):
+        if j in rows:
+            assert np.unique(f2[j]).size == 1 and f2[j][0] != 0.0
+        else:
+            assert np.array_equal(f[j], f2[j])
