@@ -146,8 +146,10 @@ typedef enum qmm_flags {
      * the 1e-4 bar of the problem statement; with the flag such rows hold the
      * bar. Costs about 5x the
      * time of the default tensor-core call (Q4_K k=4096 n=14336: 106 against
-     * 22 us at 8 tokens, 411 against 83 us at 512). Expert-indexed calls with
-     * the flag take the one-GEMV-per-pair form (exact fp32 products). The
+     * 22 us at 8 tokens, 411 against 83 us at 512), so with the flag
+     * QMM_PATH_AUTO sends calls of up to 8 tokens to the GEMV path (one
+     * launch per token, exact fp32 products, 10.7 us each on that shape).
+     * Expert-indexed calls with the flag take the one-GEMV-per-pair form. The
      * GEMV path and 16-bit formats are unaffected: their products are exact
      * in their operand types. */
     QMM_FLAG_SPLIT_W = 4

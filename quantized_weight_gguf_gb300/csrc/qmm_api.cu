@@ -39,9 +39,15 @@ size_t g_ws_bytes[kMaxDevices];
 
 // Largest token count for which the GEMV path (one launch per token) is used
 // by default; above it the tensor-core path wins. Measured on the Q4_K FFN
-// shape (k = 4096, n = 14336): one GEMV 11.0 us, so two tokens 22 us against
-// 24.7 us for the tensor-core call at N <= 32; three tokens 33 us.
+// shape (k = 4096, n = 14336): one GEMV 10.7 us, so two tokens 21.5 us against
+// 21.6-22.6 us for the tensor-core call at N <= 32; three tokens 32 us.
 constexpr int64_t kGemvMaxTokens = 2;
+// With QMM_FLAG_SPLIT_W (a quantized W carried as two fp16 terms on the
+// tensor cores, precision mode 3) the tensor-core call costs about ten
+// GEMVs at these sizes (Q4_K k = 4096, n = 14336: 106 us at 8 tokens, one
+// GEMV 10.7 us), and the GEMV's fp32 products are exact: up to 8 tokens take
+// one GEMV each.
+constexpr int64_t kGemvMaxTokensSplitW = 8;
 
 int device_info(qmm::DeviceInfo **out) {
     int dev = 0;
@@ -145,7 +151,9 @@ int validate(const qmm_args *a, int64_t *j0, int64_t *j1, int64_t *rb, bool chec
 int choose_path(const qmm_args *a) {
     if (a->path == QMM_PATH_GEMV) return QMM_PATH_GEMV;
     if (a->path == QMM_PATH_MMA) return QMM_PATH_MMA;
-    if (a->n_tokens <= kGemvMaxTokens && qmm::gemv_supports(a->fmt, a->k)) return QMM_PATH_GEMV;
+    const bool split_w = (a->flags & QMM_FLAG_SPLIT_W) && a->fmt != QMM_BF16 && a->fmt != QMM_F16;
+    const int64_t gemv_max = split_w ? kGemvMaxTokensSplitW : kGemvMaxTokens;
+    if (a->n_tokens <= gemv_max && qmm::gemv_supports(a->fmt, a->k)) return QMM_PATH_GEMV;
     return QMM_PATH_MMA;
 }
 

@@ -128,6 +128,15 @@ def test_path_policy_and_workspace(lib):
     a = _args(k=4096, n=14336, n_tokens=64, path=q.PATH_GEMV)
     assert q.qmm_select_path(a) == q.PATH_GEMV
     assert q.qmm_workspace_bytes(a) == 0
+    # W split into two fp16 terms as well: up to 8 tokens of a quantized
+    # format take one exact GEMV each; 16-bit formats are unaffected
+    for nt, path in ((8, q.PATH_GEMV), (9, q.PATH_MMA)):
+        a = _args(k=4096, n=14336, n_tokens=nt, flags=q.FLAG_SPLIT_W)
+        assert q.qmm_select_path(a) == path
+    a = _args(fmt="bf16", k=4096, n=4096, n_tokens=3, w_len=0, flags=q.FLAG_SPLIT_W)
+    assert q.qmm_select_path(a) == q.PATH_MMA
+    a = _args(k=4096, n=14336, n_tokens=64, flags=q.FLAG_SPLIT_W)
+    assert q.qmm_workspace_bytes(a) == 2 * 64 * 4096 * 2 + 256
 
 
 def test_dequant_rejects_bad_args(lib):

@@ -180,3 +180,24 @@ def test_q4_k_cancelling_constant_rows_with_split_w(code):
     y_ref, s_ref = oracle.matmul_blas("q4_k", w, x, k, n)
     y = _mma("q4_k", w, x, k, n, flags=q.FLAG_SPLIT_W)
     _assert(y, y_ref, s_ref, f"q4_k code {code} with QMM_FLAG_SPLIT_W")
+
+
+def test_split_w_few_tokens_take_the_gemv():
+    """With QMM_FLAG_SPLIT_W, QMM_PATH_AUTO sends up to 8 tokens of a
+    quantized format to the GEMV (exact fp32 products): constant rows hold
+    the bar, and the path query says so."""
+    fmt, k, n, nt = "q4_k", 4096, 256, 6
+    rng = np.random.default_rng(808)
+    w = qmm_synth.set_constant_rows(fmt, qmm_synth.gen_weights(fmt, k, n, rng), k, np.arange(n))
+    x = qmm_synth.gen_x(nt, k, rng, "abs_normal")
+    wd, xd = _dev(w), _dev(x)
+    y = torch.empty((nt, n), dtype=torch.float32, device=DEV)
+    a = q.make_args(fmt, wd, xd, y, k, n, nt, flags=q.FLAG_SPLIT_W)
+    assert q.qmm_select_path(a) == q.PATH_GEMV
+    a0 = q.make_args(fmt, wd, xd, y, k, n, nt)
+    assert q.qmm_select_path(a0) == q.PATH_MMA
+    out = q.matmul(fmt, wd, xd, k, n, flags=q.FLAG_SPLIT_W)
+    torch.cuda.synchronize()
+    q.qmm_device_status()
+    y_ref, s_ref = oracle.matmul_blas(fmt, w, x, k, n)
+    _assert(out.cpu().numpy(), y_ref, s_ref, "split W, 6 tokens, AUTO")
