@@ -94,8 +94,29 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const float *__restrict__
     }
     const int64_t t = blockIdx.x;
     const float *xt = x + src_row * k;
+    // Rows of up to kXRegs float4 per thread (k <= 8192, 16-byte aligned) are
+    // read once, with 16-byte loads, and kept in registers for the
+    // conversion; 8-byte stores write four halves at a time. Other rows are
+    // read twice (the second pass from L2) element by element. Both forms
+    // round every element the same way.
+    constexpr int kXRegs = 8;
+    const bool in_regs = (reinterpret_cast<uintptr_t>(xt) & 15u) == 0 && (k & 3) == 0 &&
+                         kp <= 4 * 256 * kXRegs && blockDim.x == 256;
+    float4 xv[kXRegs];
     float m = 0.0f;
-    for (int64_t i = threadIdx.x; i < k; i += blockDim.x) m = fmaxf(m, fabsf(__ldg(xt + i)));
+    if (in_regs) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(xt);
+        const int64_t k4 = k >> 2;
+#pragma unroll
+        for (int j = 0; j < kXRegs; ++j) {
+            const int64_t i = threadIdx.x + 256 * j;
+            xv[j] = i < k4 ? __ldg(x4 + i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(xv[j].x), fabsf(xv[j].y)),
+                               fmaxf(fabsf(xv[j].z), fabsf(xv[j].w))));
+        }
+    } else {
+        for (int64_t i = threadIdx.x; i < k; i += blockDim.x) m = fmaxf(m, fabsf(__ldg(xt + i)));
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
@@ -117,11 +138,38 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const float *__restrict__
     }
     __half *ot = x16 + t * kp;
     __half *ol = x16lo ? x16lo + t * kp : nullptr;
-    for (int64_t i = threadIdx.x; i < kp; i += blockDim.x) {
-        const float v = i < k ? ldexpf(__ldg(xt + i), -e) : 0.0f;
-        const __half hv = __float2half_rn(v);
-        ot[i] = hv;
-        if (ol) ol[i] = __float2half_rn(v - __half2float(hv));
+    if (in_regs) {
+        // kp is a multiple of 64 and the rows start 256-byte aligned: every
+        // group of four halves is one aligned 8-byte store
+        const int64_t kp4 = kp >> 2;
+#pragma unroll
+        for (int j = 0; j < kXRegs; ++j) {
+            const int64_t i = threadIdx.x + 256 * j;
+            if (i < kp4) {
+                const float v0 = ldexpf(xv[j].x, -e), v1 = ldexpf(xv[j].y, -e);
+                const float v2 = ldexpf(xv[j].z, -e), v3 = ldexpf(xv[j].w, -e);
+                const __half2 h01 = __floats2half2_rn(v0, v1), h23 = __floats2half2_rn(v2, v3);
+                const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+                uint2 hw, lw;
+                hw.x = *reinterpret_cast<const uint32_t *>(&h01);
+                hw.y = *reinterpret_cast<const uint32_t *>(&h23);
+                *reinterpret_cast<uint2 *>(ot + 4 * i) = hw;
+                if (ol) {
+                    const __half2 l01 = __floats2half2_rn(v0 - f01.x, v1 - f01.y);
+                    const __half2 l23 = __floats2half2_rn(v2 - f23.x, v3 - f23.y);
+                    lw.x = *reinterpret_cast<const uint32_t *>(&l01);
+                    lw.y = *reinterpret_cast<const uint32_t *>(&l23);
+                    *reinterpret_cast<uint2 *>(ol + 4 * i) = lw;
+                }
+            }
+        }
+    } else {
+        for (int64_t i = threadIdx.x; i < kp; i += blockDim.x) {
+            const float v = i < k ? ldexpf(__ldg(xt + i), -e) : 0.0f;
+            const __half hv = __float2half_rn(v);
+            ot[i] = hv;
+            if (ol) ol[i] = __float2half_rn(v - __half2float(hv));
+        }
     }
     if (threadIdx.x == 0) xscale[t] = ldexpf(1.0f, e);
 }
