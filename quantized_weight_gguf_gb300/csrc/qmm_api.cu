@@ -40,7 +40,8 @@ size_t g_ws_bytes[kMaxDevices];
 // Largest token count for which the GEMV path (one launch per token) is used
 // by default; above it the tensor-core path wins. Measured on the Q4_K FFN
 // shape (k = 4096, n = 14336): one GEMV 10.7 us, so two tokens 21.5 us against
-// 21.6-22.6 us for the tensor-core call at N <= 32; three tokens 32 us.
+// 20.4-21.0 us for the tensor-core call at N <= 32 (two tokens stay on the
+// GEMV, within 5 %, for its exact fp32 products); three tokens 32 us.
 constexpr int64_t kGemvMaxTokens = 2;
 // With QMM_FLAG_SPLIT_W (a quantized W carried as two fp16 terms on the
 // tensor cores, precision mode 3) the tensor-core call costs about ten

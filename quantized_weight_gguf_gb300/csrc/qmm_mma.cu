@@ -201,7 +201,9 @@ static size_t round256(size_t v) { return (v + 255) & ~(size_t)255; }
 // (a single fp16 copy errs by up to 2^-12 per element, coherently for
 // constant or repeated activations: 2.4e-4 of sum |x w| for x = 0.1). W is
 // rounded once to fp16 (16-bit formats are exact in fp16 within its range);
-// for k < 1024 it is split too, since fewer products average its rounding.
+// for k < 1024 it is split too, since fewer products average its rounding,
+// and at any k when the caller asks (QMM_FLAG_SPLIT_W: rows that repeat one
+// weight value add its rounding up coherently).
 int mma_mode(int fmt, int64_t k, bool split_w) {
     if (fmt == F_BF16 || fmt == F_F16) return 2;
     if (split_w) return 3;
