@@ -172,8 +172,9 @@ size_t qmm_weight_bytes(int fmt, int64_t k, int64_t n);
 
 /* y = x @ W over the whole output axis, on the stream last given to
  * qmm_set_stream (default: the legacy default stream), auto path, workspace
- * from the library's own grow-only buffer. The spec signature:
- * qmm_matmul(fmt, w_bytes, x, k, n, n_tokens, y). Returns a qmm_status. */
+ * from the library's own grow-only buffer: the problem statement's plain
+ * signature qmm_matmul(fmt, w_bytes, x, k, n, n_tokens, y). Returns a
+ * qmm_status. */
 int qmm_matmul(int fmt, const void *w, const float *x, int64_t k, int64_t n,
                int64_t n_tokens, float *y);
 

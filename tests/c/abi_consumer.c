@@ -27,7 +27,7 @@ int main(void) {
     EXPECT(qmm_weight_bytes(QMM_Q4_K, 300, 1) == 0);
     EXPECT(qmm_weight_bytes(QMM_AFFINE4, 128, 2) == 128);
 
-    /* the spec call with invalid shapes: rejected on the host */
+    /* the plain seven-argument call with invalid shapes: rejected on the host */
     float dummy[4];
     EXPECT(qmm_matmul(QMM_Q4_K, dummy, dummy, 300, 8, 1, dummy) == QMM_ERR_SHAPE);
     EXPECT(qmm_matmul(99, dummy, dummy, 256, 8, 1, dummy) == QMM_ERR_FORMAT);

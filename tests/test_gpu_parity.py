@@ -342,7 +342,7 @@ def test_all_zero_point_q4_0_row_is_exactly_zero():
         assert np.all(y == 0.0), path
 
 
-def test_north_star_signature_and_host_variant():
+def test_plain_signature_and_host_variant():
     fmt, k, n, w, x = qmm_synth.workload("q4_0_gemv")
     lib = q.load()
     wd, xd = _dev(w), _dev(x)
