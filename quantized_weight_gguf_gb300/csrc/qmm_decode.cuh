@@ -105,6 +105,13 @@ struct Raw32<F_Q4_0> {
 #pragma unroll
         for (int i = 0; i < 4; ++i) qw[i] = ldg_u16(p + 2 + 4 * i) | (ldg_u16(p + 4 + 4 * i) << 16);
     }
+    // the block at shared address a (2-byte aligned), from a raw W tile: a
+    // row's blocks alternate between 2 mod 4 and 0 mod 4 starts, the last
+    // one aligned, so no read leaves the row
+    __device__ __forceinline__ void load_shared(uint32_t a) {
+        dbits = lds16(a);
+        lds_words_a2_exact<4>(a + 2, qw);
+    }
     __device__ __forceinline__ void decode(float (&w)[32]) const {
         const float d = f16_bits_to_f32(dbits);
 #pragma unroll
@@ -192,6 +199,10 @@ struct Raw32<F_Q8_0> {
 #pragma unroll
         for (int i = 0; i < 8; ++i) qw[i] = ldg_u16(p + 2 + 4 * i) | (ldg_u16(p + 4 + 4 * i) << 16);
     }
+    __device__ __forceinline__ void load_shared(uint32_t a) {
+        dbits = lds16(a);
+        lds_words_a2_exact<8>(a + 2, qw);
+    }
     __device__ __forceinline__ void decode(float (&w)[32]) const {
         const float d = f16_bits_to_f32(dbits);
 #pragma unroll
@@ -212,6 +223,13 @@ struct Raw32<F_Q5_0> {
         qh = ldg_u16(p + 2) | (ldg_u16(p + 4) << 16);
 #pragma unroll
         for (int i = 0; i < 4; ++i) qw[i] = ldg_u16(p + 6 + 4 * i) | (ldg_u16(p + 8 + 4 * i) << 16);
+    }
+    __device__ __forceinline__ void load_shared(uint32_t a) {
+        dbits = lds16(a);
+        uint32_t h[1];
+        lds_words_a2_exact<1>(a + 2, h);
+        qh = h[0];
+        lds_words_a2_exact<4>(a + 6, qw);
     }
     __device__ __forceinline__ void decode(float (&w)[32]) const {
         const float d = f16_bits_to_f32(dbits);

@@ -320,6 +320,22 @@ __device__ __forceinline__ void lds_words_a2(uint32_t addr, uint32_t (&out)[NW])
     for (int i = 0; i < NW; ++i) out[i] = prmt(w[i], w[i + 1], sel);
 }
 
+// As lds_words_a2, reading no word past the last byte it returns: an
+// aligned address takes NW words, an address 2 mod 4 the NW + 1 that cover
+// it (one of them reaching 2 bytes past the data).
+template <int NW>
+__device__ __forceinline__ void lds_words_a2_exact(uint32_t addr, uint32_t (&out)[NW]) {
+    const uint32_t base = addr & ~3u;
+    const bool odd = (addr & 2u) != 0;
+    const uint32_t sel = odd ? 0x5432u : 0x3210u;
+    uint32_t w[NW + 1];
+#pragma unroll
+    for (int i = 0; i < NW; ++i) w[i] = lds32(base + 4 * i);
+    w[NW] = odd ? lds32(base + 4 * NW) : 0u;
+#pragma unroll
+    for (int i = 0; i < NW; ++i) out[i] = prmt(w[i], w[i + 1], sel);
+}
+
 // ------------------------------------------------------------ tcgen05 ----
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {

@@ -207,9 +207,9 @@ static size_t round256(size_t v) { return (v + 255) & ~(size_t)255; }
 int mma_mode(int fmt, int64_t k, bool split_w) {
     if (fmt == F_BF16 || fmt == F_F16) return 2;
     if (split_w) return 3;
-    // affine rows take the raw-tile path in whole 256-wide slices; other k
-    // decode from registers with both operands split
-    if (is_affine(fmt) && k % 256 != 0) return 3;
+    // affine and block-format rows take the raw-tile path in whole 256-wide
+    // slices; other k decode from registers with both operands split
+    if ((is_affine(fmt) || raw_block32(fmt)) && k % 256 != 0) return 3;
     if (k >= 1024) return 2;
     return 3;
 }
@@ -236,6 +236,28 @@ static EncodeTiledFn get_encode_fn() {
             fn = reinterpret_cast<EncodeTiledFn>(ptr);
     });
     return fn;
+}
+
+// Raw W tiles: the packed rows as a 2-D tensor [rows][row_bytes] (16-bit
+// elements for Q8_0, bytes otherwise), boxes of 128 rows x one 256-wide k
+// slice (Q4_K 144 B, Q4_0 144, Q5_0 176, Q8_0 272: multiples of 16 bytes, as
+// are the row strides for k % 256 == 0); affine code boxes of 128 rows x
+// 128 bytes, 128-byte swizzled (the dequant warps read 16-byte chunks of 32
+// consecutive rows).
+static bool encode_raw_w_map(EncodeTiledFn encode, CUtensorMap *tm, const uint8_t *w, int fmt,
+                             int64_t row_bytes, int64_t rows) {
+    const bool aff = is_affine(fmt);
+    const int eb = raw_elem_bytes(fmt);
+    const cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / eb), (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {aff ? 128u : (cuuint32_t)(raw_slice_bytes(fmt, 2) / eb),
+                               (cuuint32_t)kBM};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(tm, eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                  const_cast<uint8_t *>(w), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  aff ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 static bool encode_x_map(EncodeTiledFn encode, CUtensorMap *tm, void *base, int64_t kp,
@@ -308,22 +330,9 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
     CUtensorMap &tw = mp.w;
     // raw W tiles: the packed rows as a 2-D byte tensor [n][row_bytes]
     tw = tm;
-    if (raw_slice_bytes(m.fmt, mode) > 0) {
-        // raw W tiles: Q4_K boxes of 128 rows x one 144-byte super-block;
-        // affine code boxes of 128 rows x 128 bytes, 128-byte swizzled (the
-        // dequant warps read 16-byte chunks of 32 consecutive rows)
-        const bool aff = is_affine(m.fmt);
-        const cuuint64_t dims[2] = {(cuuint64_t)m.row_bytes, (cuuint64_t)m.n};
-        const cuuint64_t strides[1] = {(cuuint64_t)m.row_bytes};
-        const cuuint32_t box[2] = {aff ? 128u : 144u, (cuuint32_t)kBM};
-        const cuuint32_t estr[2] = {1, 1};
-        if (encode(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(m.w), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   aff ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
+    if (raw_slice_bytes(m.fmt, mode) > 0 &&
+        !encode_raw_w_map(encode, &tw, m.w, m.fmt, m.row_bytes, m.n))
+        return cudaErrorInvalidValue;
     // y through shared memory and tensor stores: split-x mode, rows of y
     // 16-byte aligned (n % 4 == 0) and the column tile starting on a 16-byte
     // boundary; the map's columns end at j1, so the stores never touch
@@ -512,18 +521,10 @@ cudaError_t launch_mma_grouped(const MmaGroupedLaunch &m, const DeviceInfo &dev,
         return cudaErrorInvalidValue;
     mp.w = mp.x;
     mp.y = mp.x;  // rows of y are scattered: stored from registers
-    if (raw_slice_bytes(m.fmt, 2) > 0) {
-        // the stacked slices as one 2-D byte tensor [n_experts * n][row_bytes]
-        const cuuint64_t dims[2] = {(cuuint64_t)m.row_bytes, (cuuint64_t)(m.n * m.n_experts)};
-        const cuuint64_t strides[1] = {(cuuint64_t)m.row_bytes};
-        const cuuint32_t box[2] = {144u, (cuuint32_t)kBM};
-        const cuuint32_t estr[2] = {1, 1};
-        if (encode(&mp.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(m.w), dims,
-                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
+    // the stacked slices as one 2-D tensor [n_experts * n][row_bytes]
+    if (raw_slice_bytes(m.fmt, 2) > 0 &&
+        !encode_raw_w_map(encode, &mp.w, m.w, m.fmt, m.row_bytes, m.n * m.n_experts))
+        return cudaErrorInvalidValue;
     MmaHostParams p = {};
     p.w = m.w; p.y = m.y; p.xscale = xscale;
     p.k = m.k; p.n = m.n; p.n_tokens = P; p.row_bytes = m.row_bytes;

@@ -107,12 +107,29 @@ using MmaParamsOf = typename std::conditional<
 constexpr int kRawBytes = kBM * 144;
 
 // Raw W tiles staged by TMA (one box of 128 rows x the bytes of a 256-wide k
-// slice): Q4_K super-blocks (144 B) and affine code words (128 B at 4 bits,
-// 256 B at 8; their scales and biases come from global memory per thread).
-// MODE 3 (rows split into hi / lo halves) decodes from registers instead.
+// slice): Q4_K super-blocks (144 B), eight 32-weight blocks of Q4_0 (144 B),
+// Q5_0 (176 B) or Q8_0 (272 B), and affine code words (128 B at 4 bits, 256 B
+// at 8; their scales and biases come from global memory per thread). Q6_K's
+// 210-byte super-blocks cannot start a TMA box on a 16-byte boundary and stay
+// on the per-thread path. MODE 3 (rows split into hi / lo halves) decodes
+// from registers as well; so do the block formats when k % 256 != 0.
 __host__ __device__ constexpr int raw_slice_bytes(int fmt, int mode) {
-    return mode == 3 ? 0 : fmt == F_Q4_K ? 144 : fmt == F_AFF4 ? 128 : fmt == F_AFF8 ? 256 : 0;
+    return mode == 3 ? 0
+           : fmt == F_Q4_K ? 144
+           : fmt == F_AFF4 ? 128
+           : fmt == F_AFF8 ? 256
+           : fmt == F_Q4_0 ? 144
+           : fmt == F_Q5_0 ? 176
+           : fmt == F_Q8_0 ? 272 : 0;
 }
+// Block formats whose raw tiles hold whole 32-weight blocks (read with
+// realigning loads: a block starts on a 2-byte boundary)
+__host__ __device__ constexpr bool raw_block32(int fmt) {
+    return fmt == F_Q4_0 || fmt == F_Q5_0 || fmt == F_Q8_0;
+}
+// Element size of the raw tiles' tensor map: a box row is at most 256
+// elements, so Q8_0's 272-byte slices go as 136 16-bit elements
+__host__ __device__ constexpr int raw_elem_bytes(int fmt) { return fmt == F_Q8_0 ? 2 : 1; }
 
 // Tensor memory (512 columns x 128 lanes of 32 bits, all taken by the one CTA
 // on the SM): the fp32 accumulator(s) first, then a ring of NA dequantized W
@@ -717,7 +734,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 #pragma unroll
                     for (int bx = 0; bx < kBoxes; ++bx)
                         tma_load_2d(W0 + rs * kRawB + (uint32_t)bx * (kRawB / kBoxes), &tmw,
-                                    kSliceB * (kx(t, 4 * b) >> 2) + bx * (kSliceB / kBoxes),
+                                    (kSliceB * (kx(t, 4 * b) >> 2) + bx * (kSliceB / kBoxes)) /
+                                        raw_elem_bytes(FMT),
                                     (int)t.wrow, rawFull(rs));
                 }
                 if (!ok) break;
@@ -784,7 +802,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                     // affine: the row's four scales and biases of this slice come
                     // from global memory; their loads overlap the raw-tile wait
                     uint2 sc4 = make_uint2(0u, 0u), bi4 = make_uint2(0u, 0u);
-                    if constexpr (FMT != F_Q4_K) {
+                    if constexpr (is_affine(FMT)) {
                         if (row_ok) {
                             // the unit's super-block b is k-step t.k_lo + 4 b (before rotation)
                             const int64_t ao = (t.wrow + r) * p.aux_row_bytes +
@@ -814,6 +832,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                         hdr = lds128(rb);
 #pragma unroll
                         for (int c = 0; c < 4; ++c) qv[c] = lds128(rb + 16u + 32u * c + 16u * h);
+                    } else if constexpr (raw_block32(FMT)) {
+                        // read block by block during the decode below; the raw
+                        // slot is released after it
                     } else {
                         const uint32_t sw = (uint32_t)(r & 7);
                         {
@@ -835,9 +856,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                     }
                     // the raw slot is refilled by TMA (the async proxy) once every
                     // reader has arrived: order this thread's reads of it first
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(rawEmpty(rs));  // raw tile read
+                    if constexpr (!raw_block32(FMT)) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(rawEmpty(rs));  // raw tile read
+                    }
                     // the stage's slot, once the MMAs that read it last are done
                     const int st = abase + b, slot = st % NA;
                     if (st >= NA) {
@@ -859,6 +882,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                         uint32_t hw[16];
                         if constexpr (FMT == F_Q4_K) {
                             q4k_half_chunk_to_half(kc[c], d2, qv[c], hw);
+                        } else if constexpr (raw_block32(FMT)) {
+                            // chunk c = blocks 2c and 2c + 1 of the slice; this
+                            // thread's half is block 2c + h (weights 32h + 0..31)
+                            Raw32<FMT> ra;
+                            ra.load_shared(W0 + rs * kRawB + (uint32_t)r * (uint32_t)kSliceB +
+                                           (uint32_t)(2 * c + h) * (uint32_t)(kSliceB / 8));
+                            to_half_words<FMT>(ra, hw);
                         } else {
                             Raw32<FMT> ra;
                             ra.qw[0] = qv[c].x; ra.qw[1] = qv[c].y; ra.qw[2] = qv[c].z; ra.qw[3] = qv[c].w;
@@ -879,6 +909,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                             // k-step c, weights 32h + 0..31 -> columns 16h..
                             tmem_st16(ta + 32u * c + 16u * h, hw);
                         }
+                    }
+                    if constexpr (raw_block32(FMT)) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(rawEmpty(rs));  // raw tile read
                     }
                     tmem_st_wait();
                     tc_fence_before();
