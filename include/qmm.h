@@ -266,13 +266,15 @@ size_t qmm_backward_input_workspace_bytes(const qmm_args *a);
  *    kernel sorts the pairs by expert on the device, then one tensor-core
  *    pass multiplies each expert's rows by its slice, so a slice chosen by
  *    many positions is decoded once per token tile instead of once per pair.
- *    GGUF formats with k >= 1024 (the split-x mode), n_experts <= 4096;
- *    scratch from a->workspace (qmm_experts_workspace_bytes) or the
- *    library's buffer; flags are not used.
+ *    GGUF formats with k >= 1024 (the split-x mode; Q4_0, Q5_0 and Q8_0
+ *    also k % 256 == 0), n_experts <= 4096; scratch from a->workspace
+ *    (qmm_experts_workspace_bytes) or the library's buffer. With
+ *    QMM_FLAG_SPLIT_W the pairs take the GEMV form.
  * a->path GEMV or MMA forces a form (MMA: QMM_ERR_UNSUPPORTED where the
- * grouped form cannot take the call); AUTO takes the grouped form for Q4_K
- * (whose W tiles the tensor-core path streams by TMA) when n_pos > 1 and
- * n_pos * top_k >= 2 * n_experts, the GEMV form otherwise. An id outside [0, n_experts)
+ * grouped form cannot take the call); AUTO takes the grouped form for Q4_K,
+ * Q8_0, Q5_0 and Q4_0 (whose W tiles the tensor-core path streams raw by
+ * TMA) when n_pos > 1 and n_pos * top_k >= 2 * n_experts, the GEMV form
+ * otherwise. An id outside [0, n_experts)
  * leaves that y row untouched and records an error that qmm_device_status
  * reports as QMM_ERR_BAD_ID. */
 int qmm_matmul_experts(const qmm_args *a, const int32_t *ids, int64_t n_experts, int64_t top_k);
