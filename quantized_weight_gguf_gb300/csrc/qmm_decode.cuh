@@ -173,6 +173,17 @@ struct Raw32<F_Q6_K> {
         sc2 = ldg_u16(p + 192 + 8 * h + 2 * r);
         dbits = ldg_u16(p + 208);
     }
+    // weights e0 .. e0 + 31 (e0 a multiple of 32) of the super-block at shared
+    // address sb (2-byte aligned), from a raw W tile; every read stays within
+    // the super-block's 210 bytes
+    __device__ __forceinline__ void load_shared(uint32_t sb, int e0) {
+        const int h = e0 >> 7;
+        r = (e0 & 127) >> 5;
+        lds_words_a2_exact<8>(sb + 64u * h + 32u * (r & 1), ql);
+        lds_words_a2_exact<8>(sb + 128u + 32u * h, qh);
+        sc2 = lds16(sb + 192u + 8u * h + 2u * r);
+        dbits = lds16(sb + 208u);
+    }
     __device__ __forceinline__ void decode(float (&w)[32]) const {
         const float d = f16_bits_to_f32(dbits);
         const float ds0 = __fmul_rn(d, (float)(int)(int8_t)(sc2 & 0xFFu));

@@ -330,7 +330,7 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
     CUtensorMap &tw = mp.w;
     // raw W tiles: the packed rows as a 2-D byte tensor [n][row_bytes]
     tw = tm;
-    if (raw_slice_bytes(m.fmt, mode) > 0 &&
+    if (raw_slice_bytes(m.fmt, mode) > 0 && !raw_rowcopy(m.fmt) &&
         !encode_raw_w_map(encode, &tw, m.w, m.fmt, m.row_bytes, m.n))
         return cudaErrorInvalidValue;
     // y through shared memory and tensor stores: split-x mode, rows of y
@@ -358,6 +358,7 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
     p.bi = m.bi;
     p.aux_row_bytes = (m.k / 64) * 2;
     p.k = m.k; p.n = m.n; p.n_tokens = m.n_tokens; p.row_bytes = m.row_bytes;
+    p.w_rows = m.n;
     p.j0 = m.j0; p.j1 = m.j1;
     p.KS = (int)(kp / kBK);
     p.accumulate = m.accumulate;
@@ -522,12 +523,13 @@ cudaError_t launch_mma_grouped(const MmaGroupedLaunch &m, const DeviceInfo &dev,
     mp.w = mp.x;
     mp.y = mp.x;  // rows of y are scattered: stored from registers
     // the stacked slices as one 2-D tensor [n_experts * n][row_bytes]
-    if (raw_slice_bytes(m.fmt, 2) > 0 &&
+    if (raw_slice_bytes(m.fmt, 2) > 0 && !raw_rowcopy(m.fmt) &&
         !encode_raw_w_map(encode, &mp.w, m.w, m.fmt, m.row_bytes, m.n * m.n_experts))
         return cudaErrorInvalidValue;
     MmaHostParams p = {};
     p.w = m.w; p.y = m.y; p.xscale = xscale;
     p.k = m.k; p.n = m.n; p.n_tokens = P; p.row_bytes = m.row_bytes;
+    p.w_rows = m.n * m.n_experts;
     p.j0 = m.j0; p.j1 = m.j1;
     p.KS = (int)(kp / kBK);
     p.accumulate = m.accumulate;

@@ -72,6 +72,7 @@ struct MmaParams {
     const float *gate;
     int glu;
     int tma_epi;  // y written through shared memory by tensor stores (map tmy)
+    int64_t w_rows;  // rows of the W buffer (n, or n_experts slices of n)
 };
 
 // Affine formats also read a bf16 scale and bias per group of 64 from two
@@ -106,13 +107,15 @@ using MmaParamsOf = typename std::conditional<
 // 256-wide slice of k), then decoded from shared memory.
 constexpr int kRawBytes = kBM * 144;
 
-// Raw W tiles staged by TMA (one box of 128 rows x the bytes of a 256-wide k
-// slice): Q4_K super-blocks (144 B), eight 32-weight blocks of Q4_0 (144 B),
-// Q5_0 (176 B) or Q8_0 (272 B), and affine code words (128 B at 4 bits, 256 B
-// at 8; their scales and biases come from global memory per thread). Q6_K's
-// 210-byte super-blocks cannot start a TMA box on a 16-byte boundary and stay
-// on the per-thread path. MODE 3 (rows split into hi / lo halves) decodes
-// from registers as well; so do the block formats when k % 256 != 0.
+// Raw W tiles (128 rows of a 256-wide k slice each): staged by TMA for Q4_K
+// super-blocks (144 B), eight 32-weight blocks of Q4_0 (144 B), Q5_0 (176 B)
+// or Q8_0 (272 B), and affine code words (128 B at 4 bits, 256 B at 8; their
+// scales and biases come from global memory per thread). Q6_K's 210-byte
+// super-blocks start on 2-byte boundaries, which no TMA box can: each row's
+// super-block comes with its own 1-D bulk copy of the 224 bytes from the
+// 16-byte boundary at or below it, into a 240-byte row of the tile. MODE 3
+// (rows split into hi / lo halves) decodes from registers; so do the block
+// formats when k % 256 != 0.
 __host__ __device__ constexpr int raw_slice_bytes(int fmt, int mode) {
     return mode == 3 ? 0
            : fmt == F_Q4_K ? 144
@@ -120,8 +123,12 @@ __host__ __device__ constexpr int raw_slice_bytes(int fmt, int mode) {
            : fmt == F_AFF8 ? 256
            : fmt == F_Q4_0 ? 144
            : fmt == F_Q5_0 ? 176
-           : fmt == F_Q8_0 ? 272 : 0;
+           : fmt == F_Q8_0 ? 272
+           : fmt == F_Q6_K ? 240 : 0;
 }
+// Raw tiles filled row by row with bulk copies (no tensor map)
+__host__ __device__ constexpr bool raw_rowcopy(int fmt) { return fmt == F_Q6_K; }
+constexpr int kQ6kWindow = 224;  // bytes copied per row: covers 210 from any even offset below 16
 // Block formats whose raw tiles hold whole 32-weight blocks (read with
 // realigning loads: a block starts on a 2-byte boundary)
 __host__ __device__ constexpr bool raw_block32(int fmt) {
@@ -711,7 +718,74 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         // ------------------------- raw W tiles (Q4_K, affine codes) via TMA -------------------------
         // its own warp, so that the raw ring runs as far ahead of the dequant
         // warps as it is deep (into the next tile), whatever the x ring does
-        if (kRaw && lane == 0) {
+        if (kRaw && raw_rowcopy(FMT)) {
+            // Q6_K: the 32 lanes copy four rows each. A row's super-block of
+            // this slice sits at src = w + j R + 210 sb; its window starts at
+            // src & ~15 and runs kQ6kWindow bytes, cut at the last 16-byte
+            // boundary of W, whose remaining bytes (at most 15) are copied
+            // with plain loads before the slot is armed.
+            const uintptr_t wbase = reinterpret_cast<uintptr_t>(p.w);
+            const uintptr_t wend16 = (wbase + (uintptr_t)(p.row_bytes * p.w_rows)) & ~(uintptr_t)15;
+            int rcount = 0;
+            for (int u = c0; u < n_units; u += cstep) {
+                if (*abort_flag) break;
+                const Tile t = tile_of(u);
+                bool ok = true;
+                for (int b = t.k_lo / 4; b < t.k_hi / 4; ++b, ++rcount) {  // k % 256 == 0
+                    const int rs = rcount % kNR;
+                    bool free_ok = true;
+                    if (lane == 0 && rcount >= kNR)
+                        free_ok = wait_abortable(rawEmpty(rs), ((rcount / kNR) + 1) & 1, abort_flag);
+                    if (!__shfl_sync(0xFFFFFFFFu, (int)free_ok, 0)) {
+                        if (lane == 0) {
+                            record_error(p.err, DERR_MMA_EMPTY);
+                            *abort_flag = 1;
+                        }
+                        ok = false;
+                        break;
+                    }
+                    const int64_t sbg = kx(t, 4 * b) >> 2;  // super-block index along the row
+                    const uint32_t slot = W0 + rs * kRawB;
+                    uintptr_t from[4];
+                    uint32_t size[4], total = 0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = lane + 32 * i;
+                        const int64_t j = t.wrow + r;
+                        size[i] = 0;
+                        from[i] = 0;
+                        if (j < p.w_rows) {
+                            const uintptr_t src = wbase + (uintptr_t)(j * p.row_bytes + 210 * sbg);
+                            const uintptr_t a16 = src & ~(uintptr_t)15;
+                            const uintptr_t end = a16 + kQ6kWindow < wend16 ? a16 + kQ6kWindow : wend16;
+                            from[i] = a16;
+                            size[i] = (uint32_t)(end - a16);
+                            total += size[i];
+                            // bytes past the last 16-byte boundary of W (the matrix's
+                            // last super-block only)
+                            for (uintptr_t q = end; q < src + 210; ++q)
+                                sts8(slot + (uint32_t)r * (uint32_t)kSliceB + (uint32_t)(q - a16),
+                                     *reinterpret_cast<const uint8_t *>(q));
+                        }
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xFFFFFFFFu, total, o);
+                    __syncwarp();  // the plain stores above before the arrival
+                    if (lane == 0) mbar_arrive_expect_tx(rawFull(rs), total);
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (size[i])
+                            bulk_g2s(slot + (uint32_t)(lane + 32 * i) * (uint32_t)kSliceB,
+                                     reinterpret_cast<const void *>(from[i]), size[i], rawFull(rs));
+                }
+                if (!ok) break;
+            }
+            // no copy may land after this CTA exits
+            if (lane == 0)
+                for (int s = std::max(0, rcount - kNR); s < rcount; ++s)
+                    if (!mbar_wait(rawFull(s % kNR), (s / kNR) & 1)) record_error(p.err, DERR_TEARDOWN);
+        } else if (kRaw && lane == 0) {
             prefetch_tmap(&tmw);
             int rcount = 0;
             for (int u = c0; u < n_units; u += cstep) {
@@ -811,6 +885,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                             bi4 = __ldg(reinterpret_cast<const uint2 *>(p.bi + ao));
                         }
                     }
+                    // Q6_K: where this row's super-block starts in its tile row
+                    // (its global address modulo 16, as the loader cut it)
+                    uint32_t q6_rem = 0;
+                    if constexpr (raw_rowcopy(FMT)) {
+                        const int64_t sbg = kx(t, t.k_lo + 4 * b) >> 2;
+                        q6_rem = (uint32_t)((reinterpret_cast<uintptr_t>(p.w) +
+                                             (uintptr_t)((t.wrow + r) * p.row_bytes + 210 * sbg)) &
+                                            15u);
+                    }
                     const bool ok = wait_abortable(rawFull(rs), (rc / kNR) & 1, abort_flag);
                     if (__all_sync(0xFFFFFFFFu, ok) == 0) {
                         record_error(p.err, DERR_MMA_A);
@@ -832,7 +915,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                         hdr = lds128(rb);
 #pragma unroll
                         for (int c = 0; c < 4; ++c) qv[c] = lds128(rb + 16u + 32u * c + 16u * h);
-                    } else if constexpr (raw_block32(FMT)) {
+                    } else if constexpr (raw_block32(FMT) || raw_rowcopy(FMT)) {
                         // read block by block during the decode below; the raw
                         // slot is released after it
                     } else {
@@ -856,7 +939,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                     }
                     // the raw slot is refilled by TMA (the async proxy) once every
                     // reader has arrived: order this thread's reads of it first
-                    if constexpr (!raw_block32(FMT)) {
+                    if constexpr (!raw_block32(FMT) && !raw_rowcopy(FMT)) {
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(rawEmpty(rs));  // raw tile read
@@ -889,6 +972,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                             ra.load_shared(W0 + rs * kRawB + (uint32_t)r * (uint32_t)kSliceB +
                                            (uint32_t)(2 * c + h) * (uint32_t)(kSliceB / 8));
                             to_half_words<FMT>(ra, hw);
+                        } else if constexpr (raw_rowcopy(FMT)) {
+                            // this row's super-block starts q6_rem bytes into its
+                            // tile row; weights 64c + 32h + 0..31 of it
+                            Raw32<FMT> ra;
+                            ra.load_shared(W0 + rs * kRawB + (uint32_t)r * (uint32_t)kSliceB + q6_rem,
+                                           64 * c + 32 * h);
+                            to_half_words<FMT>(ra, hw);
                         } else {
                             Raw32<FMT> ra;
                             ra.qw[0] = qv[c].x; ra.qw[1] = qv[c].y; ra.qw[2] = qv[c].z; ra.qw[3] = qv[c].w;
@@ -910,7 +1000,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                             tmem_st16(ta + 32u * c + 16u * h, hw);
                         }
                     }
-                    if constexpr (raw_block32(FMT)) {
+                    if constexpr (raw_block32(FMT) || raw_rowcopy(FMT)) {
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(rawEmpty(rs));  // raw tile read
