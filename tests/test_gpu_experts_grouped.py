@@ -56,11 +56,11 @@ def test_auto_policy_picks_the_grouped_form():
     assert q.qmm_experts_workspace_bytes(a, n_exp, top_k) == 0    # k < 1024: GEMV form
     a = q.make_args("q4_k", 16, 16, 16, 512, n, 64, path=q.PATH_MMA, stream=0)
     assert q.load().qmm_matmul_experts(ctypes.byref(a), 16, n_exp, top_k) == 10
-    # the other formats whose W tiles stream raw by TMA group as well; Q6_K
-    # (per-thread decode on the tensor cores) keeps one GEMV per pair
-    for fmt, grouped in (("q8_0", True), ("q5_0", True), ("q4_0", True), ("q6_k", False)):
-        a = q.make_args(fmt, 16, 16, 16, k, n, 64, stream=0)
-        assert (q.qmm_experts_workspace_bytes(a, n_exp, top_k) > 0) == grouped, fmt
+    # the other raw-tile formats group from two pairs per expert; Q6_K from five
+    for fmt, n_pos, grouped in (("q8_0", 64, True), ("q5_0", 64, True), ("q4_0", 64, True),
+                                ("q8_0", 8, True), ("q6_k", 64, True), ("q6_k", 16, False)):
+        a = q.make_args(fmt, 16, 16, 16, k, n, n_pos, stream=0)
+        assert (q.qmm_experts_workspace_bytes(a, n_exp, top_k) > 0) == grouped, (fmt, n_pos)
 
 
 @pytest.mark.parametrize("fmt,k", [("q4_k", 2048), ("q8_0", 2048), ("q5_0", 1024), ("q6_k", 1024),

@@ -1,6 +1,7 @@
-"""GPU parity of the tensor-core path for the block formats whose W tiles are
-staged raw by TMA (Q4_0, Q5_0, Q8_0 at k % 256 == 0, k >= 1024), against the
-oracle through the C ABI: row counts that leave a ragged last row tile (the
+"""GPU parity of the tensor-core path for the formats whose W tiles are staged
+raw (Q4_0, Q5_0, Q8_0 by TMA at k % 256 == 0, k >= 1024; Q6_K by per-row bulk
+copies from 16-byte boundaries, the matrix's last bytes by plain loads),
+against the oracle through the C ABI: row counts that leave a ragged last row tile (the
 tile's rows past n are the map's zero fill), token counts that leave a
 partial token tile, output-axis windows (the tile's first row is then j_start,
 not a multiple of 128) written or accumulated, and the k % 256 != 0 shapes
@@ -36,6 +37,8 @@ CASES = [  # (fmt, k, n, n_tokens)
     ("q8_0", 1024, 129, 3), ("q8_0", 4096, 1000, 37), ("q8_0", 2048, 257, 130),
     ("q5_0", 1024, 1, 9), ("q5_0", 4096, 383, 64), ("q5_0", 3072, 640, 200),
     ("q4_0", 2048, 127, 17), ("q4_0", 4096, 900, 129), ("q4_0", 1280, 256, 5),
+    ("q6_k", 2560, 131, 7), ("q6_k", 4096, 1000, 64), ("q6_k", 1024, 1, 33),
+    ("q6_k", 1536, 385, 130),
 ]
 
 
@@ -83,10 +86,11 @@ def test_k_not_a_multiple_of_256_keeps_the_per_thread_path(fmt):
     assert ok, msg
 
 
-def test_repeated_calls_give_the_same_bits():
+@pytest.mark.parametrize("fmt", ["q8_0", "q6_k"])
+def test_repeated_calls_give_the_same_bits(fmt):
     """The raw slot is released only after its last block is decoded: calls
     repeated into a poisoned output give identical bits."""
-    fmt, k, n, nt = "q8_0", 4096, 2000, 256
+    k, n, nt = 4096, 2000, 256
     rng = np.random.default_rng(5)
     wd = _dev(qmm_synth.gen_weights(fmt, k, n, rng))
     xd = _dev(qmm_synth.gen_x(nt, k, rng))
