@@ -395,6 +395,16 @@ __device__ __forceinline__ void tc_mma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, 
         "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// As above with A from shared memory too (a K-major, 128-byte swizzled tile
+// described like B).
+__device__ __forceinline__ void tc_mma_f16_ss(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Registers -> tensor memory: thread t of the warp writes 8 (16) consecutive
 // 32-bit columns of TMEM lane (lane field of taddr) + t. The warp may only
 // address its own quarter of the lanes: 32 * (warp id % 4) ...
@@ -464,6 +474,10 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
            | (0u << 7) | (0u << 10)         // A, B format fp16
            | ((uint32_t)(n >> 3) << 17)     // N / 8
            | ((uint32_t)(m >> 4) << 24);    // M / 16
+}
+// The same with A and B in bf16.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
+    return idesc_f16_f32(m, n) | (1u << 7) | (1u << 10);
 }
 
 }  // namespace qmm

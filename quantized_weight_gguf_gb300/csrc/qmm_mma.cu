@@ -5,6 +5,8 @@
 // compiled in the qmm_mma_inst_*.cu units.
 #include "qmm_mma_kernel.cuh"
 
+#include <cuda_bf16.h>
+
 namespace qmm {
 
 extern template cudaError_t launch_fmt<F_BF16>(int, int, const Maps &, const MmaHostParams &,
@@ -55,12 +57,15 @@ struct XGather {
 
 // X [N][k] fp32 -> X16 [N][kp] fp16 (zero padded) scaled by 2^-e per row so the
 // row's largest magnitude lands in [2^14, 2^15); xscale[t] = 2^e. With x16lo,
-// also the fp16 rounding of what X16 missed (x = hi + lo to ~22 bits).
+// also the fp16 rounding of what X16 missed (x = hi + lo to ~22 bits). With
+// bf16 set, both terms are bf16 instead (x = hi + lo to ~16 bits), for
+// products whose W tiles are bf16.
 __global__ void __launch_bounds__(256) x_to_f16_kernel(const float *__restrict__ x, int64_t k,
                                                        int64_t kp, __half *__restrict__ x16,
                                                        __half *__restrict__ x16lo,
                                                        float *__restrict__ xscale,
-                                                       const SplitZero z, const XGather gx) {
+                                                       const SplitZero z, const XGather gx,
+                                                       const int bf16) {
     __shared__ float red[8];
     // Launched as a programmatic dependent: the product kernel that follows may
     // start its W pipeline now; everything this kernel reads (x, the routing)
@@ -148,17 +153,35 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const float *__restrict__
             if (i < kp4) {
                 const float v0 = ldexpf(xv[j].x, -e), v1 = ldexpf(xv[j].y, -e);
                 const float v2 = ldexpf(xv[j].z, -e), v3 = ldexpf(xv[j].w, -e);
-                const __half2 h01 = __floats2half2_rn(v0, v1), h23 = __floats2half2_rn(v2, v3);
-                const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
                 uint2 hw, lw;
-                hw.x = *reinterpret_cast<const uint32_t *>(&h01);
-                hw.y = *reinterpret_cast<const uint32_t *>(&h23);
+                float2 f01, f23;
+                if (bf16) {
+                    const __nv_bfloat162 h01 = __floats2bfloat162_rn(v0, v1);
+                    const __nv_bfloat162 h23 = __floats2bfloat162_rn(v2, v3);
+                    f01 = __bfloat1622float2(h01);
+                    f23 = __bfloat1622float2(h23);
+                    hw.x = *reinterpret_cast<const uint32_t *>(&h01);
+                    hw.y = *reinterpret_cast<const uint32_t *>(&h23);
+                } else {
+                    const __half2 h01 = __floats2half2_rn(v0, v1), h23 = __floats2half2_rn(v2, v3);
+                    f01 = __half22float2(h01);
+                    f23 = __half22float2(h23);
+                    hw.x = *reinterpret_cast<const uint32_t *>(&h01);
+                    hw.y = *reinterpret_cast<const uint32_t *>(&h23);
+                }
                 *reinterpret_cast<uint2 *>(ot + 4 * i) = hw;
                 if (ol) {
-                    const __half2 l01 = __floats2half2_rn(v0 - f01.x, v1 - f01.y);
-                    const __half2 l23 = __floats2half2_rn(v2 - f23.x, v3 - f23.y);
-                    lw.x = *reinterpret_cast<const uint32_t *>(&l01);
-                    lw.y = *reinterpret_cast<const uint32_t *>(&l23);
+                    if (bf16) {
+                        const __nv_bfloat162 l01 = __floats2bfloat162_rn(v0 - f01.x, v1 - f01.y);
+                        const __nv_bfloat162 l23 = __floats2bfloat162_rn(v2 - f23.x, v3 - f23.y);
+                        lw.x = *reinterpret_cast<const uint32_t *>(&l01);
+                        lw.y = *reinterpret_cast<const uint32_t *>(&l23);
+                    } else {
+                        const __half2 l01 = __floats2half2_rn(v0 - f01.x, v1 - f01.y);
+                        const __half2 l23 = __floats2half2_rn(v2 - f23.x, v3 - f23.y);
+                        lw.x = *reinterpret_cast<const uint32_t *>(&l01);
+                        lw.y = *reinterpret_cast<const uint32_t *>(&l23);
+                    }
                     *reinterpret_cast<uint2 *>(ol + 4 * i) = lw;
                 }
             }
@@ -166,9 +189,16 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const float *__restrict__
     } else {
         for (int64_t i = threadIdx.x; i < kp; i += blockDim.x) {
             const float v = i < k ? ldexpf(__ldg(xt + i), -e) : 0.0f;
-            const __half hv = __float2half_rn(v);
-            ot[i] = hv;
-            if (ol) ol[i] = __float2half_rn(v - __half2float(hv));
+            if (bf16) {
+                const __nv_bfloat16 hv = __float2bfloat16_rn(v);
+                const __nv_bfloat16 lv = __float2bfloat16_rn(v - __bfloat162float(hv));
+                ot[i] = *reinterpret_cast<const __half *>(&hv);
+                if (ol) ol[i] = *reinterpret_cast<const __half *>(&lv);
+            } else {
+                const __half hv = __float2half_rn(v);
+                ot[i] = hv;
+                if (ol) ol[i] = __float2half_rn(v - __half2float(hv));
+            }
         }
     }
     if (threadIdx.x == 0) xscale[t] = ldexpf(1.0f, e);
@@ -176,7 +206,7 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const float *__restrict__
 
 // The conversion as a programmatic dependent of the preceding grid (see the
 // kernel's first lines).
-static cudaError_t launch_x_to_f16(unsigned blocks, cudaStream_t s, const float *x, int64_t k,
+static cudaError_t launch_x_to_f16(unsigned blocks, cudaStream_t s, int bf16, const float *x, int64_t k,
                                    int64_t kp, __half *x16, __half *x16lo, float *xscale,
                                    const SplitZero &z, const XGather &gx) {
     cudaLaunchConfig_t cfg = {};
@@ -188,7 +218,7 @@ static cudaError_t launch_x_to_f16(unsigned blocks, cudaStream_t s, const float 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, x_to_f16_kernel, x, k, kp, x16, x16lo, xscale, z, gx);
+    return cudaLaunchKernelEx(&cfg, x_to_f16_kernel, x, k, kp, x16, x16lo, xscale, z, gx, bf16);
 }
 
 // ------------------------------------------------------------------ host ----
@@ -278,6 +308,9 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
     EncodeTiledFn encode = get_encode_fn();
     if (!encode) return cudaErrorNotSupported;
     const int mode = mma_mode(m.fmt, m.k, m.split_w != 0);
+    // 16-bit W tiles as the MMA's A operand from shared memory: rows a tensor
+    // map can describe (2 k bytes a multiple of 16)
+    const bool ss = (m.fmt == F_BF16 || m.fmt == F_F16) && mode == 2 && m.k % 8 == 0;
     const int64_t kp = kpad(m.k);
     const size_t one = round256((size_t)m.n_tokens * kp * 2);
     uint8_t *ws = reinterpret_cast<uint8_t *>(m.workspace);
@@ -312,7 +345,8 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
         z.pairs = pairs; z.tiles_n = tiles_n; z.tok = mode == 1 ? tok : tok;
         z.rows = rows_out;
     }
-    cudaError_t e = launch_x_to_f16((unsigned)m.n_tokens, s, m.x, m.k, kp, x16, x16lo, xscale, z,
+    cudaError_t e = launch_x_to_f16((unsigned)m.n_tokens, s, ss && m.fmt == F_BF16 ? 1 : 0, m.x, m.k,
+                                    kp, x16, x16lo, xscale, z,
                                     XGather{});
     if (e != cudaSuccess) return e;
     const int bn = mode == 1 ? tok : 2 * tok;
@@ -333,6 +367,21 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
     if (raw_slice_bytes(m.fmt, mode) > 0 && !raw_rowcopy(m.fmt) &&
         !encode_raw_w_map(encode, &tw, m.w, m.fmt, m.row_bytes, m.n))
         return cudaErrorInvalidValue;
+    if (ss) {
+        // 16-bit W as [n][k] elements, 128-row x 64-wide boxes, 128-byte
+        // swizzled: the A operand's shared-memory layout (that of the x tiles)
+        const cuuint64_t dims[2] = {(cuuint64_t)m.k, (cuuint64_t)m.n};
+        const cuuint64_t strides[1] = {(cuuint64_t)m.row_bytes};
+        const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBM};
+        const cuuint32_t estr[2] = {1, 1};
+        if (encode(&tw,
+                   m.fmt == F_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                   2, const_cast<uint8_t *>(m.w), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     // y through shared memory and tensor stores: split-x mode, rows of y
     // 16-byte aligned (n % 4 == 0) and the column tile starting on a 16-byte
     // boundary; the map's columns end at j1, so the stores never touch
@@ -359,6 +408,7 @@ cudaError_t launch_mma(const MmaLaunch &m, const DeviceInfo &dev, cudaStream_t s
     p.aux_row_bytes = (m.k / 64) * 2;
     p.k = m.k; p.n = m.n; p.n_tokens = m.n_tokens; p.row_bytes = m.row_bytes;
     p.w_rows = m.n;
+    p.ss = ss ? 1 : 0;
     p.j0 = m.j0; p.j1 = m.j1;
     p.KS = (int)(kp / kBK);
     p.accumulate = m.accumulate;
@@ -511,7 +561,7 @@ cudaError_t launch_mma_grouped(const MmaGroupedLaunch &m, const DeviceInfo &dev,
     gx.top_k = (int)m.top_k;
     {
         const cudaError_t ce =
-            launch_x_to_f16((unsigned)P, s, m.x, m.k, kp, x16, x16lo, xscale, SplitZero{}, gx);
+            launch_x_to_f16((unsigned)P, s, 0, m.x, m.k, kp, x16, x16lo, xscale, SplitZero{}, gx);
         if (ce != cudaSuccess) return ce;
     }
     e = cudaGetLastError();

@@ -73,6 +73,7 @@ struct MmaParams {
     int glu;
     int tma_epi;  // y written through shared memory by tensor stores (map tmy)
     int64_t w_rows;  // rows of the W buffer (n, or n_experts slices of n)
+    int ss;          // 16-bit W tiles read as the MMA's A operand from shared memory (mma_ssable)
 };
 
 // Affine formats also read a bf16 scale and bias per group of 64 from two
@@ -128,6 +129,18 @@ __host__ __device__ constexpr int raw_slice_bytes(int fmt, int mode) {
 }
 // Raw tiles filled row by row with bulk copies (no tensor map)
 __host__ __device__ constexpr bool raw_rowcopy(int fmt) { return fmt == F_Q6_K; }
+// 16-bit formats in split-x mode (ungrouped) can take their W tiles as the
+// MMA's A operand straight from shared memory: nothing to decode. The raw
+// ring then holds one 128 x 64 tile per k-step (16 KB, 128-byte swizzled,
+// the layout of the x tiles). A call takes that form (MmaParams::ss) when its
+// rows admit a tensor map (k % 8 == 0); otherwise the same instance decodes
+// from per-thread loads.
+__host__ __device__ constexpr bool mma_ssable(int fmt, int mode, bool grp) {
+    return (fmt == F_BF16 || fmt == F_F16) && mode == 2 && !grp;
+}
+__host__ __device__ constexpr int mma_ring_bytes(int fmt, int mode, bool grp) {
+    return mma_ssable(fmt, mode, grp) ? kBM * kBK * 2 : kBM * raw_slice_bytes(fmt, mode);
+}
 constexpr int kQ6kWindow = 224;  // bytes copied per row: covers 210 from any even offset below 16
 // Block formats whose raw tiles hold whole 32-weight blocks (read with
 // realigning loads: a block starts on a 2-byte boundary)
@@ -155,7 +168,8 @@ constexpr int kEpiStageBytes = 16 * 2048;
 __host__ __device__ constexpr bool mma_tma_epilogue(int mode, bool grp) { return mode == 2 && !grp; }
 
 // EPI: bytes of the epilogue's staging area (0: y stored from registers).
-template <int BN, int RAWB, int EPI = 0>  // RAWB: bytes of one raw W tile (0: no raw ring)
+// RAWB: bytes of one raw W tile (0: no raw ring); DEEP: a deeper raw ring
+template <int BN, int RAWB, int EPI = 0, bool DEEP = false>
 struct MmaCfg {
     static constexpr bool RAW = RAWB > 0;
     static constexpr int KA = 4;
@@ -189,7 +203,10 @@ struct MmaCfg {
         RAW && KB == 1 && (kBudget - kNBWant * kBStage - EPI) / RAWB < 2;
     static constexpr int kNBMin = kShrinkX ? kNBWant - 1 : kNBWant;
     static constexpr int kRawFit = RAW ? (kBudget - kNBMin * kBStage - EPI) / RAWB : 0;
-    static constexpr int kNR = RAW ? (kRawFit > 4 ? 4 : kRawFit) : 1;
+    // 16-bit tiles read as A (DEEP) need no decode, so only the ring's depth
+    // keeps HBM busy: up to 8 slots
+    static constexpr int kNRMax = DEEP ? 8 : 4;
+    static constexpr int kNR = RAW ? (kRawFit > kNRMax ? kNRMax : kRawFit) : 1;
     static_assert(!RAW || kNR >= 2, "raw W ring too shallow");
     static constexpr int kAvail = kBudget - (RAW ? kNR * RAWB : 0) - EPI;
     static constexpr int NB = (kAvail / kBStage) > 8 ? 8 : (kAvail / kBStage);
@@ -407,19 +424,20 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     constexpr int kRowsOut = MODE == 3 ? 64 : kBM;   // output rows per CTA
     constexpr int kTokOut = MODE == 1 ? BN : BN / 2;  // tokens per CTA
     constexpr int kSliceB = raw_slice_bytes(FMT, MODE);  // raw W tiles by TMA
-    constexpr bool kRaw = kSliceB > 0;
-    constexpr int kRawB = kBM * kSliceB;
+    constexpr bool kRaw = kSliceB > 0;                    // decoded from the raw ring
+    constexpr bool kSSable = mma_ssable(FMT, MODE, GRP);
+    constexpr int kRawB = mma_ring_bytes(FMT, MODE, GRP);  // one slot of the raw ring
     // y through shared memory and tensor stores (the host enables it per call)
     constexpr bool kTmaEpi = mma_tma_epilogue(MODE, GRP);
     constexpr int kEpiB = kTmaEpi ? kEpiStageBytes : 0;
-    using C = MmaCfg<BN, kRawB, kEpiB>;
+    using C = MmaCfg<BN, kRawB, kEpiB, kSSable>;
     constexpr int NA = C::NA, NB = C::NB, kNR = C::kNR, KA = C::KA, KB = C::KB;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
     const uint32_t B0 = sbase;                                     // x ring
     const uint32_t W0 = B0 + NB * C::kBStage;                      // raw W stages (kRaw)
-    const uint32_t E0 = W0 + (kRaw ? kNR * kRawB : 0);              // epilogue staging (kTmaEpi)
+    const uint32_t E0 = W0 + (kRawB > 0 ? kNR * kRawB : 0);         // epilogue staging (kTmaEpi)
     const uint32_t bar0 = E0 + kEpiB;
     auto fullA = [&](int s) { return bar0 + 8u * s; };
     auto emptyA = [&](int s) { return bar0 + 8u * (NA + s); };
@@ -447,6 +465,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     static_assert(KA % kGroups == 0, "every group needs a k-step in every A stage");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool ss = kSSable && p.ss != 0;  // A tiles straight from the raw ring
     const uint32_t crank = cluster_ctarank();  // 0 or 1 within the CTA pair
     const int KS = p.KS;                     // 64-wide k-steps
     // Tiles: the pair of CTAs takes 128-row tiles 2q and 2q + 1 of token tile
@@ -540,7 +559,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
         for (int s = 0; s < kNR; ++s) {
             mbar_init(rawFull(s), 1);
-            mbar_init(rawEmpty(s), kDeqWarps / kGroups);  // the group that decodes it
+            // the group that decodes it, or the MMAs that read it as A
+            mbar_init(rawEmpty(s), ss ? 1 : kDeqWarps / kGroups);
         }
         mbar_init(accFull, 1);
         mbar_init(accEmpty, kDeqWarps);
@@ -655,7 +675,57 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         // either way small token tiles are paced by the decode (about 2300
         // cycles per super-block and group, the two groups overlapping).
         constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
-        if (elect_one()) {
+        const bool mma_leader = elect_one();  // the whole warp elects once
+        if (mma_leader && ss) {
+            // A from the raw ring, one k-step a slot: each k-step waits for its
+            // W tile (and, at a stage start, its x stage), issues its four
+            // K = 16 MMAs and frees the slot
+            const uint32_t idesc_ss = FMT == F_BF16 ? idesc_bf16_f32(kBM, BN) : idesc;
+            int sr = 0, sb = 0;
+            uint32_t phr = 0, phb = 0;
+            int it = 0;
+            bool failed = false;
+            for (int u = c0; u < n_units && !failed; u += cstep, ++it) {
+                const Tile t = tile_of(u);
+                const int KSu = nks(t);
+                if (it > 0) {  // the epilogue has drained the accumulator
+                    if (!wait_abortable(accEmpty, (it - 1) & 1, abort_flag)) {
+                        record_error(p.err, DERR_MMA_ACC);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                for (int ks = 0; ks < KSu; ++ks) {
+                    if (!wait_abortable(rawFull(sr), phr, abort_flag)) {
+                        record_error(p.err, DERR_MMA_A);
+                        *abort_flag = 1;
+                        failed = true;
+                        break;
+                    }
+                    if (ks % KB == 0 && !wait_abortable(fullB(sb), phb, abort_flag)) {
+                        record_error(p.err, DERR_MMA_B);
+                        *abort_flag = 1;
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const bool last = ks == KSu - 1;
+                    const uint64_t ad = sdesc_sw128(W0 + sr * kRawB);
+                    const uint64_t bd = sdesc_sw128(B0 + sb * C::kBStage + (ks % KB) * C::kBBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16: 32 bytes of A and of B
+                        tc_mma_f16_ss(tmem, ad + 2 * kk, bd + 2 * kk, idesc_ss, ks > 0 || kk > 0);
+                    tc_commit(rawEmpty(sr));
+                    if (++sr == kNR) { sr = 0; phr ^= 1u; }
+                    if (ks % KB == KB - 1 || last) {
+                        tc_commit_multicast(emptyB(sb), (uint16_t)3);  // both CTAs may refill
+                        if (++sb == NB) { sb = 0; phb ^= 1u; }
+                    }
+                    if (last) tc_commit(accFull);  // the tile's product is complete
+                }
+            }
+        } else if (mma_leader) {
             int sa = 0, sb = 0;        // A / x ring slots
             uint32_t pha = 0, phb = 0; // their phase parities
             int it = 0;
@@ -718,7 +788,35 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         // ------------------------- raw W tiles (Q4_K, affine codes) via TMA -------------------------
         // its own warp, so that the raw ring runs as far ahead of the dequant
         // warps as it is deep (into the next tile), whatever the x ring does
-        if (kRaw && raw_rowcopy(FMT)) {
+        if (ss) {
+            // 16-bit W: one 128-row x 64-wide tile a k-step, in the order the
+            // MMA lane consumes them
+            if (lane == 0) {
+                prefetch_tmap(&tmw);
+                int rcount = 0;
+                for (int u = c0; u < n_units; u += cstep) {
+                    if (*abort_flag) break;
+                    const Tile t = tile_of(u);
+                    bool ok = true;
+                    for (int ks = t.k_lo; ks < t.k_hi; ++ks, ++rcount) {
+                        const int rs = rcount % kNR;
+                        if (rcount >= kNR &&
+                            !wait_abortable(rawEmpty(rs), ((rcount / kNR) + 1) & 1, abort_flag)) {
+                            record_error(p.err, DERR_MMA_EMPTY);
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(rawFull(rs), kRawB);
+                        tma_load_2d(W0 + rs * kRawB, &tmw, kBK * kx(t, ks), (int)t.wrow, rawFull(rs));
+                    }
+                    if (!ok) break;
+                }
+                // no copy may land after this CTA exits
+                for (int s = std::max(0, rcount - kNR); s < rcount; ++s)
+                    if (!mbar_wait(rawFull(s % kNR), (s / kNR) & 1)) record_error(p.err, DERR_TEARDOWN);
+            }
+        } else if (kRaw && raw_rowcopy(FMT)) {
             // Q6_K: the 32 lanes copy four rows each. A row's super-block of
             // this slice sits at src = w + j R + 210 sb; its window starts at
             // src & ~15 and runs kQ6kWindow bytes, cut at the last 16-byte
@@ -862,6 +960,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         for (int u = c0; u < n_units && !failed; u += cstep, ++it) {
             const Tile t = tile_of(u);
             const int KSu = nks(t);
+            // ss: the A operand is the raw ring itself, nothing to decode
+            if (!ss) {
             if constexpr (kRaw) {
                 // Super-block b is one A stage. Group g takes the super-blocks
                 // whose global index has parity g, so the two groups run out of
@@ -1086,6 +1186,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                     }
                 }
             }
+            }  // !ss
             abase += nsa(t);
             if (failed) break;
             // ------------------------------ epilogue ------------------------------
@@ -1267,8 +1368,8 @@ static cudaError_t launch_t(const Maps &mp, const MmaHostParams &h, const Device
     } else {
         p = static_cast<const MmaParamsOf<FMT> &>(static_cast<const MmaAffParams &>(h));
     }
-    using C = MmaCfg<BN, kBM * raw_slice_bytes(FMT, MODE),
-                     mma_tma_epilogue(MODE, GRP) ? kEpiStageBytes : 0>;
+    using C = MmaCfg<BN, mma_ring_bytes(FMT, MODE, GRP),
+                     mma_tma_epilogue(MODE, GRP) ? kEpiStageBytes : 0, mma_ssable(FMT, MODE, GRP)>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     static int max_clusters = 0;

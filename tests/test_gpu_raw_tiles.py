@@ -106,3 +106,39 @@ def test_repeated_calls_give_the_same_bits(fmt):
             first = yh
         else:
             assert np.array_equal(first.view(np.uint32), yh.view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "f16"])
+@pytest.mark.parametrize("k,n,nt", [(4096, 1000, 8), (2048, 257, 130), (1024, 129, 3)])
+def test_16_bit_tiles_as_the_a_operand(fmt, k, n, nt):
+    """16-bit W tiles go by TMA straight into shared memory as the MMA's A
+    operand (k % 8 == 0); BF16 takes x as two bf16 terms."""
+    rng = np.random.default_rng(k + n + nt + len(fmt))
+    w = qmm_synth.gen_weights(fmt, k, n, rng)
+    x = qmm_synth.gen_x(nt, k, rng)
+    y = q.matmul(fmt, _dev(w), _dev(x), k, n, path=q.PATH_MMA)
+    torch.cuda.synchronize()
+    q.qmm_device_status()
+    y_ref, s_ref = oracle.matmul_blas(fmt, w, x, k, n)
+    ok, worst, cos, msg = oracle.check(y.cpu().numpy(), y_ref, s_ref)
+    assert ok, f"{fmt} k={k} n={n} N={nt}: {msg}"
+
+
+def test_bf16_weights_outside_the_fp16_range():
+    """BF16 weights far above fp16's largest value and far below its normal
+    range: bf16 operands carry them exactly (an fp16 copy would overflow or
+    lose bits)."""
+    k, n, nt = 4096, 256, 16
+    rng = np.random.default_rng(7)
+    vals = rng.normal(0, 1, (n, k)).astype(np.float32)
+    vals[0::4] *= 1e5
+    vals[1::4] *= 1e-6
+    u = vals.view(np.uint32)
+    w = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16).view(np.uint8).reshape(-1)
+    x = qmm_synth.gen_x(nt, k, rng)
+    y = q.matmul("bf16", _dev(w), _dev(x), k, n, path=q.PATH_MMA)
+    torch.cuda.synchronize()
+    q.qmm_device_status()
+    y_ref, s_ref = oracle.matmul_blas("bf16", w, x, k, n)
+    ok, worst, cos, msg = oracle.check(y.cpu().numpy(), y_ref, s_ref)
+    assert ok, msg
