@@ -39,6 +39,7 @@ CASES = [  # (fmt, k, n, n_tokens)
     ("q4_0", 2048, 127, 17), ("q4_0", 4096, 900, 129), ("q4_0", 1280, 256, 5),
     ("q6_k", 2560, 131, 7), ("q6_k", 4096, 1000, 64), ("q6_k", 1024, 1, 33),
     ("q6_k", 1536, 385, 130),
+    ("bf16", 4096, 1000, 37), ("f16", 2048, 257, 130), ("bf16", 1000, 129, 9),
 ]
 
 
