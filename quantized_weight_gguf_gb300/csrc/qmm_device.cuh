@@ -220,6 +220,19 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared on the load path (cp.async,
+// L1 bypassed), not the tensor-copy unit: `valid` bytes (0..16) are read from
+// src, the rest of the 16 are zero-filled. dst and src 16-byte aligned.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid)
+                 : "memory");
+}
+// One arrival on `bar` once every earlier cp.async of this thread has landed
+// (.noinc: it counts against the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // 2-D tiled tensor copy global -> shared (TMA) through a tensor map.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int c0, int c1,
                                             uint32_t bar) {
@@ -296,9 +309,6 @@ __device__ __forceinline__ uint32_t lds16(uint32_t addr) {
     unsigned short v;
     asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
     return v;
-}
-__device__ __forceinline__ void sts8(uint32_t addr, uint8_t v) {
-    asm volatile("st.shared.u8 [%0], %1;" ::"r"(addr), "h"((unsigned short)v) : "memory");
 }
 __device__ __forceinline__ void sts32f(uint32_t addr, float v) {
     asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");

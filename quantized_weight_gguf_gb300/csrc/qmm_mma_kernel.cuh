@@ -15,8 +15,9 @@
 //               into fp16 and stores them in the same swizzled K-major layout
 //               the MMA descriptor describes; after the k-loop all 16 warps
 //               drain the accumulator TMEM -> registers -> y;
-//   warp 18     Q4_K and affine formats: streams raw W tiles (128 rows x a
-//               256-wide k slice) by TMA ahead of the dequant warps.
+//   warp 18     raw-tile formats: streams raw W tiles (128 rows x a 256-wide
+//               k slice) ahead of the dequant warps, by TMA (Q6_K rows by
+//               16-byte cp.async copies of its 32 lanes).
 // X is converted to fp16 once per call by a small kernel that also scales each
 // token row by a power of two (exact) so it fits fp16's range; the epilogue
 // multiplies by the inverse power.
@@ -112,9 +113,10 @@ constexpr int kRawBytes = kBM * 144;
 // super-blocks (144 B), eight 32-weight blocks of Q4_0 (144 B), Q5_0 (176 B)
 // or Q8_0 (272 B), and affine code words (128 B at 4 bits, 256 B at 8; their
 // scales and biases come from global memory per thread). Q6_K's 210-byte
-// super-blocks start on 2-byte boundaries, which no TMA box can: each row's
-// super-block comes with its own 1-D bulk copy of the 224 bytes from the
-// 16-byte boundary at or below it, into a 240-byte row of the tile. MODE 3
+// super-blocks start on 2-byte boundaries, which no TMA box can: the raw
+// loader's 32 lanes copy each row's 224 bytes from the 16-byte boundary at or
+// below its super-block, into a 240-byte row of the tile, in 16-byte cp.async
+// copies (one arrival a lane on the slot's barrier). MODE 3
 // (rows split into hi / lo halves) decodes from registers; so do the block
 // formats when k % 256 != 0.
 __host__ __device__ constexpr int raw_slice_bytes(int fmt, int mode) {
@@ -127,7 +129,7 @@ __host__ __device__ constexpr int raw_slice_bytes(int fmt, int mode) {
            : fmt == F_Q8_0 ? 272
            : fmt == F_Q6_K ? 240 : 0;
 }
-// Raw tiles filled row by row with bulk copies (no tensor map)
+// Raw tiles filled row by row by the loader lanes (no tensor map)
 __host__ __device__ constexpr bool raw_rowcopy(int fmt) { return fmt == F_Q6_K; }
 // 16-bit formats in split-x mode (ungrouped) can take their W tiles as the
 // MMA's A operand straight from shared memory: nothing to decode. The raw
@@ -558,7 +560,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             mbar_init(emptyB(s), 2);  // both CTAs of the pair have consumed the stage
         }
         for (int s = 0; s < kNR; ++s) {
-            mbar_init(rawFull(s), 1);
+            mbar_init(rawFull(s), raw_rowcopy(FMT) ? 32 : 1);
             // the group that decodes it, or the MMAs that read it as A
             mbar_init(rawEmpty(s), ss ? 1 : kDeqWarps / kGroups);
         }
@@ -817,17 +819,24 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                     if (!mbar_wait(rawFull(s % kNR), (s / kNR) & 1)) record_error(p.err, DERR_TEARDOWN);
             }
         } else if (kRaw && raw_rowcopy(FMT)) {
-            // Q6_K: the 32 lanes copy four rows each. A row's super-block of
-            // this slice sits at src = w + j R + 210 sb; its window starts at
-            // src & ~15 and runs kQ6kWindow bytes, cut at the last 16-byte
-            // boundary of W, whose remaining bytes (at most 15) are copied
-            // with plain loads before the slot is armed.
+            // Q6_K: lane l copies 16-byte chunks l, l + 32, ... of the slot,
+            // chunk c = 14 r + q being bytes 16 q .. 16 q + 15 of row r's
+            // window, which starts at (w + j R + 210 sb) & ~15 for row j of W.
+            // Rows past the matrix and bytes past the end of W are zero-filled.
+            // (One 1-D bulk copy a row kept the tensor-copy unit so busy that
+            // a tile took about 1.35x as long.)
+            constexpr int kCh = kQ6kWindow / 16;
+            constexpr int kPerLane = kBM * kCh / 32;
+            constexpr int kDr = 32 / kCh, kDq = 32 % kCh;  // (r, q) step of c + 32
+            static_assert(kBM * kCh % 32 == 0 && kCh <= 32, "chunks per lane");
             const uintptr_t wbase = reinterpret_cast<uintptr_t>(p.w);
-            const uintptr_t wend16 = (wbase + (uintptr_t)(p.row_bytes * p.w_rows)) & ~(uintptr_t)15;
+            const uintptr_t wend = wbase + (uintptr_t)(p.row_bytes * p.w_rows);
+            const uintptr_t R = (uintptr_t)p.row_bytes;
             int rcount = 0;
             for (int u = c0; u < n_units; u += cstep) {
-                if (*abort_flag) break;
+                if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
                 const Tile t = tile_of(u);
+                const int rows_ok = (int)std::min<int64_t>(kBM, p.w_rows - t.wrow);
                 bool ok = true;
                 for (int b = t.k_lo / 4; b < t.k_hi / 4; ++b, ++rcount) {  // k % 256 == 0
                     const int rs = rcount % kNR;
@@ -844,38 +853,29 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                     }
                     const int64_t sbg = kx(t, 4 * b) >> 2;  // super-block index along the row
                     const uint32_t slot = W0 + rs * kRawB;
-                    uintptr_t from[4];
-                    uint32_t size[4], total = 0;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int r = lane + 32 * i;
-                        const int64_t j = t.wrow + r;
-                        size[i] = 0;
-                        from[i] = 0;
-                        if (j < p.w_rows) {
-                            const uintptr_t src = wbase + (uintptr_t)(j * p.row_bytes + 210 * sbg);
-                            const uintptr_t a16 = src & ~(uintptr_t)15;
-                            const uintptr_t end = a16 + kQ6kWindow < wend16 ? a16 + kQ6kWindow : wend16;
-                            from[i] = a16;
-                            size[i] = (uint32_t)(end - a16);
-                            total += size[i];
-                            // bytes past the last 16-byte boundary of W (the matrix's
-                            // last super-block only)
-                            for (uintptr_t q = end; q < src + 210; ++q)
-                                sts8(slot + (uint32_t)r * (uint32_t)kSliceB + (uint32_t)(q - a16),
-                                     *reinterpret_cast<const uint8_t *>(q));
+                    int r = lane / kCh, q = lane - (lane / kCh) * kCh;
+                    uintptr_t rb = wbase + (uintptr_t)((t.wrow + r) * p.row_bytes) + (uintptr_t)(210 * sbg);
+#pragma unroll 4
+                    for (int i = 0; i < kPerLane; ++i) {
+                        const uintptr_t a = (rb & ~(uintptr_t)15) + 16u * (uint32_t)q;
+                        uintptr_t src = wbase;  // nothing is read for a zero-filled chunk
+                        uint32_t valid = 0;
+                        if (r < rows_ok && a < wend) {
+                            src = a;
+                            valid = wend - a < 16 ? (uint32_t)(wend - a) : 16u;
+                        }
+                        cp_async16(slot + (uint32_t)(r * kSliceB + 16 * q),
+                                   reinterpret_cast<const void *>(src), valid);
+                        r += kDr;
+                        q += kDq;
+                        rb += kDr * R;
+                        if (q >= kCh) {
+                            q -= kCh;
+                            ++r;
+                            rb += R;
                         }
                     }
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xFFFFFFFFu, total, o);
-                    __syncwarp();  // the plain stores above before the arrival
-                    if (lane == 0) mbar_arrive_expect_tx(rawFull(rs), total);
-                    __syncwarp();
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        if (size[i])
-                            bulk_g2s(slot + (uint32_t)(lane + 32 * i) * (uint32_t)kSliceB,
-                                     reinterpret_cast<const void *>(from[i]), size[i], rawFull(rs));
+                    cp_async_arrive(rawFull(rs));
                 }
                 if (!ok) break;
             }
