@@ -274,7 +274,7 @@ size_t qmm_backward_input_workspace_bytes(const qmm_args *a);
  * grouped form cannot take the call); AUTO takes the grouped form for Q4_K,
  * Q8_0, Q5_0 and Q4_0 when n_pos > 1 and n_pos * top_k >= 2 * n_experts, for
  * Q6_K (whose exact decode makes the grouped form cost about the same at any
- * position count) when n_pos * top_k >= 5 * n_experts, the GEMV form
+ * position count) when n_pos * top_k >= 3 * n_experts, the GEMV form
  * otherwise. An id outside [0, n_experts)
  * leaves that y row untouched and records an error that qmm_device_status
  * reports as QMM_ERR_BAD_ID. */

@@ -309,10 +309,10 @@ size_t glu_scratch_bytes(const qmm_args *a) {
 // and on average at least two pairs per expert (top 8 of 64 experts, k = 2048,
 // n = 768; 64 positions: Q4_K 37 against 189 us in the per-pair GEMV form,
 // Q8_0 46 against 211, Q5_0 60 against 222; 16 positions: Q4_K 36 against 53,
-// Q8_0 42 against 60). Q6_K's grouped form costs about the same at any
-// position count (its exact fp32 decode paces it: 141-145 us from 16 to 64
-// positions, against 68, 132 and 255 us per pair), so it groups from five
-// pairs per expert.
+// Q8_0 42 against 60). Q6_K's grouped form costs about the same from 16
+// positions on (its exact fp32 decode paces it: 106-109 us from 16 to 64
+// positions, against 67, 131, 204 and 255 us per pair at 16, 24, 40 and 64),
+// so it groups from three pairs per expert.
 // With QMM_FLAG_SPLIT_W the pairs take the GEMV (exact fp32 products).
 bool experts_grouped_ok(const qmm_args *a, int64_t n_experts) {
     return !affine_fmt(a->fmt) && a->k > 0 && qmm::mma_mode(a->fmt, a->k) == 2 &&
@@ -323,7 +323,7 @@ bool experts_grouped(const qmm_args *a, int64_t n_experts, int64_t top_k) {
     if (a->path == QMM_PATH_MMA) return true;
     if (a->n_tokens <= 1) return false;
     const int64_t pairs = a->n_tokens * top_k;
-    if (a->fmt == QMM_Q6_K) return pairs >= 5 * n_experts;
+    if (a->fmt == QMM_Q6_K) return pairs >= 3 * n_experts;
     const bool raw_tiles = a->fmt == QMM_Q4_K || a->fmt == QMM_Q8_0 || a->fmt == QMM_Q5_0 ||
                            a->fmt == QMM_Q4_0;
     return raw_tiles && pairs >= 2 * n_experts;

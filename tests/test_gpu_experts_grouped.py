@@ -56,9 +56,10 @@ def test_auto_policy_picks_the_grouped_form():
     assert q.qmm_experts_workspace_bytes(a, n_exp, top_k) == 0    # k < 1024: GEMV form
     a = q.make_args("q4_k", 16, 16, 16, 512, n, 64, path=q.PATH_MMA, stream=0)
     assert q.load().qmm_matmul_experts(ctypes.byref(a), 16, n_exp, top_k) == 10
-    # the other raw-tile formats group from two pairs per expert; Q6_K from five
+    # the other raw-tile formats group from two pairs per expert; Q6_K from three
     for fmt, n_pos, grouped in (("q8_0", 64, True), ("q5_0", 64, True), ("q4_0", 64, True),
-                                ("q8_0", 8, True), ("q6_k", 64, True), ("q6_k", 16, False)):
+                                ("q8_0", 8, True), ("q6_k", 64, True), ("q6_k", 12, True),
+                                ("q6_k", 11, False), ("q6_k", 8, False)):
         a = q.make_args(fmt, 16, 16, 16, k, n, n_pos, stream=0)
         assert (q.qmm_experts_workspace_bytes(a, n_exp, top_k) > 0) == grouped, (fmt, n_pos)
 
